@@ -1,0 +1,140 @@
+"""fp64 CPU oracle for Kaczmarz Linear Attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product (the CUDA library and its
+Python binding) never imports, links or executes anything here, and this
+package imports nothing from the product.
+
+The arithmetic lives in ``kla_oracle.c`` (plain sequential fp64 recurrence,
+see the header there for the passages it follows).  This module only
+compiles it with gcc, converts arrays to contiguous float64 and calls it.
+
+Functions
+---------
+forward(q, k, v, alpha, eta, eps, S0=None, nthreads=1) -> (o, S_T)
+    fixed-length batch, q,k: [B,T,H,dk], v: [B,T,H,dv], alpha,eta: [B,T,H],
+    S0: [B,H,dk,dv] or None.
+forward_varlen(q, k, v, alpha, eta, eps, cu_seqlens, S0=None, nthreads=1)
+    packed batch, q,k: [total_T,H,dk], cu_seqlens: [N+1] int.
+decode(q, k, v, alpha, eta, eps, S, nthreads=1) -> (o, S_new)
+    one token per (b,h): q,k: [B,H,dk], v: [B,H,dv], alpha,eta: [B,H],
+    S: [B,H,dk,dv].  The decode step is the same recurrence applied to a
+    single token on a stored state, so it calls ``forward`` with T = 1.
+
+Every array argument may be a numpy array or a CPU torch tensor of any
+floating dtype; values are upcast exactly to float64 (bf16 and fp32 are
+subsets of fp64).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kla_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libkla_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile kla_oracle.c into libkla_oracle.so next to it (gcc, -O2, no
+    fast-math, no host-specific flags so it builds the same on x86 and Arm)."""
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+               "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int)
+            lib.kla_oracle_forward.restype = ctypes.c_int
+            lib.kla_oracle_forward.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                dp, dp, dp, dp, dp, ctypes.c_double, dp, dp, dp, ctypes.c_int]
+            lib.kla_oracle_forward_varlen.restype = ctypes.c_int
+            lib.kla_oracle_forward_varlen.argtypes = [
+                ctypes.c_int, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                dp, dp, dp, dp, dp, ctypes.c_double, dp, dp, dp, ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor (CPU); exact upcast
+        import torch
+        x = x.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def forward(q, k, v, alpha, eta, eps, S0=None, nthreads: int = 1):
+    lib = _load()
+    q, k, v, alpha, eta, S0 = map(_f64, (q, k, v, alpha, eta, S0))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    assert k.shape == (B, T, H, dk) and v.shape == (B, T, H, dv)
+    assert alpha.shape == (B, T, H) and eta.shape == (B, T, H)
+    if S0 is not None:
+        assert S0.shape == (B, H, dk, dv)
+    o = np.zeros((B, T, H, dv), dtype=np.float64)
+    S = np.zeros((B, H, dk, dv), dtype=np.float64)
+    rc = lib.kla_oracle_forward(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v),
+                                _ptr(alpha), _ptr(eta), float(eps), _ptr(S0),
+                                _ptr(o), _ptr(S), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"kla_oracle_forward failed rc={rc}")
+    return o, S
+
+
+def forward_varlen(q, k, v, alpha, eta, eps, cu_seqlens, S0=None, nthreads: int = 1):
+    lib = _load()
+    q, k, v, alpha, eta, S0 = map(_f64, (q, k, v, alpha, eta, S0))
+    cu = np.ascontiguousarray(np.asarray(
+        cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
+        dtype=np.int32))
+    N = cu.shape[0] - 1
+    total, H, dk = q.shape
+    dv = v.shape[-1]
+    assert int(cu[-1]) == total
+    if S0 is not None:
+        assert S0.shape == (N, H, dk, dv)
+    o = np.zeros((total, H, dv), dtype=np.float64)
+    S = np.zeros((N, H, dk, dv), dtype=np.float64)
+    rc = lib.kla_oracle_forward_varlen(
+        N, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), H, dk, dv,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps), _ptr(S0),
+        _ptr(o), _ptr(S), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"kla_oracle_forward_varlen failed rc={rc}")
+    return o, S
+
+
+def decode(q, k, v, alpha, eta, eps, S, nthreads: int = 1):
+    q, k, v, alpha, eta, S = map(_f64, (q, k, v, alpha, eta, S))
+    B, H, dk = q.shape
+    o, S_new = forward(q[:, None], k[:, None], v[:, None], alpha[:, None],
+                       eta[:, None], eps, S, nthreads=nthreads)
+    return o[:, 0], S_new
