@@ -1,1 +1,19 @@
-"""Kaczmarz Linear Attention for GB300 (sm_103a)."""
+"""Kaczmarz Linear Attention (KLA) for NVIDIA GB300 (sm_103a).
+
+The compute path is the CUDA library ``libkla_gb300.so`` (C ABI in
+``include/kla.h``); ``binding`` is its thin ctypes binding.  ``workloads``
+draws seeded synthetic inputs.
+"""
+from .binding import (  # noqa: F401
+    KlaError,
+    kla_chunk_fwd,
+    kla_chunk_fwd_varlen,
+    kla_chunk_fwd_varlen_workspace_size,
+    kla_chunk_fwd_workspace_size,
+    kla_decode_step,
+    kla_launch_count,
+    kla_status_str,
+    kla_version,
+    kla_workspace_status,
+    load,
+)

@@ -1,0 +1,239 @@
+"""Thin Python binding of the C ABI in include/kla.h (ctypes).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library ``libkla_gb300.so``.  PyTorch provides device memory and streams.
+There is no CPU fallback: if the library cannot be loaded, every call raises.
+
+The functions carry the C names.  Tensor arguments are torch tensors on one
+CUDA device, contiguous, in the layouts that kla.h documents; outputs and the
+workspace are allocated with torch when not supplied.  A non-OK status raises
+``KlaError`` with the library's own message.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+KLA_OK = 0
+KLA_ERR_INVALID_ARG = 1
+KLA_ERR_UNSUPPORTED = 2
+KLA_ERR_CUDA = 3
+KLA_ERR_TIMEOUT = 4
+KLA_ERR_WORKSPACE = 5
+KLA_DTYPE_F32 = 0
+KLA_DTYPE_BF16 = 1
+CHUNK = 64
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KlaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"KLA status {status}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_stale: bool = True) -> ctypes.CDLL:
+    """Load libkla_gb300.so (compiling it first when sources are newer and
+    nvcc is present).  Raises if the library is unavailable."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_stale and _build.is_stale():
+            _build.build()
+        if not os.path.exists(_build.LIB_PATH):
+            raise RuntimeError("libkla_gb300.so is missing; run __graft_entry__.build()")
+        lib = ctypes.CDLL(_build.LIB_PATH)
+        vp, fp, ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+        I, F, Z = ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.kla_status_str.restype = ctypes.c_char_p
+        lib.kla_status_str.argtypes = [I]
+        lib.kla_last_error_message.restype = ctypes.c_char_p
+        lib.kla_last_error_message.argtypes = []
+        lib.kla_version.restype = I
+        lib.kla_version.argtypes = []
+        lib.kla_launch_count.restype = ctypes.c_ulonglong
+        lib.kla_launch_count.argtypes = []
+        lib.kla_chunk_fwd_workspace_size.restype = Z
+        lib.kla_chunk_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I]
+        lib.kla_chunk_fwd_varlen_workspace_size.restype = Z
+        lib.kla_chunk_fwd_varlen_workspace_size.argtypes = [I, I, I, I, I, I, I]
+        lib.kla_chunk_fwd.restype = I
+        lib.kla_chunk_fwd.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, fp,
+                                      I, I, I, I, I, I, I, vp, Z, vp]
+        lib.kla_chunk_fwd_varlen.restype = I
+        lib.kla_chunk_fwd_varlen.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, fp, ip,
+                                             I, I, I, I, I, I, I, vp, Z, vp]
+        lib.kla_decode_step.restype = I
+        lib.kla_decode_step.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, I, I, I, I, I, vp]
+        lib.kla_workspace_status.restype = I
+        lib.kla_workspace_status.argtypes = [vp, Z, vp]
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != KLA_OK:
+        lib = load()
+        raise KlaError(status, lib.kla_last_error_message().decode() or
+                       lib.kla_status_str(status).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KLA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return KLA_DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float32")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t, name, dtype=None, shape=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def kla_status_str(status: int) -> str:
+    return load().kla_status_str(status).decode()
+
+
+def kla_version() -> int:
+    return load().kla_version()
+
+
+def kla_launch_count() -> int:
+    return int(load().kla_launch_count())
+
+
+def kla_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk=CHUNK, dtype=KLA_DTYPE_BF16) -> int:
+    return int(load().kla_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, dtype))
+
+
+def kla_chunk_fwd_varlen_workspace_size(N, total_T, H, dk, dv, chunk=CHUNK,
+                                        dtype=KLA_DTYPE_BF16) -> int:
+    return int(load().kla_chunk_fwd_varlen_workspace_size(N, total_T, H, dk, dv, chunk, dtype))
+
+
+def _workspace(nbytes, device, workspace):
+    if nbytes == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def kla_chunk_fwd(q, k, v, alpha, eta, eps, S0=None, o=None, S_T=None, workspace=None,
+                  stream=None, chunk=CHUNK, return_final_state=True):
+    """Chunkwise prefill; q,k: [B,T,H,dk], v: [B,T,H,dv], alpha,eta: [B,T,H]
+    fp32, S0: [B,H,dk,dv] fp32 or None.  Returns (o, S_T)."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _need(q, "q"); _need(k, "k", q.dtype, (B, T, H, dk)); _need(v, "v", q.dtype, (B, T, H, dv))
+    _need(alpha, "alpha", torch.float32, (B, T, H)); _need(eta, "eta", torch.float32, (B, T, H))
+    _need(S0, "S0", torch.float32, (B, H, dk, dv))
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    _need(o, "o", q.dtype, (B, T, H, dv))
+    if S_T is None and return_final_state:
+        S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    _need(S_T, "S_T", torch.float32, (B, H, dk, dv))
+    nbytes = int(lib.kla_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, dt))
+    workspace, wsb = _workspace(nbytes, q.device, workspace)
+    st = lib.kla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps),
+                           _ptr(S0), _ptr(o), _ptr(S_T), B, T, H, dk, dv, chunk, dt,
+                           _ptr(workspace), wsb, _stream(stream))
+    _check(st)
+    return o, S_T
+
+
+def kla_chunk_fwd_varlen(q, k, v, alpha, eta, eps, cu_seqlens, S0=None, o=None, S_T=None,
+                         workspace=None, stream=None, chunk=CHUNK, return_final_state=True,
+                         check_status=False):
+    """Packed prefill; q,k: [total_T,H,dk], v: [total_T,H,dv], alpha,eta:
+    [total_T,H], cu_seqlens: int32 [N+1] on the device.  Returns (o, S_T)."""
+    lib = load()
+    total, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.shape[0] - 1
+    dt = _dtype_code(q)
+    _need(q, "q"); _need(k, "k", q.dtype, (total, H, dk)); _need(v, "v", q.dtype, (total, H, dv))
+    _need(alpha, "alpha", torch.float32, (total, H)); _need(eta, "eta", torch.float32, (total, H))
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    _need(S0, "S0", torch.float32, (N, H, dk, dv))
+    if o is None:
+        o = torch.empty((total, H, dv), dtype=q.dtype, device=q.device)
+    _need(o, "o", q.dtype, (total, H, dv))
+    if S_T is None and return_final_state:
+        S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    _need(S_T, "S_T", torch.float32, (N, H, dk, dv))
+    nbytes = int(lib.kla_chunk_fwd_varlen_workspace_size(N, total, H, dk, dv, chunk, dt))
+    workspace, wsb = _workspace(nbytes, q.device, workspace)
+    s = _stream(stream)
+    st = lib.kla_chunk_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps),
+                                  _ptr(S0), _ptr(o), _ptr(S_T), _ptr(cu_seqlens), N, total,
+                                  H, dk, dv, chunk, dt, _ptr(workspace), wsb, s)
+    _check(st)
+    if check_status:
+        _check(lib.kla_workspace_status(_ptr(workspace), wsb, s))
+    return o, S_T
+
+
+def kla_decode_step(q, k, v, alpha, eta, eps, S, o=None, stream=None):
+    """One decode step; q,k: [B,H,dk], v: [B,H,dv], alpha,eta: [B,H], S:
+    [B,H,dk,dv] fp32 updated in place.  Returns o [B,H,dv]."""
+    lib = load()
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _need(q, "q"); _need(k, "k", q.dtype, (B, H, dk)); _need(v, "v", q.dtype, (B, H, dv))
+    _need(alpha, "alpha", torch.float32, (B, H)); _need(eta, "eta", torch.float32, (B, H))
+    _need(S, "S", torch.float32, (B, H, dk, dv))
+    if o is None:
+        o = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    _need(o, "o", q.dtype, (B, H, dv))
+    st = lib.kla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps),
+                             _ptr(S), _ptr(o), B, H, dk, dv, dt, _stream(stream))
+    _check(st)
+    return o
+
+
+def kla_workspace_status(workspace, stream=None) -> int:
+    """Synchronises the stream and returns the device status recorded in
+    ``workspace`` (raises KlaError when it is not OK)."""
+    lib = load()
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.kla_workspace_status(_ptr(workspace), wsb, _stream(stream))
+    _check(st)
+    return st

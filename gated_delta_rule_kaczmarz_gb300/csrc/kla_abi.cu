@@ -1,0 +1,272 @@
+// C ABI of the library (declared in include/kla.h): host-side validation,
+// path selection and launches.  No device memory is allocated here.
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+#include "../../include/kla.h"
+#include "kla_internal.h"
+
+namespace kla {
+static std::atomic<unsigned long long> g_launches{0};
+void note_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+}  // namespace kla
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kla_status fail(kla_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+kla_status ok() {
+    g_last_error.clear();
+    return KLA_OK;
+}
+
+kla_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(KLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Host-side fault hook for tests: KLA_FAULT_INJECT=launch makes every
+// launching entry point report KLA_ERR_CUDA before touching the device.
+bool inject_launch_fault() {
+    const char *s = std::getenv("KLA_FAULT_INJECT");
+    return s != nullptr && std::strcmp(s, "launch") == 0;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Common size/dtype checks.  Returns KLA_OK or the failure status.
+kla_status check_shape(int H, int dk, int dv, int chunk, int dtype) {
+    if (H <= 0 || dk <= 0 || dv <= 0 || chunk <= 0)
+        return fail(KLA_ERR_INVALID_ARG, "sizes must be positive (H=%d dk=%d dv=%d chunk=%d)",
+                    H, dk, dv, chunk);
+    if (dtype != KLA_DTYPE_F32 && dtype != KLA_DTYPE_BF16)
+        return fail(KLA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (dk != dv || (dk != 64 && dk != 128))
+        return fail(KLA_ERR_UNSUPPORTED, "supported head sizes: dk == dv in {64,128} (got %d,%d)",
+                    dk, dv);
+    if (chunk != kla::kChunk)
+        return fail(KLA_ERR_UNSUPPORTED, "supported chunk length: 64 (got %d)", chunk);
+    return KLA_OK;
+}
+
+bool use_tc_path(int d, int dtype) { return kla::chunk_tc_supported(d, dtype); }
+
+long chunks_upper(long n_seq, long total_T) {
+    // every sequence adds at most one partial chunk
+    return (total_T + kla::kChunk - 1) / kla::kChunk + n_seq;
+}
+
+// Number of chunk slots a call needs: exact for fixed length, an upper bound
+// for varlen.
+long n_chunks(bool varlen, long n_seq, long T, long total_T) {
+    return varlen ? chunks_upper(n_seq, total_T) : n_seq * ((T + kla::kChunk - 1) / kla::kChunk);
+}
+
+size_t ws_bytes(bool varlen, long n_seq, long T, long total_T, int H, int d, int dtype) {
+    if (use_tc_path(d, dtype))
+        return kla::kWsHeader +
+               kla::chunk_tc_workspace_bytes(n_chunks(varlen, n_seq, T, total_T), H);
+    return varlen ? kla::kWsHeader : 0;
+}
+
+// Writes S_T for calls with no tokens: S_T = S0 (or zeros).
+kla_status states_only(const float *S0, float *S_T, size_t n, cudaStream_t s) {
+    if (!S_T || n == 0) return ok();
+    cudaError_t e = S0 ? (S0 == S_T ? cudaSuccess
+                                    : cudaMemcpyAsync(S_T, S0, n * sizeof(float),
+                                                      cudaMemcpyDeviceToDevice, s))
+                       : cudaMemsetAsync(S_T, 0, n * sizeof(float), s);
+    if (e != cudaSuccess) return cuda_fail(e, "state copy");
+    return ok();
+}
+
+kla_status run_prefill(kla::Problem &p, bool varlen, void *workspace, size_t workspace_bytes,
+                       cudaStream_t s) {
+    const size_t need = ws_bytes(varlen, p.n_seq, p.T, p.total_T, p.H, p.d, p.dtype);
+    if (need > 0) {
+        if (workspace == nullptr || workspace_bytes < need)
+            return fail(KLA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
+                        workspace ? workspace_bytes : (size_t)0);
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return fail(KLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+        p.status = static_cast<unsigned *>(workspace);
+        p.ws = static_cast<unsigned char *>(workspace) + kla::kWsHeader;
+        p.ws_bytes = workspace_bytes - kla::kWsHeader;
+    } else {
+        p.status = nullptr;
+        p.ws = nullptr;
+        p.ws_bytes = 0;
+    }
+    if (inject_launch_fault()) return fail(KLA_ERR_CUDA, "injected launch fault (KLA_FAULT_INJECT)");
+
+    cudaError_t e = cudaSuccess;
+    if (p.status) {
+        if (varlen) {
+            e = kla::launch_check_seqlens(p, s);
+        } else {
+            e = cudaMemsetAsync(p.status, 0, sizeof(unsigned), s);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "status init");
+    }
+    if (use_tc_path(p.d, p.dtype)) {
+        e = kla::launch_chunk_tc(p, n_chunks(varlen, p.n_seq, p.T, p.total_T), s);
+    } else {
+        e = kla::launch_chunk_simt(p, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kla_status_str(int status) {
+    switch (status) {
+        case KLA_OK: return "ok";
+        case KLA_ERR_INVALID_ARG: return "invalid argument";
+        case KLA_ERR_UNSUPPORTED: return "unsupported size or dtype";
+        case KLA_ERR_CUDA: return "CUDA error";
+        case KLA_ERR_TIMEOUT: return "device wait timed out";
+        case KLA_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+const char *kla_last_error_message(void) { return g_last_error.c_str(); }
+
+int kla_version(void) { return 100; }
+
+unsigned long long kla_launch_count(void) { return kla::g_launches.load(std::memory_order_relaxed); }
+
+size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, int dtype) {
+    if (B < 0 || T < 0) return 0;
+    if (check_shape(H, dk, dv, chunk, dtype) != KLA_OK) return 0;
+    return ws_bytes(false, B, T, (long)B * T, H, dk, dtype);
+}
+
+size_t kla_chunk_fwd_varlen_workspace_size(int N, int total_T, int H, int dk, int dv, int chunk,
+                                           int dtype) {
+    if (N < 0 || total_T < 0) return 0;
+    if (check_shape(H, dk, dv, chunk, dtype) != KLA_OK) return 0;
+    return ws_bytes(true, N, 0, total_T, H, dk, dtype);
+}
+
+int kla_chunk_fwd(const void *q, const void *k, const void *v, const float *alpha,
+                  const float *eta, float eps, const float *S0, void *o, float *S_T, int B,
+                  int T, int H, int dk, int dv, int chunk, int dtype, void *workspace,
+                  size_t workspace_bytes, void *stream) {
+    if (B < 0 || T < 0) return fail(KLA_ERR_INVALID_ARG, "negative size (B=%d T=%d)", B, T);
+    kla_status st = check_shape(H, dk, dv, chunk, dtype);
+    if (st != KLA_OK) return st;
+    if (!(eps >= 0.f)) return fail(KLA_ERR_INVALID_ARG, "eps must be >= 0");
+    const long rows = (long)B * T;
+    if (rows > INT32_MAX || (long)B * H > INT32_MAX)
+        return fail(KLA_ERR_UNSUPPORTED, "problem too large (B*T and B*H must fit in int32)");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t nstate = (size_t)B * H * dk * dv;
+    if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T)))
+        return fail(KLA_ERR_INVALID_ARG, "state pointers must be 16-byte aligned");
+    if (rows == 0) {
+        if (inject_launch_fault()) return fail(KLA_ERR_CUDA, "injected launch fault (KLA_FAULT_INJECT)");
+        return states_only(S0, S_T, nstate, s);
+    }
+    if (!q || !k || !v || !alpha || !eta || !o)
+        return fail(KLA_ERR_INVALID_ARG, "q, k, v, alpha, eta and o must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(alpha) ||
+        !aligned4(eta))
+        return fail(KLA_ERR_INVALID_ARG, "q, k, v, o must be 16-byte aligned, alpha and eta 4-byte");
+    kla::Problem p{};
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.eta = eta; p.eps = eps;
+    p.S0 = S0; p.o = o; p.S_T = S_T; p.cu_seqlens = nullptr;
+    p.n_seq = B; p.T = T; p.total_T = (int)rows; p.H = H; p.d = dk; p.dtype = dtype;
+    return run_prefill(p, false, workspace, workspace_bytes, s);
+}
+
+int kla_chunk_fwd_varlen(const void *q, const void *k, const void *v, const float *alpha,
+                         const float *eta, float eps, const float *S0, void *o, float *S_T,
+                         const int *cu_seqlens, int N, int total_T, int H, int dk, int dv,
+                         int chunk, int dtype, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+    if (N < 0 || total_T < 0)
+        return fail(KLA_ERR_INVALID_ARG, "negative size (N=%d total_T=%d)", N, total_T);
+    kla_status st = check_shape(H, dk, dv, chunk, dtype);
+    if (st != KLA_OK) return st;
+    if (!(eps >= 0.f)) return fail(KLA_ERR_INVALID_ARG, "eps must be >= 0");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T)))
+        return fail(KLA_ERR_INVALID_ARG, "state pointers must be 16-byte aligned");
+    if (N == 0) {
+        if (total_T != 0) return fail(KLA_ERR_INVALID_ARG, "N == 0 requires total_T == 0");
+        return ok();
+    }
+    if (!cu_seqlens) return fail(KLA_ERR_INVALID_ARG, "cu_seqlens must be non-null");
+    if (total_T > 0) {
+        if (!q || !k || !v || !alpha || !eta || !o)
+            return fail(KLA_ERR_INVALID_ARG, "q, k, v, alpha, eta and o must be non-null");
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+            !aligned4(alpha) || !aligned4(eta))
+            return fail(KLA_ERR_INVALID_ARG,
+                        "q, k, v, o must be 16-byte aligned, alpha and eta 4-byte");
+    }
+    kla::Problem p{};
+    p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.eta = eta; p.eps = eps;
+    p.S0 = S0; p.o = o; p.S_T = S_T; p.cu_seqlens = cu_seqlens;
+    p.n_seq = N; p.T = 0; p.total_T = total_T; p.H = H; p.d = dk; p.dtype = dtype;
+    return run_prefill(p, true, workspace, workspace_bytes, s);
+}
+
+int kla_decode_step(const void *q, const void *k, const void *v, const float *alpha,
+                    const float *eta, float eps, float *S, void *o, int B, int H, int dk, int dv,
+                    int dtype, void *stream) {
+    if (B < 0) return fail(KLA_ERR_INVALID_ARG, "negative batch");
+    kla_status st = check_shape(H, dk, dv, kla::kChunk, dtype);
+    if (st != KLA_OK) return st;
+    if (!(eps >= 0.f)) return fail(KLA_ERR_INVALID_ARG, "eps must be >= 0");
+    if (B == 0) return ok();
+    if (!q || !k || !v || !alpha || !eta || !S || !o)
+        return fail(KLA_ERR_INVALID_ARG, "all pointers must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(S) || !aligned16(o) ||
+        !aligned4(alpha) || !aligned4(eta))
+        return fail(KLA_ERR_INVALID_ARG,
+                    "q, k, v, S, o must be 16-byte aligned, alpha and eta 4-byte");
+    if ((long)B * H > INT32_MAX) return fail(KLA_ERR_UNSUPPORTED, "B*H too large");
+    if (inject_launch_fault()) return fail(KLA_ERR_CUDA, "injected launch fault (KLA_FAULT_INJECT)");
+    cudaError_t e = kla::launch_decode(q, k, v, alpha, eta, eps, S, o, B * H, dk, dtype,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return ok();
+}
+
+int kla_workspace_status(const void *workspace, size_t workspace_bytes, void *stream) {
+    if (workspace == nullptr || workspace_bytes < kla::kWsHeader) return ok();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    unsigned word = 0;
+    e = cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (word == kla::kDevOk) return ok();
+    if (word == kla::kDevBadSeqlens)
+        return fail(KLA_ERR_INVALID_ARG, "cu_seqlens rejected on the device");
+    if (word == kla::kDevTimeout) return fail(KLA_ERR_TIMEOUT, "a device-side wait timed out");
+    return fail(KLA_ERR_CUDA, "unknown device status %u", word);
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// Internal declarations shared by the ABI layer and the kernel files.
+// Not part of the public interface (include/kla.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace kla {
+
+constexpr int kChunk = 64;             // chunk length C of the blockwise algorithm
+constexpr size_t kWsHeader = 256;      // status word area at the start of a workspace
+
+// Device status codes written into the workspace header (word 0).
+enum DevStatus : unsigned {
+    kDevOk = 0,
+    kDevBadSeqlens = 1,
+    kDevTimeout = 2,
+};
+
+// One prefill request after host validation.  Token row r of head h of a
+// [*, H, d] tensor sits at (r * H + h) * d.  Sequence n (fixed length: batch
+// index) covers rows seq_start(n) .. seq_start(n) + seq_len(n) - 1.
+struct Problem {
+    const void *q, *k, *v;
+    const float *alpha, *eta;
+    float eps;
+    const float *S0;
+    void *o;
+    float *S_T;
+    const int *cu_seqlens;   // device; nullptr for fixed length
+    int n_seq;               // B (fixed) or N (varlen)
+    int T;                   // fixed length (unused for varlen)
+    int total_T;             // total token rows
+    int H, d;                // heads, dk == dv
+    int dtype;               // kla_dtype
+    unsigned *status;        // device status word, or nullptr
+    void *ws;                // workspace after the header (path specific)
+    size_t ws_bytes;
+};
+
+// Counts kernel launches made by the library (kla_launch_count()).
+void note_launch(int n = 1);
+
+// Kernel-file entry points; each returns cudaSuccess or the launch error.
+cudaError_t launch_check_seqlens(const Problem &p, cudaStream_t s);
+cudaError_t launch_chunk_simt(const Problem &p, cudaStream_t s);
+cudaError_t launch_decode(const void *q, const void *k, const void *v,
+                          const float *alpha, const float *eta, float eps,
+                          float *S, void *o, int BH, int d, int dtype,
+                          cudaStream_t s);
+
+// Tensor-core (tcgen05) prefill for bf16, d = 128.
+size_t chunk_tc_workspace_bytes(long n_chunks_upper, int H);
+bool chunk_tc_supported(int d, int dtype);
+cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t s);
+
+}  // namespace kla

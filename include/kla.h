@@ -1,0 +1,167 @@
+/*
+ * kla.h -- C ABI of the GB300 (sm_103a) Kaczmarz Linear Attention library.
+ *
+ * The operation (Kaczmarz Linear Attention summary, gist.science
+ * 2605.08587, section "A Regra de Atualizacao KLA"), per (sequence, head),
+ * for t = 1..T, with a state S in R^{dk x dv} (section "Implementacao"):
+ *
+ *     beta_t = eta_t / (||k_t||^2 + eps)          (0 when the sum is 0)
+ *     S~     = alpha_t S_{t-1}                    (Gated DeltaNet scalar decay)
+ *     e_t    = v_t - S~^T k_t
+ *     S_t    = S~ + beta_t k_t e_t^T
+ *     o_t    = S_t^T q_t                          (read after the write)
+ *
+ * kla_chunk_fwd / kla_chunk_fwd_varlen compute it with the chunkwise-parallel
+ * (blockwise) algorithm that the summary says KLA keeps from Gated DeltaNet,
+ * with B = Diag(beta_1..beta_C) in the block solver (section
+ * "Implementacao"); kla_decode_step applies one token to stored states (the
+ * recurrent form behind the decode throughput of section "Eficiencia").
+ *
+ * Conventions for every entry point
+ *   - Tensors are dense, row-major, in device memory, owned by the caller.
+ *     The library never allocates, frees or retains device memory and keeps
+ *     no pointer after a call returns.
+ *   - `dtype` (kla_dtype) is the storage type of q, k, v and o.  alpha, eta
+ *     and the states are always fp32.  Arithmetic is fp32 (bf16 tensor-core
+ *     products with fp32 accumulation on the bf16 prefill path).
+ *   - Supported: dk == dv in {64, 128}, chunk == 64.  Other sizes return
+ *     KLA_ERR_UNSUPPORTED without launching anything.
+ *   - alpha must lie in (0, 1] and eps >= 0 (values are not scanned; outside
+ *     that range results are unspecified but every access stays in bounds).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous: a KLA_OK return means the work was validated and
+ *     enqueued; faults of the enqueued work surface on a later
+ *     synchronisation, and device-detected argument errors through
+ *     kla_workspace_status().
+ *   - Errors are returned as kla_status codes; nothing is thrown or aborted
+ *     across the ABI.  kla_last_error_message() gives a one-line detail for
+ *     the calling thread's last failure.
+ *   - q, k, v, o and the states must be 16-byte aligned, alpha and eta 4-byte
+ *     aligned; o and S_T may not alias inputs
+ *     except that S_T may equal S0.
+ */
+#ifndef KLA_H
+#define KLA_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define KLA_API __attribute__((visibility("default")))
+#else
+#define KLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KLA_OK = 0,
+    KLA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, negative size, bad cu_seqlens */
+    KLA_ERR_UNSUPPORTED = 2,   /* valid request outside the supported set */
+    KLA_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, attribute, ...) */
+    KLA_ERR_TIMEOUT = 4,       /* a bounded device-side wait gave up */
+    KLA_ERR_WORKSPACE = 5      /* workspace missing or smaller than required */
+} kla_status;
+
+typedef enum {
+    KLA_DTYPE_F32 = 0,
+    KLA_DTYPE_BF16 = 1
+} kla_dtype;
+
+/* Static string for a status code; never NULL. */
+KLA_API const char *kla_status_str(int status);
+
+/* One-line description of the calling thread's most recent failure
+ * ("" if none).  Valid until the next call on the same thread. */
+KLA_API const char *kla_last_error_message(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+KLA_API int kla_version(void);
+
+/* Number of CUDA kernels this library has enqueued since it was loaded
+ * (all threads, all devices).  Lets a caller count device work per call. */
+KLA_API unsigned long long kla_launch_count(void);
+
+/*
+ * Workspace bytes that kla_chunk_fwd needs for these sizes (0 when the
+ * chosen path needs none, in which case `workspace` may be NULL).  Returns 0
+ * as well for unsupported sizes; the call then reports the reason.
+ */
+KLA_API size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv,
+                                    int chunk, int dtype);
+
+/*
+ * Chunkwise prefill over a fixed-length batch.
+ *   q, k     : [B, T, H, dk]  dtype
+ *   v        : [B, T, H, dv]  dtype
+ *   alpha    : [B, T, H]      fp32 decay, in (0, 1]
+ *   eta      : [B, T, H]      fp32 relaxation gate
+ *   eps      : scalar stabiliser added once to ||k_t||^2
+ *   S0       : [B, H, dk, dv] fp32 initial states (dv fastest) or NULL = 0
+ *   o        : [B, T, H, dv]  dtype, written
+ *   S_T      : [B, H, dk, dv] fp32 final states, written; NULL = not needed;
+ *              may equal S0 (in-place state update)
+ *   workspace: device buffer of at least kla_chunk_fwd_workspace_size(...)
+ *              bytes, 256-byte aligned, owned by the caller; contents on
+ *              entry are ignored.  One workspace must not be shared by calls
+ *              that may run concurrently.
+ * T == 0 or B == 0 is valid and writes only S_T (= S0, or zeros).
+ */
+KLA_API int kla_chunk_fwd(const void *q, const void *k, const void *v,
+                  const float *alpha, const float *eta, float eps,
+                  const float *S0, void *o, float *S_T,
+                  int B, int T, int H, int dk, int dv, int chunk, int dtype,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes for kla_chunk_fwd_varlen (see kla_chunk_fwd_workspace_size). */
+KLA_API size_t kla_chunk_fwd_varlen_workspace_size(int N, int total_T, int H, int dk,
+                                           int dv, int chunk, int dtype);
+
+/*
+ * Chunkwise prefill over N packed sequences of different lengths.
+ *   q, k       : [total_T, H, dk]   v, o : [total_T, H, dv]
+ *   alpha, eta : [total_T, H]
+ *   cu_seqlens : device int32 [N + 1]; sequence n is token rows
+ *                cu_seqlens[n] .. cu_seqlens[n+1]-1.  Must satisfy
+ *                cu_seqlens[0] == 0, non-decreasing, cu_seqlens[N] == total_T.
+ *                The device checks this; a violation skips all work and is
+ *                reported by kla_workspace_status() as KLA_ERR_INVALID_ARG.
+ *                Empty sequences are allowed (their S_T is S0, or zeros).
+ *   S0, S_T    : [N, H, dk, dv] fp32 (S0 NULL = zero, S_T NULL = not needed)
+ * Chunks never straddle sequence boundaries; every sequence's last chunk
+ * may be partial.
+ */
+KLA_API int kla_chunk_fwd_varlen(const void *q, const void *k, const void *v,
+                         const float *alpha, const float *eta, float eps,
+                         const float *S0, void *o, float *S_T,
+                         const int *cu_seqlens, int N, int total_T,
+                         int H, int dk, int dv, int chunk, int dtype,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * One decode step: one new token for each of B*H (sequence, head) states,
+ * updated in place.
+ *   q, k       : [B, H, dk]  dtype     v, o : [B, H, dv] dtype
+ *   alpha, eta : [B, H] fp32
+ *   S          : [B, H, dk, dv] fp32, read and overwritten with S_t
+ * Each state is read once and written once.
+ */
+KLA_API int kla_decode_step(const void *q, const void *k, const void *v,
+                    const float *alpha, const float *eta, float eps,
+                    float *S, void *o, int B, int H, int dk, int dv, int dtype,
+                    void *stream);
+
+/*
+ * Synchronises `stream` and returns the status that the last prefill call
+ * using `workspace` recorded on the device: KLA_OK, KLA_ERR_INVALID_ARG
+ * (cu_seqlens rejected) or KLA_ERR_TIMEOUT.  A workspace of 0 bytes (NULL)
+ * has no status word and returns KLA_OK.
+ */
+KLA_API int kla_workspace_status(const void *workspace, size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KLA_H */

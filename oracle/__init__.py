@@ -41,11 +41,22 @@ _lock = threading.Lock()
 _lib = None
 
 
+def _elf_matches_host(path: str) -> bool:
+    import platform
+    want = {"x86_64": 62, "aarch64": 183, "arm64": 183}.get(platform.machine())
+    with open(path, "rb") as f:
+        head = f.read(20)
+    if len(head) < 20 or head[:4] != b"\x7fELF":
+        return False
+    return want is None or int.from_bytes(head[18:20], "little") == want
+
+
 def build(force: bool = False) -> str:
     """Compile kla_oracle.c into libkla_oracle.so next to it (gcc, -O2, no
     fast-math, no host-specific flags so it builds the same on x86 and Arm)."""
     stale = (not os.path.exists(_LIB_PATH)
-             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+             or not _elf_matches_host(_LIB_PATH))
     if force or stale:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
