@@ -61,8 +61,11 @@ def test_parity_small(B, T, H, d, dtype, sig, s0):
 
 
 def test_eta_zero_is_pure_decay():
+    """eta = 0: only the decay acts (alpha in [0.9, 1] keeps the product of
+    150 decays inside the fp32 range)."""
     inp = prefill_inputs(1, 150, 2, 64, 64, "fp32", seed=5, s0_var=1.0)
     inp["eta"].zero_()
+    inp["alpha"] = 0.9 + 0.1 * inp["alpha"]
     o, S = _run(inp)
     o_ref, S_ref = _oracle(inp)
     assert rel_err(o, o_ref) <= 1e-4 and rel_err(S, S_ref) <= 1e-4
