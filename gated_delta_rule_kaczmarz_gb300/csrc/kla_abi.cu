@@ -65,7 +65,10 @@ kla_status check_shape(int H, int dk, int dv, int chunk, int dtype) {
     return KLA_OK;
 }
 
-bool use_tc_path(int d, int dtype) { return kla::chunk_tc_supported(d, dtype); }
+// The tensor-core path needs at least one full 64-row TMA box of tokens.
+bool use_tc_path(int d, int dtype, long total_T) {
+    return total_T >= kla::kChunk && kla::chunk_tc_supported(d, dtype);
+}
 
 long chunks_upper(long n_seq, long total_T) {
     // every sequence adds at most one partial chunk
@@ -79,9 +82,9 @@ long n_chunks(bool varlen, long n_seq, long T, long total_T) {
 }
 
 size_t ws_bytes(bool varlen, long n_seq, long T, long total_T, int H, int d, int dtype) {
-    if (use_tc_path(d, dtype))
-        return kla::kWsHeader +
-               kla::chunk_tc_workspace_bytes(n_chunks(varlen, n_seq, T, total_T), H);
+    if (use_tc_path(d, dtype, total_T))
+        return kla::kWsHeader + kla::chunk_tc_workspace_bytes(n_chunks(varlen, n_seq, T, total_T),
+                                                              H, (int)n_seq);
     return varlen ? kla::kWsHeader : 0;
 }
 
@@ -116,15 +119,18 @@ kla_status run_prefill(kla::Problem &p, bool varlen, void *workspace, size_t wor
     if (inject_launch_fault()) return fail(KLA_ERR_CUDA, "injected launch fault (KLA_FAULT_INJECT)");
 
     cudaError_t e = cudaSuccess;
+    const bool tc = use_tc_path(p.d, p.dtype, p.total_T);
     if (p.status) {
-        if (varlen) {
+        // varlen: a device check of cu_seqlens writes the status (the
+        // tensor-core path does it in its own preparation kernel)
+        if (varlen && !tc) {
             e = kla::launch_check_seqlens(p, s);
         } else {
             e = cudaMemsetAsync(p.status, 0, sizeof(unsigned), s);
         }
         if (e != cudaSuccess) return cuda_fail(e, "status init");
     }
-    if (use_tc_path(p.d, p.dtype)) {
+    if (tc) {
         e = kla::launch_chunk_tc(p, n_chunks(varlen, p.n_seq, p.T, p.total_T), s);
     } else {
         e = kla::launch_chunk_simt(p, s);

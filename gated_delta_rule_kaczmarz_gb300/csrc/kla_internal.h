@@ -52,7 +52,7 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v,
                           cudaStream_t s);
 
 // Tensor-core (tcgen05) prefill for bf16, d = 128.
-size_t chunk_tc_workspace_bytes(long n_chunks_upper, int H);
+size_t chunk_tc_workspace_bytes(long n_chunks_upper, int H, int n_seq);
 bool chunk_tc_supported(int d, int dtype);
 cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t s);
 

@@ -46,6 +46,11 @@ CASES = [
     (2, 257, 4, 128, "bf16", 0.5, 0.01),
     (1, 500, 2, 128, "bf16", 1.0, 0.0),     # lognormal(0,1) key norms
     (2, 64, 2, 128, "bf16", 0.5, 0.0),
+    (1, 1, 2, 128, "bf16", 0.5, 0.01),      # fewer tokens than one chunk in total
+    (2, 63, 3, 128, "bf16", 0.5, 0.01),     # partial chunks only
+    (1, 65, 2, 128, "bf16", 1.0, 0.01),
+    (3, 129, 2, 128, "bf16", 0.5, 0.0),     # odd number of chunks per CTA pair
+    (1, 1000, 1, 128, "bf16", 1.0, 0.01),
 ]
 
 
@@ -58,6 +63,27 @@ def test_parity_small(B, T, H, d, dtype, sig, s0):
     assert o.dtype == inp["q"].dtype
     assert rel_err(o, o_ref) <= tol
     assert rel_err(S, S_ref) <= tol
+
+
+@pytest.mark.parametrize("varlen", [False, True])
+def test_bf16_d128_runs_on_the_tensor_core_kernels(varlen):
+    """bf16 with d = 128 takes the two-phase tcgen05 path: one intra-chunk
+    launch and one state-pass launch (plus a sequence-table launch for
+    varlen), and no CUDA-core chunk kernel."""
+    inp = prefill_inputs(2, 256, 2, 128, 128, "bf16", seed=11, s0_var=0.01)
+    d = cuda(inp)
+    n0 = kla.kla_launch_count()
+    if varlen:
+        cu = torch.tensor([0, 256, 512], dtype=torch.int32, device="cuda")
+        f = lambda x: x.reshape(512, *x.shape[2:])
+        kla.kla_chunk_fwd_varlen(f(d["q"]), f(d["k"]), f(d["v"]), f(d["alpha"]), f(d["eta"]),
+                                 d["eps"], cu, d["S0"])
+    else:
+        kla.kla_chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["eta"], d["eps"], d["S0"])
+    torch.cuda.synchronize()
+    assert kla.kla_launch_count() - n0 == (3 if varlen else 2)
+    ws = kla.kla_chunk_fwd_workspace_size(2, 256, 2, 128, 128)
+    assert ws > 256
 
 
 def test_eta_zero_is_pure_decay():
