@@ -66,24 +66,50 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(lib):
+    dp = ctypes.POINTER(ctypes.c_double)
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.kla_oracle_forward.restype = ctypes.c_int
+    lib.kla_oracle_forward.argtypes = [
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        dp, dp, dp, dp, dp, ctypes.c_double, dp, dp, dp, ctypes.c_int]
+    lib.kla_oracle_forward_varlen.restype = ctypes.c_int
+    lib.kla_oracle_forward_varlen.argtypes = [
+        ctypes.c_int, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        dp, dp, dp, dp, dp, ctypes.c_double, dp, dp, dp, ctypes.c_int]
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
             build()
-            lib = ctypes.CDLL(_LIB_PATH)
-            dp = ctypes.POINTER(ctypes.c_double)
-            ip = ctypes.POINTER(ctypes.c_int)
-            lib.kla_oracle_forward.restype = ctypes.c_int
-            lib.kla_oracle_forward.argtypes = [
-                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                dp, dp, dp, dp, dp, ctypes.c_double, dp, dp, dp, ctypes.c_int]
-            lib.kla_oracle_forward_varlen.restype = ctypes.c_int
-            lib.kla_oracle_forward_varlen.argtypes = [
-                ctypes.c_int, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                dp, dp, dp, dp, dp, ctypes.c_double, dp, dp, dp, ctypes.c_int]
-            _lib = lib
+            _lib = _bind(ctypes.CDLL(_LIB_PATH))
     return _lib
+
+
+def compile_variant(source_text: str, so_path: str):
+    """Compiles a modified copy of the oracle source (used by the tests that
+    plant mistakes in the oracle to show the pins catch them) and returns an
+    object with the same ``forward`` function as this module."""
+    src_path = so_path[:-3] + ".c"
+    with open(src_path, "w") as f:
+        f.write(source_text)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-fno-fast-math",
+                    "-ffp-contract=off", "-o", so_path, src_path], check=True)
+    lib = _bind(ctypes.CDLL(so_path))
+
+    class _Variant:
+        @staticmethod
+        def forward(q, k, v, alpha, eta, eps, S0=None, nthreads=1):
+            return _forward_with(lib, q, k, v, alpha, eta, eps, S0, nthreads)
+    return _Variant
+
+
+def source() -> str:
+    with open(_SRC) as f:
+        return f.read()
 
 
 def _f64(x) -> np.ndarray:
@@ -102,7 +128,10 @@ def _ptr(a):
 
 
 def forward(q, k, v, alpha, eta, eps, S0=None, nthreads: int = 1):
-    lib = _load()
+    return _forward_with(_load(), q, k, v, alpha, eta, eps, S0, nthreads)
+
+
+def _forward_with(lib, q, k, v, alpha, eta, eps, S0, nthreads):
     q, k, v, alpha, eta, S0 = map(_f64, (q, k, v, alpha, eta, S0))
     B, T, H, dk = q.shape
     dv = v.shape[-1]
