@@ -17,20 +17,20 @@
 //
 // Phase 1 (intra_kernel) is parallel over every (chunk, head): two chunks per
 // CTA so that every tensor-core product has M = 128 rows.  It computes
-// K K^T and Q K^T on tcgen05 (TMEM accumulators), solves T in fp32 by
-// forward substitution (one column per thread, registers), and forms
-// [W | U~] = (T diag(beta)) [diag(exp g) K | V] with a single N = 256 MMA.
-// W, U~, A (bf16) and g (fp32) go to the caller's workspace.
+// K K^T and Q K^T on tcgen05 (TMEM accumulators), inverts I + L in fp32 on
+// the CUDA cores in 32 x 32 blocks (forward substitution on the diagonal
+// blocks, two small products for the off-diagonal block), and forms
+// W = (T diag beta)(diag(exp g) K) and U~^T = V^T (T diag beta)^T with two
+// MMAs.  W, U~^T, A (bf16) and g (fp32) go to the caller's workspace.
 //
-// Phase 2 (state_kernel) walks the chunks of one (sequence, head) in order.
-// It works on transposed products so that M = dv = 128:
-//   P^T  = S^T W^T           (A = S^T bf16 in smem, B = W tile)
-//   X^T  = S^T Q^T
-//   U^T  = U~^T - P^T        (registers -> bf16 smem tile)
-//   Y^T  = U^T A^T
-//   Z^T  = (U diag(exp(g_C - g)))^T K
-//   O^T  = X^T diag(exp g) + Y^T ;  S^T <- exp(g_C) S^T + Z^T (fp32 in registers)
-// Its next chunk's tiles stream in by TMA while the current chunk computes.
+// Phase 2 (state_kernel) walks the chunks of one (sequence, head) in order:
+//   P^T = S^T W^T                       (M = dv = 128)
+//   U^T = U~^T - P^T                    (registers -> bf16 smem tile)
+//   O   = (diag(exp g) Q) S + A U       (M = 64 tokens, one accumulator)
+//   Z^T = U^T (diag(exp(g_C - g)) K)    (M = 128)
+//   S^T <- exp(g_C) S^T + Z^T           (fp32 in registers)
+// The next chunk's tiles stream in by TMA and are scaled in shared memory
+// while the current chunk's last products run.
 //
 // All waits are bounded (kla_tc.cuh); a wait that gives up sets the status
 // word to a timeout code and the CTA leaves after releasing TMEM.
@@ -65,7 +65,7 @@ struct TcParams {
     unsigned *status;
     float *g_ws;               // [slots][64]
     __nv_bfloat16 *W_ws;       // [slots][64][128]
-    __nv_bfloat16 *U_ws;       // [slots][64][128]
+    __nv_bfloat16 *UT_ws;      // [slots][128][64]  U~ transposed (feature-major)
     __nv_bfloat16 *A_ws;       // [slots][64][64]
 };
 
@@ -116,6 +116,26 @@ __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // a -> low half
     return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Packs 32 fp32 values (as raw bits) to bf16 and stores them (64 bytes).
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t (&r)[32]) {
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int v4 = 0; v4 < 4; ++v4)
+        d4[v4] = make_uint4(
+            pack_bf2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1])),
+            pack_bf2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3])),
+            pack_bf2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5])),
+            pack_bf2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7])));
+}
+
+// fp32 64 x 64 matrices in shared memory, one per chunk, rows of 64 floats;
+// the float4 index within a row is XORed with (row % 16) so that a thread per
+// row writing float4s, and a warp reading one row as a broadcast, are both
+// free of bank conflicts.  Offset of (row, col) within the matrix rows:
+__device__ __forceinline__ int lsw(int row, int col) {
+    return ((((col >> 2) ^ (row & 15))) << 2) | (col & 3);
 }
 
 // ===================================================================== phase 1
@@ -260,17 +280,23 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const long gidx0 = 2L * blockIdx.x + slot;
     const size_t slot_row = (size_t)(gidx0 * p.H + h) * C + t;   // row of this token in the ws
     if (ok) {
+        float *Lrow = sL + (size_t)(slot * 64 + t) * 64;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             uint32_t r[32];
             tmem_ld32(tb + lane_base + cb + half * 32, r);
             tmem_ld_wait();
-            float *Lrow = sL + (size_t)(slot * 64 + t) * 64 + half * 32;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int s = half * 32 + i;
-                const float gam = (s < t) ? __expf(gt - sG[cb + s]) : 0.f;
-                Lrow[i] = (s < t && t < nc) ? bt * gam * __uint_as_float(r[i]) : 0.f;
+            for (int i = 0; i < 32; i += 4) {
+                float v4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int s = half * 32 + i + e;
+                    v4[e] = (s < t && t < nc) ? bt * __expf(gt - sG[cb + s]) * __uint_as_float(r[i + e])
+                                              : 0.f;
+                }
+                *reinterpret_cast<float4 *>(Lrow + lsw(t, half * 32 + i)) =
+                    make_float4(v4[0], v4[1], v4[2], v4[3]);
             }
         }
 #pragma unroll
@@ -321,29 +347,128 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     __syncthreads();
     const bool abort2 = sAbort != 0;
 
-    // ---- T = (I + L)^{-1}: this thread solves column j = t of its chunk ----
-    float x[64];
+    // ---- T = (I + L)^{-1} in 32 x 32 blocks: T = [[D1, 0], [-D2 L21 D1, D2]],
+    //      D_b = (I + L_bb)^{-1} ----
     {
-        const float *Lb = sL + (size_t)slot * 64 * 64;
+        // (a) diagonal blocks: warp (p, b) solves D_b of chunk p, one column per lane
+        const int p = tid >> 6, b = (tid >> 5) & 1, c = lane, o = 32 * b;
+        float *Lb = sL + (size_t)(p * 64 + o) * 64;
+        float x[32];
 #pragma unroll
-        for (int tt = 0; tt < 64; ++tt) {
-            float acc = (tt == t) ? 1.f : 0.f;
-            const float *Lrow = Lb + tt * 64;
+        for (int r = 0; r < 32; ++r) {
+            const float *Lr = Lb + r * 64;
+            float a0 = (r == c) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int s = 0; s < tt; ++s) acc = fmaf(-Lrow[s], x[s], acc);
-            x[tt] = acc;
+            for (int s4 = 0; 4 * s4 < r; ++s4) {
+                const float4 l = *reinterpret_cast<const float4 *>(Lr + lsw(o + r, o + 4 * s4));
+                a0 = fmaf(-l.x, x[4 * s4], a0);
+                if (4 * s4 + 1 < r) a1 = fmaf(-l.y, x[4 * s4 + 1], a1);
+                if (4 * s4 + 2 < r) a2 = fmaf(-l.z, x[4 * s4 + 2], a2);
+                if (4 * s4 + 3 < r) a3 = fmaf(-l.w, x[4 * s4 + 3], a3);
+            }
+            x[r] = (a0 + a1) + (a2 + a3);
         }
-    }
-    __syncthreads();  // every thread is done with L; its region becomes the A operand
-
-    // ---- A operand = T diag(beta), block diagonal over the two chunks ----
-    {
-        const float bj = sBeta[tid];
-        unsigned char *slab = sQ + slot * 16384;   // columns of this chunk
+        __syncthreads();  // every diagonal block of L has been read
 #pragma unroll
-        for (int rr = 0; rr < 128; ++rr) {
-            const float val = ((rr >> 6) == slot) ? x[rr & 63] * bj : 0.f;
-            *reinterpret_cast<__nv_bfloat16 *>(slab + sw128_offset(rr, t)) = __float2bfloat16_rn(val);
+        for (int r = 0; r < 32; ++r) Lb[r * 64 + lsw(o + r, o + c)] = x[r];
+        __syncthreads();
+    }
+    {
+        // (b) M = L21 D1, then T21 = -D2 M; 4 x 4 output patch per thread
+        const int p = tid >> 6, q = tid & 63, pr = q >> 3, pc = q & 7;
+        float *Lp = sL + (size_t)p * 64 * 64;
+        float acc[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int n = 0; n < 4; ++n) acc[m][n] = 0.f;
+#pragma unroll
+        for (int s4 = 0; s4 < 8; ++s4) {
+            float4 a[4], bb[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int r = 32 + 4 * pr + m;
+                a[m] = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, 4 * s4));
+            }
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                const int r = 4 * s4 + n;
+                bb[n] = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, 4 * pc));
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float am[4] = {a[m].x, a[m].y, a[m].z, a[m].w};
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    acc[m][0] = fmaf(am[n], bb[n].x, acc[m][0]);
+                    acc[m][1] = fmaf(am[n], bb[n].y, acc[m][1]);
+                    acc[m][2] = fmaf(am[n], bb[n].z, acc[m][2]);
+                    acc[m][3] = fmaf(am[n], bb[n].w, acc[m][3]);
+                }
+            }
+        }
+        __syncthreads();  // L21 fully read
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int r = 32 + 4 * pr + m;
+            *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, 4 * pc)) =
+                make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+            acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+        }
+        __syncthreads();  // M stored where L21 was
+#pragma unroll
+        for (int s4 = 0; s4 < 8; ++s4) {
+            float4 a[4], bb[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int r = 32 + 4 * pr + m;
+                a[m] = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, 32 + 4 * s4));
+            }
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                const int r = 32 + 4 * s4 + n;
+                bb[n] = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, 4 * pc));
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float am[4] = {a[m].x, a[m].y, a[m].z, a[m].w};
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    acc[m][0] = fmaf(am[n], bb[n].x, acc[m][0]);
+                    acc[m][1] = fmaf(am[n], bb[n].y, acc[m][1]);
+                    acc[m][2] = fmaf(am[n], bb[n].z, acc[m][2]);
+                    acc[m][3] = fmaf(am[n], bb[n].w, acc[m][3]);
+                }
+            }
+        }
+        __syncthreads();  // M fully read
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int r = 32 + 4 * pr + m;
+            *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, 4 * pc)) =
+                make_float4(-acc[m][0], -acc[m][1], -acc[m][2], -acc[m][3]);
+        }
+        __syncthreads();  // T complete (fp32)
+    }
+
+    // ---- A operand = T diag(beta) in bf16, block diagonal over the two chunks ----
+    {
+        const float *Trow = sL + (size_t)(slot * 64 + t) * 64;
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float4 v = *reinterpret_cast<const float4 *>(Trow + lsw(t, 4 * i));
+            const float *bs = sBeta + slot * 64 + 4 * i;
+            pk[2 * i] = pack_bf2(v.x * bs[0], v.y * bs[1]);
+            pk[2 * i + 1] = pack_bf2(v.z * bs[2], v.w * bs[3]);
+        }
+        __syncthreads();  // T fully read; its region becomes the bf16 A tile
+        unsigned char *own = sQ + slot * 16384, *other = sQ + (1 - slot) * 16384;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            *reinterpret_cast<uint4 *>(own + sw128_offset(tid, ch * 8)) =
+                make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            *reinterpret_cast<uint4 *>(other + sw128_offset(tid, ch * 8)) = make_uint4(0u, 0u, 0u, 0u);
         }
     }
     fence_async_smem();
@@ -351,45 +476,54 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     __syncthreads();
     if (tid == 0 && !abort2) {
         tc_fence_after();
-        // [W | U~] = (T diag beta) [diag(exp g) K | V]: M=128, N=256, K=128 tokens.
-        // B is MN-major (rows = tokens): n-blocks of 64 at 16 KB stride
-        // (sK slab 0, sK slab 1, sV slab 0, sV slab 1).
-        const uint32_t idesc = idesc_bf16_f32(128, 256, false, true);
-        const uint32_t aA = smem_u32(sQ), aB = smem_u32(sK);
+        const uint32_t aA = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+        // W = (T diag beta) (diag(exp g) K): M = 128 tokens, N = 128, K = 128 tokens;
+        // B MN-major (rows = tokens), n-blocks of 64 features at 16 KB.
+        const uint32_t id_w = idesc_bf16_f32(128, 128, false, true);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t da = sdesc_sw128(aA + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-            const uint64_t db = sdesc_sw128(aB + ks * 2048, 16384, 1024);
-            mma_bf16(tb + 0, da, db, idesc, ks > 0);
-        }
+        for (int ks = 0; ks < 8; ++ks)
+            mma_bf16(tb + 0, sdesc_sw128(aA + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                     sdesc_sw128(aK + ks * 2048, 16384, 1024), id_w, ks > 0);
+        // U~^T = V^T (T diag beta)^T: M = 128 features (A = V, MN-major), N = 128
+        // tokens (B = the same T diag beta tile, K-major), K = 128 tokens.
+        const uint32_t id_u = idesc_bf16_f32(128, 128, true, false);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            mma_bf16(tb + 128, sdesc_sw128(aV + ks * 2048, 16384, 1024),
+                     sdesc_sw128(aA + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id_u, ks > 0);
         mma_commit(&bars[2]);
     }
     __syncthreads();
 
-    // ---- epilogue 2: W, U~ rows (bf16) and g to the workspace ----
+    // ---- epilogue 2: W rows, U~^T rows (bf16) and g to the workspace ----
     ok = !abort2 && mbar_wait(&bars[2], 0);
     if (!abort2 && !ok) set_status(p.status, kDevTimeout);
     tc_fence_after();
-    if (ok && valid[slot]) {
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            __nv_bfloat16 *dst_row = (part == 0 ? p.W_ws : p.U_ws) + slot_row * D;
+    if (ok) {
+        if (valid[slot]) {
+            __nv_bfloat16 *dst_row = p.W_ws + slot_row * D;
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 uint32_t r[32];
-                tmem_ld32(tb + lane_base + part * 128 + c4 * 32, r);
+                tmem_ld32(tb + lane_base + c4 * 32, r);
                 tmem_ld_wait();
-                uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c4 * 32);
+                store_bf16x32(dst_row + c4 * 32, r);
+            }
+            p.g_ws[slot_row] = gt;
+        }
+        // lane j of U~^T holds feature j for the tokens of both chunks
 #pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4)
-                    dst[v4] = make_uint4(
-                        pack_bf2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1])),
-                        pack_bf2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3])),
-                        pack_bf2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5])),
-                        pack_bf2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7])));
+        for (int q = 0; q < 2; ++q) {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tb + lane_base + 128 + q * 64, r0);
+            tmem_ld32(tb + lane_base + 128 + q * 64 + 32, r1);
+            tmem_ld_wait();
+            if (valid[q]) {
+                __nv_bfloat16 *dst = p.UT_ws + ((size_t)((2L * blockIdx.x + q) * p.H + h) * D + tid) * C;
+                store_bf16x32(dst, r0);
+                store_bf16x32(dst + 32, r1);
             }
         }
-        p.g_ws[slot_row] = gt;
     }
     tc_fence_before();
     __syncthreads();
@@ -398,16 +532,19 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
 // ===================================================================== phase 2
 constexpr int P2_THREADS = 256;
+// Stage layout (one chunk): W [64 t][128] (2 slabs), Q and K [64 t][128]
+// (2 slabs each, scaled in place by exp(g) and exp(g_C - g)), U~^T [128][64],
+// A [64][64], g [64].
 constexpr uint32_t ST_W = 0, ST_Q = 16384, ST_K = 32768, ST_U = 49152, ST_A = 65536,
-                   ST_G = 73728, ST_BYTES = 74752;   // stage layout (1 KB aligned pieces)
+                   ST_G = 73728, ST_BYTES = 74752;
 constexpr uint32_t ST_TX = 16384u * 4u + 8192u + 256u;  // bytes a stage receives
 constexpr uint32_t P2_OFF_S = 2 * ST_BYTES;             // S^T bf16 [128][128] (2 slabs)
 constexpr uint32_t P2_OFF_UT = P2_OFF_S + 32768;        // U^T bf16 [128][64]
-constexpr uint32_t P2_OFF_US = P2_OFF_UT + 16384;       // (U diag(exp(gC-g)))^T [128][64]
-constexpr uint32_t P2_SMEM = P2_OFF_US + 16384 + 1024;
+constexpr uint32_t P2_SMEM = P2_OFF_UT + 16384 + 1024;
 
-// TMEM columns (fp32): P^T 0..63, X^T 64..127, Y^T 128..191, Z^T 256..383.
-constexpr uint32_t TM_P = 0, TM_X = 64, TM_Y = 128, TM_Z = 256;
+// TMEM columns (fp32): P^T (M=128, N=64) 0..63; O (M=64, N=128) 64..191;
+// Z^T (M=128, N=128) 256..383.
+constexpr uint32_t TM_P = 0, TM_O = 64, TM_Z = 256;
 
 __device__ __forceinline__ void issue_stage(unsigned char *st, uint64_t *bar,
                                             const CUtensorMap *mq, const CUtensorMap *mk,
@@ -420,10 +557,33 @@ __device__ __forceinline__ void issue_stage(unsigned char *st, uint64_t *bar,
         tma_load_2d(st + ST_W + s * 8192, mw, bar, 64 * s, slot * C);
         tma_load_3d(st + ST_Q + s * 8192, mq, bar, 64 * s, h, row0);
         tma_load_3d(st + ST_K + s * 8192, mk, bar, 64 * s, h, row0);
-        tma_load_2d(st + ST_U + s * 8192, mu, bar, 64 * s, slot * C);
     }
+    tma_load_2d(st + ST_U, mu, bar, 0, slot * D);
     tma_load_2d(st + ST_A, ma, bar, 0, slot * C);
     bulk_load(st + ST_G, g_src, 256, bar);
+}
+
+// Scales a landed stage in place: Q rows by exp(g_t), K rows by
+// exp(g_C - g_t); rows at or past the chunk's valid length are cleared.
+// 256 threads: (Q or K) x 64 rows x (two 64-feature halves).
+__device__ __forceinline__ void scale_stage(unsigned char *st, int nc, int tid) {
+    const int which = tid >> 7, t = (tid >> 1) & 63, hp = tid & 1;
+    const float *g = reinterpret_cast<const float *>(st + ST_G);
+    const float f = which == 0 ? __expf(g[t]) : __expf(g[C - 1] - g[t]);
+    unsigned char *base = st + (which == 0 ? ST_Q : ST_K) + hp * 8192;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        uint4 *p4 = reinterpret_cast<uint4 *>(base + sw128_offset(t, ch * 8));
+        if (t < nc) {
+            const uint4 v = *p4;
+            *p4 = make_uint4(pack_bf2(f * bf_lo(v.x), f * bf_hi(v.x)),
+                             pack_bf2(f * bf_lo(v.y), f * bf_hi(v.y)),
+                             pack_bf2(f * bf_lo(v.z), f * bf_hi(v.z)),
+                             pack_bf2(f * bf_lo(v.w), f * bf_hi(v.w)));
+        } else {
+            *p4 = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
 }
 
 __global__ void __launch_bounds__(P2_THREADS, 1)
@@ -439,7 +599,6 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     unsigned char *sm = align1024(smraw);
     unsigned char *sS = sm + P2_OFF_S;
     unsigned char *sUt = sm + P2_OFF_UT;
-    unsigned char *sUs = sm + P2_OFF_US;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;
@@ -480,15 +639,13 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 #pragma unroll
     for (int i = 0; i < 64; ++i)
         Sr[i] = p.S0 ? p.S0[sbase + (size_t)(64 * half + i) * D + j] : 0.f;
-    // bf16 copy as the A operand S^T (row j, K-major, slab = half)
+    // bf16 copy as the operand S^T (row j, K-major, slab = half)
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch)
         *reinterpret_cast<uint4 *>(sS + half * 16384 + sw128_offset(j, ch * 8)) =
             make_uint4(pack_bf2(Sr[8 * ch + 0], Sr[8 * ch + 1]), pack_bf2(Sr[8 * ch + 2], Sr[8 * ch + 3]),
                        pack_bf2(Sr[8 * ch + 4], Sr[8 * ch + 5]), pack_bf2(Sr[8 * ch + 6], Sr[8 * ch + 7]));
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // barriers initialised, TMEM allocated
     tc_fence_after();
     const uint32_t tb = tslot;
 
@@ -499,119 +656,114 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                         p.g_ws + slot * C, h, (int)(start + (long)c * C), (int)slot);
         }
     }
+    if (nch > 0) {
+        if (!mbar_wait(&bar_ld[0], 0)) {
+            sAbort = 1;
+            set_status(p.status, kDevTimeout);
+        } else {
+            scale_stage(sm, (int)min((long)C, len), tid);
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
 
-    const uint32_t id_n64 = idesc_bf16_f32(128, 64, false, false);
+    const uint32_t id_p = idesc_bf16_f32(128, 64, false, false);
+    const uint32_t id_o = idesc_bf16_f32(64, 128, false, false);
     const uint32_t id_z = idesc_bf16_f32(128, 128, false, true);
-    bool abort = false;
-    for (int c = 0; c < nch; ++c) {
+    bool abort = sAbort != 0;
+    for (int c = 0; c < nch && !abort; ++c) {
         const int b = c & 1;
         unsigned char *st = sm + b * ST_BYTES;
-        const uint32_t par_ld = (uint32_t)((c >> 1) & 1);
         const uint32_t par = (uint32_t)(c & 1);
         const int nc = (int)min((long)C, len - (long)c * C);
         const long row0 = start + (long)c * C;
 
-        // ---- P^T = S^T W^T and X^T = S^T Q^T ----
+        // ---- P^T = S^T W^T ; O = (diag(exp g) Q) S ----
         if (tid == 0) {
-            if (!mbar_wait(&bar_ld[b], par_ld)) {
-                sAbort = 1;
-                set_status(p.status, kDevTimeout);
-            } else {
-                tc_fence_after();
-                const uint32_t aS = smem_u32(sS), aW = smem_u32(st + ST_W), aQ = smem_u32(st + ST_Q);
+            tc_fence_after();
+            const uint32_t aS = smem_u32(sS), aW = smem_u32(st + ST_W), aQ = smem_u32(st + ST_Q);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
-                    const uint32_t offS = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_bf16(tb + TM_P, sdesc_sw128(aS + offS, 16, 1024),
-                             sdesc_sw128(aW + off, 16, 1024), id_n64, ks > 0);
-                }
-                mma_commit(&bar_p);
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
+                const uint32_t offS = (ks >> 2) * 16384 + (ks & 3) * 32;
+                mma_bf16(tb + TM_P, sdesc_sw128(aS + offS, 16, 1024),
+                         sdesc_sw128(aW + off, 16, 1024), id_p, ks > 0);
+            }
+            mma_commit(&bar_p);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
-                    const uint32_t offS = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_bf16(tb + TM_X, sdesc_sw128(aS + offS, 16, 1024),
-                             sdesc_sw128(aQ + off, 16, 1024), id_n64, ks > 0);
-                }
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
+                const uint32_t offS = (ks >> 2) * 16384 + (ks & 3) * 32;
+                mma_bf16(tb + TM_O, sdesc_sw128(aQ + off, 16, 1024),
+                         sdesc_sw128(aS + offS, 16, 1024), id_o, ks > 0);
             }
         }
-        // every thread needs the stage's g and U~ as well
-        const bool landed = mbar_wait(&bar_ld[b], par_ld);
-        if (landed && nc < C) {
-            // partial chunk: clear K rows past its end (read only by the
-            // state-update product, issued after the next barrier)
-            for (int x = tid; x < (C - nc) * 16; x += P2_THREADS) {
-                const int row = nc + (x >> 4), sl = (x >> 3) & 1, ch = x & 7;
-                *reinterpret_cast<uint4 *>(st + ST_K + sl * 8192 + sw128_offset(row, ch * 8)) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        if (!landed || !mbar_wait(&bar_p, par)) {
+        if (!mbar_wait(&bar_p, par)) {
             set_status(p.status, kDevTimeout);
             sAbort = 1;
         }
-        __syncthreads();
-        if (sAbort) { abort = true; break; }
         tc_fence_after();
 
         // ---- U^T = U~^T - P^T for tokens [32*half, 32*half + 32) ----
-        const float *gch = reinterpret_cast<const float *>(st + ST_G);
-        const float gC = gch[C - 1];
         {
             uint32_t r[32];
             tmem_ld32(tb + lane_base + TM_P + half * 32, r);
             tmem_ld_wait();
-            const unsigned char *sU = st + ST_U + (j >> 6) * 8192;
-            uint32_t pu[16], ps[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const int t0 = half * 32 + i;
-                const float u0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                     sU + sw128_offset(t0, j & 63))) - __uint_as_float(r[i]);
-                const float u1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                     sU + sw128_offset(t0 + 1, j & 63))) - __uint_as_float(r[i + 1]);
-                pu[i / 2] = pack_bf2(u0, u1);
-                ps[i / 2] = pack_bf2(u0 * __expf(gC - gch[t0]), u1 * __expf(gC - gch[t0 + 1]));
-            }
-            // row j of the [128][64] K-major tiles, columns 32*half.. (4 x 16 B)
+            const unsigned char *sU = st + ST_U;
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
                 const uint32_t off = sw128_offset(j, half * 32 + v4 * 8);
-                *reinterpret_cast<uint4 *>(sUt + off) =
-                    make_uint4(pu[4 * v4], pu[4 * v4 + 1], pu[4 * v4 + 2], pu[4 * v4 + 3]);
-                *reinterpret_cast<uint4 *>(sUs + off) =
-                    make_uint4(ps[4 * v4], ps[4 * v4 + 1], ps[4 * v4 + 2], ps[4 * v4 + 3]);
+                const uint4 u = *reinterpret_cast<const uint4 *>(sU + off);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                uint32_t o4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float u0 = bf_lo(w[e]) - __uint_as_float(r[8 * v4 + 2 * e]);
+                    const float u1 = bf_hi(w[e]) - __uint_as_float(r[8 * v4 + 2 * e + 1]);
+                    o4[e] = pack_bf2(u0, u1);
+                }
+                *reinterpret_cast<uint4 *>(sUt + off) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
             }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // ---- Y^T = U^T A^T and Z^T = (U diag(exp(gC-g)))^T K ----
-        if (tid == 0) {
+        // ---- O += A U ; Z^T = U^T (diag(exp(g_C - g)) K) ----
+        if (tid == 0 && !sAbort) {
             tc_fence_after();
-            const uint32_t aUt = smem_u32(sUt), aUs = smem_u32(sUs);
-            const uint32_t aA = smem_u32(st + ST_A), aK = smem_u32(st + ST_K);
+            const uint32_t aUt = smem_u32(sUt), aA = smem_u32(st + ST_A), aK = smem_u32(st + ST_K);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tb + TM_Y, sdesc_sw128(aUt + ks * 32, 16, 1024),
-                         sdesc_sw128(aA + ks * 32, 16, 1024), id_n64, ks > 0);
+                mma_bf16(tb + TM_O, sdesc_sw128(aA + ks * 32, 16, 1024),
+                         sdesc_sw128(aUt + ks * 32, 16, 1024), id_o, 1u);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tb + TM_Z, sdesc_sw128(aUs + ks * 32, 16, 1024),
+                mma_bf16(tb + TM_Z, sdesc_sw128(aUt + ks * 32, 16, 1024),
                          sdesc_sw128(aK + ks * 2048, 8192, 1024), id_z, ks > 0);
             mma_commit(&bar_s);
         }
+
+        // ---- meanwhile: the next chunk's tiles land; scale them in place ----
+        if (c + 1 < nch) {
+            unsigned char *st1 = sm + (b ^ 1) * ST_BYTES;
+            if (!mbar_wait(&bar_ld[b ^ 1], (uint32_t)(((c + 1) >> 1) & 1))) {
+                set_status(p.status, kDevTimeout);
+                sAbort = 1;
+            } else {
+                scale_stage(st1, (int)min((long)C, len - (long)(c + 1) * C), tid);
+            }
+        }
+
         if (!mbar_wait(&bar_s, par)) {
             set_status(p.status, kDevTimeout);
             sAbort = 1;
         }
         tc_fence_after();
-
-        // ---- S^T <- exp(gC) S^T + Z^T ; new bf16 copy of S^T ----
         if (!sAbort) {
-            const float egC = __expf(gC);
+            // ---- S^T <- exp(g_C) S^T + Z^T ; new bf16 copy of S^T ----
+            const float egC = __expf(reinterpret_cast<const float *>(st + ST_G)[C - 1]);
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
                 uint32_t r[32];
@@ -629,18 +781,17 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                                pack_bf2(Sr[8 * ch + 4], Sr[8 * ch + 5]),
                                pack_bf2(Sr[8 * ch + 6], Sr[8 * ch + 7]));
 
-            // ---- O^T = X^T diag(exp g) + Y^T -> o[t][j] ----
-            uint32_t rx[32], ry[32];
-            tmem_ld32(tb + lane_base + TM_X + half * 32, rx);
-            tmem_ld32(tb + lane_base + TM_Y + half * 32, ry);
+            // ---- O rows -> o: the M = 64 accumulator keeps row t = 16*quarter + lane
+            //      (lane < 16) in TMEM lane 32*quarter + lane ----
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tb + lane_base + TM_O + half * 64, r0);
+            tmem_ld32(tb + lane_base + TM_O + half * 64 + 32, r1);
             tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int t = half * 32 + i;
-                if (t < nc) {
-                    const float ov = fmaf(__expf(gch[t]), __uint_as_float(rx[i]), __uint_as_float(ry[i]));
-                    p.o[((size_t)(row0 + t) * p.H + h) * D + j] = __float2bfloat16_rn(ov);
-                }
+            const int t = 16 * quarter + lane;
+            if (lane < 16 && t < nc) {
+                __nv_bfloat16 *dst = p.o + ((size_t)(row0 + t) * p.H + h) * D + half * 64;
+                store_bf16x32(dst, r0);
+                store_bf16x32(dst + 32, r1);
             }
         }
         fence_async_smem();
@@ -758,10 +909,10 @@ bool map_3d_rows(CUtensorMap *m, const void *base, int H, long rows) {
            CUDA_SUCCESS;
 }
 
-bool map_2d(CUtensorMap *m, const void *base, int cols, long rows) {
+bool map_2d(CUtensorMap *m, const void *base, int cols, long rows, int box_rows) {
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)C};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t es[2] = {1, 1};
     return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -818,7 +969,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     tp.status = p.status;
     tp.g_ws = reinterpret_cast<float *>(ws + L.g);
     tp.W_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.W);
-    tp.U_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.U);
+    tp.UT_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.U);
     tp.A_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.A);
     int *chunk_prefix = reinterpret_cast<int *>(ws + L.meta);
     int *order = chunk_prefix + p.n_seq + 1;
@@ -828,8 +979,8 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     CUtensorMap mq, mk, mv, mw, mu, ma;
     const long slots = n_chunks_upper * p.H;
     if (!map_3d_rows(&mq, p.q, p.H, p.total_T) || !map_3d_rows(&mk, p.k, p.H, p.total_T) ||
-        !map_3d_rows(&mv, p.v, p.H, p.total_T) || !map_2d(&mw, tp.W_ws, D, slots * C) ||
-        !map_2d(&mu, tp.U_ws, D, slots * C) || !map_2d(&ma, tp.A_ws, C, slots * C))
+        !map_3d_rows(&mv, p.v, p.H, p.total_T) || !map_2d(&mw, tp.W_ws, D, slots * C, C) ||
+        !map_2d(&mu, tp.UT_ws, C, slots * D, D) || !map_2d(&ma, tp.A_ws, C, slots * C, C))
         return cudaErrorInvalidValue;
 
     cudaError_t e;

@@ -108,8 +108,13 @@ def test_varlen_equals_per_sequence_calls():
                                    d["v"][None, a:b].contiguous(), d["alpha"][None, a:b].contiguous(),
                                    d["eta"][None, a:b].contiguous(), d["eps"], d["S0"][n:n + 1])
         torch.cuda.synchronize()
-        torch.testing.assert_close(o[a:b].float(), o1[0].float(), rtol=0, atol=1e-2)
-        torch.testing.assert_close(S[n], S1[0], rtol=0, atol=1e-3)
+        # a sequence shorter than one chunk runs on the fp32 CUDA-core kernel when
+        # called alone, so the two results agree to the bf16 tolerance, not bitwise
+        assert rel_err(o[a:b], o1[0].cpu().double().numpy()) <= 2e-2
+        assert rel_err(S[n], S1[0].cpu().double().numpy()) <= 2e-2
+        if b - a >= 64:
+            torch.testing.assert_close(S[n], S1[0], rtol=0, atol=0)
+            torch.testing.assert_close(o[a:b], o1[0], rtol=0, atol=0)
 
 
 @pytest.mark.parametrize("bad", ["decreasing", "first_nonzero", "last_mismatch"])
