@@ -7,6 +7,7 @@ draws seeded synthetic inputs.
 from .binding import (  # noqa: F401
     KlaError,
     kla_chunk_fwd,
+    kla_chunk_fwd_noalloc,
     kla_chunk_fwd_varlen,
     kla_chunk_fwd_varlen_workspace_size,
     kla_chunk_fwd_workspace_size,

@@ -77,6 +77,9 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
                                              I, I, I, I, I, I, I, vp, Z, vp]
         lib.kla_decode_step.restype = I
         lib.kla_decode_step.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, I, I, I, I, I, vp]
+        lib.kla_chunk_fwd_noalloc.restype = I
+        lib.kla_chunk_fwd_noalloc.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, fp,
+                                              I, I, I, I, I, I, I, vp]
         lib.kla_workspace_status.restype = I
         lib.kla_workspace_status.argtypes = [vp, Z, vp]
         _lib = lib
@@ -174,6 +177,31 @@ def kla_chunk_fwd(q, k, v, alpha, eta, eps, S0=None, o=None, S_T=None, workspace
     st = lib.kla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps),
                            _ptr(S0), _ptr(o), _ptr(S_T), B, T, H, dk, dv, chunk, dt,
                            _ptr(workspace), wsb, _stream(stream))
+    _check(st)
+    return o, S_T
+
+
+def kla_chunk_fwd_noalloc(q, k, v, alpha, eta, eps, S0=None, o=None, S_T=None, stream=None,
+                          chunk=CHUNK):
+    """kla_chunk_fwd for callers that cannot allocate device memory while the
+    prefill runs: the library uses its built-in device array as workspace
+    (sizes that need more than KLA_NOALLOC_SCRATCH_BYTES raise KlaError).
+    Calls sharing that array must not overlap on the GPU.  Pass ``o`` and
+    ``S_T`` to avoid any allocation here as well.  Returns (o, S_T)."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _need(q, "q"); _need(k, "k", q.dtype, (B, T, H, dk)); _need(v, "v", q.dtype, (B, T, H, dv))
+    _need(alpha, "alpha", torch.float32, (B, T, H)); _need(eta, "eta", torch.float32, (B, T, H))
+    _need(S0, "S0", torch.float32, (B, H, dk, dv))
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    _need(o, "o", q.dtype, (B, T, H, dv))
+    _need(S_T, "S_T", torch.float32, (B, H, dk, dv))
+    st = lib.kla_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps),
+                                   _ptr(S0), _ptr(o), _ptr(S_T), B, T, H, dk, dv, chunk, dt,
+                                   _stream(stream))
     _check(st)
     return o, S_T
 

@@ -141,6 +141,10 @@ kla_status run_prefill(kla::Problem &p, bool varlen, void *workspace, size_t wor
 
 }  // namespace
 
+namespace kla {
+void set_error_message(const char *msg) { g_last_error = msg; }
+}  // namespace kla
+
 extern "C" {
 
 const char *kla_status_str(int status) {

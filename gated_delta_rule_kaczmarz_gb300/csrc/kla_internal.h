@@ -43,6 +43,9 @@ struct Problem {
 // Counts kernel launches made by the library (kla_launch_count()).
 void note_launch(int n = 1);
 
+// Sets the calling thread's kla_last_error_message() text.
+void set_error_message(const char *msg);
+
 // Kernel-file entry points; each returns cudaSuccess or the launch error.
 cudaError_t launch_check_seqlens(const Problem &p, cudaStream_t s);
 cudaError_t launch_chunk_simt(const Problem &p, cudaStream_t s);

@@ -153,6 +153,38 @@ KLA_API int kla_decode_step(const void *q, const void *k, const void *v,
                     void *stream);
 
 /*
+ * Size in bytes of the device array that kla_chunk_fwd_noalloc uses as its
+ * workspace (64 MiB).  Every GPU that loads this library holds it until the
+ * process exits.
+ */
+#define KLA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * kla_chunk_fwd without a workspace argument: the same computation, results
+ * and errors as kla_chunk_fwd, for callers that cannot allocate device memory
+ * when they run the prefill (a framework that owns all device memory through
+ * its own pool, a plugin interface that is handed only input and output
+ * pointers, or a serving loop that cannot afford cudaMalloc's device-wide
+ * synchronisation).  The pages this library follows have no counterpart of
+ * this call; it is a deployment convenience.
+ *   - It allocates nothing.  Its scratch is one file-scope device array of
+ *     KLA_NOALLOC_SCRATCH_BYTES; sizes whose kla_chunk_fwd_workspace_size()
+ *     exceeds that are rejected with KLA_ERR_WORKSPACE before any device work.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the array, which keeps the last call's contents (the
+ *     status word it needs zeroed is cleared by every call).  Calls that
+ *     overlap on the GPU race on it: serialise them on one stream.
+ * Arguments are those of kla_chunk_fwd minus workspace and workspace_bytes.
+ */
+KLA_API int kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                                  const float *alpha, const float *eta, float eps,
+                                  const float *S0, void *o, float *S_T,
+                                  int B, int T, int H, int dk, int dv, int chunk,
+                                  int dtype, void *stream);
+
+/*
  * Synchronises `stream` and returns the status that the last prefill call
  * using `workspace` recorded on the device: KLA_OK, KLA_ERR_INVALID_ARG
  * (cu_seqlens rejected) or KLA_ERR_TIMEOUT.  A workspace of 0 bytes (NULL)
