@@ -23,14 +23,14 @@
 // W = (T diag beta)(diag(exp g) K) and U~^T = V^T (T diag beta)^T with two
 // MMAs.  W, U~^T, A (bf16) and g (fp32) go to the caller's workspace.
 //
-// Phase 2 (state_kernel) walks the chunks of one (sequence, head) in order:
-//   P^T = S^T W^T                       (M = dv = 128)
-//   U^T = U~^T - P^T                    (registers -> bf16 smem tile)
-//   O   = (diag(exp g) Q) S + A U       (M = 64 tokens, one accumulator)
-//   Z^T = U^T (diag(exp(g_C - g)) K)    (M = 128)
-//   S^T <- exp(g_C) S^T + Z^T           (fp32 in registers)
-// The next chunk's tiles stream in by TMA and are scaled in shared memory
-// while the current chunk's last products run.
+// Phase 2 (state_kernel) walks the chunks of one (sequence, head) in order,
+// every product with M = dv = 128 rows:
+//   P^T = S^T W^T ;  U^T = U~^T - P^T   (registers -> bf16 smem tile)
+//   Z^T = U^T (diag(exp(g_C - g)) K) ;  S^T <- exp(g_C) S^T + Z^T (fp32 registers)
+//   O^T = S^T (diag(exp g) Q)^T + U^T A^T
+// The serial chain is P -> U -> Z -> S; the output products and their
+// stores, and the scaling of the next chunk's Q and K tiles (which stream in
+// by TMA two chunks ahead), run beside it on separate warps.
 //
 // All waits are bounded (kla_tc.cuh); a wait that gives up sets the status
 // word to a timeout code and the CTA leaves after releasing TMEM.
@@ -531,7 +531,13 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 }
 
 // ===================================================================== phase 2
-constexpr int P2_THREADS = 256;
+// Warp roles: warps 0-7 ("main") run the serial chain of the state pass
+// (thread (j, half): dv index j = its TMEM lane, half = which 32 tokens / 64
+// state rows it handles); thread 0 also issues every MMA and TMA load.
+// Warps 8-11 ("aux") scale the next chunk's Q and K tiles in shared memory and
+// write each chunk's output rows (TMA store of a staged tile).
+constexpr int P2_MAIN = 256, P2_AUX = 128, P2_THREADS = P2_MAIN + P2_AUX;
+constexpr uint32_t BAR_MAIN = 1, BAR_AUX = 2;    // named barrier ids
 // Stage layout (one chunk): W [64 t][128] (2 slabs), Q and K [64 t][128]
 // (2 slabs each, scaled in place by exp(g) and exp(g_C - g)), U~^T [128][64],
 // A [64][64], g [64].
@@ -540,10 +546,11 @@ constexpr uint32_t ST_W = 0, ST_Q = 16384, ST_K = 32768, ST_U = 49152, ST_A = 65
 constexpr uint32_t ST_TX = 16384u * 4u + 8192u + 256u;  // bytes a stage receives
 constexpr uint32_t P2_OFF_S = 2 * ST_BYTES;             // S^T bf16 [128][128] (2 slabs)
 constexpr uint32_t P2_OFF_UT = P2_OFF_S + 32768;        // U^T bf16 [128][64]
-constexpr uint32_t P2_SMEM = P2_OFF_UT + 16384 + 1024;
+constexpr uint32_t P2_OFF_O = P2_OFF_UT + 16384;        // output staging [64 t][128] (2 slabs)
+constexpr uint32_t P2_SMEM = P2_OFF_O + 16384 + 1024;
 
-// TMEM columns (fp32): P^T (M=128, N=64) 0..63; O (M=64, N=128) 64..191;
-// Z^T (M=128, N=128) 256..383.
+// TMEM columns (fp32, M = 128 lanes = dv): P^T 0..63; O^T double buffer
+// 64..127 and 128..191; Z^T 256..383.
 constexpr uint32_t TM_P = 0, TM_O = 64, TM_Z = 256;
 
 __device__ __forceinline__ void issue_stage(unsigned char *st, uint64_t *bar,
@@ -563,25 +570,28 @@ __device__ __forceinline__ void issue_stage(unsigned char *st, uint64_t *bar,
     bulk_load(st + ST_G, g_src, 256, bar);
 }
 
-// Scales a landed stage in place: Q rows by exp(g_t), K rows by
+// Aux warps: scale a landed stage in place, Q rows by exp(g_t) and K rows by
 // exp(g_C - g_t); rows at or past the chunk's valid length are cleared.
-// 256 threads: (Q or K) x 64 rows x (two 64-feature halves).
-__device__ __forceinline__ void scale_stage(unsigned char *st, int nc, int tid) {
-    const int which = tid >> 7, t = (tid >> 1) & 63, hp = tid & 1;
+// Thread a (0..127): row a % 64 of Q (a < 64) or K (a >= 64), both halves.
+__device__ __forceinline__ void scale_stage(unsigned char *st, int nc, int a) {
+    const int which = a >> 6, t = a & 63;
     const float *g = reinterpret_cast<const float *>(st + ST_G);
     const float f = which == 0 ? __expf(g[t]) : __expf(g[C - 1] - g[t]);
-    unsigned char *base = st + (which == 0 ? ST_Q : ST_K) + hp * 8192;
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        uint4 *p4 = reinterpret_cast<uint4 *>(base + sw128_offset(t, ch * 8));
-        if (t < nc) {
-            const uint4 v = *p4;
-            *p4 = make_uint4(pack_bf2(f * bf_lo(v.x), f * bf_hi(v.x)),
-                             pack_bf2(f * bf_lo(v.y), f * bf_hi(v.y)),
-                             pack_bf2(f * bf_lo(v.z), f * bf_hi(v.z)),
-                             pack_bf2(f * bf_lo(v.w), f * bf_hi(v.w)));
-        } else {
-            *p4 = make_uint4(0u, 0u, 0u, 0u);
+    for (int hp = 0; hp < 2; ++hp) {
+        unsigned char *base = st + (which == 0 ? ST_Q : ST_K) + hp * 8192;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            uint4 *p4 = reinterpret_cast<uint4 *>(base + sw128_offset(t, ch * 8));
+            if (t < nc) {
+                const uint4 v = *p4;
+                *p4 = make_uint4(pack_bf2(f * bf_lo(v.x), f * bf_hi(v.x)),
+                                 pack_bf2(f * bf_lo(v.y), f * bf_hi(v.y)),
+                                 pack_bf2(f * bf_lo(v.z), f * bf_hi(v.z)),
+                                 pack_bf2(f * bf_lo(v.w), f * bf_hi(v.w)));
+            } else {
+                *p4 = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
     }
 }
@@ -589,19 +599,23 @@ __device__ __forceinline__ void scale_stage(unsigned char *st, int nc, int tid) 
 __global__ void __launch_bounds__(P2_THREADS, 1)
 state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
              const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
-             const __grid_constant__ CUtensorMap ma, const TcParams p) {
+             const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mo,
+             const TcParams p) {
     extern __shared__ unsigned char smraw[];
-    __shared__ uint64_t bar_ld[2];
-    __shared__ uint64_t bar_p, bar_s;
+    __shared__ uint64_t bar_ld[2], bar_scaled[2], bar_ofree[2];
+    __shared__ uint64_t bar_p, bar_s, bar_o;
     __shared__ uint32_t tslot;
     __shared__ int sAbort;
 
     unsigned char *sm = align1024(smraw);
     unsigned char *sS = sm + P2_OFF_S;
     unsigned char *sUt = sm + P2_OFF_UT;
+    unsigned char *sO = sm + P2_OFF_O;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3;
+    const bool is_main = tid < P2_MAIN;
+    const int half = (warp >> 2) & 1;           // main warps only
     const int j = quarter * 32 + lane;          // dv index = TMEM lane of this thread
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
 
@@ -622,10 +636,14 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const size_t sbase = ((size_t)seq * p.H + h) * D * D;
 
     if (tid == 0) {
-        mbar_init(&bar_ld[0], 1);
-        mbar_init(&bar_ld[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_ld[i], 1);
+            mbar_init(&bar_scaled[i], P2_AUX);
+            mbar_init(&bar_ofree[i], P2_AUX);
+        }
         mbar_init(&bar_p, 1);
         mbar_init(&bar_s, 1);
+        mbar_init(&bar_o, 1);
         fence_mbar_init();
         sAbort = 0;
     }
@@ -634,18 +652,23 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         tmem_relinquish();
     }
 
-    // fp32 master state: this thread keeps S[i][j] for i in [64*half, 64*half+64)
+    // fp32 master state (main warps): S[i][j] for i in [64*half, 64*half+64)
     float Sr[64];
+    if (is_main) {
 #pragma unroll
-    for (int i = 0; i < 64; ++i)
-        Sr[i] = p.S0 ? p.S0[sbase + (size_t)(64 * half + i) * D + j] : 0.f;
-    // bf16 copy as the operand S^T (row j, K-major, slab = half)
+        for (int i = 0; i < 64; ++i)
+            Sr[i] = p.S0 ? p.S0[sbase + (size_t)(64 * half + i) * D + j] : 0.f;
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4 *>(sS + half * 16384 + sw128_offset(j, ch * 8)) =
-            make_uint4(pack_bf2(Sr[8 * ch + 0], Sr[8 * ch + 1]), pack_bf2(Sr[8 * ch + 2], Sr[8 * ch + 3]),
-                       pack_bf2(Sr[8 * ch + 4], Sr[8 * ch + 5]), pack_bf2(Sr[8 * ch + 6], Sr[8 * ch + 7]));
-    __syncthreads();  // barriers initialised, TMEM allocated
+        for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4 *>(sS + half * 16384 + sw128_offset(j, ch * 8)) =
+                make_uint4(pack_bf2(Sr[8 * ch + 0], Sr[8 * ch + 1]),
+                           pack_bf2(Sr[8 * ch + 2], Sr[8 * ch + 3]),
+                           pack_bf2(Sr[8 * ch + 4], Sr[8 * ch + 5]),
+                           pack_bf2(Sr[8 * ch + 6], Sr[8 * ch + 7]));
+        fence_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();  // barriers initialised, TMEM allocated, S^T staged
     tc_fence_after();
     const uint32_t tb = tslot;
 
@@ -656,161 +679,215 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                         p.g_ws + slot * C, h, (int)(start + (long)c * C), (int)slot);
         }
     }
-    if (nch > 0) {
-        if (!mbar_wait(&bar_ld[0], 0)) {
-            sAbort = 1;
-            set_status(p.status, kDevTimeout);
-        } else {
-            scale_stage(sm, (int)min((long)C, len), tid);
-        }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
 
-    const uint32_t id_p = idesc_bf16_f32(128, 64, false, false);
-    const uint32_t id_o = idesc_bf16_f32(64, 128, false, false);
-    const uint32_t id_z = idesc_bf16_f32(128, 128, false, true);
-    bool abort = sAbort != 0;
-    for (int c = 0; c < nch && !abort; ++c) {
-        const int b = c & 1;
-        unsigned char *st = sm + b * ST_BYTES;
-        const uint32_t par = (uint32_t)(c & 1);
-        const int nc = (int)min((long)C, len - (long)c * C);
-        const long row0 = start + (long)c * C;
+    if (is_main) {
+        const uint32_t id_64 = idesc_bf16_f32(128, 64, false, false);
+        const uint32_t id_z = idesc_bf16_f32(128, 128, false, true);
+        for (int c = 0; c < nch; ++c) {
+            const int b = c & 1, ob = c & 1;
+            unsigned char *st = sm + b * ST_BYTES;
+            const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c >> 1) & 1);
 
-        // ---- P^T = S^T W^T ; O = (diag(exp g) Q) S ----
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t aS = smem_u32(sS), aW = smem_u32(st + ST_W), aQ = smem_u32(st + ST_Q);
+            // ---- P^T = S^T W^T ; O^T = S^T (diag(exp g) Q)^T ----
+            if (tid == 0) {
+                bool okw = mbar_wait(&bar_scaled[b], par_st);
+                if (okw && c >= 2) okw = mbar_wait(&bar_ofree[ob], (uint32_t)(((c - 2) >> 1) & 1));
+                if (!okw) {
+                    sAbort = 1;
+                    set_status(p.status, kDevTimeout);
+                } else {
+                    tc_fence_after();
+                    const uint32_t aS = smem_u32(sS), aW = smem_u32(st + ST_W),
+                                   aQ = smem_u32(st + ST_Q);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
-                const uint32_t offS = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_bf16(tb + TM_P, sdesc_sw128(aS + offS, 16, 1024),
-                         sdesc_sw128(aW + off, 16, 1024), id_p, ks > 0);
-            }
-            mma_commit(&bar_p);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
+                        const uint32_t offS = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16(tb + TM_P, sdesc_sw128(aS + offS, 16, 1024),
+                                 sdesc_sw128(aW + off, 16, 1024), id_64, ks > 0);
+                    }
+                    mma_commit(&bar_p);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
-                const uint32_t offS = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_bf16(tb + TM_O, sdesc_sw128(aQ + off, 16, 1024),
-                         sdesc_sw128(aS + offS, 16, 1024), id_o, ks > 0);
-            }
-        }
-        if (!mbar_wait(&bar_p, par)) {
-            set_status(p.status, kDevTimeout);
-            sAbort = 1;
-        }
-        tc_fence_after();
-
-        // ---- U^T = U~^T - P^T for tokens [32*half, 32*half + 32) ----
-        {
-            uint32_t r[32];
-            tmem_ld32(tb + lane_base + TM_P + half * 32, r);
-            tmem_ld_wait();
-            const unsigned char *sU = st + ST_U;
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-                const uint32_t off = sw128_offset(j, half * 32 + v4 * 8);
-                const uint4 u = *reinterpret_cast<const uint4 *>(sU + off);
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-                uint32_t o4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float u0 = bf_lo(w[e]) - __uint_as_float(r[8 * v4 + 2 * e]);
-                    const float u1 = bf_hi(w[e]) - __uint_as_float(r[8 * v4 + 2 * e + 1]);
-                    o4[e] = pack_bf2(u0, u1);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
+                        const uint32_t offS = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_bf16(tb + TM_O + 64 * ob, sdesc_sw128(aS + offS, 16, 1024),
+                                 sdesc_sw128(aQ + off, 16, 1024), id_64, ks > 0);
+                    }
                 }
-                *reinterpret_cast<uint4 *>(sUt + off) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
             }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- O += A U ; Z^T = U^T (diag(exp(g_C - g)) K) ----
-        if (tid == 0 && !sAbort) {
-            tc_fence_after();
-            const uint32_t aUt = smem_u32(sUt), aA = smem_u32(st + ST_A), aK = smem_u32(st + ST_K);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tb + TM_O, sdesc_sw128(aA + ks * 32, 16, 1024),
-                         sdesc_sw128(aUt + ks * 32, 16, 1024), id_o, 1u);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tb + TM_Z, sdesc_sw128(aUt + ks * 32, 16, 1024),
-                         sdesc_sw128(aK + ks * 2048, 8192, 1024), id_z, ks > 0);
-            mma_commit(&bar_s);
-        }
-
-        // ---- meanwhile: the next chunk's tiles land; scale them in place ----
-        if (c + 1 < nch) {
-            unsigned char *st1 = sm + (b ^ 1) * ST_BYTES;
-            if (!mbar_wait(&bar_ld[b ^ 1], (uint32_t)(((c + 1) >> 1) & 1))) {
+            if (!mbar_wait(&bar_ld[b], par_st) || !mbar_wait(&bar_p, par)) {
                 set_status(p.status, kDevTimeout);
                 sAbort = 1;
-            } else {
-                scale_stage(st1, (int)min((long)C, len - (long)(c + 1) * C), tid);
             }
-        }
+            tc_fence_after();
 
-        if (!mbar_wait(&bar_s, par)) {
-            set_status(p.status, kDevTimeout);
-            sAbort = 1;
-        }
-        tc_fence_after();
-        if (!sAbort) {
-            // ---- S^T <- exp(g_C) S^T + Z^T ; new bf16 copy of S^T ----
-            const float egC = __expf(reinterpret_cast<const float *>(st + ST_G)[C - 1]);
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
+            // ---- U^T = U~^T - P^T for tokens [32*half, 32*half + 32) ----
+            {
                 uint32_t r[32];
-                tmem_ld32(tb + lane_base + TM_Z + half * 64 + c2 * 32, r);
+                tmem_ld32(tb + lane_base + TM_P + half * 32, r);
                 tmem_ld_wait();
+                const unsigned char *sU = st + ST_U;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    Sr[c2 * 32 + i] = fmaf(egC, Sr[c2 * 32 + i], __uint_as_float(r[i]));
+                for (int v4 = 0; v4 < 4; ++v4) {
+                    const uint32_t off = sw128_offset(j, half * 32 + v4 * 8);
+                    const uint4 u = *reinterpret_cast<const uint4 *>(sU + off);
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                    uint32_t o4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float u0 = bf_lo(w[e]) - __uint_as_float(r[8 * v4 + 2 * e]);
+                        const float u1 = bf_hi(w[e]) - __uint_as_float(r[8 * v4 + 2 * e + 1]);
+                        o4[e] = pack_bf2(u0, u1);
+                    }
+                    *reinterpret_cast<uint4 *>(sUt + off) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                }
             }
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4 *>(sS + half * 16384 + sw128_offset(j, ch * 8)) =
-                    make_uint4(pack_bf2(Sr[8 * ch + 0], Sr[8 * ch + 1]),
-                               pack_bf2(Sr[8 * ch + 2], Sr[8 * ch + 3]),
-                               pack_bf2(Sr[8 * ch + 4], Sr[8 * ch + 5]),
-                               pack_bf2(Sr[8 * ch + 6], Sr[8 * ch + 7]));
+            fence_async_smem();
+            tc_fence_before();
+            named_sync(BAR_MAIN, P2_MAIN);
 
-            // ---- O rows -> o: the M = 64 accumulator keeps row t = 16*quarter + lane
-            //      (lane < 16) in TMEM lane 32*quarter + lane ----
+            // ---- Z^T = U^T (diag(exp(g_C - g)) K) first (it gates the next chunk),
+            //      then O^T += U^T A^T ----
+            if (tid == 0 && !sAbort) {
+                tc_fence_after();
+                const uint32_t aUt = smem_u32(sUt), aA = smem_u32(st + ST_A),
+                               aK = smem_u32(st + ST_K);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tb + TM_Z, sdesc_sw128(aUt + ks * 32, 16, 1024),
+                             sdesc_sw128(aK + ks * 2048, 8192, 1024), id_z, ks > 0);
+                mma_commit(&bar_s);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tb + TM_O + 64 * ob, sdesc_sw128(aUt + ks * 32, 16, 1024),
+                             sdesc_sw128(aA + ks * 32, 16, 1024), id_64, 1u);
+                mma_commit(&bar_o);
+            }
+            if (!mbar_wait(&bar_s, par)) {
+                set_status(p.status, kDevTimeout);
+                sAbort = 1;
+            }
+            tc_fence_after();
+
+            // ---- S^T <- exp(g_C) S^T + Z^T ; new bf16 copy of S^T ----
+            if (!sAbort) {
+                const float egC = __expf(reinterpret_cast<const float *>(st + ST_G)[C - 1]);
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t r[32];
+                    tmem_ld32(tb + lane_base + TM_Z + half * 64 + c2 * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        Sr[c2 * 32 + i] = fmaf(egC, Sr[c2 * 32 + i], __uint_as_float(r[i]));
+                }
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4 *>(sS + half * 16384 + sw128_offset(j, ch * 8)) =
+                        make_uint4(pack_bf2(Sr[8 * ch + 0], Sr[8 * ch + 1]),
+                                   pack_bf2(Sr[8 * ch + 2], Sr[8 * ch + 3]),
+                                   pack_bf2(Sr[8 * ch + 4], Sr[8 * ch + 5]),
+                                   pack_bf2(Sr[8 * ch + 6], Sr[8 * ch + 7]));
+            }
+            fence_async_smem();
+            tc_fence_before();
+            named_sync(BAR_MAIN, P2_MAIN);
+            if (sAbort) break;
+
+            // ---- refill this stage with chunk c + 2 once O^T += U^T A^T has read it ----
+            if (tid == 0 && c + 2 < nch) {
+                if (!mbar_wait(&bar_o, par)) {
+                    sAbort = 1;
+                    set_status(p.status, kDevTimeout);
+                } else {
+                    const long slot = (chunk0 + c + 2) * p.H + h;
+                    issue_stage(st, &bar_ld[b], &mq, &mk, &mw, &mu, &ma, p.g_ws + slot * C, h,
+                                (int)(start + (long)(c + 2) * C), (int)slot);
+                }
+            }
+        }
+        if (!sAbort && p.S_T) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)(64 * half + i) * D + j] = Sr[i];
+        }
+    } else {
+        // ----------------------------------------------------------------- aux warps
+        const int a = tid - P2_MAIN;     // 0..127; TMEM lane quarter = warp & 3
+        const bool leader = a == 0;
+        if (nch > 0) {
+            if (!mbar_wait(&bar_ld[0], 0)) {
+                sAbort = 1;
+                set_status(p.status, kDevTimeout);
+            } else {
+                scale_stage(sm, (int)min((long)C, len), a);
+            }
+            fence_async_smem();
+            mbar_arrive(&bar_scaled[0]);
+        }
+        for (int c = 0; c < nch && !sAbort; ++c) {
+            const int ob = c & 1;
+            // scale the next chunk as soon as it lands
+            if (c + 1 < nch) {
+                const int b1 = (c + 1) & 1;
+                if (!mbar_wait(&bar_ld[b1], (uint32_t)(((c + 1) >> 1) & 1))) {
+                    sAbort = 1;
+                    set_status(p.status, kDevTimeout);
+                    break;
+                }
+                scale_stage(sm + b1 * ST_BYTES, (int)min((long)C, len - (long)(c + 1) * C), a);
+                fence_async_smem();
+                mbar_arrive(&bar_scaled[b1]);
+            }
+            // output rows of chunk c: O^T row j (64 tokens) from TMEM
+            if (!mbar_wait(&bar_o, (uint32_t)(c & 1))) {
+                sAbort = 1;
+                set_status(p.status, kDevTimeout);
+                break;
+            }
+            tc_fence_after();
             uint32_t r0[32], r1[32];
-            tmem_ld32(tb + lane_base + TM_O + half * 64, r0);
-            tmem_ld32(tb + lane_base + TM_O + half * 64 + 32, r1);
+            tmem_ld32(tb + lane_base + TM_O + 64 * ob, r0);
+            tmem_ld32(tb + lane_base + TM_O + 64 * ob + 32, r1);
             tmem_ld_wait();
-            const int t = 16 * quarter + lane;
-            if (lane < 16 && t < nc) {
-                __nv_bfloat16 *dst = p.o + ((size_t)(row0 + t) * p.H + h) * D + half * 64;
-                store_bf16x32(dst, r0);
-                store_bf16x32(dst + 32, r1);
+            tc_fence_before();
+            mbar_arrive(&bar_ofree[ob]);
+            const int nc = (int)min((long)C, len - (long)c * C);
+            const long row0 = start + (long)c * C;
+            if (nc == C) {
+                // full chunk: stage [64 t][128] (SW128, 2 slabs) and store with TMA
+                if (leader) bulk_wait_group_read0();
+                named_sync(BAR_AUX, P2_AUX);
+                unsigned char *slab = sO + (j >> 6) * 8192;
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    *reinterpret_cast<__nv_bfloat16 *>(slab + sw128_offset(t, j & 63)) =
+                        __float2bfloat16_rn(__uint_as_float(r0[t]));
+                    *reinterpret_cast<__nv_bfloat16 *>(slab + sw128_offset(t + 32, j & 63)) =
+                        __float2bfloat16_rn(__uint_as_float(r1[t]));
+                }
+                fence_async_smem();
+                named_sync(BAR_AUX, P2_AUX);
+                if (leader) {
+                    tma_store_3d(&mo, sO, 0, h, (int)row0);
+                    tma_store_3d(&mo, sO + 8192, 64, h, (int)row0);
+                    bulk_commit_group();
+                }
+            } else {
+                // partial last chunk: plain stores of the valid rows only
+                __nv_bfloat16 *dst = p.o + (size_t)row0 * p.H * D + (size_t)h * D + j;
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    if (t < nc)
+                        dst[(size_t)t * p.H * D] = __float2bfloat16_rn(__uint_as_float(r0[t]));
+                    if (t + 32 < nc)
+                        dst[(size_t)(t + 32) * p.H * D] = __float2bfloat16_rn(__uint_as_float(r1[t]));
+                }
             }
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (sAbort) { abort = true; break; }
-
-        // ---- refill this stage with chunk c + 2 ----
-        if (tid == 0 && c + 2 < nch) {
-            const long slot = (chunk0 + c + 2) * p.H + h;
-            issue_stage(st, &bar_ld[b], &mq, &mk, &mw, &mu, &ma, p.g_ws + slot * C, h,
-                        (int)(start + (long)(c + 2) * C), (int)slot);
-        }
+        if (leader) bulk_wait_group0();
     }
 
-    if (!abort && p.S_T) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)(64 * half + i) * D + j] = Sr[i];
-    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 512);
@@ -976,11 +1053,12 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     tp.chunk_prefix = p.cu_seqlens ? chunk_prefix : nullptr;
     tp.order = p.cu_seqlens ? order : nullptr;
 
-    CUtensorMap mq, mk, mv, mw, mu, ma;
+    CUtensorMap mq, mk, mv, mw, mu, ma, mo;
     const long slots = n_chunks_upper * p.H;
     if (!map_3d_rows(&mq, p.q, p.H, p.total_T) || !map_3d_rows(&mk, p.k, p.H, p.total_T) ||
         !map_3d_rows(&mv, p.v, p.H, p.total_T) || !map_2d(&mw, tp.W_ws, D, slots * C, C) ||
-        !map_2d(&mu, tp.UT_ws, C, slots * D, D) || !map_2d(&ma, tp.A_ws, C, slots * C, C))
+        !map_2d(&mu, tp.UT_ws, C, slots * D, D) || !map_2d(&ma, tp.A_ws, C, slots * C, C) ||
+        !map_3d_rows(&mo, p.o, p.H, p.total_T))
         return cudaErrorInvalidValue;
 
     cudaError_t e;
@@ -1004,7 +1082,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     intra_kernel<<<g1, P1_THREADS, P1_SMEM, s>>>(mq, mk, mv, tp);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    state_kernel<<<(unsigned)(p.n_seq * p.H), P2_THREADS, P2_SMEM, s>>>(mq, mk, mw, mu, ma, tp);
+    state_kernel<<<(unsigned)(p.n_seq * p.H), P2_THREADS, P2_SMEM, s>>>(mq, mk, mw, mu, ma, mo, tp);
     note_launch();
     return cudaGetLastError();
 }
