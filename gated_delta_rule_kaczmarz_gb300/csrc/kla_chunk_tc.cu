@@ -16,10 +16,10 @@
 //   S' = exp(g_C) S + K^T diag(exp(g_C - g)) U
 //
 // Phase 1 (intra_kernel) is parallel over every (chunk, head): two chunks per
-// CTA so that every tensor-core product has M = 128 rows.  It computes
-// K K^T and Q K^T on tcgen05 (TMEM accumulators), inverts I + L in fp32 on
-// the CUDA cores in 32 x 32 blocks (forward substitution on the diagonal
-// blocks, two small products for the off-diagonal block), and forms
+// work item so that every tensor-core product has M = 128 rows; CTAs are
+// persistent.  It computes K K^T and Q K^T on tcgen05 (TMEM accumulators),
+// inverts I + L in fp32 on the CUDA cores (forward substitution on 16 x 16
+// diagonal blocks, then two doubling steps made of small products), and forms
 // W = (T diag beta)(diag(exp g) K) and U~^T = V^T (T diag beta)^T with two
 // MMAs.  W, U~^T, A (bf16) and g (fp32) go to the caller's workspace.
 //
@@ -138,13 +138,97 @@ __device__ __forceinline__ int lsw(int row, int col) {
     return ((((col >> 2) ^ (row & 15))) << 2) | (col & 3);
 }
 
+// One doubling step of the blocked inverse, in place in the fp32 L storage
+// of both chunks: for every diagonal block of size 2n whose two diagonal
+// n x n blocks already hold D1 = (I + L11)^{-1} and D2 = (I + L22)^{-1},
+// replace its lower-left block L21 by -D2 L21 D1.  128 threads; each computes
+// an (n/8) x 4 patch of the n x n products.
+template <int n>
+__device__ __forceinline__ void merge_level(float *sL, int tid) {
+    constexpr int nblk = 64 / (2 * n);               // blocks of size 2n per chunk
+    constexpr int tpb = 128 / (2 * nblk);            // threads per block (both chunks)
+    constexpr int rows = n * n / 4 / tpb;            // patch rows per thread (4 columns each)
+    static_assert(rows * 4 * tpb == n * n, "patch tiling");
+    const int blkid = tid / tpb, q = tid % tpb;
+    const int p = blkid / nblk, o = 2 * n * (blkid % nblk);
+    constexpr int pcols = n / 4;                     // column patches per row band
+    const int pr = q / pcols, pc = q % pcols;        // rows [rows*pr, +rows), cols [4pc, +4)
+    float *Lp = sL + (size_t)p * 64 * 64;
+    float acc[rows][4];
+    // M = L21 D1
+#pragma unroll
+    for (int m = 0; m < rows; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+#pragma unroll 2
+    for (int s4 = 0; s4 < n / 4; ++s4) {
+        float4 bb[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int r = o + 4 * s4 + e;
+            bb[e] = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, o + 4 * pc));
+        }
+#pragma unroll
+        for (int m = 0; m < rows; ++m) {
+            const int r = o + n + rows * pr + m;
+            const float4 a = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, o + 4 * s4));
+            const float am[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[m][0] = fmaf(am[e], bb[e].x, acc[m][0]);
+                acc[m][1] = fmaf(am[e], bb[e].y, acc[m][1]);
+                acc[m][2] = fmaf(am[e], bb[e].z, acc[m][2]);
+                acc[m][3] = fmaf(am[e], bb[e].w, acc[m][3]);
+            }
+        }
+    }
+    __syncthreads();  // L21 fully read
+#pragma unroll
+    for (int m = 0; m < rows; ++m) {
+        const int r = o + n + rows * pr + m;
+        *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, o + 4 * pc)) =
+            make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+        acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+    }
+    __syncthreads();  // M stored where L21 was
+    // X = -D2 M
+#pragma unroll 2
+    for (int s4 = 0; s4 < n / 4; ++s4) {
+        float4 bb[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int r = o + n + 4 * s4 + e;
+            bb[e] = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, o + 4 * pc));
+        }
+#pragma unroll
+        for (int m = 0; m < rows; ++m) {
+            const int r = o + n + rows * pr + m;
+            const float4 a = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, o + n + 4 * s4));
+            const float am[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[m][0] = fmaf(am[e], bb[e].x, acc[m][0]);
+                acc[m][1] = fmaf(am[e], bb[e].y, acc[m][1]);
+                acc[m][2] = fmaf(am[e], bb[e].z, acc[m][2]);
+                acc[m][3] = fmaf(am[e], bb[e].w, acc[m][3]);
+            }
+        }
+    }
+    __syncthreads();  // M fully read
+#pragma unroll
+    for (int m = 0; m < rows; ++m) {
+        const int r = o + n + rows * pr + m;
+        *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, o + 4 * pc)) =
+            make_float4(-acc[m][0], -acc[m][1], -acc[m][2], -acc[m][3]);
+    }
+    __syncthreads();
+}
+
 // ===================================================================== phase 1
 constexpr int P1_THREADS = 128;
 constexpr uint32_t P1_SMEM = 3 * 32768 + 1024;  // K, V, Q/L/A regions + alignment slack
 
 __global__ void __launch_bounds__(P1_THREADS, 2)
 intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-             const __grid_constant__ CUtensorMap mv, const TcParams p) {
+             const __grid_constant__ CUtensorMap mv, const TcParams p, long n_pairs) {
     extern __shared__ unsigned char smraw[];
     __shared__ uint64_t bars[3];
     __shared__ uint32_t tslot;
@@ -157,47 +241,56 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     unsigned char *sQ = sm + 65536;   // Q tile -> fp32 L[2][64][64] -> A operand T diag(beta)
     float *sL = reinterpret_cast<float *>(sQ);
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.y;
+    const int tid0 = threadIdx.x;
     if (status_bad(p.status)) return;
 
-    int seqs[2], ncs[2];
-    long row0s[2];
-    bool valid[2];
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        valid[q] = slot_info(p, 2L * blockIdx.x + q, seqs[q], row0s[q], ncs[q]);
-        if (!valid[q]) { ncs[q] = 0; row0s[q] = 0; }
-    }
-    if (!valid[0] && !valid[1]) return;
-
-    const int slot = tid >> 6, t = tid & 63;
-    const int nc = ncs[slot];
-
-    if (tid == 0) {
+    if (tid0 == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
         mbar_init(&bars[2], 1);
         fence_mbar_init();
         sAbort = 0;
     }
-    if (warp == 0) {
+    if ((tid0 >> 5) == 0) {
         tmem_alloc(&tslot, 256);
         tmem_relinquish();
     }
     __syncthreads();
     tc_fence_after();
+
+    // Persistent: work items are (pair of chunks, head), head fastest, so that
+    // CTAs running side by side read the same token rows of different heads.
+    const long n_items = n_pairs * p.H;
+    uint32_t ph = 0;   // mbarrier phase parity of this CTA's current item
+    for (long item = blockIdx.x; item < n_items; item += gridDim.x) {
+    // The thread index is re-read through an opaque move every item so that
+    // the compiler does not hoist (and keep live) the many thread-dependent
+    // shared-memory addresses across items.
+    int tid = tid0;
+    asm volatile("" : "+r"(tid));
+    const int warp = tid >> 5, lane = tid & 31;
+    const int slot = tid >> 6, t = tid & 63;
     const uint32_t tb = tslot;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const long pair = item / p.H;
+    const int h = (int)(item % p.H);
+    int seq0, seq1, nc0, nc1;
+    long r00, r01;
+    const bool v0 = slot_info(p, 2 * pair, seq0, r00, nc0);
+    const bool v1 = slot_info(p, 2 * pair + 1, seq1, r01, nc1);
+    if (!v0) { nc0 = 0; r00 = 0; }
+    if (!v1) { nc1 = 0; r01 = 0; }
+    if (!v0 && !v1) continue;
+    const int nc = slot ? nc1 : nc0;
+    const bool vslot = slot ? v1 : v0;
 
     if (tid == 0) {
-        tma_prefetch_map(&mk);
         mbar_expect_tx(&bars[0], 3u * 32768u);
 #pragma unroll
         for (int q = 0; q < 2; ++q)
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
-                const int z = (int)row0s[q];
+                const int z = (int)(q ? r01 : r00);
                 tma_load_3d(sK + s * 16384 + q * 8192, &mk, &bars[0], 64 * s, h, z);
                 tma_load_3d(sQ + s * 16384 + q * 8192, &mq, &bars[0], 64 * s, h, z);
                 tma_load_3d(sV + s * 16384 + q * 8192, &mv, &bars[0], 64 * s, h, z);
@@ -207,7 +300,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     // ---- decay: g = inclusive prefix sum of log alpha within each chunk ----
     float a = 1.f, et = 0.f;
     if (t < nc) {
-        const size_t row = (size_t)(row0s[slot] + t) * p.H + h;
+        const size_t row = (size_t)((slot ? r01 : r00) + t) * p.H + h;
         a = p.alpha[row];
         et = p.eta[row];
     }
@@ -223,7 +316,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     sG[tid] = (float)gs;
 
     // ---- tiles landed: Gram products on the tensor cores ----
-    if (!mbar_wait(&bars[0], 0)) {
+    if (!mbar_wait(&bars[0], ph)) {
         sAbort = 1;
         set_status(p.status, kDevTimeout);
     }
@@ -271,54 +364,53 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     __syncthreads();
 
     // ---- epilogue 1: L = strict_lower(beta Gamma o KK^T) (fp32 smem), A = lower(Gamma o QK^T) ----
-    bool ok = !abort1 && mbar_wait(&bars[1], 0);
+    bool ok = !abort1 && mbar_wait(&bars[1], ph);
     if (!abort1 && !ok) set_status(p.status, kDevTimeout);
     tc_fence_after();
     const float gt = sG[tid];
     const float bt = sBeta[tid];
     const int cb = slot * 64;
-    const long gidx0 = 2L * blockIdx.x + slot;
+    const long gidx0 = 2L * pair + slot;
     const size_t slot_row = (size_t)(gidx0 * p.H + h) * C + t;   // row of this token in the ws
     if (ok) {
         float *Lrow = sL + (size_t)(slot * 64 + t) * 64;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint32_t r[32];
-            tmem_ld32(tb + lane_base + cb + half * 32, r);
+#pragma unroll 1
+        for (int g16 = 0; g16 < 4; ++g16) {
+            uint32_t r[16];
+            tmem_ld16(tb + lane_base + cb + g16 * 16, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
+            for (int i = 0; i < 16; i += 4) {
                 float v4[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int s = half * 32 + i + e;
+                    const int s = g16 * 16 + i + e;
                     v4[e] = (s < t && t < nc) ? bt * __expf(gt - sG[cb + s]) * __uint_as_float(r[i + e])
                                               : 0.f;
                 }
-                *reinterpret_cast<float4 *>(Lrow + lsw(t, half * 32 + i)) =
+                *reinterpret_cast<float4 *>(Lrow + lsw(t, g16 * 16 + i)) =
                     make_float4(v4[0], v4[1], v4[2], v4[3]);
             }
         }
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint32_t r[32];
-            tmem_ld32(tb + lane_base + 128 + cb + half * 32, r);
+#pragma unroll 1
+        for (int g16 = 0; g16 < 4; ++g16) {
+            uint32_t r[16];
+            tmem_ld16(tb + lane_base + 128 + cb + g16 * 16, r);
             tmem_ld_wait();
-            uint32_t pk[16];
+            uint32_t pk[8];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const int s = half * 32 + i;
+            for (int i = 0; i < 16; i += 2) {
+                const int s = g16 * 16 + i;
                 const float a0 = (s <= t && t < nc)
                                      ? __expf(gt - sG[cb + s]) * __uint_as_float(r[i]) : 0.f;
                 const float a1 = (s + 1 <= t && t < nc)
                                      ? __expf(gt - sG[cb + s + 1]) * __uint_as_float(r[i + 1]) : 0.f;
                 pk[i / 2] = pack_bf2(a0, a1);
             }
-            if (valid[slot]) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.A_ws + slot_row * 64 + half * 32);
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4)
-                    dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            if (vslot) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.A_ws + slot_row * 64 + g16 * 16);
+                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
         }
         // K row -> diag(exp g) K; rows past the chunk's end (another
@@ -326,9 +418,9 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         // nothing from them can reach the products.
         const float gam_t = __expf(gt);
         const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
+#pragma unroll 1
         for (int s = 0; s < 2; ++s)
-#pragma unroll
+#pragma unroll 2
             for (int ch = 0; ch < 8; ++ch) {
                 uint4 *pk4 = reinterpret_cast<uint4 *>(sK + s * 16384 + sw128_offset(tid, ch * 8));
                 if (t < nc) {
@@ -347,109 +439,37 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     __syncthreads();
     const bool abort2 = sAbort != 0;
 
-    // ---- T = (I + L)^{-1} in 32 x 32 blocks: T = [[D1, 0], [-D2 L21 D1, D2]],
-    //      D_b = (I + L_bb)^{-1} ----
+    // ---- T = (I + L)^{-1}, built up in block sizes 16 -> 32 -> 64: the
+    //      diagonal 16 x 16 blocks by forward substitution, then at each level
+    //      [[D1, 0], [X, D2]] with X = -D2 L21 D1 from two small products ----
     {
-        // (a) diagonal blocks: warp (p, b) solves D_b of chunk p, one column per lane
-        const int p = tid >> 6, b = (tid >> 5) & 1, c = lane, o = 32 * b;
+        // diagonal 16 x 16 blocks: 16 threads per block, one column each
+        const int p = tid >> 6, blk = (tid >> 4) & 3, c = tid & 15, o = 16 * blk;
         float *Lb = sL + (size_t)(p * 64 + o) * 64;
-        float x[32];
+        float x[16];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
+        for (int r = 0; r < 16; ++r) {
             const float *Lr = Lb + r * 64;
-            float a0 = (r == c) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            float a0 = (r == c) ? 1.f : 0.f, a1 = 0.f;
 #pragma unroll
-            for (int s4 = 0; 4 * s4 < r; ++s4) {
-                const float4 l = *reinterpret_cast<const float4 *>(Lr + lsw(o + r, o + 4 * s4));
-                a0 = fmaf(-l.x, x[4 * s4], a0);
-                if (4 * s4 + 1 < r) a1 = fmaf(-l.y, x[4 * s4 + 1], a1);
-                if (4 * s4 + 2 < r) a2 = fmaf(-l.z, x[4 * s4 + 2], a2);
-                if (4 * s4 + 3 < r) a3 = fmaf(-l.w, x[4 * s4 + 3], a3);
+            for (int s4 = 0; s4 < 4; ++s4) {
+                if (4 * s4 < r) {
+                    const float4 l = *reinterpret_cast<const float4 *>(Lr + lsw(o + r, o + 4 * s4));
+                    a0 = fmaf(-l.x, x[4 * s4], a0);
+                    if (4 * s4 + 1 < r) a1 = fmaf(-l.y, x[4 * s4 + 1], a1);
+                    if (4 * s4 + 2 < r) a0 = fmaf(-l.z, x[4 * s4 + 2], a0);
+                    if (4 * s4 + 3 < r) a1 = fmaf(-l.w, x[4 * s4 + 3], a1);
+                }
             }
-            x[r] = (a0 + a1) + (a2 + a3);
+            x[r] = a0 + a1;
         }
-        __syncthreads();  // every diagonal block of L has been read
+        __syncthreads();  // the diagonal blocks of L have been read
 #pragma unroll
-        for (int r = 0; r < 32; ++r) Lb[r * 64 + lsw(o + r, o + c)] = x[r];
+        for (int r = 0; r < 16; ++r) Lb[r * 64 + lsw(o + r, o + c)] = x[r];
         __syncthreads();
     }
-    {
-        // (b) M = L21 D1, then T21 = -D2 M; 4 x 4 output patch per thread
-        const int p = tid >> 6, q = tid & 63, pr = q >> 3, pc = q & 7;
-        float *Lp = sL + (size_t)p * 64 * 64;
-        float acc[4][4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-            for (int n = 0; n < 4; ++n) acc[m][n] = 0.f;
-#pragma unroll
-        for (int s4 = 0; s4 < 8; ++s4) {
-            float4 a[4], bb[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int r = 32 + 4 * pr + m;
-                a[m] = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, 4 * s4));
-            }
-#pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                const int r = 4 * s4 + n;
-                bb[n] = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, 4 * pc));
-            }
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const float am[4] = {a[m].x, a[m].y, a[m].z, a[m].w};
-#pragma unroll
-                for (int n = 0; n < 4; ++n) {
-                    acc[m][0] = fmaf(am[n], bb[n].x, acc[m][0]);
-                    acc[m][1] = fmaf(am[n], bb[n].y, acc[m][1]);
-                    acc[m][2] = fmaf(am[n], bb[n].z, acc[m][2]);
-                    acc[m][3] = fmaf(am[n], bb[n].w, acc[m][3]);
-                }
-            }
-        }
-        __syncthreads();  // L21 fully read
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int r = 32 + 4 * pr + m;
-            *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, 4 * pc)) =
-                make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
-            acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
-        }
-        __syncthreads();  // M stored where L21 was
-#pragma unroll
-        for (int s4 = 0; s4 < 8; ++s4) {
-            float4 a[4], bb[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int r = 32 + 4 * pr + m;
-                a[m] = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, 32 + 4 * s4));
-            }
-#pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                const int r = 32 + 4 * s4 + n;
-                bb[n] = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, 4 * pc));
-            }
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const float am[4] = {a[m].x, a[m].y, a[m].z, a[m].w};
-#pragma unroll
-                for (int n = 0; n < 4; ++n) {
-                    acc[m][0] = fmaf(am[n], bb[n].x, acc[m][0]);
-                    acc[m][1] = fmaf(am[n], bb[n].y, acc[m][1]);
-                    acc[m][2] = fmaf(am[n], bb[n].z, acc[m][2]);
-                    acc[m][3] = fmaf(am[n], bb[n].w, acc[m][3]);
-                }
-            }
-        }
-        __syncthreads();  // M fully read
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int r = 32 + 4 * pr + m;
-            *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, 4 * pc)) =
-                make_float4(-acc[m][0], -acc[m][1], -acc[m][2], -acc[m][3]);
-        }
-        __syncthreads();  // T complete (fp32)
-    }
+    merge_level<16>(sL, tid);   // 32 x 32 diagonal blocks
+    merge_level<32>(sL, tid);   // the whole 64 x 64 inverse
 
     // ---- A operand = T diag(beta) in bf16, block diagonal over the two chunks ----
     {
@@ -496,13 +516,13 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     __syncthreads();
 
     // ---- epilogue 2: W rows, U~^T rows (bf16) and g to the workspace ----
-    ok = !abort2 && mbar_wait(&bars[2], 0);
+    ok = !abort2 && mbar_wait(&bars[2], ph);
     if (!abort2 && !ok) set_status(p.status, kDevTimeout);
     tc_fence_after();
     if (ok) {
-        if (valid[slot]) {
+        if (vslot) {
             __nv_bfloat16 *dst_row = p.W_ws + slot_row * D;
-#pragma unroll
+#pragma unroll 1
             for (int c4 = 0; c4 < 4; ++c4) {
                 uint32_t r[32];
                 tmem_ld32(tb + lane_base + c4 * 32, r);
@@ -512,22 +532,25 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             p.g_ws[slot_row] = gt;
         }
         // lane j of U~^T holds feature j for the tokens of both chunks
-#pragma unroll
+#pragma unroll 1
         for (int q = 0; q < 2; ++q) {
             uint32_t r0[32], r1[32];
             tmem_ld32(tb + lane_base + 128 + q * 64, r0);
             tmem_ld32(tb + lane_base + 128 + q * 64 + 32, r1);
             tmem_ld_wait();
-            if (valid[q]) {
-                __nv_bfloat16 *dst = p.UT_ws + ((size_t)((2L * blockIdx.x + q) * p.H + h) * D + tid) * C;
+            if (q ? v1 : v0) {
+                __nv_bfloat16 *dst = p.UT_ws + ((size_t)((2L * pair + q) * p.H + h) * D + tid) * C;
                 store_bf16x32(dst, r0);
                 store_bf16x32(dst + 32, r1);
             }
         }
     }
     tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tb, 256);
+    __syncthreads();   // smem and TMEM free for the next item
+    ph ^= 1u;
+    if (sAbort) break;
+    }  // items
+    if ((tid0 >> 5) == 0) tmem_dealloc(tslot, 256);
 }
 
 // ===================================================================== phase 2
@@ -999,6 +1022,15 @@ bool map_2d(CUtensorMap *m, const void *base, int cols, long rows, int box_rows)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Number of SMs of the current device (persistent grids).
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 148;
+    return n;
+}
+
 struct WsLayout {
     size_t meta, g, W, U, A, total;
 };
@@ -1078,8 +1110,10 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
             return e;
         attrs = true;
     }
-    dim3 g1((unsigned)((n_chunks_upper + 1) / 2), (unsigned)p.H);
-    intra_kernel<<<g1, P1_THREADS, P1_SMEM, s>>>(mq, mk, mv, tp);
+    const long n_pairs = (n_chunks_upper + 1) / 2;
+    const long n_items = n_pairs * p.H;
+    const long grid1 = n_items < 2L * sm_count() ? n_items : 2L * sm_count();
+    intra_kernel<<<(unsigned)grid1, P1_THREADS, P1_SMEM, s>>>(mq, mk, mv, tp, n_pairs);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     state_kernel<<<(unsigned)(p.n_seq * p.H), P2_THREADS, P2_SMEM, s>>>(mq, mk, mw, mu, ma, mo, tp);
