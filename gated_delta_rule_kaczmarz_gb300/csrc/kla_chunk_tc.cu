@@ -29,8 +29,9 @@
 //   Z^T = U^T (diag(exp(g_C - g)) K) ;  S^T <- exp(g_C) S^T + Z^T (fp32 registers)
 //   O^T = S^T (diag(exp g) Q)^T + U^T A^T
 // The serial chain is P -> U -> Z -> S; the output products and their
-// stores, and the scaling of the next chunk's Q and K tiles (which stream in
-// by TMA two chunks ahead), run beside it on separate warps.
+// stores, and the scaling of the next chunk's Q and K tiles (three chunks
+// stream in by TMA ahead of use), run beside it on separate warps.  S^T and
+// U^T, the bf16 A operands, are kept in tensor memory.
 //
 // All waits are bounded (kla_tc.cuh); a wait that gives up sets the status
 // word to a timeout code and the CTA leaves after releasing TMEM.
@@ -558,23 +559,24 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 // (thread (j, half): dv index j = its TMEM lane, half = which 32 tokens / 64
 // state rows it handles); thread 0 also issues every MMA and TMA load.
 // Warps 8-11 ("aux") scale the next chunk's Q and K tiles in shared memory and
-// write each chunk's output rows (TMA store of a staged tile).
+// write each chunk's output rows.
+// The bf16 operands S^T and U^T live in tensor memory (A operands of the
+// MMAs), which leaves shared memory for three chunk stages in flight.
 constexpr int P2_MAIN = 256, P2_AUX = 128, P2_THREADS = P2_MAIN + P2_AUX;
-constexpr uint32_t BAR_MAIN = 1, BAR_AUX = 2;    // named barrier ids
+constexpr uint32_t BAR_MAIN = 1;                 // named barrier id (main warps)
+constexpr int NSTAGE = 3;
 // Stage layout (one chunk): W [64 t][128] (2 slabs), Q and K [64 t][128]
 // (2 slabs each, scaled in place by exp(g) and exp(g_C - g)), U~^T [128][64],
 // A [64][64], g [64].
 constexpr uint32_t ST_W = 0, ST_Q = 16384, ST_K = 32768, ST_U = 49152, ST_A = 65536,
                    ST_G = 73728, ST_BYTES = 74752;
 constexpr uint32_t ST_TX = 16384u * 4u + 8192u + 256u;  // bytes a stage receives
-constexpr uint32_t P2_OFF_S = 2 * ST_BYTES;             // S^T bf16 [128][128] (2 slabs)
-constexpr uint32_t P2_OFF_UT = P2_OFF_S + 32768;        // U^T bf16 [128][64]
-constexpr uint32_t P2_OFF_O = P2_OFF_UT + 16384;        // output staging [64 t][128] (2 slabs)
-constexpr uint32_t P2_SMEM = P2_OFF_O + 16384 + 1024;
+constexpr uint32_t P2_SMEM = NSTAGE * ST_BYTES + 1024;
 
-// TMEM columns (fp32, M = 128 lanes = dv): P^T 0..63; O^T double buffer
-// 64..127 and 128..191; Z^T 256..383.
-constexpr uint32_t TM_P = 0, TM_O = 64, TM_Z = 256;
+// TMEM columns (M = 128 lanes = dv): fp32 P^T 0..63; fp32 O^T double buffer
+// 64..127 and 128..191; fp32 Z^T 256..383; bf16 S^T (128 packed as 64)
+// 384..447; bf16 U^T (64 packed as 32) 448..479.
+constexpr uint32_t TM_P = 0, TM_O = 64, TM_Z = 256, TM_S = 384, TM_U = 448;
 
 __device__ __forceinline__ void issue_stage(unsigned char *st, uint64_t *bar,
                                             const CUtensorMap *mq, const CUtensorMap *mk,
@@ -619,21 +621,29 @@ __device__ __forceinline__ void scale_stage(unsigned char *st, int nc, int a) {
     }
 }
 
+// Main warps: bf16 copy of the 64 state values S[64*half + i][j] into the
+// TMEM operand S^T (row j, packed columns 32*half ..).
+__device__ __forceinline__ void store_state_bf16(uint32_t taddr, const float (&Sr)[64]) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf2(Sr[32 * hh + 2 * i], Sr[32 * hh + 2 * i + 1]);
+        tmem_st16(taddr + 16 * hh, pk);
+    }
+}
+
 __global__ void __launch_bounds__(P2_THREADS, 1)
 state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
              const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
-             const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mo,
-             const TcParams p) {
+             const __grid_constant__ CUtensorMap ma, const TcParams p) {
     extern __shared__ unsigned char smraw[];
-    __shared__ uint64_t bar_ld[2], bar_scaled[2], bar_ofree[2];
+    __shared__ uint64_t bar_ld[NSTAGE], bar_scaled[NSTAGE], bar_ofree[2];
     __shared__ uint64_t bar_p, bar_s, bar_o;
     __shared__ uint32_t tslot;
     __shared__ int sAbort;
 
     unsigned char *sm = align1024(smraw);
-    unsigned char *sS = sm + P2_OFF_S;
-    unsigned char *sUt = sm + P2_OFF_UT;
-    unsigned char *sO = sm + P2_OFF_O;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;
@@ -659,11 +669,12 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const size_t sbase = ((size_t)seq * p.H + h) * D * D;
 
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NSTAGE; ++i) {
             mbar_init(&bar_ld[i], 1);
             mbar_init(&bar_scaled[i], P2_AUX);
-            mbar_init(&bar_ofree[i], P2_AUX);
         }
+        mbar_init(&bar_ofree[0], P2_AUX);
+        mbar_init(&bar_ofree[1], P2_AUX);
         mbar_init(&bar_p, 1);
         mbar_init(&bar_s, 1);
         mbar_init(&bar_o, 1);
@@ -674,6 +685,9 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         tmem_alloc(&tslot, 512);
         tmem_relinquish();
     }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tslot;
 
     // fp32 master state (main warps): S[i][j] for i in [64*half, 64*half+64)
     float Sr[64];
@@ -681,62 +695,54 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 #pragma unroll
         for (int i = 0; i < 64; ++i)
             Sr[i] = p.S0 ? p.S0[sbase + (size_t)(64 * half + i) * D + j] : 0.f;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4 *>(sS + half * 16384 + sw128_offset(j, ch * 8)) =
-                make_uint4(pack_bf2(Sr[8 * ch + 0], Sr[8 * ch + 1]),
-                           pack_bf2(Sr[8 * ch + 2], Sr[8 * ch + 3]),
-                           pack_bf2(Sr[8 * ch + 4], Sr[8 * ch + 5]),
-                           pack_bf2(Sr[8 * ch + 6], Sr[8 * ch + 7]));
-        fence_async_smem();
+        store_state_bf16(tb + lane_base + TM_S + 32 * half, Sr);
+        tmem_st_wait();
     }
-    tc_fence_before();
-    __syncthreads();  // barriers initialised, TMEM allocated, S^T staged
-    tc_fence_after();
-    const uint32_t tb = tslot;
-
     if (tid == 0) {
-        for (int c = 0; c < 2 && c < nch; ++c) {
+        for (int c = 0; c < NSTAGE && c < nch; ++c) {
             const long slot = (chunk0 + c) * p.H + h;
             issue_stage(sm + c * ST_BYTES, &bar_ld[c], &mq, &mk, &mw, &mu, &ma,
                         p.g_ws + slot * C, h, (int)(start + (long)c * C), (int)slot);
         }
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 
     if (is_main) {
         const uint32_t id_64 = idesc_bf16_f32(128, 64, false, false);
         const uint32_t id_z = idesc_bf16_f32(128, 128, false, true);
         for (int c = 0; c < nch; ++c) {
-            const int b = c & 1, ob = c & 1;
+            const int b = c % NSTAGE, ob = c & 1;
             unsigned char *st = sm + b * ST_BYTES;
-            const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c >> 1) & 1);
+            const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NSTAGE) & 1);
 
-            // ---- P^T = S^T W^T ; O^T = S^T (diag(exp g) Q)^T ----
+            // ---- P^T = S^T W^T (gates the chain), then O^T = S^T (diag(exp g) Q)^T ----
             if (tid == 0) {
-                bool okw = mbar_wait(&bar_scaled[b], par_st);
-                if (okw && c >= 2) okw = mbar_wait(&bar_ofree[ob], (uint32_t)(((c - 2) >> 1) & 1));
+                bool okw = mbar_wait(&bar_ld[b], par_st);
+                if (okw) {
+                    tc_fence_after();
+                    const uint32_t aW = smem_u32(st + ST_W);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ta(tb + TM_P, tb + TM_S + 8 * ks,
+                                    sdesc_sw128(aW + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
+                                    id_64, ks > 0);
+                    mma_commit(&bar_p);
+                    okw = mbar_wait(&bar_scaled[b], par_st);
+                    if (okw && c >= 2) okw = mbar_wait(&bar_ofree[ob], (uint32_t)(((c - 2) >> 1) & 1));
+                }
                 if (!okw) {
                     sAbort = 1;
                     set_status(p.status, kDevTimeout);
                 } else {
                     tc_fence_after();
-                    const uint32_t aS = smem_u32(sS), aW = smem_u32(st + ST_W),
-                                   aQ = smem_u32(st + ST_Q);
+                    const uint32_t aQ = smem_u32(st + ST_Q);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
-                        const uint32_t offS = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16(tb + TM_P, sdesc_sw128(aS + offS, 16, 1024),
-                                 sdesc_sw128(aW + off, 16, 1024), id_64, ks > 0);
-                    }
-                    mma_commit(&bar_p);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
-                        const uint32_t offS = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_bf16(tb + TM_O + 64 * ob, sdesc_sw128(aS + offS, 16, 1024),
-                                 sdesc_sw128(aQ + off, 16, 1024), id_64, ks > 0);
-                    }
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ta(tb + TM_O + 64 * ob, tb + TM_S + 8 * ks,
+                                    sdesc_sw128(aQ + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
+                                    id_64, ks > 0);
                 }
             }
             if (!mbar_wait(&bar_ld[b], par_st) || !mbar_wait(&bar_p, par)) {
@@ -744,29 +750,27 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 sAbort = 1;
             }
             tc_fence_after();
+            const float egC = __expf(reinterpret_cast<const float *>(st + ST_G)[C - 1]);
 
-            // ---- U^T = U~^T - P^T for tokens [32*half, 32*half + 32) ----
+            // ---- U^T = U~^T - P^T for tokens [32*half, 32*half + 32) -> TMEM (bf16) ----
             {
                 uint32_t r[32];
                 tmem_ld32(tb + lane_base + TM_P + half * 32, r);
                 tmem_ld_wait();
                 const unsigned char *sU = st + ST_U;
+                uint32_t pk[16];
 #pragma unroll
                 for (int v4 = 0; v4 < 4; ++v4) {
-                    const uint32_t off = sw128_offset(j, half * 32 + v4 * 8);
-                    const uint4 u = *reinterpret_cast<const uint4 *>(sU + off);
+                    const uint4 u = *reinterpret_cast<const uint4 *>(sU + sw128_offset(j, half * 32 + v4 * 8));
                     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-                    uint32_t o4[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float u0 = bf_lo(w[e]) - __uint_as_float(r[8 * v4 + 2 * e]);
-                        const float u1 = bf_hi(w[e]) - __uint_as_float(r[8 * v4 + 2 * e + 1]);
-                        o4[e] = pack_bf2(u0, u1);
-                    }
-                    *reinterpret_cast<uint4 *>(sUt + off) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                    for (int e = 0; e < 4; ++e)
+                        pk[4 * v4 + e] = pack_bf2(bf_lo(w[e]) - __uint_as_float(r[8 * v4 + 2 * e]),
+                                                  bf_hi(w[e]) - __uint_as_float(r[8 * v4 + 2 * e + 1]));
                 }
+                tmem_st16(tb + lane_base + TM_U + 16 * half, pk);
+                tmem_st_wait();
             }
-            fence_async_smem();
             tc_fence_before();
             named_sync(BAR_MAIN, P2_MAIN);
 
@@ -774,17 +778,16 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             //      then O^T += U^T A^T ----
             if (tid == 0 && !sAbort) {
                 tc_fence_after();
-                const uint32_t aUt = smem_u32(sUt), aA = smem_u32(st + ST_A),
-                               aK = smem_u32(st + ST_K);
+                const uint32_t aA = smem_u32(st + ST_A), aK = smem_u32(st + ST_K);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tb + TM_Z, sdesc_sw128(aUt + ks * 32, 16, 1024),
-                             sdesc_sw128(aK + ks * 2048, 8192, 1024), id_z, ks > 0);
+                    mma_bf16_ta(tb + TM_Z, tb + TM_U + 8 * ks,
+                                sdesc_sw128(aK + ks * 2048, 8192, 1024), id_z, ks > 0);
                 mma_commit(&bar_s);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tb + TM_O + 64 * ob, sdesc_sw128(aUt + ks * 32, 16, 1024),
-                             sdesc_sw128(aA + ks * 32, 16, 1024), id_64, 1u);
+                    mma_bf16_ta(tb + TM_O + 64 * ob, tb + TM_U + 8 * ks,
+                                sdesc_sw128(aA + ks * 32, 16, 1024), id_64, 1u);
                 mma_commit(&bar_o);
             }
             if (!mbar_wait(&bar_s, par)) {
@@ -793,9 +796,8 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             }
             tc_fence_after();
 
-            // ---- S^T <- exp(g_C) S^T + Z^T ; new bf16 copy of S^T ----
+            // ---- S^T <- exp(g_C) S^T + Z^T ; new bf16 copy of S^T in TMEM ----
             if (!sAbort) {
-                const float egC = __expf(reinterpret_cast<const float *>(st + ST_G)[C - 1]);
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
                     uint32_t r[32];
@@ -805,28 +807,22 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                     for (int i = 0; i < 32; ++i)
                         Sr[c2 * 32 + i] = fmaf(egC, Sr[c2 * 32 + i], __uint_as_float(r[i]));
                 }
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    *reinterpret_cast<uint4 *>(sS + half * 16384 + sw128_offset(j, ch * 8)) =
-                        make_uint4(pack_bf2(Sr[8 * ch + 0], Sr[8 * ch + 1]),
-                                   pack_bf2(Sr[8 * ch + 2], Sr[8 * ch + 3]),
-                                   pack_bf2(Sr[8 * ch + 4], Sr[8 * ch + 5]),
-                                   pack_bf2(Sr[8 * ch + 6], Sr[8 * ch + 7]));
+                store_state_bf16(tb + lane_base + TM_S + 32 * half, Sr);
+                tmem_st_wait();
             }
-            fence_async_smem();
             tc_fence_before();
             named_sync(BAR_MAIN, P2_MAIN);
             if (sAbort) break;
 
-            // ---- refill this stage with chunk c + 2 once O^T += U^T A^T has read it ----
-            if (tid == 0 && c + 2 < nch) {
+            // ---- refill this stage with chunk c + NSTAGE once O^T += U^T A^T has read it ----
+            if (tid == 0 && c + NSTAGE < nch) {
                 if (!mbar_wait(&bar_o, par)) {
                     sAbort = 1;
                     set_status(p.status, kDevTimeout);
                 } else {
-                    const long slot = (chunk0 + c + 2) * p.H + h;
+                    const long slot = (chunk0 + c + NSTAGE) * p.H + h;
                     issue_stage(st, &bar_ld[b], &mq, &mk, &mw, &mu, &ma, p.g_ws + slot * C, h,
-                                (int)(start + (long)(c + 2) * C), (int)slot);
+                                (int)(start + (long)(c + NSTAGE) * C), (int)slot);
                 }
             }
         }
@@ -837,7 +833,6 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     } else {
         // ----------------------------------------------------------------- aux warps
         const int a = tid - P2_MAIN;     // 0..127; TMEM lane quarter = warp & 3
-        const bool leader = a == 0;
         if (nch > 0) {
             if (!mbar_wait(&bar_ld[0], 0)) {
                 sAbort = 1;
@@ -852,8 +847,8 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             const int ob = c & 1;
             // scale the next chunk as soon as it lands
             if (c + 1 < nch) {
-                const int b1 = (c + 1) & 1;
-                if (!mbar_wait(&bar_ld[b1], (uint32_t)(((c + 1) >> 1) & 1))) {
+                const int b1 = (c + 1) % NSTAGE;
+                if (!mbar_wait(&bar_ld[b1], (uint32_t)(((c + 1) / NSTAGE) & 1))) {
                     sAbort = 1;
                     set_status(p.status, kDevTimeout);
                     break;
@@ -876,39 +871,14 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             tc_fence_before();
             mbar_arrive(&bar_ofree[ob]);
             const int nc = (int)min((long)C, len - (long)c * C);
-            const long row0 = start + (long)c * C;
-            if (nc == C) {
-                // full chunk: stage [64 t][128] (SW128, 2 slabs) and store with TMA
-                if (leader) bulk_wait_group_read0();
-                named_sync(BAR_AUX, P2_AUX);
-                unsigned char *slab = sO + (j >> 6) * 8192;
+            __nv_bfloat16 *dst = p.o + (size_t)(start + (long)c * C) * p.H * D + (size_t)h * D + j;
+            const size_t rs = (size_t)p.H * D;
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    *reinterpret_cast<__nv_bfloat16 *>(slab + sw128_offset(t, j & 63)) =
-                        __float2bfloat16_rn(__uint_as_float(r0[t]));
-                    *reinterpret_cast<__nv_bfloat16 *>(slab + sw128_offset(t + 32, j & 63)) =
-                        __float2bfloat16_rn(__uint_as_float(r1[t]));
-                }
-                fence_async_smem();
-                named_sync(BAR_AUX, P2_AUX);
-                if (leader) {
-                    tma_store_3d(&mo, sO, 0, h, (int)row0);
-                    tma_store_3d(&mo, sO + 8192, 64, h, (int)row0);
-                    bulk_commit_group();
-                }
-            } else {
-                // partial last chunk: plain stores of the valid rows only
-                __nv_bfloat16 *dst = p.o + (size_t)row0 * p.H * D + (size_t)h * D + j;
-#pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    if (t < nc)
-                        dst[(size_t)t * p.H * D] = __float2bfloat16_rn(__uint_as_float(r0[t]));
-                    if (t + 32 < nc)
-                        dst[(size_t)(t + 32) * p.H * D] = __float2bfloat16_rn(__uint_as_float(r1[t]));
-                }
+            for (int t = 0; t < 32; ++t) {
+                if (t < nc) dst[t * rs] = __float2bfloat16_rn(__uint_as_float(r0[t]));
+                if (t + 32 < nc) dst[(t + 32) * rs] = __float2bfloat16_rn(__uint_as_float(r1[t]));
             }
         }
-        if (leader) bulk_wait_group0();
     }
 
     tc_fence_before();
@@ -1085,12 +1055,11 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     tp.chunk_prefix = p.cu_seqlens ? chunk_prefix : nullptr;
     tp.order = p.cu_seqlens ? order : nullptr;
 
-    CUtensorMap mq, mk, mv, mw, mu, ma, mo;
+    CUtensorMap mq, mk, mv, mw, mu, ma;
     const long slots = n_chunks_upper * p.H;
     if (!map_3d_rows(&mq, p.q, p.H, p.total_T) || !map_3d_rows(&mk, p.k, p.H, p.total_T) ||
         !map_3d_rows(&mv, p.v, p.H, p.total_T) || !map_2d(&mw, tp.W_ws, D, slots * C, C) ||
-        !map_2d(&mu, tp.UT_ws, C, slots * D, D) || !map_2d(&ma, tp.A_ws, C, slots * C, C) ||
-        !map_3d_rows(&mo, p.o, p.H, p.total_T))
+        !map_2d(&mu, tp.UT_ws, C, slots * D, D) || !map_2d(&ma, tp.A_ws, C, slots * C, C))
         return cudaErrorInvalidValue;
 
     cudaError_t e;
@@ -1116,7 +1085,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     intra_kernel<<<(unsigned)grid1, P1_THREADS, P1_SMEM, s>>>(mq, mk, mv, tp, n_pairs);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    state_kernel<<<(unsigned)(p.n_seq * p.H), P2_THREADS, P2_SMEM, s>>>(mq, mk, mw, mu, ma, mo, tp);
+    state_kernel<<<(unsigned)(p.n_seq * p.H), P2_THREADS, P2_SMEM, s>>>(mq, mk, mw, mu, ma, tp);
     note_launch();
     return cudaGetLastError();
 }
