@@ -24,14 +24,15 @@
 // MMAs.  W, U~^T, A (bf16) and g (fp32) go to the caller's workspace.
 //
 // Phase 2 (state_kernel) walks the chunks of one (sequence, head) in order,
-// every product with M = dv = 128 rows:
-//   P^T = S^T W^T ;  U^T = U~^T - P^T   (registers -> bf16 smem tile)
-//   Z^T = U^T (diag(exp(g_C - g)) K) ;  S^T <- exp(g_C) S^T + Z^T (fp32 registers)
-//   O^T = S^T (diag(exp g) Q)^T + U^T A^T
-// The serial chain is P -> U -> Z -> S; the output products and their
-// stores, and the scaling of the next chunk's Q and K tiles (three chunks
-// stream in by TMA ahead of use), run beside it on separate warps.  S^T and
-// U^T, the bf16 A operands, are kept in tensor memory.
+// every product with M = dv = 128 rows and the two products of a step fused
+// into one wide MMA (issue cost per tcgen05.mma is nearly independent of N):
+//   [P^T | X^T] = S^T [W ; diag(exp g) Q]^T ;  U^T = U~^T - P^T
+//   [Z^T | Y^T] = U^T [diag(exp(g_C - g)) K | A^T]
+//   S^T <- exp(g_C) S^T + Z^T (fp32 registers) ;  O^T = X^T + Y^T
+// The serial chain is P -> U -> Z -> S; a dedicated warp issues the MMAs and
+// TMA loads (three chunks in flight), and separate warps scale the next
+// chunk's Q and K tiles and store the outputs.  S^T and U^T, the bf16 A
+// operands, are kept in tensor memory.
 //
 // All waits are bounded (kla_tc.cuh); a wait that gives up sets the status
 // word to a timeout code and the CTA leaves after releasing TMEM.
@@ -67,7 +68,7 @@ struct TcParams {
     float *g_ws;               // [slots][64]
     __nv_bfloat16 *W_ws;       // [slots][64][128]
     __nv_bfloat16 *UT_ws;      // [slots][128][64]  U~ transposed (feature-major)
-    __nv_bfloat16 *A_ws;       // [slots][64][64]
+    __nv_bfloat16 *A_ws;       // [slots][64 keys s][64 queries t]  A^T
 };
 
 __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
@@ -139,13 +140,19 @@ __device__ __forceinline__ int lsw(int row, int col) {
     return ((((col >> 2) ^ (row & 15))) << 2) | (col & 3);
 }
 
+// fp32 64 x 64 matrix of chunk p (L, then T) in phase 1: it occupies the
+// 16 KB that chunk p's half of the Q tile used, in 64-feature slab p.
+__device__ __forceinline__ float *lslot(unsigned char *kq, int p) {
+    return reinterpret_cast<float *>(kq + p * 32768 + 16384);
+}
+
 // One doubling step of the blocked inverse, in place in the fp32 L storage
 // of both chunks: for every diagonal block of size 2n whose two diagonal
 // n x n blocks already hold D1 = (I + L11)^{-1} and D2 = (I + L22)^{-1},
 // replace its lower-left block L21 by -D2 L21 D1.  128 threads; each computes
 // an (n/8) x 4 patch of the n x n products.
 template <int n>
-__device__ __forceinline__ void merge_level(float *sL, int tid) {
+__device__ __forceinline__ void merge_level(unsigned char *kq, int tid) {
     constexpr int nblk = 64 / (2 * n);               // blocks of size 2n per chunk
     constexpr int tpb = 128 / (2 * nblk);            // threads per block (both chunks)
     constexpr int rows = n * n / 4 / tpb;            // patch rows per thread (4 columns each)
@@ -154,7 +161,7 @@ __device__ __forceinline__ void merge_level(float *sL, int tid) {
     const int p = blkid / nblk, o = 2 * n * (blkid % nblk);
     constexpr int pcols = n / 4;                     // column patches per row band
     const int pr = q / pcols, pc = q % pcols;        // rows [rows*pr, +rows), cols [4pc, +4)
-    float *Lp = sL + (size_t)p * 64 * 64;
+    float *Lp = lslot(kq, p);
     float acc[rows][4];
     // M = L21 D1
 #pragma unroll
@@ -237,10 +244,12 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     __shared__ int sAbort;
 
     unsigned char *sm = align1024(smraw);
-    unsigned char *sK = sm;           // [2 slabs][128 rows][128 B]; later diag(exp g) K
-    unsigned char *sV = sm + 32768;   // same layout (n-block stride 16 KB continues from sK)
-    unsigned char *sQ = sm + 65536;   // Q tile -> fp32 L[2][64][64] -> A operand T diag(beta)
-    float *sL = reinterpret_cast<float *>(sQ);
+    // KQ: two 64-feature slabs of 32 KB, each [K rows 0..127 | Q rows 0..127]
+    // (128-byte rows, 128-byte swizzle), so that [K; Q] is one N = 256
+    // operand.  After the Gram products the Q half of slab p holds chunk p's
+    // fp32 L / T and then slab p of the bf16 operand T diag(beta).
+    unsigned char *KQ = sm;
+    unsigned char *sV = sm + 65536;   // [2 slabs][128 rows][128 B]
 
     const int tid0 = threadIdx.x;
     if (status_bad(p.status)) return;
@@ -292,8 +301,8 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
                 const int z = (int)(q ? r01 : r00);
-                tma_load_3d(sK + s * 16384 + q * 8192, &mk, &bars[0], 64 * s, h, z);
-                tma_load_3d(sQ + s * 16384 + q * 8192, &mq, &bars[0], 64 * s, h, z);
+                tma_load_3d(KQ + s * 32768 + q * 8192, &mk, &bars[0], 64 * s, h, z);
+                tma_load_3d(KQ + s * 32768 + 16384 + q * 8192, &mq, &bars[0], 64 * s, h, z);
                 tma_load_3d(sV + s * 16384 + q * 8192, &mv, &bars[0], 64 * s, h, z);
             }
     }
@@ -325,18 +334,13 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const bool abort1 = sAbort != 0;
     if (tid == 0 && !abort1) {
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
-        const uint32_t aK = smem_u32(sK), aQ = smem_u32(sQ);
+        // [K K^T | K Q^T]: A = K (128 tokens), B = [K; Q] (256 rows), K = 128 features
+        const uint32_t idesc = idesc_bf16_f32(128, 256, false, false);
+        const uint32_t aKQ = smem_u32(KQ);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_bf16(tb + 0, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024),
-                     idesc, ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_bf16(tb + 128, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024),
+            const uint32_t off = (ks >> 2) * 32768 + (ks & 3) * 32;
+            mma_bf16(tb + 0, sdesc_sw128(aKQ + off, 16, 1024), sdesc_sw128(aKQ + off, 16, 1024),
                      idesc, ks > 0);
         }
         mma_commit(&bars[1]);
@@ -349,7 +353,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         for (int s = 0; s < 2; ++s)
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(sK + s * 16384 +
+                const uint4 v = *reinterpret_cast<const uint4 *>(KQ + s * 32768 +
                                                                 sw128_offset(tid, ch * 8));
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -364,7 +368,8 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     }
     __syncthreads();
 
-    // ---- epilogue 1: L = strict_lower(beta Gamma o KK^T) (fp32 smem), A = lower(Gamma o QK^T) ----
+    // ---- epilogue 1: L = strict_lower(beta Gamma o KK^T) (fp32 smem) from row t of
+    //      K K^T; row s of (K Q^T) gives row s of A^T, A = lower(Gamma o QK^T) ----
     bool ok = !abort1 && mbar_wait(&bars[1], ph);
     if (!abort1 && !ok) set_status(p.status, kDevTimeout);
     tc_fence_after();
@@ -374,7 +379,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const long gidx0 = 2L * pair + slot;
     const size_t slot_row = (size_t)(gidx0 * p.H + h) * C + t;   // row of this token in the ws
     if (ok) {
-        float *Lrow = sL + (size_t)(slot * 64 + t) * 64;
+        float *Lrow = lslot(KQ, slot) + t * 64;
 #pragma unroll 1
         for (int g16 = 0; g16 < 4; ++g16) {
             uint32_t r[16];
@@ -398,14 +403,15 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             uint32_t r[16];
             tmem_ld16(tb + lane_base + 128 + cb + g16 * 16, r);
             tmem_ld_wait();
+            // this thread's token is the key s = t; the columns are queries u
             uint32_t pk[8];
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
-                const int s = g16 * 16 + i;
-                const float a0 = (s <= t && t < nc)
-                                     ? __expf(gt - sG[cb + s]) * __uint_as_float(r[i]) : 0.f;
-                const float a1 = (s + 1 <= t && t < nc)
-                                     ? __expf(gt - sG[cb + s + 1]) * __uint_as_float(r[i + 1]) : 0.f;
+                const int u = g16 * 16 + i;
+                const float a0 = (t <= u && u < nc)
+                                     ? __expf(sG[cb + u] - gt) * __uint_as_float(r[i]) : 0.f;
+                const float a1 = (t <= u + 1 && u + 1 < nc)
+                                     ? __expf(sG[cb + u + 1] - gt) * __uint_as_float(r[i + 1]) : 0.f;
                 pk[i / 2] = pack_bf2(a0, a1);
             }
             if (vslot) {
@@ -423,7 +429,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         for (int s = 0; s < 2; ++s)
 #pragma unroll 2
             for (int ch = 0; ch < 8; ++ch) {
-                uint4 *pk4 = reinterpret_cast<uint4 *>(sK + s * 16384 + sw128_offset(tid, ch * 8));
+                uint4 *pk4 = reinterpret_cast<uint4 *>(KQ + s * 32768 + sw128_offset(tid, ch * 8));
                 if (t < nc) {
                     const uint4 v = *pk4;
                     *pk4 = make_uint4(pack_bf2(gam_t * bf_lo(v.x), gam_t * bf_hi(v.x)),
@@ -446,7 +452,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     {
         // diagonal 16 x 16 blocks: 16 threads per block, one column each
         const int p = tid >> 6, blk = (tid >> 4) & 3, c = tid & 15, o = 16 * blk;
-        float *Lb = sL + (size_t)(p * 64 + o) * 64;
+        float *Lb = lslot(KQ, p) + o * 64;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
@@ -469,12 +475,12 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         for (int r = 0; r < 16; ++r) Lb[r * 64 + lsw(o + r, o + c)] = x[r];
         __syncthreads();
     }
-    merge_level<16>(sL, tid);   // 32 x 32 diagonal blocks
-    merge_level<32>(sL, tid);   // the whole 64 x 64 inverse
+    merge_level<16>(KQ, tid);   // 32 x 32 diagonal blocks
+    merge_level<32>(KQ, tid);   // the whole 64 x 64 inverse
 
     // ---- A operand = T diag(beta) in bf16, block diagonal over the two chunks ----
     {
-        const float *Trow = sL + (size_t)(slot * 64 + t) * 64;
+        const float *Trow = lslot(KQ, slot) + t * 64;
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -484,7 +490,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             pk[2 * i + 1] = pack_bf2(v.z * bs[2], v.w * bs[3]);
         }
         __syncthreads();  // T fully read; its region becomes the bf16 A tile
-        unsigned char *own = sQ + slot * 16384, *other = sQ + (1 - slot) * 16384;
+        unsigned char *own = KQ + slot * 32768 + 16384, *other = KQ + (1 - slot) * 32768 + 16384;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
             *reinterpret_cast<uint4 *>(own + sw128_offset(tid, ch * 8)) =
@@ -497,21 +503,22 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     __syncthreads();
     if (tid == 0 && !abort2) {
         tc_fence_after();
-        const uint32_t aA = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+        const uint32_t aA = smem_u32(KQ + 16384), aK = smem_u32(KQ), aV = smem_u32(sV);
         // W = (T diag beta) (diag(exp g) K): M = 128 tokens, N = 128, K = 128 tokens;
-        // B MN-major (rows = tokens), n-blocks of 64 features at 16 KB.
+        // A slabs (one per chunk's columns) at 32 KB; B = diag(exp g) K MN-major
+        // (rows = tokens), its two 64-feature n-blocks 32 KB apart.
         const uint32_t id_w = idesc_bf16_f32(128, 128, false, true);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-            mma_bf16(tb + 0, sdesc_sw128(aA + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                     sdesc_sw128(aK + ks * 2048, 16384, 1024), id_w, ks > 0);
+            mma_bf16(tb + 0, sdesc_sw128(aA + (ks >> 2) * 32768 + (ks & 3) * 32, 16, 1024),
+                     sdesc_sw128(aK + ks * 2048, 32768, 1024), id_w, ks > 0);
         // U~^T = V^T (T diag beta)^T: M = 128 features (A = V, MN-major), N = 128
         // tokens (B = the same T diag beta tile, K-major), K = 128 tokens.
         const uint32_t id_u = idesc_bf16_f32(128, 128, true, false);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
             mma_bf16(tb + 128, sdesc_sw128(aV + ks * 2048, 16384, 1024),
-                     sdesc_sw128(aA + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id_u, ks > 0);
+                     sdesc_sw128(aA + (ks >> 2) * 32768 + (ks & 3) * 32, 16, 1024), id_u, ks > 0);
         mma_commit(&bars[2]);
     }
     __syncthreads();
@@ -555,28 +562,33 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 }
 
 // ===================================================================== phase 2
-// Warp roles: warps 0-7 ("main") run the serial chain of the state pass
-// (thread (j, half): dv index j = its TMEM lane, half = which 32 tokens / 64
-// state rows it handles); thread 0 also issues every MMA and TMA load.
-// Warps 8-11 ("aux") scale the next chunk's Q and K tiles in shared memory and
-// write each chunk's output rows.
-// The bf16 operands S^T and U^T live in tensor memory (A operands of the
-// MMAs), which leaves shared memory for three chunk stages in flight.
+// Warp roles:
+//   warps 0-7  ("main"): the serial chain; thread (j, half) owns dv index j
+//              (its TMEM lane) and tokens [32*half, +32) / state rows
+//              [64*half, +64).  Thread 0 also issues every MMA and TMA load.
+//   warps 8-11 ("aux"):  scale the next chunk's Q and K tiles in shared
+//              memory and write each chunk's output rows.
+// Per chunk the tensor core runs two wide products:
+//   [P^T | X^T] = S^T [W ; diag(exp g) Q]^T                 M=128, N=128, K=128
+//   [Z^T | Y^T] = U^T [diag(exp(g_C - g)) K | A^T]           M=128, N=192, K=64
+// with U^T = U~^T - P^T, S^T <- exp(g_C) S^T + Z^T and O^T = X^T + Y^T.
+// The bf16 A operands S^T and U^T live in tensor memory, which leaves shared
+// memory for three chunk stages in flight.
 constexpr int P2_MAIN = 256, P2_AUX = 128, P2_THREADS = P2_MAIN + P2_AUX;
-constexpr uint32_t BAR_MAIN = 1;                 // named barrier id (main warps)
 constexpr int NSTAGE = 3;
-// Stage layout (one chunk): W [64 t][128] (2 slabs), Q and K [64 t][128]
-// (2 slabs each, scaled in place by exp(g) and exp(g_C - g)), U~^T [128][64],
-// A [64][64], g [64].
-constexpr uint32_t ST_W = 0, ST_Q = 16384, ST_K = 32768, ST_U = 49152, ST_A = 65536,
-                   ST_G = 73728, ST_BYTES = 74752;
+// Stage layout (one chunk):
+//   WQ: two 64-feature slabs of 16 KB, each [W rows 0..63 | Q rows 0..63]
+//   KA: K slab 0, K slab 1, A^T (8 KB each): MN-major n-blocks 8 KB apart
+//   U:  U~^T [128][64];  G: g [64]
+constexpr uint32_t ST_WQ = 0, ST_KA = 32768, ST_A = 49152, ST_U = 57344, ST_G = 73728,
+                   ST_BYTES = 74752;
 constexpr uint32_t ST_TX = 16384u * 4u + 8192u + 256u;  // bytes a stage receives
 constexpr uint32_t P2_SMEM = NSTAGE * ST_BYTES + 1024;
 
-// TMEM columns (M = 128 lanes = dv): fp32 P^T 0..63; fp32 O^T double buffer
-// 64..127 and 128..191; fp32 Z^T 256..383; bf16 S^T (128 packed as 64)
-// 384..447; bf16 U^T (64 packed as 32) 448..479.
-constexpr uint32_t TM_P = 0, TM_O = 64, TM_Z = 256, TM_S = 384, TM_U = 448;
+// TMEM columns (M = 128 lanes = dv): fp32 [P^T | X^T] 0..127; fp32
+// [Z^T | Y^T] 128..319; bf16 S^T (128 packed as 64) 320..383; bf16 U^T (64
+// packed as 32) 384..415.
+constexpr uint32_t TM_PX = 0, TM_ZY = 128, TM_S = 320, TM_U = 384;
 
 __device__ __forceinline__ void issue_stage(unsigned char *st, uint64_t *bar,
                                             const CUtensorMap *mq, const CUtensorMap *mk,
@@ -586,12 +598,12 @@ __device__ __forceinline__ void issue_stage(unsigned char *st, uint64_t *bar,
     mbar_expect_tx(bar, ST_TX);
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
-        tma_load_2d(st + ST_W + s * 8192, mw, bar, 64 * s, slot * C);
-        tma_load_3d(st + ST_Q + s * 8192, mq, bar, 64 * s, h, row0);
-        tma_load_3d(st + ST_K + s * 8192, mk, bar, 64 * s, h, row0);
+        tma_load_2d(st + ST_WQ + s * 16384, mw, bar, 64 * s, slot * C);
+        tma_load_3d(st + ST_WQ + s * 16384 + 8192, mq, bar, 64 * s, h, row0);
+        tma_load_3d(st + ST_KA + s * 8192, mk, bar, 64 * s, h, row0);
     }
-    tma_load_2d(st + ST_U, mu, bar, 0, slot * D);
     tma_load_2d(st + ST_A, ma, bar, 0, slot * C);
+    tma_load_2d(st + ST_U, mu, bar, 0, slot * D);
     bulk_load(st + ST_G, g_src, 256, bar);
 }
 
@@ -604,7 +616,7 @@ __device__ __forceinline__ void scale_stage(unsigned char *st, int nc, int a) {
     const float f = which == 0 ? __expf(g[t]) : __expf(g[C - 1] - g[t]);
 #pragma unroll
     for (int hp = 0; hp < 2; ++hp) {
-        unsigned char *base = st + (which == 0 ? ST_Q : ST_K) + hp * 8192;
+        unsigned char *base = which == 0 ? st + ST_WQ + hp * 16384 + 8192 : st + ST_KA + hp * 8192;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
             uint4 *p4 = reinterpret_cast<uint4 *>(base + sw128_offset(t, ch * 8));
@@ -638,8 +650,8 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
              const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
              const __grid_constant__ CUtensorMap ma, const TcParams p) {
     extern __shared__ unsigned char smraw[];
-    __shared__ uint64_t bar_ld[NSTAGE], bar_scaled[NSTAGE], bar_ofree[2];
-    __shared__ uint64_t bar_p, bar_s, bar_o;
+    __shared__ uint64_t bar_ld[NSTAGE], bar_scaled[NSTAGE];
+    __shared__ uint64_t bar_p, bar_u, bar_zy, bar_sready, bar_ofree;
     __shared__ uint32_t tslot;
     __shared__ int sAbort;
 
@@ -673,11 +685,11 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             mbar_init(&bar_ld[i], 1);
             mbar_init(&bar_scaled[i], P2_AUX);
         }
-        mbar_init(&bar_ofree[0], P2_AUX);
-        mbar_init(&bar_ofree[1], P2_AUX);
         mbar_init(&bar_p, 1);
-        mbar_init(&bar_s, 1);
-        mbar_init(&bar_o, 1);
+        mbar_init(&bar_u, P2_MAIN);
+        mbar_init(&bar_zy, 1);
+        mbar_init(&bar_sready, P2_MAIN);
+        mbar_init(&bar_ofree, P2_AUX);
         fence_mbar_init();
         sAbort = 0;
     }
@@ -698,64 +710,56 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         store_state_bf16(tb + lane_base + TM_S + 32 * half, Sr);
         tmem_st_wait();
     }
-    if (tid == 0) {
-        for (int c = 0; c < NSTAGE && c < nch; ++c) {
-            const long slot = (chunk0 + c) * p.H + h;
-            issue_stage(sm + c * ST_BYTES, &bar_ld[c], &mq, &mk, &mw, &mu, &ma,
-                        p.g_ws + slot * C, h, (int)(start + (long)c * C), (int)slot);
-        }
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
+    auto fail = [&]() {
+        sAbort = 1;
+        set_status(p.status, kDevTimeout);
+    };
+
     if (is_main) {
-        const uint32_t id_64 = idesc_bf16_f32(128, 64, false, false);
-        const uint32_t id_z = idesc_bf16_f32(128, 128, false, true);
+        // ----------------------------------------------------------------- main
+        const uint32_t id_px = idesc_bf16_f32(128, 128, false, false);
+        const uint32_t id_zy = idesc_bf16_f32(128, 192, false, true);
+        if (tid == 0) {
+            for (int c = 0; c < NSTAGE && c < nch; ++c) {
+                const long slot = (chunk0 + c) * p.H + h;
+                issue_stage(sm + c * ST_BYTES, &bar_ld[c], &mq, &mk, &mw, &mu, &ma,
+                            p.g_ws + slot * C, h, (int)(start + (long)c * C), (int)slot);
+            }
+        }
         for (int c = 0; c < nch; ++c) {
-            const int b = c % NSTAGE, ob = c & 1;
+            const int b = c % NSTAGE;
             unsigned char *st = sm + b * ST_BYTES;
             const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NSTAGE) & 1);
 
-            // ---- P^T = S^T W^T (gates the chain), then O^T = S^T (diag(exp g) Q)^T ----
+            // ---- [P^T | X^T] = S^T [W ; diag(exp g) Q]^T ----
             if (tid == 0) {
-                bool okw = mbar_wait(&bar_ld[b], par_st);
-                if (okw) {
-                    tc_fence_after();
-                    const uint32_t aW = smem_u32(st + ST_W);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16_ta(tb + TM_P, tb + TM_S + 8 * ks,
-                                    sdesc_sw128(aW + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
-                                    id_64, ks > 0);
-                    mma_commit(&bar_p);
-                    okw = mbar_wait(&bar_scaled[b], par_st);
-                    if (okw && c >= 2) okw = mbar_wait(&bar_ofree[ob], (uint32_t)(((c - 2) >> 1) & 1));
-                }
-                if (!okw) {
-                    sAbort = 1;
-                    set_status(p.status, kDevTimeout);
+                bool ok = mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_scaled[b], par_st);
+                if (ok && c >= 1)   // previous chunk's state written, its outputs read
+                    ok = mbar_wait(&bar_sready, par ^ 1u) && mbar_wait(&bar_ofree, par ^ 1u);
+                if (!ok) {
+                    fail();
                 } else {
                     tc_fence_after();
-                    const uint32_t aQ = smem_u32(st + ST_Q);
+                    const uint32_t aWQ = smem_u32(st + ST_WQ);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16_ta(tb + TM_O + 64 * ob, tb + TM_S + 8 * ks,
-                                    sdesc_sw128(aQ + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
-                                    id_64, ks > 0);
+                        mma_bf16_ta(tb + TM_PX, tb + TM_S + 8 * ks,
+                                    sdesc_sw128(aWQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                    id_px, ks > 0);
+                    mma_commit(&bar_p);
                 }
             }
-            if (!mbar_wait(&bar_ld[b], par_st) || !mbar_wait(&bar_p, par)) {
-                set_status(p.status, kDevTimeout);
-                sAbort = 1;
-            }
+            if (!mbar_wait(&bar_ld[b], par_st) || !mbar_wait(&bar_p, par)) { fail(); break; }
             tc_fence_after();
             const float egC = __expf(reinterpret_cast<const float *>(st + ST_G)[C - 1]);
-
             // ---- U^T = U~^T - P^T for tokens [32*half, 32*half + 32) -> TMEM (bf16) ----
             {
                 uint32_t r[32];
-                tmem_ld32(tb + lane_base + TM_P + half * 32, r);
+                tmem_ld32(tb + lane_base + TM_PX + half * 32, r);
                 tmem_ld_wait();
                 const unsigned char *sU = st + ST_U;
                 uint32_t pk[16];
@@ -772,71 +776,55 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 tmem_st_wait();
             }
             tc_fence_before();
-            named_sync(BAR_MAIN, P2_MAIN);
+            mbar_arrive(&bar_u);
 
-            // ---- Z^T = U^T (diag(exp(g_C - g)) K) first (it gates the next chunk),
-            //      then O^T += U^T A^T ----
-            if (tid == 0 && !sAbort) {
-                tc_fence_after();
-                const uint32_t aA = smem_u32(st + ST_A), aK = smem_u32(st + ST_K);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ta(tb + TM_Z, tb + TM_U + 8 * ks,
-                                sdesc_sw128(aK + ks * 2048, 8192, 1024), id_z, ks > 0);
-                mma_commit(&bar_s);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ta(tb + TM_O + 64 * ob, tb + TM_U + 8 * ks,
-                                sdesc_sw128(aA + ks * 32, 16, 1024), id_64, 1u);
-                mma_commit(&bar_o);
-            }
-            if (!mbar_wait(&bar_s, par)) {
-                set_status(p.status, kDevTimeout);
-                sAbort = 1;
-            }
-            tc_fence_after();
-
-            // ---- S^T <- exp(g_C) S^T + Z^T ; new bf16 copy of S^T in TMEM ----
-            if (!sAbort) {
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    uint32_t r[32];
-                    tmem_ld32(tb + lane_base + TM_Z + half * 64 + c2 * 32, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        Sr[c2 * 32 + i] = fmaf(egC, Sr[c2 * 32 + i], __uint_as_float(r[i]));
-                }
-                store_state_bf16(tb + lane_base + TM_S + 32 * half, Sr);
-                tmem_st_wait();
-            }
-            tc_fence_before();
-            named_sync(BAR_MAIN, P2_MAIN);
-            if (sAbort) break;
-
-            // ---- refill this stage with chunk c + NSTAGE once O^T += U^T A^T has read it ----
-            if (tid == 0 && c + NSTAGE < nch) {
-                if (!mbar_wait(&bar_o, par)) {
-                    sAbort = 1;
-                    set_status(p.status, kDevTimeout);
+            // ---- [Z^T | Y^T] = U^T [diag(exp(g_C - g)) K | A^T] ----
+            if (tid == 0) {
+                if (!mbar_wait(&bar_u, par)) {
+                    fail();
                 } else {
-                    const long slot = (chunk0 + c + NSTAGE) * p.H + h;
-                    issue_stage(st, &bar_ld[b], &mq, &mk, &mw, &mu, &ma, p.g_ws + slot * C, h,
-                                (int)(start + (long)(c + NSTAGE) * C), (int)slot);
+                    tc_fence_after();
+                    const uint32_t aKA = smem_u32(st + ST_KA);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ta(tb + TM_ZY, tb + TM_U + 8 * ks,
+                                    sdesc_sw128(aKA + ks * 2048, 8192, 1024), id_zy, ks > 0);
+                    mma_commit(&bar_zy);
                 }
             }
+            if (!mbar_wait(&bar_zy, par)) { fail(); break; }
+            tc_fence_after();
+            // both products have read this stage: refill it with chunk c + NSTAGE
+            if (tid == 0 && c + NSTAGE < nch) {
+                const long slot = (chunk0 + c + NSTAGE) * p.H + h;
+                issue_stage(st, &bar_ld[b], &mq, &mk, &mw, &mu, &ma, p.g_ws + slot * C, h,
+                            (int)(start + (long)(c + NSTAGE) * C), (int)slot);
+            }
+            // ---- S^T <- exp(g_C) S^T + Z^T ; new bf16 copy of S^T in TMEM ----
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+                uint32_t r[32];
+                tmem_ld32(tb + lane_base + TM_ZY + half * 64 + c2 * 32, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    Sr[c2 * 32 + i] = fmaf(egC, Sr[c2 * 32 + i], __uint_as_float(r[i]));
+            }
+            store_state_bf16(tb + lane_base + TM_S + 32 * half, Sr);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bar_sready);
         }
         if (!sAbort && p.S_T) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)(64 * half + i) * D + j] = Sr[i];
         }
     } else {
-        // ----------------------------------------------------------------- aux warps
+        // ----------------------------------------------------------------- aux
         const int a = tid - P2_MAIN;     // 0..127; TMEM lane quarter = warp & 3
         if (nch > 0) {
             if (!mbar_wait(&bar_ld[0], 0)) {
-                sAbort = 1;
-                set_status(p.status, kDevTimeout);
+                fail();
             } else {
                 scale_stage(sm, (int)min((long)C, len), a);
             }
@@ -844,39 +832,35 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             mbar_arrive(&bar_scaled[0]);
         }
         for (int c = 0; c < nch && !sAbort; ++c) {
-            const int ob = c & 1;
             // scale the next chunk as soon as it lands
             if (c + 1 < nch) {
                 const int b1 = (c + 1) % NSTAGE;
-                if (!mbar_wait(&bar_ld[b1], (uint32_t)(((c + 1) / NSTAGE) & 1))) {
-                    sAbort = 1;
-                    set_status(p.status, kDevTimeout);
-                    break;
-                }
+                if (!mbar_wait(&bar_ld[b1], (uint32_t)(((c + 1) / NSTAGE) & 1))) { fail(); break; }
                 scale_stage(sm + b1 * ST_BYTES, (int)min((long)C, len - (long)(c + 1) * C), a);
                 fence_async_smem();
                 mbar_arrive(&bar_scaled[b1]);
             }
-            // output rows of chunk c: O^T row j (64 tokens) from TMEM
-            if (!mbar_wait(&bar_o, (uint32_t)(c & 1))) {
-                sAbort = 1;
-                set_status(p.status, kDevTimeout);
-                break;
-            }
+            // output rows of chunk c: O^T row j = X^T + Y^T (64 tokens)
+            if (!mbar_wait(&bar_zy, (uint32_t)(c & 1))) { fail(); break; }
             tc_fence_after();
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tb + lane_base + TM_O + 64 * ob, r0);
-            tmem_ld32(tb + lane_base + TM_O + 64 * ob + 32, r1);
+            uint32_t x0[32], x1[32], y0[32], y1[32];
+            tmem_ld32(tb + lane_base + TM_PX + 64, x0);
+            tmem_ld32(tb + lane_base + TM_PX + 96, x1);
+            tmem_ld32(tb + lane_base + TM_ZY + 128, y0);
+            tmem_ld32(tb + lane_base + TM_ZY + 160, y1);
             tmem_ld_wait();
             tc_fence_before();
-            mbar_arrive(&bar_ofree[ob]);
+            mbar_arrive(&bar_ofree);
             const int nc = (int)min((long)C, len - (long)c * C);
             __nv_bfloat16 *dst = p.o + (size_t)(start + (long)c * C) * p.H * D + (size_t)h * D + j;
             const size_t rs = (size_t)p.H * D;
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
-                if (t < nc) dst[t * rs] = __float2bfloat16_rn(__uint_as_float(r0[t]));
-                if (t + 32 < nc) dst[(t + 32) * rs] = __float2bfloat16_rn(__uint_as_float(r1[t]));
+                if (t < nc)
+                    dst[t * rs] = __float2bfloat16_rn(__uint_as_float(x0[t]) + __uint_as_float(y0[t]));
+                if (t + 32 < nc)
+                    dst[(t + 32) * rs] =
+                        __float2bfloat16_rn(__uint_as_float(x1[t]) + __uint_as_float(y1[t]));
             }
         }
     }
