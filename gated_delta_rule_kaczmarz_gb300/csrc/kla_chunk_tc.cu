@@ -753,7 +753,15 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                     mma_commit(&bar_p);
                 }
             }
-            if (!mbar_wait(&bar_ld[b], par_st) || !mbar_wait(&bar_p, par)) { fail(); break; }
+            // Warp 0 reconverges here so that its other lanes never sit in an
+            // mbarrier wait for work that lane 0 has yet to issue (a waiting
+            // warp is suspended, which would stall lane 0 as well).
+            if (warp == 0) __syncwarp();
+            // every lane of a warp takes the same branch, even on a timeout
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_p, par))) {
+                fail();
+                break;
+            }
             tc_fence_after();
             const float egC = __expf(reinterpret_cast<const float *>(st + ST_G)[C - 1]);
             // ---- U^T = U~^T - P^T for tokens [32*half, 32*half + 32) -> TMEM (bf16) ----
@@ -792,7 +800,11 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                     mma_commit(&bar_zy);
                 }
             }
-            if (!mbar_wait(&bar_zy, par)) { fail(); break; }
+            if (warp == 0) __syncwarp();
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_zy, par))) {
+                fail();
+                break;
+            }
             tc_fence_after();
             // both products have read this stage: refill it with chunk c + NSTAGE
             if (tid == 0 && c + NSTAGE < nch) {
@@ -800,6 +812,7 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 issue_stage(st, &bar_ld[b], &mq, &mk, &mw, &mu, &ma, p.g_ws + slot * C, h,
                             (int)(start + (long)(c + NSTAGE) * C), (int)slot);
             }
+            if (warp == 0) __syncwarp();
             // ---- S^T <- exp(g_C) S^T + Z^T ; new bf16 copy of S^T in TMEM ----
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
