@@ -30,9 +30,10 @@
 //   [Z^T | Y^T] = U^T [diag(exp(g_C - g)) K | A^T]
 //   S^T <- exp(g_C) S^T + Z^T (fp32 registers) ;  O^T = X^T + Y^T
 // The serial chain is P -> U -> Z -> S; a dedicated warp issues the MMAs and
-// TMA loads (three chunks in flight), and separate warps scale the next
-// chunk's Q and K tiles and store the outputs.  S^T and U^T, the bf16 A
-// operands, are kept in tensor memory.
+// TMA loads (three chunks in flight), separate warps scale each chunk's Q and
+// K tiles as they land, and the chain's warps store a chunk's outputs while
+// the next chunk's first product runs.  S^T and U^T, the bf16 A operands, are
+// kept in tensor memory.
 //
 // All waits are bounded (kla_tc.cuh); a wait that gives up sets the status
 // word to a timeout code and the CTA leaves after releasing TMEM.
@@ -563,18 +564,20 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
 // ===================================================================== phase 2
 // Warp roles:
-//   warps 0-7  ("main"): the serial chain; thread (j, half) owns dv index j
-//              (its TMEM lane) and tokens [32*half, +32) / state rows
-//              [64*half, +64).  Thread 0 also issues every MMA and TMA load.
-//   warps 8-11 ("aux"):  scale the next chunk's Q and K tiles in shared
-//              memory and write each chunk's output rows.
+//   warps 0-7  ("main"): the serial chain and the outputs; thread (j, half)
+//              owns dv index j (its TMEM lane) and tokens [32*half, +32) /
+//              state rows [64*half, +64).
+//   warps 8-10 ("scale"): scale each chunk's Q and K tiles in shared memory
+//              as soon as they land.
+//   warp 11    ("issuer"): issues every MMA and TMA load from lane 0; the
+//              warp waits on its barriers converged.
 // Per chunk the tensor core runs two wide products:
 //   [P^T | X^T] = S^T [W ; diag(exp g) Q]^T                 M=128, N=128, K=128
 //   [Z^T | Y^T] = U^T [diag(exp(g_C - g)) K | A^T]           M=128, N=192, K=64
 // with U^T = U~^T - P^T, S^T <- exp(g_C) S^T + Z^T and O^T = X^T + Y^T.
 // The bf16 A operands S^T and U^T live in tensor memory, which leaves shared
 // memory for three chunk stages in flight.
-constexpr int P2_MAIN = 256, P2_AUX = 128, P2_THREADS = P2_MAIN + P2_AUX;
+constexpr int P2_MAIN = 256, P2_SCALE = 96, P2_THREADS = P2_MAIN + P2_SCALE + 32;
 constexpr int NSTAGE = 3;
 // Stage layout (one chunk):
 //   WQ: two 64-feature slabs of 16 KB, each [W rows 0..63 | Q rows 0..63]
@@ -607,15 +610,14 @@ __device__ __forceinline__ void issue_stage(unsigned char *st, uint64_t *bar,
     bulk_load(st + ST_G, g_src, 256, bar);
 }
 
-// Aux warps: scale a landed stage in place, Q rows by exp(g_t) and K rows by
-// exp(g_C - g_t); rows at or past the chunk's valid length are cleared.
-// Thread a (0..127): row a % 64 of Q (a < 64) or K (a >= 64), both halves.
+// Scale warps: scale a landed stage in place, Q rows by exp(g_t) and K rows
+// by exp(g_C - g_t); rows at or past the chunk's valid length are cleared.
+// Work item x (0..255): tensor x >> 7 (Q, K), row (x >> 1) & 63, half x & 1.
 __device__ __forceinline__ void scale_stage(unsigned char *st, int nc, int a) {
-    const int which = a >> 6, t = a & 63;
     const float *g = reinterpret_cast<const float *>(st + ST_G);
-    const float f = which == 0 ? __expf(g[t]) : __expf(g[C - 1] - g[t]);
-#pragma unroll
-    for (int hp = 0; hp < 2; ++hp) {
+    for (int x = a; x < 256; x += P2_SCALE) {
+        const int which = x >> 7, t = (x >> 1) & 63, hp = x & 1;
+        const float f = which == 0 ? __expf(g[t]) : __expf(g[C - 1] - g[t]);
         unsigned char *base = which == 0 ? st + ST_WQ + hp * 16384 + 8192 : st + ST_KA + hp * 8192;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
@@ -651,7 +653,7 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
              const __grid_constant__ CUtensorMap ma, const TcParams p) {
     extern __shared__ unsigned char smraw[];
     __shared__ uint64_t bar_ld[NSTAGE], bar_scaled[NSTAGE];
-    __shared__ uint64_t bar_p, bar_u, bar_zy, bar_sready, bar_ofree;
+    __shared__ uint64_t bar_p, bar_u, bar_zy, bar_sready;
     __shared__ uint32_t tslot;
     __shared__ int sAbort;
 
@@ -659,7 +661,6 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;
-    const bool is_main = tid < P2_MAIN;
     const int half = (warp >> 2) & 1;           // main warps only
     const int j = quarter * 32 + lane;          // dv index = TMEM lane of this thread
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -683,13 +684,12 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     if (tid == 0) {
         for (int i = 0; i < NSTAGE; ++i) {
             mbar_init(&bar_ld[i], 1);
-            mbar_init(&bar_scaled[i], P2_AUX);
+            mbar_init(&bar_scaled[i], P2_SCALE);
         }
         mbar_init(&bar_p, 1);
         mbar_init(&bar_u, P2_MAIN);
         mbar_init(&bar_zy, 1);
         mbar_init(&bar_sready, P2_MAIN);
-        mbar_init(&bar_ofree, P2_AUX);
         fence_mbar_init();
         sAbort = 0;
     }
@@ -703,7 +703,7 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
     // fp32 master state (main warps): S[i][j] for i in [64*half, 64*half+64)
     float Sr[64];
-    if (is_main) {
+    if (tid < P2_MAIN) {
 #pragma unroll
         for (int i = 0; i < 64; ++i)
             Sr[i] = p.S0 ? p.S0[sbase + (size_t)(64 * half + i) * D + j] : 0.f;
@@ -719,45 +719,65 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         set_status(p.status, kDevTimeout);
     };
 
-    if (is_main) {
-        // ----------------------------------------------------------------- main
+    if (warp == 11) {
+        // ----------------------------------------------------------------- issuer
         const uint32_t id_px = idesc_bf16_f32(128, 128, false, false);
         const uint32_t id_zy = idesc_bf16_f32(128, 192, false, true);
-        if (tid == 0) {
+        if (lane == 0) {
             for (int c = 0; c < NSTAGE && c < nch; ++c) {
                 const long slot = (chunk0 + c) * p.H + h;
                 issue_stage(sm + c * ST_BYTES, &bar_ld[c], &mq, &mk, &mw, &mu, &ma,
                             p.g_ws + slot * C, h, (int)(start + (long)c * C), (int)slot);
             }
         }
+        __syncwarp();
         for (int c = 0; c < nch; ++c) {
             const int b = c % NSTAGE;
             unsigned char *st = sm + b * ST_BYTES;
             const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NSTAGE) & 1);
-
-            // ---- [P^T | X^T] = S^T [W ; diag(exp g) Q]^T ----
-            if (tid == 0) {
-                bool ok = mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_scaled[b], par_st);
-                if (ok && c >= 1)   // previous chunk's state written, its outputs read
-                    ok = mbar_wait(&bar_sready, par ^ 1u) && mbar_wait(&bar_ofree, par ^ 1u);
-                if (!ok) {
-                    fail();
-                } else {
-                    tc_fence_after();
-                    const uint32_t aWQ = smem_u32(st + ST_WQ);
+            bool ok = mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_scaled[b], par_st);
+            if (ok && c >= 1) ok = mbar_wait(&bar_sready, par ^ 1u);  // chunk c-1 finished
+            if (!__all_sync(0xffffffffu, ok)) { fail(); break; }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t aWQ = smem_u32(st + ST_WQ);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16_ta(tb + TM_PX, tb + TM_S + 8 * ks,
-                                    sdesc_sw128(aWQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                                    id_px, ks > 0);
-                    mma_commit(&bar_p);
-                }
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ta(tb + TM_PX, tb + TM_S + 8 * ks,
+                                sdesc_sw128(aWQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                id_px, ks > 0);
+                mma_commit(&bar_p);
             }
-            // Warp 0 reconverges here so that its other lanes never sit in an
-            // mbarrier wait for work that lane 0 has yet to issue (a waiting
-            // warp is suspended, which would stall lane 0 as well).
-            if (warp == 0) __syncwarp();
-            // every lane of a warp takes the same branch, even on a timeout
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_u, par))) { fail(); break; }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t aKA = smem_u32(st + ST_KA);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16_ta(tb + TM_ZY, tb + TM_U + 8 * ks,
+                                sdesc_sw128(aKA + ks * 2048, 8192, 1024), id_zy, ks > 0);
+                mma_commit(&bar_zy);
+            }
+            __syncwarp();
+            // both products have read this stage: refill it with chunk c + NSTAGE
+            if (c + NSTAGE < nch) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_zy, par))) { fail(); break; }
+                if (lane == 0) {
+                    const long slot = (chunk0 + c + NSTAGE) * p.H + h;
+                    issue_stage(st, &bar_ld[b], &mq, &mk, &mw, &mu, &ma, p.g_ws + slot * C, h,
+                                (int)(start + (long)(c + NSTAGE) * C), (int)slot);
+                }
+                __syncwarp();
+            }
+        }
+    } else if (tid < P2_MAIN) {
+        // ----------------------------------------------------------------- main
+        const size_t rs = (size_t)p.H * D;
+        for (int c = 0; c < nch; ++c) {
+            const int b = c % NSTAGE;
+            unsigned char *st = sm + b * ST_BYTES;
+            const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NSTAGE) & 1);
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_p, par))) {
                 fail();
                 break;
@@ -786,33 +806,20 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             tc_fence_before();
             mbar_arrive(&bar_u);
 
-            // ---- [Z^T | Y^T] = U^T [diag(exp(g_C - g)) K | A^T] ----
-            if (tid == 0) {
-                if (!mbar_wait(&bar_u, par)) {
-                    fail();
-                } else {
-                    tc_fence_after();
-                    const uint32_t aKA = smem_u32(st + ST_KA);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ta(tb + TM_ZY, tb + TM_U + 8 * ks,
-                                    sdesc_sw128(aKA + ks * 2048, 8192, 1024), id_zy, ks > 0);
-                    mma_commit(&bar_zy);
-                }
-            }
-            if (warp == 0) __syncwarp();
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_zy, par))) {
-                fail();
-                break;
-            }
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_zy, par))) { fail(); break; }
             tc_fence_after();
-            // both products have read this stage: refill it with chunk c + NSTAGE
-            if (tid == 0 && c + NSTAGE < nch) {
-                const long slot = (chunk0 + c + NSTAGE) * p.H + h;
-                issue_stage(st, &bar_ld[b], &mq, &mk, &mw, &mu, &ma, p.g_ws + slot * C, h,
-                            (int)(start + (long)(c + NSTAGE) * C), (int)slot);
+            // ---- outputs of this chunk: O^T = X^T + Y^T for tokens [32*half, +32) ----
+            uint32_t opk[16];
+            {
+                uint32_t xr[32], yr[32];
+                tmem_ld32(tb + lane_base + TM_PX + 64 + half * 32, xr);
+                tmem_ld32(tb + lane_base + TM_ZY + 128 + half * 32, yr);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    opk[i] = pack_bf2(__uint_as_float(xr[2 * i]) + __uint_as_float(yr[2 * i]),
+                                      __uint_as_float(xr[2 * i + 1]) + __uint_as_float(yr[2 * i + 1]));
             }
-            if (warp == 0) __syncwarp();
             // ---- S^T <- exp(g_C) S^T + Z^T ; new bf16 copy of S^T in TMEM ----
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
@@ -827,54 +834,32 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bar_sready);
+            // stores overlap the next chunk's first product
+            const int nc = (int)min((long)C, len - (long)c * C);
+            __nv_bfloat16 *dst = p.o + (size_t)(start + (long)c * C + 32 * half) * rs + (size_t)h * D + j;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t = 32 * half + 2 * i;
+                if (t < nc) dst[(2 * i) * rs] = __ushort_as_bfloat16((unsigned short)(opk[i] & 0xffffu));
+                if (t + 1 < nc) dst[(2 * i + 1) * rs] = __ushort_as_bfloat16((unsigned short)(opk[i] >> 16));
+            }
         }
         if (!sAbort && p.S_T) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)(64 * half + i) * D + j] = Sr[i];
         }
     } else {
-        // ----------------------------------------------------------------- aux
-        const int a = tid - P2_MAIN;     // 0..127; TMEM lane quarter = warp & 3
-        if (nch > 0) {
-            if (!mbar_wait(&bar_ld[0], 0)) {
+        // ----------------------------------------------------------------- scale
+        const int a = tid - P2_MAIN;     // 0..95
+        for (int c = 0; c < nch; ++c) {
+            const int b = c % NSTAGE;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_ld[b], (uint32_t)((c / NSTAGE) & 1)))) {
                 fail();
-            } else {
-                scale_stage(sm, (int)min((long)C, len), a);
+                break;
             }
+            scale_stage(sm + b * ST_BYTES, (int)min((long)C, len - (long)c * C), a);
             fence_async_smem();
-            mbar_arrive(&bar_scaled[0]);
-        }
-        for (int c = 0; c < nch && !sAbort; ++c) {
-            // scale the next chunk as soon as it lands
-            if (c + 1 < nch) {
-                const int b1 = (c + 1) % NSTAGE;
-                if (!mbar_wait(&bar_ld[b1], (uint32_t)(((c + 1) / NSTAGE) & 1))) { fail(); break; }
-                scale_stage(sm + b1 * ST_BYTES, (int)min((long)C, len - (long)(c + 1) * C), a);
-                fence_async_smem();
-                mbar_arrive(&bar_scaled[b1]);
-            }
-            // output rows of chunk c: O^T row j = X^T + Y^T (64 tokens)
-            if (!mbar_wait(&bar_zy, (uint32_t)(c & 1))) { fail(); break; }
-            tc_fence_after();
-            uint32_t x0[32], x1[32], y0[32], y1[32];
-            tmem_ld32(tb + lane_base + TM_PX + 64, x0);
-            tmem_ld32(tb + lane_base + TM_PX + 96, x1);
-            tmem_ld32(tb + lane_base + TM_ZY + 128, y0);
-            tmem_ld32(tb + lane_base + TM_ZY + 160, y1);
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&bar_ofree);
-            const int nc = (int)min((long)C, len - (long)c * C);
-            __nv_bfloat16 *dst = p.o + (size_t)(start + (long)c * C) * p.H * D + (size_t)h * D + j;
-            const size_t rs = (size_t)p.H * D;
-#pragma unroll
-            for (int t = 0; t < 32; ++t) {
-                if (t < nc)
-                    dst[t * rs] = __float2bfloat16_rn(__uint_as_float(x0[t]) + __uint_as_float(y0[t]));
-                if (t + 32 < nc)
-                    dst[(t + 32) * rs] =
-                        __float2bfloat16_rn(__uint_as_float(x1[t]) + __uint_as_float(y1[t]));
-            }
+            mbar_arrive(&bar_scaled[b]);
         }
     }
 
