@@ -21,19 +21,19 @@
 // inverts I + L in fp32 on the CUDA cores (forward substitution on 16 x 16
 // diagonal blocks, then two doubling steps made of small products), and forms
 // W = (T diag beta)(diag(exp g) K) and U~^T = V^T (T diag beta)^T with two
-// MMAs.  W, U~^T, A (bf16) and g (fp32) go to the caller's workspace.
+// MMAs.  W, U~^T, A^T and diag(exp(g_C - g)) K (bf16) and exp(g) (fp32) go to
+// the caller's workspace.
 //
 // Phase 2 (state_kernel) walks the chunks of one (sequence, head) in order,
 // every product with M = dv = 128 rows and the two products of a step fused
 // into one wide MMA (issue cost per tcgen05.mma is nearly independent of N):
-//   [P^T | X^T] = S^T [W ; diag(exp g) Q]^T ;  U^T = U~^T - P^T
+//   [P^T | X^T] = S^T [W ; Q]^T ;  U^T = U~^T - P^T
 //   [Z^T | Y^T] = U^T [diag(exp(g_C - g)) K | A^T]
-//   S^T <- exp(g_C) S^T + Z^T (fp32 registers) ;  O^T = X^T + Y^T
+//   S^T <- exp(g_C) S^T + Z^T (fp32 registers) ;  O^T = X^T diag(exp g) + Y^T
 // The serial chain is P -> U -> Z -> S; a dedicated warp issues the MMAs and
-// TMA loads (three chunks in flight), separate warps scale each chunk's Q and
-// K tiles as they land, and the chain's warps store a chunk's outputs while
-// the next chunk's first product runs.  S^T and U^T, the bf16 A operands, are
-// kept in tensor memory.
+// TMA loads (three chunks in flight), and the chain's warps store a chunk's
+// outputs while the next chunk's first product runs.  S^T and U^T, the bf16 A
+// operands, are kept in tensor memory.
 //
 // All waits are bounded (kla_tc.cuh); a wait that gives up sets the status
 // word to a timeout code and the CTA leaves after releasing TMEM.
@@ -66,7 +66,8 @@ struct TcParams {
     const int *chunk_prefix;   // varlen only: first chunk of each sequence, [N+1]
     const int *order;          // varlen only: sequences by decreasing length, [N]
     unsigned *status;
-    float *g_ws;               // [slots][64]
+    float *eg_ws;              // [slots][64]        exp(g_t)
+    __nv_bfloat16 *Kt_ws;      // [slots][64][128]   diag(exp(g_C - g)) K
     __nv_bfloat16 *W_ws;       // [slots][64][128]
     __nv_bfloat16 *UT_ws;      // [slots][128][64]  U~ transposed (feature-major)
     __nv_bfloat16 *A_ws;       // [slots][64 keys s][64 queries t]  A^T
@@ -424,8 +425,11 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         // K row -> diag(exp g) K; rows past the chunk's end (another
         // sequence's tokens or TMA zero fill) are cleared in K and V so that
         // nothing from them can reach the products.
+        // The state pass needs diag(exp(g_C - g)) K; it goes to the workspace.
         const float gam_t = __expf(gt);
+        const float gam_c = __expf(sG[cb + C - 1] - gt);
         const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+        uint4 *kt_row = reinterpret_cast<uint4 *>(p.Kt_ws + slot_row * D);
 #pragma unroll 1
         for (int s = 0; s < 2; ++s)
 #pragma unroll 2
@@ -437,7 +441,13 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                                       pack_bf2(gam_t * bf_lo(v.y), gam_t * bf_hi(v.y)),
                                       pack_bf2(gam_t * bf_lo(v.z), gam_t * bf_hi(v.z)),
                                       pack_bf2(gam_t * bf_lo(v.w), gam_t * bf_hi(v.w)));
+                    if (vslot)
+                        kt_row[s * 8 + ch] = make_uint4(pack_bf2(gam_c * bf_lo(v.x), gam_c * bf_hi(v.x)),
+                                                        pack_bf2(gam_c * bf_lo(v.y), gam_c * bf_hi(v.y)),
+                                                        pack_bf2(gam_c * bf_lo(v.z), gam_c * bf_hi(v.z)),
+                                                        pack_bf2(gam_c * bf_lo(v.w), gam_c * bf_hi(v.w)));
                 } else {
+                    if (vslot) kt_row[s * 8 + ch] = zero4;
                     *pk4 = zero4;
                     *reinterpret_cast<uint4 *>(sV + s * 16384 + sw128_offset(tid, ch * 8)) = zero4;
                 }
@@ -538,7 +548,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 tmem_ld_wait();
                 store_bf16x32(dst_row + c4 * 32, r);
             }
-            p.g_ws[slot_row] = gt;
+            p.eg_ws[slot_row] = __expf(gt);
         }
         // lane j of U~^T holds feature j for the tokens of both chunks
 #pragma unroll 1
@@ -564,26 +574,25 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
 // ===================================================================== phase 2
 // Warp roles:
-//   warps 0-7  ("main"): the serial chain and the outputs; thread (j, half)
-//              owns dv index j (its TMEM lane) and tokens [32*half, +32) /
-//              state rows [64*half, +64).
-//   warps 8-10 ("scale"): scale each chunk's Q and K tiles in shared memory
-//              as soon as they land.
-//   warp 11    ("issuer"): issues every MMA and TMA load from lane 0; the
-//              warp waits on its barriers converged.
+//   warps 0-7 ("main"): the serial chain and the outputs; thread (j, half)
+//             owns dv index j (its TMEM lane) and tokens [32*half, +32) /
+//             state rows [64*half, +64).
+//   warp 8    ("issuer"): issues every MMA and TMA load from lane 0; the warp
+//             waits on its barriers converged.
 // Per chunk the tensor core runs two wide products:
-//   [P^T | X^T] = S^T [W ; diag(exp g) Q]^T                 M=128, N=128, K=128
-//   [Z^T | Y^T] = U^T [diag(exp(g_C - g)) K | A^T]           M=128, N=192, K=64
-// with U^T = U~^T - P^T, S^T <- exp(g_C) S^T + Z^T and O^T = X^T + Y^T.
-// The bf16 A operands S^T and U^T live in tensor memory, which leaves shared
-// memory for three chunk stages in flight.
-constexpr int P2_MAIN = 256, P2_SCALE = 96, P2_THREADS = P2_MAIN + P2_SCALE + 32;
+//   [P^T | X^T] = S^T [W ; Q]^T                                M=128, N=128, K=128
+//   [Z^T | Y^T] = U^T [diag(exp(g_C - g)) K | A^T]             M=128, N=192, K=64
+// with U^T = U~^T - P^T, S^T <- exp(g_C) S^T + Z^T and
+// O^T = X^T diag(exp g) + Y^T.  diag(exp(g_C - g)) K and exp(g) come from
+// phase 1.  The bf16 A operands S^T and U^T live in tensor memory, which
+// leaves shared memory for three chunk stages in flight.
+constexpr int P2_MAIN = 256, P2_THREADS = P2_MAIN + 32;
 constexpr int NSTAGE = 3;
 // Stage layout (one chunk):
 //   WQ: two 64-feature slabs of 16 KB, each [W rows 0..63 | Q rows 0..63]
-//   KA: K slab 0, K slab 1, A^T (8 KB each): MN-major n-blocks 8 KB apart
-//   U:  U~^T [128][64];  G: g [64]
-constexpr uint32_t ST_WQ = 0, ST_KA = 32768, ST_A = 49152, ST_U = 57344, ST_G = 73728,
+//   KA: K~ slab 0, K~ slab 1, A^T (8 KB each): MN-major n-blocks 8 KB apart
+//   U:  U~^T [128][64];  EG: exp(g) [64]
+constexpr uint32_t ST_WQ = 0, ST_KA = 32768, ST_A = 49152, ST_U = 57344, ST_EG = 73728,
                    ST_BYTES = 74752;
 constexpr uint32_t ST_TX = 16384u * 4u + 8192u + 256u;  // bytes a stage receives
 constexpr uint32_t P2_SMEM = NSTAGE * ST_BYTES + 1024;
@@ -594,45 +603,20 @@ constexpr uint32_t P2_SMEM = NSTAGE * ST_BYTES + 1024;
 constexpr uint32_t TM_PX = 0, TM_ZY = 128, TM_S = 320, TM_U = 384;
 
 __device__ __forceinline__ void issue_stage(unsigned char *st, uint64_t *bar,
-                                            const CUtensorMap *mq, const CUtensorMap *mk,
+                                            const CUtensorMap *mq, const CUtensorMap *mkt,
                                             const CUtensorMap *mw, const CUtensorMap *mu,
-                                            const CUtensorMap *ma, const float *g_src, int h,
+                                            const CUtensorMap *ma, const float *eg_src, int h,
                                             int row0, int slot) {
     mbar_expect_tx(bar, ST_TX);
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
         tma_load_2d(st + ST_WQ + s * 16384, mw, bar, 64 * s, slot * C);
         tma_load_3d(st + ST_WQ + s * 16384 + 8192, mq, bar, 64 * s, h, row0);
-        tma_load_3d(st + ST_KA + s * 8192, mk, bar, 64 * s, h, row0);
+        tma_load_2d(st + ST_KA + s * 8192, mkt, bar, 64 * s, slot * C);
     }
     tma_load_2d(st + ST_A, ma, bar, 0, slot * C);
     tma_load_2d(st + ST_U, mu, bar, 0, slot * D);
-    bulk_load(st + ST_G, g_src, 256, bar);
-}
-
-// Scale warps: scale a landed stage in place, Q rows by exp(g_t) and K rows
-// by exp(g_C - g_t); rows at or past the chunk's valid length are cleared.
-// Work item x (0..255): tensor x >> 7 (Q, K), row (x >> 1) & 63, half x & 1.
-__device__ __forceinline__ void scale_stage(unsigned char *st, int nc, int a) {
-    const float *g = reinterpret_cast<const float *>(st + ST_G);
-    for (int x = a; x < 256; x += P2_SCALE) {
-        const int which = x >> 7, t = (x >> 1) & 63, hp = x & 1;
-        const float f = which == 0 ? __expf(g[t]) : __expf(g[C - 1] - g[t]);
-        unsigned char *base = which == 0 ? st + ST_WQ + hp * 16384 + 8192 : st + ST_KA + hp * 8192;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            uint4 *p4 = reinterpret_cast<uint4 *>(base + sw128_offset(t, ch * 8));
-            if (t < nc) {
-                const uint4 v = *p4;
-                *p4 = make_uint4(pack_bf2(f * bf_lo(v.x), f * bf_hi(v.x)),
-                                 pack_bf2(f * bf_lo(v.y), f * bf_hi(v.y)),
-                                 pack_bf2(f * bf_lo(v.z), f * bf_hi(v.z)),
-                                 pack_bf2(f * bf_lo(v.w), f * bf_hi(v.w)));
-            } else {
-                *p4 = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-    }
+    bulk_load(st + ST_EG, eg_src, 256, bar);
 }
 
 // Main warps: bf16 copy of the 64 state values S[64*half + i][j] into the
@@ -648,11 +632,11 @@ __device__ __forceinline__ void store_state_bf16(uint32_t taddr, const float (&S
 }
 
 __global__ void __launch_bounds__(P2_THREADS, 1)
-state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mkt,
              const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
              const __grid_constant__ CUtensorMap ma, const TcParams p) {
     extern __shared__ unsigned char smraw[];
-    __shared__ uint64_t bar_ld[NSTAGE], bar_scaled[NSTAGE];
+    __shared__ uint64_t bar_ld[NSTAGE];
     __shared__ uint64_t bar_p, bar_u, bar_zy, bar_sready;
     __shared__ uint32_t tslot;
     __shared__ int sAbort;
@@ -682,10 +666,7 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const size_t sbase = ((size_t)seq * p.H + h) * D * D;
 
     if (tid == 0) {
-        for (int i = 0; i < NSTAGE; ++i) {
-            mbar_init(&bar_ld[i], 1);
-            mbar_init(&bar_scaled[i], P2_SCALE);
-        }
+        for (int i = 0; i < NSTAGE; ++i) mbar_init(&bar_ld[i], 1);
         mbar_init(&bar_p, 1);
         mbar_init(&bar_u, P2_MAIN);
         mbar_init(&bar_zy, 1);
@@ -719,15 +700,15 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         set_status(p.status, kDevTimeout);
     };
 
-    if (warp == 11) {
+    if (warp == 8) {
         // ----------------------------------------------------------------- issuer
         const uint32_t id_px = idesc_bf16_f32(128, 128, false, false);
         const uint32_t id_zy = idesc_bf16_f32(128, 192, false, true);
         if (lane == 0) {
             for (int c = 0; c < NSTAGE && c < nch; ++c) {
                 const long slot = (chunk0 + c) * p.H + h;
-                issue_stage(sm + c * ST_BYTES, &bar_ld[c], &mq, &mk, &mw, &mu, &ma,
-                            p.g_ws + slot * C, h, (int)(start + (long)c * C), (int)slot);
+                issue_stage(sm + c * ST_BYTES, &bar_ld[c], &mq, &mkt, &mw, &mu, &ma,
+                            p.eg_ws + slot * C, h, (int)(start + (long)c * C), (int)slot);
             }
         }
         __syncwarp();
@@ -735,7 +716,7 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             const int b = c % NSTAGE;
             unsigned char *st = sm + b * ST_BYTES;
             const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NSTAGE) & 1);
-            bool ok = mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_scaled[b], par_st);
+            bool ok = mbar_wait(&bar_ld[b], par_st);
             if (ok && c >= 1) ok = mbar_wait(&bar_sready, par ^ 1u);  // chunk c-1 finished
             if (!__all_sync(0xffffffffu, ok)) { fail(); break; }
             tc_fence_after();
@@ -765,13 +746,13 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 if (!__all_sync(0xffffffffu, mbar_wait(&bar_zy, par))) { fail(); break; }
                 if (lane == 0) {
                     const long slot = (chunk0 + c + NSTAGE) * p.H + h;
-                    issue_stage(st, &bar_ld[b], &mq, &mk, &mw, &mu, &ma, p.g_ws + slot * C, h,
+                    issue_stage(st, &bar_ld[b], &mq, &mkt, &mw, &mu, &ma, p.eg_ws + slot * C, h,
                                 (int)(start + (long)(c + NSTAGE) * C), (int)slot);
                 }
                 __syncwarp();
             }
         }
-    } else if (tid < P2_MAIN) {
+    } else {
         // ----------------------------------------------------------------- main
         const size_t rs = (size_t)p.H * D;
         for (int c = 0; c < nch; ++c) {
@@ -783,7 +764,8 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 break;
             }
             tc_fence_after();
-            const float egC = __expf(reinterpret_cast<const float *>(st + ST_G)[C - 1]);
+            const float *eg = reinterpret_cast<const float *>(st + ST_EG);
+            const float egC = eg[C - 1];
             // ---- U^T = U~^T - P^T for tokens [32*half, 32*half + 32) -> TMEM (bf16) ----
             {
                 uint32_t r[32];
@@ -808,18 +790,6 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_zy, par))) { fail(); break; }
             tc_fence_after();
-            // ---- outputs of this chunk: O^T = X^T + Y^T for tokens [32*half, +32) ----
-            uint32_t opk[16];
-            {
-                uint32_t xr[32], yr[32];
-                tmem_ld32(tb + lane_base + TM_PX + 64 + half * 32, xr);
-                tmem_ld32(tb + lane_base + TM_ZY + 128 + half * 32, yr);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    opk[i] = pack_bf2(__uint_as_float(xr[2 * i]) + __uint_as_float(yr[2 * i]),
-                                      __uint_as_float(xr[2 * i + 1]) + __uint_as_float(yr[2 * i + 1]));
-            }
             // ---- S^T <- exp(g_C) S^T + Z^T ; new bf16 copy of S^T in TMEM ----
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
@@ -831,35 +801,39 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                     Sr[c2 * 32 + i] = fmaf(egC, Sr[c2 * 32 + i], __uint_as_float(r[i]));
             }
             store_state_bf16(tb + lane_base + TM_S + 32 * half, Sr);
+            // ---- O = diag(exp g) X + Y for this chunk's tokens, read before the next
+            //      product overwrites X^T, stored while that product runs ----
+            uint32_t opk[16];
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                uint32_t xr[16], yr[16];
+                tmem_ld16(tb + lane_base + TM_PX + 64 + half * 32 + 16 * q2, xr);
+                tmem_ld16(tb + lane_base + TM_ZY + 128 + half * 32 + 16 * q2, yr);
+                tmem_ld_wait();
+                const float *egt = eg + 32 * half + 16 * q2;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    opk[8 * q2 + i] =
+                        pack_bf2(fmaf(egt[2 * i], __uint_as_float(xr[2 * i]), __uint_as_float(yr[2 * i])),
+                                 fmaf(egt[2 * i + 1], __uint_as_float(xr[2 * i + 1]),
+                                      __uint_as_float(yr[2 * i + 1])));
+            }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bar_sready);
-            // stores overlap the next chunk's first product
             const int nc = (int)min((long)C, len - (long)c * C);
             __nv_bfloat16 *dst = p.o + (size_t)(start + (long)c * C + 32 * half) * rs + (size_t)h * D + j;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int t = 32 * half + 2 * i;
-                if (t < nc) dst[(2 * i) * rs] = __ushort_as_bfloat16((unsigned short)(opk[i] & 0xffffu));
-                if (t + 1 < nc) dst[(2 * i + 1) * rs] = __ushort_as_bfloat16((unsigned short)(opk[i] >> 16));
+                if (t < nc) dst[(size_t)(2 * i) * rs] = __ushort_as_bfloat16((unsigned short)(opk[i] & 0xffffu));
+                if (t + 1 < nc)
+                    dst[(size_t)(2 * i + 1) * rs] = __ushort_as_bfloat16((unsigned short)(opk[i] >> 16));
             }
         }
         if (!sAbort && p.S_T) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)(64 * half + i) * D + j] = Sr[i];
-        }
-    } else {
-        // ----------------------------------------------------------------- scale
-        const int a = tid - P2_MAIN;     // 0..95
-        for (int c = 0; c < nch; ++c) {
-            const int b = c % NSTAGE;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_ld[b], (uint32_t)((c / NSTAGE) & 1)))) {
-                fail();
-                break;
-            }
-            scale_stage(sm + b * ST_BYTES, (int)min((long)C, len - (long)c * C), a);
-            fence_async_smem();
-            mbar_arrive(&bar_scaled[b]);
         }
     }
 
@@ -984,7 +958,7 @@ int sm_count() {
 }
 
 struct WsLayout {
-    size_t meta, g, W, U, A, total;
+    size_t meta, g, W, U, A, Kt, total;
 };
 
 WsLayout layout(long n_chunks, int H, int n_seq) {
@@ -995,7 +969,8 @@ WsLayout layout(long n_chunks, int H, int n_seq) {
     L.W = L.g + align_up(slots * C * sizeof(float), 1024);
     L.U = L.W + slots * C * D * 2;
     L.A = L.U + slots * C * D * 2;
-    L.total = L.A + slots * C * C * 2;
+    L.Kt = L.A + slots * C * C * 2;
+    L.total = L.Kt + slots * C * D * 2;
     return L;
 }
 
@@ -1028,7 +1003,8 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     tp.o = static_cast<__nv_bfloat16 *>(p.o);
     tp.cu_seqlens = p.cu_seqlens;
     tp.status = p.status;
-    tp.g_ws = reinterpret_cast<float *>(ws + L.g);
+    tp.eg_ws = reinterpret_cast<float *>(ws + L.g);
+    tp.Kt_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.Kt);
     tp.W_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.W);
     tp.UT_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.U);
     tp.A_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.A);
@@ -1037,11 +1013,12 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     tp.chunk_prefix = p.cu_seqlens ? chunk_prefix : nullptr;
     tp.order = p.cu_seqlens ? order : nullptr;
 
-    CUtensorMap mq, mk, mv, mw, mu, ma;
+    CUtensorMap mq, mk, mv, mw, mu, ma, mkt;
     const long slots = n_chunks_upper * p.H;
     if (!map_3d_rows(&mq, p.q, p.H, p.total_T) || !map_3d_rows(&mk, p.k, p.H, p.total_T) ||
         !map_3d_rows(&mv, p.v, p.H, p.total_T) || !map_2d(&mw, tp.W_ws, D, slots * C, C) ||
-        !map_2d(&mu, tp.UT_ws, C, slots * D, D) || !map_2d(&ma, tp.A_ws, C, slots * C, C))
+        !map_2d(&mu, tp.UT_ws, C, slots * D, D) || !map_2d(&ma, tp.A_ws, C, slots * C, C) ||
+        !map_2d(&mkt, tp.Kt_ws, D, slots * C, C))
         return cudaErrorInvalidValue;
 
     cudaError_t e;
@@ -1067,7 +1044,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     intra_kernel<<<(unsigned)grid1, P1_THREADS, P1_SMEM, s>>>(mq, mk, mv, tp, n_pairs);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    state_kernel<<<(unsigned)(p.n_seq * p.H), P2_THREADS, P2_SMEM, s>>>(mq, mk, mw, mu, ma, tp);
+    state_kernel<<<(unsigned)(p.n_seq * p.H), P2_THREADS, P2_SMEM, s>>>(mq, mkt, mw, mu, ma, tp);
     note_launch();
     return cudaGetLastError();
 }
