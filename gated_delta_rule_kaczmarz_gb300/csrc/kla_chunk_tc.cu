@@ -20,21 +20,20 @@
 // persistent.  It computes K K^T and Q K^T on tcgen05 (TMEM accumulators),
 // inverts I + L in fp32 on the CUDA cores (forward substitution on 16 x 16
 // diagonal blocks, then two doubling steps made of small products), and forms
-// W = (T diag beta)(diag(exp g) K) and U~^T = V^T (T diag beta)^T with two
-// MMAs.  W, U~^T, A^T and diag(exp(g_C - g)) K (bf16) and exp(g) (fp32) go to
-// the caller's workspace.
+// W = (T diag beta)(diag(exp g) K) and U~ = (T diag beta) V with two MMAs.
+// W, U~, A^T and diag(exp(g_C - g)) K (bf16) and exp(g) (fp32) go to the
+// caller's workspace.
 //
-// Phase 2 (state_kernel) walks the chunks of one (sequence, head) in order,
-// every product with M = dv = 128 rows and the two products of a step fused
-// into one wide MMA (issue cost per tcgen05.mma is nearly independent of N):
-//   [P^T | X^T] = S^T [W ; Q]^T ;  U^T = U~^T - P^T
-//   [Z^T | Y^T] = U^T [diag(exp(g_C - g)) K | A^T]
-//   S^T <- exp(g_C) S^T + Z^T (fp32 registers) ;  O^T = X^T diag(exp g) + Y^T
-// The serial chain is P -> U -> Z -> S; a dedicated warp issues the MMAs and
-// TMA loads (three chunks in flight), and the chain's warps store a chunk's
-// outputs while the next chunk's first product runs.  S^T and U^T, the bf16 A
-// operands, are kept in tensor memory.
-//
+// Phase 2 (state_kernel) walks the chunks of one (sequence, head) in order;
+// the two 64-column halves of the state run in two CTAs, since the columns
+// of S evolve independently.  Per chunk, with S_b the CTA's dk x 64 slice:
+//   [X | P] = [Q ; W] S_b ;  U = U~_b - P
+//   Z = K~^T U ;  Y = A U     (K~ = diag(exp(g_C - g)) K)
+//   S_b <- exp(g_C) S_b + Z (fp32 registers) ;  O_b = diag(exp g) X + Y
+// The serial chain is [X | P] -> U -> Z -> S; a dedicated warp issues the
+// MMAs and TMA loads (three chunks in flight), and the outputs of a chunk are
+// formed and stored while the next chunk's first product runs.
+
 // All waits are bounded (kla_tc.cuh); a wait that gives up sets the status
 // word to a timeout code and the CTA leaves after releasing TMEM.
 
@@ -69,7 +68,7 @@ struct TcParams {
     float *eg_ws;              // [slots][64]        exp(g_t)
     __nv_bfloat16 *Kt_ws;      // [slots][64][128]   diag(exp(g_C - g)) K
     __nv_bfloat16 *W_ws;       // [slots][64][128]
-    __nv_bfloat16 *UT_ws;      // [slots][128][64]  U~ transposed (feature-major)
+    __nv_bfloat16 *U_ws;       // [slots][64][128]   U~
     __nv_bfloat16 *A_ws;       // [slots][64 keys s][64 queries t]  A^T
 };
 
@@ -148,17 +147,19 @@ __device__ __forceinline__ float *lslot(unsigned char *kq, int p) {
     return reinterpret_cast<float *>(kq + p * 32768 + 16384);
 }
 
+constexpr int P1_THREADS = 256;
+
 // One doubling step of the blocked inverse, in place in the fp32 L storage
 // of both chunks: for every diagonal block of size 2n whose two diagonal
 // n x n blocks already hold D1 = (I + L11)^{-1} and D2 = (I + L22)^{-1},
-// replace its lower-left block L21 by -D2 L21 D1.  128 threads; each computes
-// an (n/8) x 4 patch of the n x n products.
+// replace its lower-left block L21 by -D2 L21 D1.  All P1_THREADS threads;
+// each computes a (rows x 4) patch of the n x n products.
 template <int n>
 __device__ __forceinline__ void merge_level(unsigned char *kq, int tid) {
     constexpr int nblk = 64 / (2 * n);               // blocks of size 2n per chunk
-    constexpr int tpb = 128 / (2 * nblk);            // threads per block (both chunks)
+    constexpr int tpb = P1_THREADS / (2 * nblk);     // threads per block (both chunks)
     constexpr int rows = n * n / 4 / tpb;            // patch rows per thread (4 columns each)
-    static_assert(rows * 4 * tpb == n * n, "patch tiling");
+    static_assert(rows >= 1 && rows * 4 * tpb == n * n, "patch tiling");
     const int blkid = tid / tpb, q = tid % tpb;
     const int p = blkid / nblk, o = 2 * n * (blkid % nblk);
     constexpr int pcols = n / 4;                     // column patches per row band
@@ -233,7 +234,10 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, int tid) {
 }
 
 // ===================================================================== phase 1
-constexpr int P1_THREADS = 128;
+// Two threads per token row r of the item (r = tid % 128, the TMEM lane its
+// warp reads): thread half hf = tid / 128 takes one of two column halves of
+// every per-row task (64-feature slab hf of K and V; the L rows or the A^T
+// rows; 32 of the 64 columns of T diag beta; the W rows or the U~ rows).
 constexpr uint32_t P1_SMEM = 3 * 32768 + 1024;  // K, V, Q/L/A regions + alignment slack
 
 __global__ void __launch_bounds__(P1_THREADS, 2)
@@ -242,7 +246,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     extern __shared__ unsigned char smraw[];
     __shared__ uint64_t bars[3];
     __shared__ uint32_t tslot;
-    __shared__ float sG[128], sBeta[128], sCarry[4];
+    __shared__ float sG[128], sBeta[128], sN2[128], sCarry[4];
     __shared__ int sAbort;
 
     unsigned char *sm = align1024(smraw);
@@ -281,9 +285,10 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     int tid = tid0;
     asm volatile("" : "+r"(tid));
     const int warp = tid >> 5, lane = tid & 31;
-    const int slot = tid >> 6, t = tid & 63;
+    const int r = tid & 127, hf = tid >> 7;      // token row of the item, column half
+    const int slot = r >> 6, t = r & 63;
     const uint32_t tb = tslot;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const long pair = item / p.H;
     const int h = (int)(item % p.H);
     int seq0, seq1, nc0, nc1;
@@ -309,23 +314,30 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             }
     }
 
-    // ---- decay: g = inclusive prefix sum of log alpha within each chunk ----
-    float a = 1.f, et = 0.f;
-    if (t < nc) {
-        const size_t row = (size_t)((slot ? r01 : r00) + t) * p.H + h;
-        a = p.alpha[row];
-        et = p.eta[row];
-    }
-    double gs = (double)logf(a);
+    // ---- decay: g = inclusive prefix sum of log alpha within each chunk
+    //      (first thread half; the second half has no per-row gate work) ----
+    float et = 0.f;
+    double gs = 0.0;
+    if (hf == 0) {
+        float a = 1.f;
+        if (t < nc) {
+            const size_t row = (size_t)((slot ? r01 : r00) + t) * p.H + h;
+            a = p.alpha[row];
+            et = p.eta[row];
+        }
+        gs = (double)logf(a);
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const double u = __shfl_up_sync(0xffffffffu, gs, off);
-        if (lane >= off) gs += u;
+        for (int off = 1; off < 32; off <<= 1) {
+            const double u = __shfl_up_sync(0xffffffffu, gs, off);
+            if (lane >= off) gs += u;
+        }
+        if (lane == 31) sCarry[warp] = (float)gs;
     }
-    if (lane == 31) sCarry[warp] = (float)gs;
     __syncthreads();
-    if (warp & 1) gs += (double)sCarry[warp - 1];
-    sG[tid] = (float)gs;
+    if (hf == 0) {
+        if (warp & 1) gs += (double)sCarry[warp - 1];
+        sG[r] = (float)gs;
+    }
 
     // ---- tiles landed: Gram products on the tensor cores ----
     if (!mbar_wait(&bars[0], ph)) {
@@ -348,165 +360,177 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         mma_commit(&bars[1]);
     }
 
-    // ---- beta_t from the key's squared norm (fp32 over the bf16 values) ----
-    {
-        float n2 = 0.f;
+    // ---- beta_t from the key's squared norm (fp32 over the bf16 values);
+    //      each thread half sums one 64-feature slab ----
+    float n2 = 0.f;
 #pragma unroll
-        for (int s = 0; s < 2; ++s)
+    for (int ch = 0; ch < 8; ++ch) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(KQ + hf * 32768 + sw128_offset(r, ch * 8));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(KQ + s * 32768 +
-                                                                sw128_offset(tid, ch * 8));
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float x0 = bf_lo(w[i]), x1 = bf_hi(w[i]);
-                    n2 = fmaf(x0, x0, n2);
-                    n2 = fmaf(x1, x1, n2);
-                }
-            }
-        const float den = n2 + p.eps;
-        sBeta[tid] = (t < nc && den != 0.f) ? et / den : 0.f;
+        for (int i = 0; i < 4; ++i) {
+            const float x0 = bf_lo(w[i]), x1 = bf_hi(w[i]);
+            n2 = fmaf(x0, x0, n2);
+            n2 = fmaf(x1, x1, n2);
+        }
     }
+    if (hf) sN2[r] = n2;
     __syncthreads();
+    float bt = 0.f;
+    if (hf == 0) {
+        const float den = (n2 + sN2[r]) + p.eps;
+        bt = (t < nc && den != 0.f) ? et / den : 0.f;
+        sBeta[r] = bt;
+    }
 
     // ---- epilogue 1: L = strict_lower(beta Gamma o KK^T) (fp32 smem) from row t of
-    //      K K^T; row s of (K Q^T) gives row s of A^T, A = lower(Gamma o QK^T) ----
+    //      K K^T (first half); row s of (K Q^T) gives row s of A^T, A = lower(Gamma o
+    //      QK^T) (second half) ----
     bool ok = !abort1 && mbar_wait(&bars[1], ph);
     if (!abort1 && !ok) set_status(p.status, kDevTimeout);
     tc_fence_after();
-    const float gt = sG[tid];
-    const float bt = sBeta[tid];
+    const float gt = sG[r];
     const int cb = slot * 64;
     const long gidx0 = 2L * pair + slot;
     const size_t slot_row = (size_t)(gidx0 * p.H + h) * C + t;   // row of this token in the ws
     if (ok) {
-        float *Lrow = lslot(KQ, slot) + t * 64;
+        if (hf == 0) {
+            float *Lrow = lslot(KQ, slot) + t * 64;
 #pragma unroll 1
-        for (int g16 = 0; g16 < 4; ++g16) {
-            uint32_t r[16];
-            tmem_ld16(tb + lane_base + cb + g16 * 16, r);
-            tmem_ld_wait();
+            for (int g16 = 0; g16 < 4; ++g16) {
+                uint32_t rr[16];
+                tmem_ld16(tb + lane_base + cb + g16 * 16, rr);
+                tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-                float v4[4];
+                for (int i = 0; i < 16; i += 4) {
+                    float v4[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int s = g16 * 16 + i + e;
-                    v4[e] = (s < t && t < nc) ? bt * __expf(gt - sG[cb + s]) * __uint_as_float(r[i + e])
-                                              : 0.f;
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = g16 * 16 + i + e;
+                        v4[e] = (s < t && t < nc)
+                                    ? bt * __expf(gt - sG[cb + s]) * __uint_as_float(rr[i + e])
+                                    : 0.f;
+                    }
+                    *reinterpret_cast<float4 *>(Lrow + lsw(t, g16 * 16 + i)) =
+                        make_float4(v4[0], v4[1], v4[2], v4[3]);
                 }
-                *reinterpret_cast<float4 *>(Lrow + lsw(t, g16 * 16 + i)) =
-                    make_float4(v4[0], v4[1], v4[2], v4[3]);
             }
-        }
+        } else {
 #pragma unroll 1
-        for (int g16 = 0; g16 < 4; ++g16) {
-            uint32_t r[16];
-            tmem_ld16(tb + lane_base + 128 + cb + g16 * 16, r);
-            tmem_ld_wait();
-            // this thread's token is the key s = t; the columns are queries u
-            uint32_t pk[8];
+            for (int g16 = 0; g16 < 4; ++g16) {
+                uint32_t rr[16];
+                tmem_ld16(tb + lane_base + 128 + cb + g16 * 16, rr);
+                tmem_ld_wait();
+                // this thread's token is the key s = t; the columns are queries u
+                uint32_t pk[8];
 #pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-                const int u = g16 * 16 + i;
-                const float a0 = (t <= u && u < nc)
-                                     ? __expf(sG[cb + u] - gt) * __uint_as_float(r[i]) : 0.f;
-                const float a1 = (t <= u + 1 && u + 1 < nc)
-                                     ? __expf(sG[cb + u + 1] - gt) * __uint_as_float(r[i + 1]) : 0.f;
-                pk[i / 2] = pack_bf2(a0, a1);
-            }
-            if (vslot) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.A_ws + slot_row * 64 + g16 * 16);
-                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                for (int i = 0; i < 16; i += 2) {
+                    const int u = g16 * 16 + i;
+                    const float a0 = (t <= u && u < nc)
+                                         ? __expf(sG[cb + u] - gt) * __uint_as_float(rr[i]) : 0.f;
+                    const float a1 = (t <= u + 1 && u + 1 < nc)
+                                         ? __expf(sG[cb + u + 1] - gt) * __uint_as_float(rr[i + 1])
+                                         : 0.f;
+                    pk[i / 2] = pack_bf2(a0, a1);
+                }
+                if (vslot) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.A_ws + slot_row * 64 + g16 * 16);
+                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
             }
         }
-        // K row -> diag(exp g) K; rows past the chunk's end (another
+        // K row (slab hf) -> diag(exp g) K; rows past the chunk's end (another
         // sequence's tokens or TMA zero fill) are cleared in K and V so that
         // nothing from them can reach the products.
         // The state pass needs diag(exp(g_C - g)) K; it goes to the workspace.
         const float gam_t = __expf(gt);
         const float gam_c = __expf(sG[cb + C - 1] - gt);
         const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-        uint4 *kt_row = reinterpret_cast<uint4 *>(p.Kt_ws + slot_row * D);
-#pragma unroll 1
-        for (int s = 0; s < 2; ++s)
+        uint4 *kt_row = reinterpret_cast<uint4 *>(p.Kt_ws + slot_row * D) + hf * 8;
 #pragma unroll 2
-            for (int ch = 0; ch < 8; ++ch) {
-                uint4 *pk4 = reinterpret_cast<uint4 *>(KQ + s * 32768 + sw128_offset(tid, ch * 8));
-                if (t < nc) {
-                    const uint4 v = *pk4;
-                    *pk4 = make_uint4(pack_bf2(gam_t * bf_lo(v.x), gam_t * bf_hi(v.x)),
-                                      pack_bf2(gam_t * bf_lo(v.y), gam_t * bf_hi(v.y)),
-                                      pack_bf2(gam_t * bf_lo(v.z), gam_t * bf_hi(v.z)),
-                                      pack_bf2(gam_t * bf_lo(v.w), gam_t * bf_hi(v.w)));
-                    if (vslot)
-                        kt_row[s * 8 + ch] = make_uint4(pack_bf2(gam_c * bf_lo(v.x), gam_c * bf_hi(v.x)),
-                                                        pack_bf2(gam_c * bf_lo(v.y), gam_c * bf_hi(v.y)),
-                                                        pack_bf2(gam_c * bf_lo(v.z), gam_c * bf_hi(v.z)),
-                                                        pack_bf2(gam_c * bf_lo(v.w), gam_c * bf_hi(v.w)));
-                } else {
-                    if (vslot) kt_row[s * 8 + ch] = zero4;
-                    *pk4 = zero4;
-                    *reinterpret_cast<uint4 *>(sV + s * 16384 + sw128_offset(tid, ch * 8)) = zero4;
-                }
+        for (int ch = 0; ch < 8; ++ch) {
+            uint4 *pk4 = reinterpret_cast<uint4 *>(KQ + hf * 32768 + sw128_offset(r, ch * 8));
+            if (t < nc) {
+                const uint4 v = *pk4;
+                *pk4 = make_uint4(pack_bf2(gam_t * bf_lo(v.x), gam_t * bf_hi(v.x)),
+                                  pack_bf2(gam_t * bf_lo(v.y), gam_t * bf_hi(v.y)),
+                                  pack_bf2(gam_t * bf_lo(v.z), gam_t * bf_hi(v.z)),
+                                  pack_bf2(gam_t * bf_lo(v.w), gam_t * bf_hi(v.w)));
+                if (vslot)
+                    kt_row[ch] = make_uint4(pack_bf2(gam_c * bf_lo(v.x), gam_c * bf_hi(v.x)),
+                                            pack_bf2(gam_c * bf_lo(v.y), gam_c * bf_hi(v.y)),
+                                            pack_bf2(gam_c * bf_lo(v.z), gam_c * bf_hi(v.z)),
+                                            pack_bf2(gam_c * bf_lo(v.w), gam_c * bf_hi(v.w)));
+            } else {
+                if (vslot) kt_row[ch] = zero4;
+                *pk4 = zero4;
+                *reinterpret_cast<uint4 *>(sV + hf * 16384 + sw128_offset(r, ch * 8)) = zero4;
             }
+        }
     }
     if (!ok) sAbort = 1;
     __syncthreads();
     const bool abort2 = sAbort != 0;
 
     // ---- T = (I + L)^{-1}, built up in block sizes 16 -> 32 -> 64: the
-    //      diagonal 16 x 16 blocks by forward substitution, then at each level
-    //      [[D1, 0], [X, D2]] with X = -D2 L21 D1 from two small products ----
+    //      diagonal 16 x 16 blocks by forward substitution (first half of the
+    //      threads), then at each level [[D1, 0], [X, D2]] with X = -D2 L21 D1
+    //      from two small products (all threads) ----
     {
         // diagonal 16 x 16 blocks: 16 threads per block, one column each
-        const int p = tid >> 6, blk = (tid >> 4) & 3, c = tid & 15, o = 16 * blk;
-        float *Lb = lslot(KQ, p) + o * 64;
+        const int pp = (tid >> 6) & 1, blk = (tid >> 4) & 3, c = tid & 15, o = 16 * blk;
+        float *Lb = lslot(KQ, pp) + o * 64;
         float x[16];
+        if (hf == 0) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const float *Lr = Lb + r * 64;
-            float a0 = (r == c) ? 1.f : 0.f, a1 = 0.f;
+            for (int rw = 0; rw < 16; ++rw) {
+                const float *Lr = Lb + rw * 64;
+                float a0 = (rw == c) ? 1.f : 0.f, a1 = 0.f;
 #pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4) {
-                if (4 * s4 < r) {
-                    const float4 l = *reinterpret_cast<const float4 *>(Lr + lsw(o + r, o + 4 * s4));
-                    a0 = fmaf(-l.x, x[4 * s4], a0);
-                    if (4 * s4 + 1 < r) a1 = fmaf(-l.y, x[4 * s4 + 1], a1);
-                    if (4 * s4 + 2 < r) a0 = fmaf(-l.z, x[4 * s4 + 2], a0);
-                    if (4 * s4 + 3 < r) a1 = fmaf(-l.w, x[4 * s4 + 3], a1);
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    if (4 * s4 < rw) {
+                        const float4 l = *reinterpret_cast<const float4 *>(Lr + lsw(o + rw, o + 4 * s4));
+                        a0 = fmaf(-l.x, x[4 * s4], a0);
+                        if (4 * s4 + 1 < rw) a1 = fmaf(-l.y, x[4 * s4 + 1], a1);
+                        if (4 * s4 + 2 < rw) a0 = fmaf(-l.z, x[4 * s4 + 2], a0);
+                        if (4 * s4 + 3 < rw) a1 = fmaf(-l.w, x[4 * s4 + 3], a1);
+                    }
                 }
+                x[rw] = a0 + a1;
             }
-            x[r] = a0 + a1;
         }
         __syncthreads();  // the diagonal blocks of L have been read
+        if (hf == 0) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Lb[r * 64 + lsw(o + r, o + c)] = x[r];
+            for (int rw = 0; rw < 16; ++rw) Lb[rw * 64 + lsw(o + rw, o + c)] = x[rw];
+        }
         __syncthreads();
     }
     merge_level<16>(KQ, tid);   // 32 x 32 diagonal blocks
     merge_level<32>(KQ, tid);   // the whole 64 x 64 inverse
 
-    // ---- A operand = T diag(beta) in bf16, block diagonal over the two chunks ----
+    // ---- A operand = T diag(beta) in bf16, block diagonal over the two chunks;
+    //      thread half hf converts columns [32 hf, 32 hf + 32) of row t ----
     {
         const float *Trow = lslot(KQ, slot) + t * 64;
-        uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float4 v = *reinterpret_cast<const float4 *>(Trow + lsw(t, 4 * i));
-            const float *bs = sBeta + slot * 64 + 4 * i;
+        for (int i = 0; i < 8; ++i) {
+            const int c4 = 8 * hf + i;
+            const float4 v = *reinterpret_cast<const float4 *>(Trow + lsw(t, 4 * c4));
+            const float *bs = sBeta + slot * 64 + 4 * c4;
             pk[2 * i] = pack_bf2(v.x * bs[0], v.y * bs[1]);
             pk[2 * i + 1] = pack_bf2(v.z * bs[2], v.w * bs[3]);
         }
         __syncthreads();  // T fully read; its region becomes the bf16 A tile
         unsigned char *own = KQ + slot * 32768 + 16384, *other = KQ + (1 - slot) * 32768 + 16384;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            *reinterpret_cast<uint4 *>(own + sw128_offset(tid, ch * 8)) =
+        for (int ch = 0; ch < 4; ++ch) {
+            const int cc = 4 * hf + ch;
+            *reinterpret_cast<uint4 *>(own + sw128_offset(r, cc * 8)) =
                 make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            *reinterpret_cast<uint4 *>(other + sw128_offset(tid, ch * 8)) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(other + sw128_offset(r, cc * 8)) = make_uint4(0u, 0u, 0u, 0u);
         }
     }
     fence_async_smem();
@@ -523,46 +547,30 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         for (int ks = 0; ks < 8; ++ks)
             mma_bf16(tb + 0, sdesc_sw128(aA + (ks >> 2) * 32768 + (ks & 3) * 32, 16, 1024),
                      sdesc_sw128(aK + ks * 2048, 32768, 1024), id_w, ks > 0);
-        // U~^T = V^T (T diag beta)^T: M = 128 features (A = V, MN-major), N = 128
-        // tokens (B = the same T diag beta tile, K-major), K = 128 tokens.
-        const uint32_t id_u = idesc_bf16_f32(128, 128, true, false);
+        // U~ = (T diag beta) V: the same A; B = V MN-major, n-blocks 16 KB apart.
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-            mma_bf16(tb + 128, sdesc_sw128(aV + ks * 2048, 16384, 1024),
-                     sdesc_sw128(aA + (ks >> 2) * 32768 + (ks & 3) * 32, 16, 1024), id_u, ks > 0);
+            mma_bf16(tb + 128, sdesc_sw128(aA + (ks >> 2) * 32768 + (ks & 3) * 32, 16, 1024),
+                     sdesc_sw128(aV + ks * 2048, 16384, 1024), id_w, ks > 0);
         mma_commit(&bars[2]);
     }
     __syncthreads();
 
-    // ---- epilogue 2: W rows, U~^T rows (bf16) and g to the workspace ----
+    // ---- epilogue 2: W rows (first half) and U~ rows (second half) of token
+    //      row r, and exp(g), to the workspace ----
     ok = !abort2 && mbar_wait(&bars[2], ph);
     if (!abort2 && !ok) set_status(p.status, kDevTimeout);
     tc_fence_after();
-    if (ok) {
-        if (vslot) {
-            __nv_bfloat16 *dst_row = p.W_ws + slot_row * D;
+    if (ok && vslot) {
+        __nv_bfloat16 *dst_row = (hf ? p.U_ws : p.W_ws) + slot_row * D;
 #pragma unroll 1
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t r[32];
-                tmem_ld32(tb + lane_base + c4 * 32, r);
-                tmem_ld_wait();
-                store_bf16x32(dst_row + c4 * 32, r);
-            }
-            p.eg_ws[slot_row] = __expf(gt);
-        }
-        // lane j of U~^T holds feature j for the tokens of both chunks
-#pragma unroll 1
-        for (int q = 0; q < 2; ++q) {
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tb + lane_base + 128 + q * 64, r0);
-            tmem_ld32(tb + lane_base + 128 + q * 64 + 32, r1);
+        for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t rr[32];
+            tmem_ld32(tb + lane_base + 128 * hf + c4 * 32, rr);
             tmem_ld_wait();
-            if (q ? v1 : v0) {
-                __nv_bfloat16 *dst = p.UT_ws + ((size_t)((2L * pair + q) * p.H + h) * D + tid) * C;
-                store_bf16x32(dst, r0);
-                store_bf16x32(dst + 32, r1);
-            }
+            store_bf16x32(dst_row + c4 * 32, rr);
         }
+        if (hf == 0) p.eg_ws[slot_row] = __expf(gt);
     }
     tc_fence_before();
     __syncthreads();   // smem and TMEM free for the next item
@@ -573,62 +581,68 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 }
 
 // ===================================================================== phase 2
-// Warp roles:
-//   warps 0-7 ("main"): the serial chain and the outputs; thread (j, half)
-//             owns dv index j (its TMEM lane) and tokens [32*half, +32) /
-//             state rows [64*half, +64).
-//   warp 8    ("issuer"): issues every MMA and TMA load from lane 0; the warp
-//             waits on its barriers converged.
-// Per chunk the tensor core runs two wide products:
-//   [P^T | X^T] = S^T [W ; Q]^T                                M=128, N=128, K=128
-//   [Z^T | Y^T] = U^T [diag(exp(g_C - g)) K | A^T]             M=128, N=192, K=64
-// with U^T = U~^T - P^T, S^T <- exp(g_C) S^T + Z^T and
-// O^T = X^T diag(exp g) + Y^T.  diag(exp(g_C - g)) K and exp(g) come from
-// phase 1.  The bf16 A operands S^T and U^T live in tensor memory, which
-// leaves shared memory for three chunk stages in flight.
+// One CTA per (sequence, head, half of dv): the columns of S evolve
+// independently (S_t = S~ + beta_t k_t e_t^T with e_t = v_t - S~^T k_t acts
+// column by column), so the two 64-column halves of a head's state run on two
+// SMs side by side.  Per chunk, with S_b = S[:, j0 : j0 + 64] (dk x 64):
+//   [X | P] = [Q ; W] S_b                           M=128, N=64, K=128 (dk)
+//   U = U~_b - P  (bf16 -> shared memory)
+//   Z = K~^T U,  Y = A U                             M=128, N=64, K=64 (tokens)
+//   S_b <- exp(g_C) S_b + Z ;  O_b = diag(exp g) X + Y
+// where K~ = diag(exp(g_C - g)) K, A = lower(Gamma o Q K^T), and W, U~, K~,
+// A^T and exp(g) come from phase 1.  The serial chain per chunk is one
+// 8-step MMA, the U update, one 4-step MMA and the S update.
+//
+// Warp roles: warps 0-7 ("main") own TMEM lane L = 32 (warp % 4) + lane
+// (= dk row L of S_b, = token L of X / Y for L < 64, = token L - 64 of P for
+// L >= 64) and the 32 columns [32 hf, 32 hf + 32) of the tile, hf = warp / 4;
+// warp 8 issues every MMA and TMA load from lane 0 and waits converged.
 constexpr int P2_MAIN = 256, P2_THREADS = P2_MAIN + 32;
 constexpr int NSTAGE = 3;
+constexpr int DVB = 64;   // dv columns per CTA
 // Stage layout (one chunk):
-//   WQ: two 64-feature slabs of 16 KB, each [W rows 0..63 | Q rows 0..63]
-//   KA: K~ slab 0, K~ slab 1, A^T (8 KB each): MN-major n-blocks 8 KB apart
-//   U:  U~^T [128][64];  EG: exp(g) [64]
-constexpr uint32_t ST_WQ = 0, ST_KA = 32768, ST_A = 49152, ST_U = 57344, ST_EG = 73728,
-                   ST_BYTES = 74752;
-constexpr uint32_t ST_TX = 16384u * 4u + 8192u + 256u;  // bytes a stage receives
-constexpr uint32_t P2_SMEM = NSTAGE * ST_BYTES + 1024;
+//   QW: two 64-feature slabs of 16 KB, each [Q rows 0..63 | W rows 0..63]
+//   KT: K~ slab 0, K~ slab 1 (8 KB each)
+//   A:  A^T [64 keys][64 queries];  U: U~[:, j0 : j0 + 64] [64 tokens][64]
+//   EG: exp(g) [64]
+constexpr uint32_t ST_QW = 0, ST_KT = 32768, ST_A = 49152, ST_U = 57344, ST_EG = 65536,
+                   ST_BYTES = 66560;
+constexpr uint32_t ST_TX = 32768u + 16384u + 8192u + 8192u + 256u;  // bytes a stage receives
+// After the stages: the bf16 MMA operands S_b [128 dk rows][64] and U [64
+// tokens][64] (MN-major, 128-byte swizzle).
+constexpr uint32_t SM_S = NSTAGE * ST_BYTES, SM_U = SM_S + 16384;
+constexpr uint32_t P2_SMEM = SM_U + 8192 + 1024;
 
-// TMEM columns (M = 128 lanes = dv): fp32 [P^T | X^T] 0..127; fp32
-// [Z^T | Y^T] 128..319; bf16 S^T (128 packed as 64) 320..383; bf16 U^T (64
-// packed as 32) 384..415.
-constexpr uint32_t TM_PX = 0, TM_ZY = 128, TM_S = 320, TM_U = 384;
+// TMEM columns (fp32 accumulators, 128 lanes): [X | P] in two buffers, Z, and
+// Y in two buffers (chunk c uses buffer c % 2).
+constexpr uint32_t TM_PX = 0, TM_Z = 128, TM_Y = 192;
 
 __device__ __forceinline__ void issue_stage(unsigned char *st, uint64_t *bar,
                                             const CUtensorMap *mq, const CUtensorMap *mkt,
                                             const CUtensorMap *mw, const CUtensorMap *mu,
                                             const CUtensorMap *ma, const float *eg_src, int h,
-                                            int row0, int slot) {
+                                            int row0, int slot, int j0) {
     mbar_expect_tx(bar, ST_TX);
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
-        tma_load_2d(st + ST_WQ + s * 16384, mw, bar, 64 * s, slot * C);
-        tma_load_3d(st + ST_WQ + s * 16384 + 8192, mq, bar, 64 * s, h, row0);
-        tma_load_2d(st + ST_KA + s * 8192, mkt, bar, 64 * s, slot * C);
+        tma_load_3d(st + ST_QW + s * 16384, mq, bar, 64 * s, h, row0);
+        tma_load_2d(st + ST_QW + s * 16384 + 8192, mw, bar, 64 * s, slot * C);
+        tma_load_2d(st + ST_KT + s * 8192, mkt, bar, 64 * s, slot * C);
     }
     tma_load_2d(st + ST_A, ma, bar, 0, slot * C);
-    tma_load_2d(st + ST_U, mu, bar, 0, slot * D);
+    tma_load_2d(st + ST_U, mu, bar, j0, slot * C);
     bulk_load(st + ST_EG, eg_src, 256, bar);
 }
 
-// Main warps: bf16 copy of the 64 state values S[64*half + i][j] into the
-// TMEM operand S^T (row j, packed columns 32*half ..).
-__device__ __forceinline__ void store_state_bf16(uint32_t taddr, const float (&Sr)[64]) {
+// 32 fp32 values -> 32 bf16 at columns [c0, c0 + 32) of row `row` of a
+// 128-byte-swizzled tile.
+__device__ __forceinline__ void st_row_bf16x32(unsigned char *tile, int row, int c0,
+                                               const float (&x)[32]) {
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf2(Sr[32 * hh + 2 * i], Sr[32 * hh + 2 * i + 1]);
-        tmem_st16(taddr + 16 * hh, pk);
-    }
+    for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<uint4 *>(tile + sw128_offset(row, c0 + 8 * k)) =
+            make_uint4(pack_bf2(x[8 * k + 0], x[8 * k + 1]), pack_bf2(x[8 * k + 2], x[8 * k + 3]),
+                       pack_bf2(x[8 * k + 4], x[8 * k + 5]), pack_bf2(x[8 * k + 6], x[8 * k + 7]));
 }
 
 __global__ void __launch_bounds__(P2_THREADS, 1)
@@ -637,20 +651,23 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
              const __grid_constant__ CUtensorMap ma, const TcParams p) {
     extern __shared__ unsigned char smraw[];
     __shared__ uint64_t bar_ld[NSTAGE];
-    __shared__ uint64_t bar_p, bar_u, bar_zy, bar_sready;
+    __shared__ uint64_t bar_px, bar_u, bar_z, bar_s, bar_fin;
+    __shared__ uint64_t bar_y[2];   // Y of chunk c completes on bar_y[c % 2]
     __shared__ uint32_t tslot;
     __shared__ int sAbort;
 
     unsigned char *sm = align1024(smraw);
+    unsigned char *sS = sm + SM_S, *sU = sm + SM_U;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3;
-    const int half = (warp >> 2) & 1;           // main warps only
-    const int j = quarter * 32 + lane;          // dv index = TMEM lane of this thread
-    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const int L = (warp & 3) * 32 + lane;       // TMEM lane (main warps)
+    const int hf = (warp >> 2) & 1;             // column half (main warps)
+    const int c0 = 32 * hf;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     if (status_bad(p.status)) return;
-    const int rank = blockIdx.x / p.H, h = blockIdx.x % p.H;
+    const int unit = blockIdx.x >> 1, jh = blockIdx.x & 1, j0 = DVB * jh;
+    const int rank = unit / p.H, h = unit % p.H;
     const int seq = p.order ? p.order[rank] : rank;
     long start, len, chunk0;
     if (p.cu_seqlens) {
@@ -667,10 +684,13 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
     if (tid == 0) {
         for (int i = 0; i < NSTAGE; ++i) mbar_init(&bar_ld[i], 1);
-        mbar_init(&bar_p, 1);
-        mbar_init(&bar_u, P2_MAIN);
-        mbar_init(&bar_zy, 1);
-        mbar_init(&bar_sready, P2_MAIN);
+        mbar_init(&bar_px, 1);
+        mbar_init(&bar_u, 4);      // one arrival per P warp (2, 3, 6, 7)
+        mbar_init(&bar_z, 1);
+        mbar_init(&bar_y[0], 1);
+        mbar_init(&bar_y[1], 1);
+        mbar_init(&bar_s, 8);      // one arrival per main warp
+        mbar_init(&bar_fin, 1);
         fence_mbar_init();
         sAbort = 0;
     }
@@ -682,19 +702,6 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     tc_fence_after();
     const uint32_t tb = tslot;
 
-    // fp32 master state (main warps): S[i][j] for i in [64*half, 64*half+64)
-    float Sr[64];
-    if (tid < P2_MAIN) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-            Sr[i] = p.S0 ? p.S0[sbase + (size_t)(64 * half + i) * D + j] : 0.f;
-        store_state_bf16(tb + lane_base + TM_S + 32 * half, Sr);
-        tmem_st_wait();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
     auto fail = [&]() {
         sAbort = 1;
         set_status(p.status, kDevTimeout);
@@ -702,138 +709,191 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
     if (warp == 8) {
         // ----------------------------------------------------------------- issuer
-        const uint32_t id_px = idesc_bf16_f32(128, 128, false, false);
-        const uint32_t id_zy = idesc_bf16_f32(128, 192, false, true);
+        const uint32_t id_px = idesc_bf16_f32(128, DVB, false, true);
+        const uint32_t id_zy = idesc_bf16_f32(128, DVB, true, true);
+        const uint32_t aS = smem_u32(sS), aU = smem_u32(sU);
+        int loads = 0;     // stage loads issued
         if (lane == 0) {
             for (int c = 0; c < NSTAGE && c < nch; ++c) {
                 const long slot = (chunk0 + c) * p.H + h;
                 issue_stage(sm + c * ST_BYTES, &bar_ld[c], &mq, &mkt, &mw, &mu, &ma,
-                            p.eg_ws + slot * C, h, (int)(start + (long)c * C), (int)slot);
+                            p.eg_ws + slot * C, h, (int)(start + (long)c * C), (int)slot, j0);
             }
         }
+        loads = nch < NSTAGE ? nch : NSTAGE;
         __syncwarp();
-        for (int c = 0; c < nch; ++c) {
+        int c = 0;
+        for (; c < nch; ++c) {
             const int b = c % NSTAGE;
             unsigned char *st = sm + b * ST_BYTES;
             const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NSTAGE) & 1);
-            bool ok = mbar_wait(&bar_ld[b], par_st);
-            if (ok && c >= 1) ok = mbar_wait(&bar_sready, par ^ 1u);  // chunk c-1 finished
+            // stage landed, and S_c written to shared memory by the main warps
+            const bool ok = mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_s, par);
             if (!__all_sync(0xffffffffu, ok)) { fail(); break; }
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t aWQ = smem_u32(st + ST_WQ);
+                const uint32_t aQW = smem_u32(st + ST_QW);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_ta(tb + TM_PX, tb + TM_S + 8 * ks,
-                                sdesc_sw128(aWQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                                id_px, ks > 0);
-                mma_commit(&bar_p);
+                    mma_bf16(tb + TM_PX + 64 * (c & 1),
+                             sdesc_sw128(aQW + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                             sdesc_sw128(aS + ks * 2048, 8192, 1024), id_px, ks > 0);
+                mma_commit(&bar_px);
             }
             __syncwarp();
+            // the previous chunk's products are done with its stage: refill it
+            if (c >= 1 && c - 1 + NSTAGE < nch) {
+                const int cp = c - 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_y[cp & 1], (uint32_t)((cp >> 1) & 1)))) {
+                    fail();
+                    break;
+                }
+                if (lane == 0) {
+                    const int cn = c - 1 + NSTAGE, bn = (c - 1) % NSTAGE;
+                    const long slot = (chunk0 + cn) * p.H + h;
+                    issue_stage(sm + bn * ST_BYTES, &bar_ld[bn], &mq, &mkt, &mw, &mu, &ma,
+                                p.eg_ws + slot * C, h, (int)(start + (long)cn * C), (int)slot, j0);
+                }
+                ++loads;
+                __syncwarp();
+            }
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_u, par))) { fail(); break; }
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t aKA = smem_u32(st + ST_KA);
+                const uint32_t aKT = smem_u32(st + ST_KT), aA = smem_u32(st + ST_A);
+                // Z = K~^T U: A = K~ read MN-major (M = dk, two 64-feature blocks)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ta(tb + TM_ZY, tb + TM_U + 8 * ks,
-                                sdesc_sw128(aKA + ks * 2048, 8192, 1024), id_zy, ks > 0);
-                mma_commit(&bar_zy);
+                    mma_bf16(tb + TM_Z, sdesc_sw128(aKT + ks * 2048, 8192, 1024),
+                             sdesc_sw128(aU + ks * 2048, 8192, 1024), id_zy, ks > 0);
+                mma_commit(&bar_z);
+                // Y = A U: A read MN-major from A^T; its second 64-row block
+                // (rows 64..127 of the product, never read) points at U~
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tb + TM_Y + 64 * (c & 1), sdesc_sw128(aA + ks * 2048, 8192, 1024),
+                             sdesc_sw128(aU + ks * 2048, 8192, 1024), id_zy, ks > 0);
+                mma_commit(&bar_y[c & 1]);
             }
             __syncwarp();
-            // both products have read this stage: refill it with chunk c + NSTAGE
-            if (c + NSTAGE < nch) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&bar_zy, par))) { fail(); break; }
-                if (lane == 0) {
-                    const long slot = (chunk0 + c + NSTAGE) * p.H + h;
-                    issue_stage(st, &bar_ld[b], &mq, &mkt, &mw, &mu, &ma, p.eg_ws + slot * C, h,
-                                (int)(start + (long)(c + NSTAGE) * C), (int)slot);
-                }
-                __syncwarp();
-            }
+        }
+        // every MMA issued has completed before the CTA releases its TMEM
+        if (lane == 0) mma_commit(&bar_fin);
+        __syncwarp();
+        (void)mbar_wait(&bar_fin, 0u);
+        // on an early exit, let the loads still in flight land before leaving
+        if (c < nch) {
+            for (int k = c; k < loads; ++k)
+                (void)mbar_wait(&bar_ld[k % NSTAGE], (uint32_t)((k / NSTAGE) & 1));
         }
     } else {
         // ----------------------------------------------------------------- main
         const size_t rs = (size_t)p.H * D;
+        float Sr[32];
+        {
+            const float4 *src = reinterpret_cast<const float4 *>(p.S0 + sbase + (size_t)L * D + j0 + c0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = p.S0 ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                Sr[4 * i] = v.x; Sr[4 * i + 1] = v.y; Sr[4 * i + 2] = v.z; Sr[4 * i + 3] = v.w;
+            }
+            st_row_bf16x32(sS, L, c0, Sr);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_s);
+        }
+        const bool pwarp = (warp & 2) != 0;    // lanes 64..127: P rows (tokens L - 64)
         for (int c = 0; c < nch; ++c) {
             const int b = c % NSTAGE;
             unsigned char *st = sm + b * ST_BYTES;
             const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NSTAGE) & 1);
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_p, par))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_px, par))) {
                 fail();
                 break;
             }
             tc_fence_after();
             const float *eg = reinterpret_cast<const float *>(st + ST_EG);
             const float egC = eg[C - 1];
-            // ---- U^T = U~^T - P^T for tokens [32*half, 32*half + 32) -> TMEM (bf16) ----
+            float egt = 0.f;
+            if (pwarp) {
+                // ---- U = U~_b - P for token t = L - 64, columns [c0, c0 + 32) ----
+                const int t = L - 64;
+                uint32_t r[32];
+                tmem_ld32(tb + lane_base + TM_PX + 64 * (c & 1) + c0, r);
+                tmem_ld_wait();
+                float u[32];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(st + ST_U + sw128_offset(t, c0 + 8 * k));
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        u[8 * k + 2 * e] = bf_lo(ww[e]) - __uint_as_float(r[8 * k + 2 * e]);
+                        u[8 * k + 2 * e + 1] = bf_hi(ww[e]) - __uint_as_float(r[8 * k + 2 * e + 1]);
+                    }
+                }
+                st_row_bf16x32(sU, t, c0, u);
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_u);
+            } else {
+                egt = eg[L];   // read now: the stage may be refilled once S_{c+1} is published
+            }
+
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_z, par))) { fail(); break; }
+            tc_fence_after();
+            // ---- S_b <- exp(g_C) S_b + Z (row L, columns [c0, c0 + 32)) ----
             {
                 uint32_t r[32];
-                tmem_ld32(tb + lane_base + TM_PX + half * 32, r);
+                tmem_ld32(tb + lane_base + TM_Z + c0, r);
                 tmem_ld_wait();
-                const unsigned char *sU = st + ST_U;
-                uint32_t pk[16];
 #pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(sU + sw128_offset(j, half * 32 + v4 * 8));
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        pk[4 * v4 + e] = pack_bf2(bf_lo(w[e]) - __uint_as_float(r[8 * v4 + 2 * e]),
-                                                  bf_hi(w[e]) - __uint_as_float(r[8 * v4 + 2 * e + 1]));
+                for (int i = 0; i < 32; ++i) Sr[i] = fmaf(egC, Sr[i], __uint_as_float(r[i]));
+            }
+            if (c + 1 < nch) {
+                st_row_bf16x32(sS, L, c0, Sr);
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_s);
+            }
+            // ---- O_b = diag(exp g) X + Y for token t = L (X rows), after S is published ----
+            if (!pwarp) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_y[c & 1], (uint32_t)((c >> 1) & 1)))) {
+                    fail();
+                    break;
                 }
-                tmem_st16(tb + lane_base + TM_U + 16 * half, pk);
-                tmem_st_wait();
-            }
-            tc_fence_before();
-            mbar_arrive(&bar_u);
-
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_zy, par))) { fail(); break; }
-            tc_fence_after();
-            // ---- S^T <- exp(g_C) S^T + Z^T ; new bf16 copy of S^T in TMEM ----
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                uint32_t r[32];
-                tmem_ld32(tb + lane_base + TM_ZY + half * 64 + c2 * 32, r);
+                tc_fence_after();
+                uint32_t xr[32], yr[32];
+                tmem_ld32(tb + lane_base + TM_PX + 64 * (c & 1) + c0, xr);
+                tmem_ld32(tb + lane_base + TM_Y + 64 * (c & 1) + c0, yr);
                 tmem_ld_wait();
+                tc_fence_before();
+                const int nc = (int)min((long)C, len - (long)c * C);
+                if (L < nc) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(start + (long)c * C + L) * rs +
+                                                           (size_t)h * D + j0 + c0);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    Sr[c2 * 32 + i] = fmaf(egC, Sr[c2 * 32 + i], __uint_as_float(r[i]));
-            }
-            store_state_bf16(tb + lane_base + TM_S + 32 * half, Sr);
-            // ---- O = diag(exp g) X + Y for this chunk's tokens, read before the next
-            //      product overwrites X^T, stored while that product runs ----
-            uint32_t opk[16];
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t w[4];
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t xr[16], yr[16];
-                tmem_ld16(tb + lane_base + TM_PX + 64 + half * 32 + 16 * q2, xr);
-                tmem_ld16(tb + lane_base + TM_ZY + 128 + half * 32 + 16 * q2, yr);
-                tmem_ld_wait();
-                const float *egt = eg + 32 * half + 16 * q2;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    opk[8 * q2 + i] =
-                        pack_bf2(fmaf(egt[2 * i], __uint_as_float(xr[2 * i]), __uint_as_float(yr[2 * i])),
-                                 fmaf(egt[2 * i + 1], __uint_as_float(xr[2 * i + 1]),
-                                      __uint_as_float(yr[2 * i + 1])));
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&bar_sready);
-            const int nc = (int)min((long)C, len - (long)c * C);
-            __nv_bfloat16 *dst = p.o + (size_t)(start + (long)c * C + 32 * half) * rs + (size_t)h * D + j;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int t = 32 * half + 2 * i;
-                if (t < nc) dst[(size_t)(2 * i) * rs] = __ushort_as_bfloat16((unsigned short)(opk[i] & 0xffffu));
-                if (t + 1 < nc)
-                    dst[(size_t)(2 * i + 1) * rs] = __ushort_as_bfloat16((unsigned short)(opk[i] >> 16));
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 8 * k + 2 * e;
+                            w[e] = pack_bf2(fmaf(egt, __uint_as_float(xr[i]), __uint_as_float(yr[i])),
+                                            fmaf(egt, __uint_as_float(xr[i + 1]),
+                                                 __uint_as_float(yr[i + 1])));
+                        }
+                        dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
             }
         }
         if (!sAbort && p.S_T) {
+            float4 *dst = reinterpret_cast<float4 *>(p.S_T + sbase + (size_t)L * D + j0 + c0);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) p.S_T[sbase + (size_t)(64 * half + i) * D + j] = Sr[i];
+            for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(Sr[4 * i], Sr[4 * i + 1], Sr[4 * i + 2], Sr[4 * i + 3]);
         }
     }
 
@@ -1006,7 +1066,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     tp.eg_ws = reinterpret_cast<float *>(ws + L.g);
     tp.Kt_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.Kt);
     tp.W_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.W);
-    tp.UT_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.U);
+    tp.U_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.U);
     tp.A_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.A);
     int *chunk_prefix = reinterpret_cast<int *>(ws + L.meta);
     int *order = chunk_prefix + p.n_seq + 1;
@@ -1017,7 +1077,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     const long slots = n_chunks_upper * p.H;
     if (!map_3d_rows(&mq, p.q, p.H, p.total_T) || !map_3d_rows(&mk, p.k, p.H, p.total_T) ||
         !map_3d_rows(&mv, p.v, p.H, p.total_T) || !map_2d(&mw, tp.W_ws, D, slots * C, C) ||
-        !map_2d(&mu, tp.UT_ws, C, slots * D, D) || !map_2d(&ma, tp.A_ws, C, slots * C, C) ||
+        !map_2d(&mu, tp.U_ws, D, slots * C, C) || !map_2d(&ma, tp.A_ws, C, slots * C, C) ||
         !map_2d(&mkt, tp.Kt_ws, D, slots * C, C))
         return cudaErrorInvalidValue;
 
@@ -1044,7 +1104,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     intra_kernel<<<(unsigned)grid1, P1_THREADS, P1_SMEM, s>>>(mq, mk, mv, tp, n_pairs);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    state_kernel<<<(unsigned)(p.n_seq * p.H), P2_THREADS, P2_SMEM, s>>>(mq, mkt, mw, mu, ma, tp);
+    state_kernel<<<(unsigned)(2L * p.n_seq * p.H), P2_THREADS, P2_SMEM, s>>>(mq, mkt, mw, mu, ma, tp);
     note_launch();
     return cudaGetLastError();
 }
