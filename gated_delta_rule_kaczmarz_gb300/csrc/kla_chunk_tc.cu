@@ -121,18 +121,6 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// Packs 32 fp32 values (as raw bits) to bf16 and stores them (64 bytes).
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t (&r)[32]) {
-    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-    for (int v4 = 0; v4 < 4; ++v4)
-        d4[v4] = make_uint4(
-            pack_bf2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1])),
-            pack_bf2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3])),
-            pack_bf2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5])),
-            pack_bf2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7])));
-}
-
 // fp32 64 x 64 matrices in shared memory, one per chunk, rows of 64 floats;
 // the float4 index within a row is XORed with (row % 16) so that a thread per
 // row writing float4s, and a warp reading one row as a broadcast, are both
@@ -242,7 +230,8 @@ constexpr uint32_t P1_SMEM = 3 * 32768 + 1024;  // K, V, Q/L/A regions + alignme
 
 __global__ void __launch_bounds__(P1_THREADS, 2)
 intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-             const __grid_constant__ CUtensorMap mv, const TcParams p, long n_pairs) {
+             const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mw,
+             const __grid_constant__ CUtensorMap mu, const TcParams p, long n_pairs) {
     extern __shared__ unsigned char smraw[];
     __shared__ uint64_t bars[3];
     __shared__ uint32_t tslot;
@@ -302,6 +291,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const bool vslot = slot ? v1 : v0;
 
     if (tid == 0) {
+        bulk_wait_group_read0();   // the previous item's W / U~ stores have left shared memory
         mbar_expect_tx(&bars[0], 3u * 32768u);
 #pragma unroll
         for (int q = 0; q < 2; ++q)
@@ -556,27 +546,53 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     }
     __syncthreads();
 
-    // ---- epilogue 2: W rows (first half) and U~ rows (second half) of token
-    //      row r, and exp(g), to the workspace ----
+    // ---- epilogue 2: W (first half) and U~ (second half) rows of token row r,
+    //      bf16, staged in the now free K and V regions with the 128-byte
+    //      swizzle of the tensor maps, then written by TMA stores; exp(g) ----
     ok = !abort2 && mbar_wait(&bars[2], ph);
     if (!abort2 && !ok) set_status(p.status, kDevTimeout);
     tc_fence_after();
-    if (ok && vslot) {
-        __nv_bfloat16 *dst_row = (hf ? p.U_ws : p.W_ws) + slot_row * D;
+    if (ok) {
+        unsigned char *stg = hf ? sV : KQ;
+        const uint32_t slab_stride = hf ? 16384u : 32768u;
 #pragma unroll 1
         for (int c4 = 0; c4 < 4; ++c4) {
             uint32_t rr[32];
             tmem_ld32(tb + lane_base + 128 * hf + c4 * 32, rr);
             tmem_ld_wait();
-            store_bf16x32(dst_row + c4 * 32, rr);
+            unsigned char *tile = stg + (c4 >> 1) * slab_stride;
+            const int col0 = (32 * c4) & 63;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint4 *>(tile + sw128_offset(r, col0 + 8 * k)) = make_uint4(
+                    pack_bf2(__uint_as_float(rr[8 * k + 0]), __uint_as_float(rr[8 * k + 1])),
+                    pack_bf2(__uint_as_float(rr[8 * k + 2]), __uint_as_float(rr[8 * k + 3])),
+                    pack_bf2(__uint_as_float(rr[8 * k + 4]), __uint_as_float(rr[8 * k + 5])),
+                    pack_bf2(__uint_as_float(rr[8 * k + 6]), __uint_as_float(rr[8 * k + 7])));
         }
-        if (hf == 0) p.eg_ws[slot_row] = __expf(gt);
+        if (hf == 0 && vslot) p.eg_ws[slot_row] = __expf(gt);
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0 && ok) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            if (!(q ? v1 : v0)) continue;
+            const int y = (int)(((2L * pair + q) * p.H + h) * C);
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                tma_store_2d(&mw, KQ + s * 32768 + q * 8192, 64 * s, y);
+                tma_store_2d(&mu, sV + s * 16384 + q * 8192, 64 * s, y);
+            }
+        }
+        bulk_commit_group();
     }
     tc_fence_before();
     __syncthreads();   // smem and TMEM free for the next item
     ph ^= 1u;
     if (sAbort) break;
     }  // items
+    if (tid0 == 0) bulk_wait_group0();   // every TMA store complete before the CTA leaves
     if ((tid0 >> 5) == 0) tmem_dealloc(tslot, 256);
 }
 
@@ -1101,7 +1117,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     const long n_pairs = (n_chunks_upper + 1) / 2;
     const long n_items = n_pairs * p.H;
     const long grid1 = n_items < 2L * sm_count() ? n_items : 2L * sm_count();
-    intra_kernel<<<(unsigned)grid1, P1_THREADS, P1_SMEM, s>>>(mq, mk, mv, tp, n_pairs);
+    intra_kernel<<<(unsigned)grid1, P1_THREADS, P1_SMEM, s>>>(mq, mk, mv, mw, mu, tp, n_pairs);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     state_kernel<<<(unsigned)(2L * p.n_seq * p.H), P2_THREADS, P2_SMEM, s>>>(mq, mkt, mw, mu, ma, tp);
