@@ -21,14 +21,13 @@
 // inverts I + L in fp32 on the CUDA cores (forward substitution on 16 x 16
 // diagonal blocks, then two doubling steps made of small products), and forms
 // W = (T diag beta)(diag(exp g) K) and U~ = (T diag beta) V with two MMAs.
-// W, U~, A^T and diag(exp(g_C - g)) K (bf16) and exp(g) (fp32) go to the
-// caller's workspace.
+// W, U~, A^T (bf16) and g (fp32) go to the caller's workspace.
 //
 // Phase 2 (state_kernel) walks the chunks of one (sequence, head) in order;
 // the two 64-column halves of the state run in two CTAs, since the columns
 // of S evolve independently.  Per chunk, with S_b the CTA's dk x 64 slice:
 //   [X | P] = [Q ; W] S_b ;  U = U~_b - P
-//   Z = K~^T U ;  Y = A U     (K~ = diag(exp(g_C - g)) K)
+//   Z = K^T (diag(exp(g_C - g)) U) ;  Y = A U
 //   S_b <- exp(g_C) S_b + Z (fp32 registers) ;  O_b = diag(exp g) X + Y
 // The serial chain is [X | P] -> U -> Z -> S; a dedicated warp issues the
 // MMAs and TMA loads (three chunks in flight), and the outputs of a chunk are
@@ -65,8 +64,7 @@ struct TcParams {
     const int *chunk_prefix;   // varlen only: first chunk of each sequence, [N+1]
     const int *order;          // varlen only: sequences by decreasing length, [N]
     unsigned *status;
-    float *eg_ws;              // [slots][64]        exp(g_t)
-    __nv_bfloat16 *Kt_ws;      // [slots][64][128]   diag(exp(g_C - g)) K
+    float *g_ws;               // [slots][64]        g_t (in-chunk cumulative log decay)
     __nv_bfloat16 *W_ws;       // [slots][64][128]
     __nv_bfloat16 *U_ws;       // [slots][64][128]   U~
     __nv_bfloat16 *A_ws;       // [slots][64 keys s][64 queries t]  A^T
@@ -430,14 +428,12 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 }
             }
         }
-        // K row (slab hf) -> diag(exp g) K; rows past the chunk's end (another
-        // sequence's tokens or TMA zero fill) are cleared in K and V so that
-        // nothing from them can reach the products.
-        // The state pass needs diag(exp(g_C - g)) K; it goes to the workspace.
+        // K row (slab hf) -> diag(exp g) K, in place for the W product; rows
+        // past the chunk's end (another sequence's tokens or TMA zero fill)
+        // are cleared in K and V so that nothing from them can reach the
+        // products.
         const float gam_t = __expf(gt);
-        const float gam_c = __expf(sG[cb + C - 1] - gt);
         const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-        uint4 *kt_row = reinterpret_cast<uint4 *>(p.Kt_ws + slot_row * D) + hf * 8;
 #pragma unroll 2
         for (int ch = 0; ch < 8; ++ch) {
             uint4 *pk4 = reinterpret_cast<uint4 *>(KQ + hf * 32768 + sw128_offset(r, ch * 8));
@@ -447,13 +443,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                                   pack_bf2(gam_t * bf_lo(v.y), gam_t * bf_hi(v.y)),
                                   pack_bf2(gam_t * bf_lo(v.z), gam_t * bf_hi(v.z)),
                                   pack_bf2(gam_t * bf_lo(v.w), gam_t * bf_hi(v.w)));
-                if (vslot)
-                    kt_row[ch] = make_uint4(pack_bf2(gam_c * bf_lo(v.x), gam_c * bf_hi(v.x)),
-                                            pack_bf2(gam_c * bf_lo(v.y), gam_c * bf_hi(v.y)),
-                                            pack_bf2(gam_c * bf_lo(v.z), gam_c * bf_hi(v.z)),
-                                            pack_bf2(gam_c * bf_lo(v.w), gam_c * bf_hi(v.w)));
             } else {
-                if (vslot) kt_row[ch] = zero4;
                 *pk4 = zero4;
                 *reinterpret_cast<uint4 *>(sV + hf * 16384 + sw128_offset(r, ch * 8)) = zero4;
             }
@@ -548,7 +538,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
     // ---- epilogue 2: W (first half) and U~ (second half) rows of token row r,
     //      bf16, staged in the now free K and V regions with the 128-byte
-    //      swizzle of the tensor maps, then written by TMA stores; exp(g) ----
+    //      swizzle of the tensor maps, then written by TMA stores; g ----
     ok = !abort2 && mbar_wait(&bars[2], ph);
     if (!abort2 && !ok) set_status(p.status, kDevTimeout);
     tc_fence_after();
@@ -570,7 +560,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                     pack_bf2(__uint_as_float(rr[8 * k + 4]), __uint_as_float(rr[8 * k + 5])),
                     pack_bf2(__uint_as_float(rr[8 * k + 6]), __uint_as_float(rr[8 * k + 7])));
         }
-        if (hf == 0 && vslot) p.eg_ws[slot_row] = __expf(gt);
+        if (hf == 0 && vslot) p.g_ws[slot_row] = gt;
     }
     fence_async_smem();
     __syncthreads();
@@ -602,12 +592,12 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 // column by column), so the two 64-column halves of a head's state run on two
 // SMs side by side.  Per chunk, with S_b = S[:, j0 : j0 + 64] (dk x 64):
 //   [X | P] = [Q ; W] S_b                           M=128, N=64, K=128 (dk)
-//   U = U~_b - P  (bf16 -> shared memory)
-//   Z = K~^T U,  Y = A U                             M=128, N=64, K=64 (tokens)
+//   U = U~_b - P,  U' = diag(exp(g_C - g)) U  (bf16 -> shared memory)
+//   Z = K^T U',  Y = A U                             M=128, N=64, K=64 (tokens)
 //   S_b <- exp(g_C) S_b + Z ;  O_b = diag(exp g) X + Y
-// where K~ = diag(exp(g_C - g)) K, A = lower(Gamma o Q K^T), and W, U~, K~,
-// A^T and exp(g) come from phase 1.  The serial chain per chunk is one
-// 8-step MMA, the U update, one 4-step MMA and the S update.
+// where A = lower(Gamma o Q K^T), and W, U~, A^T and g come from phase 1; Q
+// and K are read from the inputs.  The serial chain per chunk is one 8-step
+// MMA, the U update, one 4-step MMA and the S update.
 //
 // Warp roles: warps 0-7 ("main") own TMEM lane L = 32 (warp % 4) + lane
 // (= dk row L of S_b, = token L of X / Y for L < 64, = token L - 64 of P for
@@ -618,36 +608,36 @@ constexpr int NSTAGE = 3;
 constexpr int DVB = 64;   // dv columns per CTA
 // Stage layout (one chunk):
 //   QW: two 64-feature slabs of 16 KB, each [Q rows 0..63 | W rows 0..63]
-//   KT: K~ slab 0, K~ slab 1 (8 KB each)
+//   KT: K slab 0, K slab 1 (8 KB each)
 //   A:  A^T [64 keys][64 queries];  U: U~[:, j0 : j0 + 64] [64 tokens][64]
-//   EG: exp(g) [64]
-constexpr uint32_t ST_QW = 0, ST_KT = 32768, ST_A = 49152, ST_U = 57344, ST_EG = 65536,
-                   ST_BYTES = 66560;
+// and, in a separate small region, g [64] per stage.
+constexpr uint32_t ST_QW = 0, ST_KT = 32768, ST_A = 49152, ST_U = 57344, ST_BYTES = 65536;
 constexpr uint32_t ST_TX = 32768u + 16384u + 8192u + 8192u + 256u;  // bytes a stage receives
-// After the stages: the bf16 MMA operands S_b [128 dk rows][64] and U [64
-// tokens][64] (MN-major, 128-byte swizzle).
-constexpr uint32_t SM_S = NSTAGE * ST_BYTES, SM_U = SM_S + 16384;
-constexpr uint32_t P2_SMEM = SM_U + 8192 + 1024;
+// After the stages: the bf16 MMA operands S_b [128 dk rows][64], U and U'
+// [64 tokens][64] (MN-major, 128-byte swizzle), then g of each stage.
+constexpr uint32_t SM_S = NSTAGE * ST_BYTES, SM_U = SM_S + 16384, SM_UZ = SM_U + 8192,
+                   SM_G = SM_UZ + 8192;
+constexpr uint32_t P2_SMEM = SM_G + NSTAGE * 256 + 1024;
 
 // TMEM columns (fp32 accumulators, 128 lanes): [X | P] in two buffers, Z, and
 // Y in two buffers (chunk c uses buffer c % 2).
 constexpr uint32_t TM_PX = 0, TM_Z = 128, TM_Y = 192;
 
-__device__ __forceinline__ void issue_stage(unsigned char *st, uint64_t *bar,
-                                            const CUtensorMap *mq, const CUtensorMap *mkt,
+__device__ __forceinline__ void issue_stage(unsigned char *st, float *g_dst, uint64_t *bar,
+                                            const CUtensorMap *mq, const CUtensorMap *mk,
                                             const CUtensorMap *mw, const CUtensorMap *mu,
-                                            const CUtensorMap *ma, const float *eg_src, int h,
+                                            const CUtensorMap *ma, const float *g_src, int h,
                                             int row0, int slot, int j0) {
     mbar_expect_tx(bar, ST_TX);
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
         tma_load_3d(st + ST_QW + s * 16384, mq, bar, 64 * s, h, row0);
         tma_load_2d(st + ST_QW + s * 16384 + 8192, mw, bar, 64 * s, slot * C);
-        tma_load_2d(st + ST_KT + s * 8192, mkt, bar, 64 * s, slot * C);
+        tma_load_3d(st + ST_KT + s * 8192, mk, bar, 64 * s, h, row0);
     }
     tma_load_2d(st + ST_A, ma, bar, 0, slot * C);
     tma_load_2d(st + ST_U, mu, bar, j0, slot * C);
-    bulk_load(st + ST_EG, eg_src, 256, bar);
+    bulk_load(g_dst, g_src, 256, bar);
 }
 
 // 32 fp32 values -> 32 bf16 at columns [c0, c0 + 32) of row `row` of a
@@ -662,7 +652,7 @@ __device__ __forceinline__ void st_row_bf16x32(unsigned char *tile, int row, int
 }
 
 __global__ void __launch_bounds__(P2_THREADS, 1)
-state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mkt,
+state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
              const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
              const __grid_constant__ CUtensorMap ma, const TcParams p) {
     extern __shared__ unsigned char smraw[];
@@ -673,7 +663,8 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     __shared__ int sAbort;
 
     unsigned char *sm = align1024(smraw);
-    unsigned char *sS = sm + SM_S, *sU = sm + SM_U;
+    unsigned char *sS = sm + SM_S, *sU = sm + SM_U, *sUz = sm + SM_UZ;
+    float *sG = reinterpret_cast<float *>(sm + SM_G);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = (warp & 3) * 32 + lane;       // TMEM lane (main warps)
@@ -727,13 +718,13 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         // ----------------------------------------------------------------- issuer
         const uint32_t id_px = idesc_bf16_f32(128, DVB, false, true);
         const uint32_t id_zy = idesc_bf16_f32(128, DVB, true, true);
-        const uint32_t aS = smem_u32(sS), aU = smem_u32(sU);
+        const uint32_t aS = smem_u32(sS), aU = smem_u32(sU), aUz = smem_u32(sUz);
         int loads = 0;     // stage loads issued
         if (lane == 0) {
             for (int c = 0; c < NSTAGE && c < nch; ++c) {
                 const long slot = (chunk0 + c) * p.H + h;
-                issue_stage(sm + c * ST_BYTES, &bar_ld[c], &mq, &mkt, &mw, &mu, &ma,
-                            p.eg_ws + slot * C, h, (int)(start + (long)c * C), (int)slot, j0);
+                issue_stage(sm + c * ST_BYTES, sG + c * C, &bar_ld[c], &mq, &mk, &mw, &mu, &ma,
+                            p.g_ws + slot * C, h, (int)(start + (long)c * C), (int)slot, j0);
             }
         }
         loads = nch < NSTAGE ? nch : NSTAGE;
@@ -767,8 +758,9 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 if (lane == 0) {
                     const int cn = c - 1 + NSTAGE, bn = (c - 1) % NSTAGE;
                     const long slot = (chunk0 + cn) * p.H + h;
-                    issue_stage(sm + bn * ST_BYTES, &bar_ld[bn], &mq, &mkt, &mw, &mu, &ma,
-                                p.eg_ws + slot * C, h, (int)(start + (long)cn * C), (int)slot, j0);
+                    issue_stage(sm + bn * ST_BYTES, sG + bn * C, &bar_ld[bn], &mq, &mk, &mw, &mu,
+                                &ma, p.g_ws + slot * C, h, (int)(start + (long)cn * C), (int)slot,
+                                j0);
                 }
                 ++loads;
                 __syncwarp();
@@ -777,11 +769,11 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t aKT = smem_u32(st + ST_KT), aA = smem_u32(st + ST_A);
-                // Z = K~^T U: A = K~ read MN-major (M = dk, two 64-feature blocks)
+                // Z = K^T U': A = K read MN-major (M = dk, two 64-feature blocks)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16(tb + TM_Z, sdesc_sw128(aKT + ks * 2048, 8192, 1024),
-                             sdesc_sw128(aU + ks * 2048, 8192, 1024), id_zy, ks > 0);
+                             sdesc_sw128(aUz + ks * 2048, 8192, 1024), id_zy, ks > 0);
                 mma_commit(&bar_z);
                 // Y = A U: A read MN-major from A^T; its second 64-row block
                 // (rows 64..127 of the product, never read) points at U~
@@ -828,16 +820,20 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 break;
             }
             tc_fence_after();
-            const float *eg = reinterpret_cast<const float *>(st + ST_EG);
-            const float egC = eg[C - 1];
+            const float *g = sG + b * C;
+            const float gC = g[C - 1];
+            const float egC = __expf(gC);
+            const int nc = (int)min((long)C, len - (long)c * C);
             float egt = 0.f;
             if (pwarp) {
-                // ---- U = U~_b - P for token t = L - 64, columns [c0, c0 + 32) ----
+                // ---- U = U~_b - P and U' = exp(g_C - g_t) U for token t = L - 64,
+                //      columns [c0, c0 + 32) ----
                 const int t = L - 64;
+                const float ft = __expf(gC - g[t]);
                 uint32_t r[32];
                 tmem_ld32(tb + lane_base + TM_PX + 64 * (c & 1) + c0, r);
                 tmem_ld_wait();
-                float u[32];
+                float u[32], uz[32];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const uint4 w = *reinterpret_cast<const uint4 *>(st + ST_U + sw128_offset(t, c0 + 8 * k));
@@ -848,13 +844,27 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                         u[8 * k + 2 * e + 1] = bf_hi(ww[e]) - __uint_as_float(r[8 * k + 2 * e + 1]);
                     }
                 }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) uz[i] = ft * u[i];
                 st_row_bf16x32(sU, t, c0, u);
+                st_row_bf16x32(sUz, t, c0, uz);
+                if (t >= nc) {
+                    // rows past the sequence's end: clear this column half of K
+                    // (the next sequence's tokens or zero fill) in both slabs
+                    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        *reinterpret_cast<uint4 *>(st + ST_KT + sw128_offset(t, c0 + 8 * k)) = zero4;
+                        *reinterpret_cast<uint4 *>(st + ST_KT + 8192 + sw128_offset(t, c0 + 8 * k)) =
+                            zero4;
+                    }
+                }
                 fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_u);
             } else {
-                egt = eg[L];   // read now: the stage may be refilled once S_{c+1} is published
+                egt = __expf(g[L]);   // read now: the stage may be refilled once S_{c+1} is published
             }
 
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_z, par))) { fail(); break; }
@@ -886,7 +896,6 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 tmem_ld32(tb + lane_base + TM_Y + 64 * (c & 1) + c0, yr);
                 tmem_ld_wait();
                 tc_fence_before();
-                const int nc = (int)min((long)C, len - (long)c * C);
                 if (L < nc) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(start + (long)c * C + L) * rs +
                                                            (size_t)h * D + j0 + c0);
@@ -1034,7 +1043,7 @@ int sm_count() {
 }
 
 struct WsLayout {
-    size_t meta, g, W, U, A, Kt, total;
+    size_t meta, g, W, U, A, total;
 };
 
 WsLayout layout(long n_chunks, int H, int n_seq) {
@@ -1045,8 +1054,7 @@ WsLayout layout(long n_chunks, int H, int n_seq) {
     L.W = L.g + align_up(slots * C * sizeof(float), 1024);
     L.U = L.W + slots * C * D * 2;
     L.A = L.U + slots * C * D * 2;
-    L.Kt = L.A + slots * C * C * 2;
-    L.total = L.Kt + slots * C * D * 2;
+    L.total = L.A + slots * C * C * 2;
     return L;
 }
 
@@ -1079,8 +1087,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     tp.o = static_cast<__nv_bfloat16 *>(p.o);
     tp.cu_seqlens = p.cu_seqlens;
     tp.status = p.status;
-    tp.eg_ws = reinterpret_cast<float *>(ws + L.g);
-    tp.Kt_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.Kt);
+    tp.g_ws = reinterpret_cast<float *>(ws + L.g);
     tp.W_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.W);
     tp.U_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.U);
     tp.A_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.A);
@@ -1089,12 +1096,11 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     tp.chunk_prefix = p.cu_seqlens ? chunk_prefix : nullptr;
     tp.order = p.cu_seqlens ? order : nullptr;
 
-    CUtensorMap mq, mk, mv, mw, mu, ma, mkt;
+    CUtensorMap mq, mk, mv, mw, mu, ma;
     const long slots = n_chunks_upper * p.H;
     if (!map_3d_rows(&mq, p.q, p.H, p.total_T) || !map_3d_rows(&mk, p.k, p.H, p.total_T) ||
         !map_3d_rows(&mv, p.v, p.H, p.total_T) || !map_2d(&mw, tp.W_ws, D, slots * C, C) ||
-        !map_2d(&mu, tp.U_ws, D, slots * C, C) || !map_2d(&ma, tp.A_ws, C, slots * C, C) ||
-        !map_2d(&mkt, tp.Kt_ws, D, slots * C, C))
+        !map_2d(&mu, tp.U_ws, D, slots * C, C) || !map_2d(&ma, tp.A_ws, C, slots * C, C))
         return cudaErrorInvalidValue;
 
     cudaError_t e;
@@ -1120,7 +1126,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     intra_kernel<<<(unsigned)grid1, P1_THREADS, P1_SMEM, s>>>(mq, mk, mv, mw, mu, tp, n_pairs);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    state_kernel<<<(unsigned)(2L * p.n_seq * p.H), P2_THREADS, P2_SMEM, s>>>(mq, mkt, mw, mu, ma, tp);
+    state_kernel<<<(unsigned)(2L * p.n_seq * p.H), P2_THREADS, P2_SMEM, s>>>(mq, mk, mw, mu, ma, tp);
     note_launch();
     return cudaGetLastError();
 }
