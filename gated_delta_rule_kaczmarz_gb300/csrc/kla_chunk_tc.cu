@@ -112,6 +112,14 @@ __device__ __forceinline__ bool slot_info(const TcParams &p, long g, int &seq, l
     return nc > 0;
 }
 
+// 2^x with the hardware approximation (PTX ex2.approx, relative error about
+// 2^-22; 0 for large negative x).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
@@ -233,7 +241,9 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     extern __shared__ unsigned char smraw[];
     __shared__ uint64_t bars[3];
     __shared__ uint32_t tslot;
-    __shared__ float sG[128], sBeta[128], sN2[128], sCarry[4];
+    __shared__ __align__(16) float sG[128];    // g of each token row
+    __shared__ __align__(16) float sG2[128];   // g * log2(e)
+    __shared__ float sBeta[128], sN2[128], sCarry[4];
     __shared__ int sAbort;
 
     unsigned char *sm = align1024(smraw);
@@ -325,6 +335,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     if (hf == 0) {
         if (warp & 1) gs += (double)sCarry[warp - 1];
         sG[r] = (float)gs;
+        sG2[r] = (float)(gs * 1.4426950408889634);
     }
 
     // ---- tiles landed: Gram products on the tensor cores ----
@@ -381,13 +392,24 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const int cb = slot * 64;
     const long gidx0 = 2L * pair + slot;
     const size_t slot_row = (size_t)(gidx0 * p.H + h) * C + t;   // row of this token in the ws
+    // Gamma_ts = exp(g_t - g_s) = exp2(g2_t - g2_s) is evaluated for every
+    // element (exponent clamped at 0, where the mask discards it) and masked
+    // by a select, so that the loop has no data-dependent branch.
+    const float gt2 = sG2[r];
     if (ok) {
         if (hf == 0) {
             float *Lrow = lslot(KQ, slot) + t * 64;
+            const int lim = (t < nc) ? t : 0;     // L row t has columns s < t
 #pragma unroll 1
             for (int g16 = 0; g16 < 4; ++g16) {
                 uint32_t rr[16];
                 tmem_ld16(tb + lane_base + cb + g16 * 16, rr);
+                float gs[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 v = *reinterpret_cast<const float4 *>(sG2 + cb + g16 * 16 + 4 * i);
+                    gs[4 * i] = v.x; gs[4 * i + 1] = v.y; gs[4 * i + 2] = v.z; gs[4 * i + 3] = v.w;
+                }
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 16; i += 4) {
@@ -395,30 +417,36 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int s = g16 * 16 + i + e;
-                        v4[e] = (s < t && t < nc)
-                                    ? bt * __expf(gt - sG[cb + s]) * __uint_as_float(rr[i + e])
-                                    : 0.f;
+                        const float ex = ex2_approx(fminf(gt2 - gs[i + e], 0.f));
+                        const float x = bt * ex * __uint_as_float(rr[i + e]);
+                        v4[e] = (s < lim) ? x : 0.f;
                     }
                     *reinterpret_cast<float4 *>(Lrow + lsw(t, g16 * 16 + i)) =
                         make_float4(v4[0], v4[1], v4[2], v4[3]);
                 }
             }
         } else {
+            const int hi = nc;                      // A^T row t has columns u in [t, nc)
 #pragma unroll 1
             for (int g16 = 0; g16 < 4; ++g16) {
                 uint32_t rr[16];
                 tmem_ld16(tb + lane_base + 128 + cb + g16 * 16, rr);
+                float gu[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 v = *reinterpret_cast<const float4 *>(sG2 + cb + g16 * 16 + 4 * i);
+                    gu[4 * i] = v.x; gu[4 * i + 1] = v.y; gu[4 * i + 2] = v.z; gu[4 * i + 3] = v.w;
+                }
                 tmem_ld_wait();
                 // this thread's token is the key s = t; the columns are queries u
                 uint32_t pk[8];
 #pragma unroll
                 for (int i = 0; i < 16; i += 2) {
                     const int u = g16 * 16 + i;
-                    const float a0 = (t <= u && u < nc)
-                                         ? __expf(sG[cb + u] - gt) * __uint_as_float(rr[i]) : 0.f;
-                    const float a1 = (t <= u + 1 && u + 1 < nc)
-                                         ? __expf(sG[cb + u + 1] - gt) * __uint_as_float(rr[i + 1])
-                                         : 0.f;
+                    const float x0 = ex2_approx(fminf(gu[i] - gt2, 0.f)) * __uint_as_float(rr[i]);
+                    const float x1 = ex2_approx(fminf(gu[i + 1] - gt2, 0.f)) * __uint_as_float(rr[i + 1]);
+                    const float a0 = (t <= u && u < hi) ? x0 : 0.f;
+                    const float a1 = (t <= u + 1 && u + 1 < hi) ? x1 : 0.f;
                     pk[i / 2] = pack_bf2(a0, a1);
                 }
                 if (vslot) {
