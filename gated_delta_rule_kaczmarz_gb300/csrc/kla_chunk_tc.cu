@@ -147,9 +147,11 @@ constexpr int P1_THREADS = 256;
 // of both chunks: for every diagonal block of size 2n whose two diagonal
 // n x n blocks already hold D1 = (I + L11)^{-1} and D2 = (I + L22)^{-1},
 // replace its lower-left block L21 by -D2 L21 D1.  All P1_THREADS threads;
-// each computes a (rows x 4) patch of the n x n products.
+// each computes a (rows x 4) patch of the n x n products.  M = L21 D1 goes
+// through `scratch` (row-major n x n per block), so the step needs two
+// barriers.
 template <int n>
-__device__ __forceinline__ void merge_level(unsigned char *kq, int tid) {
+__device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, int tid) {
     constexpr int nblk = 64 / (2 * n);               // blocks of size 2n per chunk
     constexpr int tpb = P1_THREADS / (2 * nblk);     // threads per block (both chunks)
     constexpr int rows = n * n / 4 / tpb;            // patch rows per thread (4 columns each)
@@ -159,11 +161,12 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, int tid) {
     constexpr int pcols = n / 4;                     // column patches per row band
     const int pr = q / pcols, pc = q % pcols;        // rows [rows*pr, +rows), cols [4pc, +4)
     float *Lp = lslot(kq, p);
+    float *Mp = scratch + blkid * n * n;
     float acc[rows][4];
     // M = L21 D1
 #pragma unroll
     for (int m = 0; m < rows; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
-#pragma unroll 2
+#pragma unroll
     for (int s4 = 0; s4 < n / 4; ++s4) {
         float4 bb[4];
 #pragma unroll
@@ -185,24 +188,20 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, int tid) {
             }
         }
     }
-    __syncthreads();  // L21 fully read
 #pragma unroll
     for (int m = 0; m < rows; ++m) {
-        const int r = o + n + rows * pr + m;
-        *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, o + 4 * pc)) =
+        *reinterpret_cast<float4 *>(Mp + (rows * pr + m) * n + 4 * pc) =
             make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
         acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
     }
-    __syncthreads();  // M stored where L21 was
-    // X = -D2 M
-#pragma unroll 2
+    __syncthreads();  // M complete; L21 no longer read
+    // X = -D2 M, written over L21
+#pragma unroll
     for (int s4 = 0; s4 < n / 4; ++s4) {
         float4 bb[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int r = o + n + 4 * s4 + e;
-            bb[e] = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, o + 4 * pc));
-        }
+        for (int e = 0; e < 4; ++e)
+            bb[e] = *reinterpret_cast<const float4 *>(Mp + (4 * s4 + e) * n + 4 * pc);
 #pragma unroll
         for (int m = 0; m < rows; ++m) {
             const int r = o + n + rows * pr + m;
@@ -217,7 +216,6 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, int tid) {
             }
         }
     }
-    __syncthreads();  // M fully read
 #pragma unroll
     for (int m = 0; m < rows; ++m) {
         const int r = o + n + rows * pr + m;
@@ -232,7 +230,7 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, int tid) {
 // warp reads): thread half hf = tid / 128 takes one of two column halves of
 // every per-row task (64-feature slab hf of K and V; the L rows or the A^T
 // rows; 32 of the 64 columns of T diag beta; the W rows or the U~ rows).
-constexpr uint32_t P1_SMEM = 3 * 32768 + 1024;  // K, V, Q/L/A regions + alignment slack
+constexpr uint32_t P1_SMEM = 3 * 32768 + 8192 + 1024;  // K, V, Q/L/A, merge scratch + slack
 
 __global__ void __launch_bounds__(P1_THREADS, 2)
 intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -253,6 +251,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     // fp32 L / T and then slab p of the bf16 operand T diag(beta).
     unsigned char *KQ = sm;
     unsigned char *sV = sm + 65536;   // [2 slabs][128 rows][128 B]
+    float *scratch = reinterpret_cast<float *>(sm + 98304);   // 8 KB, the inverse's products
 
     const int tid0 = threadIdx.x;
     if (status_bad(p.status)) return;
@@ -460,21 +459,24 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         // past the chunk's end (another sequence's tokens or TMA zero fill)
         // are cleared in K and V so that nothing from them can reach the
         // products.
-        const float gam_t = __expf(gt);
-        const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll 2
+        const bool live = t < nc;
+        const float gam_t = live ? ex2_approx(gt2) : 0.f;
+#pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
             uint4 *pk4 = reinterpret_cast<uint4 *>(KQ + hf * 32768 + sw128_offset(r, ch * 8));
-            if (t < nc) {
-                const uint4 v = *pk4;
-                *pk4 = make_uint4(pack_bf2(gam_t * bf_lo(v.x), gam_t * bf_hi(v.x)),
-                                  pack_bf2(gam_t * bf_lo(v.y), gam_t * bf_hi(v.y)),
-                                  pack_bf2(gam_t * bf_lo(v.z), gam_t * bf_hi(v.z)),
-                                  pack_bf2(gam_t * bf_lo(v.w), gam_t * bf_hi(v.w)));
-            } else {
-                *pk4 = zero4;
-                *reinterpret_cast<uint4 *>(sV + hf * 16384 + sw128_offset(r, ch * 8)) = zero4;
-            }
+            const uint4 v = *pk4;
+            uint4 w = make_uint4(pack_bf2(gam_t * bf_lo(v.x), gam_t * bf_hi(v.x)),
+                                 pack_bf2(gam_t * bf_lo(v.y), gam_t * bf_hi(v.y)),
+                                 pack_bf2(gam_t * bf_lo(v.z), gam_t * bf_hi(v.z)),
+                                 pack_bf2(gam_t * bf_lo(v.w), gam_t * bf_hi(v.w)));
+            if (!live) w = make_uint4(0u, 0u, 0u, 0u);
+            *pk4 = w;
+        }
+        if (!live) {
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4 *>(sV + hf * 16384 + sw128_offset(r, ch * 8)) =
+                    make_uint4(0u, 0u, 0u, 0u);
         }
     }
     if (!ok) sAbort = 1;
@@ -515,8 +517,8 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         }
         __syncthreads();
     }
-    merge_level<16>(KQ, tid);   // 32 x 32 diagonal blocks
-    merge_level<32>(KQ, tid);   // the whole 64 x 64 inverse
+    merge_level<16>(KQ, scratch, tid);   // 32 x 32 diagonal blocks
+    merge_level<32>(KQ, scratch, tid);   // the whole 64 x 64 inverse
 
     // ---- A operand = T diag(beta) in bf16, block diagonal over the two chunks;
     //      thread half hf converts columns [32 hf, 32 hf + 32) of row t ----
