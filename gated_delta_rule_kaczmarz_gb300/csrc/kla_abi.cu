@@ -126,7 +126,9 @@ kla_status run_prefill(kla::Problem &p, bool varlen, void *workspace, size_t wor
         if (varlen && !tc) {
             e = kla::launch_check_seqlens(p, s);
         } else {
-            e = cudaMemsetAsync(p.status, 0, sizeof(unsigned), s);
+            const size_t reset =
+                tc ? kla::chunk_tc_reset_bytes(p, n_chunks(varlen, p.n_seq, p.T, p.total_T)) : 0;
+            e = cudaMemsetAsync(p.status, 0, reset ? kla::kWsHeader + reset : sizeof(unsigned), s);
         }
         if (e != cudaSuccess) return cuda_fail(e, "status init");
     }

@@ -40,6 +40,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "kla_internal.h"
@@ -68,6 +69,8 @@ struct TcParams {
     __nv_bfloat16 *W_ws;       // [slots][64][128]
     __nv_bfloat16 *U_ws;       // [slots][64][128]   U~
     __nv_bfloat16 *A_ws;       // [slots][64 keys s][64 queries t]  A^T
+    unsigned *flags;           // fused launch: one ready flag per work item (zeroed per call)
+    int n_units;               // fused launch: sequences x heads
 };
 
 __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
@@ -151,7 +154,7 @@ constexpr int P1_THREADS = 256;
 // through `scratch` (row-major n x n per block), so the step needs two
 // barriers.
 template <int n>
-__device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, int tid) {
+__device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, int tid, int bar) {
     constexpr int nblk = 64 / (2 * n);               // blocks of size 2n per chunk
     constexpr int tpb = P1_THREADS / (2 * nblk);     // threads per block (both chunks)
     constexpr int rows = n * n / 4 / tpb;            // patch rows per thread (4 columns each)
@@ -194,7 +197,7 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, i
             make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
         acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
     }
-    __syncthreads();  // M complete; L21 no longer read
+    named_sync(bar, P1_THREADS);  // M complete; L21 no longer read
     // X = -D2 M, written over L21
 #pragma unroll
     for (int s4 = 0; s4 < n / 4; ++s4) {
@@ -222,7 +225,7 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, i
         *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, o + 4 * pc)) =
             make_float4(-acc[m][0], -acc[m][1], -acc[m][2], -acc[m][3]);
     }
-    __syncthreads();
+    named_sync(bar, P1_THREADS);
 }
 
 // ===================================================================== phase 1
@@ -230,21 +233,24 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, i
 // warp reads): thread half hf = tid / 128 takes one of two column halves of
 // every per-row task (64-feature slab hf of K and V; the L rows or the A^T
 // rows; 32 of the 64 columns of T diag beta; the W rows or the U~ rows).
-constexpr uint32_t P1_SMEM = 3 * 32768 + 8192 + 1024;  // K, V, Q/L/A, merge scratch + slack
+// Shared memory of one phase-1 worker: K|Q slabs (64 KB), V (32 KB), the
+// inverse's scratch (8 KB), then barriers and per-row scalars.
+constexpr uint32_t P1_SMALL = 3 * 32768 + 8192;
+constexpr uint32_t P1_REGION = 109568;
+static_assert(P1_SMALL + 64 + 4 * 512 <= P1_REGION, "phase-1 region");
+constexpr uint32_t P1_SMEM = P1_REGION + 1024;   // + alignment slack
 
-__global__ void __launch_bounds__(P1_THREADS, 2)
-intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-             const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mw,
-             const __grid_constant__ CUtensorMap mu, const TcParams p, long n_pairs) {
-    extern __shared__ unsigned char smraw[];
-    __shared__ uint64_t bars[3];
-    __shared__ uint32_t tslot;
-    __shared__ __align__(16) float sG[128];    // g of each token row
-    __shared__ __align__(16) float sG2[128];   // g * log2(e)
-    __shared__ float sBeta[128], sN2[128], sCarry[4];
-    __shared__ int sAbort;
-
-    unsigned char *sm = align1024(smraw);
+// Phase-1 worker: 256 threads (tid0 = 0..255) with named barrier `bar` over
+// them, shared memory `sm` (1024-aligned, P1_REGION bytes), work items
+// item0, item0 + step, ...  kFused: items run chunk-pair-major over all
+// (sequence, head) units, and each finished item is published through
+// p.flags for the state pass running in the same launch.
+template <bool kFused>
+__device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorMap *mk,
+                                          const CUtensorMap *mv, const CUtensorMap *mw,
+                                          const CUtensorMap *mu, const TcParams &p, long n_pairs,
+                                          unsigned char *sm, int tid0, int bar, long item0,
+                                          long step) {
     // KQ: two 64-feature slabs of 32 KB, each [K rows 0..127 | Q rows 0..127]
     // (128-byte rows, 128-byte swizzle), so that [K; Q] is one N = 256
     // operand.  After the Gram products the Q half of slab p holds chunk p's
@@ -252,8 +258,15 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     unsigned char *KQ = sm;
     unsigned char *sV = sm + 65536;   // [2 slabs][128 rows][128 B]
     float *scratch = reinterpret_cast<float *>(sm + 98304);   // 8 KB, the inverse's products
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + P1_SMALL);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P1_SMALL + 32);
+    volatile int *sAbort = reinterpret_cast<volatile int *>(sm + P1_SMALL + 36);
+    float *sCarry = reinterpret_cast<float *>(sm + P1_SMALL + 48);
+    float *sG = reinterpret_cast<float *>(sm + P1_SMALL + 64);   // g of each token row
+    float *sG2 = sG + 128;                                         // g * log2(e)
+    float *sBeta = sG2 + 128;
+    float *sN2 = sBeta + 128;
 
-    const int tid0 = threadIdx.x;
     if (status_bad(p.status)) return;
 
     if (tid0 == 0) {
@@ -261,20 +274,23 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         mbar_init(&bars[1], 1);
         mbar_init(&bars[2], 1);
         fence_mbar_init();
-        sAbort = 0;
+        *sAbort = 0;
     }
     if ((tid0 >> 5) == 0) {
-        tmem_alloc(&tslot, 256);
-        tmem_relinquish();
+        tmem_alloc(tslot, 256);
+        // the allocation permit is per CTA: in the fused launch the CTA's
+        // other worker still has to allocate, so it is kept
+        if (!kFused) tmem_relinquish();
     }
-    __syncthreads();
+    named_sync(bar, P1_THREADS);
     tc_fence_after();
 
     // Persistent: work items are (pair of chunks, head), head fastest, so that
     // CTAs running side by side read the same token rows of different heads.
     const long n_items = n_pairs * p.H;
-    uint32_t ph = 0;   // mbarrier phase parity of this CTA's current item
-    for (long item = blockIdx.x; item < n_items; item += gridDim.x) {
+    uint32_t ph = 0;      // mbarrier phase parity of this worker's current item
+    long pending = -1;    // fused: item written but not yet published (thread 0)
+    for (long item = item0; item < n_items; item += step) {
     // The thread index is re-read through an opaque move every item so that
     // the compiler does not hoist (and keep live) the many thread-dependent
     // shared-memory addresses across items.
@@ -283,10 +299,18 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const int warp = tid >> 5, lane = tid & 31;
     const int r = tid & 127, hf = tid >> 7;      // token row of the item, column half
     const int slot = r >> 6, t = r & 63;
-    const uint32_t tb = tslot;
+    const uint32_t tb = *tslot;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const long pair = item / p.H;
-    const int h = (int)(item % p.H);
+    long pair;
+    int h;
+    if (kFused) {   // item = (pair within the sequence) * units + (sequence * H + head)
+        const long u = item % p.n_units;
+        pair = (item / p.n_units) + (u / p.H) * (p.nch_fixed / 2);
+        h = (int)(u % p.H);
+    } else {
+        pair = item / p.H;
+        h = (int)(item % p.H);
+    }
     int seq0, seq1, nc0, nc1;
     long r00, r01;
     const bool v0 = slot_info(p, 2 * pair, seq0, r00, nc0);
@@ -305,10 +329,17 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
                 const int z = (int)(q ? r01 : r00);
-                tma_load_3d(KQ + s * 32768 + q * 8192, &mk, &bars[0], 64 * s, h, z);
-                tma_load_3d(KQ + s * 32768 + 16384 + q * 8192, &mq, &bars[0], 64 * s, h, z);
-                tma_load_3d(sV + s * 16384 + q * 8192, &mv, &bars[0], 64 * s, h, z);
+                tma_load_3d(KQ + s * 32768 + q * 8192, mk, &bars[0], 64 * s, h, z);
+                tma_load_3d(KQ + s * 32768 + 16384 + q * 8192, mq, &bars[0], 64 * s, h, z);
+                tma_load_3d(sV + s * 16384 + q * 8192, mv, &bars[0], 64 * s, h, z);
             }
+        if (kFused && pending >= 0) {   // the previous item's outputs are complete
+            bulk_wait_group0();
+            fence_proxy_async_global();
+            __threadfence();
+            st_release_u32(p.flags + pending, 1u);
+            pending = -1;
+        }
     }
 
     // ---- decay: g = inclusive prefix sum of log alpha within each chunk
@@ -330,7 +361,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         }
         if (lane == 31) sCarry[warp] = (float)gs;
     }
-    __syncthreads();
+    named_sync(bar, P1_THREADS);
     if (hf == 0) {
         if (warp & 1) gs += (double)sCarry[warp - 1];
         sG[r] = (float)gs;
@@ -339,11 +370,11 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
     // ---- tiles landed: Gram products on the tensor cores ----
     if (!mbar_wait(&bars[0], ph)) {
-        sAbort = 1;
+        *sAbort = 1;
         set_status(p.status, kDevTimeout);
     }
-    __syncthreads();
-    const bool abort1 = sAbort != 0;
+    named_sync(bar, P1_THREADS);
+    const bool abort1 = *sAbort != 0;
     if (tid == 0 && !abort1) {
         tc_fence_after();
         // [K K^T | K Q^T]: A = K (128 tokens), B = [K; Q] (256 rows), K = 128 features
@@ -373,7 +404,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         }
     }
     if (hf) sN2[r] = n2;
-    __syncthreads();
+    named_sync(bar, P1_THREADS);
     float bt = 0.f;
     if (hf == 0) {
         const float den = (n2 + sN2[r]) + p.eps;
@@ -479,9 +510,9 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                     make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    if (!ok) sAbort = 1;
-    __syncthreads();
-    const bool abort2 = sAbort != 0;
+    if (!ok) *sAbort = 1;
+    named_sync(bar, P1_THREADS);
+    const bool abort2 = *sAbort != 0;
 
     // ---- T = (I + L)^{-1}, built up in block sizes 16 -> 32 -> 64: the
     //      diagonal 16 x 16 blocks by forward substitution (first half of the
@@ -510,15 +541,15 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 x[rw] = a0 + a1;
             }
         }
-        __syncthreads();  // the diagonal blocks of L have been read
+        named_sync(bar, P1_THREADS);  // the diagonal blocks of L have been read
         if (hf == 0) {
 #pragma unroll
             for (int rw = 0; rw < 16; ++rw) Lb[rw * 64 + lsw(o + rw, o + c)] = x[rw];
         }
-        __syncthreads();
+        named_sync(bar, P1_THREADS);
     }
-    merge_level<16>(KQ, scratch, tid);   // 32 x 32 diagonal blocks
-    merge_level<32>(KQ, scratch, tid);   // the whole 64 x 64 inverse
+    merge_level<16>(KQ, scratch, tid, bar);   // 32 x 32 diagonal blocks
+    merge_level<32>(KQ, scratch, tid, bar);   // the whole 64 x 64 inverse
 
     // ---- A operand = T diag(beta) in bf16, block diagonal over the two chunks;
     //      thread half hf converts columns [32 hf, 32 hf + 32) of row t ----
@@ -533,7 +564,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             pk[2 * i] = pack_bf2(v.x * bs[0], v.y * bs[1]);
             pk[2 * i + 1] = pack_bf2(v.z * bs[2], v.w * bs[3]);
         }
-        __syncthreads();  // T fully read; its region becomes the bf16 A tile
+        named_sync(bar, P1_THREADS);  // T fully read; its region becomes the bf16 A tile
         unsigned char *own = KQ + slot * 32768 + 16384, *other = KQ + (1 - slot) * 32768 + 16384;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
@@ -545,7 +576,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     }
     fence_async_smem();
     tc_fence_before();
-    __syncthreads();
+    named_sync(bar, P1_THREADS);
     if (tid == 0 && !abort2) {
         tc_fence_after();
         const uint32_t aA = smem_u32(KQ + 16384), aK = smem_u32(KQ), aV = smem_u32(sV);
@@ -564,7 +595,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                      sdesc_sw128(aV + ks * 2048, 16384, 1024), id_w, ks > 0);
         mma_commit(&bars[2]);
     }
-    __syncthreads();
+    named_sync(bar, P1_THREADS);
 
     // ---- epilogue 2: W (first half) and U~ (second half) rows of token row r,
     //      bf16, staged in the now free K and V regions with the 128-byte
@@ -592,8 +623,9 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         }
         if (hf == 0 && vslot) p.g_ws[slot_row] = gt;
     }
+    if (kFused) __threadfence();   // A^T and g rows before the item is published
     fence_async_smem();
-    __syncthreads();
+    named_sync(bar, P1_THREADS);
     if (tid == 0 && ok) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -601,19 +633,36 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             const int y = (int)(((2L * pair + q) * p.H + h) * C);
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
-                tma_store_2d(&mw, KQ + s * 32768 + q * 8192, 64 * s, y);
-                tma_store_2d(&mu, sV + s * 16384 + q * 8192, 64 * s, y);
+                tma_store_2d(mw, KQ + s * 32768 + q * 8192, 64 * s, y);
+                tma_store_2d(mu, sV + s * 16384 + q * 8192, 64 * s, y);
             }
         }
         bulk_commit_group();
+        if (kFused) pending = item;
     }
     tc_fence_before();
-    __syncthreads();   // smem and TMEM free for the next item
+    named_sync(bar, P1_THREADS);   // smem and TMEM free for the next item
     ph ^= 1u;
-    if (sAbort) break;
+    if (*sAbort) break;
     }  // items
-    if (tid0 == 0) bulk_wait_group0();   // every TMA store complete before the CTA leaves
-    if ((tid0 >> 5) == 0) tmem_dealloc(tslot, 256);
+    if (tid0 == 0) {
+        bulk_wait_group0();   // every TMA store complete before the worker leaves
+        if (kFused && pending >= 0) {
+            fence_proxy_async_global();
+            __threadfence();
+            st_release_u32(p.flags + pending, 1u);
+        }
+    }
+    if ((tid0 >> 5) == 0) tmem_dealloc(*tslot, 256);
+}
+
+__global__ void __launch_bounds__(P1_THREADS, 2)
+intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+             const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mw,
+             const __grid_constant__ CUtensorMap mu, const TcParams p, long n_pairs) {
+    extern __shared__ unsigned char smraw[];
+    intra_run<false>(&mq, &mk, &mv, &mw, &mu, p, n_pairs, align1024(smraw), (int)threadIdx.x, 1,
+                     (long)blockIdx.x, (long)gridDim.x);
 }
 
 // ===================================================================== phase 2
@@ -681,29 +730,32 @@ __device__ __forceinline__ void st_row_bf16x32(unsigned char *tile, int row, int
                        pack_bf2(x[8 * k + 4], x[8 * k + 5]), pack_bf2(x[8 * k + 6], x[8 * k + 7]));
 }
 
-__global__ void __launch_bounds__(P2_THREADS, 1)
-state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-             const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
-             const __grid_constant__ CUtensorMap ma, const TcParams p) {
-    extern __shared__ unsigned char smraw[];
+// State pass of CTA `bid` (unit bid / 2, column half bid % 2) with threads
+// tid = 0 .. P2_THREADS-1 and shared memory `sm` (1024-aligned, P2_SMEM - 1024
+// bytes).  kFused: phase 1 runs in the same launch, and the load of chunk c
+// waits for the ready flag of the work item that holds it.
+template <bool kFused>
+__device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorMap *mk,
+                                          const CUtensorMap *mw, const CUtensorMap *mu,
+                                          const CUtensorMap *ma, const TcParams &p,
+                                          unsigned char *sm, int bid, int tid) {
     __shared__ uint64_t bar_ld[NSTAGE];
     __shared__ uint64_t bar_px, bar_u, bar_z, bar_s, bar_fin;
     __shared__ uint64_t bar_y[2];   // Y of chunk c completes on bar_y[c % 2]
     __shared__ uint32_t tslot;
     __shared__ int sAbort;
 
-    unsigned char *sm = align1024(smraw);
     unsigned char *sS = sm + SM_S, *sU = sm + SM_U, *sUz = sm + SM_UZ;
     float *sG = reinterpret_cast<float *>(sm + SM_G);
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int warp = tid >> 5, lane = tid & 31;
     const int L = (warp & 3) * 32 + lane;       // TMEM lane (main warps)
     const int hf = (warp >> 2) & 1;             // column half (main warps)
     const int c0 = 32 * hf;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     if (status_bad(p.status)) return;
-    const int unit = blockIdx.x >> 1, jh = blockIdx.x & 1, j0 = DVB * jh;
+    const int unit = bid >> 1, jh = bid & 1, j0 = DVB * jh;
     const int rank = unit / p.H, h = unit % p.H;
     const int seq = p.order ? p.order[rank] : rank;
     long start, len, chunk0;
@@ -735,7 +787,7 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         tmem_alloc(&tslot, 512);
         tmem_relinquish();
     }
-    __syncthreads();
+    named_sync(3, P2_THREADS);
     tc_fence_after();
     const uint32_t tb = tslot;
 
@@ -749,21 +801,49 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         const uint32_t id_px = idesc_bf16_f32(128, DVB, false, true);
         const uint32_t id_zy = idesc_bf16_f32(128, DVB, true, true);
         const uint32_t aS = smem_u32(sS), aU = smem_u32(sU), aUz = smem_u32(sUz);
-        int loads = 0;     // stage loads issued
-        if (lane == 0) {
-            for (int c = 0; c < NSTAGE && c < nch; ++c) {
-                const long slot = (chunk0 + c) * p.H + h;
-                issue_stage(sm + c * ST_BYTES, sG + c * C, &bar_ld[c], &mq, &mk, &mw, &mu, &ma,
-                            p.g_ws + slot * C, h, (int)(start + (long)c * C), (int)slot, j0);
+        // Stage loads go out in chunk order.  Chunk n's load needs its stage
+        // free (Y of chunk n - NSTAGE done) and, in a fused launch, the
+        // phase-1 item holding chunk n published (flag of pair n / 2).
+        int next = 0;   // next chunk to load (the same in every lane)
+        // Loads chunks next .. upto - 1 whose flags are set; with `block`, a
+        // flag not yet set is waited for (bounded).  False on a timeout.
+        auto load_upto = [&](int upto, bool block) -> bool {
+            if (upto > nch) upto = nch;
+            while (next < upto) {
+                int st = 1;
+                if (kFused && lane == 0) {
+                    const unsigned *f = p.flags + (long)(next >> 1) * p.n_units + unit;
+                    st = ld_acquire_u32(f) != 0u;
+                    if (!st && block) {
+                        const long long t0 = clock64();
+                        while (!(st = ld_acquire_u32(f) != 0u))
+                            if (clock64() - t0 > kWaitLimitCycles) { st = -1; break; }
+                    }
+                }
+                st = __shfl_sync(0xffffffffu, st, 0);
+                if (st < 0) return false;
+                if (st == 0) break;
+                if (lane == 0) {
+                    if (kFused) fence_proxy_async_global();
+                    const int bn = next % NSTAGE;
+                    const long slot = (chunk0 + next) * p.H + h;
+                    issue_stage(sm + bn * ST_BYTES, sG + bn * C, &bar_ld[bn], mq, mk, mw, mu, ma,
+                                p.g_ws + slot * C, h, (int)(start + (long)next * C), (int)slot, j0);
+                }
+                __syncwarp();
+                ++next;
             }
-        }
-        loads = nch < NSTAGE ? nch : NSTAGE;
-        __syncwarp();
+            return true;
+        };
+        bool lok = load_upto(1, true) && load_upto(NSTAGE, false);
         int c = 0;
+        if (!lok) { fail(); c = nch; }
         for (; c < nch; ++c) {
             const int b = c % NSTAGE;
             unsigned char *st = sm + b * ST_BYTES;
             const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NSTAGE) & 1);
+            // chunk c's load out (its stage is free: Y of chunk c - NSTAGE is done)
+            if (next <= c && !load_upto(c + 1, true)) { fail(); break; }
             // stage landed, and S_c written to shared memory by the main warps
             const bool ok = mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_s, par);
             if (!__all_sync(0xffffffffu, ok)) { fail(); break; }
@@ -778,22 +858,19 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 mma_commit(&bar_px);
             }
             __syncwarp();
-            // the previous chunk's products are done with its stage: refill it
-            if (c >= 1 && c - 1 + NSTAGE < nch) {
-                const int cp = c - 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(&bar_y[cp & 1], (uint32_t)((cp >> 1) & 1)))) {
-                    fail();
-                    break;
+            // loads ahead: chunks up to c + 1 have free stages; chunk c + 2 reuses
+            // the stage of chunk c - 1 once that chunk's last product is done
+            if (!load_upto(c + 2, false)) { fail(); break; }
+            if (next == c + 2 && next < nch) {
+                if (c >= 1) {
+                    const int cp = c - 1;
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(&bar_y[cp & 1], (uint32_t)((cp >> 1) & 1)))) {
+                        fail();
+                        break;
+                    }
                 }
-                if (lane == 0) {
-                    const int cn = c - 1 + NSTAGE, bn = (c - 1) % NSTAGE;
-                    const long slot = (chunk0 + cn) * p.H + h;
-                    issue_stage(sm + bn * ST_BYTES, sG + bn * C, &bar_ld[bn], &mq, &mk, &mw, &mu,
-                                &ma, p.g_ws + slot * C, h, (int)(start + (long)cn * C), (int)slot,
-                                j0);
-                }
-                ++loads;
-                __syncwarp();
+                if (!load_upto(c + 3, false)) { fail(); break; }
             }
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_u, par))) { fail(); break; }
             tc_fence_after();
@@ -821,7 +898,7 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         (void)mbar_wait(&bar_fin, 0u);
         // on an early exit, let the loads still in flight land before leaving
         if (c < nch) {
-            for (int k = c; k < loads; ++k)
+            for (int k = c; k < next; ++k)
                 (void)mbar_wait(&bar_ld[k % NSTAGE], (uint32_t)((k / NSTAGE) & 1));
         }
     } else {
@@ -953,8 +1030,46 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     }
 
     tc_fence_before();
-    __syncthreads();
+    named_sync(3, P2_THREADS);
     if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+__global__ void __launch_bounds__(P2_THREADS, 1)
+state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+             const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
+             const __grid_constant__ CUtensorMap ma, const TcParams p) {
+    extern __shared__ unsigned char smraw[];
+    state_run<false>(&mq, &mk, &mw, &mu, &ma, p, align1024(smraw), (int)blockIdx.x,
+                     (int)threadIdx.x);
+}
+
+// ===================================================================== fused launch
+// Phase 1 and the state pass in one cooperative launch, one CTA per SM: CTAs
+// [0, n_state) run the state pass (two per unit); every other CTA runs two
+// phase-1 workers over the work items in chunk-pair-major order, so that the
+// state pass consumes chunk pairs as they are published instead of waiting
+// for the whole of phase 1.  Only the consumer waits (bounded), and every CTA
+// is resident (cooperative launch), so the hand-off cannot deadlock.
+constexpr int FU_THREADS = 2 * P1_THREADS;
+static_assert(FU_THREADS >= P2_THREADS, "fused block size");
+constexpr uint32_t FU_SMEM = P2_SMEM > 2 * P1_REGION + 1024 ? P2_SMEM : 2 * P1_REGION + 1024;
+
+__global__ void __launch_bounds__(FU_THREADS, 1)
+fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+             const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mw,
+             const __grid_constant__ CUtensorMap mu, const __grid_constant__ CUtensorMap ma,
+             const TcParams p, long n_pairs, int n_state) {
+    extern __shared__ unsigned char smraw[];
+    unsigned char *sm = align1024(smraw);
+    const int tid = (int)threadIdx.x;
+    if ((int)blockIdx.x < n_state) {
+        if (tid < P2_THREADS) state_run<true>(&mq, &mk, &mw, &mu, &ma, p, sm, (int)blockIdx.x, tid);
+        return;
+    }
+    const int w = tid / P1_THREADS;
+    const long n_workers = 2L * ((long)gridDim.x - n_state);
+    intra_run<true>(&mq, &mk, &mv, &mw, &mu, p, n_pairs, sm + w * P1_REGION, tid % P1_THREADS,
+                    1 + w, 2L * ((long)blockIdx.x - n_state) + w, n_workers);
 }
 
 // ===================================================================== varlen prep
@@ -1078,9 +1193,11 @@ struct WsLayout {
 
 WsLayout layout(long n_chunks, int H, int n_seq) {
     const size_t slots = (size_t)n_chunks * H;
+    // meta: the varlen chunk table and order, or the fused launch's ready flags
+    const size_t meta_ints = std::max((size_t)2 * n_seq + 1, (size_t)((n_chunks + 1) / 2) * H);
     WsLayout L;
     L.meta = 0;
-    L.g = align_up(((size_t)2 * n_seq + 1) * sizeof(int), 1024);
+    L.g = align_up(meta_ints * sizeof(int), 1024);
     L.W = L.g + align_up(slots * C * sizeof(float), 1024);
     L.U = L.W + slots * C * D * 2;
     L.A = L.U + slots * C * D * 2;
@@ -1088,9 +1205,21 @@ WsLayout layout(long n_chunks, int H, int n_seq) {
     return L;
 }
 
+// The fused launch serves fixed-length batches with an even number of chunks
+// per sequence whose state pass fits on at most half of the SMs.
+bool use_fused(const Problem &p) {
+    if (p.cu_seqlens != nullptr || p.T <= 0) return false;
+    const int nch = (p.T + C - 1) / C;
+    return nch % 2 == 0 && 2L * p.n_seq * p.H <= sm_count() / 2;
+}
+
 }  // namespace
 
 bool chunk_tc_supported(int d, int dtype) { return d == 128 && dtype == 1; }
+
+size_t chunk_tc_reset_bytes(const Problem &p, long n_chunks_upper) {
+    return use_fused(p) ? (size_t)((n_chunks_upper + 1) / 2) * p.H * sizeof(unsigned) : 0;
+}
 
 size_t chunk_tc_workspace_bytes(long n_chunks_upper, int H, int n_seq) {
     return layout(n_chunks_upper, H, n_seq).total;
@@ -1152,6 +1281,38 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     }
     const long n_pairs = (n_chunks_upper + 1) / 2;
     const long n_items = n_pairs * p.H;
+    if (use_fused(p)) {
+        static bool fattr = false;
+        if (!fattr) {
+            if ((e = cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)FU_SMEM)) != cudaSuccess)
+                return e;
+            fattr = true;
+        }
+        tp.flags = reinterpret_cast<unsigned *>(ws + L.meta);   // zeroed with the status word
+        tp.n_units = p.n_seq * p.H;
+        const int n_state = 2 * p.n_seq * p.H;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)sm_count());
+        cfg.blockDim = dim3(FU_THREADS);
+        cfg.dynamicSmemBytes = FU_SMEM;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, fused_kernel, mq, mk, mv, mw, mu, ma, tp, n_pairs, n_state);
+        if (e == cudaSuccess) {
+            note_launch();
+            return cudaSuccess;
+        }
+        // not every CTA could be resident (the device is shared or smaller):
+        // the two-launch path below needs no co-residency
+        (void)cudaGetLastError();
+        tp.flags = nullptr;
+        tp.n_units = 0;
+    }
     const long grid1 = n_items < 2L * sm_count() ? n_items : 2L * sm_count();
     intra_kernel<<<(unsigned)grid1, P1_THREADS, P1_SMEM, s>>>(mq, mk, mv, mw, mu, tp, n_pairs);
     note_launch();

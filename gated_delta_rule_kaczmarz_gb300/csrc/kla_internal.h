@@ -58,5 +58,8 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v,
 size_t chunk_tc_workspace_bytes(long n_chunks_upper, int H, int n_seq);
 bool chunk_tc_supported(int d, int dtype);
 cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t s);
+// Bytes after the workspace header that must be zero when launch_chunk_tc
+// starts (the single-launch path's ready flags); cleared with the status word.
+size_t chunk_tc_reset_bytes(const Problem &p, long n_chunks_upper);
 
 }  // namespace kla

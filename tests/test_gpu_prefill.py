@@ -67,9 +67,10 @@ def test_parity_small(B, T, H, d, dtype, sig, s0):
 
 @pytest.mark.parametrize("varlen", [False, True])
 def test_bf16_d128_runs_on_the_tensor_core_kernels(varlen):
-    """bf16 with d = 128 takes the two-phase tcgen05 path: one intra-chunk
-    launch and one state-pass launch (plus a sequence-table launch for
-    varlen), and no CUDA-core chunk kernel."""
+    """bf16 with d = 128 takes the tcgen05 path.  A fixed-length batch with an
+    even number of chunks per sequence and a small state pass is one fused
+    launch (phase 1 and the state pass together); varlen is a sequence-table
+    launch, the intra-chunk launch and the state-pass launch."""
     inp = prefill_inputs(2, 256, 2, 128, 128, "bf16", seed=11, s0_var=0.01)
     d = cuda(inp)
     n0 = kla.kla_launch_count()
@@ -81,9 +82,41 @@ def test_bf16_d128_runs_on_the_tensor_core_kernels(varlen):
     else:
         kla.kla_chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["eta"], d["eps"], d["S0"])
     torch.cuda.synchronize()
-    assert kla.kla_launch_count() - n0 == (3 if varlen else 2)
+    assert kla.kla_launch_count() - n0 == (3 if varlen else 1)
     ws = kla.kla_chunk_fwd_workspace_size(2, 256, 2, 128, 128)
     assert ws > 256
+
+
+def test_odd_chunk_count_uses_two_launches():
+    """Three chunks per sequence: the intra-chunk and state-pass launches."""
+    inp = prefill_inputs(1, 129, 2, 128, 128, "bf16", seed=12, s0_var=0.01)
+    d = cuda(inp)
+    n0 = kla.kla_launch_count()
+    kla.kla_chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["eta"], d["eps"], d["S0"])
+    torch.cuda.synchronize()
+    assert kla.kla_launch_count() - n0 == 2
+
+
+def test_fused_launch_equals_two_launch_path():
+    """Sequences of a batch are independent: 48 sequences x 2 heads (too many
+    state-pass CTAs for the fused launch: two launches) give bitwise the same
+    outputs and states as the same sequences in batches of 4 (fused launch)."""
+    inp = prefill_inputs(48, 128, 2, 128, 128, "bf16", seed=13, s0_var=0.01)
+    d = cuda(inp)
+    n0 = kla.kla_launch_count()
+    o_all, S_all = kla.kla_chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["eta"], d["eps"],
+                                     d["S0"])
+    torch.cuda.synchronize()
+    assert kla.kla_launch_count() - n0 == 2
+    for b0 in range(0, 48, 4):
+        sl = lambda x: x[b0:b0 + 4].contiguous()
+        n1 = kla.kla_launch_count()
+        o, S = kla.kla_chunk_fwd(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["alpha"]), sl(d["eta"]),
+                                 d["eps"], sl(d["S0"]))
+        torch.cuda.synchronize()
+        assert kla.kla_launch_count() - n1 == 1
+        torch.testing.assert_close(o, o_all[b0:b0 + 4], rtol=0, atol=0)
+        torch.testing.assert_close(S, S_all[b0:b0 + 4], rtol=0, atol=0)
 
 
 def test_eta_zero_is_pure_decay():
