@@ -681,8 +681,9 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 // Warp roles: warps 0-7 ("main") own TMEM lane L = 32 (warp % 4) + lane
 // (= dk row L of S_b, = token L of X / Y for L < 64, = token L - 64 of P for
 // L >= 64) and the 32 columns [32 hf, 32 hf + 32) of the tile, hf = warp / 4;
-// warp 8 issues every MMA and TMA load from lane 0 and waits converged.
-constexpr int P2_MAIN = 256, P2_THREADS = P2_MAIN + 32;
+// warp 8 issues every MMA from lane 0; warp 9 issues the stage loads (and, in
+// the fused launch, waits for the ready flags).  Both wait converged.
+constexpr int P2_MAIN = 256, P2_THREADS = P2_MAIN + 64;
 constexpr int NSTAGE = 3;
 constexpr int DVB = 64;   // dv columns per CTA
 // Stage layout (one chunk):
@@ -740,6 +741,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                                           const CUtensorMap *ma, const TcParams &p,
                                           unsigned char *sm, int bid, int tid) {
     __shared__ uint64_t bar_ld[NSTAGE];
+    __shared__ uint64_t bar_empty[NSTAGE];   // the products of a stage's chunk are done
     __shared__ uint64_t bar_px, bar_u, bar_z, bar_s, bar_fin;
     __shared__ uint64_t bar_y[2];   // Y of chunk c completes on bar_y[c % 2]
     __shared__ uint32_t tslot;
@@ -772,9 +774,12 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
     const size_t sbase = ((size_t)seq * p.H + h) * D * D;
 
     if (tid == 0) {
-        for (int i = 0; i < NSTAGE; ++i) mbar_init(&bar_ld[i], 1);
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&bar_ld[i], 1);
+            mbar_init(&bar_empty[i], 1);
+        }
         mbar_init(&bar_px, 1);
-        mbar_init(&bar_u, 4);      // one arrival per P warp (2, 3, 6, 7)
+        mbar_init(&bar_u, 8);      // one arrival per main warp
         mbar_init(&bar_z, 1);
         mbar_init(&bar_y[0], 1);
         mbar_init(&bar_y[1], 1);
@@ -801,49 +806,11 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         const uint32_t id_px = idesc_bf16_f32(128, DVB, false, true);
         const uint32_t id_zy = idesc_bf16_f32(128, DVB, true, true);
         const uint32_t aS = smem_u32(sS), aU = smem_u32(sU), aUz = smem_u32(sUz);
-        // Stage loads go out in chunk order.  Chunk n's load needs its stage
-        // free (Y of chunk n - NSTAGE done) and, in a fused launch, the
-        // phase-1 item holding chunk n published (flag of pair n / 2).
-        int next = 0;   // next chunk to load (the same in every lane)
-        // Loads chunks next .. upto - 1 whose flags are set; with `block`, a
-        // flag not yet set is waited for (bounded).  False on a timeout.
-        auto load_upto = [&](int upto, bool block) -> bool {
-            if (upto > nch) upto = nch;
-            while (next < upto) {
-                int st = 1;
-                if (kFused && lane == 0) {
-                    const unsigned *f = p.flags + (long)(next >> 1) * p.n_units + unit;
-                    st = ld_acquire_u32(f) != 0u;
-                    if (!st && block) {
-                        const long long t0 = clock64();
-                        while (!(st = ld_acquire_u32(f) != 0u))
-                            if (clock64() - t0 > kWaitLimitCycles) { st = -1; break; }
-                    }
-                }
-                st = __shfl_sync(0xffffffffu, st, 0);
-                if (st < 0) return false;
-                if (st == 0) break;
-                if (lane == 0) {
-                    if (kFused) fence_proxy_async_global();
-                    const int bn = next % NSTAGE;
-                    const long slot = (chunk0 + next) * p.H + h;
-                    issue_stage(sm + bn * ST_BYTES, sG + bn * C, &bar_ld[bn], mq, mk, mw, mu, ma,
-                                p.g_ws + slot * C, h, (int)(start + (long)next * C), (int)slot, j0);
-                }
-                __syncwarp();
-                ++next;
-            }
-            return true;
-        };
-        bool lok = load_upto(1, true) && load_upto(NSTAGE, false);
         int c = 0;
-        if (!lok) { fail(); c = nch; }
         for (; c < nch; ++c) {
             const int b = c % NSTAGE;
             unsigned char *st = sm + b * ST_BYTES;
             const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NSTAGE) & 1);
-            // chunk c's load out (its stage is free: Y of chunk c - NSTAGE is done)
-            if (next <= c && !load_upto(c + 1, true)) { fail(); break; }
             // stage landed, and S_c written to shared memory by the main warps
             const bool ok = mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_s, par);
             if (!__all_sync(0xffffffffu, ok)) { fail(); break; }
@@ -858,20 +825,6 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 mma_commit(&bar_px);
             }
             __syncwarp();
-            // loads ahead: chunks up to c + 1 have free stages; chunk c + 2 reuses
-            // the stage of chunk c - 1 once that chunk's last product is done
-            if (!load_upto(c + 2, false)) { fail(); break; }
-            if (next == c + 2 && next < nch) {
-                if (c >= 1) {
-                    const int cp = c - 1;
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait(&bar_y[cp & 1], (uint32_t)((cp >> 1) & 1)))) {
-                        fail();
-                        break;
-                    }
-                }
-                if (!load_upto(c + 3, false)) { fail(); break; }
-            }
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_u, par))) { fail(); break; }
             tc_fence_after();
             if (lane == 0) {
@@ -889,6 +842,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                     mma_bf16(tb + TM_Y + 64 * (c & 1), sdesc_sw128(aA + ks * 2048, 8192, 1024),
                              sdesc_sw128(aU + ks * 2048, 8192, 1024), id_zy, ks > 0);
                 mma_commit(&bar_y[c & 1]);
+                mma_commit(&bar_empty[b]);   // the stage may be refilled
             }
             __syncwarp();
         }
@@ -896,11 +850,41 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         if (lane == 0) mma_commit(&bar_fin);
         __syncwarp();
         (void)mbar_wait(&bar_fin, 0u);
-        // on an early exit, let the loads still in flight land before leaving
-        if (c < nch) {
-            for (int k = c; k < next; ++k)
-                (void)mbar_wait(&bar_ld[k % NSTAGE], (uint32_t)((k / NSTAGE) & 1));
+    } else if (warp == 9) {
+        // ----------------------------------------------------------------- loads
+        // Chunk n goes to stage n % NSTAGE once the products of chunk
+        // n - NSTAGE are done with it (bar_empty) and, in the fused launch,
+        // once the phase-1 item holding chunk n is published (flag of pair
+        // n / 2, counted per unit).
+        int n = 0;
+        for (; n < nch; ++n) {
+            const int b = n % NSTAGE, k = n / NSTAGE;
+            if (k >= 1 &&
+                !__all_sync(0xffffffffu, mbar_wait(&bar_empty[b], (uint32_t)((k - 1) & 1)))) {
+                fail();
+                break;
+            }
+            int st = 1;
+            if (kFused && lane == 0) {
+                const unsigned *f = p.flags + (long)(n >> 1) * p.n_units + unit;
+                const long long t0 = clock64();
+                while (ld_acquire_u32(f) == 0u)
+                    if (clock64() - t0 > kWaitLimitCycles) { st = 0; break; }
+            }
+            if (!__shfl_sync(0xffffffffu, st, 0)) { fail(); break; }
+            if (lane == 0) {
+                if (kFused) fence_proxy_async_global();
+                const long slot = (chunk0 + n) * p.H + h;
+                issue_stage(sm + b * ST_BYTES, sG + b * C, &bar_ld[b], mq, mk, mw, mu, ma,
+                            p.g_ws + slot * C, h, (int)(start + (long)n * C), (int)slot, j0);
+            }
+            __syncwarp();
         }
+        // on an early exit, the loads still in flight (at most one per stage)
+        // land before the CTA leaves
+        if (sAbort)
+            for (int k = n > NSTAGE ? n - NSTAGE : 0; k < n; ++k)
+                (void)mbar_wait(&bar_ld[k % NSTAGE], (uint32_t)((k / NSTAGE) & 1));
     } else {
         // ----------------------------------------------------------------- main
         const size_t rs = (size_t)p.H * D;
@@ -971,7 +955,12 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_u);
             } else {
-                egt = __expf(g[L]);   // read now: the stage may be refilled once S_{c+1} is published
+                // every read of this stage by the main warps precedes their
+                // bar_u arrival, which precedes the products whose completion
+                // frees the stage for the next load
+                egt = __expf(g[L]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_u);
             }
 
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_z, par))) { fail(); break; }
