@@ -24,6 +24,11 @@ decode(q, k, v, alpha, eta, eps, S, nthreads=1) -> (o, S_new)
 Every array argument may be a numpy array or a CPU torch tensor of any
 floating dtype; values are upcast exactly to float64 (bf16 and fp32 are
 subsets of fp64).
+
+Every function also takes ``beta_mode``: "kaczmarz" (default, beta_t =
+eta_t / (||k_t||^2 + eps)) or "given" (beta_t = eta_t, the learned write
+strength of Gated DeltaNet); and ``alpha`` may be None (alpha_t = 1, no
+decay: DeltaNet).
 """
 from __future__ import annotations
 
@@ -77,7 +82,14 @@ def _bind(lib):
     lib.kla_oracle_forward_varlen.argtypes = [
         ctypes.c_int, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         dp, dp, dp, dp, dp, ctypes.c_double, dp, dp, dp, ctypes.c_int]
+    lib.kla_oracle_forward_ex.restype = ctypes.c_int
+    lib.kla_oracle_forward_ex.argtypes = lib.kla_oracle_forward.argtypes + [ctypes.c_int]
+    lib.kla_oracle_forward_varlen_ex.restype = ctypes.c_int
+    lib.kla_oracle_forward_varlen_ex.argtypes = lib.kla_oracle_forward_varlen.argtypes + [ctypes.c_int]
     return lib
+
+
+_MODES = {"kaczmarz": 0, "given": 1}
 
 
 def _load():
@@ -102,8 +114,8 @@ def compile_variant(source_text: str, so_path: str):
 
     class _Variant:
         @staticmethod
-        def forward(q, k, v, alpha, eta, eps, S0=None, nthreads=1):
-            return _forward_with(lib, q, k, v, alpha, eta, eps, S0, nthreads)
+        def forward(q, k, v, alpha, eta, eps, S0=None, nthreads=1, beta_mode="kaczmarz"):
+            return _forward_with(lib, q, k, v, alpha, eta, eps, S0, nthreads, beta_mode)
     return _Variant
 
 
@@ -127,29 +139,30 @@ def _ptr(a):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
-def forward(q, k, v, alpha, eta, eps, S0=None, nthreads: int = 1):
-    return _forward_with(_load(), q, k, v, alpha, eta, eps, S0, nthreads)
+def forward(q, k, v, alpha, eta, eps, S0=None, nthreads: int = 1, beta_mode: str = "kaczmarz"):
+    return _forward_with(_load(), q, k, v, alpha, eta, eps, S0, nthreads, beta_mode)
 
 
-def _forward_with(lib, q, k, v, alpha, eta, eps, S0, nthreads):
+def _forward_with(lib, q, k, v, alpha, eta, eps, S0, nthreads, beta_mode="kaczmarz"):
     q, k, v, alpha, eta, S0 = map(_f64, (q, k, v, alpha, eta, S0))
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     assert k.shape == (B, T, H, dk) and v.shape == (B, T, H, dv)
-    assert alpha.shape == (B, T, H) and eta.shape == (B, T, H)
+    assert (alpha is None or alpha.shape == (B, T, H)) and eta.shape == (B, T, H)
     if S0 is not None:
         assert S0.shape == (B, H, dk, dv)
     o = np.zeros((B, T, H, dv), dtype=np.float64)
     S = np.zeros((B, H, dk, dv), dtype=np.float64)
-    rc = lib.kla_oracle_forward(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v),
-                                _ptr(alpha), _ptr(eta), float(eps), _ptr(S0),
-                                _ptr(o), _ptr(S), int(nthreads))
+    rc = lib.kla_oracle_forward_ex(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(alpha), _ptr(eta), float(eps), _ptr(S0),
+                                   _ptr(o), _ptr(S), int(nthreads), _MODES[beta_mode])
     if rc != 0:
         raise RuntimeError(f"kla_oracle_forward failed rc={rc}")
     return o, S
 
 
-def forward_varlen(q, k, v, alpha, eta, eps, cu_seqlens, S0=None, nthreads: int = 1):
+def forward_varlen(q, k, v, alpha, eta, eps, cu_seqlens, S0=None, nthreads: int = 1,
+                   beta_mode: str = "kaczmarz"):
     lib = _load()
     q, k, v, alpha, eta, S0 = map(_f64, (q, k, v, alpha, eta, S0))
     cu = np.ascontiguousarray(np.asarray(
@@ -163,18 +176,19 @@ def forward_varlen(q, k, v, alpha, eta, eps, cu_seqlens, S0=None, nthreads: int 
         assert S0.shape == (N, H, dk, dv)
     o = np.zeros((total, H, dv), dtype=np.float64)
     S = np.zeros((N, H, dk, dv), dtype=np.float64)
-    rc = lib.kla_oracle_forward_varlen(
+    rc = lib.kla_oracle_forward_varlen_ex(
         N, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), H, dk, dv,
         _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps), _ptr(S0),
-        _ptr(o), _ptr(S), int(nthreads))
+        _ptr(o), _ptr(S), int(nthreads), _MODES[beta_mode])
     if rc != 0:
         raise RuntimeError(f"kla_oracle_forward_varlen failed rc={rc}")
     return o, S
 
 
-def decode(q, k, v, alpha, eta, eps, S, nthreads: int = 1):
+def decode(q, k, v, alpha, eta, eps, S, nthreads: int = 1, beta_mode: str = "kaczmarz"):
     q, k, v, alpha, eta, S = map(_f64, (q, k, v, alpha, eta, S))
     B, H, dk = q.shape
-    o, S_new = forward(q[:, None], k[:, None], v[:, None], alpha[:, None],
-                       eta[:, None], eps, S, nthreads=nthreads)
+    o, S_new = forward(q[:, None], k[:, None], v[:, None],
+                       None if alpha is None else alpha[:, None],
+                       eta[:, None], eps, S, nthreads=nthreads, beta_mode=beta_mode)
     return o[:, 0], S_new

@@ -30,6 +30,15 @@
  * the residual; the write with ||k||^2 + eps == 0 is the limit 0 (beta
  * taken as 0); no normalisation or scaling of q or k is applied.
  *
+ * Write-coefficient modes (beta_mode): 0 = Kaczmarz, beta_t as above;
+ * 1 = given, beta_t = eta_t itself -- the learned write strength of Gated
+ * DeltaNet, which KLA replaces by the Kaczmarz coefficient (KLA summary,
+ * "Contribuicoes Principais" item 2 and "Implementacao": only the diagonal
+ * B = Diag(beta) of the block solver changes; Linear Attention
+ * Architectures, "Metodologia e Estrutura", items DeltaNet and Gated
+ * DeltaNet).  alpha == NULL means alpha_t = 1 for every token (no decay:
+ * DeltaNet's recurrence).
+ *
  * Layouts (dense, row-major, doubles):
  *   q, k : [B, T, H, dk]     v, o : [B, T, H, dv]
  *   alpha, eta : [B, T, H]   S0, S_out : [B, H, dk, dv] (dv fastest)
@@ -44,6 +53,7 @@ typedef struct {
     int T, H, dk, dv;
     const double *q, *k, *v, *alpha, *eta, *S0;
     double eps;
+    int beta_mode;        /* 0: Kaczmarz, 1: given (beta = eta) */
     double *o, *S_out;
     /* varlen: token offsets of each unit's sequence; NULL for fixed length */
     const int *cu_seqlens;
@@ -72,15 +82,19 @@ static void run_unit(const job_t *J, int unit_seq, int h, long t0, int len,
         const double *kt = J->k + row * dk;
         const double *qt = J->q + row * dk;
         const double *vt = J->v + row * dv;
-        const double a = J->alpha[row];
+        const double a = J->alpha ? J->alpha[row] : 1.0;
         const double et = J->eta[row];
 
-        /* beta_t = eta_t / (||k_t||^2 + eps); a zero denominator means a
-         * zero key with eps = 0, whose write is taken as 0. */
-        double n2 = 0.0;
-        for (int i = 0; i < dk; ++i) n2 += kt[i] * kt[i];
-        const double den = n2 + J->eps;
-        const double beta = (den == 0.0) ? 0.0 : et / den;
+        /* Kaczmarz: beta_t = eta_t / (||k_t||^2 + eps); a zero denominator
+         * means a zero key with eps = 0, whose write is taken as 0.
+         * Given: beta_t = eta_t. */
+        double beta = et;
+        if (J->beta_mode == 0) {
+            double n2 = 0.0;
+            for (int i = 0; i < dk; ++i) n2 += kt[i] * kt[i];
+            const double den = n2 + J->eps;
+            beta = (den == 0.0) ? 0.0 : et / den;
+        }
 
         /* decayed previous state S~ = alpha_t S_{t-1} */
         for (size_t x = 0; x < sd; ++x) St[x] = a * S[x];
@@ -168,32 +182,46 @@ static int run_job(job_t *J, int nthreads)
 }
 
 /* Fixed-length batch.  Returns 0 on success, nonzero on bad arguments or
- * allocation failure. */
-int kla_oracle_forward(int B, int T, int H, int dk, int dv,
-                       const double *q, const double *k, const double *v,
-                       const double *alpha, const double *eta, double eps,
-                       const double *S0, double *o, double *S_out, int nthreads)
+ * allocation failure.  alpha may be NULL (alpha_t = 1). */
+int kla_oracle_forward_ex(int B, int T, int H, int dk, int dv,
+                          const double *q, const double *k, const double *v,
+                          const double *alpha, const double *eta, double eps,
+                          const double *S0, double *o, double *S_out, int nthreads,
+                          int beta_mode)
 {
     if (B < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0) return 2;
+    if (beta_mode != 0 && beta_mode != 1) return 2;
     job_t J;
     memset(&J, 0, sizeof J);
     J.T = T; J.H = H; J.dk = dk; J.dv = dv;
     J.q = q; J.k = k; J.v = v; J.alpha = alpha; J.eta = eta; J.S0 = S0;
     J.eps = eps; J.o = o; J.S_out = S_out;
+    J.beta_mode = beta_mode;
     J.cu_seqlens = NULL;
     J.n_units = B * H;
     return run_job(&J, nthreads);
 }
 
+int kla_oracle_forward(int B, int T, int H, int dk, int dv,
+                       const double *q, const double *k, const double *v,
+                       const double *alpha, const double *eta, double eps,
+                       const double *S0, double *o, double *S_out, int nthreads)
+{
+    return kla_oracle_forward_ex(B, T, H, dk, dv, q, k, v, alpha, eta, eps, S0, o, S_out,
+                                 nthreads, 0);
+}
+
 /* Packed variable-length batch: sequence n occupies token rows
  * cu_seqlens[n] .. cu_seqlens[n+1]-1 of q, k, v, alpha, eta, o
  * ([total_T, H, *]); S0 and S_out are [N, H, dk, dv]. */
-int kla_oracle_forward_varlen(int N, const int *cu_seqlens, int H, int dk, int dv,
-                              const double *q, const double *k, const double *v,
-                              const double *alpha, const double *eta, double eps,
-                              const double *S0, double *o, double *S_out, int nthreads)
+int kla_oracle_forward_varlen_ex(int N, const int *cu_seqlens, int H, int dk, int dv,
+                                 const double *q, const double *k, const double *v,
+                                 const double *alpha, const double *eta, double eps,
+                                 const double *S0, double *o, double *S_out, int nthreads,
+                                 int beta_mode)
 {
     if (N < 0 || H <= 0 || dk <= 0 || dv <= 0 || !cu_seqlens) return 2;
+    if (beta_mode != 0 && beta_mode != 1) return 2;
     if (cu_seqlens[0] != 0) return 2;
     for (int n = 0; n < N; ++n)
         if (cu_seqlens[n + 1] < cu_seqlens[n]) return 2;
@@ -202,7 +230,17 @@ int kla_oracle_forward_varlen(int N, const int *cu_seqlens, int H, int dk, int d
     J.T = 0; J.H = H; J.dk = dk; J.dv = dv;
     J.q = q; J.k = k; J.v = v; J.alpha = alpha; J.eta = eta; J.S0 = S0;
     J.eps = eps; J.o = o; J.S_out = S_out;
+    J.beta_mode = beta_mode;
     J.cu_seqlens = cu_seqlens;
     J.n_units = N * H;
     return run_job(&J, nthreads);
+}
+
+int kla_oracle_forward_varlen(int N, const int *cu_seqlens, int H, int dk, int dv,
+                              const double *q, const double *k, const double *v,
+                              const double *alpha, const double *eta, double eps,
+                              const double *S0, double *o, double *S_out, int nthreads)
+{
+    return kla_oracle_forward_varlen_ex(N, cu_seqlens, H, dk, dv, q, k, v, alpha, eta, eps, S0,
+                                        o, S_out, nthreads, 0);
 }

@@ -24,7 +24,7 @@ import pytest
 import oracle
 
 
-def chunked_unit(q, k, v, alpha, eta, eps, S0, C, normalise_keys=False):
+def chunked_unit(q, k, v, alpha, eta, eps, S0, C, normalise_keys=False, beta_given=False):
     T, dk = q.shape
     dv = v.shape[1]
     S = np.zeros((dk, dv)) if S0 is None else S0.copy()
@@ -37,6 +37,8 @@ def chunked_unit(q, k, v, alpha, eta, eps, S0, C, normalise_keys=False):
         n2 = np.sum(Kc * Kc, axis=1)
         den = n2 + eps
         beta = np.where(den == 0, 0.0, eta[sl] / np.where(den == 0, 1.0, den))
+        if beta_given:   # Gated DeltaNet: the write strength is eta itself
+            beta = eta[sl].copy()
         if normalise_keys:
             # k = |k| k^: beta k e^T = (beta |k|^2) k^ (v/|k| - S~^T k^)^T
             nk = np.sqrt(n2)
@@ -105,3 +107,16 @@ def test_a_planted_mistake_is_caught():
     o, _ = chunked_unit(q[0, :, 0], k[0, :, 0], v[0, :, 0], alpha_shift[0, :, 0], eta[0, :, 0],
                         1e-6, S0[0, 0], C)
     assert np.abs(o - o_ref[0, :, 0]).max() > 1e-3 * np.abs(o_ref).max()
+
+
+@pytest.mark.parametrize("C", [4, 16, 64])
+def test_chunked_equals_sequential_given_beta(C):
+    """The same block algorithm with B = Diag(beta) for a given beta (Gated
+    DeltaNet) matches the oracle's "given" mode."""
+    T, dk, dv = 75, 8, 6
+    q, k, v, alpha, eta, S0 = _case(40 + C, T, dk, dv, 0.5)
+    o_ref, S_ref = oracle.forward(q, k, v, alpha, eta, 1e-6, S0, beta_mode="given")
+    o, S = chunked_unit(q[0, :, 0], k[0, :, 0], v[0, :, 0], alpha[0, :, 0], eta[0, :, 0],
+                        1e-6, S0[0, 0], C, beta_given=True)
+    assert np.abs(o - o_ref[0, :, 0]).max() <= 1e-11 * np.abs(o_ref).max()
+    assert np.abs(S - S_ref[0, 0]).max() <= 1e-11 * np.abs(S_ref).max()
