@@ -32,6 +32,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "KLA chunkwise prefill tokens/s & % roofline; decode steps/s at B=256"
+# DRAM bytes (read + write) of one prefill launch (fused_kernel) and one decode
+# launch scaled to B=256, from the ncu captures summarised in profiles/
+# (fused_kernel_layer_prefill.md, decode_kernel_b128.md).
+TRAFFIC_PREFILL = 71.71e6
+TRAFFIC_DECODE = 2 * (135.83e6 + 74.59e6)
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 BYTES_PER_TOKEN_HEAD = 1032          # q,k,v,o bf16 (4 x 256 B) + alpha, eta fp32 (8 B)
 
@@ -321,8 +326,8 @@ def ours(args):
     avg_s = t_total_s / args.steps
     achieved = alg_bytes / avg_s / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / pk["hbm_gbs"], "traffic": None,
-            "kernel": "prefill call", "peak_source": pk_src,
+            "frac": achieved / pk["hbm_gbs"], "traffic": TRAFFIC_PREFILL,
+            "kernel": "fused_kernel (the whole prefill call)", "peak_source": pk_src,
             "algorithmic_bytes_per_launch": alg_bytes}
 
     dec = time_decode(args, dev, reps=args.decode_reps)
@@ -332,7 +337,7 @@ def ours(args):
                          "dk": dec["wl"].d, "dv": dec["wl"].d, "steps": dec["wl"].steps},
               "roofline": {"bound": "hbm", "achieved": dec_achieved, "peak": pk["hbm_gbs"],
                            "unit": "GB/s", "frac": dec_achieved / pk["hbm_gbs"],
-                           "traffic": None, "kernel": "decode_kernel",
+                           "traffic": TRAFFIC_DECODE, "kernel": "decode_kernel",
                            "algorithmic_bytes_per_launch": dec["bytes_per_launch"]}}
 
     cpu = None

@@ -7,11 +7,14 @@ draws seeded synthetic inputs.
 from .binding import (  # noqa: F401
     KlaError,
     kla_chunk_fwd,
+    kla_chunk_fwd_ex,
     kla_chunk_fwd_noalloc,
     kla_chunk_fwd_varlen,
+    kla_chunk_fwd_varlen_ex,
     kla_chunk_fwd_varlen_workspace_size,
     kla_chunk_fwd_workspace_size,
     kla_decode_step,
+    kla_decode_step_ex,
     kla_launch_count,
     kla_status_str,
     kla_version,

@@ -27,6 +27,9 @@ KLA_ERR_TIMEOUT = 4
 KLA_ERR_WORKSPACE = 5
 KLA_DTYPE_F32 = 0
 KLA_DTYPE_BF16 = 1
+KLA_BETA_KACZMARZ = 0
+KLA_BETA_GIVEN = 1
+_BETA_MODES = {"kaczmarz": KLA_BETA_KACZMARZ, "given": KLA_BETA_GIVEN}
 CHUNK = 64
 
 _lock = threading.Lock()
@@ -77,6 +80,14 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
                                              I, I, I, I, I, I, I, vp, Z, vp]
         lib.kla_decode_step.restype = I
         lib.kla_decode_step.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, I, I, I, I, I, vp]
+        lib.kla_chunk_fwd_ex.restype = I
+        lib.kla_chunk_fwd_ex.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, fp,
+                                         I, I, I, I, I, I, I, I, vp, Z, vp]
+        lib.kla_chunk_fwd_varlen_ex.restype = I
+        lib.kla_chunk_fwd_varlen_ex.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, fp, ip,
+                                                I, I, I, I, I, I, I, I, vp, Z, vp]
+        lib.kla_decode_step_ex.restype = I
+        lib.kla_decode_step_ex.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, I, I, I, I, I, I, vp]
         lib.kla_chunk_fwd_noalloc.restype = I
         lib.kla_chunk_fwd_noalloc.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, fp,
                                               I, I, I, I, I, I, I, vp]
@@ -145,6 +156,12 @@ def kla_chunk_fwd_varlen_workspace_size(N, total_T, H, dk, dv, chunk=CHUNK,
     return int(load().kla_chunk_fwd_varlen_workspace_size(N, total_T, H, dk, dv, chunk, dtype))
 
 
+def _mode(beta_mode) -> int:
+    if beta_mode not in _BETA_MODES:
+        raise ValueError(f"beta_mode must be one of {sorted(_BETA_MODES)}")
+    return _BETA_MODES[beta_mode]
+
+
 def _workspace(nbytes, device, workspace):
     if nbytes == 0:
         return None, 0
@@ -156,9 +173,11 @@ def _workspace(nbytes, device, workspace):
 
 
 def kla_chunk_fwd(q, k, v, alpha, eta, eps, S0=None, o=None, S_T=None, workspace=None,
-                  stream=None, chunk=CHUNK, return_final_state=True):
+                  stream=None, chunk=CHUNK, return_final_state=True, beta_mode="kaczmarz"):
     """Chunkwise prefill; q,k: [B,T,H,dk], v: [B,T,H,dv], alpha,eta: [B,T,H]
-    fp32, S0: [B,H,dk,dv] fp32 or None.  Returns (o, S_T)."""
+    fp32 (alpha None: no decay), S0: [B,H,dk,dv] fp32 or None.  beta_mode
+    "kaczmarz" (beta = eta / (||k||^2 + eps)) or "given" (beta = eta).
+    Returns (o, S_T)."""
     lib = load()
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -174,9 +193,9 @@ def kla_chunk_fwd(q, k, v, alpha, eta, eps, S0=None, o=None, S_T=None, workspace
     _need(S_T, "S_T", torch.float32, (B, H, dk, dv))
     nbytes = int(lib.kla_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, dt))
     workspace, wsb = _workspace(nbytes, q.device, workspace)
-    st = lib.kla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps),
-                           _ptr(S0), _ptr(o), _ptr(S_T), B, T, H, dk, dv, chunk, dt,
-                           _ptr(workspace), wsb, _stream(stream))
+    st = lib.kla_chunk_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps),
+                              _ptr(S0), _ptr(o), _ptr(S_T), B, T, H, dk, dv, chunk, dt,
+                              _mode(beta_mode), _ptr(workspace), wsb, _stream(stream))
     _check(st)
     return o, S_T
 
@@ -208,7 +227,7 @@ def kla_chunk_fwd_noalloc(q, k, v, alpha, eta, eps, S0=None, o=None, S_T=None, s
 
 def kla_chunk_fwd_varlen(q, k, v, alpha, eta, eps, cu_seqlens, S0=None, o=None, S_T=None,
                          workspace=None, stream=None, chunk=CHUNK, return_final_state=True,
-                         check_status=False):
+                         check_status=False, beta_mode="kaczmarz"):
     """Packed prefill; q,k: [total_T,H,dk], v: [total_T,H,dv], alpha,eta:
     [total_T,H], cu_seqlens: int32 [N+1] on the device.  Returns (o, S_T)."""
     lib = load()
@@ -229,16 +248,17 @@ def kla_chunk_fwd_varlen(q, k, v, alpha, eta, eps, cu_seqlens, S0=None, o=None, 
     nbytes = int(lib.kla_chunk_fwd_varlen_workspace_size(N, total, H, dk, dv, chunk, dt))
     workspace, wsb = _workspace(nbytes, q.device, workspace)
     s = _stream(stream)
-    st = lib.kla_chunk_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps),
-                                  _ptr(S0), _ptr(o), _ptr(S_T), _ptr(cu_seqlens), N, total,
-                                  H, dk, dv, chunk, dt, _ptr(workspace), wsb, s)
+    st = lib.kla_chunk_fwd_varlen_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta),
+                                     float(eps), _ptr(S0), _ptr(o), _ptr(S_T), _ptr(cu_seqlens),
+                                     N, total, H, dk, dv, chunk, dt, _mode(beta_mode),
+                                     _ptr(workspace), wsb, s)
     _check(st)
     if check_status:
         _check(lib.kla_workspace_status(_ptr(workspace), wsb, s))
     return o, S_T
 
 
-def kla_decode_step(q, k, v, alpha, eta, eps, S, o=None, stream=None):
+def kla_decode_step(q, k, v, alpha, eta, eps, S, o=None, stream=None, beta_mode="kaczmarz"):
     """One decode step; q,k: [B,H,dk], v: [B,H,dv], alpha,eta: [B,H], S:
     [B,H,dk,dv] fp32 updated in place.  Returns o [B,H,dv]."""
     lib = load()
@@ -251,8 +271,9 @@ def kla_decode_step(q, k, v, alpha, eta, eps, S, o=None, stream=None):
     if o is None:
         o = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
     _need(o, "o", q.dtype, (B, H, dv))
-    st = lib.kla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps),
-                             _ptr(S), _ptr(o), B, H, dk, dv, dt, _stream(stream))
+    st = lib.kla_decode_step_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps),
+                                _ptr(S), _ptr(o), B, H, dk, dv, dt, _mode(beta_mode),
+                                _stream(stream))
     _check(st)
     return o
 
@@ -265,3 +286,18 @@ def kla_workspace_status(workspace, stream=None) -> int:
     st = lib.kla_workspace_status(_ptr(workspace), wsb, _stream(stream))
     _check(st)
     return st
+
+
+# The *_ex C entry points: the same calls with the write-coefficient mode as a
+# required argument ("kaczmarz" or "given").
+def kla_chunk_fwd_ex(q, k, v, alpha, eta, eps, beta_mode, S0=None, **kw):
+    return kla_chunk_fwd(q, k, v, alpha, eta, eps, S0, beta_mode=beta_mode, **kw)
+
+
+def kla_chunk_fwd_varlen_ex(q, k, v, alpha, eta, eps, cu_seqlens, beta_mode, S0=None, **kw):
+    return kla_chunk_fwd_varlen(q, k, v, alpha, eta, eps, cu_seqlens, S0, beta_mode=beta_mode,
+                                **kw)
+
+
+def kla_decode_step_ex(q, k, v, alpha, eta, eps, S, beta_mode, **kw):
+    return kla_decode_step(q, k, v, alpha, eta, eps, S, beta_mode=beta_mode, **kw)

@@ -180,13 +180,15 @@ size_t kla_chunk_fwd_varlen_workspace_size(int N, int total_T, int H, int dk, in
     return ws_bytes(true, N, 0, total_T, H, dk, dtype);
 }
 
-int kla_chunk_fwd(const void *q, const void *k, const void *v, const float *alpha,
-                  const float *eta, float eps, const float *S0, void *o, float *S_T, int B,
-                  int T, int H, int dk, int dv, int chunk, int dtype, void *workspace,
-                  size_t workspace_bytes, void *stream) {
+int kla_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *alpha,
+                     const float *eta, float eps, const float *S0, void *o, float *S_T, int B,
+                     int T, int H, int dk, int dv, int chunk, int dtype, int beta_mode,
+                     void *workspace, size_t workspace_bytes, void *stream) {
     if (B < 0 || T < 0) return fail(KLA_ERR_INVALID_ARG, "negative size (B=%d T=%d)", B, T);
     kla_status st = check_shape(H, dk, dv, chunk, dtype);
     if (st != KLA_OK) return st;
+    if (beta_mode != KLA_BETA_KACZMARZ && beta_mode != KLA_BETA_GIVEN)
+        return fail(KLA_ERR_INVALID_ARG, "unknown beta_mode %d", beta_mode);
     if (!(eps >= 0.f)) return fail(KLA_ERR_INVALID_ARG, "eps must be >= 0");
     const long rows = (long)B * T;
     if (rows > INT32_MAX || (long)B * H > INT32_MAX)
@@ -199,8 +201,8 @@ int kla_chunk_fwd(const void *q, const void *k, const void *v, const float *alph
         if (inject_launch_fault()) return fail(KLA_ERR_CUDA, "injected launch fault (KLA_FAULT_INJECT)");
         return states_only(S0, S_T, nstate, s);
     }
-    if (!q || !k || !v || !alpha || !eta || !o)
-        return fail(KLA_ERR_INVALID_ARG, "q, k, v, alpha, eta and o must be non-null");
+    if (!q || !k || !v || !eta || !o)
+        return fail(KLA_ERR_INVALID_ARG, "q, k, v, eta and o must be non-null");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(alpha) ||
         !aligned4(eta))
         return fail(KLA_ERR_INVALID_ARG, "q, k, v, o must be 16-byte aligned, alpha and eta 4-byte");
@@ -208,18 +210,29 @@ int kla_chunk_fwd(const void *q, const void *k, const void *v, const float *alph
     p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.eta = eta; p.eps = eps;
     p.S0 = S0; p.o = o; p.S_T = S_T; p.cu_seqlens = nullptr;
     p.n_seq = B; p.T = T; p.total_T = (int)rows; p.H = H; p.d = dk; p.dtype = dtype;
+    p.beta_mode = beta_mode;
     return run_prefill(p, false, workspace, workspace_bytes, s);
 }
 
-int kla_chunk_fwd_varlen(const void *q, const void *k, const void *v, const float *alpha,
-                         const float *eta, float eps, const float *S0, void *o, float *S_T,
-                         const int *cu_seqlens, int N, int total_T, int H, int dk, int dv,
-                         int chunk, int dtype, void *workspace, size_t workspace_bytes,
-                         void *stream) {
+int kla_chunk_fwd(const void *q, const void *k, const void *v, const float *alpha,
+                  const float *eta, float eps, const float *S0, void *o, float *S_T, int B,
+                  int T, int H, int dk, int dv, int chunk, int dtype, void *workspace,
+                  size_t workspace_bytes, void *stream) {
+    return kla_chunk_fwd_ex(q, k, v, alpha, eta, eps, S0, o, S_T, B, T, H, dk, dv, chunk, dtype,
+                            KLA_BETA_KACZMARZ, workspace, workspace_bytes, stream);
+}
+
+int kla_chunk_fwd_varlen_ex(const void *q, const void *k, const void *v, const float *alpha,
+                            const float *eta, float eps, const float *S0, void *o, float *S_T,
+                            const int *cu_seqlens, int N, int total_T, int H, int dk, int dv,
+                            int chunk, int dtype, int beta_mode, void *workspace,
+                            size_t workspace_bytes, void *stream) {
     if (N < 0 || total_T < 0)
         return fail(KLA_ERR_INVALID_ARG, "negative size (N=%d total_T=%d)", N, total_T);
     kla_status st = check_shape(H, dk, dv, chunk, dtype);
     if (st != KLA_OK) return st;
+    if (beta_mode != KLA_BETA_KACZMARZ && beta_mode != KLA_BETA_GIVEN)
+        return fail(KLA_ERR_INVALID_ARG, "unknown beta_mode %d", beta_mode);
     if (!(eps >= 0.f)) return fail(KLA_ERR_INVALID_ARG, "eps must be >= 0");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T)))
@@ -230,8 +243,8 @@ int kla_chunk_fwd_varlen(const void *q, const void *k, const void *v, const floa
     }
     if (!cu_seqlens) return fail(KLA_ERR_INVALID_ARG, "cu_seqlens must be non-null");
     if (total_T > 0) {
-        if (!q || !k || !v || !alpha || !eta || !o)
-            return fail(KLA_ERR_INVALID_ARG, "q, k, v, alpha, eta and o must be non-null");
+        if (!q || !k || !v || !eta || !o)
+            return fail(KLA_ERR_INVALID_ARG, "q, k, v, eta and o must be non-null");
         if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
             !aligned4(alpha) || !aligned4(eta))
             return fail(KLA_ERR_INVALID_ARG,
@@ -241,19 +254,32 @@ int kla_chunk_fwd_varlen(const void *q, const void *k, const void *v, const floa
     p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.eta = eta; p.eps = eps;
     p.S0 = S0; p.o = o; p.S_T = S_T; p.cu_seqlens = cu_seqlens;
     p.n_seq = N; p.T = 0; p.total_T = total_T; p.H = H; p.d = dk; p.dtype = dtype;
+    p.beta_mode = beta_mode;
     return run_prefill(p, true, workspace, workspace_bytes, s);
 }
 
-int kla_decode_step(const void *q, const void *k, const void *v, const float *alpha,
-                    const float *eta, float eps, float *S, void *o, int B, int H, int dk, int dv,
-                    int dtype, void *stream) {
+int kla_chunk_fwd_varlen(const void *q, const void *k, const void *v, const float *alpha,
+                         const float *eta, float eps, const float *S0, void *o, float *S_T,
+                         const int *cu_seqlens, int N, int total_T, int H, int dk, int dv,
+                         int chunk, int dtype, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+    return kla_chunk_fwd_varlen_ex(q, k, v, alpha, eta, eps, S0, o, S_T, cu_seqlens, N, total_T,
+                                   H, dk, dv, chunk, dtype, KLA_BETA_KACZMARZ, workspace,
+                                   workspace_bytes, stream);
+}
+
+int kla_decode_step_ex(const void *q, const void *k, const void *v, const float *alpha,
+                       const float *eta, float eps, float *S, void *o, int B, int H, int dk,
+                       int dv, int dtype, int beta_mode, void *stream) {
     if (B < 0) return fail(KLA_ERR_INVALID_ARG, "negative batch");
     kla_status st = check_shape(H, dk, dv, kla::kChunk, dtype);
     if (st != KLA_OK) return st;
+    if (beta_mode != KLA_BETA_KACZMARZ && beta_mode != KLA_BETA_GIVEN)
+        return fail(KLA_ERR_INVALID_ARG, "unknown beta_mode %d", beta_mode);
     if (!(eps >= 0.f)) return fail(KLA_ERR_INVALID_ARG, "eps must be >= 0");
     if (B == 0) return ok();
-    if (!q || !k || !v || !alpha || !eta || !S || !o)
-        return fail(KLA_ERR_INVALID_ARG, "all pointers must be non-null");
+    if (!q || !k || !v || !eta || !S || !o)
+        return fail(KLA_ERR_INVALID_ARG, "q, k, v, eta, S and o must be non-null");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(S) || !aligned16(o) ||
         !aligned4(alpha) || !aligned4(eta))
         return fail(KLA_ERR_INVALID_ARG,
@@ -261,9 +287,16 @@ int kla_decode_step(const void *q, const void *k, const void *v, const float *al
     if ((long)B * H > INT32_MAX) return fail(KLA_ERR_UNSUPPORTED, "B*H too large");
     if (inject_launch_fault()) return fail(KLA_ERR_CUDA, "injected launch fault (KLA_FAULT_INJECT)");
     cudaError_t e = kla::launch_decode(q, k, v, alpha, eta, eps, S, o, B * H, dk, dtype,
-                                       static_cast<cudaStream_t>(stream));
+                                       beta_mode, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return ok();
+}
+
+int kla_decode_step(const void *q, const void *k, const void *v, const float *alpha,
+                    const float *eta, float eps, float *S, void *o, int B, int H, int dk, int dv,
+                    int dtype, void *stream) {
+    return kla_decode_step_ex(q, k, v, alpha, eta, eps, S, o, B, H, dk, dv, dtype,
+                              KLA_BETA_KACZMARZ, stream);
 }
 
 int kla_workspace_status(const void *workspace, size_t workspace_bytes, void *stream) {

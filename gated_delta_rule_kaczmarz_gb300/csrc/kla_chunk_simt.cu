@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_simt_kernel(Problem p) {
         if (tid < C) {
             const bool ok = tid < nc;
             const size_t row = (size_t)(start + c0 + tid) * H + h;
-            sm.alpha[tid] = ok ? p.alpha[row] : 1.f;
+            sm.alpha[tid] = (ok && p.alpha) ? p.alpha[row] : 1.f;
             sm.eta[tid] = ok ? p.eta[row] : 0.f;
         }
         __syncthreads();
@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_simt_kernel(Problem p) {
             float n2 = 0.f;
             for (int i = 0; i < D; ++i) n2 = fmaf(sm.K[tid][i], sm.K[tid][i], n2);
             const float den = n2 + p.eps;
-            sm.beta[tid] = (tid < nc && den != 0.f) ? sm.eta[tid] / den : 0.f;
+            const float b = p.beta_mode ? sm.eta[tid] : (den != 0.f ? sm.eta[tid] / den : 0.f);
+            sm.beta[tid] = tid < nc ? b : 0.f;
         } else if (tid < C + 32) {
             // warp 2: inclusive scan of log alpha over 64 positions, in double
             const int lane = tid - C;

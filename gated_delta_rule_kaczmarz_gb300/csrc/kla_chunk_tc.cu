@@ -69,6 +69,7 @@ struct TcParams {
     __nv_bfloat16 *W_ws;       // [slots][64][128]
     __nv_bfloat16 *U_ws;       // [slots][64][128]   U~
     __nv_bfloat16 *A_ws;       // [slots][64 keys s][64 queries t]  A^T
+    int beta_mode;             // 0: beta = eta / (||k||^2 + eps); 1: beta = eta
     unsigned *flags;           // fused launch: one ready flag per work item (zeroed per call)
     int n_units;               // fused launch: sequences x heads
 };
@@ -350,7 +351,7 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
         float a = 1.f;
         if (t < nc) {
             const size_t row = (size_t)((slot ? r01 : r00) + t) * p.H + h;
-            a = p.alpha[row];
+            a = p.alpha ? p.alpha[row] : 1.f;   // no alpha: no decay
             et = p.eta[row];
         }
         gs = (double)logf(a);
@@ -408,7 +409,8 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     float bt = 0.f;
     if (hf == 0) {
         const float den = (n2 + sN2[r]) + p.eps;
-        bt = (t < nc && den != 0.f) ? et / den : 0.f;
+        const float b = p.beta_mode ? et : (den != 0.f ? et / den : 0.f);
+        bt = t < nc ? b : 0.f;
         sBeta[r] = bt;
     }
 
@@ -1228,6 +1230,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     tp.total_T = p.total_T;
     tp.nch_fixed = p.cu_seqlens ? 0 : (p.T + C - 1) / C;
     tp.eps = p.eps;
+    tp.beta_mode = p.beta_mode;
     tp.alpha = p.alpha;
     tp.eta = p.eta;
     tp.S0 = p.S0;

@@ -8,7 +8,8 @@
 //   e = v - alpha y                        (residual against alpha S)
 //   S <- alpha S + beta k e^T              (one write of S)
 //   o = S_new^T q = alpha z + beta (k.q) e
-//   beta = eta / (||k||^2 + eps), 0 when the denominator is 0
+//   beta = eta / (||k||^2 + eps), 0 when the denominator is 0 (or beta = eta
+//   in the given-beta mode); alpha == NULL means alpha = 1
 //
 // The kernel is bound by HBM: each (b,h) state (dk*dv*4 bytes) is streamed in
 // once and out once.  One CTA of 256 threads owns one state; every thread
@@ -38,8 +39,8 @@ template <typename Tin, int D>
 __global__ void __launch_bounds__(kDecThreads, 2)
 decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
               const Tin *__restrict__ v, const float *__restrict__ alpha,
-              const float *__restrict__ eta, float eps, float *__restrict__ S,
-              Tin *__restrict__ o) {
+              const float *__restrict__ eta, float eps, int beta_given,
+              float *__restrict__ S, Tin *__restrict__ o) {
     constexpr int C4 = D / 4;                 // float4 groups per state row
     constexpr int RSTEP = kDecThreads / C4;   // row stride between a thread's rows
     constexpr int R = D / RSTEP;              // rows per thread
@@ -67,7 +68,7 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         ks[tid] = ld_in(k, vbase + tid);
         qs[tid] = ld_in(q, vbase + tid);
     }
-    const float a = alpha[unit];
+    const float a = alpha ? alpha[unit] : 1.f;   // no alpha: no decay
     const float et = eta[unit];
     __syncthreads();
 
@@ -85,7 +86,7 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         }
         if (tid == 0) {
             const float den = n2 + eps;
-            scal[0] = (den == 0.f) ? 0.f : et / den;
+            scal[0] = beta_given ? et : ((den == 0.f) ? 0.f : et / den);
             scal[1] = kq;
         }
     }
@@ -132,11 +133,11 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 
 template <typename Tin, int D>
 cudaError_t launch_t(const void *q, const void *k, const void *v, const float *alpha,
-                     const float *eta, float eps, float *S, void *o, int BH,
+                     const float *eta, float eps, int beta_mode, float *S, void *o, int BH,
                      cudaStream_t s) {
     decode_kernel<Tin, D><<<BH, kDecThreads, 0, s>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k),
-        static_cast<const Tin *>(v), alpha, eta, eps, S, static_cast<Tin *>(o));
+        static_cast<const Tin *>(v), alpha, eta, eps, beta_mode, S, static_cast<Tin *>(o));
     note_launch();
     return cudaGetLastError();
 }
@@ -145,15 +146,15 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *a
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v,
                           const float *alpha, const float *eta, float eps,
-                          float *S, void *o, int BH, int d, int dtype,
+                          float *S, void *o, int BH, int d, int dtype, int beta_mode,
                           cudaStream_t s) {
     if (BH == 0) return cudaSuccess;
     if (dtype == 1) {
-        if (d == 128) return launch_t<__nv_bfloat16, 128>(q, k, v, alpha, eta, eps, S, o, BH, s);
-        return launch_t<__nv_bfloat16, 64>(q, k, v, alpha, eta, eps, S, o, BH, s);
+        if (d == 128) return launch_t<__nv_bfloat16, 128>(q, k, v, alpha, eta, eps, beta_mode, S, o, BH, s);
+        return launch_t<__nv_bfloat16, 64>(q, k, v, alpha, eta, eps, beta_mode, S, o, BH, s);
     }
-    if (d == 128) return launch_t<float, 128>(q, k, v, alpha, eta, eps, S, o, BH, s);
-    return launch_t<float, 64>(q, k, v, alpha, eta, eps, S, o, BH, s);
+    if (d == 128) return launch_t<float, 128>(q, k, v, alpha, eta, eps, beta_mode, S, o, BH, s);
+    return launch_t<float, 64>(q, k, v, alpha, eta, eps, beta_mode, S, o, BH, s);
 }
 
 }  // namespace kla

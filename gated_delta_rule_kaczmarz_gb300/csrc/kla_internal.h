@@ -35,6 +35,7 @@ struct Problem {
     int total_T;             // total token rows
     int H, d;                // heads, dk == dv
     int dtype;               // kla_dtype
+    int beta_mode;           // 0: beta = eta / (||k||^2 + eps); 1: beta = eta
     unsigned *status;        // device status word, or nullptr
     void *ws;                // workspace after the header (path specific)
     size_t ws_bytes;
@@ -51,7 +52,7 @@ cudaError_t launch_check_seqlens(const Problem &p, cudaStream_t s);
 cudaError_t launch_chunk_simt(const Problem &p, cudaStream_t s);
 cudaError_t launch_decode(const void *q, const void *k, const void *v,
                           const float *alpha, const float *eta, float eps,
-                          float *S, void *o, int BH, int d, int dtype,
+                          float *S, void *o, int BH, int d, int dtype, int beta_mode,
                           cudaStream_t s);
 
 // Tensor-core (tcgen05) prefill for bf16, d = 128.

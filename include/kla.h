@@ -28,6 +28,15 @@
  *     KLA_ERR_UNSUPPORTED without launching anything.
  *   - alpha must lie in (0, 1] and eps >= 0 (values are not scanned; outside
  *     that range results are unspecified but every access stays in bounds).
+ *     alpha may be NULL: alpha_t = 1 for every token (no decay, DeltaNet's
+ *     recurrence).
+ *   - The *_ex entry points take a write-coefficient mode (kla_beta_mode):
+ *     KLA_BETA_KACZMARZ is the rule above; KLA_BETA_GIVEN uses beta_t = eta_t
+ *     itself, the learned write strength of Gated DeltaNet that KLA replaces
+ *     (KLA summary, "Contribuicoes Principais" item 2 and "Implementacao":
+ *     only B = Diag(beta) of the block solver changes).  With alpha == NULL
+ *     and KLA_BETA_GIVEN the calls compute DeltaNet.  The entry points
+ *     without _ex use KLA_BETA_KACZMARZ.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *     asynchronous: a KLA_OK return means the work was validated and
  *     enqueued; faults of the enqueued work surface on a later
@@ -68,6 +77,11 @@ typedef enum {
     KLA_DTYPE_F32 = 0,
     KLA_DTYPE_BF16 = 1
 } kla_dtype;
+
+typedef enum {
+    KLA_BETA_KACZMARZ = 0,     /* beta_t = eta_t / (||k_t||^2 + eps), 0 if the sum is 0 */
+    KLA_BETA_GIVEN = 1         /* beta_t = eta_t */
+} kla_beta_mode;
 
 /* Static string for a status code; never NULL. */
 KLA_API const char *kla_status_str(int status);
@@ -114,6 +128,15 @@ KLA_API int kla_chunk_fwd(const void *q, const void *k, const void *v,
                   int B, int T, int H, int dk, int dv, int chunk, int dtype,
                   void *workspace, size_t workspace_bytes, void *stream);
 
+/* kla_chunk_fwd with a write-coefficient mode (kla_beta_mode); an unknown
+ * mode returns KLA_ERR_INVALID_ARG.  Same workspace size. */
+KLA_API int kla_chunk_fwd_ex(const void *q, const void *k, const void *v,
+                             const float *alpha, const float *eta, float eps,
+                             const float *S0, void *o, float *S_T,
+                             int B, int T, int H, int dk, int dv, int chunk, int dtype,
+                             int beta_mode, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
 /* Workspace bytes for kla_chunk_fwd_varlen (see kla_chunk_fwd_workspace_size). */
 KLA_API size_t kla_chunk_fwd_varlen_workspace_size(int N, int total_T, int H, int dk,
                                            int dv, int chunk, int dtype);
@@ -139,6 +162,15 @@ KLA_API int kla_chunk_fwd_varlen(const void *q, const void *k, const void *v,
                          int H, int dk, int dv, int chunk, int dtype,
                          void *workspace, size_t workspace_bytes, void *stream);
 
+/* kla_chunk_fwd_varlen with a write-coefficient mode (kla_beta_mode). */
+KLA_API int kla_chunk_fwd_varlen_ex(const void *q, const void *k, const void *v,
+                                    const float *alpha, const float *eta, float eps,
+                                    const float *S0, void *o, float *S_T,
+                                    const int *cu_seqlens, int N, int total_T,
+                                    int H, int dk, int dv, int chunk, int dtype,
+                                    int beta_mode, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
 /*
  * One decode step: one new token for each of B*H (sequence, head) states,
  * updated in place.
@@ -151,6 +183,12 @@ KLA_API int kla_decode_step(const void *q, const void *k, const void *v,
                     const float *alpha, const float *eta, float eps,
                     float *S, void *o, int B, int H, int dk, int dv, int dtype,
                     void *stream);
+
+/* kla_decode_step with a write-coefficient mode (kla_beta_mode). */
+KLA_API int kla_decode_step_ex(const void *q, const void *k, const void *v,
+                               const float *alpha, const float *eta, float eps,
+                               float *S, void *o, int B, int H, int dk, int dv,
+                               int dtype, int beta_mode, void *stream);
 
 /*
  * Size in bytes of the device array that kla_chunk_fwd_noalloc uses as its

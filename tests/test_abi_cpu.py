@@ -142,3 +142,16 @@ def test_binding_raises_on_cpu_tensors():
     q = torch.zeros(1, 64, 1, 64)
     with pytest.raises(ValueError):
         kla.kla_chunk_fwd(q, q, q, torch.ones(1, 64, 1), torch.ones(1, 64, 1), 1e-6)
+
+
+@no_gpu_only
+def test_unknown_beta_mode_is_rejected_before_device_work():
+    lib = binding.load()
+    assert lib.kla_chunk_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1e-6, None, FAKE, None, 1, 64, 1,
+                                64, 64, 64, 0, 2, None, 0, None) == binding.KLA_ERR_INVALID_ARG
+    assert lib.kla_chunk_fwd_varlen_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1e-6, None, FAKE, None, FAKE,
+                                       2, 10, 1, 64, 64, 64, 0, -1, None, 0, None) == \
+        binding.KLA_ERR_INVALID_ARG
+    assert lib.kla_decode_step_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1e-6, FAKE, FAKE, 2, 2, 64, 64, 1,
+                                  9, None) == binding.KLA_ERR_INVALID_ARG
+    assert "beta_mode" in lib.kla_last_error_message().decode()
