@@ -41,6 +41,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kla_oracle.c")
+_SRC_CCQ = os.path.join(_HERE, "ccq_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libkla_oracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -60,12 +61,13 @@ def build(force: bool = False) -> str:
     """Compile kla_oracle.c into libkla_oracle.so next to it (gcc, -O2, no
     fast-math, no host-specific flags so it builds the same on x86 and Arm)."""
     stale = (not os.path.exists(_LIB_PATH)
-             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+             or os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(_SRC),
+                                                  os.path.getmtime(_SRC_CCQ))
              or not _elf_matches_host(_LIB_PATH))
     if force or stale:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-               "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC]
+               "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, _SRC_CCQ]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -86,6 +88,9 @@ def _bind(lib):
     lib.kla_oracle_forward_ex.argtypes = lib.kla_oracle_forward.argtypes + [ctypes.c_int]
     lib.kla_oracle_forward_varlen_ex.restype = ctypes.c_int
     lib.kla_oracle_forward_varlen_ex.argtypes = lib.kla_oracle_forward_varlen.argtypes + [ctypes.c_int]
+    if hasattr(lib, "ccq_oracle_query"):
+        lib.ccq_oracle_query.restype = ctypes.c_int
+        lib.ccq_oracle_query.argtypes = [ctypes.c_int] * 4 + [dp] * 10
     return lib
 
 
@@ -192,3 +197,25 @@ def decode(q, k, v, alpha, eta, eps, S, nthreads: int = 1, beta_mode: str = "kac
                        None if alpha is None else alpha[:, None],
                        eta[:, None], eps, S, nthreads=nthreads, beta_mode=beta_mode)
     return o[:, 0], S_new
+
+
+def ccq_query(q, k, lam, stats0=None):
+    """CCQ read-side contraction (see ccq_oracle.c): q_clean_t = (I - lambda_t
+    Sigma_t) q_t with Sigma_t the running population covariance of the keys up
+    to token t.  q, k: [B,T,H,dk]; lam: [B,T,H]; stats0: None or (Ms [B,H,dk,dk],
+    ms [B,H,dk], ns [B,H]).  Returns (q_clean, (Ms, ms, ns)).  The CCQ layer
+    output is ``forward(q_clean, k, v, ...)``: the write rule is unchanged."""
+    lib = _load()
+    q, k, lam = map(_f64, (q, k, lam))
+    B, T, H, dk = q.shape
+    assert k.shape == q.shape and lam.shape == (B, T, H)
+    M0 = m0 = n0 = None
+    if stats0 is not None:
+        M0, m0, n0 = map(_f64, stats0)
+    qc = np.zeros_like(q)
+    Ms = np.zeros((B, H, dk, dk)); ms = np.zeros((B, H, dk)); ns = np.zeros((B, H))
+    rc = lib.ccq_oracle_query(B, T, H, dk, _ptr(q), _ptr(k), _ptr(lam), _ptr(M0), _ptr(m0),
+                              _ptr(n0), _ptr(qc), _ptr(Ms), _ptr(ms), _ptr(ns))
+    if rc != 0:
+        raise RuntimeError(f"ccq_oracle_query failed rc={rc}")
+    return qc, (Ms, ms, ns)
