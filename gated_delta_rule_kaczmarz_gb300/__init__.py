@@ -6,6 +6,9 @@ draws seeded synthetic inputs.
 """
 from .binding import (  # noqa: F401
     KlaError,
+    kla_ccq_query,
+    kla_ccq_query_step,
+    kla_ccq_query_workspace_size,
     kla_chunk_fwd,
     kla_chunk_fwd_ex,
     kla_chunk_fwd_noalloc,

@@ -88,6 +88,13 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
                                                 I, I, I, I, I, I, I, I, vp, Z, vp]
         lib.kla_decode_step_ex.restype = I
         lib.kla_decode_step_ex.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, I, I, I, I, I, I, vp]
+        lib.kla_ccq_query_workspace_size.restype = Z
+        lib.kla_ccq_query_workspace_size.argtypes = [I, I, I, I, I]
+        lib.kla_ccq_query.restype = I
+        lib.kla_ccq_query.argtypes = [vp, vp, fp, fp, fp, fp, vp, fp, fp, fp,
+                                      I, I, I, I, I, vp, Z, vp]
+        lib.kla_ccq_query_step.restype = I
+        lib.kla_ccq_query_step.argtypes = [vp, vp, fp, fp, fp, fp, vp, I, I, I, I, vp]
         lib.kla_chunk_fwd_noalloc.restype = I
         lib.kla_chunk_fwd_noalloc.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, fp,
                                               I, I, I, I, I, I, I, vp]
@@ -301,3 +308,58 @@ def kla_chunk_fwd_varlen_ex(q, k, v, alpha, eta, eps, cu_seqlens, beta_mode, S0=
 
 def kla_decode_step_ex(q, k, v, alpha, eta, eps, S, beta_mode, **kw):
     return kla_decode_step(q, k, v, alpha, eta, eps, S, beta_mode=beta_mode, **kw)
+
+
+
+def kla_ccq_query_workspace_size(B, T, H, dk, dtype=KLA_DTYPE_BF16) -> int:
+    return int(load().kla_ccq_query_workspace_size(B, T, H, dk, dtype))
+
+
+def kla_ccq_query(q, k, lam, stats0=None, q_clean=None, return_stats=True, workspace=None,
+                  stream=None):
+    """Curvature-Conditioned Query contraction: q_clean = (I - lam Sigma_t) q with
+    Sigma_t the running covariance of the keys.  q, k: [B,T,H,dk]; lam: [B,T,H]
+    fp32; stats0: None or (Ms [B,H,dk,dk], ms [B,H,dk], ns [B,H]) fp32.
+    Returns (q_clean, stats_T); a CCQ layer is kla_chunk_fwd(q_clean, k, ...)."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dt = _dtype_code(q)
+    _need(q, "q"); _need(k, "k", q.dtype, (B, T, H, dk)); _need(lam, "lam", torch.float32, (B, T, H))
+    M0 = m0 = n0 = None
+    if stats0 is not None:
+        M0, m0, n0 = stats0
+        _need(M0, "Ms0", torch.float32, (B, H, dk, dk)); _need(m0, "ms0", torch.float32, (B, H, dk))
+        _need(n0, "ns0", torch.float32, (B, H))
+    if q_clean is None:
+        q_clean = torch.empty_like(q)
+    _need(q_clean, "q_clean", q.dtype, (B, T, H, dk))
+    Ms = ms = ns = None
+    if return_stats:
+        Ms = torch.empty((B, H, dk, dk), dtype=torch.float32, device=q.device)
+        ms = torch.empty((B, H, dk), dtype=torch.float32, device=q.device)
+        ns = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    nbytes = int(lib.kla_ccq_query_workspace_size(B, T, H, dk, dt))
+    workspace, wsb = _workspace(nbytes, q.device, workspace)
+    st = lib.kla_ccq_query(_ptr(q), _ptr(k), _ptr(lam), _ptr(M0), _ptr(m0), _ptr(n0),
+                           _ptr(q_clean), _ptr(Ms), _ptr(ms), _ptr(ns), B, T, H, dk, dt,
+                           _ptr(workspace), wsb, _stream(stream))
+    _check(st)
+    return q_clean, (Ms, ms, ns)
+
+
+def kla_ccq_query_step(q, k, lam, Ms, ms, ns, q_clean=None, stream=None):
+    """One CCQ token per (b, h): the statistics (Ms, ms, ns) are updated in place
+    with k; returns q_clean [B,H,dk]."""
+    lib = load()
+    B, H, dk = q.shape
+    dt = _dtype_code(q)
+    _need(q, "q"); _need(k, "k", q.dtype, (B, H, dk)); _need(lam, "lam", torch.float32, (B, H))
+    _need(Ms, "Ms", torch.float32, (B, H, dk, dk)); _need(ms, "ms", torch.float32, (B, H, dk))
+    _need(ns, "ns", torch.float32, (B, H))
+    if q_clean is None:
+        q_clean = torch.empty_like(q)
+    _need(q_clean, "q_clean", q.dtype, (B, H, dk))
+    st = lib.kla_ccq_query_step(_ptr(q), _ptr(k), _ptr(lam), _ptr(Ms), _ptr(ms), _ptr(ns),
+                                _ptr(q_clean), B, H, dk, dt, _stream(stream))
+    _check(st)
+    return q_clean

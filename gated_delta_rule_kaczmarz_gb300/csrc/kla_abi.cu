@@ -299,6 +299,77 @@ int kla_decode_step(const void *q, const void *k, const void *v, const float *al
                               KLA_BETA_KACZMARZ, stream);
 }
 
+size_t kla_ccq_query_workspace_size(int B, int T, int H, int dk, int dtype) {
+    if (B < 0 || T < 0) return 0;
+    if (check_shape(H, dk, dk, kla::kChunk, dtype) != KLA_OK) return 0;
+    return kla::ccq_workspace_bytes(B, T, H, dk, dtype);
+}
+
+int kla_ccq_query(const void *q, const void *k, const float *lambda, const float *Ms0,
+                  const float *ms0, const float *ns0, void *q_clean, float *Ms_T, float *ms_T,
+                  float *ns_T, int B, int T, int H, int dk, int dtype, void *workspace,
+                  size_t workspace_bytes, void *stream) {
+    if (B < 0 || T < 0) return fail(KLA_ERR_INVALID_ARG, "negative size (B=%d T=%d)", B, T);
+    kla_status st = check_shape(H, dk, dk, kla::kChunk, dtype);
+    if (st != KLA_OK) return st;
+    if ((long)B * T > INT32_MAX || (long)B * H > INT32_MAX)
+        return fail(KLA_ERR_UNSUPPORTED, "problem too large (B*T and B*H must fit in int32)");
+    if ((long)B * T > 0 && (!q || !k || !lambda || !q_clean))
+        return fail(KLA_ERR_INVALID_ARG, "q, k, lambda and q_clean must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(q_clean) || !aligned4(lambda) ||
+        !aligned4(Ms0) || !aligned4(ms0) || !aligned4(ns0) || !aligned4(Ms_T) ||
+        !aligned4(ms_T) || !aligned4(ns_T))
+        return fail(KLA_ERR_INVALID_ARG, "q, k, q_clean must be 16-byte aligned, the rest 4-byte");
+    const size_t need = kla::ccq_workspace_bytes(B, T, H, dk, dtype);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+        return fail(KLA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (inject_launch_fault()) return fail(KLA_ERR_CUDA, "injected launch fault (KLA_FAULT_INJECT)");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if ((long)B * T == 0) {
+        // no tokens: the statistics pass through
+        const size_t nM = (size_t)B * H * dk * dk, nm = (size_t)B * H * dk, nn = (size_t)B * H;
+        if (Ms_T && e == cudaSuccess)
+            e = Ms0 ? cudaMemcpyAsync(Ms_T, Ms0, nM * 4, cudaMemcpyDeviceToDevice, s)
+                    : cudaMemsetAsync(Ms_T, 0, nM * 4, s);
+        if (ms_T && e == cudaSuccess)
+            e = ms0 ? cudaMemcpyAsync(ms_T, ms0, nm * 4, cudaMemcpyDeviceToDevice, s)
+                    : cudaMemsetAsync(ms_T, 0, nm * 4, s);
+        if (ns_T && e == cudaSuccess)
+            e = ns0 ? cudaMemcpyAsync(ns_T, ns0, nn * 4, cudaMemcpyDeviceToDevice, s)
+                    : cudaMemsetAsync(ns_T, 0, nn * 4, s);
+        if (e != cudaSuccess) return cuda_fail(e, "statistics copy");
+        return ok();
+    }
+    kla::CcqProblem p{};
+    p.q = q; p.k = k; p.lambda = lambda; p.Ms0 = Ms0; p.ms0 = ms0; p.ns0 = ns0;
+    p.q_clean = q_clean; p.Ms_T = Ms_T; p.ms_T = ms_T; p.ns_T = ns_T;
+    p.B = B; p.T = T; p.H = H; p.d = dk; p.dtype = dtype; p.ws = workspace;
+    e = kla::launch_ccq(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ccq launch");
+    return ok();
+}
+
+int kla_ccq_query_step(const void *q, const void *k, const float *lambda, float *Ms, float *ms,
+                       float *ns, void *q_clean, int B, int H, int dk, int dtype, void *stream) {
+    if (B < 0) return fail(KLA_ERR_INVALID_ARG, "negative batch");
+    kla_status st = check_shape(H, dk, dk, kla::kChunk, dtype);
+    if (st != KLA_OK) return st;
+    if (B == 0) return ok();
+    if (!q || !k || !lambda || !Ms || !ms || !ns || !q_clean)
+        return fail(KLA_ERR_INVALID_ARG, "all pointers must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(q_clean) || !aligned4(lambda) ||
+        !aligned4(Ms) || !aligned4(ms) || !aligned4(ns))
+        return fail(KLA_ERR_INVALID_ARG, "q, k, q_clean must be 16-byte aligned, the rest 4-byte");
+    if ((long)B * H > INT32_MAX) return fail(KLA_ERR_UNSUPPORTED, "B*H too large");
+    if (inject_launch_fault()) return fail(KLA_ERR_CUDA, "injected launch fault (KLA_FAULT_INJECT)");
+    cudaError_t e = kla::launch_ccq_step(q, k, lambda, Ms, ms, ns, q_clean, B * H, dk, dtype,
+                                         static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ccq step launch");
+    return ok();
+}
+
 int kla_workspace_status(const void *workspace, size_t workspace_bytes, void *stream) {
     if (workspace == nullptr || workspace_bytes < kla::kWsHeader) return ok();
     cudaStream_t s = static_cast<cudaStream_t>(stream);

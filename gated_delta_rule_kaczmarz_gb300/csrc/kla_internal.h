@@ -55,6 +55,23 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v,
                           float *S, void *o, int BH, int d, int dtype, int beta_mode,
                           cudaStream_t s);
 
+// CCQ query contraction (kla_ccq.cu): q_clean for a fixed-length batch, and
+// the one-token step with the statistics updated in place.
+struct CcqProblem {
+    const void *q, *k;
+    const float *lambda;
+    const float *Ms0, *ms0, *ns0;   // initial statistics or nullptr (zero)
+    void *q_clean;
+    float *Ms_T, *ms_T, *ns_T;      // final statistics or nullptr
+    int B, T, H, d, dtype;
+    void *ws;                       // ccq_workspace_bytes(B, T, H, d, dtype)
+};
+size_t ccq_workspace_bytes(int B, int T, int H, int d, int dtype);
+cudaError_t launch_ccq(const CcqProblem &p, cudaStream_t s);
+cudaError_t launch_ccq_step(const void *q, const void *k, const float *lambda, float *Ms,
+                            float *ms, float *ns, void *q_clean, int BH, int d, int dtype,
+                            cudaStream_t s);
+
 // Tensor-core (tcgen05) prefill for bf16, d = 128.
 size_t chunk_tc_workspace_bytes(long n_chunks_upper, int H, int n_seq);
 bool chunk_tc_supported(int d, int dtype);

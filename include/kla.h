@@ -223,6 +223,45 @@ KLA_API int kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                                   int dtype, void *stream);
 
 /*
+ * Curvature-Conditioned Query (CCQ) read-side contraction ("Don't Read
+ * Everything: A Curvature-Conditioned Query for Linear Attention",
+ * gist.science 2606.01294, sections "O Mecanismo" and "Integracao"):
+ *
+ *     Sigma_t   = M_t / n_t - mu_t mu_t^T,   mu_t = m_t / n_t
+ *     q_clean_t = q_t - lambda_t Sigma_t q_t
+ *
+ * with the running statistics of the keys of each (sequence, head) up to and
+ * including token t: M_t = sum k k^T (dk x dk), m_t = sum k (dk), n_t =
+ * count.  The write rule is unchanged and the read is o_t = S_t^T q_clean_t,
+ * so a CCQ layer is kla_chunk_fwd / kla_decode_step called with q_clean in
+ * place of q.
+ *   q, k, q_clean : [B, T, H, dk] dtype     lambda : [B, T, H] fp32 gate
+ *   Ms0, Ms_T     : [B, H, dk, dk] fp32 (symmetric), ms0, ms_T : [B, H, dk],
+ *   ns0, ns_T     : [B, H] fp32 counts; the initial statistics may be NULL
+ *                   (zero), the final ones NULL (not needed).  Ms_T may not
+ *                   alias Ms0 (likewise ms, ns).
+ *   workspace     : kla_ccq_query_workspace_size(...) bytes (per chunk the
+ *                   statistics that precede it), owned by the caller.
+ * dk in {64, 128}.  Arithmetic fp32; the per-chunk M is stored in the input
+ * dtype.
+ */
+KLA_API size_t kla_ccq_query_workspace_size(int B, int T, int H, int dk, int dtype);
+KLA_API int kla_ccq_query(const void *q, const void *k, const float *lambda,
+                          const float *Ms0, const float *ms0, const float *ns0,
+                          void *q_clean, float *Ms_T, float *ms_T, float *ns_T,
+                          int B, int T, int H, int dk, int dtype,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * One CCQ token per (b, h) for decoding: the statistics Ms [B, H, dk, dk],
+ * ms [B, H, dk], ns [B, H] (fp32) are updated in place with k, then q_clean
+ * [B, H, dk] = q - lambda Sigma q.  q, k: [B, H, dk]; lambda: [B, H].
+ */
+KLA_API int kla_ccq_query_step(const void *q, const void *k, const float *lambda, float *Ms,
+                               float *ms, float *ns, void *q_clean, int B, int H, int dk,
+                               int dtype, void *stream);
+
+/*
  * Synchronises `stream` and returns the status that the last prefill call
  * using `workspace` recorded on the device: KLA_OK, KLA_ERR_INVALID_ARG
  * (cu_seqlens rejected) or KLA_ERR_TIMEOUT.  A workspace of 0 bytes (NULL)

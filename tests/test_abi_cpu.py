@@ -155,3 +155,23 @@ def test_unknown_beta_mode_is_rejected_before_device_work():
     assert lib.kla_decode_step_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1e-6, FAKE, FAKE, 2, 2, 64, 64, 1,
                                   9, None) == binding.KLA_ERR_INVALID_ARG
     assert "beta_mode" in lib.kla_last_error_message().decode()
+
+
+@no_gpu_only
+def test_ccq_host_validation():
+    lib = binding.load()
+    f = lib.kla_ccq_query
+    # dk 96 unsupported
+    assert f(FAKE, FAKE, FAKE, None, None, None, FAKE, None, None, None, 1, 64, 1, 96, 1,
+             None, 0, None) == binding.KLA_ERR_UNSUPPORTED
+    # missing q
+    assert f(None, FAKE, FAKE, None, None, None, FAKE, None, None, None, 1, 64, 1, 64, 1,
+             None, 0, None) == binding.KLA_ERR_INVALID_ARG
+    # missing workspace
+    assert f(FAKE, FAKE, FAKE, None, None, None, FAKE, None, None, None, 1, 64, 1, 64, 1,
+             None, 0, None) == binding.KLA_ERR_WORKSPACE
+    assert lib.kla_ccq_query_workspace_size(1, 64, 1, 64, 1) > 0
+    g = lib.kla_ccq_query_step
+    assert g(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 2, 2, 64, 1, None) == \
+        binding.KLA_ERR_INVALID_ARG
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 2, 64, 1, None) == binding.KLA_OK

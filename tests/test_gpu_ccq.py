@@ -1,0 +1,83 @@
+"""GPU parity of the CCQ query contraction (kla_ccq_query, kla_ccq_query_step)
+and of a whole CCQ layer (the KLA forward on q_clean) against the fp64
+oracle; error measure max|gpu - oracle| / max|oracle|, 1e-4 (fp32) and 2e-2
+(bf16)."""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_kaczmarz_gb300 as kla
+import oracle
+from gated_delta_rule_kaczmarz_gb300.workloads import prefill_inputs
+from tests._util import TOL, cuda, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _lam(shape, seed):
+    rng = np.random.default_rng(seed)
+    return torch.from_numpy((1.0 / (1.0 + np.exp(-rng.standard_normal(shape)))).astype(np.float32))
+
+
+def _stats(B, H, d, seed):
+    rng = np.random.default_rng(seed)
+    K = rng.standard_normal((B, H, 50, d)) / np.sqrt(d)
+    Ms = np.einsum("bhti,bhtj->bhij", K, K).astype(np.float32)
+    ms = K.sum(2).astype(np.float32)
+    ns = np.full((B, H), 50.0, np.float32)
+    return tuple(torch.from_numpy(x) for x in (Ms, ms, ns))
+
+
+@pytest.mark.parametrize("B,T,H,d,dtype,with_stats", [
+    (2, 200, 2, 64, "fp32", False), (1, 130, 2, 128, "fp32", True),
+    (2, 257, 2, 128, "bf16", False), (1, 64, 3, 128, "bf16", True), (2, 1, 2, 64, "bf16", True)])
+def test_ccq_query_parity(B, T, H, d, dtype, with_stats):
+    inp = prefill_inputs(B, T, H, d, d, dtype, seed=120 + T)
+    lam = _lam((B, T, H), 7)
+    st0 = _stats(B, H, d, 8) if with_stats else None
+    g = cuda(inp)
+    qc, (Ms, ms, ns) = kla.kla_ccq_query(g["q"], g["k"], lam.cuda(),
+                                         None if st0 is None else tuple(x.cuda() for x in st0))
+    torch.cuda.synchronize()
+    qc_ref, (Ms_ref, ms_ref, ns_ref) = oracle.ccq_query(inp["q"], inp["k"], lam, st0)
+    tol = TOL[inp["q"].dtype]
+    assert rel_err(qc, qc_ref) <= tol
+    assert rel_err(Ms, Ms_ref) <= 1e-5 and rel_err(ms, ms_ref) <= 1e-5
+    assert np.array_equal(ns.cpu().numpy(), ns_ref)
+
+
+def test_ccq_layer_end_to_end():
+    """A CCQ-KLA layer: q_clean on the GPU, then the tensor-core forward on it,
+    against the oracle's q_clean and forward."""
+    inp = prefill_inputs(2, 256, 2, 128, 128, "bf16", seed=130, s0_var=0.01)
+    lam = _lam((2, 256, 2), 9)
+    g = cuda(inp)
+    qc, _ = kla.kla_ccq_query(g["q"], g["k"], lam.cuda())
+    o, S = kla.kla_chunk_fwd(qc, g["k"], g["v"], g["alpha"], g["eta"], g["eps"], g["S0"])
+    torch.cuda.synchronize()
+    qc_ref, _ = oracle.ccq_query(inp["q"], inp["k"], lam)
+    o_ref, S_ref = oracle.forward(qc_ref, inp["k"], inp["v"], inp["alpha"], inp["eta"],
+                                  inp["eps"], inp["S0"], nthreads=8)
+    assert rel_err(o, o_ref) <= 2e-2
+    assert rel_err(S, S_ref) <= 2e-2
+
+
+@pytest.mark.parametrize("d,dtype", [(64, "fp32"), (128, "bf16")])
+def test_ccq_step_equals_prefill(d, dtype):
+    """Token-by-token CCQ steps from given statistics equal the chunked pass."""
+    B, T, H = 2, 9, 3
+    inp = prefill_inputs(B, T, H, d, d, dtype, seed=140 + d)
+    lam = _lam((B, T, H), 10)
+    st0 = _stats(B, H, d, 11)
+    g = cuda(inp)
+    Ms, ms, ns = (x.cuda().clone() for x in st0)
+    outs = []
+    for t in range(T):
+        outs.append(kla.kla_ccq_query_step(g["q"][:, t].contiguous(), g["k"][:, t].contiguous(),
+                                           lam[:, t].contiguous().cuda(), Ms, ms, ns))
+    torch.cuda.synchronize()
+    qc_ref, (Ms_ref, ms_ref, ns_ref) = oracle.ccq_query(inp["q"], inp["k"], lam, st0)
+    tol = TOL[inp["q"].dtype]
+    assert rel_err(torch.stack(outs, 1), qc_ref) <= tol
+    assert rel_err(Ms, Ms_ref) <= 1e-5
+    assert np.array_equal(ns.cpu().numpy(), ns_ref)
