@@ -11,7 +11,10 @@ reports it under "decode".
 
 Timing: CUDA events on the launching stream around each step; L2 is flushed
 (256 MiB write) between timed prefill steps, outside the events; the decode
-state (268 MB) is larger than L2.  For N > 1 (torchrun) every rank runs its
+state (268 MB) is larger than L2.  The end-to-end figure copies every step's
+inputs from pinned host memory and its outputs back, pipelined over two
+device buffer sets (copies in, compute and copies out of consecutive steps
+overlap on three streams); it is the total time of all steps / steps.  For N > 1 (torchrun) every rank runs its
 own replica; times are max-reduced over ranks and value = total tokens / time.
 The reference arm (--impl reference) times the fp64 CPU oracle on the host.
 """
@@ -234,29 +237,58 @@ def time_prefill(args, world, dev):
     times = [a.elapsed_time(b) for a, b in evs]
     barrier(world)
 
-    # end to end through the public API from pinned host buffers
+    # end to end through the public API from pinned host buffers: every step
+    # copies its own inputs (q, k, v, alpha, eta, S0) in and its outputs (o,
+    # S_T) out.  Steps are pipelined over two device buffer sets: step i+1's
+    # inputs and step i-1's outputs move on their own streams while step i
+    # computes (the L2 flush stays on the compute stream before every step).
     host = {n: (x.pin_memory() if isinstance(x, torch.Tensor) else x) for n, x in inp_cpu.items()}
-    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    S_h = torch.empty(S_T.shape, dtype=S_T.dtype).pin_memory()
     names = ("q", "k", "v", "alpha", "eta", "S0")
+    nb = 2
+    dbuf = [{n: torch.empty_like(g[n]) for n in names} for _ in range(nb)]
+    obuf = [(torch.empty_like(o), torch.empty_like(S_T)) for _ in range(nb)]
+    hout = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+             torch.empty(S_T.shape, dtype=S_T.dtype).pin_memory()) for _ in range(nb)]
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
-    d2h = o_h.numel() * o_h.element_size() + S_h.numel() * S_h.element_size()
-    e2e_evs = []
-    for _ in range(args.steps):
-        flush.zero_()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for n in names:
-            g[n].copy_(host[n], non_blocking=True)
-        step()
-        o_h.copy_(o, non_blocking=True)
-        S_h.copy_(S_T, non_blocking=True)
-        e1.record(stream)
-        e2e_evs.append((e0, e1))
+    d2h = o.numel() * o.element_size() + S_T.numel() * S_T.element_size()
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(nb)]
+    ev_done = [torch.cuda.Event() for _ in range(nb)]
+    ev_out = [torch.cuda.Event() for _ in range(nb)]
     torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(s_in)
+    stream.wait_event(t_start)
+    s_out.wait_event(t_start)
+    for i in range(args.steps):
+        bi = i % nb
+        if i >= nb:
+            s_in.wait_event(ev_done[bi])          # step i-2 finished reading these inputs
+        with torch.cuda.stream(s_in):
+            for n in names:
+                dbuf[bi][n].copy_(host[n], non_blocking=True)
+            ev_in[bi].record(s_in)
+        stream.wait_event(ev_in[bi])
+        if i >= nb:
+            stream.wait_event(ev_out[bi])         # step i-2's outputs have left
+        flush.zero_()
+        d = dbuf[bi]
+        kla.kla_chunk_fwd(d["q"], d["k"], d["v"], d["alpha"], d["eta"], wl.eps, d["S0"],
+                          o=obuf[bi][0], S_T=obuf[bi][1], workspace=ws, stream=stream)
+        ev_done[bi].record(stream)
+        s_out.wait_event(ev_done[bi])
+        with torch.cuda.stream(s_out):
+            hout[bi][0].copy_(obuf[bi][0], non_blocking=True)
+            hout[bi][1].copy_(obuf[bi][1], non_blocking=True)
+            ev_out[bi].record(s_out)
+    s_out.wait_stream(stream)
+    s_out.wait_stream(s_in)
+    t_end.record(s_out)
+    torch.cuda.synchronize()
+    e2e_total_ms = t_start.elapsed_time(t_end)
+    e2e_times = [e2e_total_ms / args.steps] * args.steps
     clocks = sampler.stop()
-    e2e_times = [a.elapsed_time(b) for a, b in e2e_evs]
     return dict(wl=wl, times=times, e2e_times=e2e_times, h2d=h2d, d2h=d2h, launches=launches,
                 clocks=clocks, inp_cpu=inp_cpu, kernels_per_call=launches / max(1, args.steps))
 
