@@ -70,7 +70,8 @@ struct TcParams {
     __nv_bfloat16 *U_ws;       // [slots][64][128]   U~
     __nv_bfloat16 *A_ws;       // [slots][64 keys s][64 queries t]  A^T
     int beta_mode;             // 0: beta = eta / (||k||^2 + eps); 1: beta = eta
-    unsigned *flags;           // fused launch: one ready flag per work item (zeroed per call)
+    unsigned *flags;           // fused launch: one ready flag per work item, then the work-item
+                               // counter (all zeroed per call)
     int n_units;               // fused launch: sequences x heads
 };
 
@@ -262,6 +263,7 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + P1_SMALL);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P1_SMALL + 32);
     volatile int *sAbort = reinterpret_cast<volatile int *>(sm + P1_SMALL + 36);
+    volatile long *sItem = reinterpret_cast<volatile long *>(sm + P1_SMALL + 40);
     float *sCarry = reinterpret_cast<float *>(sm + P1_SMALL + 48);
     float *sG = reinterpret_cast<float *>(sm + P1_SMALL + 64);   // g of each token row
     float *sG2 = sG + 128;                                         // g * log2(e)
@@ -291,7 +293,17 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     const long n_items = n_pairs * p.H;
     uint32_t ph = 0;      // mbarrier phase parity of this worker's current item
     long pending = -1;    // fused: item written but not yet published (thread 0)
-    for (long item = item0; item < n_items; item += step) {
+    // Work items: item0, item0 + step, ...; or, with step == 0, items item0 +
+    // (a global counter's next value), handed out in order as workers free up
+    // (the fused launch: a late item then delays only its own unit).
+    for (long item = item0;; item += step) {
+    if (step == 0) {
+        if (tid0 == 0) *sItem = item0 + (long)atomicAdd(p.flags + n_items, 1u);
+        named_sync(bar, P1_THREADS);
+        item = *sItem;
+        named_sync(bar, P1_THREADS);
+    }
+    if (item >= n_items) break;
     // The thread index is re-read through an opaque move every item so that
     // the compiler does not hoist (and keep live) the many thread-dependent
     // shared-memory addresses across items.
@@ -1039,8 +1051,12 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 // [0, n_state) run the state pass (two per unit); every other CTA runs two
 // phase-1 workers over the work items in chunk-pair-major order, so that the
 // state pass consumes chunk pairs as they are published instead of waiting
-// for the whole of phase 1.  Only the consumer waits (bounded), and every CTA
-// is resident (cooperative launch), so the hand-off cannot deadlock.
+// for the whole of phase 1.  The state-pass CTAs first compute the first two
+// chunk pairs of their own unit themselves (CTA 2u pair 0, CTA 2u + 1 pair
+// 1), which they would otherwise wait for, and then start the chain; the
+// workers take the items from pair 2 on.  Only the consumer waits (bounded),
+// and every CTA is resident (cooperative launch), so the hand-offs cannot
+// deadlock.
 constexpr int FU_THREADS = 2 * P1_THREADS;
 static_assert(FU_THREADS >= P2_THREADS, "fused block size");
 constexpr uint32_t FU_SMEM = P2_SMEM > 2 * P1_REGION + 1024 ? P2_SMEM : 2 * P1_REGION + 1024;
@@ -1053,14 +1069,19 @@ fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     extern __shared__ unsigned char smraw[];
     unsigned char *sm = align1024(smraw);
     const int tid = (int)threadIdx.x;
+    const long n_items = n_pairs * p.H;
+    const int pre = p.nch_fixed >= 4 ? 2 : 1;   // leading chunk pairs done by the state CTAs
     if ((int)blockIdx.x < n_state) {
+        const int unit = (int)blockIdx.x >> 1, jh = (int)blockIdx.x & 1;
+        if (jh < pre && tid < P1_THREADS)
+            intra_run<true>(&mq, &mk, &mv, &mw, &mu, p, n_pairs, sm, tid, 1,
+                            (long)jh * p.n_units + unit, n_items);
         if (tid < P2_THREADS) state_run<true>(&mq, &mk, &mw, &mu, &ma, p, sm, (int)blockIdx.x, tid);
         return;
     }
     const int w = tid / P1_THREADS;
-    const long n_workers = 2L * ((long)gridDim.x - n_state);
     intra_run<true>(&mq, &mk, &mv, &mw, &mu, p, n_pairs, sm + w * P1_REGION, tid % P1_THREADS,
-                    1 + w, 2L * ((long)blockIdx.x - n_state) + w, n_workers);
+                    1 + w, (long)pre * p.n_units, 0);   // items from the shared counter
 }
 
 // ===================================================================== varlen prep
@@ -1185,7 +1206,7 @@ struct WsLayout {
 WsLayout layout(long n_chunks, int H, int n_seq) {
     const size_t slots = (size_t)n_chunks * H;
     // meta: the varlen chunk table and order, or the fused launch's ready flags
-    const size_t meta_ints = std::max((size_t)2 * n_seq + 1, (size_t)((n_chunks + 1) / 2) * H);
+    const size_t meta_ints = std::max((size_t)2 * n_seq + 1, (size_t)((n_chunks + 1) / 2) * H + 1);
     WsLayout L;
     L.meta = 0;
     L.g = align_up(meta_ints * sizeof(int), 1024);
@@ -1209,7 +1230,8 @@ bool use_fused(const Problem &p) {
 bool chunk_tc_supported(int d, int dtype) { return d == 128 && dtype == 1; }
 
 size_t chunk_tc_reset_bytes(const Problem &p, long n_chunks_upper) {
-    return use_fused(p) ? (size_t)((n_chunks_upper + 1) / 2) * p.H * sizeof(unsigned) : 0;
+    // the ready flags and the work-item counter after them
+    return use_fused(p) ? ((size_t)((n_chunks_upper + 1) / 2) * p.H + 1) * sizeof(unsigned) : 0;
 }
 
 size_t chunk_tc_workspace_bytes(long n_chunks_upper, int H, int n_seq) {
