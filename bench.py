@@ -333,6 +333,61 @@ def time_decode(args, dev, reps):
                 bytes_per_launch=bytes_per_launch)
 
 
+def time_ccq(args, dev, reps):
+    """CCQ read-side contraction on the layer workload (bf16, B4 H8 T2048
+    d128, lambda ~ sigmoid(N(0,1))): kla_ccq_query alone, and a whole CCQ
+    layer (kla_ccq_query then kla_chunk_fwd on q_clean).  Inputs resident, L2
+    flushed between timed calls."""
+    import numpy as np
+    import torch
+
+    import gated_delta_rule_kaczmarz_gb300 as kla
+    from gated_delta_rule_kaczmarz_gb300.workloads import WORKLOADS
+
+    wl = WORKLOADS["layer_prefill"]
+    inp = wl.make()
+    g = {n: (x.to(dev) if isinstance(x, torch.Tensor) else x) for n, x in inp.items()}
+    rng = np.random.default_rng(5)
+    lam = torch.from_numpy((1.0 / (1.0 + np.exp(-rng.standard_normal((wl.B, wl.T, wl.H)))))
+                           .astype(np.float32)).to(dev)
+    qc = torch.empty_like(g["q"])
+    ws = torch.empty(max(1, kla.kla_ccq_query_workspace_size(wl.B, wl.T, wl.H, wl.d)),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def query():
+        kla.kla_ccq_query(g["q"], g["k"], lam, q_clean=qc, return_stats=False, workspace=ws,
+                          stream=stream)
+
+    def layer():
+        query()
+        kla.kla_chunk_fwd(qc, g["k"], g["v"], g["alpha"], g["eta"], wl.eps, g["S0"],
+                          stream=stream)
+
+    out = {}
+    for name, f in (("query", query), ("layer", layer)):
+        for _ in range(2):
+            f()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            f()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        out[name] = sum(ms) / len(ms)
+    th = wl.B * wl.T * wl.H
+    # fp32 CUDA-core work of the query (d = 128, chunk 64): M_prev q (2 d^2), the
+    # in-chunk key products and sums (about 4 * 32 * d on average) and the
+    # per-token share of K^T K (2 d^2), in flop per token-head
+    flop = th * (2 * wl.d * wl.d + 4 * 32 * wl.d + 2 * wl.d * wl.d)
+    return dict(wl=wl, query_ms=out["query"], layer_ms=out["layer"], flop=flop)
+
+
 def ours(args):
     import torch
     world, rank, local = dist_env()
@@ -372,6 +427,17 @@ def ours(args):
                            "traffic": TRAFFIC_DECODE, "kernel": "decode_kernel",
                            "algorithmic_bytes_per_launch": dec["bytes_per_launch"]}}
 
+    cq = time_ccq(args, dev, reps=5)
+    fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12     # TFLOP/s: SMs x FP32 lanes x FMA x max clock
+    ccq = {"workload": "layer_prefill with the CCQ read (lambda ~ sigmoid(N(0,1)))",
+           "query_us": cq["query_ms"] * 1e3, "layer_us": cq["layer_ms"] * 1e3,
+           "layer_value": wl.B * wl.T / (cq["layer_ms"] / 1e3), "unit": "tokens/s",
+           "roofline": {"bound": "alu", "achieved": cq["flop"] / (cq["query_ms"] / 1e3) / 1e12,
+                        "peak": fp32_peak, "unit": "TFLOP/s",
+                        "frac": cq["flop"] / (cq["query_ms"] / 1e3) / 1e12 / fp32_peak,
+                        "traffic": None, "kernel": "ccq_prefix_kernel + ccq_query_kernel",
+                        "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz"}}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
@@ -397,6 +463,7 @@ def ours(args):
         "gpu_launches": pre["launches"],
         "clocks": pre["clocks"],
         "decode": decode,
+        "ccq": ccq,
     }
     if rank == 0:
         print(json.dumps(line))

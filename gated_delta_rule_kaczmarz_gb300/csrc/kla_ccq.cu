@@ -60,6 +60,19 @@ ccq_prefix_kernel(const Tin *__restrict__ k, const float *__restrict__ Ms0,
         acc[x] = Ms0 ? Ms0[(unit * D + i) * D + cg * CPT + x] : 0.f;
     float msum = 0.f;   // m[row0 + tid] for tid < RB
     if (tid < RB) msum = ms0 ? ms0[unit * D + row0 + tid] : 0.f;
+    // chunk keys go through registers: the next chunk's loads are in flight
+    // while the current chunk is accumulated
+    constexpr int LPT = CC * D / CQ_THREADS;   // key values per thread and chunk
+    float pre[LPT];
+    auto load_chunk = [&](int cc) {
+#pragma unroll
+        for (int x = 0; x < LPT; ++x) {
+            const int e = tid + x * CQ_THREADS, t = e / D, j = e % D;
+            const int tok = cc * CC + t;
+            pre[x] = (cc < nch && tok < T) ? ldf(k, (((size_t)b * T + tok) * H + h) * D + j) : 0.f;
+        }
+    };
+    load_chunk(0);
     for (int c = 0; c < nch; ++c) {
         // statistics before chunk c
         Tin *dst = Mprev + (((size_t)unit * nch + c) * D + i) * D + cg * CPT;
@@ -67,12 +80,13 @@ ccq_prefix_kernel(const Tin *__restrict__ k, const float *__restrict__ Ms0,
         for (int x = 0; x < CPT; ++x) stf(dst, x, acc[x]);
         if (tid < RB) mprev[((size_t)unit * nch + c) * D + row0 + tid] = msum;
         __syncthreads();   // previous chunk's keys no longer read
-        for (int e = tid; e < CC * D; e += CQ_THREADS) {
-            const int t = e / D, j = e % D;
-            const int tok = c * CC + t;
-            Ks[t][j] = tok < T ? ldf(k, (((size_t)b * T + tok) * H + h) * D + j) : 0.f;
+#pragma unroll
+        for (int x = 0; x < LPT; ++x) {
+            const int e = tid + x * CQ_THREADS;
+            Ks[e / D][e % D] = pre[x];
         }
         __syncthreads();
+        load_chunk(c + 1);
 #pragma unroll 4
         for (int t = 0; t < CC; ++t) {
             const float ki = Ks[t][i];
@@ -98,11 +112,14 @@ ccq_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                  int nch, const Tin *__restrict__ Mprev,
                  const float *__restrict__ mprev, Tin *__restrict__ q_clean) {
     constexpr int DPT = D / 4;   // dims per thread
+    // rows padded to an odd stride so that lanes walking different rows hit
+    // different banks
+    constexpr int LD = D + 1;
     extern __shared__ float smq[];
-    float *Ks = smq;                 // [CC][D]
-    float *Qs = Ks + CC * D;         // [CC][D]
-    float *MT = Qs + CC * D;         // [D][D], MT[j][i] = M_prev[i][j]
-    float *Dm = MT + D * D;          // [CC][CC + 1]: k_j . q_t for j <= t, else 0
+    float *Ks = smq;                 // [CC][LD]
+    float *Qs = Ks + CC * LD;        // [CC][LD]
+    float *MT = Qs + CC * LD;        // [D][LD], MT[j][i] = M_prev[i][j]
+    float *Dm = MT + D * LD;         // [CC][CC + 1]: k_j . q_t for j <= t, else 0
     const int tid = threadIdx.x;
     const int c = blockIdx.x;
     const long unit = blockIdx.y;
@@ -111,20 +128,20 @@ ccq_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         const int t = e / D, j = e % D;
         const int tok = c * CC + t;
         const size_t g = (((size_t)b * T + tok) * H + h) * D + j;
-        Ks[e] = tok < T ? ldf(k, g) : 0.f;
-        Qs[e] = tok < T ? ldf(q, g) : 0.f;
+        Ks[t * LD + j] = tok < T ? ldf(k, g) : 0.f;
+        Qs[t * LD + j] = tok < T ? ldf(q, g) : 0.f;
     }
     const Tin *Mp = Mprev + ((size_t)unit * nch + c) * D * D;
     for (int e = tid; e < D * D; e += CQ_THREADS) {
         const int i = e / D, j = e % D;
-        MT[j * D + i] = ldf(Mp, e);
+        MT[j * LD + i] = ldf(Mp, e);
     }
     __syncthreads();
     for (int e = tid; e < CC * CC; e += CQ_THREADS) {
         const int t = e / CC, j = e % CC;
         float d = 0.f;
         if (j <= t)
-            for (int x = 0; x < D; ++x) d = fmaf(Ks[j * D + x], Qs[t * D + x], d);
+            for (int x = 0; x < D; ++x) d = fmaf(Ks[j * LD + x], Qs[t * LD + x], d);
         Dm[t * (CC + 1) + j] = d;
     }
     __syncthreads();
@@ -138,16 +155,16 @@ ccq_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         mc[x] = mprev[((size_t)unit * nch + c) * D + i0 + x];
     }
     for (int j = 0; j < D; ++j) {          // M_prev q_t
-        const float qj = Qs[t * D + j];
+        const float qj = Qs[t * LD + j];
 #pragma unroll
-        for (int x = 0; x < DPT; ++x) y[x] = fmaf(MT[j * D + i0 + x], qj, y[x]);
+        for (int x = 0; x < DPT; ++x) y[x] = fmaf(MT[j * LD + i0 + x], qj, y[x]);
     }
     for (int j = 0; j < CC; ++j) {         // keys of this chunk up to t (Dm is 0 past t)
         const float d = Dm[t * (CC + 1) + j];
         const float on = j <= t ? 1.f : 0.f;
 #pragma unroll
         for (int x = 0; x < DPT; ++x) {
-            const float kv = Ks[j * D + i0 + x];
+            const float kv = Ks[j * LD + i0 + x];
             y[x] = fmaf(kv, d, y[x]);
             mc[x] = fmaf(kv, on, mc[x]);
         }
@@ -156,7 +173,7 @@ ccq_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     const float inv_n = 1.f / n;
     float muq = 0.f;
 #pragma unroll
-    for (int x = 0; x < DPT; ++x) muq = fmaf(mc[x] * inv_n, Qs[t * D + i0 + x], muq);
+    for (int x = 0; x < DPT; ++x) muq = fmaf(mc[x] * inv_n, Qs[t * LD + i0 + x], muq);
     muq += __shfl_xor_sync(0xffffffffu, muq, 1);
     muq += __shfl_xor_sync(0xffffffffu, muq, 2);
     if (tok < T) {
@@ -165,7 +182,7 @@ ccq_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll
         for (int x = 0; x < DPT; ++x) {
             const float sq = y[x] * inv_n - (mc[x] * inv_n) * muq;
-            stf(q_clean, g + x, Qs[t * D + i0 + x] - lam * sq);
+            stf(q_clean, g + x, Qs[t * LD + i0 + x] - lam * sq);
         }
     }
 }
@@ -183,7 +200,7 @@ cudaError_t launch_ccq_t(const CcqProblem &p, cudaStream_t s) {
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const size_t smem = (size_t)(2 * CC * D + D * D + CC * (CC + 1)) * sizeof(float);
+    const size_t smem = (size_t)(2 * CC * (D + 1) + D * (D + 1) + CC * (CC + 1)) * sizeof(float);
     static bool attr = false;
     if (!attr) {
         if ((e = cudaFuncSetAttribute(ccq_query_kernel<Tin, D>,

@@ -171,7 +171,7 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, i
     // M = L21 D1
 #pragma unroll
     for (int m = 0; m < rows; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
-#pragma unroll
+#pragma unroll 2
     for (int s4 = 0; s4 < n / 4; ++s4) {
         float4 bb[4];
 #pragma unroll
@@ -201,7 +201,7 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, i
     }
     named_sync(bar, P1_THREADS);  // M complete; L21 no longer read
     // X = -D2 M, written over L21
-#pragma unroll
+#pragma unroll 2
     for (int s4 = 0; s4 < n / 4; ++s4) {
         float4 bb[4];
 #pragma unroll
@@ -506,7 +506,7 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
         // products.
         const bool live = t < nc;
         const float gam_t = live ? ex2_approx(gt2) : 0.f;
-#pragma unroll
+#pragma unroll 2
         for (int ch = 0; ch < 8; ++ch) {
             uint4 *pk4 = reinterpret_cast<uint4 *>(KQ + hf * 32768 + sw128_offset(r, ch * 8));
             const uint4 v = *pk4;
