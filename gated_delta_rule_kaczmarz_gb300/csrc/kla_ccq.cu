@@ -41,7 +41,8 @@ __device__ __forceinline__ void stf(float *p, size_t i, float x) { p[i] = x; }
 __device__ __forceinline__ void stf(__nv_bfloat16 *p, size_t i, float x) { p[i] = __float2bfloat16_rn(x); }
 
 // grid (D / RB, B * H); 256 threads: thread (r = tid / 16, cg = tid % 16)
-// owns M[row0 + r][cg * D/16 .. +D/16).
+// owns M[row0 + r][cg + 16 x], x < D/16 (interleaved, so that the 16 lanes
+// reading one key row hit 16 banks).
 template <typename Tin, int D>
 __global__ void __launch_bounds__(CQ_THREADS)
 ccq_prefix_kernel(const Tin *__restrict__ k, const float *__restrict__ Ms0,
@@ -57,7 +58,7 @@ ccq_prefix_kernel(const Tin *__restrict__ k, const float *__restrict__ Ms0,
     float acc[CPT];
 #pragma unroll
     for (int x = 0; x < CPT; ++x)
-        acc[x] = Ms0 ? Ms0[(unit * D + i) * D + cg * CPT + x] : 0.f;
+        acc[x] = Ms0 ? Ms0[(unit * D + i) * D + cg + 16 * x] : 0.f;
     float msum = 0.f;   // m[row0 + tid] for tid < RB
     if (tid < RB) msum = ms0 ? ms0[unit * D + row0 + tid] : 0.f;
     // chunk keys go through registers: the next chunk's loads are in flight
@@ -75,9 +76,9 @@ ccq_prefix_kernel(const Tin *__restrict__ k, const float *__restrict__ Ms0,
     load_chunk(0);
     for (int c = 0; c < nch; ++c) {
         // statistics before chunk c
-        Tin *dst = Mprev + (((size_t)unit * nch + c) * D + i) * D + cg * CPT;
+        Tin *dst = Mprev + (((size_t)unit * nch + c) * D + i) * D + cg;
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) stf(dst, x, acc[x]);
+        for (int x = 0; x < CPT; ++x) stf(dst, 16 * x, acc[x]);
         if (tid < RB) mprev[((size_t)unit * nch + c) * D + row0 + tid] = msum;
         __syncthreads();   // previous chunk's keys no longer read
 #pragma unroll
@@ -91,20 +92,21 @@ ccq_prefix_kernel(const Tin *__restrict__ k, const float *__restrict__ Ms0,
         for (int t = 0; t < CC; ++t) {
             const float ki = Ks[t][i];
 #pragma unroll
-            for (int x = 0; x < CPT; ++x) acc[x] = fmaf(ki, Ks[t][cg * CPT + x], acc[x]);
+            for (int x = 0; x < CPT; ++x) acc[x] = fmaf(ki, Ks[t][cg + 16 * x], acc[x]);
         }
         if (tid < RB)
             for (int t = 0; t < CC; ++t) msum += Ks[t][row0 + tid];
     }
 #pragma unroll
     for (int x = 0; x < CPT; ++x)
-        if (Ms_T) Ms_T[(unit * D + i) * D + cg * CPT + x] = acc[x];
+        if (Ms_T) Ms_T[(unit * D + i) * D + cg + 16 * x] = acc[x];
     if (tid < RB && ms_T) ms_T[unit * D + row0 + tid] = msum;
     if (blockIdx.x == 0 && tid == 0 && ns_T) ns_T[unit] = (ns0 ? ns0[unit] : 0.f) + (float)T;
 }
 
 // grid (nch, B * H); 256 threads: thread (t = tid / 4, ib = tid % 4) owns
-// token t of the chunk and dims [ib * D/4, +D/4).
+// token t of the chunk and dims ib + 4 x, x < D/4 (interleaved, so that the
+// four threads of a token read four different banks).
 template <typename Tin, int D>
 __global__ void __launch_bounds__(CQ_THREADS)
 ccq_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
@@ -146,25 +148,25 @@ ccq_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     }
     __syncthreads();
 
-    const int t = tid / 4, ib = tid % 4, i0 = ib * DPT;
+    const int t = tid / 4, ib = tid % 4;
     const int tok = c * CC + t;
     float y[DPT], mc[DPT];
 #pragma unroll
     for (int x = 0; x < DPT; ++x) {
         y[x] = 0.f;
-        mc[x] = mprev[((size_t)unit * nch + c) * D + i0 + x];
+        mc[x] = mprev[((size_t)unit * nch + c) * D + ib + 4 * x];
     }
     for (int j = 0; j < D; ++j) {          // M_prev q_t
         const float qj = Qs[t * LD + j];
 #pragma unroll
-        for (int x = 0; x < DPT; ++x) y[x] = fmaf(MT[j * LD + i0 + x], qj, y[x]);
+        for (int x = 0; x < DPT; ++x) y[x] = fmaf(MT[j * LD + ib + 4 * x], qj, y[x]);
     }
     for (int j = 0; j < CC; ++j) {         // keys of this chunk up to t (Dm is 0 past t)
         const float d = Dm[t * (CC + 1) + j];
         const float on = j <= t ? 1.f : 0.f;
 #pragma unroll
         for (int x = 0; x < DPT; ++x) {
-            const float kv = Ks[j * LD + i0 + x];
+            const float kv = Ks[j * LD + ib + 4 * x];
             y[x] = fmaf(kv, d, y[x]);
             mc[x] = fmaf(kv, on, mc[x]);
         }
@@ -173,16 +175,16 @@ ccq_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     const float inv_n = 1.f / n;
     float muq = 0.f;
 #pragma unroll
-    for (int x = 0; x < DPT; ++x) muq = fmaf(mc[x] * inv_n, Qs[t * LD + i0 + x], muq);
+    for (int x = 0; x < DPT; ++x) muq = fmaf(mc[x] * inv_n, Qs[t * LD + ib + 4 * x], muq);
     muq += __shfl_xor_sync(0xffffffffu, muq, 1);
     muq += __shfl_xor_sync(0xffffffffu, muq, 2);
     if (tok < T) {
         const float lam = lambda[((size_t)b * T + tok) * H + h];
-        const size_t g = (((size_t)b * T + tok) * H + h) * D + i0;
+        const size_t g = (((size_t)b * T + tok) * H + h) * D + ib;
 #pragma unroll
         for (int x = 0; x < DPT; ++x) {
             const float sq = y[x] * inv_n - (mc[x] * inv_n) * muq;
-            stf(q_clean, g + x, Qs[t * LD + i0 + x] - lam * sq);
+            stf(q_clean, g + 4 * x, Qs[t * LD + ib + 4 * x] - lam * sq);
         }
     }
 }

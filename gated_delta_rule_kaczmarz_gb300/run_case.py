@@ -5,7 +5,8 @@
 
 A fixed, short launch sequence for profilers: prefill and varlen workloads
 run ``calls`` full calls (one chunkwise forward each); ``decode`` runs
-``calls`` single-token steps on a [B, 16, 128, 128] state.  Inputs are
+``calls`` single-token steps on a [B, 16, 128, 128] state; ``ccq`` runs
+the CCQ query contraction on the layer_prefill workload's q and k.  Inputs are
 uploaded before the first call.  Prints one line with the mean time per call
 (CUDA events, inputs resident; not a benchmark figure when run under a
 profiler).
@@ -27,12 +28,17 @@ def _dev(inp):
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=sorted(list(WORKLOADS) + ["decode"]))
+    ap.add_argument("case", choices=sorted(list(WORKLOADS) + ["decode", "ccq"]))
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--B", type=int, default=128, help="batch of the decode case")
     a = ap.parse_args(argv)
     calls = []
-    if a.case == "decode":
+    if a.case == "ccq":
+        # the CCQ query contraction on the layer workload's q and k
+        inp = _dev(WORKLOADS["layer_prefill"].make())
+        lam = torch.full(inp["eta"].shape, 0.5, dtype=torch.float32, device="cuda")
+        calls = [lambda: kla.kla_ccq_query(inp["q"], inp["k"], lam)] * a.calls
+    elif a.case == "decode":
         inp = _dev(decode_inputs(a.B, 16, 128, 128, steps=a.calls, dtype="bf16", seed=3))
         S = inp["S"]
         o = torch.empty_like(inp["v"][0])
