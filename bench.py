@@ -381,11 +381,9 @@ def time_ccq(args, dev, reps):
             ms.append(e0.elapsed_time(e1))
         out[name] = sum(ms) / len(ms)
     th = wl.B * wl.T * wl.H
-    # fp32 CUDA-core work of the query (d = 128, chunk 64): M_prev q (2 d^2), the
-    # in-chunk key products and sums (about 4 * 32 * d on average) and the
-    # per-token share of K^T K (2 d^2), in flop per token-head
-    flop = th * (2 * wl.d * wl.d + 4 * 32 * wl.d + 2 * wl.d * wl.d)
-    return dict(wl=wl, query_ms=out["query"], layer_ms=out["layer"], flop=flop)
+    # algorithmic bytes of the query: q and k read, q_clean written (bf16), lambda read
+    nbytes = th * (3 * wl.d * 2 + 4)
+    return dict(wl=wl, query_ms=out["query"], layer_ms=out["layer"], bytes=nbytes)
 
 
 def ours(args):
@@ -428,15 +426,14 @@ def ours(args):
                            "algorithmic_bytes_per_launch": dec["bytes_per_launch"]}}
 
     cq = time_ccq(args, dev, reps=5)
-    fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12     # TFLOP/s: SMs x FP32 lanes x FMA x max clock
+    cq_gbs = cq["bytes"] / (cq["query_ms"] / 1e3) / 1e9
     ccq = {"workload": "layer_prefill with the CCQ read (lambda ~ sigmoid(N(0,1)))",
            "query_us": cq["query_ms"] * 1e3, "layer_us": cq["layer_ms"] * 1e3,
            "layer_value": wl.B * wl.T / (cq["layer_ms"] / 1e3), "unit": "tokens/s",
-           "roofline": {"bound": "alu", "achieved": cq["flop"] / (cq["query_ms"] / 1e3) / 1e12,
-                        "peak": fp32_peak, "unit": "TFLOP/s",
-                        "frac": cq["flop"] / (cq["query_ms"] / 1e3) / 1e12 / fp32_peak,
-                        "traffic": None, "kernel": "ccq_prefix_kernel + ccq_query_kernel",
-                        "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz"}}
+           "roofline": {"bound": "hbm", "achieved": cq_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": cq_gbs / pk["hbm_gbs"], "traffic": None,
+                        "kernel": "fused_kernel (CCQ mode) + ccq_keysum_kernel + ccq_finish_kernel",
+                        "algorithmic_bytes_per_call": cq["bytes"]}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

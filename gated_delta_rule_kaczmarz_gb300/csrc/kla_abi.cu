@@ -324,6 +324,8 @@ int kla_ccq_query(const void *q, const void *k, const float *lambda, const float
     if (need > 0 && (workspace == nullptr || workspace_bytes < need))
         return fail(KLA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
                     workspace ? workspace_bytes : (size_t)0);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(KLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     if (inject_launch_fault()) return fail(KLA_ERR_CUDA, "injected launch fault (KLA_FAULT_INJECT)");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;

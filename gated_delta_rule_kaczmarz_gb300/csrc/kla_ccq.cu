@@ -11,7 +11,15 @@
 // is unchanged and the read is o_t = S_t q_clean_t, so the CCQ layer is the
 // KLA forward run on q_clean.
 //
-// Two passes on the CUDA cores, fp32 arithmetic:
+// bf16 inputs with d = 128 take the tensor cores: y_t = M_t q_t is a gated
+// delta-rule product with no decay whose chunk write is K^T K, so the chunked
+// tcgen05 forward runs it in its CCQ mode (W = 0, U~ = K: the state pass
+// gives y = Q M_prev + lower(Q K^T) K and carries M); then
+//   ccq_keysum_kernel: per (chunk, sequence, head) the sum of the chunk's keys;
+//   ccq_finish_kernel: per (chunk, sequence, head) m_prev from those sums, the
+//     running key sum m_t inside the chunk, n_t, mu_t . q_t and q_clean_t.
+//
+// Other inputs: two passes on the CUDA cores, fp32 arithmetic:
 //   ccq_prefix_kernel: per (sequence, head, 16-row block of M) the chunks in
 //     order; before adding chunk c it records M (in the input dtype: bf16 for
 //     bf16 inputs, whose q_clean is rounded to bf16 anyway, fp32 otherwise)
@@ -189,12 +197,204 @@ ccq_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     }
 }
 
+// ---- tensor-core path (bf16, D = 128) ----
+constexpr int TD = 128;
+
+__device__ __forceinline__ void unpack8(const uint4 v, float *f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// grid (nch, B * H); 256 threads: thread (tg = tid / 64, pair j2 = tid % 64)
+// adds dims 2 j2, 2 j2 + 1 over tokens tg, tg + 4, ... of the chunk.
+__global__ void __launch_bounds__(CQ_THREADS)
+ccq_keysum_kernel(const __nv_bfloat16 *__restrict__ k, int T, int H, int nch,
+                  float *__restrict__ csum) {
+    __shared__ float2 part[CQ_THREADS / 64][64];
+    const int tid = threadIdx.x, tg = tid >> 6, j2 = tid & 63;
+    const int c = blockIdx.x;
+    const long unit = blockIdx.y, b = unit / H, h = unit % H;
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll 4
+    for (int t = tg; t < CC; t += 4) {
+        const int tok = c * CC + t;
+        if (tok < T) {
+            const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(
+                k + (((size_t)b * T + tok) * H + h) * TD + 2 * j2);
+            const float2 f = __bfloat1622float2(v);
+            acc.x += f.x;
+            acc.y += f.y;
+        }
+    }
+    part[tg][j2] = acc;
+    __syncthreads();
+    if (tid < 64) {
+        float2 s2 = part[0][tid];
+#pragma unroll
+        for (int g = 1; g < CQ_THREADS / 64; ++g) {
+            s2.x += part[g][tid].x;
+            s2.y += part[g][tid].y;
+        }
+        *reinterpret_cast<float2 *>(csum + ((size_t)unit * nch + c) * TD + 2 * tid) = s2;
+    }
+}
+
+// grid (nch, B * H); 256 threads.  The chunk's keys go to shared memory and
+// are turned, column by column, into the running sums m_t (thread j < 128
+// owns dim j, starting from m before the chunk); then thread (t = tid / 4,
+// part = tid % 4) finishes token t on the 16-byte pieces part + 4 x.
+__global__ void __launch_bounds__(CQ_THREADS)
+ccq_finish_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                  const __nv_bfloat16 *__restrict__ y, const float *__restrict__ lambda,
+                  const float *__restrict__ ms0, const float *__restrict__ ns0,
+                  const float *__restrict__ csum, int T, int H, int nch,
+                  __nv_bfloat16 *__restrict__ q_clean, float *__restrict__ ms_T,
+                  float *__restrict__ ns_T) {
+    constexpr int LD = TD + 1;
+    __shared__ float Ks[CC * LD];
+    const int tid = threadIdx.x, c = blockIdx.x;
+    const long unit = blockIdx.y, b = unit / H, h = unit % H;
+    for (int e = tid; e < CC * (TD / 8); e += CQ_THREADS) {
+        const int t = e >> 4, pc = e & 15, tok = c * CC + t;
+        float f[8];
+        if (tok < T) {
+            unpack8(*reinterpret_cast<const uint4 *>(k + (((size_t)b * T + tok) * H + h) * TD + pc * 8), f);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) Ks[t * LD + pc * 8 + i] = f[i];
+    }
+    const float n0 = ns0 ? ns0[unit] : 0.f;
+    __syncthreads();
+    if (tid < TD) {
+        float run = ms0 ? ms0[unit * TD + tid] : 0.f;
+        for (int cc = 0; cc < c; ++cc) run += csum[((size_t)unit * nch + cc) * TD + tid];
+#pragma unroll 8
+        for (int t = 0; t < CC; ++t) {
+            run += Ks[t * LD + tid];
+            Ks[t * LD + tid] = run;
+        }
+        if (c == nch - 1 && ms_T) ms_T[unit * TD + tid] = run;
+    }
+    if (c == nch - 1 && tid == 0 && ns_T) ns_T[unit] = n0 + (float)T;
+    __syncthreads();
+
+    const int t = tid >> 2, part = tid & 3, tok = c * CC + t;
+    const bool live = tok < T;
+    const size_t row = (((size_t)b * T + (live ? tok : 0)) * H + h) * TD;
+    float qv[32], yv[32];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        const int pc = part + 4 * x;
+        uint4 a = make_uint4(0u, 0u, 0u, 0u), bb = a;
+        if (live) {
+            a = *reinterpret_cast<const uint4 *>(q + row + pc * 8);
+            bb = *reinterpret_cast<const uint4 *>(y + row + pc * 8);
+        }
+        unpack8(a, qv + 8 * x);
+        unpack8(bb, yv + 8 * x);
+    }
+    const float inv_n = 1.f / (n0 + (float)(c * CC + t + 1));
+    const float *mrow = Ks + t * LD;
+    float muq = 0.f;
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) muq = fmaf(mrow[(part + 4 * x) * 8 + i], qv[8 * x + i], muq);
+    muq *= inv_n;   // mu_t . q_t
+    muq += __shfl_xor_sync(0xffffffffu, muq, 1);
+    muq += __shfl_xor_sync(0xffffffffu, muq, 2);
+    if (live) {
+        const float lam = lambda[((size_t)b * T + tok) * H + h];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const int pc = part + 4 * x;
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                const float c0 = yv[8 * x + i] * inv_n - mrow[pc * 8 + i] * inv_n * muq;
+                const float c1 = yv[8 * x + i + 1] * inv_n - mrow[pc * 8 + i + 1] * inv_n * muq;
+                const __nv_bfloat162 o2 = __floats2bfloat162_rn(qv[8 * x + i] - lam * c0,
+                                                                qv[8 * x + i + 1] - lam * c1);
+                w[i / 2] = *reinterpret_cast<const uint32_t *>(&o2);
+            }
+            *reinterpret_cast<uint4 *>(q_clean + row + pc * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool ccq_use_tc(int B, int T, int d, int dtype) {
+    return chunk_tc_supported(d, dtype) && (long)B * T >= CC;
+}
+
+// Tensor-core workspace after the header: the chunked forward's workspace,
+// y [B, T, H, 128] bf16, the chunk key sums [B, H, nch, 128] fp32.
+struct CcqTcLayout {
+    size_t tc, y, csum, total;
+};
+CcqTcLayout ccq_tc_layout(int B, int T, int H) {
+    const long nch = (T + CC - 1) / CC;
+    CcqTcLayout L;
+    L.tc = 0;
+    L.y = align_up(chunk_tc_workspace_bytes((long)B * nch, H, B), 256);
+    L.csum = align_up(L.y + (size_t)B * T * H * TD * 2, 256);
+    L.total = L.csum + (size_t)B * H * nch * TD * 4;
+    return L;
+}
+
+cudaError_t launch_ccq_tc(const CcqProblem &p, cudaStream_t s) {
+    const int nch = (p.T + CC - 1) / CC;
+    const CcqTcLayout L = ccq_tc_layout(p.B, p.T, p.H);
+    unsigned char *ws = static_cast<unsigned char *>(p.ws) + kWsHeader;
+    __nv_bfloat16 *yb = reinterpret_cast<__nv_bfloat16 *>(ws + L.y);
+    float *csum = reinterpret_cast<float *>(ws + L.csum);
+    // y = M_t q_t on the tensor cores: the chunked forward in its CCQ mode,
+    // with the statistics M as its state (v = k feeds only the unused V tile;
+    // eta, here lambda, is read but does not enter)
+    Problem f{};
+    f.q = p.q; f.k = p.k; f.v = p.k;
+    f.alpha = nullptr; f.eta = p.lambda; f.eps = 0.f;
+    f.S0 = p.Ms0; f.S_T = p.Ms_T; f.o = yb;
+    f.cu_seqlens = nullptr;
+    f.n_seq = p.B; f.T = p.T; f.total_T = p.B * p.T; f.H = p.H; f.d = TD; f.dtype = p.dtype;
+    f.beta_mode = 1; f.mode = 1;
+    f.status = static_cast<unsigned *>(p.ws);
+    f.ws = ws + L.tc;
+    f.ws_bytes = L.y - L.tc;
+    const long nchunks = (long)p.B * nch;
+    cudaError_t e = cudaMemsetAsync(p.ws, 0, kWsHeader + chunk_tc_reset_bytes(f, nchunks), s);
+    if (e != cudaSuccess) return e;
+    if ((e = launch_chunk_tc(f, nchunks, s)) != cudaSuccess) return e;
+    const dim3 grid(nch, p.B * p.H);
+    ccq_keysum_kernel<<<grid, CQ_THREADS, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.k), p.T, p.H,
+                                                  nch, csum);
+    note_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ccq_finish_kernel<<<grid, CQ_THREADS, 0, s>>>(
+        static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k), yb,
+        p.lambda, p.ms0, p.ns0, csum, p.T, p.H, nch, static_cast<__nv_bfloat16 *>(p.q_clean),
+        p.ms_T, p.ns_T);
+    note_launch();
+    return cudaGetLastError();
+}
+
+// ---- CUDA-core path ----
 template <typename Tin, int D>
 cudaError_t launch_ccq_t(const CcqProblem &p, cudaStream_t s) {
     const int nch = (p.T + CC - 1) / CC;
     const int units = p.B * p.H;
-    Tin *Mprev = static_cast<Tin *>(p.ws);
-    float *mprev = reinterpret_cast<float *>(static_cast<unsigned char *>(p.ws) +
+    cudaError_t e0 = cudaMemsetAsync(p.ws, 0, sizeof(unsigned), s);   // status word
+    if (e0 != cudaSuccess) return e0;
+    Tin *Mprev = reinterpret_cast<Tin *>(static_cast<unsigned char *>(p.ws) + kWsHeader);
+    float *mprev = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(Mprev) +
                                              (size_t)units * nch * D * D * sizeof(Tin));
     ccq_prefix_kernel<Tin, D><<<dim3(D / RB, units), CQ_THREADS, 0, s>>>(
         static_cast<const Tin *>(p.k), p.Ms0, p.ms0, p.ns0, p.T, p.H, nch, Mprev, mprev, p.Ms_T,
@@ -282,13 +482,15 @@ cudaError_t launch_ccq_step(const void *q, const void *k, const float *lambda, f
 }
 
 size_t ccq_workspace_bytes(int B, int T, int H, int d, int dtype) {
+    if (ccq_use_tc(B, T, d, dtype)) return kWsHeader + ccq_tc_layout(B, T, H).total;
     const size_t nch = (size_t)(T + CC - 1) / CC;
     const size_t es = dtype == 1 ? 2 : 4;
-    return (size_t)B * H * nch * ((size_t)d * d * es + (size_t)d * 4);
+    return kWsHeader + (size_t)B * H * nch * ((size_t)d * d * es + (size_t)d * 4);
 }
 
 cudaError_t launch_ccq(const CcqProblem &p, cudaStream_t s) {
     if (p.B == 0 || p.T == 0) return cudaSuccess;
+    if (ccq_use_tc(p.B, p.T, p.d, p.dtype)) return launch_ccq_tc(p, s);
     if (p.dtype == 1)
         return p.d == 128 ? launch_ccq_t<__nv_bfloat16, 128>(p, s)
                           : launch_ccq_t<__nv_bfloat16, 64>(p, s);

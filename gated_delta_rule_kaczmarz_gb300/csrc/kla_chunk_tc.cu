@@ -70,6 +70,7 @@ struct TcParams {
     __nv_bfloat16 *U_ws;       // [slots][64][128]   U~
     __nv_bfloat16 *A_ws;       // [slots][64 keys s][64 queries t]  A^T
     int beta_mode;             // 0: beta = eta / (||k||^2 + eps); 1: beta = eta
+    int mode;                  // 0: KLA; 1: the CCQ product (W = 0, U~ = K, no decay)
     unsigned *flags;           // fused launch: one ready flag per work item, then the work-item
                                // counter (all zeroed per call)
     int n_units;               // fused launch: sequences x heads
@@ -527,6 +528,40 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     if (!ok) *sAbort = 1;
     named_sync(bar, P1_THREADS);
     const bool abort2 = *sAbort != 0;
+
+    if (p.mode == 1) {
+        // ---- the CCQ product y_t = M_t q_t: with W = 0, U~ = K, g = 0 and
+        //      A = lower(Q K^T) the state pass computes y = Q M_prev + A K
+        //      and M <- M + K^T K.  K (decayed by exp(0) = 1, tails cleared) is
+        //      stored as U~; the V region, zeroed, as W ----
+#pragma unroll 2
+        for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4 *>(sV + hf * 16384 + sw128_offset(r, ch * 8)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        if (hf == 0 && vslot && !abort2) p.g_ws[slot_row] = 0.f;
+        if (kFused) __threadfence();
+        fence_async_smem();
+        named_sync(bar, P1_THREADS);
+        if (tid == 0 && !abort2) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                if (!(q ? v1 : v0)) continue;
+                const int y = (int)(((2L * pair + q) * p.H + h) * C);
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    tma_store_2d(mw, sV + s * 16384 + q * 8192, 64 * s, y);
+                    tma_store_2d(mu, KQ + s * 32768 + q * 8192, 64 * s, y);
+                }
+            }
+            bulk_commit_group();
+            if (kFused) pending = item;
+        }
+        tc_fence_before();
+        named_sync(bar, P1_THREADS);   // smem and TMEM free for the next item
+        ph ^= 1u;                      // (bars[2] is not used in this mode)
+        if (*sAbort) break;
+        continue;
+    }
 
     // ---- T = (I + L)^{-1}, built up in block sizes 16 -> 32 -> 64: the
     //      diagonal 16 x 16 blocks by forward substitution (first half of the
@@ -1253,6 +1288,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     tp.nch_fixed = p.cu_seqlens ? 0 : (p.T + C - 1) / C;
     tp.eps = p.eps;
     tp.beta_mode = p.beta_mode;
+    tp.mode = p.mode;
     tp.alpha = p.alpha;
     tp.eta = p.eta;
     tp.S0 = p.S0;

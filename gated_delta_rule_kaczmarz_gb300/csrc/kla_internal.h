@@ -36,6 +36,7 @@ struct Problem {
     int H, d;                // heads, dk == dv
     int dtype;               // kla_dtype
     int beta_mode;           // 0: beta = eta / (||k||^2 + eps); 1: beta = eta
+    int mode;                // 0: KLA; 1: the CCQ product y = M_t q (tensor-core path only)
     unsigned *status;        // device status word, or nullptr
     void *ws;                // workspace after the header (path specific)
     size_t ws_bytes;

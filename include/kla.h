@@ -240,10 +240,16 @@ KLA_API int kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
  *   ns0, ns_T     : [B, H] fp32 counts; the initial statistics may be NULL
  *                   (zero), the final ones NULL (not needed).  Ms_T may not
  *                   alias Ms0 (likewise ms, ns).
- *   workspace     : kla_ccq_query_workspace_size(...) bytes (per chunk the
- *                   statistics that precede it), owned by the caller.
- * dk in {64, 128}.  Arithmetic fp32; the per-chunk M is stored in the input
- * dtype.
+ *   workspace     : kla_ccq_query_workspace_size(...) bytes, 256-byte
+ *                   aligned, owned by the caller.  It starts with the device
+ *                   status word (read with kla_workspace_status after the
+ *                   call); the rest is scratch.
+ * dk in {64, 128}.  bf16 inputs with dk = 128 (and B*T >= 64) take the tensor
+ * cores: M_t q_t comes from the chunked forward's tcgen05 kernels run with
+ * W = 0, U~ = K and no decay (products of bf16 values accumulated in fp32,
+ * the carried M rounded to bf16 as the operand of its product with Q, M q
+ * rounded to bf16 before the fp32 finish).  Other inputs: fp32 arithmetic
+ * on the CUDA cores, the per-chunk M stored in the input dtype.
  */
 KLA_API size_t kla_ccq_query_workspace_size(int B, int T, int H, int dk, int dtype);
 KLA_API int kla_ccq_query(const void *q, const void *k, const float *lambda,

@@ -170,7 +170,13 @@ def test_ccq_host_validation():
     # missing workspace
     assert f(FAKE, FAKE, FAKE, None, None, None, FAKE, None, None, None, 1, 64, 1, 64, 1,
              None, 0, None) == binding.KLA_ERR_WORKSPACE
+    # workspace not 256-byte aligned
+    assert f(FAKE, FAKE, FAKE, None, None, None, FAKE, None, None, None, 1, 64, 1, 64, 1,
+             ctypes.c_void_p(0x10010), 1 << 30, None) == binding.KLA_ERR_INVALID_ARG
+    assert "aligned" in lib.kla_last_error_message().decode()
     assert lib.kla_ccq_query_workspace_size(1, 64, 1, 64, 1) > 0
+    # the tensor-core layout (bf16, dk 128) holds at least y and the chunk key sums
+    assert lib.kla_ccq_query_workspace_size(2, 256, 2, 128, 1) >= 2 * 256 * 2 * 128 * 2 + 2 * 2 * 4 * 128 * 4
     g = lib.kla_ccq_query_step
     assert g(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 2, 2, 64, 1, None) == \
         binding.KLA_ERR_INVALID_ARG

@@ -30,7 +30,11 @@ def _stats(B, H, d, seed):
 
 @pytest.mark.parametrize("B,T,H,d,dtype,with_stats", [
     (2, 200, 2, 64, "fp32", False), (1, 130, 2, 128, "fp32", True),
-    (2, 257, 2, 128, "bf16", False), (1, 64, 3, 128, "bf16", True), (2, 1, 2, 64, "bf16", True)])
+    (2, 257, 2, 128, "bf16", False), (1, 64, 3, 128, "bf16", True), (2, 1, 2, 64, "bf16", True),
+    # tensor-core path: fused launch (even chunk count), two launches (odd),
+    # sequences shorter than a chunk (B*T >= 64)
+    (2, 256, 2, 128, "bf16", True), (3, 448, 2, 128, "bf16", False), (1, 323, 5, 128, "bf16", True),
+    (80, 1, 1, 128, "bf16", True), (3, 40, 2, 128, "bf16", False)])
 def test_ccq_query_parity(B, T, H, d, dtype, with_stats):
     inp = prefill_inputs(B, T, H, d, d, dtype, seed=120 + T)
     lam = _lam((B, T, H), 7)
@@ -81,3 +85,47 @@ def test_ccq_step_equals_prefill(d, dtype):
     assert rel_err(torch.stack(outs, 1), qc_ref) <= tol
     assert rel_err(Ms, Ms_ref) <= 1e-5
     assert np.array_equal(ns.cpu().numpy(), ns_ref)
+
+
+@pytest.mark.parametrize("T,launches", [(256, 3), (320, 4)])
+def test_ccq_tensor_core_launches(T, launches):
+    """bf16 dk 128 runs the chunked tcgen05 forward in its CCQ mode (one fused
+    launch for an even chunk count, two otherwise) plus the key-sum and finish
+    kernels; the status word in the workspace stays 0."""
+    B, H, d = 2, 2, 128
+    inp = prefill_inputs(B, T, H, d, d, "bf16", seed=150)
+    lam = _lam((B, T, H), 12)
+    g = cuda(inp)
+    ws = torch.zeros(kla.kla_ccq_query_workspace_size(B, T, H, d), dtype=torch.uint8,
+                     device="cuda")
+    kla.kla_ccq_query(g["q"], g["k"], lam.cuda(), workspace=ws)   # first call sets attributes
+    torch.cuda.synchronize()
+    n0 = kla.kla_launch_count()
+    qc, _ = kla.kla_ccq_query(g["q"], g["k"], lam.cuda(), workspace=ws)
+    torch.cuda.synchronize()
+    assert kla.kla_launch_count() - n0 == launches
+    assert kla.kla_workspace_status(ws) == 0
+    qc_ref, _ = oracle.ccq_query(inp["q"], inp["k"], lam)
+    assert rel_err(qc, qc_ref) <= TOL[inp["q"].dtype]
+
+
+def test_ccq_full_size_sampled():
+    """The layer workload (B4 H8 T2048 d128 bf16): q_clean and the final
+    statistics of two sampled (sequence, head) units against the oracle run on
+    those units alone."""
+    from gated_delta_rule_kaczmarz_gb300.workloads import WORKLOADS
+    wl = WORKLOADS["layer_prefill"]
+    inp = wl.make()
+    lam = _lam((wl.B, wl.T, wl.H), 13)
+    g = cuda(inp)
+    qc, (Ms, ms, ns) = kla.kla_ccq_query(g["q"], g["k"], lam.cuda())
+    torch.cuda.synchronize()
+    for b, h in ((0, 0), (3, 5)):
+        q1 = inp["q"][b:b + 1, :, h:h + 1].contiguous()
+        k1 = inp["k"][b:b + 1, :, h:h + 1].contiguous()
+        l1 = lam[b:b + 1, :, h:h + 1].contiguous()
+        ref, (M_ref, m_ref, n_ref) = oracle.ccq_query(q1, k1, l1)
+        assert rel_err(qc[b:b + 1, :, h:h + 1], ref) <= TOL[inp["q"].dtype]
+        assert rel_err(Ms[b:b + 1, h:h + 1], M_ref) <= 1e-5
+        assert rel_err(ms[b:b + 1, h:h + 1], m_ref) <= 1e-5
+        assert float(ns[b, h]) == float(n_ref.reshape(-1)[0])
