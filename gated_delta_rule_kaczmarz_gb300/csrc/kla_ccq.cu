@@ -15,7 +15,7 @@
 // delta-rule product with no decay whose chunk write is K^T K, so the chunked
 // tcgen05 forward runs it in its CCQ mode (W = 0, U~ = K: the state pass
 // gives y = Q M_prev + lower(Q K^T) K and carries M); then
-//   ccq_keysum_kernel: per (chunk, sequence, head) the sum of the chunk's keys;
+// whose first phase also writes the sum of each chunk's keys; then
 //   ccq_finish_kernel: per (chunk, sequence, head) m_prev from those sums, the
 //     running key sum m_t inside the chunk, n_t, mu_t . q_t and q_clean_t.
 //
@@ -209,45 +209,13 @@ __device__ __forceinline__ void unpack8(const uint4 v, float *f) {
     }
 }
 
-// grid (nch, B * H); 256 threads: thread (tg = tid / 64, pair j2 = tid % 64)
-// adds dims 2 j2, 2 j2 + 1 over tokens tg, tg + 4, ... of the chunk.
-__global__ void __launch_bounds__(CQ_THREADS)
-ccq_keysum_kernel(const __nv_bfloat16 *__restrict__ k, int T, int H, int nch,
-                  float *__restrict__ csum) {
-    __shared__ float2 part[CQ_THREADS / 64][64];
-    const int tid = threadIdx.x, tg = tid >> 6, j2 = tid & 63;
-    const int c = blockIdx.x;
-    const long unit = blockIdx.y, b = unit / H, h = unit % H;
-    float2 acc = make_float2(0.f, 0.f);
-#pragma unroll 4
-    for (int t = tg; t < CC; t += 4) {
-        const int tok = c * CC + t;
-        if (tok < T) {
-            const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(
-                k + (((size_t)b * T + tok) * H + h) * TD + 2 * j2);
-            const float2 f = __bfloat1622float2(v);
-            acc.x += f.x;
-            acc.y += f.y;
-        }
-    }
-    part[tg][j2] = acc;
-    __syncthreads();
-    if (tid < 64) {
-        float2 s2 = part[0][tid];
-#pragma unroll
-        for (int g = 1; g < CQ_THREADS / 64; ++g) {
-            s2.x += part[g][tid].x;
-            s2.y += part[g][tid].y;
-        }
-        *reinterpret_cast<float2 *>(csum + ((size_t)unit * nch + c) * TD + 2 * tid) = s2;
-    }
-}
-
-// grid (nch, B * H); 256 threads.  The chunk's keys go to shared memory and
-// are turned, column by column, into the running sums m_t (thread j < 128
-// owns dim j, starting from m before the chunk); then thread (t = tid / 4,
-// part = tid % 4) finishes token t on the 16-byte pieces part + 4 x.
-__global__ void __launch_bounds__(CQ_THREADS)
+// grid (nch, B * H); 256 threads.  Every load is issued up front: this
+// thread's token pieces of q and y (token tid / 4, 16-byte pieces tid % 4 +
+// 4 x), its share of the chunk's keys, and half of the key sums of the
+// preceding chunks for feature tid % 128.  The keys then go to shared memory
+// and thread j < 128 turns column j into the running sums m_t (from m before
+// the chunk); last, each thread finishes its token's pieces.
+__global__ void __launch_bounds__(CQ_THREADS, 2)
 ccq_finish_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                   const __nv_bfloat16 *__restrict__ y, const float *__restrict__ lambda,
                   const float *__restrict__ ms0, const float *__restrict__ ns0,
@@ -256,75 +224,105 @@ ccq_finish_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
                   float *__restrict__ ns_T) {
     constexpr int LD = TD + 1;
     __shared__ float Ks[CC * LD];
+    __shared__ float mp[2][TD];
     const int tid = threadIdx.x, c = blockIdx.x;
     const long unit = blockIdx.y, b = unit / H, h = unit % H;
-    for (int e = tid; e < CC * (TD / 8); e += CQ_THREADS) {
-        const int t = e >> 4, pc = e & 15, tok = c * CC + t;
-        float f[8];
-        if (tok < T) {
-            unpack8(*reinterpret_cast<const uint4 *>(k + (((size_t)b * T + tok) * H + h) * TD + pc * 8), f);
-        } else {
+    const size_t tok_stride = (size_t)H * TD;
+    const size_t base = ((size_t)b * T * H + h) * TD;   // token 0 of (b, h)
+
+    const int t = tid >> 2, part = tid & 3, tok = c * CC + t;
+    const bool live = tok < T;
+    uint4 qa[4], ya[4], ka[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = 0.f;
+    for (int x = 0; x < 4; ++x) {
+        qa[x] = ya[x] = make_uint4(0u, 0u, 0u, 0u);
+        if (live) {
+            const size_t o = base + (size_t)tok * tok_stride + (part + 4 * x) * 8;
+            qa[x] = *reinterpret_cast<const uint4 *>(q + o);
+            ya[x] = *reinterpret_cast<const uint4 *>(y + o);
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) Ks[t * LD + pc * 8 + i] = f[i];
     }
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {   // key piece e: token e / 16, piece e % 16
+        const int e = tid + x * CQ_THREADS, kt = c * CC + (e >> 4);
+        ka[x] = kt < T ? *reinterpret_cast<const uint4 *>(k + base + (size_t)kt * tok_stride +
+                                                          (e & 15) * 8)
+                       : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // m before the chunk: the initial sum plus the preceding chunks' sums,
+    // chunks cc = half, half + 2, ... for this thread
+    const int j = tid & (TD - 1), half = tid >> 7;
+    const float *cs = csum + ((size_t)b * nch * H + h) * TD + j;   // chunk cc at cc * H * TD
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int cc = half;
+    for (; cc + 6 < c; cc += 8) {
+        a0 += cs[(size_t)cc * H * TD];
+        a1 += cs[(size_t)(cc + 2) * H * TD];
+        a2 += cs[(size_t)(cc + 4) * H * TD];
+        a3 += cs[(size_t)(cc + 6) * H * TD];
+    }
+    for (; cc < c; cc += 2) a0 += cs[(size_t)cc * H * TD];
+    mp[half][j] = (a0 + a1) + (a2 + a3) + (half == 0 && ms0 ? ms0[unit * TD + j] : 0.f);
+    const float lam = live ? lambda[((size_t)b * T + tok) * H + h] : 0.f;
     const float n0 = ns0 ? ns0[unit] : 0.f;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        const int e = tid + x * CQ_THREADS;
+        float f[8];
+        unpack8(ka[x], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) Ks[(e >> 4) * LD + (e & 15) * 8 + i] = f[i];
+    }
     __syncthreads();
     if (tid < TD) {
-        float run = ms0 ? ms0[unit * TD + tid] : 0.f;
-        for (int cc = 0; cc < c; ++cc) run += csum[((size_t)unit * nch + cc) * TD + tid];
-#pragma unroll 8
-        for (int t = 0; t < CC; ++t) {
-            run += Ks[t * LD + tid];
-            Ks[t * LD + tid] = run;
+        float run = mp[0][tid] + mp[1][tid];
+#pragma unroll
+        for (int t0 = 0; t0 < CC; t0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = Ks[(t0 + i) * LD + tid];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                run += v[i];
+                Ks[(t0 + i) * LD + tid] = run;
+            }
         }
         if (c == nch - 1 && ms_T) ms_T[unit * TD + tid] = run;
     }
     if (c == nch - 1 && tid == 0 && ns_T) ns_T[unit] = n0 + (float)T;
     __syncthreads();
 
-    const int t = tid >> 2, part = tid & 3, tok = c * CC + t;
-    const bool live = tok < T;
-    const size_t row = (((size_t)b * T + (live ? tok : 0)) * H + h) * TD;
-    float qv[32], yv[32];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-        const int pc = part + 4 * x;
-        uint4 a = make_uint4(0u, 0u, 0u, 0u), bb = a;
-        if (live) {
-            a = *reinterpret_cast<const uint4 *>(q + row + pc * 8);
-            bb = *reinterpret_cast<const uint4 *>(y + row + pc * 8);
-        }
-        unpack8(a, qv + 8 * x);
-        unpack8(bb, yv + 8 * x);
-    }
     const float inv_n = 1.f / (n0 + (float)(c * CC + t + 1));
     const float *mrow = Ks + t * LD;
     float muq = 0.f;
 #pragma unroll
-    for (int x = 0; x < 4; ++x)
+    for (int x = 0; x < 4; ++x) {
+        float qf[8];
+        unpack8(qa[x], qf);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) muq = fmaf(mrow[(part + 4 * x) * 8 + i], qv[8 * x + i], muq);
+        for (int i = 0; i < 8; ++i) muq = fmaf(mrow[(part + 4 * x) * 8 + i], qf[i], muq);
+    }
     muq *= inv_n;   // mu_t . q_t
     muq += __shfl_xor_sync(0xffffffffu, muq, 1);
     muq += __shfl_xor_sync(0xffffffffu, muq, 2);
     if (live) {
-        const float lam = lambda[((size_t)b * T + tok) * H + h];
+        const size_t o0 = base + (size_t)tok * tok_stride;
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
             const int pc = part + 4 * x;
+            float qf[8], yf[8];
+            unpack8(qa[x], qf);
+            unpack8(ya[x], yf);
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 8; i += 2) {
-                const float c0 = yv[8 * x + i] * inv_n - mrow[pc * 8 + i] * inv_n * muq;
-                const float c1 = yv[8 * x + i + 1] * inv_n - mrow[pc * 8 + i + 1] * inv_n * muq;
-                const __nv_bfloat162 o2 = __floats2bfloat162_rn(qv[8 * x + i] - lam * c0,
-                                                                qv[8 * x + i + 1] - lam * c1);
+                const float c0 = yf[i] * inv_n - mrow[pc * 8 + i] * inv_n * muq;
+                const float c1 = yf[i + 1] * inv_n - mrow[pc * 8 + i + 1] * inv_n * muq;
+                const __nv_bfloat162 o2 = __floats2bfloat162_rn(qf[i] - lam * c0,
+                                                                qf[i + 1] - lam * c1);
                 w[i / 2] = *reinterpret_cast<const uint32_t *>(&o2);
             }
-            *reinterpret_cast<uint4 *>(q_clean + row + pc * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4 *>(q_clean + o0 + pc * 8) = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
 }
@@ -336,7 +334,7 @@ bool ccq_use_tc(int B, int T, int d, int dtype) {
 }
 
 // Tensor-core workspace after the header: the chunked forward's workspace,
-// y [B, T, H, 128] bf16, the chunk key sums [B, H, nch, 128] fp32.
+// y [B, T, H, 128] bf16, the chunk key sums [B, nch, H, 128] fp32.
 struct CcqTcLayout {
     size_t tc, y, csum, total;
 };
@@ -365,7 +363,7 @@ cudaError_t launch_ccq_tc(const CcqProblem &p, cudaStream_t s) {
     f.S0 = p.Ms0; f.S_T = p.Ms_T; f.o = yb;
     f.cu_seqlens = nullptr;
     f.n_seq = p.B; f.T = p.T; f.total_T = p.B * p.T; f.H = p.H; f.d = TD; f.dtype = p.dtype;
-    f.beta_mode = 1; f.mode = 1;
+    f.beta_mode = 1; f.mode = 1; f.csum = csum;
     f.status = static_cast<unsigned *>(p.ws);
     f.ws = ws + L.tc;
     f.ws_bytes = L.y - L.tc;
@@ -374,10 +372,6 @@ cudaError_t launch_ccq_tc(const CcqProblem &p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if ((e = launch_chunk_tc(f, nchunks, s)) != cudaSuccess) return e;
     const dim3 grid(nch, p.B * p.H);
-    ccq_keysum_kernel<<<grid, CQ_THREADS, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.k), p.T, p.H,
-                                                  nch, csum);
-    note_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ccq_finish_kernel<<<grid, CQ_THREADS, 0, s>>>(
         static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k), yb,
         p.lambda, p.ms0, p.ns0, csum, p.T, p.H, nch, static_cast<__nv_bfloat16 *>(p.q_clean),

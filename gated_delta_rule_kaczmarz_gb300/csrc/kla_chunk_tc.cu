@@ -71,6 +71,7 @@ struct TcParams {
     __nv_bfloat16 *A_ws;       // [slots][64 keys s][64 queries t]  A^T
     int beta_mode;             // 0: beta = eta / (||k||^2 + eps); 1: beta = eta
     int mode;                  // 0: KLA; 1: the CCQ product (W = 0, U~ = K, no decay)
+    float *csum;               // CCQ mode: [slots][128] the sum of each chunk's keys
     unsigned *flags;           // fused launch: one ready flag per work item, then the work-item
                                // counter (all zeroed per call)
     int n_units;               // fused launch: sequences x heads
@@ -533,7 +534,22 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
         // ---- the CCQ product y_t = M_t q_t: with W = 0, U~ = K, g = 0 and
         //      A = lower(Q K^T) the state pass computes y = Q M_prev + A K
         //      and M <- M + K^T K.  K (decayed by exp(0) = 1, tails cleared) is
-        //      stored as U~; the V region, zeroed, as W ----
+        //      stored as U~; the V region, zeroed, as W.  Thread (chunk tid /
+        //      128, feature tid % 128) also sums its feature over the chunk ----
+        {
+            const int j = tid & 127, sl = tid >> 7;
+            const unsigned char *kb = KQ + (j >> 6) * 32768;
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll 8
+            for (int u = 0; u < 64; u += 2) {
+                s0 += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                    kb + sw128_offset(sl * 64 + u, j & 63)));
+                s1 += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                    kb + sw128_offset(sl * 64 + u + 1, j & 63)));
+            }
+            if ((sl ? v1 : v0) && !abort2)
+                p.csum[((2L * pair + sl) * p.H + h) * D + j] = s0 + s1;
+        }
 #pragma unroll 2
         for (int ch = 0; ch < 8; ++ch)
             *reinterpret_cast<uint4 *>(sV + hf * 16384 + sw128_offset(r, ch * 8)) =
@@ -1289,6 +1305,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     tp.eps = p.eps;
     tp.beta_mode = p.beta_mode;
     tp.mode = p.mode;
+    tp.csum = p.csum;
     tp.alpha = p.alpha;
     tp.eta = p.eta;
     tp.S0 = p.S0;

@@ -37,6 +37,8 @@ struct Problem {
     int dtype;               // kla_dtype
     int beta_mode;           // 0: beta = eta / (||k||^2 + eps); 1: beta = eta
     int mode;                // 0: KLA; 1: the CCQ product y = M_t q (tensor-core path only)
+    float *csum;             // mode 1: [chunk slots][d] per-chunk key sums (fixed length:
+                             // slot (b * n_chunks + c) * H + h)
     unsigned *status;        // device status word, or nullptr
     void *ws;                // workspace after the header (path specific)
     size_t ws_bytes;

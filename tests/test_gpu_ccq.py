@@ -87,11 +87,11 @@ def test_ccq_step_equals_prefill(d, dtype):
     assert np.array_equal(ns.cpu().numpy(), ns_ref)
 
 
-@pytest.mark.parametrize("T,launches", [(256, 3), (320, 4)])
+@pytest.mark.parametrize("T,launches", [(256, 2), (320, 3)])
 def test_ccq_tensor_core_launches(T, launches):
     """bf16 dk 128 runs the chunked tcgen05 forward in its CCQ mode (one fused
-    launch for an even chunk count, two otherwise) plus the key-sum and finish
-    kernels; the status word in the workspace stays 0."""
+    launch for an even chunk count, two otherwise; it also sums each chunk's
+    keys) plus the finish kernel; the status word in the workspace stays 0."""
     B, H, d = 2, 2, 128
     inp = prefill_inputs(B, T, H, d, d, "bf16", seed=150)
     lam = _lam((B, T, H), 12)
