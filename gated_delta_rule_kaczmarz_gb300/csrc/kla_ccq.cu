@@ -209,46 +209,58 @@ __device__ __forceinline__ void unpack8(const uint4 v, float *f) {
     }
 }
 
-// grid (nch, B * H); 256 threads.  Every load is issued up front: this
-// thread's token pieces of q and y (token tid / 4, 16-byte pieces tid % 4 +
-// 4 x), its share of the chunk's keys, and half of the key sums of the
-// preceding chunks for feature tid % 128.  The keys then go to shared memory
-// and thread j < 128 turns column j into the running sums m_t (from m before
-// the chunk); last, each thread finishes its token's pieces.
-__global__ void __launch_bounds__(CQ_THREADS, 2)
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+
+// grid (nch, B * H); 256 threads, three CTAs per SM.  Every load is issued up
+// front: q and y rows of the chunk go to shared memory by asynchronous copies
+// (16-byte piece pc of token row t at position pc ^ 4 (t & 1), so that the
+// two tokens read by eight consecutive lanes fall in different banks), the
+// keys through registers into an fp32 tile, and half of the key sums of the
+// preceding chunks for feature tid % 128 into registers.  Thread j < 128 then
+// turns key column j into the running sums m_t (from m before the chunk), and
+// thread (t = tid / 4, part = tid % 4) finishes token t on the pieces part +
+// 4 x.
+constexpr int FK_LD = TD + 4;   // fp32 key row stride: 16-byte aligned rows
+constexpr size_t FK_SMEM = (size_t)CC * FK_LD * 4 + 2 * (size_t)CC * TD * 2 + 2 * TD * 4;
+
+__global__ void __launch_bounds__(CQ_THREADS, 3)
 ccq_finish_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                   const __nv_bfloat16 *__restrict__ y, const float *__restrict__ lambda,
                   const float *__restrict__ ms0, const float *__restrict__ ns0,
                   const float *__restrict__ csum, int T, int H, int nch,
                   __nv_bfloat16 *__restrict__ q_clean, float *__restrict__ ms_T,
                   float *__restrict__ ns_T) {
-    constexpr int LD = TD + 1;
-    __shared__ float Ks[CC * LD];
-    __shared__ float mp[2][TD];
+    extern __shared__ __align__(16) unsigned char fsm[];
+    float *Ks = reinterpret_cast<float *>(fsm);                        // [CC][FK_LD]
+    unsigned char *Qs = fsm + (size_t)CC * FK_LD * 4;                  // [CC][256 B]
+    unsigned char *Ys = Qs + (size_t)CC * TD * 2;                      // [CC][256 B]
+    float *mp = reinterpret_cast<float *>(Ys + (size_t)CC * TD * 2);   // [2][TD]
     const int tid = threadIdx.x, c = blockIdx.x;
     const long unit = blockIdx.y, b = unit / H, h = unit % H;
     const size_t tok_stride = (size_t)H * TD;
     const size_t base = ((size_t)b * T * H + h) * TD;   // token 0 of (b, h)
 
-    const int t = tid >> 2, part = tid & 3, tok = c * CC + t;
-    const bool live = tok < T;
-    uint4 qa[4], ya[4], ka[4];
+    // piece e of the chunk: token e / 16, 16-byte piece e % 16
+    uint4 ka[4];
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
-        qa[x] = ya[x] = make_uint4(0u, 0u, 0u, 0u);
-        if (live) {
-            const size_t o = base + (size_t)tok * tok_stride + (part + 4 * x) * 8;
-            qa[x] = *reinterpret_cast<const uint4 *>(q + o);
-            ya[x] = *reinterpret_cast<const uint4 *>(y + o);
+        const int e = tid + x * CQ_THREADS, te = e >> 4, pc = e & 15, kt = c * CC + te;
+        if (kt < T) {
+            const size_t o = base + (size_t)kt * tok_stride + pc * 8;
+            const int pos = te * 256 + ((pc ^ ((te & 1) << 2)) << 4);
+            cp_async16(Qs + pos, q + o);
+            cp_async16(Ys + pos, y + o);
+            ka[x] = *reinterpret_cast<const uint4 *>(k + o);
+        } else {
+            ka[x] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {   // key piece e: token e / 16, piece e % 16
-        const int e = tid + x * CQ_THREADS, kt = c * CC + (e >> 4);
-        ka[x] = kt < T ? *reinterpret_cast<const uint4 *>(k + base + (size_t)kt * tok_stride +
-                                                          (e & 15) * 8)
-                       : make_uint4(0u, 0u, 0u, 0u);
-    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
     // m before the chunk: the initial sum plus the preceding chunks' sums,
     // chunks cc = half, half + 2, ... for this thread
     const int j = tid & (TD - 1), half = tid >> 7;
@@ -262,62 +274,77 @@ ccq_finish_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__re
         a3 += cs[(size_t)(cc + 6) * H * TD];
     }
     for (; cc < c; cc += 2) a0 += cs[(size_t)cc * H * TD];
-    mp[half][j] = (a0 + a1) + (a2 + a3) + (half == 0 && ms0 ? ms0[unit * TD + j] : 0.f);
-    const float lam = live ? lambda[((size_t)b * T + tok) * H + h] : 0.f;
-    const float n0 = ns0 ? ns0[unit] : 0.f;
+    mp[half * TD + j] = (a0 + a1) + (a2 + a3) + (half == 0 && ms0 ? ms0[unit * TD + j] : 0.f);
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
         const int e = tid + x * CQ_THREADS;
         float f[8];
         unpack8(ka[x], f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) Ks[(e >> 4) * LD + (e & 15) * 8 + i] = f[i];
+        float4 *dst = reinterpret_cast<float4 *>(Ks + (e >> 4) * FK_LD + (e & 15) * 8);
+        dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+        dst[1] = make_float4(f[4], f[5], f[6], f[7]);
     }
+    const int t = tid >> 2, part = tid & 3, tok = c * CC + t;
+    const bool live = tok < T;
+    const float lam = live ? lambda[((size_t)b * T + tok) * H + h] : 0.f;
+    const float n0 = ns0 ? ns0[unit] : 0.f;
     __syncthreads();
     if (tid < TD) {
-        float run = mp[0][tid] + mp[1][tid];
+        float run = mp[tid] + mp[TD + tid];
 #pragma unroll
         for (int t0 = 0; t0 < CC; t0 += 16) {
             float v[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = Ks[(t0 + i) * LD + tid];
+            for (int i = 0; i < 16; ++i) v[i] = Ks[(t0 + i) * FK_LD + tid];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 run += v[i];
-                Ks[(t0 + i) * LD + tid] = run;
+                Ks[(t0 + i) * FK_LD + tid] = run;
             }
         }
         if (c == nch - 1 && ms_T) ms_T[unit * TD + tid] = run;
     }
     if (c == nch - 1 && tid == 0 && ns_T) ns_T[unit] = n0 + (float)T;
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
     __syncthreads();
 
     const float inv_n = 1.f / (n0 + (float)(c * CC + t + 1));
-    const float *mrow = Ks + t * LD;
+    const float *mrow = Ks + t * FK_LD;
+    const int sw = (t & 1) << 2;
     float muq = 0.f;
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
+        const int pc = part + 4 * x;
         float qf[8];
-        unpack8(qa[x], qf);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) muq = fmaf(mrow[(part + 4 * x) * 8 + i], qf[i], muq);
+        unpack8(*reinterpret_cast<const uint4 *>(Qs + t * 256 + ((pc ^ sw) << 4)), qf);
+        const float4 m0 = *reinterpret_cast<const float4 *>(mrow + pc * 8);
+        const float4 m1 = *reinterpret_cast<const float4 *>(mrow + pc * 8 + 4);
+        muq = fmaf(m0.x, qf[0], muq); muq = fmaf(m0.y, qf[1], muq);
+        muq = fmaf(m0.z, qf[2], muq); muq = fmaf(m0.w, qf[3], muq);
+        muq = fmaf(m1.x, qf[4], muq); muq = fmaf(m1.y, qf[5], muq);
+        muq = fmaf(m1.z, qf[6], muq); muq = fmaf(m1.w, qf[7], muq);
     }
     muq *= inv_n;   // mu_t . q_t
     muq += __shfl_xor_sync(0xffffffffu, muq, 1);
     muq += __shfl_xor_sync(0xffffffffu, muq, 2);
     if (live) {
         const size_t o0 = base + (size_t)tok * tok_stride;
+        const float mscale = inv_n * muq;
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
             const int pc = part + 4 * x;
-            float qf[8], yf[8];
-            unpack8(qa[x], qf);
-            unpack8(ya[x], yf);
+            float qf[8], yf[8], mf[8];
+            unpack8(*reinterpret_cast<const uint4 *>(Qs + t * 256 + ((pc ^ sw) << 4)), qf);
+            unpack8(*reinterpret_cast<const uint4 *>(Ys + t * 256 + ((pc ^ sw) << 4)), yf);
+            const float4 m0 = *reinterpret_cast<const float4 *>(mrow + pc * 8);
+            const float4 m1 = *reinterpret_cast<const float4 *>(mrow + pc * 8 + 4);
+            mf[0] = m0.x; mf[1] = m0.y; mf[2] = m0.z; mf[3] = m0.w;
+            mf[4] = m1.x; mf[5] = m1.y; mf[6] = m1.z; mf[7] = m1.w;
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 8; i += 2) {
-                const float c0 = yf[i] * inv_n - mrow[pc * 8 + i] * inv_n * muq;
-                const float c1 = yf[i + 1] * inv_n - mrow[pc * 8 + i + 1] * inv_n * muq;
+                const float c0 = yf[i] * inv_n - mf[i] * mscale;
+                const float c1 = yf[i + 1] * inv_n - mf[i + 1] * mscale;
                 const __nv_bfloat162 o2 = __floats2bfloat162_rn(qf[i] - lam * c0,
                                                                 qf[i + 1] - lam * c1);
                 w[i / 2] = *reinterpret_cast<const uint32_t *>(&o2);
@@ -371,8 +398,15 @@ cudaError_t launch_ccq_tc(const CcqProblem &p, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(p.ws, 0, kWsHeader + chunk_tc_reset_bytes(f, nchunks), s);
     if (e != cudaSuccess) return e;
     if ((e = launch_chunk_tc(f, nchunks, s)) != cudaSuccess) return e;
+    static bool fattr = false;
+    if (!fattr) {
+        if ((e = cudaFuncSetAttribute(ccq_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)FK_SMEM)) != cudaSuccess)
+            return e;
+        fattr = true;
+    }
     const dim3 grid(nch, p.B * p.H);
-    ccq_finish_kernel<<<grid, CQ_THREADS, 0, s>>>(
+    ccq_finish_kernel<<<grid, CQ_THREADS, FK_SMEM, s>>>(
         static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k), yb,
         p.lambda, p.ms0, p.ns0, csum, p.T, p.H, nch, static_cast<__nv_bfloat16 *>(p.q_clean),
         p.ms_T, p.ns_T);
