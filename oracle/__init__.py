@@ -16,6 +16,10 @@ forward(q, k, v, alpha, eta, eps, S0=None, nthreads=1) -> (o, S_T)
     S0: [B,H,dk,dv] or None.
 forward_varlen(q, k, v, alpha, eta, eps, cu_seqlens, S0=None, nthreads=1)
     packed batch, q,k: [total_T,H,dk], cu_seqlens: [N+1] int.
+backward(q, k, v, alpha, eta, eps, S0, do, dS_T=None, nthreads=1)
+    -> (dq, dk, dv, dalpha, deta, dS0): the gradient of
+    L = sum <do, o> + <dS_T, S_T> by reverse-mode differentiation of the
+    recurrence (``kla_oracle_bwd.c``); dalpha is None when alpha is None.
 decode(q, k, v, alpha, eta, eps, S, nthreads=1) -> (o, S_new)
     one token per (b,h): q,k: [B,H,dk], v: [B,H,dv], alpha,eta: [B,H],
     S: [B,H,dk,dv].  The decode step is the same recurrence applied to a
@@ -42,6 +46,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kla_oracle.c")
 _SRC_CCQ = os.path.join(_HERE, "ccq_oracle.c")
+_SRC_BWD = os.path.join(_HERE, "kla_oracle_bwd.c")
 _LIB_PATH = os.path.join(_HERE, "libkla_oracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -62,12 +67,13 @@ def build(force: bool = False) -> str:
     fast-math, no host-specific flags so it builds the same on x86 and Arm)."""
     stale = (not os.path.exists(_LIB_PATH)
              or os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(_SRC),
-                                                  os.path.getmtime(_SRC_CCQ))
+                                                  os.path.getmtime(_SRC_CCQ),
+                                                  os.path.getmtime(_SRC_BWD))
              or not _elf_matches_host(_LIB_PATH))
     if force or stale:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-               "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, _SRC_CCQ]
+               "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, _SRC_CCQ, _SRC_BWD]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -88,6 +94,10 @@ def _bind(lib):
     lib.kla_oracle_forward_ex.argtypes = lib.kla_oracle_forward.argtypes + [ctypes.c_int]
     lib.kla_oracle_forward_varlen_ex.restype = ctypes.c_int
     lib.kla_oracle_forward_varlen_ex.argtypes = lib.kla_oracle_forward_varlen.argtypes + [ctypes.c_int]
+    if hasattr(lib, "kla_oracle_backward"):
+        lib.kla_oracle_backward.restype = ctypes.c_int
+        lib.kla_oracle_backward.argtypes = (
+            [ctypes.c_int] * 5 + [dp] * 5 + [ctypes.c_double] + [dp] * 9 + [ctypes.c_int] * 2)
     if hasattr(lib, "ccq_oracle_query"):
         lib.ccq_oracle_query.restype = ctypes.c_int
         lib.ccq_oracle_query.argtypes = [ctypes.c_int] * 4 + [dp] * 10
@@ -219,3 +229,59 @@ def ccq_query(q, k, lam, stats0=None):
     if rc != 0:
         raise RuntimeError(f"ccq_oracle_query failed rc={rc}")
     return qc, (Ms, ms, ns)
+
+
+def backward(q, k, v, alpha, eta, eps, S0, do, dS_T=None, nthreads: int = 1,
+             beta_mode: str = "kaczmarz"):
+    """Gradient of L = sum_t <do_t, o_t> + <dS_T, S_T> for the fixed-length
+    forward (see kla_oracle_bwd.c).  Returns (dq, dk, dv, dalpha, deta, dS0)."""
+    return _backward_with(_load(), q, k, v, alpha, eta, eps, S0, do, dS_T, nthreads, beta_mode)
+
+
+def _backward_with(lib, q, k, v, alpha, eta, eps, S0, do, dS_T, nthreads, beta_mode):
+    q, k, v, alpha, eta, S0, do, dS_T = map(_f64, (q, k, v, alpha, eta, S0, do, dS_T))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    assert k.shape == (B, T, H, dk) and v.shape == (B, T, H, dv) and do.shape == v.shape
+    assert (alpha is None or alpha.shape == (B, T, H)) and eta.shape == (B, T, H)
+    for x in (S0, dS_T):
+        assert x is None or x.shape == (B, H, dk, dv)
+    dq = np.zeros_like(q); dkk = np.zeros_like(k); dvv = np.zeros_like(v)
+    da = None if alpha is None else np.zeros_like(alpha)
+    de = np.zeros_like(eta)
+    dS0 = np.zeros((B, H, dk, dv))
+    rc = lib.kla_oracle_backward(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                                 _ptr(eta), float(eps), _ptr(S0), _ptr(do), _ptr(dS_T),
+                                 _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(da), _ptr(de),
+                                 _ptr(dS0), int(nthreads), _MODES[beta_mode])
+    if rc != 0:
+        raise RuntimeError(f"kla_oracle_backward failed rc={rc}")
+    return dq, dkk, dvv, da, de, dS0
+
+
+def source_bwd() -> str:
+    with open(_SRC_BWD) as f:
+        return f.read()
+
+
+def compile_bwd_variant(source_text: str, so_path: str):
+    """Compiles a modified copy of kla_oracle_bwd.c (for the tests that plant
+    mistakes in it) and returns an object with the same ``backward``."""
+    src_path = so_path[:-3] + ".c"
+    with open(src_path, "w") as f:
+        f.write(source_text)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-fno-fast-math",
+                    "-ffp-contract=off", "-o", so_path, src_path], check=True)
+    lib = ctypes.CDLL(so_path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.kla_oracle_backward.restype = ctypes.c_int
+    lib.kla_oracle_backward.argtypes = (
+        [ctypes.c_int] * 5 + [dp] * 5 + [ctypes.c_double] + [dp] * 9 + [ctypes.c_int] * 2)
+
+    class _Variant:
+        @staticmethod
+        def backward(q, k, v, alpha, eta, eps, S0, do, dS_T=None, nthreads=1,
+                     beta_mode="kaczmarz"):
+            return _backward_with(lib, q, k, v, alpha, eta, eps, S0, do, dS_T, nthreads,
+                                  beta_mode)
+    return _Variant
