@@ -95,6 +95,11 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
                                       I, I, I, I, I, vp, Z, vp]
         lib.kla_ccq_query_step.restype = I
         lib.kla_ccq_query_step.argtypes = [vp, vp, fp, fp, fp, fp, vp, I, I, I, I, vp]
+        lib.kla_chunk_bwd_workspace_size.restype = Z
+        lib.kla_chunk_bwd_workspace_size.argtypes = [I, I, I, I, I]
+        lib.kla_chunk_bwd.restype = I
+        lib.kla_chunk_bwd.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, fp, vp, vp, vp, fp, fp, fp,
+                                      I, I, I, I, I, I, I, I, vp, Z, vp]
         lib.kla_chunk_fwd_noalloc.restype = I
         lib.kla_chunk_fwd_noalloc.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, fp,
                                               I, I, I, I, I, I, I, vp]
@@ -205,6 +210,40 @@ def kla_chunk_fwd(q, k, v, alpha, eta, eps, S0=None, o=None, S_T=None, workspace
                               _mode(beta_mode), _ptr(workspace), wsb, _stream(stream))
     _check(st)
     return o, S_T
+
+
+def kla_chunk_bwd_workspace_size(B, T, H, dk, dtype=KLA_DTYPE_BF16) -> int:
+    return int(load().kla_chunk_bwd_workspace_size(B, T, H, dk, dtype))
+
+
+def kla_chunk_bwd(q, k, v, alpha, eta, eps, S0, d_o, dS_T=None, workspace=None, stream=None,
+                  chunk=CHUNK, beta_mode="kaczmarz", want_dS0=True):
+    """Backward of kla_chunk_fwd: the gradients of sum <d_o, o> + <dS_T, S_T>.
+    Inputs as kla_chunk_fwd; d_o: [B,T,H,dv] in q's dtype; dS_T: [B,H,dk,dv]
+    fp32 or None.  Returns (dq, dk, dv, dalpha, deta, dS0); dalpha is None when
+    alpha is None, dS0 None unless want_dS0."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    _need(q, "q"); _need(k, "k", q.dtype, (B, T, H, dk)); _need(v, "v", q.dtype, (B, T, H, dv))
+    _need(alpha, "alpha", torch.float32, (B, T, H)); _need(eta, "eta", torch.float32, (B, T, H))
+    _need(S0, "S0", torch.float32, (B, H, dk, dv)); _need(d_o, "d_o", q.dtype, (B, T, H, dv))
+    _need(dS_T, "dS_T", torch.float32, (B, H, dk, dv))
+    dq = torch.empty_like(q)
+    dkk = torch.empty_like(k)
+    dvv = torch.empty_like(v)
+    dalpha = None if alpha is None else torch.empty_like(alpha)
+    deta = torch.empty_like(eta)
+    dS0 = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device) if want_dS0 else None
+    nbytes = int(lib.kla_chunk_bwd_workspace_size(B, T, H, dk, dt))
+    workspace, wsb = _workspace(nbytes, q.device, workspace)
+    st = lib.kla_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps),
+                           _ptr(S0), _ptr(d_o), _ptr(dS_T), _ptr(dq), _ptr(dkk), _ptr(dvv),
+                           _ptr(dalpha), _ptr(deta), _ptr(dS0), B, T, H, dk, dv, chunk, dt,
+                           _mode(beta_mode), _ptr(workspace), wsb, _stream(stream))
+    _check(st)
+    return dq, dkk, dvv, dalpha, deta, dS0
 
 
 def kla_chunk_fwd_noalloc(q, k, v, alpha, eta, eps, S0=None, o=None, S_T=None, stream=None,

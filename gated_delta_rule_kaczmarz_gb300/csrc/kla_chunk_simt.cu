@@ -92,9 +92,17 @@ __global__ void __launch_bounds__(NT, 1) chunk_simt_kernel(Problem p) {
         sm.S[i][j] = p.S0 ? p.S0[sbase + (size_t)i * D + jb + j] : 0.f;
     }
 
+    const long nch = (len + C - 1) / C;
     for (long c0 = 0; c0 < len; c0 += C) {
         const int nc = (int)min((long)C, len - c0);
         __syncthreads();  // previous chunk finished with K, Q, V, S
+        if (p.S_chk) {    // the state at the chunk's start, for the backward pass
+            float *dst = p.S_chk + (((size_t)seq * H + h) * nch + c0 / C) * D * D;
+            for (int x = tid; x < D * DVB; x += NT) {
+                const int i = x / DVB, j = x % DVB;
+                dst[(size_t)i * D + jb + j] = sm.S[i][j];
+            }
+        }
 
         // ---- load the chunk (masked tail = identity tokens) ----
         for (int x = tid; x < C * D; x += NT) {
@@ -252,7 +260,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_simt_kernel(Problem p) {
 #pragma unroll
                 for (int n = 0; n < 8; ++n) acc[n] = fmaf(a, sm.U[s][jq + n], acc[n]);
             }
-            if (t < nc) {
+            if (o && t < nc) {
                 const size_t row = (size_t)(start + c0 + t) * H + h;
 #pragma unroll
                 for (int n = 0; n < 8; ++n) st_out(o, row * D + jb + jq + n, acc[n]);

@@ -39,6 +39,8 @@ struct Problem {
     int mode;                // 0: KLA; 1: the CCQ product y = M_t q (tensor-core path only)
     float *csum;             // mode 1: [chunk slots][d] per-chunk key sums (fixed length:
                              // slot (b * n_chunks + c) * H + h)
+    float *S_chk;            // CUDA-core path: the state at every chunk start
+                             // ([n_seq, H, n_chunks, d, d] fp32), or nullptr
     unsigned *status;        // device status word, or nullptr
     void *ws;                // workspace after the header (path specific)
     size_t ws_bytes;
@@ -74,6 +76,20 @@ cudaError_t launch_ccq(const CcqProblem &p, cudaStream_t s);
 cudaError_t launch_ccq_step(const void *q, const void *k, const float *lambda, float *Ms,
                             float *ms, float *ns, void *q_clean, int BH, int d, int dtype,
                             cudaStream_t s);
+
+// Backward of the fixed-length chunkwise forward (kla_chunk_bwd.cu).
+struct BwdProblem {
+    const void *q, *k, *v, *dout;
+    const float *alpha, *eta, *S0, *dS_T;
+    float eps;
+    void *dq, *dk, *dv;
+    float *dalpha, *deta, *dS0;
+    int B, T, H, d, dtype, beta_mode;
+    unsigned *status;
+    void *ws;                // chunk_bwd_workspace_bytes(B, T, H, d) after the header
+};
+size_t chunk_bwd_workspace_bytes(int B, int T, int H, int d);
+cudaError_t launch_chunk_bwd(const BwdProblem &p, cudaStream_t s);
 
 // Tensor-core (tcgen05) prefill for bf16, d = 128.
 size_t chunk_tc_workspace_bytes(long n_chunks_upper, int H, int n_seq);

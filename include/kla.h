@@ -223,6 +223,41 @@ KLA_API int kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                                   int dtype, void *stream);
 
 /*
+ * Backward pass of the fixed-length chunkwise forward (kla_chunk_fwd_ex with
+ * the same inputs and beta_mode): the gradients of the scalar
+ *
+ *     L = sum_t <d_o_t, o_t> + <dS_T, S_T>
+ *
+ * with respect to every input, by reverse-mode differentiation of the
+ * recurrence of the KLA summary (gist.science 2605.08587, "A Regra de
+ * Atualizacao KLA"), including the path through beta_t's key norm
+ * (d beta / d k = -2 eta k / (||k||^2 + eps)^2).  The chunk form it uses is
+ * the derivative of the blockwise solver of the same summary's
+ * "Implementacao" section.
+ *   q, k, v, alpha, eta, eps, S0, beta_mode : as kla_chunk_fwd_ex
+ *   d_o   : [B, T, H, dv] dtype, the gradient of o
+ *   dS_T  : [B, H, dk, dv] fp32, the gradient of S_T, or NULL (zero)
+ *   dq, dk, dv : [B, T, H, *] dtype (written)
+ *   dalpha, deta : [B, T, H] fp32 (written unless NULL; dalpha must be NULL
+ *           when alpha is NULL)
+ *   dS0   : [B, H, dk, dv] fp32 (written unless NULL)
+ *   workspace : kla_chunk_bwd_workspace_size(...) bytes, 256-byte aligned,
+ *           owned by the caller; it starts with the device status word and
+ *           holds the state and its gradient at every chunk boundary.
+ * dk == dv in {64, 128}, chunk 64, fp32 or bf16; arithmetic fp32 on the CUDA
+ * cores (three launches: the forward recording the chunk-start states, the
+ * chain of state gradients over the chunks in reverse, the per-chunk token
+ * gradients).  Asynchronous on `stream`.
+ */
+KLA_API size_t kla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dtype);
+KLA_API int kla_chunk_bwd(const void *q, const void *k, const void *v, const float *alpha,
+                          const float *eta, float eps, const float *S0, const void *d_o,
+                          const float *dS_T, void *dq, void *dk, void *dv, float *dalpha,
+                          float *deta, float *dS0, int B, int T, int H, int dk_, int dv_,
+                          int chunk, int dtype, int beta_mode, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+/*
  * Curvature-Conditioned Query (CCQ) read-side contraction ("Don't Read
  * Everything: A Curvature-Conditioned Query for Linear Attention",
  * gist.science 2606.01294, sections "O Mecanismo" and "Integracao"):

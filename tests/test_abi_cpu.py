@@ -181,3 +181,29 @@ def test_ccq_host_validation():
     assert g(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 2, 2, 64, 1, None) == \
         binding.KLA_ERR_INVALID_ARG
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 2, 64, 1, None) == binding.KLA_OK
+
+
+@no_gpu_only
+def test_backward_host_validation():
+    lib = binding.load()
+    f = lib.kla_chunk_bwd
+    base = [FAKE, FAKE, FAKE, FAKE, FAKE, 1e-6, None, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE,
+            None, 1, 64, 1, 64, 64, 64, 1, 0]
+    def call(over=None, ws=None, wsb=0):
+        a = list(base)
+        for i, x in (over or {}).items():
+            a[i] = x
+        return f(*a, ws, wsb, None)
+    # missing workspace
+    assert call() == binding.KLA_ERR_WORKSPACE
+    # dalpha without alpha
+    assert call({3: None}) == binding.KLA_ERR_INVALID_ARG
+    assert "dalpha" in lib.kla_last_error_message().decode()
+    # unknown beta mode, unsupported head size, missing d_o
+    assert call({22: 7}) == binding.KLA_ERR_INVALID_ARG
+    assert call({18: 96, 19: 96}) == binding.KLA_ERR_UNSUPPORTED
+    assert call({7: None}, ctypes.c_void_p(0x100000), 1 << 40) == binding.KLA_ERR_INVALID_ARG
+    # misaligned workspace
+    assert call(None, ctypes.c_void_p(0x100010), 1 << 40) == binding.KLA_ERR_INVALID_ARG
+    n = lib.kla_chunk_bwd_workspace_size(1, 64, 1, 64, 1)
+    assert n >= 2 * 64 * 64 * 4

@@ -1,0 +1,101 @@
+"""GPU parity of the backward pass (kla_chunk_bwd) against the fp64 backward
+oracle: every gradient (dq, dk, dv, dalpha, deta, dS0) element by element,
+error max|gpu - oracle| / max|oracle| within 1e-4 (fp32) and 2e-2 (bf16)."""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_kaczmarz_gb300 as kla
+import oracle
+from gated_delta_rule_kaczmarz_gb300.workloads import prefill_inputs
+from tests._util import TOL, cuda, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _grad_inputs(B, T, H, d, dtype, seed):
+    rng = np.random.default_rng(seed)
+    t = torch.bfloat16 if dtype == "bf16" else torch.float32
+    do = torch.from_numpy(rng.standard_normal((B, T, H, d)).astype(np.float32)).to(t)
+    dST = torch.from_numpy((0.1 * rng.standard_normal((B, H, d, d))).astype(np.float32))
+    return do, dST
+
+
+def _check(g, ref, tol, names=("dq", "dk", "dv", "dalpha", "deta", "dS0")):
+    for n, a, b in zip(names, g, ref):
+        if b is None:
+            assert a is None, n
+            continue
+        e = rel_err(a, b)
+        assert e <= tol, f"{n}: {e:.3e} > {tol}"
+
+
+@pytest.mark.parametrize("B,T,H,d,dtype,mode,no_alpha,with_dST,with_S0", [
+    (1, 256, 2, 64, "fp32", "kaczmarz", False, True, True),
+    (2, 130, 2, 128, "fp32", "kaczmarz", False, True, True),
+    (1, 77, 3, 64, "fp32", "given", False, False, True),
+    (2, 64, 2, 128, "fp32", "kaczmarz", True, True, False),
+    (2, 200, 2, 128, "bf16", "kaczmarz", False, True, True),
+    (1, 320, 2, 128, "bf16", "given", False, True, False),
+    (3, 5, 2, 64, "bf16", "kaczmarz", False, False, True)])
+def test_backward_parity(B, T, H, d, dtype, mode, no_alpha, with_dST, with_S0):
+    inp = prefill_inputs(B, T, H, d, d, dtype, seed=200 + T, s0_var=0.01)
+    do, dST = _grad_inputs(B, T, H, d, dtype, 300 + T)
+    alpha = None if no_alpha else inp["alpha"]
+    S0 = inp["S0"] if with_S0 else None
+    dST = dST if with_dST else None
+    g = cuda(dict(inp, do=do, dST=dST))
+    got = kla.kla_chunk_bwd(g["q"], g["k"], g["v"], None if no_alpha else g["alpha"], g["eta"],
+                            inp["eps"], g["S0"] if with_S0 else None, g["do"],
+                            g["dST"] if with_dST else None, beta_mode=mode)
+    torch.cuda.synchronize()
+    ref = oracle.backward(inp["q"], inp["k"], inp["v"], alpha, inp["eta"], inp["eps"], S0, do,
+                          dST, nthreads=8, beta_mode=mode)
+    _check(got, ref, TOL[inp["q"].dtype])
+
+
+def test_backward_launches_and_status():
+    B, T, H, d = 2, 192, 2, 128
+    inp = prefill_inputs(B, T, H, d, d, "bf16", seed=5)
+    do, dST = _grad_inputs(B, T, H, d, "bf16", 6)
+    g = cuda(dict(inp, do=do, dST=dST))
+    ws = torch.zeros(kla.kla_chunk_bwd_workspace_size(B, T, H, d), dtype=torch.uint8,
+                     device="cuda")
+    args = (g["q"], g["k"], g["v"], g["alpha"], g["eta"], inp["eps"], g["S0"], g["do"], g["dST"])
+    kla.kla_chunk_bwd(*args, workspace=ws)
+    torch.cuda.synchronize()
+    n0 = kla.kla_launch_count()
+    kla.kla_chunk_bwd(*args, workspace=ws)
+    torch.cuda.synchronize()
+    assert kla.kla_launch_count() - n0 == 3
+    assert kla.kla_workspace_status(ws) == 0
+
+
+def test_backward_no_tokens_passes_the_state_gradient():
+    B, H, d = 2, 2, 64
+    q = torch.zeros((B, 0, H, d), device="cuda")
+    eta = torch.zeros((B, 0, H), device="cuda")
+    dST = torch.randn((B, H, d, d), device="cuda")
+    _, _, _, _, _, dS0 = kla.kla_chunk_bwd(q, q, q, eta, eta, 1e-6, None, q, dST)
+    torch.cuda.synchronize()
+    assert torch.equal(dS0, dST)
+
+
+def test_backward_full_size_sampled():
+    """The layer workload (B4 H8 T2048 d128 bf16): all gradients of two sampled
+    (batch, head) units against the oracle run on those units alone."""
+    from gated_delta_rule_kaczmarz_gb300.workloads import WORKLOADS
+    wl = WORKLOADS["layer_prefill"]
+    inp = wl.make()
+    do, dST = _grad_inputs(wl.B, wl.T, wl.H, wl.d, "bf16", 7)
+    g = cuda(dict(inp, do=do, dST=dST))
+    got = kla.kla_chunk_bwd(g["q"], g["k"], g["v"], g["alpha"], g["eta"], wl.eps, g["S0"],
+                            g["do"], g["dST"])
+    torch.cuda.synchronize()
+    for b, h in ((0, 0), (3, 5)):
+        tok = lambda x: x[b:b + 1, :, h:h + 1].contiguous()
+        st = lambda x: x[b:b + 1, h:h + 1].contiguous()
+        ref = oracle.backward(tok(inp["q"]), tok(inp["k"]), tok(inp["v"]), tok(inp["alpha"]),
+                              tok(inp["eta"]), wl.eps, st(inp["S0"]), tok(do), st(dST))
+        sub = [tok(got[0]), tok(got[1]), tok(got[2]), tok(got[3]), tok(got[4]), st(got[5])]
+        _check(sub, ref, TOL[torch.bfloat16])
