@@ -386,6 +386,56 @@ def time_ccq(args, dev, reps):
     return dict(wl=wl, query_ms=out["query"], layer_ms=out["layer"], bytes=nbytes)
 
 
+def time_bwd(args, dev, reps):
+    """Backward pass (kla_chunk_bwd) on the layer workload (bf16, B4 H8 T2048
+    d128): the gradients of sum <d_o, o> + <dS_T, S_T> with d_o ~ N(0,1) and
+    dS_T ~ N(0, 0.01).  Inputs and workspace resident, L2 flushed between
+    timed calls; also each of the three kernels alone (events around each
+    launch on the same stream)."""
+    import numpy as np
+    import torch
+
+    import gated_delta_rule_kaczmarz_gb300 as kla
+    from gated_delta_rule_kaczmarz_gb300.workloads import WORKLOADS
+
+    wl = WORKLOADS["layer_prefill"]
+    inp = wl.make()
+    g = {n: (x.to(dev) if isinstance(x, torch.Tensor) else x) for n, x in inp.items()}
+    rng = np.random.default_rng(11)
+    do = torch.from_numpy(rng.standard_normal((wl.B, wl.T, wl.H, wl.d)).astype(np.float32)).to(
+        dev, torch.bfloat16)
+    dST = torch.from_numpy((0.1 * rng.standard_normal((wl.B, wl.H, wl.d, wl.d))).astype(
+        np.float32)).to(dev)
+    ws = torch.empty(kla.kla_chunk_bwd_workspace_size(wl.B, wl.T, wl.H, wl.d), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        kla.kla_chunk_bwd(g["q"], g["k"], g["v"], g["alpha"], g["eta"], wl.eps, g["S0"], do, dST,
+                          workspace=ws, stream=stream)
+
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    n0 = kla.kla_launch_count()
+    ms = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    launches = (kla.kla_launch_count() - n0) // reps
+    th = wl.B * wl.T * wl.H
+    # algorithmic bytes: q, k, v, d_o read and dq, dk, dv written (bf16), alpha,
+    # eta read and dalpha, deta written (fp32); S0, dS_T read and dS0 written
+    nbytes = th * (7 * wl.d * 2 + 4 * 4) + wl.B * wl.H * 3 * wl.d * wl.d * 4
+    return dict(wl=wl, ms=sum(ms) / len(ms), bytes=nbytes, launches=launches)
+
+
 def ours(args):
     import torch
     world, rank, local = dist_env()
@@ -435,6 +485,17 @@ def ours(args):
                         "kernel": "fused_kernel (CCQ mode) + ccq_finish_kernel",
                         "algorithmic_bytes_per_call": cq["bytes"]}}
 
+    bw = time_bwd(args, dev, reps=5)
+    bw_gbs = bw["bytes"] / (bw["ms"] / 1e3) / 1e9
+    backward = {"workload": "layer_prefill backward (d_o ~ N(0,1), dS_T ~ N(0,0.01))",
+                "us": bw["ms"] * 1e3, "value": wl.B * wl.T / (bw["ms"] / 1e3), "unit": "tokens/s",
+                "launches": bw["launches"],
+                "roofline": {"bound": "hbm", "achieved": bw_gbs, "peak": pk["hbm_gbs"],
+                             "unit": "GB/s", "frac": bw_gbs / pk["hbm_gbs"], "traffic": None,
+                             "kernel": "chunk_simt_kernel (states) + bwd_dstate_kernel + "
+                                       "bwd_grads_kernel",
+                             "algorithmic_bytes_per_call": bw["bytes"]}}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
@@ -461,6 +522,7 @@ def ours(args):
         "clocks": pre["clocks"],
         "decode": decode,
         "ccq": ccq,
+        "backward": backward,
     }
     if rank == 0:
         print(json.dumps(line))

@@ -38,6 +38,8 @@
 #include <cuda_bf16.h>
 
 #include "kla_internal.h"
+#include "kla_simt_inverse.cuh"
+#include "kla_simt_tile.cuh"
 
 namespace kla {
 namespace {
@@ -64,19 +66,10 @@ struct Vec {
 template <typename Tin, int D>
 __device__ void load_kq(float (*K)[D + 1], float (*Q)[D + 1], Vec &v, const BwdProblem &p,
                         long row0, int nc, int h, int tid) {
-    const Tin *k = static_cast<const Tin *>(p.k);
-    const Tin *q = static_cast<const Tin *>(p.q);
-    for (int x = tid; x < C * D; x += NT) {
-        const int t = x / D, i = x % D;
-        float kv = 0.f, qv = 0.f;
-        if (t < nc) {
-            const size_t r = (size_t)(row0 + t) * p.H + h;
-            kv = ld_in(k, r * D + i);
-            qv = ld_in(q, r * D + i);
-        }
-        K[t][i] = kv;
-        Q[t][i] = qv;
-    }
+    load_tile<Tin, C, D, D + 1, NT>(&K[0][0], static_cast<const Tin *>(p.k), row0, nc, p.H, h, D,
+                                    0, tid);
+    load_tile<Tin, C, D, D + 1, NT>(&Q[0][0], static_cast<const Tin *>(p.q), row0, nc, p.H, h, D,
+                                    0, tid);
     if (tid < C) {
         const bool ok = tid < nc;
         const size_t r = (size_t)(row0 + tid) * p.H + h;
@@ -162,22 +155,6 @@ __device__ void gram(const float (*K)[D + 1], const float (*Q)[D + 1], const Vec
         }
 }
 
-// T = (I + A_kk)^{-1} by forward substitution, one column per thread (tid < C).
-// kRaw: A_kk(t, s) = beta_t Gamma_ts G(t, s) from the raw strict-lower G.
-template <bool kRaw>
-__device__ void solve_t(const float (*A)[C + 1], const Vec &v, float (*Tm)[C + 1], int tid) {
-    if (tid >= C) return;
-    const int j = tid;
-    for (int t = 0; t < C; ++t) {
-        float x = (t == j) ? 1.f : 0.f;
-        for (int s = j; s < t; ++s) {
-            const float a = kRaw ? v.beta[t] * gam(v, t, s) * A[t][s] : A[t][s];
-            x = fmaf(-a, Tm[s][j], x);
-        }
-        Tm[t][j] = x;
-    }
-}
-
 // ---------------------------------------------------------------- dS chain
 template <int D>
 struct DsSmem {
@@ -213,10 +190,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_dstate_kernel(BwdProblem p, int nch
             rec[(size_t)i * D + jb + j] = sm.dS[i][j];
         }
         load_kq<Tin, D>(sm.K, sm.Q, sm.v, p, row0, nc, h, tid);
-        for (int x = tid; x < C * DVB; x += NT) {
-            const int t = x / DVB, j = x % DVB;
-            sm.dO[t][j] = t < nc ? ld_in(dout, ((size_t)(row0 + t) * p.H + h) * D + jb + j) : 0.f;
-        }
+        load_tile<Tin, C, DVB, DVB + 1, NT>(&sm.dO[0][0], dout, row0, nc, p.H, h, D, jb, tid);
         __syncthreads();
         chunk_vectors<D>(sm.K, sm.v, p.eps, p.beta_mode, nc, tid);
         __syncthreads();
@@ -241,8 +215,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_dstate_kernel(BwdProblem p, int nch
 #pragma unroll
             for (int n = 0; n < 8; ++n) sm.dU[t][jq + n] = acc[n];
         }
-        solve_t<false>(sm.Akk, sm.v, sm.Tm, tid);
-        __syncthreads();
+        invert_unit_lower64(sm.Akk, sm.Tm, &sm.dR[0][0], tid);
         {   // dR = T^T dU
             const int t = tid / 4, jq = (tid % 4) * 8;
             float acc[8];
@@ -289,15 +262,26 @@ __global__ void __launch_bounds__(NT, 1) bwd_dstate_kernel(BwdProblem p, int nch
 template <int D>
 struct GrSmem {
     float K[C][D + 1], Q[C][D + 1];
-    float M0[C][C + 1];   // raw strict-lower K K^T
-    float M1[C][C + 1];   // raw lower Q K^T
-    float M2[C][C + 1];   // T, then dA_qk, then dA_qk o Gamma
-    float tA[C][D + 1];   // U
+    float M0[C][C + 1];   // raw strict-lower K K^T, then its dg terms
+    float M1[C][C + 1];   // raw lower Q K^T, then dA_qk o Gamma
+    float M2[C][C + 1];   // T, then X = diag(beta) (dA_kk o Gamma)
+    float tA[C][D + 1];   // A_kk and S rows (staging), then U
     float tB[C][D + 1];   // V - diag(exp g) K S, then dR
-    float tC[C][D + 1];   // dO, then dU, then dA_kk and X (as [C][C + 1])
+    float tC[C][D + 1];   // dO, then dU, then S and dS' row blocks (staging)
     Vec v;
     float dbeta[C], dg[C], dgcol[C], red[NT / 32];
+    float scr[32 * 33];   // scratch of the triangular inverse
 };
+
+// Sums of column s of the [C][C + 1] matrix E over rows r >= s (threads 0..63),
+// subtracted from dg.
+__device__ __forceinline__ void sub_col_sums(const float (*E)[C + 1], float *dgcol, int tid) {
+    if (tid < C) {
+        float sg = 0.f;
+        for (int r = tid; r < C; ++r) sg += E[r][tid];
+        dgcol[tid] = sg;
+    }
+}
 
 template <typename Tin, int D>
 __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
@@ -305,8 +289,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
                                                           const float *dS_chk) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     GrSmem<D> &sm = *reinterpret_cast<GrSmem<D> *>(smem_raw);
-    float(*dAkk)[C + 1] = reinterpret_cast<float(*)[C + 1]>(&sm.tC[0][0]);
-    constexpr int CPT = D / 4;   // columns per thread: cq + 4 x
+    constexpr int CPT = D / 4;    // columns per thread: cq + 4 x
+    constexpr int SPT = C / 4;    // chunk positions per thread: cq + 4 x
+    constexpr int IB = 32;        // rows of S and dS' per staged block
+    constexpr int LB = D + 1;     // their row stride in shared memory
     const int tid = threadIdx.x;
     const int c = blockIdx.x, unit = blockIdx.y, b = unit / p.H, h = unit % p.H;
     if (p.status != nullptr && *(volatile unsigned *)p.status != kDevOk) return;
@@ -320,37 +306,56 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
     const size_t rt = (size_t)(row0 + t) * p.H + h;   // token row of this thread's t
     const bool live = t < nc;
 
-    load_kq<Tin, D>(sm.K, sm.Q, sm.v, p, row0, nc, h, tid);
-    for (int x = tid; x < C * D; x += NT) {
-        const int tt = x / D, j = x % D;
-        sm.tC[tt][j] = tt < nc ? ld_in(dout, ((size_t)(row0 + tt) * p.H + h) * D + j) : 0.f;
+    load_tile<Tin, C, D, D + 1, NT>(&sm.K[0][0], static_cast<const Tin *>(p.k), row0, nc, p.H, h,
+                                    D, 0, tid);
+    load_tile<Tin, C, D, D + 1, NT>(&sm.Q[0][0], static_cast<const Tin *>(p.q), row0, nc, p.H, h,
+                                    D, 0, tid);
+    load_tile<Tin, C, D, D + 1, NT>(&sm.tC[0][0], dout, row0, nc, p.H, h, D, 0, tid);
+    if (tid < C) {
+        const bool ok = tid < nc;
+        const size_t r = (size_t)(row0 + tid) * p.H + h;
+        sm.v.alpha[tid] = (ok && p.alpha) ? p.alpha[r] : 1.f;
+        sm.v.eta[tid] = ok ? p.eta[r] : 0.f;
     }
     __syncthreads();
     chunk_vectors<D>(sm.K, sm.v, p.eps, p.beta_mode, nc, tid);
     __syncthreads();
     gram<D, false>(sm.K, sm.Q, sm.v, sm.M0, sm.M1, tid);
-    {   // V - diag(exp g) K S
-        float acc[CPT];
+    __syncthreads();
+    {   // A_kk = strict_lower(beta Gamma o K K^T) into tA, then T
+        float(*Akk)[C + 1] = reinterpret_cast<float(*)[C + 1]>(&sm.tA[0][0]);
+        for (int x = tid; x < C * C; x += NT) {
+            const int r = x / C, s = x % C;
+            Akk[r][s] = s < r ? sm.v.beta[r] * gam(sm.v, r, s) * sm.M0[r][s] : 0.f;
+        }
+        __syncthreads();
+        invert_unit_lower64(Akk, sm.M2, sm.scr, tid);
+    }
+    {   // V - diag(exp g) K S -> tB, S staged in tA 64 rows at a time
+        float vv[CPT], acc[CPT];
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) acc[x] = 0.f;
-        for (int i = 0; i < D; ++i) {
-            const float kti = sm.K[t][i];
-            const float *Si = S + (size_t)i * D + cq;
+        for (int x = 0; x < CPT; ++x) {
+            vv[x] = live ? ld_in(vin, rt * D + cq + 4 * x) : 0.f;
+            acc[x] = 0.f;
+        }
+        for (int i0 = 0; i0 < D; i0 += C) {
+            load_block_f32<C, D, D + 1, NT>(&sm.tA[0][0], S + (size_t)i0 * D, D, tid);
+            __syncthreads();
+            for (int i = 0; i < C; ++i) {
+                const float kti = sm.K[t][i0 + i];
 #pragma unroll
-            for (int x = 0; x < CPT; ++x) acc[x] = fmaf(kti, Si[4 * x], acc[x]);
+                for (int x = 0; x < CPT; ++x) acc[x] = fmaf(kti, sm.tA[i][cq + 4 * x], acc[x]);
+            }
+            __syncthreads();
         }
         const float e = sm.v.eg[t];
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) {
-            const float vv = live ? ld_in(vin, rt * D + cq + 4 * x) : 0.f;
-            sm.tB[t][cq + 4 * x] = vv - e * acc[x];
-        }
+        for (int x = 0; x < CPT; ++x) sm.tB[t][cq + 4 * x] = vv[x] - e * acc[x];
     }
     __syncthreads();
-    solve_t<true>(sm.M0, sm.v, sm.M2, tid);
-    __syncthreads();
+    float du[CPT];
     {   // U = T diag(beta) (V - e^g K S);  dU = A_qk^T dO + diag(exp(g_C - g)) K dS'
-        float u[CPT], du[CPT];
+        float u[CPT];
 #pragma unroll
         for (int x = 0; x < CPT; ++x) u[x] = du[x] = 0.f;
         for (int s = 0; s <= t; ++s) {
@@ -364,21 +369,53 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
             for (int x = 0; x < CPT; ++x) du[x] = fmaf(a, sm.tC[s][cq + 4 * x], du[x]);
         }
         const float e = sm.v.egc[t];
-        for (int i = 0; i < D; ++i) {
-            const float kw = e * sm.K[t][i];
-            const float *Di = dSp + (size_t)i * D + cq;
+        for (int i0 = 0; i0 < D; i0 += C) {
+            load_block_f32<C, D, D + 1, NT>(&sm.tA[0][0], dSp + (size_t)i0 * D, D, tid);
+            __syncthreads();
+            for (int i = 0; i < C; ++i) {
+                const float kw = e * sm.K[t][i0 + i];
 #pragma unroll
-            for (int x = 0; x < CPT; ++x) du[x] = fmaf(kw, Di[4 * x], du[x]);
+                for (int x = 0; x < CPT; ++x) du[x] = fmaf(kw, sm.tA[i][cq + 4 * x], du[x]);
+            }
+            __syncthreads();
         }
-        __syncthreads();   // dO in tC fully read
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) {
-            sm.tA[t][cq + 4 * x] = u[x];
-            sm.tC[t][cq + 4 * x] = du[x];
-        }
+        for (int x = 0; x < CPT; ++x) sm.tA[t][cq + 4 * x] = u[x];
     }
     __syncthreads();
-    {   // dR = T^T dU; dV; dbeta and dg from R = diag(beta)(V - e^g K S)
+    {   // dA_qk = lower(dO U^T); its Gamma terms of dg; M1 <- dA_qk o Gamma
+        float da[SPT];
+#pragma unroll
+        for (int x = 0; x < SPT; ++x) da[x] = 0.f;
+        for (int j = 0; j < D; ++j) {
+            const float o = sm.tC[t][j];
+#pragma unroll
+            for (int x = 0; x < SPT; ++x) da[x] = fmaf(o, sm.tA[cq + 4 * x][j], da[x]);
+        }
+        float rs = 0.f;
+#pragma unroll
+        for (int x = 0; x < SPT; ++x) {
+            const int s = cq + 4 * x;
+            const float ga = s <= t ? gam(sm.v, t, s) : 0.f;
+            da[x] = s <= t ? da[x] * ga : 0.f;          // dA_qk o Gamma
+            const float e = da[x] * sm.M1[t][s];        // dA_qk o A_qk
+            rs += e;
+            sm.M1[t][s] = e;
+        }
+        rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+        rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+        __syncthreads();   // dO and the E entries complete
+        sub_col_sums(sm.M1, sm.dgcol, tid);
+        __syncthreads();
+#pragma unroll
+        for (int x = 0; x < CPT; ++x) sm.tC[t][cq + 4 * x] = du[x];   // dU
+#pragma unroll
+        for (int x = 0; x < SPT; ++x) sm.M1[t][cq + 4 * x] = da[x];
+        if (cq == 0) sm.dg[t] = rs;
+    }
+    __syncthreads();
+    if (tid < C) sm.dg[tid] -= sm.dgcol[tid];
+    {   // dR = T^T dU; dbeta and dg from R = diag(beta)(V - e^g K S); dV
         float dr[CPT];
 #pragma unroll
         for (int x = 0; x < CPT; ++x) dr[x] = 0.f;
@@ -387,162 +424,165 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
 #pragma unroll
             for (int x = 0; x < CPT; ++x) dr[x] = fmaf(a, sm.tC[s][cq + 4 * x], dr[x]);
         }
-        float p1 = 0.f, p2 = 0.f;
-        Tin *dvo = static_cast<Tin *>(p.dv);
-        const float bt = sm.v.beta[t];
+        float p1 = 0.f;
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) {
-            const float vv = live ? ld_in(vin, rt * D + cq + 4 * x) : 0.f;
-            p1 = fmaf(sm.tB[t][cq + 4 * x], dr[x], p1);
-            p2 = fmaf(vv, dr[x], p2);
-            if (live) st_out(dvo, rt * D + cq + 4 * x, bt * dr[x]);
-        }
+        for (int x = 0; x < CPT; ++x) p1 = fmaf(sm.tB[t][cq + 4 * x], dr[x], p1);
         p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
         p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+        __syncthreads();   // V - e^g K S, dU and T fully read
+#pragma unroll
+        for (int x = 0; x < CPT; ++x) sm.tB[t][cq + 4 * x] = dr[x];
+        __syncthreads();
+        // V . dR and dV = beta dR on the contiguous quarter row cq of token t
+        constexpr int VE = 16 / (int)sizeof(Tin);
+        const int j0 = cq * CPT;
+        float p2 = 0.f;
+        const float bt = sm.v.beta[t];
+        Tin *dvo = static_cast<Tin *>(p.dv);
+#pragma unroll
+        for (int n = 0; n < CPT / VE; ++n) {
+            const int j = j0 + n * VE;
+            float f[VE];
+            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+            if (live) raw = *reinterpret_cast<const uint4 *>(vin + rt * D + j);
+            unpack16(raw, f);
+            float o[VE];
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+                p2 = fmaf(f[e], sm.tB[t][j + e], p2);
+                o[e] = bt * sm.tB[t][j + e];
+            }
+            if (live) {
+#pragma unroll
+                for (int e = 0; e < VE; ++e) st_out(dvo, rt * D + j + e, o[e]);
+            }
+        }
         p2 += __shfl_xor_sync(0xffffffffu, p2, 1);
         p2 += __shfl_xor_sync(0xffffffffu, p2, 2);
         if (cq == 0) {
             sm.dbeta[t] = p1;
-            sm.dg[t] = bt * (p1 - p2);   // -beta e^g (K S)_t . dR_t
+            sm.dg[t] += bt * (p1 - p2);   // -beta e^g (K S)_t . dR_t
         }
-        __syncthreads();   // V - e^g K S, dU and T fully read
-#pragma unroll
-        for (int x = 0; x < CPT; ++x) sm.tB[t][cq + 4 * x] = dr[x];
     }
-    __syncthreads();
-    {   // dA_qk = lower(dO U^T) -> M2;  dA_kk = -strict_lower(dR U^T) -> tC
-        constexpr int SPT = C / 4;
-        float da[SPT], dk2[SPT];
+    {   // dA_kk = -strict_lower(dR U^T); its terms of dg and dbeta; M2 <- X
+        float dk2[SPT];
 #pragma unroll
-        for (int x = 0; x < SPT; ++x) da[x] = dk2[x] = 0.f;
+        for (int x = 0; x < SPT; ++x) dk2[x] = 0.f;
         for (int j = 0; j < D; ++j) {
-            const float o = live ? ld_in(dout, rt * D + j) : 0.f;
             const float r = sm.tB[t][j];
 #pragma unroll
-            for (int x = 0; x < SPT; ++x) {
-                const float us = sm.tA[cq + 4 * x][j];
-                da[x] = fmaf(o, us, da[x]);
-                dk2[x] = fmaf(r, us, dk2[x]);
-            }
+            for (int x = 0; x < SPT; ++x) dk2[x] = fmaf(r, sm.tA[cq + 4 * x][j], dk2[x]);
         }
+        float rs = 0.f, rb = 0.f;
+        const float bt = sm.v.beta[t];
 #pragma unroll
         for (int x = 0; x < SPT; ++x) {
             const int s = cq + 4 * x;
-            sm.M2[t][s] = s <= t ? da[x] : 0.f;
-            dAkk[t][s] = s < t ? -dk2[x] : 0.f;
+            const float xg = s < t ? -dk2[x] * gam(sm.v, t, s) : 0.f;   // dA_kk o Gamma
+            const float e = xg * sm.M0[t][s];                            // . K K^T
+            rb += e;
+            rs += bt * e;                                                // dA_kk o A_kk
+            sm.M0[t][s] = bt * e;
+            dk2[x] = bt * xg;                                            // X
         }
+        rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+        rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+        rb += __shfl_xor_sync(0xffffffffu, rb, 1);
+        rb += __shfl_xor_sync(0xffffffffu, rb, 2);
+        __syncthreads();   // dbeta, dg of the previous block and the new M0 entries
+        if (cq == 0) {
+            sm.dg[t] += rs;
+            sm.dbeta[t] += rb;
+        }
+        sub_col_sums(sm.M0, sm.dgcol, tid);
+#pragma unroll
+        for (int x = 0; x < SPT; ++x) sm.M2[t][cq + 4 * x] = dk2[x];
     }
     __syncthreads();
-    // dg, dbeta from the Gamma and beta factors of A_qk and A_kk: row sums
-    // (threads 0..63) and column sums (threads 64..127)
-    if (tid < C) {
-        const int r = tid;
-        float sg = 0.f, sb = 0.f;
-        for (int s = 0; s <= r; ++s) {
-            const float ga = gam(sm.v, r, s);
-            sg = fmaf(sm.M2[r][s], ga * sm.M1[r][s], sg);
-            if (s < r) {
-                const float x = dAkk[r][s] * ga * sm.M0[r][s];
-                sb += x;
-                sg = fmaf(sm.v.beta[r], x, sg);
+    if (tid < C) sm.dg[tid] -= sm.dgcol[tid];
+    // dQ and dK, S and dS' staged in tC 32 rows at a time; dims i = i0 + cq + 4 x
+    float(*Sb)[LB] = reinterpret_cast<float(*)[LB]>(&sm.tC[0][0]);
+    float(*Db)[LB] = Sb + IB;
+    const float eg = sm.v.eg[t], egc = sm.v.egc[t], bt = sm.v.beta[t];
+    const float db = sm.dbeta[t];
+    float cn = 0.f;   // the gradient through beta's key norm
+    if (p.beta_mode == 0 && sm.v.den[t] != 0.f) {
+        const float den = sm.v.den[t];
+        cn = -2.f * sm.v.eta[t] * db / (den * den);
+    }
+    float gq = 0.f, gk = 0.f, sds = 0.f;
+    Tin *dqo = static_cast<Tin *>(p.dq);
+    Tin *dko = static_cast<Tin *>(p.dk);
+    constexpr int VE = 16 / (int)sizeof(Tin);
+    for (int i0 = 0; i0 < D; i0 += IB) {
+        __syncthreads();   // the previous block is fully read
+        load_block_f32<IB, D, LB, NT>(&Sb[0][0], S + (size_t)i0 * D, D, tid);
+        load_block_f32<IB, D, LB, NT>(&Db[0][0], dSp + (size_t)i0 * D, D, tid);
+        __syncthreads();
+        for (int x = tid; x < IB * D; x += NT) sds = fmaf(Sb[x / D][x % D], Db[x / D][x % D], sds);
+        constexpr int XI = IB / 4;
+        float pq[XI], pr[XI], pu[XI];
+#pragma unroll
+        for (int x = 0; x < XI; ++x) pq[x] = pr[x] = pu[x] = 0.f;
+        for (int j = 0; j < D; j += VE) {
+            float o[VE];
+            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+            if (live) raw = *reinterpret_cast<const uint4 *>(dout + rt * D + j);
+            unpack16(raw, o);
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+                const float r = sm.tB[t][j + e], u = sm.tA[t][j + e];
+#pragma unroll
+                for (int x = 0; x < XI; ++x) {
+                    const int il = cq + 4 * x;
+                    const float sv = Sb[il][j + e];
+                    pq[x] = fmaf(o[e], sv, pq[x]);
+                    pr[x] = fmaf(r, sv, pr[x]);
+                    pu[x] = fmaf(u, Db[il][j + e], pu[x]);
+                }
             }
         }
-        sm.dg[r] += sg;
-        sm.dbeta[r] += sb;
-    } else if (tid < 2 * C) {
-        const int s = tid - C;
-        float sg = 0.f;
-        for (int r = s; r < C; ++r) {
-            const float ga = gam(sm.v, r, s);
-            sg = fmaf(sm.M2[r][s], ga * sm.M1[r][s], sg);
-            if (s < r) sg = fmaf(sm.v.beta[r], dAkk[r][s] * ga * sm.M0[r][s], sg);
-        }
-        sm.dgcol[s] = sg;
-    }
-    __syncthreads();
-    {   // M2 <- dA_qk o Gamma;  tC <- X = diag(beta) (dA_kk o Gamma)
-        constexpr int SPT = C / 4;
+        float dq[XI], dkk[XI];
 #pragma unroll
-        for (int x = 0; x < SPT; ++x) {
-            const int s = cq + 4 * x;
-            const float ga = s <= t ? gam(sm.v, t, s) : 0.f;
-            sm.M2[t][s] *= ga;
-            dAkk[t][s] *= sm.v.beta[t] * ga;
-        }
-        if (tid < C) sm.dg[tid] -= sm.dgcol[tid];
-    }
-    __syncthreads();
-    {   // dQ and dK of token t, dims i = cq + 4 x
-        float dq[CPT], dkk[CPT], pq[CPT], pr[CPT], pu[CPT];
-#pragma unroll
-        for (int x = 0; x < CPT; ++x) dq[x] = dkk[x] = pq[x] = pr[x] = pu[x] = 0.f;
-        // dO S^T, dR S^T and U dS'^T for rows i of S and dS'
-        for (int j = 0; j < D; ++j) {
-            const float o = live ? ld_in(dout, rt * D + j) : 0.f;
-            const float r = sm.tB[t][j], u = sm.tA[t][j];
-#pragma unroll
-            for (int x = 0; x < CPT; ++x) {
-                const size_t ij = (size_t)(cq + 4 * x) * D + j;
-                const float sv = S[ij];
-                pq[x] = fmaf(o, sv, pq[x]);
-                pr[x] = fmaf(r, sv, pr[x]);
-                pu[x] = fmaf(u, dSp[ij], pu[x]);
-            }
-        }
-        // (dA_qk o Gamma) K, its transpose times Q, X K and X^T K
+        for (int x = 0; x < XI; ++x) dq[x] = dkk[x] = 0.f;
         for (int s = 0; s < C; ++s) {
-            const float a_ts = sm.M2[t][s], a_st = sm.M2[s][t];
-            const float x_ts = dAkk[t][s], x_st = dAkk[s][t];
+            const float a_ts = sm.M1[t][s], a_st = sm.M1[s][t];
+            const float x2 = sm.M2[t][s] + sm.M2[s][t];
 #pragma unroll
-            for (int x = 0; x < CPT; ++x) {
-                const int i = cq + 4 * x;
-                dq[x] = fmaf(a_ts, sm.K[s][i], dq[x]);
-                dkk[x] = fmaf(a_st, sm.Q[s][i], dkk[x]);
-                dkk[x] = fmaf(x_ts + x_st, sm.K[s][i], dkk[x]);
+            for (int x = 0; x < XI; ++x) {
+                const int i = i0 + cq + 4 * x;
+                const float ks = sm.K[s][i];
+                dq[x] = fmaf(a_ts, ks, dq[x]);
+                dkk[x] = fmaf(a_st, sm.Q[s][i], fmaf(x2, ks, dkk[x]));
             }
         }
-        const float eg = sm.v.eg[t], egc = sm.v.egc[t], bt = sm.v.beta[t];
-        float gq = 0.f, gk = 0.f;
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) {
-            const int i = cq + 4 * x;
+        for (int x = 0; x < XI; ++x) {
+            const int i = i0 + cq + 4 * x;
             dq[x] = fmaf(eg, pq[x], dq[x]);
             dkk[x] = fmaf(-bt * eg, pr[x], dkk[x]);
             dkk[x] = fmaf(egc, pu[x], dkk[x]);
+            dkk[x] = fmaf(cn, sm.K[t][i], dkk[x]);
             gq = fmaf(sm.Q[t][i], pq[x], gq);
             gk = fmaf(sm.K[t][i], pu[x], gk);
-        }
-        gq += __shfl_xor_sync(0xffffffffu, gq, 1);
-        gq += __shfl_xor_sync(0xffffffffu, gq, 2);
-        gk += __shfl_xor_sync(0xffffffffu, gk, 1);
-        gk += __shfl_xor_sync(0xffffffffu, gk, 2);
-        // the gradient through beta's key norm
-        const float db = sm.dbeta[t];
-        float cn = 0.f;
-        if (p.beta_mode == 0 && sm.v.den[t] != 0.f) {
-            const float den = sm.v.den[t];
-            cn = -2.f * sm.v.eta[t] * db / (den * den);
-        }
-        if (live) {
-            Tin *dqo = static_cast<Tin *>(p.dq);
-            Tin *dko = static_cast<Tin *>(p.dk);
-#pragma unroll
-            for (int x = 0; x < CPT; ++x) {
-                const int i = cq + 4 * x;
+            if (live) {
                 st_out(dqo, rt * D + i, dq[x]);
-                st_out(dko, rt * D + i, fmaf(cn, sm.K[t][i], dkk[x]));
+                st_out(dko, rt * D + i, dkk[x]);
             }
         }
-        // dg: exp(g) of the Q S read, exp(g_C - g) of the state write
-        const float wk = egc * gk;
-        if (cq == 0) sm.dg[t] += eg * gq - wk;
-        // dg_C: the state write and exp(g_C) S
-        float red = (cq == 0) ? wk : 0.f;
-        for (int x = tid; x < D * D; x += NT) red = fmaf(sm.v.eg[C - 1] * dSp[x], S[x], red);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) red += __shfl_xor_sync(0xffffffffu, red, off);
-        if ((tid & 31) == 0) sm.red[tid >> 5] = red;
     }
+    gq += __shfl_xor_sync(0xffffffffu, gq, 1);
+    gq += __shfl_xor_sync(0xffffffffu, gq, 2);
+    gk += __shfl_xor_sync(0xffffffffu, gk, 1);
+    gk += __shfl_xor_sync(0xffffffffu, gk, 2);
+    // dg: exp(g) of the Q S read, exp(g_C - g) of the state write; dg_C: the
+    // state write and exp(g_C) S
+    const float wk = egc * gk;
+    if (cq == 0) sm.dg[t] += eg * gq - wk;
+    float red = ((cq == 0) ? wk : 0.f) + sm.v.eg[C - 1] * sds;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) red += __shfl_xor_sync(0xffffffffu, red, off);
+    if ((tid & 31) == 0) sm.red[tid >> 5] = red;
     __syncthreads();
     if (tid < 32) {   // dg_C onto g_{C-1}; reverse cumulative sum -> dlog(alpha)
         float gc = 0.f;
@@ -551,9 +591,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
         const int lane = tid;
         float d0 = sm.dg[lane], d1 = sm.dg[lane + 32];
         if (lane == 31) d1 += gc;
-        // reverse inclusive scan over 64 positions: suffix sums
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
+        for (int off = 1; off < 32; off <<= 1) {   // suffix sums
             const float u0 = __shfl_down_sync(0xffffffffu, d0, off);
             const float u1 = __shfl_down_sync(0xffffffffu, d1, off);
             if (lane + off < 32) { d0 += u0; d1 += u1; }
@@ -567,9 +606,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
                 const size_t r = (size_t)(row0 + tt) * p.H + h;
                 if (p.dalpha && p.alpha) p.dalpha[r] = dl[q2] / sm.v.alpha[tt];
                 if (p.deta) {
-                    const float db = sm.dbeta[tt];
+                    const float dbt = sm.dbeta[tt];
                     const float den = sm.v.den[tt];
-                    p.deta[r] = p.beta_mode ? db : (den != 0.f ? db / den : 0.f);
+                    p.deta[r] = p.beta_mode ? dbt : (den != 0.f ? dbt / den : 0.f);
                 }
             }
         }

@@ -24,6 +24,8 @@
 #include <cuda_bf16.h>
 
 #include "kla_internal.h"
+#include "kla_simt_inverse.cuh"
+#include "kla_simt_tile.cuh"
 
 namespace kla {
 namespace {
@@ -32,10 +34,6 @@ constexpr int C = kChunk;
 constexpr int DVB = 32;          // dv columns per CTA
 constexpr int NT = 256;          // threads per CTA
 
-__device__ __forceinline__ float ld_in(const float *p, size_t i) { return p[i]; }
-__device__ __forceinline__ float ld_in(const __nv_bfloat16 *p, size_t i) {
-    return __bfloat162float(p[i]);
-}
 __device__ __forceinline__ void st_out(float *p, size_t i, float x) { p[i] = x; }
 __device__ __forceinline__ void st_out(__nv_bfloat16 *p, size_t i, float x) {
     p[i] = __float2bfloat16_rn(x);
@@ -105,26 +103,9 @@ __global__ void __launch_bounds__(NT, 1) chunk_simt_kernel(Problem p) {
         }
 
         // ---- load the chunk (masked tail = identity tokens) ----
-        for (int x = tid; x < C * D; x += NT) {
-            const int t = x / D, i = x % D;
-            float kv = 0.f, qv = 0.f;
-            if (t < nc) {
-                const size_t row = (size_t)(start + c0 + t) * H + h;
-                kv = ld_in(k, row * D + i);
-                qv = ld_in(q, row * D + i);
-            }
-            sm.K[t][i] = kv;
-            sm.Q[t][i] = qv;
-        }
-        for (int x = tid; x < C * DVB; x += NT) {
-            const int t = x / DVB, j = x % DVB;
-            float vv = 0.f;
-            if (t < nc) {
-                const size_t row = (size_t)(start + c0 + t) * H + h;
-                vv = ld_in(v, row * D + jb + j);
-            }
-            sm.V[t][j] = vv;
-        }
+        load_tile<Tin, C, D, D + 1, NT>(&sm.K[0][0], k, start + c0, nc, H, h, D, 0, tid);
+        load_tile<Tin, C, D, D + 1, NT>(&sm.Q[0][0], q, start + c0, nc, H, h, D, 0, tid);
+        load_tile<Tin, C, DVB, DVB + 1, NT>(&sm.V[0][0], v, start + c0, nc, H, h, D, jb, tid);
         if (tid < C) {
             const bool ok = tid < nc;
             const size_t row = (size_t)(start + c0 + tid) * H + h;
@@ -201,15 +182,8 @@ __global__ void __launch_bounds__(NT, 1) chunk_simt_kernel(Problem p) {
         }
         __syncthreads();
 
-        // ---- T = (I + A_kk)^{-1}, one column per thread; K S and Q S ----
-        if (tid < C) {
-            const int j = tid;
-            for (int t = 0; t < C; ++t) {
-                float x = (t == j) ? 1.f : 0.f;
-                for (int s = 0; s < t; ++s) x = fmaf(-sm.Akk[t][s], sm.Tm[s][j], x);
-                sm.Tm[t][j] = x;
-            }
-        }
+        // ---- T = (I + A_kk)^{-1} (blocked; U is its scratch); K S and Q S ----
+        invert_unit_lower64(sm.Akk, sm.Tm, &sm.U[0][0], tid);
         {
             const int t = tid / 4, jq = (tid % 4) * 8;
             float ks[8], qs[8];
