@@ -35,10 +35,12 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "KLA chunkwise prefill tokens/s & % roofline; decode steps/s at B=256"
-# DRAM bytes (read + write) of one prefill launch (fused_kernel) and one decode
-# launch scaled to B=256, from the ncu captures summarised in profiles/
-# (fused_kernel_layer_prefill.md, decode_kernel_b128.md).
-TRAFFIC_PREFILL = 71.71e6
+# DRAM bytes (read + write) of one prefill launch (fused_kernel), one decode
+# launch scaled to B=256 and one CCQ query call (its two launches), from the ncu
+# captures summarised in profiles/ (fused_kernel_layer_prefill.md,
+# decode_kernel_b128.md, ccq_layer_prefill.md).
+TRAFFIC_PREFILL = 68.59e6
+TRAFFIC_CCQ = 46.1e6 + 51.6e6
 TRAFFIC_DECODE = 2 * (135.83e6 + 74.59e6)
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 BYTES_PER_TOKEN_HEAD = 1032          # q,k,v,o bf16 (4 x 256 B) + alpha, eta fp32 (8 B)
@@ -481,7 +483,7 @@ def ours(args):
            "query_us": cq["query_ms"] * 1e3, "layer_us": cq["layer_ms"] * 1e3,
            "layer_value": wl.B * wl.T / (cq["layer_ms"] / 1e3), "unit": "tokens/s",
            "roofline": {"bound": "hbm", "achieved": cq_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                        "frac": cq_gbs / pk["hbm_gbs"], "traffic": None,
+                        "frac": cq_gbs / pk["hbm_gbs"], "traffic": TRAFFIC_CCQ,
                         "kernel": "fused_kernel (CCQ mode) + ccq_finish_kernel",
                         "algorithmic_bytes_per_call": cq["bytes"]}}
 
