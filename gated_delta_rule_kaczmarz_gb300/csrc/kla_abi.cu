@@ -83,8 +83,9 @@ long n_chunks(bool varlen, long n_seq, long T, long total_T) {
 
 size_t ws_bytes(bool varlen, long n_seq, long T, long total_T, int H, int d, int dtype) {
     if (use_tc_path(d, dtype, total_T))
-        return kla::kWsHeader + kla::chunk_tc_workspace_bytes(n_chunks(varlen, n_seq, T, total_T),
-                                                              H, (int)n_seq);
+        return kla::kWsHeader +
+               kla::chunk_tc_workspace_bytes(n_chunks(varlen, n_seq, T, total_T), H, (int)n_seq) +
+               (varlen ? 0 : kla::chunk_tc_split_bytes((int)n_seq, (int)T, H));
     return varlen ? kla::kWsHeader : 0;
 }
 

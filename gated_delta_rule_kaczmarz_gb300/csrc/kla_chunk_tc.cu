@@ -42,6 +42,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 
 #include "kla_internal.h"
 #include "kla_tc.cuh"
@@ -72,6 +73,14 @@ struct TcParams {
     int beta_mode;             // 0: beta = eta / (||k||^2 + eps); 1: beta = eta
     int mode;                  // 0: KLA; 1: the CCQ product (W = 0, U~ = K, no decay)
     float *csum;               // CCQ mode: [slots][128] the sum of each chunk's keys
+    // Sequence split (fixed length): every sequence is run as seg_P virtual
+    // sequences of T / seg_P tokens.  State CTAs [0, phi_first) run the state
+    // pass of the virtual sequences (S0 only for the first segment); CTAs from
+    // phi_first on run the transition pass of the later segments (S0 = I,
+    // U~ read as 0), whose outputs are Q_corr rows (o_phi) and Phi (S_T_phi).
+    int seg_P, phi_first;
+    __nv_bfloat16 *o_phi;
+    float *S_T_phi;
     unsigned *flags;           // fused launch: one ready flag per work item, then the work-item
                                // counter (all zeroed per call)
     int n_units;               // fused launch: sequences x heads
@@ -822,6 +831,18 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     if (status_bad(p.status)) return;
+    // transition-pass CTAs: two per (batch, segment >= 1, head), in that order
+    // (the split runs without the fused launch)
+    const bool phi = !kFused && p.phi_first > 0 && bid >= p.phi_first;
+    const int segP = kFused ? 1 : p.seg_P;
+    size_t phi_base = 0;
+    if (phi) {
+        const int k = bid - p.phi_first, idx = k >> 1;
+        const int hh = idx % p.H, r = idx / p.H, P1 = p.seg_P - 1;
+        const int seqv = (r / P1) * p.seg_P + 1 + r % P1;
+        bid = ((seqv * p.H + hh) << 1) | (k & 1);
+        phi_base = (size_t)idx * D * D;
+    }
     const int unit = bid >> 1, jh = bid & 1, j0 = DVB * jh;
     const int rank = unit / p.H, h = unit % p.H;
     const int seq = p.order ? p.order[rank] : rank;
@@ -955,11 +976,24 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         const size_t rs = (size_t)p.H * D;
         float Sr[32];
         {
-            const float4 *src = reinterpret_cast<const float4 *>(p.S0 + sbase + (size_t)L * D + j0 + c0);
+            // the initial state: S0, zero for a later segment of a split
+            // sequence, the identity's columns for a transition pass
+            const float *s0 = p.S0;
+            if (segP > 1)
+                s0 = (!phi && p.S0 && seq % segP == 0)
+                         ? p.S0 + ((size_t)(seq / segP) * p.H + h) * D * D
+                         : nullptr;
+            else if (s0)
+                s0 += sbase;
+            const float4 *src = reinterpret_cast<const float4 *>(s0 + (size_t)L * D + j0 + c0);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float4 v = p.S0 ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 v = s0 ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
                 Sr[4 * i] = v.x; Sr[4 * i + 1] = v.y; Sr[4 * i + 2] = v.z; Sr[4 * i + 3] = v.w;
+            }
+            if (phi) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) Sr[i] = (L == j0 + c0 + i) ? 1.f : 0.f;
             }
             st_row_bf16x32(sS, L, c0, Sr);
             fence_async_smem();
@@ -992,7 +1026,8 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 float u[32], uz[32];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(st + ST_U + sw128_offset(t, c0 + 8 * k));
+                    uint4 w = *reinterpret_cast<const uint4 *>(st + ST_U + sw128_offset(t, c0 + 8 * k));
+                    if (phi) w = make_uint4(0u, 0u, 0u, 0u);   // U~ = 0 in a transition pass
                     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -1058,7 +1093,8 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 tmem_ld_wait();
                 tc_fence_before();
                 if (L < nc) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(start + (long)c * C + L) * rs +
+                    uint4 *dst = reinterpret_cast<uint4 *>((phi ? p.o_phi : p.o) +
+                                                           (size_t)(start + (long)c * C + L) * rs +
                                                            (size_t)h * D + j0 + c0);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -1075,8 +1111,9 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 }
             }
         }
-        if (!sAbort && p.S_T) {
-            float4 *dst = reinterpret_cast<float4 *>(p.S_T + sbase + (size_t)L * D + j0 + c0);
+        if (!sAbort && (phi ? p.S_T_phi != nullptr : p.S_T != nullptr)) {
+            float4 *dst = reinterpret_cast<float4 *>((phi ? p.S_T_phi + phi_base : p.S_T + sbase) +
+                                                     (size_t)L * D + j0 + c0);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 dst[i] = make_float4(Sr[4 * i], Sr[4 * i + 1], Sr[4 * i + 2], Sr[4 * i + 3]);
@@ -1202,6 +1239,171 @@ prep_kernel(const int *cu, int N, int total_T, int *chunk_prefix, int *order, un
     if (tid == 0) *status = kDevOk;
 }
 
+// ===================================================================== sequence split
+// A fixed-length sequence run as P segments (the state pass of each segment
+// has a P times shorter chain).  The forward is linear in (V, S0) jointly, so
+// for a later segment s with start state S_s
+//   o = o(V, 0) + Q_corr S_s,   S_end = N_s + Phi_s S_s,
+// where o(V, 0), N_s are the segment's outputs from a zero state and
+// Q_corr = o(0, I), Phi_s = S_T(0, I) those of the transition pass (U~ = 0,
+// S0 = I).  The segment start states follow in order from S_1 = S_end of
+// segment 0.
+
+// Per (batch, head, 32 columns): S_1 .. S_{P-1} into Sst (bf16, the
+// correction's operand) and S_P as S_T.  The columns are independent.
+constexpr int CB_THREADS = 256;
+
+__global__ void __launch_bounds__(CB_THREADS)
+split_combine_kernel(const float *__restrict__ Nbuf, const float *__restrict__ Phi,
+                     __nv_bfloat16 *__restrict__ Sst, float *__restrict__ S_T, int H, int P,
+                     const unsigned *status) {
+    __shared__ float Ss[D][33];
+    if (status_bad(status)) return;
+    const int unit = blockIdx.x, b = unit / H, h = unit % H, jb = blockIdx.y * 32;
+    const int tid = threadIdx.x, i = tid >> 1, j0 = (tid & 1) * 16;
+    float cur[16];
+    const float *n0 = Nbuf + ((size_t)b * P * H + h) * D * D + (size_t)i * D + jb + j0;
+#pragma unroll
+    for (int x = 0; x < 16; ++x) cur[x] = n0[x];
+    for (int sg = 1; sg < P; ++sg) {
+        const size_t pidx = ((size_t)(b * (P - 1) + sg - 1) * H + h) * D * D;
+        __nv_bfloat16 *dst = Sst + pidx + (size_t)i * D + jb + j0;
+#pragma unroll
+        for (int x = 0; x < 16; ++x) dst[x] = __float2bfloat16_rn(cur[x]);
+        __syncthreads();   // the previous segment's product is done with Ss
+#pragma unroll
+        for (int x = 0; x < 16; ++x) Ss[i][j0 + x] = cur[x];
+        __syncthreads();
+        const float *ph = Phi + pidx + (size_t)i * D;
+        const float *ns = Nbuf + ((size_t)(b * P + sg) * H + h) * D * D + (size_t)i * D + jb + j0;
+#pragma unroll
+        for (int x = 0; x < 16; ++x) cur[x] = ns[x];
+#pragma unroll 4
+        for (int kk = 0; kk < D; ++kk) {
+            const float f = ph[kk];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) cur[x] = fmaf(f, Ss[kk][j0 + x], cur[x]);
+        }
+    }
+    if (S_T) {
+        float *dst = S_T + ((size_t)unit * D + i) * D + jb + j0;
+#pragma unroll
+        for (int x = 0; x < 16; ++x) dst[x] = cur[x];
+    }
+}
+
+// o[rows] += Q_corr[rows] S_s for 128 token rows of one (batch, segment >= 1,
+// head): one tcgen05 MMA chain (M = 128 tokens, N = 128, K = 128), A = Q_corr
+// rows (K-major, TMA), B = S_s in bf16 (MN-major, TMA), o rows loaded by TMA,
+// added to in shared memory and stored by TMA.
+constexpr int CR_THREADS = 128;
+constexpr uint32_t CR_A = 0, CR_B = 32768, CR_O = 65536, CR_SMEM = 98304 + 1024;
+
+__global__ void __launch_bounds__(CR_THREADS)
+split_correct_kernel(const __grid_constant__ CUtensorMap mqc, const __grid_constant__ CUtensorMap mo,
+                     const __grid_constant__ CUtensorMap mss, int H, int T, int P,
+                     int tiles_per_seg, unsigned *status) {
+    extern __shared__ unsigned char smraw[];
+    unsigned char *sm = align1024(smraw);
+    __shared__ uint64_t bar_ld, bar_mma;
+    __shared__ uint32_t tslot;
+    __shared__ int sok;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (status_bad(status)) return;
+    long r = blockIdx.x;
+    const int t_in = (int)(r % tiles_per_seg);
+    r /= tiles_per_seg;
+    const int h = (int)(r % H);
+    r /= H;   // b * (P - 1) + (segment - 1)
+    const long b = r / (P - 1);
+    const int sg = 1 + (int)(r % (P - 1));
+    const int row0 = (int)(b * T + (long)sg * (T / P) + (long)t_in * 128);
+    const int srow = (int)((r * H + h) * D);   // first row of S_s in the bf16 array
+    if (tid == 0) {
+        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+        sok = 1;
+    }
+    if (warp == 0) {
+        tmem_alloc(&tslot, 128);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tslot;
+    if (tid == 0) {
+        mbar_expect_tx(&bar_ld, 3u * 32768u);
+#pragma unroll
+        for (int sl = 0; sl < 2; ++sl)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                tma_load_3d(sm + CR_A + sl * 16384 + hf * 8192, &mqc, &bar_ld, 64 * sl, h, row0 + 64 * hf);
+                tma_load_3d(sm + CR_O + sl * 16384 + hf * 8192, &mo, &bar_ld, 64 * sl, h, row0 + 64 * hf);
+            }
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) tma_load_2d(sm + CR_B + nb * 16384, &mss, &bar_ld, 64 * nb, srow);
+        bool ok = mbar_wait(&bar_ld, 0u);
+        if (ok) {
+            tc_fence_after();
+            const uint32_t aA = smem_u32(sm + CR_A), aB = smem_u32(sm + CR_B);
+            const uint32_t id = idesc_bf16_f32(128, 128, false, true);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tb, sdesc_sw128(aA + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                         sdesc_sw128(aB + ks * 2048, 16384, 1024), id, ks > 0);
+            mma_commit(&bar_mma);
+            ok = mbar_wait(&bar_mma, 0u);
+            if (!ok) (void)mbar_wait(&bar_mma, 0u);   // the MMAs finish before TMEM is freed
+        } else {
+            (void)mbar_wait(&bar_ld, 0u);             // copies in flight land before the CTA leaves
+        }
+        if (!ok) {
+            sok = 0;
+            set_status(status, kDevTimeout);
+        }
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (sok) {
+        const int rrow = warp * 32 + lane;
+#pragma unroll 1
+        for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t rr[32];
+            tmem_ld32(tb + ((uint32_t)(warp * 32) << 16) + c4 * 32, rr);
+            tmem_ld_wait();
+            unsigned char *tile = sm + CR_O + (c4 >> 1) * 16384;
+            const int col0 = (32 * c4) & 63;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint4 *pk = reinterpret_cast<uint4 *>(tile + sw128_offset(rrow, col0 + 8 * k));
+                const uint4 v = *pk;
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t o4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    o4[e] = pack_bf2(bf_lo(w[e]) + __uint_as_float(rr[8 * k + 2 * e]),
+                                     bf_hi(w[e]) + __uint_as_float(rr[8 * k + 2 * e + 1]));
+                *pk = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            }
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && sok) {
+#pragma unroll
+        for (int sl = 0; sl < 2; ++sl)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+                tma_store_3d(&mo, sm + CR_O + sl * 16384 + hf * 8192, 64 * sl, h, row0 + 64 * hf);
+        bulk_commit_group();
+        bulk_wait_group0();
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 128);
+}
+
 // ===================================================================== host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1268,10 +1470,51 @@ WsLayout layout(long n_chunks, int H, int n_seq) {
     return L;
 }
 
+// Sequence split factor P for a fixed-length batch (1: none).  Each segment
+// is a whole number of 128-token tiles; by default the largest P in {8, 4, 2}
+// whose segments hold at least 1024 tokens and whose state and transition
+// passes (2 B H P + 2 B H (P - 1) CTAs) fit on the SMs at once -- few heads and
+// long sequences, where the serial chain of the state pass dominates.  The
+// environment variable KLA_SEQ_SPLIT=P sets it (any P whose segments are whole
+// 128-token tiles; KLA_SEQ_SPLIT=1 disables the split).
+int split_factor(int n_seq, int T, int H, bool varlen) {
+    if (varlen || T <= 0) return 1;
+    auto valid = [&](int P) { return P >= 2 && T % (P * 128) == 0; };
+    if (const char *e = getenv("KLA_SEQ_SPLIT")) {
+        const int P = atoi(e);
+        return valid(P) ? P : 1;
+    }
+    const long units = (long)n_seq * H;
+    for (int P = 8; P >= 2; P >>= 1)
+        if (valid(P) && T / P >= 1024 && 2 * units * P + 2 * units * (P - 1) <= sm_count())
+            return P;
+    return 1;
+}
+
+struct SplitLayout {
+    size_t N, Phi, Qc, Sst, total;
+};
+
+// After the chunk workspace: N (the end states of every segment from its own
+// start, fp32), Phi (segments >= 1, fp32), Q_corr rows ([total_T][H][128]
+// bf16), the segment start states S_1.. in bf16.
+SplitLayout split_layout(int n_seq, int T, int H, int P) {
+    SplitLayout L{};
+    if (P <= 1) return L;
+    const size_t dd = (size_t)D * D;
+    L.N = 0;
+    L.Phi = L.N + (size_t)n_seq * P * H * dd * 4;
+    L.Qc = L.Phi + (size_t)n_seq * (P - 1) * H * dd * 4;
+    L.Sst = L.Qc + align_up((size_t)n_seq * T * H * D * 2, 1024);
+    L.total = L.Sst + (size_t)n_seq * (P - 1) * H * dd * 2;
+    return L;
+}
+
 // The fused launch serves fixed-length batches with an even number of chunks
 // per sequence whose state pass fits on at most half of the SMs.
 bool use_fused(const Problem &p) {
     if (p.cu_seqlens != nullptr || p.T <= 0) return false;
+    if (p.mode == 0 && split_factor(p.n_seq, p.T, p.H, false) > 1) return false;
     const int nch = (p.T + C - 1) / C;
     return nch % 2 == 0 && 2L * p.n_seq * p.H <= sm_count() / 2;
 }
@@ -1289,12 +1532,31 @@ size_t chunk_tc_workspace_bytes(long n_chunks_upper, int H, int n_seq) {
     return layout(n_chunks_upper, H, n_seq).total;
 }
 
-cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t s) {
-    if (p.n_seq == 0) return cudaSuccess;
+size_t chunk_tc_split_bytes(int n_seq, int T, int H) {
+    const int P = split_factor(n_seq, T, H, false);
+    if (P <= 1) return 0;
+    // the chunk workspace of the P-times-more virtual sequences, then the split buffers
+    const long n_chunks = (long)n_seq * ((T + C - 1) / C);
+    const size_t base = align_up(layout(n_chunks, H, n_seq * P).total, 1024);
+    return base + split_layout(n_seq, T, H, P).total - layout(n_chunks, H, n_seq).total;
+}
+
+cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t s) {
+    if (p0.n_seq == 0) return cudaSuccess;
     if (encode_fn() == nullptr) return cudaErrorNotSupported;
+    // a split sequence runs as P virtual sequences of T / P tokens (same rows,
+    // same chunk slots); the CCQ mode does not split
+    const int P = p0.mode == 0 ? split_factor(p0.n_seq, p0.T, p0.H, p0.cu_seqlens != nullptr) : 1;
+    Problem p = p0;
+    if (P > 1) {
+        p.n_seq = p0.n_seq * P;
+        p.T = p0.T / P;
+    }
     const WsLayout L = layout(n_chunks_upper, p.H, p.n_seq);
     unsigned char *ws = static_cast<unsigned char *>(p.ws);
-    if (p.ws_bytes < L.total) return cudaErrorInvalidValue;
+    const size_t split_base = align_up(L.total, 1024);
+    const SplitLayout SL = split_layout(p0.n_seq, p0.T, p0.H, P);
+    if (p.ws_bytes < (P > 1 ? split_base + SL.total : L.total)) return cudaErrorInvalidValue;
 
     TcParams tp{};
     tp.H = p.H;
@@ -1306,10 +1568,17 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     tp.beta_mode = p.beta_mode;
     tp.mode = p.mode;
     tp.csum = p.csum;
+    tp.seg_P = P;
     tp.alpha = p.alpha;
     tp.eta = p.eta;
     tp.S0 = p.S0;
     tp.S_T = p.S_T;
+    if (P > 1) {   // the virtual sequences' end states go to N, not to S_T
+        tp.S_T = reinterpret_cast<float *>(ws + split_base + SL.N);
+        tp.phi_first = 2 * p.n_seq * p.H;
+        tp.o_phi = reinterpret_cast<__nv_bfloat16 *>(ws + split_base + SL.Qc);
+        tp.S_T_phi = reinterpret_cast<float *>(ws + split_base + SL.Phi);
+    }
     tp.o = static_cast<__nv_bfloat16 *>(p.o);
     tp.cu_seqlens = p.cu_seqlens;
     tp.status = p.status;
@@ -1348,7 +1617,7 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     }
     const long n_pairs = (n_chunks_upper + 1) / 2;
     const long n_items = n_pairs * p.H;
-    if (use_fused(p)) {
+    if (P == 1 && use_fused(p)) {
         static bool fattr = false;
         if (!fattr) {
             if ((e = cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1384,7 +1653,34 @@ cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t 
     intra_kernel<<<(unsigned)grid1, P1_THREADS, P1_SMEM, s>>>(mq, mk, mv, mw, mu, tp, n_pairs);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    state_kernel<<<(unsigned)(2L * p.n_seq * p.H), P2_THREADS, P2_SMEM, s>>>(mq, mk, mw, mu, ma, tp);
+    const long n_phi = P > 1 ? 2L * p0.n_seq * (P - 1) * p.H : 0;
+    state_kernel<<<(unsigned)(2L * p.n_seq * p.H + n_phi), P2_THREADS, P2_SMEM, s>>>(mq, mk, mw, mu,
+                                                                                     ma, tp);
+    note_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess || P == 1) return e;
+
+    // split: the segment start states, then the corrections of the later segments
+    __nv_bfloat16 *Sst = reinterpret_cast<__nv_bfloat16 *>(ws + split_base + SL.Sst);
+    split_combine_kernel<<<dim3((unsigned)(p0.n_seq * p0.H), D / 32), CB_THREADS, 0, s>>>(
+        tp.S_T, tp.S_T_phi, Sst, p0.S_T, p0.H, P, p0.status);
+    note_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    CUtensorMap mqc, mo, mss;
+    if (!map_3d_rows(&mqc, tp.o_phi, p.H, p.total_T) || !map_3d_rows(&mo, p0.o, p.H, p.total_T) ||
+        !map_2d(&mss, Sst, D, (long)p0.n_seq * (P - 1) * p.H * D, 128))
+        return cudaErrorInvalidValue;
+    static bool cattr = false;
+    if (!cattr) {
+        if ((e = cudaFuncSetAttribute(split_correct_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)CR_SMEM)) != cudaSuccess)
+            return e;
+        cattr = true;
+    }
+    const int tiles_per_seg = p0.T / P / 128;
+    const long n_tiles = (long)p0.n_seq * (P - 1) * p.H * tiles_per_seg;
+    split_correct_kernel<<<(unsigned)n_tiles, CR_THREADS, CR_SMEM, s>>>(mqc, mo, mss, p.H, p0.T, P,
+                                                                        tiles_per_seg, p0.status);
     note_launch();
     return cudaGetLastError();
 }

@@ -93,6 +93,9 @@ cudaError_t launch_chunk_bwd(const BwdProblem &p, cudaStream_t s);
 
 // Tensor-core (tcgen05) prefill for bf16, d = 128.
 size_t chunk_tc_workspace_bytes(long n_chunks_upper, int H, int n_seq);
+// Extra workspace bytes of a fixed-length batch that runs with the sequence
+// split (0 when it does not).
+size_t chunk_tc_split_bytes(int n_seq, int T, int H);
 bool chunk_tc_supported(int d, int dtype);
 cudaError_t launch_chunk_tc(const Problem &p, long n_chunks_upper, cudaStream_t s);
 // Bytes after the workspace header that must be zero when launch_chunk_tc
