@@ -809,7 +809,7 @@ __device__ __forceinline__ void st_row_bf16x32(unsigned char *tile, int row, int
 // tid = 0 .. P2_THREADS-1 and shared memory `sm` (1024-aligned, P2_SMEM - 1024
 // bytes).  kFused: phase 1 runs in the same launch, and the load of chunk c
 // waits for the ready flag of the work item that holds it.
-template <bool kFused>
+template <bool kFused, bool kSplit>
 __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorMap *mk,
                                           const CUtensorMap *mw, const CUtensorMap *mu,
                                           const CUtensorMap *ma, const TcParams &p,
@@ -832,9 +832,8 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
 
     if (status_bad(p.status)) return;
     // transition-pass CTAs: two per (batch, segment >= 1, head), in that order
-    // (the split runs without the fused launch)
-    const bool phi = !kFused && p.phi_first > 0 && bid >= p.phi_first;
-    const int segP = kFused ? 1 : p.seg_P;
+    const bool phi = kSplit && p.phi_first > 0 && bid >= p.phi_first;
+    const int segP = kSplit ? p.seg_P : 1;
     size_t phi_base = 0;
     if (phi) {
         const int k = bid - p.phi_first, idx = k >> 1;
@@ -1130,8 +1129,8 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
              const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
              const __grid_constant__ CUtensorMap ma, const TcParams p) {
     extern __shared__ unsigned char smraw[];
-    state_run<false>(&mq, &mk, &mw, &mu, &ma, p, align1024(smraw), (int)blockIdx.x,
-                     (int)threadIdx.x);
+    state_run<false, true>(&mq, &mk, &mw, &mu, &ma, p, align1024(smraw), (int)blockIdx.x,
+                           (int)threadIdx.x);
 }
 
 // ===================================================================== fused launch
@@ -1149,22 +1148,26 @@ constexpr int FU_THREADS = 2 * P1_THREADS;
 static_assert(FU_THREADS >= P2_THREADS, "fused block size");
 constexpr uint32_t FU_SMEM = P2_SMEM > 2 * P1_REGION + 1024 ? P2_SMEM : 2 * P1_REGION + 1024;
 
+template <bool kSplit>
 __global__ void __launch_bounds__(FU_THREADS, 1)
 fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mw,
              const __grid_constant__ CUtensorMap mu, const __grid_constant__ CUtensorMap ma,
-             const TcParams p, long n_pairs, int n_state) {
+             const TcParams p, long n_pairs, int n_state, int n_phi) {
     extern __shared__ unsigned char smraw[];
     unsigned char *sm = align1024(smraw);
     const int tid = (int)threadIdx.x;
     const long n_items = n_pairs * p.H;
     const int pre = p.nch_fixed >= 4 ? 2 : 1;   // leading chunk pairs done by the state CTAs
-    if ((int)blockIdx.x < n_state) {
+    if ((int)blockIdx.x < n_state + n_phi) {
+        // state-pass CTAs (then, with the sequence split, transition-pass CTAs,
+        // which only consume)
         const int unit = (int)blockIdx.x >> 1, jh = (int)blockIdx.x & 1;
-        if (jh < pre && tid < P1_THREADS)
+        if ((int)blockIdx.x < n_state && jh < pre && tid < P1_THREADS)
             intra_run<true>(&mq, &mk, &mv, &mw, &mu, p, n_pairs, sm, tid, 1,
                             (long)jh * p.n_units + unit, n_items);
-        if (tid < P2_THREADS) state_run<true>(&mq, &mk, &mw, &mu, &ma, p, sm, (int)blockIdx.x, tid);
+        if (tid < P2_THREADS)
+            state_run<true, kSplit>(&mq, &mk, &mw, &mu, &ma, p, sm, (int)blockIdx.x, tid);
         return;
     }
     const int w = tid / P1_THREADS;
@@ -1252,12 +1255,15 @@ prep_kernel(const int *cu, int N, int total_T, int *chunk_prefix, int *order, un
 // Per (batch, head, 32 columns): S_1 .. S_{P-1} into Sst (bf16, the
 // correction's operand) and S_P as S_T.  The columns are independent.
 constexpr int CB_THREADS = 256;
+constexpr size_t CB_SMEM = ((size_t)D * (D + 1) + (size_t)D * 33) * sizeof(float);
 
 __global__ void __launch_bounds__(CB_THREADS)
 split_combine_kernel(const float *__restrict__ Nbuf, const float *__restrict__ Phi,
                      __nv_bfloat16 *__restrict__ Sst, float *__restrict__ S_T, int H, int P,
                      const unsigned *status) {
-    __shared__ float Ss[D][33];
+    extern __shared__ float cb_sm[];
+    float(*Ph)[D + 1] = reinterpret_cast<float(*)[D + 1]>(cb_sm);              // Phi_s
+    float(*Ss)[33] = reinterpret_cast<float(*)[33]>(cb_sm + (size_t)D * (D + 1));   // S_s block
     if (status_bad(status)) return;
     const int unit = blockIdx.x, b = unit / H, h = unit % H, jb = blockIdx.y * 32;
     const int tid = threadIdx.x, i = tid >> 1, j0 = (tid & 1) * 16;
@@ -1270,17 +1276,29 @@ split_combine_kernel(const float *__restrict__ Nbuf, const float *__restrict__ P
         __nv_bfloat16 *dst = Sst + pidx + (size_t)i * D + jb + j0;
 #pragma unroll
         for (int x = 0; x < 16; ++x) dst[x] = __float2bfloat16_rn(cur[x]);
-        __syncthreads();   // the previous segment's product is done with Ss
+        __syncthreads();   // the previous segment's product is done with Ph and Ss
+        {   // Phi_s into shared memory: 16 float4 per thread, all issued first
+            constexpr int NV = D * D / 4 / CB_THREADS;
+            float4 buf[NV];
+            const float4 *src = reinterpret_cast<const float4 *>(Phi + pidx);
+#pragma unroll
+            for (int n = 0; n < NV; ++n) buf[n] = src[tid + n * CB_THREADS];
+#pragma unroll
+            for (int n = 0; n < NV; ++n) {
+                const int e = (tid + n * CB_THREADS) * 4, r = e / D, c = e % D;
+                Ph[r][c] = buf[n].x; Ph[r][c + 1] = buf[n].y;
+                Ph[r][c + 2] = buf[n].z; Ph[r][c + 3] = buf[n].w;
+            }
+        }
 #pragma unroll
         for (int x = 0; x < 16; ++x) Ss[i][j0 + x] = cur[x];
         __syncthreads();
-        const float *ph = Phi + pidx + (size_t)i * D;
         const float *ns = Nbuf + ((size_t)(b * P + sg) * H + h) * D * D + (size_t)i * D + jb + j0;
 #pragma unroll
         for (int x = 0; x < 16; ++x) cur[x] = ns[x];
 #pragma unroll 4
         for (int kk = 0; kk < D; ++kk) {
-            const float f = ph[kk];
+            const float f = Ph[i][kk];
 #pragma unroll
             for (int x = 0; x < 16; ++x) cur[x] = fmaf(f, Ss[kk][j0 + x], cur[x]);
         }
@@ -1511,12 +1529,17 @@ SplitLayout split_layout(int n_seq, int T, int H, int P) {
 }
 
 // The fused launch serves fixed-length batches with an even number of chunks
-// per sequence whose state pass fits on at most half of the SMs.
+// per (virtual) sequence whose state pass (with the sequence split: state and
+// transition passes) fits on at most half of the SMs; with fewer SMs left to
+// phase 1 its items arrive more slowly than the chain consumes them (measured
+// on long_context: 684 us fused against 650 us in two launches).
 bool use_fused(const Problem &p) {
     if (p.cu_seqlens != nullptr || p.T <= 0) return false;
-    if (p.mode == 0 && split_factor(p.n_seq, p.T, p.H, false) > 1) return false;
-    const int nch = (p.T + C - 1) / C;
-    return nch % 2 == 0 && 2L * p.n_seq * p.H <= sm_count() / 2;
+    const int P = p.mode == 0 ? split_factor(p.n_seq, p.T, p.H, false) : 1;
+    const int nch = (p.T / P + C - 1) / C;
+    if (nch % 2 != 0) return false;
+    const long n_state = 2L * p.n_seq * P * p.H;
+    return n_state + (P > 1 ? 2L * p.n_seq * (P - 1) * p.H : 0) <= sm_count() / 2;
 }
 
 }  // namespace
@@ -1540,6 +1563,9 @@ size_t chunk_tc_split_bytes(int n_seq, int T, int H) {
     const size_t base = align_up(layout(n_chunks, H, n_seq * P).total, 1024);
     return base + split_layout(n_seq, T, H, P).total - layout(n_chunks, H, n_seq).total;
 }
+
+cudaError_t launch_split_tail(const Problem &p0, const Problem &p, const TcParams &tp, int P,
+                              unsigned char *sws, const SplitLayout &SL, cudaStream_t s);
 
 cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t s) {
     if (p0.n_seq == 0) return cudaSuccess;
@@ -1617,10 +1643,14 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     }
     const long n_pairs = (n_chunks_upper + 1) / 2;
     const long n_items = n_pairs * p.H;
-    if (P == 1 && use_fused(p)) {
+    if (use_fused(p0)) {
         static bool fattr = false;
         if (!fattr) {
-            if ((e = cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if ((e = cudaFuncSetAttribute(fused_kernel<false>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)FU_SMEM)) != cudaSuccess ||
+                (e = cudaFuncSetAttribute(fused_kernel<true>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)FU_SMEM)) != cudaSuccess)
                 return e;
             fattr = true;
@@ -1628,6 +1658,7 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
         tp.flags = reinterpret_cast<unsigned *>(ws + L.meta);   // zeroed with the status word
         tp.n_units = p.n_seq * p.H;
         const int n_state = 2 * p.n_seq * p.H;
+        const int n_phi = P > 1 ? 2 * p0.n_seq * (P - 1) * p.H : 0;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)sm_count());
         cfg.blockDim = dim3(FU_THREADS);
@@ -1638,10 +1669,14 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, fused_kernel, mq, mk, mv, mw, mu, ma, tp, n_pairs, n_state);
+        e = P > 1 ? cudaLaunchKernelEx(&cfg, fused_kernel<true>, mq, mk, mv, mw, mu, ma, tp,
+                                       n_pairs, n_state, n_phi)
+                  : cudaLaunchKernelEx(&cfg, fused_kernel<false>, mq, mk, mv, mw, mu, ma, tp,
+                                       n_pairs, n_state, n_phi);
         if (e == cudaSuccess) {
             note_launch();
-            return cudaSuccess;
+            if (P == 1) return cudaSuccess;
+            return launch_split_tail(p0, p, tp, P, ws + split_base, SL, s);
         }
         // not every CTA could be resident (the device is shared or smaller):
         // the two-launch path below needs no co-residency
@@ -1658,10 +1693,23 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
                                                                                      ma, tp);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess || P == 1) return e;
+    return launch_split_tail(p0, p, tp, P, ws + split_base, SL, s);
+}
 
-    // split: the segment start states, then the corrections of the later segments
-    __nv_bfloat16 *Sst = reinterpret_cast<__nv_bfloat16 *>(ws + split_base + SL.Sst);
-    split_combine_kernel<<<dim3((unsigned)(p0.n_seq * p0.H), D / 32), CB_THREADS, 0, s>>>(
+// Split: the segment start states, then the corrections of the later segments.
+cudaError_t launch_split_tail(const Problem &p0, const Problem &p, const TcParams &tp, int P,
+                              unsigned char *sws, const SplitLayout &SL, cudaStream_t s) {
+    cudaError_t e;
+    __nv_bfloat16 *Sst = reinterpret_cast<__nv_bfloat16 *>(sws + SL.Sst);
+    static bool battr = false;
+    if (!battr) {
+        if ((e = cudaFuncSetAttribute(split_combine_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)CB_SMEM)) != cudaSuccess)
+            return e;
+        battr = true;
+    }
+    split_combine_kernel<<<dim3((unsigned)(p0.n_seq * p0.H), D / 32), CB_THREADS, CB_SMEM, s>>>(
         tp.S_T, tp.S_T_phi, Sst, p0.S_T, p0.H, P, p0.status);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -26,11 +26,14 @@ def split(monkeypatch):
     return set_p
 
 
-@pytest.mark.parametrize("B,T,H,P,with_S0,no_alpha,mode", [
-    (1, 512, 2, 2, True, False, "kaczmarz"), (2, 512, 2, 4, True, False, "kaczmarz"),
-    (2, 768, 3, 3, False, False, "kaczmarz"), (1, 1024, 2, 8, True, True, "kaczmarz"),
-    (2, 256, 2, 2, True, False, "given")])
-def test_split_forward_parity(split, B, T, H, P, with_S0, no_alpha, mode):
+# launches: the fused launch (phase 1, state and transition passes) when the
+# state and transition CTAs fit on half of the SMs, else phase 1 and the state
+# + transition launch; then the combine and the correction
+@pytest.mark.parametrize("B,T,H,P,with_S0,no_alpha,mode,launches", [
+    (1, 512, 2, 2, True, False, "kaczmarz", 3), (2, 512, 2, 4, True, False, "kaczmarz", 3),
+    (2, 768, 3, 3, False, False, "kaczmarz", 3), (1, 1024, 2, 8, True, True, "kaczmarz", 3),
+    (2, 256, 2, 2, True, False, "given", 3), (4, 1024, 8, 2, True, False, "kaczmarz", 4)])
+def test_split_forward_parity(split, B, T, H, P, with_S0, no_alpha, mode, launches):
     split(P)
     inp = prefill_inputs(B, T, H, 128, 128, "bf16", seed=400 + T + P, s0_var=0.01)
     g = cuda(inp)
@@ -39,7 +42,7 @@ def test_split_forward_parity(split, B, T, H, P, with_S0, no_alpha, mode):
     o, S = kla.kla_chunk_fwd(g["q"], g["k"], g["v"], None if no_alpha else g["alpha"], g["eta"],
                              inp["eps"], g["S0"] if with_S0 else None, beta_mode=mode)
     torch.cuda.synchronize()
-    assert kla.kla_launch_count() - n0 == 4   # phase 1, state + transition, combine, correct
+    assert kla.kla_launch_count() - n0 == launches
     o_ref, S_ref = oracle.forward(inp["q"], inp["k"], inp["v"], None if no_alpha else inp["alpha"],
                                   inp["eta"], inp["eps"], S0, nthreads=8, beta_mode=mode)
     assert rel_err(o, o_ref) <= 2e-2
@@ -85,7 +88,7 @@ def test_long_context_takes_the_split_sampled(monkeypatch):
     n0 = kla.kla_launch_count()
     o, S = kla.kla_chunk_fwd(g["q"], g["k"], g["v"], g["alpha"], g["eta"], wl.eps, g["S0"])
     torch.cuda.synchronize()
-    assert kla.kla_launch_count() - n0 == 4
+    assert kla.kla_launch_count() - n0 == 4   # 96 state + transition CTAs: two launches
     for h in (0, 11):
         sl = lambda x: x[:, :, h:h + 1].contiguous()
         o_ref, S_ref = oracle.forward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["alpha"]),
