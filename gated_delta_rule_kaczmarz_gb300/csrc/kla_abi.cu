@@ -303,7 +303,7 @@ int kla_decode_step(const void *q, const void *k, const void *v, const float *al
 size_t kla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dtype) {
     if (B < 0 || T < 0) return 0;
     if (check_shape(H, dk, dk, kla::kChunk, dtype) != KLA_OK) return 0;
-    return kla::kWsHeader + kla::chunk_bwd_workspace_bytes(B, T, H, dk);
+    return kla::kWsHeader + kla::chunk_bwd_workspace_bytes(B, T, H, dk, dtype);
 }
 
 int kla_chunk_bwd(const void *q, const void *k, const void *v, const float *alpha,
@@ -336,7 +336,7 @@ int kla_chunk_bwd(const void *q, const void *k, const void *v, const float *alph
     }
     if (!q || !k || !v || !eta || !d_o || !dq || !dk || !dv)
         return fail(KLA_ERR_INVALID_ARG, "q, k, v, eta, d_o, dq, dk and dv must be non-null");
-    const size_t need = kla::kWsHeader + kla::chunk_bwd_workspace_bytes(B, T, H, dk_);
+    const size_t need = kla::kWsHeader + kla::chunk_bwd_workspace_bytes(B, T, H, dk_, dtype);
     if (workspace == nullptr || workspace_bytes < need)
         return fail(KLA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
                     workspace ? workspace_bytes : (size_t)0);

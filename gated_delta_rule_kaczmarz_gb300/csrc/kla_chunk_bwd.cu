@@ -258,6 +258,182 @@ __global__ void __launch_bounds__(NT, 1) bwd_dstate_kernel(BwdProblem p, int nch
     }
 }
 
+// dS chain for bf16, d = 128 from the tensor-core forward's chunk workspace:
+// W = T diag(beta exp g) K (bf16), A^T (bf16, row = key, column = query) and g
+// of every chunk, so that the chain needs no Gram product and no inverse:
+//   dU = A_qk^T dO + diag(exp(g_C - g)) K dS'
+//   dS = exp(g_C) dS' + Q^T diag(exp g) dO - W^T dU
+// Row strides are multiples of 4 floats (float4 operands) offset from 32 banks.
+struct DsTcSmem {
+    float K[C][132], Q[C][132], W[C][132];
+    float At[C][C + 4];
+    float dS[128][DVB + 4];
+    float dO[C][DVB + 4], dU[C][DVB + 4];
+    float g[C], eg[C], egc[C];
+    // the next chunk's tiles as they arrive (bf16, cp.async), converted at the
+    // start of its iteration
+    __nv_bfloat16 Kb[C][128], Qb[C][128], Wb[C][128], Ab[C][C], dOb[C][DVB];
+    float gb[C];
+};
+
+__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+// Issues the asynchronous copies of chunk c's tiles into the staging arrays
+// (rows past the sequence end are zero filled).
+__device__ __forceinline__ void ds_prefetch(DsTcSmem &sm, const BwdProblem &p, int c, int nch,
+                                            int b, int h, int jb, const float *g_ws,
+                                            const __nv_bfloat16 *W_ws,
+                                            const __nv_bfloat16 *A_ws, int tid) {
+    constexpr int D = 128;
+    const long row0 = (long)b * p.T + (long)c * C;
+    const int nc = min(C, p.T - c * C);
+    const long slot = ((long)b * nch + c) * p.H + h;
+    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+    const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(p.dout);
+    for (int e = tid; e < C * 16; e += NT) {   // K, Q, W: 16 pieces of 16 B per row
+        const int t = e >> 4, pc = e & 15;
+        const bool ok = t < nc;
+        const size_t src = ((size_t)(row0 + (ok ? t : 0)) * p.H + h) * D + pc * 8;
+        cp_async16_zfill(&sm.Kb[t][pc * 8], k + src, ok);
+        cp_async16_zfill(&sm.Qb[t][pc * 8], q + src, ok);
+        cp_async16_zfill(&sm.Wb[t][pc * 8], W_ws + ((size_t)slot * C + t) * D + pc * 8, true);
+    }
+    for (int e = tid; e < C * 8; e += NT) {    // A^T: 8 pieces per row
+        const int t = e >> 3, pc = e & 7;
+        cp_async16_zfill(&sm.Ab[t][pc * 8], A_ws + ((size_t)slot * C + t) * C + pc * 8, true);
+    }
+    for (int e = tid; e < C * (DVB / 8); e += NT) {   // dO columns [jb, jb + 32): 4 pieces per row
+        const int t = e >> 2, pc = e & 3;
+        const bool ok = t < nc;
+        cp_async16_zfill(&sm.dOb[t][pc * 8],
+                         dout + ((size_t)(row0 + (ok ? t : 0)) * p.H + h) * D + jb + pc * 8, ok);
+    }
+    if (tid < C / 4)
+        cp_async16_zfill(&sm.gb[tid * 4], g_ws + (size_t)slot * C + tid * 4, true);
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+__global__ void __launch_bounds__(NT, 1)
+bwd_dstate_tc_kernel(BwdProblem p, int nch, float *dS_chk, const float *g_ws,
+                     const __nv_bfloat16 *W_ws, const __nv_bfloat16 *A_ws) {
+    constexpr int D = 128;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    DsTcSmem &sm = *reinterpret_cast<DsTcSmem *>(smem_raw);
+    const int tid = threadIdx.x;
+    const int unit = blockIdx.x, b = unit / p.H, h = unit % p.H;
+    const int jb = blockIdx.y * DVB;
+    if (p.status != nullptr && *(volatile unsigned *)p.status != kDevOk) return;
+    const size_t sbase = (size_t)unit * D * D;
+    for (int x = tid; x < D * DVB; x += NT) {
+        const int i = x / DVB, j = x % DVB;
+        sm.dS[i][j] = p.dS_T ? p.dS_T[sbase + (size_t)i * D + jb + j] : 0.f;
+    }
+    ds_prefetch(sm, p, nch - 1, nch, b, h, jb, g_ws, W_ws, A_ws, tid);
+    for (int c = nch - 1; c >= 0; --c) {
+        const int nc = min(C, p.T - c * C);
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
+        __syncthreads();   // chunk c's tiles have landed; the previous chunk is done
+        float *rec = dS_chk + ((size_t)unit * nch + c) * D * D;   // dS' of chunk c
+        for (int x = tid; x < D * DVB; x += NT) {
+            const int i = x / DVB, j = x % DVB;
+            rec[(size_t)i * D + jb + j] = sm.dS[i][j];
+        }
+        for (int x = tid; x < C * D; x += NT) {
+            const int t = x >> 7, i = x & 127;
+            sm.K[t][i] = __bfloat162float(sm.Kb[t][i]);
+            sm.Q[t][i] = __bfloat162float(sm.Qb[t][i]);
+            sm.W[t][i] = __bfloat162float(sm.Wb[t][i]);
+        }
+        for (int x = tid; x < C * C; x += NT) sm.At[x >> 6][x & 63] = __bfloat162float(sm.Ab[x >> 6][x & 63]);
+        for (int x = tid; x < C * DVB; x += NT) sm.dO[x / DVB][x % DVB] = __bfloat162float(sm.dOb[x / DVB][x % DVB]);
+        if (tid < C) sm.g[tid] = sm.gb[tid];
+        __syncthreads();   // staging free: the next chunk's copies overlap this one's work
+        if (c > 0) ds_prefetch(sm, p, c - 1, nch, b, h, jb, g_ws, W_ws, A_ws, tid);
+        if (tid < C) {
+            sm.eg[tid] = __expf(sm.g[tid]);
+            sm.egc[tid] = __expf(sm.g[C - 1] - sm.g[tid]);
+        }
+        __syncthreads();
+        {   // dU = A_qk^T dO + diag(exp(g_C - g)) K dS': thread = tokens 2 tp, 2 tp + 1 x
+            // columns 4 jb4 .. 4 jb4 + 3 (float4 rows of dO and dS')
+            const int tp = tid >> 3, jb4 = (tid & 7) * 4, t0 = 2 * tp;
+            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int s2 = t0; s2 < C; ++s2) {   // A^T rows are zero left of the diagonal
+                const float4 o = *reinterpret_cast<const float4 *>(&sm.dO[s2][jb4]);
+                const float x0 = sm.At[t0][s2], x1 = sm.At[t0 + 1][s2];
+                a0[0] = fmaf(x0, o.x, a0[0]); a0[1] = fmaf(x0, o.y, a0[1]);
+                a0[2] = fmaf(x0, o.z, a0[2]); a0[3] = fmaf(x0, o.w, a0[3]);
+                a1[0] = fmaf(x1, o.x, a1[0]); a1[1] = fmaf(x1, o.y, a1[1]);
+                a1[2] = fmaf(x1, o.z, a1[2]); a1[3] = fmaf(x1, o.w, a1[3]);
+            }
+            float b0[4] = {0.f, 0.f, 0.f, 0.f}, b1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int i = 0; i < D; ++i) {
+                const float4 d4 = *reinterpret_cast<const float4 *>(&sm.dS[i][jb4]);
+                const float k0 = sm.K[t0][i], k1 = sm.K[t0 + 1][i];
+                b0[0] = fmaf(k0, d4.x, b0[0]); b0[1] = fmaf(k0, d4.y, b0[1]);
+                b0[2] = fmaf(k0, d4.z, b0[2]); b0[3] = fmaf(k0, d4.w, b0[3]);
+                b1[0] = fmaf(k1, d4.x, b1[0]); b1[1] = fmaf(k1, d4.y, b1[1]);
+                b1[2] = fmaf(k1, d4.z, b1[2]); b1[3] = fmaf(k1, d4.w, b1[3]);
+            }
+            const float e0 = sm.egc[t0], e1 = sm.egc[t0 + 1];
+            *reinterpret_cast<float4 *>(&sm.dU[t0][jb4]) =
+                make_float4(fmaf(e0, b0[0], a0[0]), fmaf(e0, b0[1], a0[1]),
+                            fmaf(e0, b0[2], a0[2]), fmaf(e0, b0[3], a0[3]));
+            *reinterpret_cast<float4 *>(&sm.dU[t0 + 1][jb4]) =
+                make_float4(fmaf(e1, b1[0], a1[0]), fmaf(e1, b1[1], a1[1]),
+                            fmaf(e1, b1[2], a1[2]), fmaf(e1, b1[3], a1[3]));
+        }
+        __syncthreads();
+        {   // dS <- exp(g_C) dS' + Q^T diag(exp g) dO - W^T dU: thread = rows 4 ib .. 4 ib + 3
+            // x columns 4 jb4 .. 4 jb4 + 3
+            const int ib = tid >> 3, jb4 = (tid & 7) * 4, i0 = 4 * ib;
+            float acc[4][4];
+            const float egC = sm.eg[C - 1];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float4 d4 = *reinterpret_cast<const float4 *>(&sm.dS[i0 + m][jb4]);
+                acc[m][0] = egC * d4.x; acc[m][1] = egC * d4.y;
+                acc[m][2] = egC * d4.z; acc[m][3] = egC * d4.w;
+            }
+            for (int t = 0; t < nc; ++t) {
+                const float4 q4 = *reinterpret_cast<const float4 *>(&sm.Q[t][i0]);
+                const float4 w4 = *reinterpret_cast<const float4 *>(&sm.W[t][i0]);
+                const float4 o4 = *reinterpret_cast<const float4 *>(&sm.dO[t][jb4]);
+                const float4 u4 = *reinterpret_cast<const float4 *>(&sm.dU[t][jb4]);
+                const float et = sm.eg[t];
+                const float qv[4] = {q4.x * et, q4.y * et, q4.z * et, q4.w * et};
+                const float wv[4] = {-w4.x, -w4.y, -w4.z, -w4.w};
+                const float ov[4] = {o4.x, o4.y, o4.z, o4.w};
+                const float uv[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+#pragma unroll
+                    for (int n = 0; n < 4; ++n)
+                        acc[m][n] = fmaf(qv[m], ov[n], fmaf(wv[m], uv[n], acc[m][n]));
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                *reinterpret_cast<float4 *>(&sm.dS[i0 + m][jb4]) =
+                    make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+        }
+    }
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+    __syncthreads();
+    if (p.dS0) {
+        for (int x = tid; x < D * DVB; x += NT) {
+            const int i = x / DVB, j = x % DVB;
+            p.dS0[sbase + (size_t)i * D + jb + j] = sm.dS[i][j];
+        }
+    }
+}
+
 // ------------------------------------------------------------ token gradients
 template <int D>
 struct GrSmem {
@@ -615,19 +791,37 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
     }
 }
 
+// bf16 with d = 128 and at least one 64-row TMA box: the tensor-core forward
+// records the chunk-start states, and the dS chain reads its chunk workspace.
+bool bwd_uses_tc(int B, int T, int d, int dtype) {
+    return chunk_tc_supported(d, dtype) && (long)B * T >= C;
+}
+
 template <typename Tin, int D>
 cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t s) {
     const int nch = (p.T + C - 1) / C;
     const int units = p.B * p.H;
     float *S_chk = static_cast<float *>(p.ws);
     float *dS_chk = S_chk + (size_t)units * nch * D * D;
+    const bool tc = bwd_uses_tc(p.B, p.T, D, p.dtype);
     // 1. states at the chunk starts (the forward, no outputs)
     Problem f{};
     f.q = p.q; f.k = p.k; f.v = p.v; f.alpha = p.alpha; f.eta = p.eta; f.eps = p.eps;
     f.S0 = p.S0; f.o = nullptr; f.S_T = nullptr; f.cu_seqlens = nullptr;
     f.n_seq = p.B; f.T = p.T; f.total_T = p.B * p.T; f.H = p.H; f.d = D; f.dtype = p.dtype;
     f.beta_mode = p.beta_mode; f.S_chk = S_chk; f.status = p.status;
-    cudaError_t e = launch_chunk_simt(f, s);
+    cudaError_t e;
+    float *g_ws = nullptr;
+    void *W_ws = nullptr, *A_ws = nullptr;
+    if (tc) {
+        const long nchunks = (long)p.B * nch;
+        f.ws = dS_chk + (size_t)units * nch * D * D;
+        f.ws_bytes = chunk_tc_workspace_bytes(nchunks, p.H, p.B);
+        chunk_tc_ws_views(f.ws, nchunks, p.H, p.B, &g_ws, &W_ws, &A_ws);
+        e = launch_chunk_tc(f, nchunks, s);
+    } else {
+        e = launch_chunk_simt(f, s);
+    }
     if (e != cudaSuccess) return e;
     // 2. the dS chain
     static bool attr = false;
@@ -640,9 +834,18 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t s) {
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)sizeof(GrSmem<D>))) != cudaSuccess)
             return e;
+        if ((e = cudaFuncSetAttribute(bwd_dstate_tc_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)sizeof(DsTcSmem))) != cudaSuccess)
+            return e;
         attr = true;
     }
-    bwd_dstate_kernel<Tin, D><<<dim3(units, D / DVB), NT, sizeof(DsSmem<D>), s>>>(p, nch, dS_chk);
+    if (tc)
+        bwd_dstate_tc_kernel<<<dim3(units, D / DVB), NT, sizeof(DsTcSmem), s>>>(
+            p, nch, dS_chk, g_ws, static_cast<const __nv_bfloat16 *>(W_ws),
+            static_cast<const __nv_bfloat16 *>(A_ws));
+    else
+        bwd_dstate_kernel<Tin, D><<<dim3(units, D / DVB), NT, sizeof(DsSmem<D>), s>>>(p, nch, dS_chk);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 3. token gradients
@@ -653,9 +856,11 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t s) {
 
 }  // namespace
 
-size_t chunk_bwd_workspace_bytes(int B, int T, int H, int d) {
+size_t chunk_bwd_workspace_bytes(int B, int T, int H, int d, int dtype) {
     const size_t nch = (size_t)(T + C - 1) / C;
-    return 2 * (size_t)B * H * nch * d * d * sizeof(float);
+    const size_t states = 2 * (size_t)B * H * nch * d * d * sizeof(float);
+    if (!bwd_uses_tc(B, T, d, dtype)) return states;
+    return states + chunk_tc_workspace_bytes((long)B * nch, H, B);
 }
 
 cudaError_t launch_chunk_bwd(const BwdProblem &p, cudaStream_t s) {

@@ -81,6 +81,11 @@ struct TcParams {
     int seg_P, phi_first;
     __nv_bfloat16 *o_phi;
     float *S_T_phi;
+    // Recording for the backward pass (two-launch path only): the state at
+    // every chunk start ([units][nch][128][128] fp32) and T of every chunk
+    // slot ([slots][64][64] bf16); o may then be null.
+    float *S_chk;
+    __nv_bfloat16 *T_chk;
     unsigned *flags;           // fused launch: one ready flag per work item, then the work-item
                                // counter (all zeroed per call)
     int n_units;               // fused launch: sequences x heads
@@ -638,6 +643,20 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
             pk[2 * i] = pack_bf2(v.x * bs[0], v.y * bs[1]);
             pk[2 * i + 1] = pack_bf2(v.z * bs[2], v.w * bs[3]);
         }
+        if (!kFused && p.T_chk && vslot) {   // T row t, columns [32 hf, 32 hf + 32), for the backward
+            uint4 *dst = reinterpret_cast<uint4 *>(p.T_chk + slot_row * 64 + 32 * hf);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float4 a = *reinterpret_cast<const float4 *>(Trow + lsw(t, 32 * hf + 8 * q4 + 4 * e));
+                    w[2 * e] = pack_bf2(a.x, a.y);
+                    w[2 * e + 1] = pack_bf2(a.z, a.w);
+                }
+                dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
         named_sync(bar, P1_THREADS);  // T fully read; its region becomes the bf16 A tile
         unsigned char *own = KQ + slot * 32768 + 16384, *other = KQ + (1 - slot) * 32768 + 16384;
 #pragma unroll
@@ -1009,6 +1028,13 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 break;
             }
             tc_fence_after();
+            if (!kFused && p.S_chk) {   // S at the chunk's start, for the backward
+                float4 *dst = reinterpret_cast<float4 *>(p.S_chk + sbase * nch + (size_t)c * D * D +
+                                                         (size_t)L * D + j0 + c0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    dst[i] = make_float4(Sr[4 * i], Sr[4 * i + 1], Sr[4 * i + 2], Sr[4 * i + 3]);
+            }
             const float *g = sG + b * C;
             const float gC = g[C - 1];
             const float egC = __expf(gC);
@@ -1091,7 +1117,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 tmem_ld32(tb + lane_base + TM_Y + 64 * (c & 1) + c0, yr);
                 tmem_ld_wait();
                 tc_fence_before();
-                if (L < nc) {
+                if (L < nc && (kFused || p.o != nullptr)) {
                     uint4 *dst = reinterpret_cast<uint4 *>((phi ? p.o_phi : p.o) +
                                                            (size_t)(start + (long)c * C + L) * rs +
                                                            (size_t)h * D + j0 + c0);
@@ -1555,6 +1581,15 @@ size_t chunk_tc_workspace_bytes(long n_chunks_upper, int H, int n_seq) {
     return layout(n_chunks_upper, H, n_seq).total;
 }
 
+void chunk_tc_ws_views(void *ws, long n_chunks_upper, int H, int n_seq, float **g, void **W,
+                       void **A) {
+    const WsLayout L = layout(n_chunks_upper, H, n_seq);
+    unsigned char *b = static_cast<unsigned char *>(ws);
+    *g = reinterpret_cast<float *>(b + L.g);
+    *W = b + L.W;
+    *A = b + L.A;
+}
+
 size_t chunk_tc_split_bytes(int n_seq, int T, int H) {
     const int P = split_factor(n_seq, T, H, false);
     if (P <= 1) return 0;
@@ -1572,7 +1607,10 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     if (encode_fn() == nullptr) return cudaErrorNotSupported;
     // a split sequence runs as P virtual sequences of T / P tokens (same rows,
     // same chunk slots); the CCQ mode does not split
-    const int P = p0.mode == 0 ? split_factor(p0.n_seq, p0.T, p0.H, p0.cu_seqlens != nullptr) : 1;
+    const bool record = p0.S_chk != nullptr;   // backward recording: two launches, no split
+    const int P = (p0.mode == 0 && !record)
+                      ? split_factor(p0.n_seq, p0.T, p0.H, p0.cu_seqlens != nullptr)
+                      : 1;
     Problem p = p0;
     if (P > 1) {
         p.n_seq = p0.n_seq * P;
@@ -1643,7 +1681,9 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     }
     const long n_pairs = (n_chunks_upper + 1) / 2;
     const long n_items = n_pairs * p.H;
-    if (use_fused(p0)) {
+    tp.S_chk = p0.S_chk;
+    tp.T_chk = static_cast<__nv_bfloat16 *>(p0.T_chk);
+    if (!record && use_fused(p0)) {
         static bool fattr = false;
         if (!fattr) {
             if ((e = cudaFuncSetAttribute(fused_kernel<false>,

@@ -39,8 +39,10 @@ struct Problem {
     int mode;                // 0: KLA; 1: the CCQ product y = M_t q (tensor-core path only)
     float *csum;             // mode 1: [chunk slots][d] per-chunk key sums (fixed length:
                              // slot (b * n_chunks + c) * H + h)
-    float *S_chk;            // CUDA-core path: the state at every chunk start
-                             // ([n_seq, H, n_chunks, d, d] fp32), or nullptr
+    float *S_chk;            // the state at every chunk start ([n_seq, H, n_chunks, d, d]
+                             // fp32) for the backward pass, or nullptr
+    void *T_chk;             // tensor-core path with S_chk: T of every chunk slot
+                             // ([slots, 64, 64] bf16), or nullptr
     unsigned *status;        // device status word, or nullptr
     void *ws;                // workspace after the header (path specific)
     size_t ws_bytes;
@@ -86,13 +88,17 @@ struct BwdProblem {
     float *dalpha, *deta, *dS0;
     int B, T, H, d, dtype, beta_mode;
     unsigned *status;
-    void *ws;                // chunk_bwd_workspace_bytes(B, T, H, d) after the header
+    void *ws;                // chunk_bwd_workspace_bytes(B, T, H, d, dtype) after the header
 };
-size_t chunk_bwd_workspace_bytes(int B, int T, int H, int d);
+size_t chunk_bwd_workspace_bytes(int B, int T, int H, int d, int dtype);
 cudaError_t launch_chunk_bwd(const BwdProblem &p, cudaStream_t s);
 
 // Tensor-core (tcgen05) prefill for bf16, d = 128.
 size_t chunk_tc_workspace_bytes(long n_chunks_upper, int H, int n_seq);
+// The g [slots][64] fp32, W [slots][64][128] bf16 and A^T [slots][64][64] bf16
+// arrays inside a tensor-core workspace (after its header).
+void chunk_tc_ws_views(void *ws, long n_chunks_upper, int H, int n_seq, float **g, void **W,
+                       void **A);
 // Extra workspace bytes of a fixed-length batch that runs with the sequence
 // split (0 when it does not).
 size_t chunk_tc_split_bytes(int n_seq, int T, int H);

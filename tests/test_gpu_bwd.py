@@ -55,6 +55,7 @@ def test_backward_parity(B, T, H, d, dtype, mode, no_alpha, with_dST, with_S0):
 
 
 def test_backward_launches_and_status():
+    """Launch count of the bf16 d128 backward and a clean status word."""
     B, T, H, d = 2, 192, 2, 128
     inp = prefill_inputs(B, T, H, d, d, "bf16", seed=5)
     do, dST = _grad_inputs(B, T, H, d, "bf16", 6)
@@ -67,7 +68,10 @@ def test_backward_launches_and_status():
     n0 = kla.kla_launch_count()
     kla.kla_chunk_bwd(*args, workspace=ws)
     torch.cuda.synchronize()
-    assert kla.kla_launch_count() - n0 == 3
+    # bf16, d 128: the tensor-core forward recording the chunk-start states
+    # (phase 1, state pass), the dS chain over its chunk workspace, the token
+    # gradients
+    assert kla.kla_launch_count() - n0 == 4
     assert kla.kla_workspace_status(ws) == 0
 
 
@@ -99,3 +103,18 @@ def test_backward_full_size_sampled():
                               tok(inp["eta"]), wl.eps, st(inp["S0"]), tok(do), st(dST))
         sub = [tok(got[0]), tok(got[1]), tok(got[2]), tok(got[3]), tok(got[4]), st(got[5])]
         _check(sub, ref, TOL[torch.bfloat16])
+
+
+def test_backward_cuda_core_launches():
+    """fp32 (and d 64) take the CUDA-core forward for the states: three launches."""
+    B, T, H, d = 1, 128, 2, 64
+    inp = prefill_inputs(B, T, H, d, d, "fp32", seed=12)
+    do, dST = _grad_inputs(B, T, H, d, "fp32", 13)
+    g = cuda(dict(inp, do=do, dST=dST))
+    args = (g["q"], g["k"], g["v"], g["alpha"], g["eta"], inp["eps"], g["S0"], g["do"], g["dST"])
+    kla.kla_chunk_bwd(*args)
+    torch.cuda.synchronize()
+    n0 = kla.kla_launch_count()
+    kla.kla_chunk_bwd(*args)
+    torch.cuda.synchronize()
+    assert kla.kla_launch_count() - n0 == 3
