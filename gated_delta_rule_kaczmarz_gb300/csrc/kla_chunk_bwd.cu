@@ -48,14 +48,6 @@ constexpr int C = kChunk;
 constexpr int NT = 256;
 constexpr int DVB = 32;   // dv columns per CTA of the state-gradient chain
 
-__device__ __forceinline__ float ld_in(const float *p, size_t i) { return p[i]; }
-__device__ __forceinline__ float ld_in(const __nv_bfloat16 *p, size_t i) {
-    return __bfloat162float(p[i]);
-}
-__device__ __forceinline__ void st_out(float *p, size_t i, float x) { p[i] = x; }
-__device__ __forceinline__ void st_out(__nv_bfloat16 *p, size_t i, float x) {
-    p[i] = __float2bfloat16_rn(x);
-}
 
 // Per-chunk vectors.  Tail positions of a partial chunk are identity tokens
 // (k = q = v = 0, alpha = 1, eta = 0, beta = 0).
@@ -80,12 +72,20 @@ __device__ void load_kq(float (*K)[D + 1], float (*Q)[D + 1], Vec &v, const BwdP
 
 // beta, ||k||^2 + eps and the in-chunk log-decay prefix sums (after K, alpha
 // and eta are in shared memory).
-template <int D>
-__device__ void chunk_vectors(const float (*K)[D + 1], Vec &v, float eps, int beta_mode, int nc,
+template <int D, int LK = D + 1>
+__device__ void chunk_vectors(const float (*K)[LK], Vec &v, float eps, int beta_mode, int nc,
                               int tid) {
     if (tid < C) {
         float n2 = 0.f;
-        for (int i = 0; i < D; ++i) n2 = fmaf(K[tid][i], K[tid][i], n2);
+        if constexpr (LK % 4 == 0) {
+            for (int i = 0; i < D; i += 4) {
+                const float4 k4 = *reinterpret_cast<const float4 *>(&K[tid][i]);
+                n2 = fmaf(k4.x, k4.x, n2); n2 = fmaf(k4.y, k4.y, n2);
+                n2 = fmaf(k4.z, k4.z, n2); n2 = fmaf(k4.w, k4.w, n2);
+            }
+        } else {
+            for (int i = 0; i < D; ++i) n2 = fmaf(K[tid][i], K[tid][i], n2);
+        }
         const float den = n2 + eps;
         v.den[tid] = den;
         const float b = beta_mode ? v.eta[tid] : (den != 0.f ? v.eta[tid] / den : 0.f);
@@ -116,9 +116,9 @@ __device__ __forceinline__ float gam(const Vec &v, int t, int s) { return expf(v
 // Gram products over the chunk, 4 x 4 register blocks on the lower triangle.
 // kApply: Mkk = strict_lower(beta Gamma o K K^T), Mqk = lower(Gamma o Q K^T);
 // otherwise the raw products (strict lower K K^T, lower Q K^T); zero above.
-template <int D, bool kApply>
-__device__ void gram(const float (*K)[D + 1], const float (*Q)[D + 1], const Vec &v,
-                     float (*Mkk)[C + 1], float (*Mqk)[C + 1], int tid) {
+template <int D, bool kApply, int LK = D + 1, int LM = C + 1>
+__device__ void gram(const float (*K)[LK], const float (*Q)[LK], const Vec &v,
+                     float (*Mkk)[LM], float (*Mqk)[LM], int tid) {
     const int bt = tid / 16, bs = tid % 16;
     float akk[4][4], aqk[4][4];
 #pragma unroll
@@ -435,23 +435,32 @@ bwd_dstate_tc_kernel(BwdProblem p, int nch, float *dS_chk, const float *g_ws,
 }
 
 // ------------------------------------------------------------ token gradients
+// Row strides are multiples of 4 floats so that the products read float4
+// operands; every product runs on 2D register tiles:
+//   layout A (64 x D outputs): tokens 2 tp, 2 tp + 1 x columns cg JT .. + JT;
+//   layout B (64 x 64 outputs): tokens 4 tb + m x positions sb + 16 n;
+//   layout P (products with rows of S or dS'): tokens 2 tp, 2 tp + 1 x rows
+//   cg + 8 n.
+// The rows a thread reads in layouts B and P are 16 or 8 apart, so that the
+// float4 loads of a warp spread over all banks.
 template <int D>
 struct GrSmem {
-    float K[C][D + 1], Q[C][D + 1];
-    float M0[C][C + 1];   // raw strict-lower K K^T, then its dg terms
-    float M1[C][C + 1];   // raw lower Q K^T, then dA_qk o Gamma
-    float M2[C][C + 1];   // T, then X = diag(beta) (dA_kk o Gamma)
-    float tA[C][D + 1];   // A_kk and S rows (staging), then U
-    float tB[C][D + 1];   // V - diag(exp g) K S, then dR
-    float tC[C][D + 1];   // dO, then dU, then S and dS' row blocks (staging)
+    static constexpr int LK = D + 4, LM = C + 4;
+    float K[C][LK], Q[C][LK];
+    float M0[C][LM];   // raw strict-lower K K^T, its dg terms, then X + X^T
+    float M1[C][LM];   // raw lower Q K^T, its dg terms, then dA_qk o Gamma
+    float M2[C][LM];   // T, then X = diag(beta) (dA_kk o Gamma)
+    float tA[C][LK];   // A_kk and S / dS' rows (staging), then U
+    float tB[C][LK];   // V - diag(exp g) K S, then dR
+    float tC[C][LK];   // dO, then dU, then S and dS' row blocks (staging)
     Vec v;
     float dbeta[C], dg[C], dgcol[C], red[NT / 32];
     float scr[32 * 33];   // scratch of the triangular inverse
 };
 
-// Sums of column s of the [C][C + 1] matrix E over rows r >= s (threads 0..63),
-// subtracted from dg.
-__device__ __forceinline__ void sub_col_sums(const float (*E)[C + 1], float *dgcol, int tid) {
+// Column sums of the [C][LM] matrix E over rows r >= s (threads 0..63).
+template <int LM>
+__device__ __forceinline__ void col_sums(const float (*E)[LM], float *dgcol, int tid) {
     if (tid < C) {
         float sg = 0.f;
         for (int r = tid; r < C; ++r) sg += E[r][tid];
@@ -459,16 +468,97 @@ __device__ __forceinline__ void sub_col_sums(const float (*E)[C + 1], float *dgc
     }
 }
 
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float dot4(const float4 a, const float4 b) {
+    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+// N consecutive input values (N a multiple of 4) as floats.
+template <int N>
+__device__ __forceinline__ void ld_row(const float *p, float (&f)[N]) {
+#pragma unroll
+    for (int k = 0; k < N / 4; ++k) {
+        const float4 v = *reinterpret_cast<const float4 *>(p + 4 * k);
+        f[4 * k] = v.x; f[4 * k + 1] = v.y; f[4 * k + 2] = v.z; f[4 * k + 3] = v.w;
+    }
+}
+template <int N>
+__device__ __forceinline__ void ld_row(const __nv_bfloat16 *p, float (&f)[N]) {
+#pragma unroll
+    for (int k = 0; k < N / 4; ++k) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p + 4 * k);
+        f[4 * k] = __uint_as_float(v.x << 16); f[4 * k + 1] = __uint_as_float(v.x & 0xffff0000u);
+        f[4 * k + 2] = __uint_as_float(v.y << 16); f[4 * k + 3] = __uint_as_float(v.y & 0xffff0000u);
+    }
+}
+template <int N>
+__device__ __forceinline__ void st_row(float *p, const float (&f)[N]) {
+#pragma unroll
+    for (int k = 0; k < N / 4; ++k)
+        *reinterpret_cast<float4 *>(p + 4 * k) = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+}
+template <int N>
+__device__ __forceinline__ void st_row(__nv_bfloat16 *p, const float (&f)[N]) {
+#pragma unroll
+    for (int k = 0; k < N / 4; ++k) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(f[4 * k], f[4 * k + 1]);
+        const __nv_bfloat162 c = __floats2bfloat162_rn(f[4 * k + 2], f[4 * k + 3]);
+        *reinterpret_cast<uint2 *>(p + 4 * k) =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&c));
+    }
+}
+
+// Raw Gram products for rows of stride LK (a multiple of 4): Mkk = strict
+// lower K K^T, Mqk = lower Q K^T.  Thread (bt, bs) forms rows bt + 16 m x
+// columns bs + 16 n of both, reading float4 along the features: the 16 rows
+// a warp reads per load are 16 apart (two wavefronts, the minimum for 16
+// distinct float4 rows).
+template <int D, int LK, int LM>
+__device__ void gram_v(const float (*K)[LK], const float (*Q)[LK], float (*Mkk)[LM],
+                       float (*Mqk)[LM], int tid) {
+    const int bt = tid >> 4, bs = tid & 15;
+    float akk[4][4], aqk[4][4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) akk[m][n] = aqk[m][n] = 0.f;
+#pragma unroll 2
+    for (int i = 0; i < D; i += 4) {
+        float4 kt[4], qt[4], ks[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            kt[m] = ld4(&K[bt + 16 * m][i]);
+            qt[m] = ld4(&Q[bt + 16 * m][i]);
+            ks[m] = ld4(&K[bs + 16 * m][i]);
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                akk[m][n] += dot4(kt[m], ks[n]);
+                aqk[m][n] += dot4(qt[m], ks[n]);
+            }
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            const int t = bt + 16 * m, s2 = bs + 16 * n;
+            Mkk[t][s2] = s2 < t ? akk[m][n] : 0.f;
+            Mqk[t][s2] = s2 <= t ? aqk[m][n] : 0.f;
+        }
+}
+
 template <typename Tin, int D>
 __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
                                                           const float *S_chk,
                                                           const float *dS_chk) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    GrSmem<D> &sm = *reinterpret_cast<GrSmem<D> *>(smem_raw);
-    constexpr int CPT = D / 4;    // columns per thread: cq + 4 x
-    constexpr int SPT = C / 4;    // chunk positions per thread: cq + 4 x
-    constexpr int IB = 32;        // rows of S and dS' per staged block
-    constexpr int LB = D + 1;     // their row stride in shared memory
+    using Sm = GrSmem<D>;
+    constexpr int LK = Sm::LK, LM = Sm::LM;
+    constexpr int JT = D / 8;   // layout A: columns per thread
+    constexpr int IB = 32;      // rows of S and dS' per staged block
+    Sm &sm = *reinterpret_cast<Sm *>(smem_raw);
     const int tid = threadIdx.x;
     const int c = blockIdx.x, unit = blockIdx.y, b = unit / p.H, h = unit % p.H;
     if (p.status != nullptr && *(volatile unsigned *)p.status != kDevOk) return;
@@ -478,15 +568,22 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
     const float *dSp = dS_chk + ((size_t)unit * nch + c) * D * D;  // gradient at its end
     const Tin *dout = static_cast<const Tin *>(p.dout);
     const Tin *vin = static_cast<const Tin *>(p.v);
-    const int t = tid >> 2, cq = tid & 3;
-    const size_t rt = (size_t)(row0 + t) * p.H + h;   // token row of this thread's t
-    const bool live = t < nc;
+    // layout A / P thread coordinates
+    const int tp = tid >> 3, cg = tid & 7;
+    const int ta[2] = {2 * tp, 2 * tp + 1};
+    // layout A columns of this thread: 4 cg + 32 q + e (q < JT / 4, e < 4)
+    auto colA = [cg](int q) { return 4 * cg + 32 * q; };
+    const bool liveA[2] = {ta[0] < nc, ta[1] < nc};
+    const size_t rowA[2] = {(size_t)(row0 + (liveA[0] ? ta[0] : 0)) * p.H + h,
+                            (size_t)(row0 + (liveA[1] ? ta[1] : 0)) * p.H + h};
+    // layout B
+    const int tb = tid >> 4, sb = tid & 15;
 
-    load_tile<Tin, C, D, D + 1, NT>(&sm.K[0][0], static_cast<const Tin *>(p.k), row0, nc, p.H, h,
-                                    D, 0, tid);
-    load_tile<Tin, C, D, D + 1, NT>(&sm.Q[0][0], static_cast<const Tin *>(p.q), row0, nc, p.H, h,
-                                    D, 0, tid);
-    load_tile<Tin, C, D, D + 1, NT>(&sm.tC[0][0], dout, row0, nc, p.H, h, D, 0, tid);
+    load_tile<Tin, C, D, LK, NT>(&sm.K[0][0], static_cast<const Tin *>(p.k), row0, nc, p.H, h, D,
+                                 0, tid);
+    load_tile<Tin, C, D, LK, NT>(&sm.Q[0][0], static_cast<const Tin *>(p.q), row0, nc, p.H, h, D,
+                                 0, tid);
+    load_tile<Tin, C, D, LK, NT>(&sm.tC[0][0], dout, row0, nc, p.H, h, D, 0, tid);
     if (tid < C) {
         const bool ok = tid < nc;
         const size_t r = (size_t)(row0 + tid) * p.H + h;
@@ -494,268 +591,437 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
         sm.v.eta[tid] = ok ? p.eta[r] : 0.f;
     }
     __syncthreads();
-    chunk_vectors<D>(sm.K, sm.v, p.eps, p.beta_mode, nc, tid);
+    chunk_vectors<D, LK>(sm.K, sm.v, p.eps, p.beta_mode, nc, tid);
     __syncthreads();
-    gram<D, false>(sm.K, sm.Q, sm.v, sm.M0, sm.M1, tid);
+    gram_v<D, LK, LM>(sm.K, sm.Q, sm.M0, sm.M1, tid);
     __syncthreads();
     {   // A_kk = strict_lower(beta Gamma o K K^T) into tA, then T
-        float(*Akk)[C + 1] = reinterpret_cast<float(*)[C + 1]>(&sm.tA[0][0]);
+        float(*Akk)[LM] = reinterpret_cast<float(*)[LM]>(&sm.tA[0][0]);
         for (int x = tid; x < C * C; x += NT) {
-            const int r = x / C, s = x % C;
-            Akk[r][s] = s < r ? sm.v.beta[r] * gam(sm.v, r, s) * sm.M0[r][s] : 0.f;
+            const int r = x / C, s2 = x % C;
+            Akk[r][s2] = s2 < r ? sm.v.beta[r] * gam(sm.v, r, s2) * sm.M0[r][s2] : 0.f;
         }
         __syncthreads();
-        invert_unit_lower64(Akk, sm.M2, sm.scr, tid);
+        invert_unit_lower64<LM, LM>(Akk, sm.M2, sm.scr, tid);
     }
-    {   // V - diag(exp g) K S -> tB, S staged in tA 64 rows at a time
-        float vv[CPT], acc[CPT];
+    // dO S^T for rows i = cg + 8 n of S (layout P), formed while S is staged
+    float pq[2][D / 8];
+    {   // (A) V - diag(exp g) K S -> tB, S staged in tA 64 rows at a time
+        float acc[2][JT], vv[2][JT];
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) {
-            vv[x] = live ? ld_in(vin, rt * D + cq + 4 * x) : 0.f;
-            acc[x] = 0.f;
+        for (int m = 0; m < 2; ++m) {
+#pragma unroll
+            for (int q = 0; q < JT / 4; ++q) {
+                float v4[4];
+                ld_row<4>(vin + rowA[m] * D + colA(q), v4);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) vv[m][4 * q + e] = liveA[m] ? v4[e] : 0.f;
+            }
+#pragma unroll
+            for (int x = 0; x < JT; ++x) acc[m][x] = 0.f;
         }
-        for (int i0 = 0; i0 < D; i0 += C) {
-            load_block_f32<C, D, D + 1, NT>(&sm.tA[0][0], S + (size_t)i0 * D, D, tid);
-            __syncthreads();
-            for (int i = 0; i < C; ++i) {
-                const float kti = sm.K[t][i0 + i];
 #pragma unroll
-                for (int x = 0; x < CPT; ++x) acc[x] = fmaf(kti, sm.tA[i][cq + 4 * x], acc[x]);
+        for (int i0 = 0; i0 < D; i0 += C) {
+            load_block_f32<C, D, LK, NT>(&sm.tA[0][0], S + (size_t)i0 * D, D, tid);
+            __syncthreads();
+#pragma unroll 2
+            for (int i = 0; i < C; ++i) {
+                const float k0 = sm.K[ta[0]][i0 + i], k1 = sm.K[ta[1]][i0 + i];
+#pragma unroll
+                for (int q = 0; q < JT / 4; ++q) {
+                    const float4 s4 = ld4(&sm.tA[i][colA(q)]);
+                    acc[0][4 * q] = fmaf(k0, s4.x, acc[0][4 * q]); acc[0][4 * q + 1] = fmaf(k0, s4.y, acc[0][4 * q + 1]);
+                    acc[0][4 * q + 2] = fmaf(k0, s4.z, acc[0][4 * q + 2]); acc[0][4 * q + 3] = fmaf(k0, s4.w, acc[0][4 * q + 3]);
+                    acc[1][4 * q] = fmaf(k1, s4.x, acc[1][4 * q]); acc[1][4 * q + 1] = fmaf(k1, s4.y, acc[1][4 * q + 1]);
+                    acc[1][4 * q + 2] = fmaf(k1, s4.z, acc[1][4 * q + 2]); acc[1][4 * q + 3] = fmaf(k1, s4.w, acc[1][4 * q + 3]);
+                }
+            }
+            // pq[t][i0 + cg + 8 n] = dO_t . S_i for the 8 staged rows of this thread
+            float pp[2][8];
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int n = 0; n < 8; ++n) pp[m][n] = 0.f;
+#pragma unroll 2
+            for (int j = 0; j < D; j += 4) {
+                const float4 o0 = ld4(&sm.tC[ta[0]][j]), o1 = ld4(&sm.tC[ta[1]][j]);
+#pragma unroll
+                for (int n = 0; n < 8; ++n) {
+                    const float4 s4 = ld4(&sm.tA[cg + 8 * n][j]);
+                    pp[0][n] += dot4(o0, s4);
+                    pp[1][n] += dot4(o1, s4);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int n = 0; n < 8; ++n) pq[m][i0 / 8 + n] = pp[m][n];
+            __syncthreads();
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const float e = sm.v.eg[ta[m]];
+#pragma unroll
+            for (int x = 0; x < JT; ++x) acc[m][x] = vv[m][x] - e * acc[m][x];
+#pragma unroll
+            for (int q = 0; q < JT / 4; ++q)
+                *reinterpret_cast<float4 *>(&sm.tB[ta[m]][colA(q)]) =
+                    make_float4(acc[m][4 * q], acc[m][4 * q + 1], acc[m][4 * q + 2], acc[m][4 * q + 3]);
+        }
+    }
+    __syncthreads();
+    float du[2][JT];
+    {   // (A) U = T diag(beta) (V - e^g K S);  dU = A_qk^T dO + diag(exp(g_C - g)) K dS'
+        float u[2][JT];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int x = 0; x < JT; ++x) u[m][x] = du[m][x] = 0.f;
+        for (int s2 = 0; s2 <= ta[1]; ++s2) {   // T is lower triangular
+            const float bs = sm.v.beta[s2];
+            const float a0 = sm.M2[ta[0]][s2] * bs, a1 = sm.M2[ta[1]][s2] * bs;
+#pragma unroll
+            for (int q = 0; q < JT / 4; ++q) {
+                const float4 w = ld4(&sm.tB[s2][colA(q)]);
+                u[0][4 * q] = fmaf(a0, w.x, u[0][4 * q]); u[0][4 * q + 1] = fmaf(a0, w.y, u[0][4 * q + 1]);
+                u[0][4 * q + 2] = fmaf(a0, w.z, u[0][4 * q + 2]); u[0][4 * q + 3] = fmaf(a0, w.w, u[0][4 * q + 3]);
+                u[1][4 * q] = fmaf(a1, w.x, u[1][4 * q]); u[1][4 * q + 1] = fmaf(a1, w.y, u[1][4 * q + 1]);
+                u[1][4 * q + 2] = fmaf(a1, w.z, u[1][4 * q + 2]); u[1][4 * q + 3] = fmaf(a1, w.w, u[1][4 * q + 3]);
+            }
+        }
+        for (int s2 = ta[0]; s2 < C; ++s2) {   // A_qk[s][t] = Gamma_st (q_s . k_t), s >= t
+            const float a0 = gam(sm.v, s2, ta[0]) * sm.M1[s2][ta[0]];
+            const float a1 = s2 >= ta[1] ? gam(sm.v, s2, ta[1]) * sm.M1[s2][ta[1]] : 0.f;
+#pragma unroll
+            for (int q = 0; q < JT / 4; ++q) {
+                const float4 o = ld4(&sm.tC[s2][colA(q)]);
+                du[0][4 * q] = fmaf(a0, o.x, du[0][4 * q]); du[0][4 * q + 1] = fmaf(a0, o.y, du[0][4 * q + 1]);
+                du[0][4 * q + 2] = fmaf(a0, o.z, du[0][4 * q + 2]); du[0][4 * q + 3] = fmaf(a0, o.w, du[0][4 * q + 3]);
+                du[1][4 * q] = fmaf(a1, o.x, du[1][4 * q]); du[1][4 * q + 1] = fmaf(a1, o.y, du[1][4 * q + 1]);
+                du[1][4 * q + 2] = fmaf(a1, o.z, du[1][4 * q + 2]); du[1][4 * q + 3] = fmaf(a1, o.w, du[1][4 * q + 3]);
+            }
+        }
+        const float e0 = sm.v.egc[ta[0]], e1 = sm.v.egc[ta[1]];
+        for (int i0 = 0; i0 < D; i0 += C) {
+            load_block_f32<C, D, LK, NT>(&sm.tA[0][0], dSp + (size_t)i0 * D, D, tid);
+            __syncthreads();
+#pragma unroll 2
+            for (int i = 0; i < C; ++i) {
+                const float k0 = e0 * sm.K[ta[0]][i0 + i], k1 = e1 * sm.K[ta[1]][i0 + i];
+#pragma unroll
+                for (int q = 0; q < JT / 4; ++q) {
+                    const float4 d4 = ld4(&sm.tA[i][colA(q)]);
+                    du[0][4 * q] = fmaf(k0, d4.x, du[0][4 * q]); du[0][4 * q + 1] = fmaf(k0, d4.y, du[0][4 * q + 1]);
+                    du[0][4 * q + 2] = fmaf(k0, d4.z, du[0][4 * q + 2]); du[0][4 * q + 3] = fmaf(k0, d4.w, du[0][4 * q + 3]);
+                    du[1][4 * q] = fmaf(k1, d4.x, du[1][4 * q]); du[1][4 * q + 1] = fmaf(k1, d4.y, du[1][4 * q + 1]);
+                    du[1][4 * q + 2] = fmaf(k1, d4.z, du[1][4 * q + 2]); du[1][4 * q + 3] = fmaf(k1, d4.w, du[1][4 * q + 3]);
+                }
             }
             __syncthreads();
         }
-        const float e = sm.v.eg[t];
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) sm.tB[t][cq + 4 * x] = vv[x] - e * acc[x];
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int q = 0; q < JT / 4; ++q)
+                *reinterpret_cast<float4 *>(&sm.tA[ta[m]][colA(q)]) =
+                    make_float4(u[m][4 * q], u[m][4 * q + 1], u[m][4 * q + 2], u[m][4 * q + 3]);
     }
     __syncthreads();
-    float du[CPT];
-    {   // U = T diag(beta) (V - e^g K S);  dU = A_qk^T dO + diag(exp(g_C - g)) K dS'
-        float u[CPT];
+    {   // (B) dA_qk = lower(dO U^T); its Gamma terms of dg; M1 <- dA_qk o Gamma
+        float da[4][4];
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) u[x] = du[x] = 0.f;
-        for (int s = 0; s <= t; ++s) {
-            const float a = sm.M2[t][s] * sm.v.beta[s];
+        for (int m = 0; m < 4; ++m)
 #pragma unroll
-            for (int x = 0; x < CPT; ++x) u[x] = fmaf(a, sm.tB[s][cq + 4 * x], u[x]);
+            for (int n = 0; n < 4; ++n) da[m][n] = 0.f;
+#pragma unroll 2
+        for (int j = 0; j < D; j += 4) {
+            float4 o[4], u4[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) o[m] = ld4(&sm.tC[4 * tb + m][j]);
+#pragma unroll
+            for (int n = 0; n < 4; ++n) u4[n] = ld4(&sm.tA[sb + 16 * n][j]);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int n = 0; n < 4; ++n) da[m][n] += dot4(o[m], u4[n]);
         }
-        for (int s = t; s < C; ++s) {
-            const float a = gam(sm.v, s, t) * sm.M1[s][t];
+        float rs[4], ev[4][4];
 #pragma unroll
-            for (int x = 0; x < CPT; ++x) du[x] = fmaf(a, sm.tC[s][cq + 4 * x], du[x]);
-        }
-        const float e = sm.v.egc[t];
-        for (int i0 = 0; i0 < D; i0 += C) {
-            load_block_f32<C, D, D + 1, NT>(&sm.tA[0][0], dSp + (size_t)i0 * D, D, tid);
-            __syncthreads();
-            for (int i = 0; i < C; ++i) {
-                const float kw = e * sm.K[t][i0 + i];
+        for (int m = 0; m < 4; ++m) {
+            rs[m] = 0.f;
+            const int t = 4 * tb + m;
 #pragma unroll
-                for (int x = 0; x < CPT; ++x) du[x] = fmaf(kw, sm.tA[i][cq + 4 * x], du[x]);
+            for (int n = 0; n < 4; ++n) {
+                const int s2 = sb + 16 * n;
+                const float ga = s2 <= t ? gam(sm.v, t, s2) : 0.f;
+                da[m][n] = s2 <= t ? da[m][n] * ga : 0.f;   // dA_qk o Gamma
+                ev[m][n] = da[m][n] * sm.M1[t][s2];         // dA_qk o A_qk
+                rs[m] += ev[m][n];
             }
-            __syncthreads();
+#pragma unroll
+            for (int off = 1; off < 16; off <<= 1) rs[m] += __shfl_xor_sync(0xffffffffu, rs[m], off);
         }
+        __syncthreads();   // dO reads and raw Q K^T reads are complete
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) sm.tA[t][cq + 4 * x] = u[x];
-    }
-    __syncthreads();
-    {   // dA_qk = lower(dO U^T); its Gamma terms of dg; M1 <- dA_qk o Gamma
-        float da[SPT];
+        for (int m = 0; m < 4; ++m)
 #pragma unroll
-        for (int x = 0; x < SPT; ++x) da[x] = 0.f;
-        for (int j = 0; j < D; ++j) {
-            const float o = sm.tC[t][j];
-#pragma unroll
-            for (int x = 0; x < SPT; ++x) da[x] = fmaf(o, sm.tA[cq + 4 * x][j], da[x]);
-        }
-        float rs = 0.f;
-#pragma unroll
-        for (int x = 0; x < SPT; ++x) {
-            const int s = cq + 4 * x;
-            const float ga = s <= t ? gam(sm.v, t, s) : 0.f;
-            da[x] = s <= t ? da[x] * ga : 0.f;          // dA_qk o Gamma
-            const float e = da[x] * sm.M1[t][s];        // dA_qk o A_qk
-            rs += e;
-            sm.M1[t][s] = e;
-        }
-        rs += __shfl_xor_sync(0xffffffffu, rs, 1);
-        rs += __shfl_xor_sync(0xffffffffu, rs, 2);
-        __syncthreads();   // dO and the E entries complete
-        sub_col_sums(sm.M1, sm.dgcol, tid);
+            for (int n = 0; n < 4; ++n) sm.M1[4 * tb + m][sb + 16 * n] = ev[m][n];
+        __syncthreads();
+        col_sums<LM>(sm.M1, sm.dgcol, tid);
         __syncthreads();
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) sm.tC[t][cq + 4 * x] = du[x];   // dU
+        for (int m = 0; m < 4; ++m)
 #pragma unroll
-        for (int x = 0; x < SPT; ++x) sm.M1[t][cq + 4 * x] = da[x];
-        if (cq == 0) sm.dg[t] = rs;
+            for (int n = 0; n < 4; ++n) sm.M1[4 * tb + m][sb + 16 * n] = da[m][n];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)   // dU
+#pragma unroll
+            for (int q = 0; q < JT / 4; ++q)
+                *reinterpret_cast<float4 *>(&sm.tC[ta[m]][colA(q)]) =
+                    make_float4(du[m][4 * q], du[m][4 * q + 1], du[m][4 * q + 2], du[m][4 * q + 3]);
+        if (sb == 0) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) sm.dg[4 * tb + m] = rs[m] - sm.dgcol[4 * tb + m];
+        }
     }
     __syncthreads();
-    if (tid < C) sm.dg[tid] -= sm.dgcol[tid];
-    {   // dR = T^T dU; dbeta and dg from R = diag(beta)(V - e^g K S); dV
-        float dr[CPT];
+    {   // (A) dR = T^T dU; dbeta and dg from R = diag(beta)(V - e^g K S); dV
+        float dr[2][JT];
 #pragma unroll
-        for (int x = 0; x < CPT; ++x) dr[x] = 0.f;
-        for (int s = t; s < C; ++s) {
-            const float a = sm.M2[s][t];
+        for (int m = 0; m < 2; ++m)
 #pragma unroll
-            for (int x = 0; x < CPT; ++x) dr[x] = fmaf(a, sm.tC[s][cq + 4 * x], dr[x]);
+            for (int x = 0; x < JT; ++x) dr[m][x] = 0.f;
+        for (int s2 = ta[0]; s2 < C; ++s2) {   // T[s][t], s >= t
+            const float a0 = sm.M2[s2][ta[0]], a1 = sm.M2[s2][ta[1]];
+#pragma unroll
+            for (int q = 0; q < JT / 4; ++q) {
+                const float4 w = ld4(&sm.tC[s2][colA(q)]);
+                dr[0][4 * q] = fmaf(a0, w.x, dr[0][4 * q]); dr[0][4 * q + 1] = fmaf(a0, w.y, dr[0][4 * q + 1]);
+                dr[0][4 * q + 2] = fmaf(a0, w.z, dr[0][4 * q + 2]); dr[0][4 * q + 3] = fmaf(a0, w.w, dr[0][4 * q + 3]);
+                dr[1][4 * q] = fmaf(a1, w.x, dr[1][4 * q]); dr[1][4 * q + 1] = fmaf(a1, w.y, dr[1][4 * q + 1]);
+                dr[1][4 * q + 2] = fmaf(a1, w.z, dr[1][4 * q + 2]); dr[1][4 * q + 3] = fmaf(a1, w.w, dr[1][4 * q + 3]);
+            }
         }
-        float p1 = 0.f;
-#pragma unroll
-        for (int x = 0; x < CPT; ++x) p1 = fmaf(sm.tB[t][cq + 4 * x], dr[x], p1);
-        p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
-        p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
-        __syncthreads();   // V - e^g K S, dU and T fully read
-#pragma unroll
-        for (int x = 0; x < CPT; ++x) sm.tB[t][cq + 4 * x] = dr[x];
-        __syncthreads();
-        // V . dR and dV = beta dR on the contiguous quarter row cq of token t
-        constexpr int VE = 16 / (int)sizeof(Tin);
-        const int j0 = cq * CPT;
-        float p2 = 0.f;
-        const float bt = sm.v.beta[t];
+        float p1[2] = {0.f, 0.f}, p2[2] = {0.f, 0.f};
         Tin *dvo = static_cast<Tin *>(p.dv);
 #pragma unroll
-        for (int n = 0; n < CPT / VE; ++n) {
-            const int j = j0 + n * VE;
-            float f[VE];
-            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-            if (live) raw = *reinterpret_cast<const uint4 *>(vin + rt * D + j);
-            unpack16(raw, f);
-            float o[VE];
+        for (int m = 0; m < 2; ++m) {
+            const float bt = sm.v.beta[ta[m]];
 #pragma unroll
-            for (int e = 0; e < VE; ++e) {
-                p2 = fmaf(f[e], sm.tB[t][j + e], p2);
-                o[e] = bt * sm.tB[t][j + e];
+            for (int q = 0; q < JT / 4; ++q) {
+                float vv[4], dvv[4];
+                ld_row<4>(vin + rowA[m] * D + colA(q), vv);
+                const float4 w4 = ld4(&sm.tB[ta[m]][colA(q)]);
+                const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float d = dr[m][4 * q + e];
+                    p1[m] = fmaf(wv[e], d, p1[m]);
+                    p2[m] = fmaf(liveA[m] ? vv[e] : 0.f, d, p2[m]);
+                    dvv[e] = bt * d;
+                }
+                if (liveA[m]) st_row<4>(dvo + rowA[m] * D + colA(q), dvv);
             }
-            if (live) {
 #pragma unroll
-                for (int e = 0; e < VE; ++e) st_out(dvo, rt * D + j + e, o[e]);
+            for (int off = 1; off < 8; off <<= 1) {
+                p1[m] += __shfl_xor_sync(0xffffffffu, p1[m], off);
+                p2[m] += __shfl_xor_sync(0xffffffffu, p2[m], off);
             }
         }
-        p2 += __shfl_xor_sync(0xffffffffu, p2, 1);
-        p2 += __shfl_xor_sync(0xffffffffu, p2, 2);
-        if (cq == 0) {
-            sm.dbeta[t] = p1;
-            sm.dg[t] += bt * (p1 - p2);   // -beta e^g (K S)_t . dR_t
-        }
-    }
-    {   // dA_kk = -strict_lower(dR U^T); its terms of dg and dbeta; M2 <- X
-        float dk2[SPT];
+        __syncthreads();   // V - e^g K S, dU and T fully read
 #pragma unroll
-        for (int x = 0; x < SPT; ++x) dk2[x] = 0.f;
-        for (int j = 0; j < D; ++j) {
-            const float r = sm.tB[t][j];
+        for (int m = 0; m < 2; ++m)
 #pragma unroll
-            for (int x = 0; x < SPT; ++x) dk2[x] = fmaf(r, sm.tA[cq + 4 * x][j], dk2[x]);
-        }
-        float rs = 0.f, rb = 0.f;
-        const float bt = sm.v.beta[t];
+            for (int q = 0; q < JT / 4; ++q)
+                *reinterpret_cast<float4 *>(&sm.tB[ta[m]][colA(q)]) =
+                    make_float4(dr[m][4 * q], dr[m][4 * q + 1], dr[m][4 * q + 2], dr[m][4 * q + 3]);
+        if (cg == 0) {
 #pragma unroll
-        for (int x = 0; x < SPT; ++x) {
-            const int s = cq + 4 * x;
-            const float xg = s < t ? -dk2[x] * gam(sm.v, t, s) : 0.f;   // dA_kk o Gamma
-            const float e = xg * sm.M0[t][s];                            // . K K^T
-            rb += e;
-            rs += bt * e;                                                // dA_kk o A_kk
-            sm.M0[t][s] = bt * e;
-            dk2[x] = bt * xg;                                            // X
+            for (int m = 0; m < 2; ++m) {
+                sm.dbeta[ta[m]] = p1[m];
+                sm.dg[ta[m]] += sm.v.beta[ta[m]] * (p1[m] - p2[m]);   // -beta e^g (K S)_t . dR_t
+            }
         }
-        rs += __shfl_xor_sync(0xffffffffu, rs, 1);
-        rs += __shfl_xor_sync(0xffffffffu, rs, 2);
-        rb += __shfl_xor_sync(0xffffffffu, rb, 1);
-        rb += __shfl_xor_sync(0xffffffffu, rb, 2);
-        __syncthreads();   // dbeta, dg of the previous block and the new M0 entries
-        if (cq == 0) {
-            sm.dg[t] += rs;
-            sm.dbeta[t] += rb;
-        }
-        sub_col_sums(sm.M0, sm.dgcol, tid);
-#pragma unroll
-        for (int x = 0; x < SPT; ++x) sm.M2[t][cq + 4 * x] = dk2[x];
     }
     __syncthreads();
-    if (tid < C) sm.dg[tid] -= sm.dgcol[tid];
-    // dQ and dK, S and dS' staged in tC 32 rows at a time; dims i = i0 + cq + 4 x
-    float(*Sb)[LB] = reinterpret_cast<float(*)[LB]>(&sm.tC[0][0]);
-    float(*Db)[LB] = Sb + IB;
-    const float eg = sm.v.eg[t], egc = sm.v.egc[t], bt = sm.v.beta[t];
-    const float db = sm.dbeta[t];
-    float cn = 0.f;   // the gradient through beta's key norm
-    if (p.beta_mode == 0 && sm.v.den[t] != 0.f) {
-        const float den = sm.v.den[t];
-        cn = -2.f * sm.v.eta[t] * db / (den * den);
+    {   // (B) dA_kk = -strict_lower(dR U^T); its terms of dg and dbeta; M2 <- X
+        float dk2[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int n = 0; n < 4; ++n) dk2[m][n] = 0.f;
+#pragma unroll 2
+        for (int j = 0; j < D; j += 4) {
+            float4 r4[4], u4[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) r4[m] = ld4(&sm.tB[4 * tb + m][j]);
+#pragma unroll
+            for (int n = 0; n < 4; ++n) u4[n] = ld4(&sm.tA[sb + 16 * n][j]);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int n = 0; n < 4; ++n) dk2[m][n] += dot4(r4[m], u4[n]);
+        }
+        float rs[4], rb[4], fv[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int t = 4 * tb + m;
+            const float bt = sm.v.beta[t];
+            rs[m] = rb[m] = 0.f;
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                const int s2 = sb + 16 * n;
+                const float xg = s2 < t ? -dk2[m][n] * gam(sm.v, t, s2) : 0.f;   // dA_kk o Gamma
+                const float e = xg * sm.M0[t][s2];                               // . K K^T
+                rb[m] += e;
+                rs[m] += bt * e;                                                 // dA_kk o A_kk
+                fv[m][n] = bt * e;
+                dk2[m][n] = bt * xg;                                             // X
+            }
+#pragma unroll
+            for (int off = 1; off < 16; off <<= 1) {
+                rs[m] += __shfl_xor_sync(0xffffffffu, rs[m], off);
+                rb[m] += __shfl_xor_sync(0xffffffffu, rb[m], off);
+            }
+        }
+        __syncthreads();   // raw K K^T reads complete
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                sm.M0[4 * tb + m][sb + 16 * n] = fv[m][n];
+                sm.M2[4 * tb + m][sb + 16 * n] = dk2[m][n];
+            }
+        if (sb == 0) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                sm.dg[4 * tb + m] += rs[m];
+                sm.dbeta[4 * tb + m] += rb[m];
+            }
+        }
+        __syncthreads();
+        col_sums<LM>(sm.M0, sm.dgcol, tid);
+        __syncthreads();
+        if (tid < C) sm.dg[tid] -= sm.dgcol[tid];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)   // M0 <- X + X^T
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                const int t = 4 * tb + m, s2 = sb + 16 * n;
+                sm.M0[t][s2] = sm.M2[t][s2] + sm.M2[s2][t];
+            }
     }
-    float gq = 0.f, gk = 0.f, sds = 0.f;
+    __syncthreads();
+    // (P) dQ and dK; S and dS' staged in tC 32 rows at a time
+    float(*Sb)[LK] = reinterpret_cast<float(*)[LK]>(&sm.tC[0][0]);
+    float(*Db)[LK] = Sb + IB;
+    float eg[2], egc[2], bt[2], cn[2];
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        const int t = ta[m];
+        eg[m] = sm.v.eg[t]; egc[m] = sm.v.egc[t]; bt[m] = sm.v.beta[t];
+        cn[m] = 0.f;   // the gradient through beta's key norm
+        if (p.beta_mode == 0 && sm.v.den[t] != 0.f) {
+            const float den = sm.v.den[t];
+            cn[m] = -2.f * sm.v.eta[t] * sm.dbeta[t] / (den * den);
+        }
+    }
+    float gq[2] = {0.f, 0.f}, gk[2] = {0.f, 0.f}, sds = 0.f;
     Tin *dqo = static_cast<Tin *>(p.dq);
     Tin *dko = static_cast<Tin *>(p.dk);
-    constexpr int VE = 16 / (int)sizeof(Tin);
+#pragma unroll
     for (int i0 = 0; i0 < D; i0 += IB) {
         __syncthreads();   // the previous block is fully read
-        load_block_f32<IB, D, LB, NT>(&Sb[0][0], S + (size_t)i0 * D, D, tid);
-        load_block_f32<IB, D, LB, NT>(&Db[0][0], dSp + (size_t)i0 * D, D, tid);
+        load_block_f32<IB, D, LK, NT>(&Sb[0][0], S + (size_t)i0 * D, D, tid);
+        load_block_f32<IB, D, LK, NT>(&Db[0][0], dSp + (size_t)i0 * D, D, tid);
         __syncthreads();
         for (int x = tid; x < IB * D; x += NT) sds = fmaf(Sb[x / D][x % D], Db[x / D][x % D], sds);
-        constexpr int XI = IB / 4;
-        float pq[XI], pr[XI], pu[XI];
+        float pr[2][4], pu[2][4];
 #pragma unroll
-        for (int x = 0; x < XI; ++x) pq[x] = pr[x] = pu[x] = 0.f;
-        for (int j = 0; j < D; j += VE) {
-            float o[VE];
-            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-            if (live) raw = *reinterpret_cast<const uint4 *>(dout + rt * D + j);
-            unpack16(raw, o);
+        for (int m = 0; m < 2; ++m)
 #pragma unroll
-            for (int e = 0; e < VE; ++e) {
-                const float r = sm.tB[t][j + e], u = sm.tA[t][j + e];
+            for (int n = 0; n < 4; ++n) pr[m][n] = pu[m][n] = 0.f;
+#pragma unroll 2
+        for (int j = 0; j < D; j += 4) {
+            float4 r4[2], u4[2], s4[4], d4[4];
 #pragma unroll
-                for (int x = 0; x < XI; ++x) {
-                    const int il = cq + 4 * x;
-                    const float sv = Sb[il][j + e];
-                    pq[x] = fmaf(o[e], sv, pq[x]);
-                    pr[x] = fmaf(r, sv, pr[x]);
-                    pu[x] = fmaf(u, Db[il][j + e], pu[x]);
+            for (int m = 0; m < 2; ++m) {
+                r4[m] = ld4(&sm.tB[ta[m]][j]);
+                u4[m] = ld4(&sm.tA[ta[m]][j]);
+            }
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                s4[n] = ld4(&Sb[cg + 8 * n][j]);
+                d4[n] = ld4(&Db[cg + 8 * n][j]);
+            }
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    pr[m][n] += dot4(r4[m], s4[n]);
+                    pu[m][n] += dot4(u4[m], d4[n]);
+                }
+        }
+        // (dA_qk o Gamma) K, its transpose times Q, (X + X^T) K
+        float dq[2][4], dkk[2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int n = 0; n < 4; ++n) dq[m][n] = dkk[m][n] = 0.f;
+#pragma unroll 2
+        for (int s2 = 0; s2 < C; ++s2) {
+            float kv[4], qv[4];
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                kv[n] = sm.K[s2][i0 + cg + 8 * n];
+                qv[n] = sm.Q[s2][i0 + cg + 8 * n];
+            }
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const float a_ts = sm.M1[ta[m]][s2], a_st = sm.M1[s2][ta[m]], x2 = sm.M0[ta[m]][s2];
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    dq[m][n] = fmaf(a_ts, kv[n], dq[m][n]);
+                    dkk[m][n] = fmaf(a_st, qv[n], fmaf(x2, kv[n], dkk[m][n]));
                 }
             }
         }
-        float dq[XI], dkk[XI];
 #pragma unroll
-        for (int x = 0; x < XI; ++x) dq[x] = dkk[x] = 0.f;
-        for (int s = 0; s < C; ++s) {
-            const float a_ts = sm.M1[t][s], a_st = sm.M1[s][t];
-            const float x2 = sm.M2[t][s] + sm.M2[s][t];
+        for (int m = 0; m < 2; ++m) {
 #pragma unroll
-            for (int x = 0; x < XI; ++x) {
-                const int i = i0 + cq + 4 * x;
-                const float ks = sm.K[s][i];
-                dq[x] = fmaf(a_ts, ks, dq[x]);
-                dkk[x] = fmaf(a_st, sm.Q[s][i], fmaf(x2, ks, dkk[x]));
-            }
-        }
-#pragma unroll
-        for (int x = 0; x < XI; ++x) {
-            const int i = i0 + cq + 4 * x;
-            dq[x] = fmaf(eg, pq[x], dq[x]);
-            dkk[x] = fmaf(-bt * eg, pr[x], dkk[x]);
-            dkk[x] = fmaf(egc, pu[x], dkk[x]);
-            dkk[x] = fmaf(cn, sm.K[t][i], dkk[x]);
-            gq = fmaf(sm.Q[t][i], pq[x], gq);
-            gk = fmaf(sm.K[t][i], pu[x], gk);
-            if (live) {
-                st_out(dqo, rt * D + i, dq[x]);
-                st_out(dko, rt * D + i, dkk[x]);
+            for (int n = 0; n < 4; ++n) {
+                const int i = i0 + cg + 8 * n;
+                const float kv = sm.K[ta[m]][i], qv = sm.Q[ta[m]][i];
+                const float pqv = pq[m][i0 / 8 + n];
+                dq[m][n] = fmaf(eg[m], pqv, dq[m][n]);
+                dkk[m][n] = fmaf(-bt[m] * eg[m], pr[m][n], dkk[m][n]);
+                dkk[m][n] = fmaf(egc[m], pu[m][n], dkk[m][n]);
+                dkk[m][n] = fmaf(cn[m], kv, dkk[m][n]);
+                gq[m] = fmaf(qv, pqv, gq[m]);
+                gk[m] = fmaf(kv, pu[m][n], gk[m]);
+                if (liveA[m]) {
+                    dqo[rowA[m] * D + i] = static_cast<Tin>(dq[m][n]);
+                    dko[rowA[m] * D + i] = static_cast<Tin>(dkk[m][n]);
+                }
             }
         }
     }
-    gq += __shfl_xor_sync(0xffffffffu, gq, 1);
-    gq += __shfl_xor_sync(0xffffffffu, gq, 2);
-    gk += __shfl_xor_sync(0xffffffffu, gk, 1);
-    gk += __shfl_xor_sync(0xffffffffu, gk, 2);
     // dg: exp(g) of the Q S read, exp(g_C - g) of the state write; dg_C: the
     // state write and exp(g_C) S
-    const float wk = egc * gk;
-    if (cq == 0) sm.dg[t] += eg * gq - wk;
-    float red = ((cq == 0) ? wk : 0.f) + sm.v.eg[C - 1] * sds;
+    float red = sm.v.eg[C - 1] * sds;
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1) {
+            gq[m] += __shfl_xor_sync(0xffffffffu, gq[m], off);
+            gk[m] += __shfl_xor_sync(0xffffffffu, gk[m], off);
+        }
+        const float wk = egc[m] * gk[m];
+        if (cg == 0) {
+            sm.dg[ta[m]] += eg[m] * gq[m] - wk;
+            red += wk;
+        }
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) red += __shfl_xor_sync(0xffffffffu, red, off);
     if ((tid & 31) == 0) sm.red[tid >> 5] = red;

@@ -9,10 +9,11 @@ namespace kla {
 // substitution (64 threads, one column each), then twice the merge
 //   [[D1, 0], [L21, D2]]^{-1} = [[D1^{-1}, 0], [-D2^{-1} L21 D1^{-1}, D2^{-1}]]
 // (32 x 32 blocks from pairs of 16 x 16, then the whole 64 x 64), whose two
-// products use all 256 threads.  A and T are [64][65] (padded rows);
-// scratch holds 32 x 33 floats.  Every thread of the 256-thread block calls
-// it; it ends with a barrier.
-__device__ inline void invert_unit_lower64(const float (*A)[65], float (*Tm)[65], float *scratch,
+// products use all 256 threads.  A and T are 64-row arrays with padded rows
+// of LA and LT floats; scratch holds 32 x 33 floats.  Every thread of the
+// 256-thread block calls it; it ends with a barrier.
+template <int LA, int LT>
+__device__ inline void invert_unit_lower64(const float (*A)[LA], float (*Tm)[LT], float *scratch,
                                            int tid) {
     for (int x = tid; x < 64 * 64; x += 256) {
         const int t = x >> 6, s = x & 63;
