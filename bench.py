@@ -494,8 +494,8 @@ def ours(args):
                 "launches": bw["launches"],
                 "roofline": {"bound": "hbm", "achieved": bw_gbs, "peak": pk["hbm_gbs"],
                              "unit": "GB/s", "frac": bw_gbs / pk["hbm_gbs"], "traffic": None,
-                             "kernel": "chunk_simt_kernel (states) + bwd_dstate_kernel + "
-                                       "bwd_grads_kernel",
+                             "kernel": "intra_kernel + state_kernel (recording the states) + "
+                                       "bwd_dstate_tc_kernel + bwd_grads_kernel",
                              "algorithmic_bytes_per_call": bw["bytes"]}}
 
     cpu = None
