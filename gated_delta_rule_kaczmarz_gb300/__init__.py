@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     kla_ccq_query,
     kla_ccq_query_step,
     kla_ccq_query_workspace_size,
+    kla_chunk,
     kla_chunk_bwd,
     kla_chunk_bwd_workspace_size,
     kla_chunk_fwd,

@@ -246,6 +246,37 @@ def kla_chunk_bwd(q, k, v, alpha, eta, eps, S0, d_o, dS_T=None, workspace=None, 
     return dq, dkk, dvv, dalpha, deta, dS0
 
 
+class _KlaChunk(torch.autograd.Function):
+    """kla_chunk_fwd as an autograd function: its backward is kla_chunk_bwd."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, alpha, eta, S0, eps, beta_mode):
+        o, S_T = kla_chunk_fwd(q, k, v, alpha, eta, eps, S0, beta_mode=beta_mode)
+        ctx.save_for_backward(q, k, v, alpha, eta, S0)
+        ctx.has_alpha, ctx.has_S0 = alpha is not None, S0 is not None
+        ctx.eps, ctx.beta_mode = eps, beta_mode
+        return o, S_T
+
+    @staticmethod
+    def backward(ctx, d_o, dS_T):
+        q, k, v, alpha, eta, S0 = ctx.saved_tensors
+        alpha = alpha if ctx.has_alpha else None
+        S0 = S0 if ctx.has_S0 else None
+        if d_o is None:
+            d_o = torch.zeros_like(v)
+        dq, dk, dv, da, de, dS0 = kla_chunk_bwd(
+            q, k, v, alpha, eta, ctx.eps, S0, d_o.contiguous().to(q.dtype),
+            None if dS_T is None else dS_T.contiguous().float(), beta_mode=ctx.beta_mode,
+            want_dS0=ctx.has_S0)
+        return dq, dk, dv, da, de, dS0, None, None
+
+
+def kla_chunk(q, k, v, alpha, eta, eps, S0=None, beta_mode="kaczmarz"):
+    """Differentiable chunkwise forward: (o, S_T) = kla_chunk_fwd(...), with
+    gradients for q, k, v, alpha, eta and S0 from kla_chunk_bwd."""
+    return _KlaChunk.apply(q, k, v, alpha, eta, S0, float(eps), beta_mode)
+
+
 def kla_chunk_fwd_noalloc(q, k, v, alpha, eta, eps, S0=None, o=None, S_T=None, stream=None,
                           chunk=CHUNK):
     """kla_chunk_fwd for callers that cannot allocate device memory while the
