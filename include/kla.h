@@ -121,6 +121,19 @@ KLA_API size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv,
  *              entry are ignored.  One workspace must not be shared by calls
  *              that may run concurrently.
  * T == 0 or B == 0 is valid and writes only S_T (= S0, or zeros).
+ *
+ * Execution (bf16, dk = dv = 128, B*T >= 64): the tensor-core kernels, as one
+ * cooperative launch when the state pass of every (batch, head) fits on half
+ * of the SMs and each sequence has an even number of chunks, else as two.
+ * Few heads with long sequences run the sequence split: each sequence as P
+ * segments (P in {2, 4, 8}, segments of whole 128-token tiles and at least
+ * 1024 tokens, chosen so that the state and transition passes fit on the
+ * SMs), whose start states are chained and whose outputs are corrected (four
+ * launches, or three when fused).  The environment variable KLA_SEQ_SPLIT=P
+ * forces a factor (1 disables the split); the workspace size depends on that
+ * choice and on the SM count of the current device, so query it on the device
+ * and with the environment of the call.  Other dtypes and sizes run on the
+ * CUDA cores (fp32 arithmetic).
  */
 KLA_API int kla_chunk_fwd(const void *q, const void *k, const void *v,
                   const float *alpha, const float *eta, float eps,
