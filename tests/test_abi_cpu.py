@@ -207,3 +207,19 @@ def test_backward_host_validation():
     assert call(None, ctypes.c_void_p(0x100010), 1 << 40) == binding.KLA_ERR_INVALID_ARG
     n = lib.kla_chunk_bwd_workspace_size(1, 64, 1, 64, 1)
     assert n >= 2 * 64 * 64 * 4
+
+
+def test_sequence_split_workspace(monkeypatch):
+    """The split's buffers (per-segment end states, transitions, the
+    correction rows, the start states) enlarge the forward's workspace; a
+    factor whose segments are not whole 128-token tiles is ignored."""
+    lib = binding.load()
+    size = lambda: lib.kla_chunk_fwd_workspace_size(1, 32768, 16, 128, 128, 64, 1)
+    monkeypatch.setenv("KLA_SEQ_SPLIT", "1")
+    base = size()
+    monkeypatch.setenv("KLA_SEQ_SPLIT", "2")
+    split2 = size()
+    # correction rows alone: T * H * 128 bf16
+    assert split2 - base >= 32768 * 16 * 128 * 2
+    monkeypatch.setenv("KLA_SEQ_SPLIT", "3")   # 32768 is not a multiple of 3 * 128
+    assert size() == base
