@@ -11,6 +11,8 @@ from .binding import (  # noqa: F401
     kla_ccq_query_workspace_size,
     kla_chunk,
     kla_chunk_bwd,
+    kla_chunk_bwd_varlen,
+    kla_chunk_bwd_varlen_workspace_size,
     kla_chunk_bwd_workspace_size,
     kla_chunk_fwd,
     kla_chunk_fwd_ex,

@@ -100,6 +100,11 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
         lib.kla_chunk_bwd.restype = I
         lib.kla_chunk_bwd.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, fp, vp, vp, vp, fp, fp, fp,
                                       I, I, I, I, I, I, I, I, vp, Z, vp]
+        lib.kla_chunk_bwd_varlen_workspace_size.restype = Z
+        lib.kla_chunk_bwd_varlen_workspace_size.argtypes = [I, I, I, I, I]
+        lib.kla_chunk_bwd_varlen.restype = I
+        lib.kla_chunk_bwd_varlen.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, fp, vp, vp, vp, fp, fp,
+                                             fp, ip, I, I, I, I, I, I, I, I, vp, Z, vp]
         lib.kla_chunk_fwd_noalloc.restype = I
         lib.kla_chunk_fwd_noalloc.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, fp,
                                               I, I, I, I, I, I, I, vp]
@@ -242,6 +247,42 @@ def kla_chunk_bwd(q, k, v, alpha, eta, eps, S0, d_o, dS_T=None, workspace=None, 
                            _ptr(S0), _ptr(d_o), _ptr(dS_T), _ptr(dq), _ptr(dkk), _ptr(dvv),
                            _ptr(dalpha), _ptr(deta), _ptr(dS0), B, T, H, dk, dv, chunk, dt,
                            _mode(beta_mode), _ptr(workspace), wsb, _stream(stream))
+    _check(st)
+    return dq, dkk, dvv, dalpha, deta, dS0
+
+
+def kla_chunk_bwd_varlen_workspace_size(N, total_T, H, dk, dtype=KLA_DTYPE_BF16) -> int:
+    return int(load().kla_chunk_bwd_varlen_workspace_size(N, total_T, H, dk, dtype))
+
+
+def kla_chunk_bwd_varlen(q, k, v, alpha, eta, eps, cu_seqlens, S0, d_o, dS_T=None,
+                         workspace=None, stream=None, chunk=CHUNK, beta_mode="kaczmarz",
+                         want_dS0=True):
+    """Backward of kla_chunk_fwd_varlen: packed q, k: [total_T,H,dk], v, d_o:
+    [total_T,H,dv], alpha, eta: [total_T,H] fp32, cu_seqlens: int32 [N+1] on the
+    device, S0, dS_T: [N,H,dk,dv] fp32 or None.  Returns (dq, dk, dv, dalpha,
+    deta, dS0) like kla_chunk_bwd."""
+    lib = load()
+    total_T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.shape[0] - 1
+    dt = _dtype_code(q)
+    _need(q, "q"); _need(k, "k", q.dtype, (total_T, H, dk)); _need(v, "v", q.dtype, (total_T, H, dv))
+    _need(alpha, "alpha", torch.float32, (total_T, H)); _need(eta, "eta", torch.float32, (total_T, H))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,))
+    _need(S0, "S0", torch.float32, (N, H, dk, dv)); _need(d_o, "d_o", q.dtype, (total_T, H, dv))
+    _need(dS_T, "dS_T", torch.float32, (N, H, dk, dv))
+    dq, dkk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dalpha = None if alpha is None else torch.empty_like(alpha)
+    deta = torch.empty_like(eta)
+    dS0 = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device) if want_dS0 else None
+    nbytes = int(lib.kla_chunk_bwd_varlen_workspace_size(N, total_T, H, dk, dt))
+    workspace, wsb = _workspace(nbytes, q.device, workspace)
+    st = lib.kla_chunk_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), float(eps),
+                                  _ptr(S0), _ptr(d_o), _ptr(dS_T), _ptr(dq), _ptr(dkk), _ptr(dvv),
+                                  _ptr(dalpha), _ptr(deta), _ptr(dS0), _ptr(cu_seqlens), N,
+                                  total_T, H, dk, dv, chunk, dt, _mode(beta_mode),
+                                  _ptr(workspace), wsb, _stream(stream))
     _check(st)
     return dq, dkk, dvv, dalpha, deta, dS0
 

@@ -148,6 +148,63 @@ namespace kla {
 void set_error_message(const char *msg) { g_last_error = msg; }
 }  // namespace kla
 
+namespace {
+// Shared by the fixed-length and varlen backward entries (cu_seqlens NULL:
+// fixed length, n_seq = B, T given).
+int run_bwd(const void *q, const void *k, const void *v, const float *alpha, const float *eta,
+            float eps, const float *S0, const void *d_o, const float *dS_T, void *dq, void *dk,
+            void *dv, float *dalpha, float *deta, float *dS0, const int *cu_seqlens, int n_seq,
+            int T, int total_T, int H, int dk_, int dv_, int chunk, int dtype, int beta_mode,
+            void *workspace, size_t workspace_bytes, void *stream) {
+    kla_status st = check_shape(H, dk_, dv_, chunk, dtype);
+    if (st != KLA_OK) return st;
+    if (beta_mode != KLA_BETA_KACZMARZ && beta_mode != KLA_BETA_GIVEN)
+        return fail(KLA_ERR_INVALID_ARG, "unknown beta_mode %d", beta_mode);
+    if (!(eps >= 0.f)) return fail(KLA_ERR_INVALID_ARG, "eps must be >= 0");
+    const long rows = total_T;
+    if ((long)n_seq * H > INT32_MAX)
+        return fail(KLA_ERR_UNSUPPORTED, "problem too large (sequences x H must fit in int32)");
+    if (dalpha && !alpha)
+        return fail(KLA_ERR_INVALID_ARG, "dalpha requires alpha (no decay has no alpha gradient)");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv) || !aligned4(alpha) || !aligned4(eta) ||
+        !aligned4(dalpha) || !aligned4(deta) || !aligned16(S0) || !aligned16(dS_T) ||
+        !aligned16(dS0))
+        return fail(KLA_ERR_INVALID_ARG,
+                    "q, k, v, d_o, dq, dk, dv and the states must be 16-byte aligned, the "
+                    "per-token gates 4-byte");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (rows == 0 || n_seq == 0) {   // no tokens: dS0 = dS_T
+        if (inject_launch_fault()) return fail(KLA_ERR_CUDA, "injected launch fault (KLA_FAULT_INJECT)");
+        return states_only(dS_T, dS0, (size_t)n_seq * H * dk_ * dv_, s);
+    }
+    if (!q || !k || !v || !eta || !d_o || !dq || !dk || !dv)
+        return fail(KLA_ERR_INVALID_ARG, "q, k, v, eta, d_o, dq, dk and dv must be non-null");
+    const size_t need = kla::kWsHeader + kla::chunk_bwd_workspace_bytes(
+                                             cu_seqlens != nullptr, n_seq, T, total_T, H, dk_,
+                                             dtype);
+    if (workspace == nullptr || workspace_bytes < need)
+        return fail(KLA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(KLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (inject_launch_fault()) return fail(KLA_ERR_CUDA, "injected launch fault (KLA_FAULT_INJECT)");
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(unsigned), s);   // status word
+    if (e != cudaSuccess) return cuda_fail(e, "status init");
+    kla::BwdProblem p{};
+    p.q = q; p.k = k; p.v = v; p.dout = d_o; p.alpha = alpha; p.eta = eta; p.S0 = S0;
+    p.dS_T = dS_T; p.eps = eps; p.dq = dq; p.dk = dk; p.dv = dv; p.dalpha = dalpha;
+    p.deta = deta; p.dS0 = dS0; p.n_seq = n_seq; p.T = T; p.total_T = total_T;
+    p.cu_seqlens = cu_seqlens; p.H = H; p.d = dk_; p.dtype = dtype;
+    p.beta_mode = beta_mode;
+    p.status = static_cast<unsigned *>(workspace);
+    p.ws = static_cast<unsigned char *>(workspace) + kla::kWsHeader;
+    e = kla::launch_chunk_bwd(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return ok();
+}
+}  // namespace
+
 extern "C" {
 
 const char *kla_status_str(int status) {
@@ -303,7 +360,14 @@ int kla_decode_step(const void *q, const void *k, const void *v, const float *al
 size_t kla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dtype) {
     if (B < 0 || T < 0) return 0;
     if (check_shape(H, dk, dk, kla::kChunk, dtype) != KLA_OK) return 0;
-    return kla::kWsHeader + kla::chunk_bwd_workspace_bytes(B, T, H, dk, dtype);
+    return kla::kWsHeader +
+           kla::chunk_bwd_workspace_bytes(false, B, T, (int)((long)B * T), H, dk, dtype);
+}
+
+size_t kla_chunk_bwd_varlen_workspace_size(int N, int total_T, int H, int dk, int dtype) {
+    if (N < 0 || total_T < 0) return 0;
+    if (check_shape(H, dk, dk, kla::kChunk, dtype) != KLA_OK) return 0;
+    return kla::kWsHeader + kla::chunk_bwd_workspace_bytes(true, N, 0, total_T, H, dk, dtype);
 }
 
 int kla_chunk_bwd(const void *q, const void *k, const void *v, const float *alpha,
@@ -312,49 +376,27 @@ int kla_chunk_bwd(const void *q, const void *k, const void *v, const float *alph
                   float *dS0, int B, int T, int H, int dk_, int dv_, int chunk, int dtype,
                   int beta_mode, void *workspace, size_t workspace_bytes, void *stream) {
     if (B < 0 || T < 0) return fail(KLA_ERR_INVALID_ARG, "negative size (B=%d T=%d)", B, T);
-    kla_status st = check_shape(H, dk_, dv_, chunk, dtype);
-    if (st != KLA_OK) return st;
-    if (beta_mode != KLA_BETA_KACZMARZ && beta_mode != KLA_BETA_GIVEN)
-        return fail(KLA_ERR_INVALID_ARG, "unknown beta_mode %d", beta_mode);
-    if (!(eps >= 0.f)) return fail(KLA_ERR_INVALID_ARG, "eps must be >= 0");
-    const long rows = (long)B * T;
-    if (rows > INT32_MAX || (long)B * H > INT32_MAX)
-        return fail(KLA_ERR_UNSUPPORTED, "problem too large (B*T and B*H must fit in int32)");
-    if (dalpha && !alpha)
-        return fail(KLA_ERR_INVALID_ARG, "dalpha requires alpha (no decay has no alpha gradient)");
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) || !aligned16(dq) ||
-        !aligned16(dk) || !aligned16(dv) || !aligned4(alpha) || !aligned4(eta) ||
-        !aligned4(dalpha) || !aligned4(deta) || !aligned16(S0) || !aligned16(dS_T) ||
-        !aligned16(dS0))
-        return fail(KLA_ERR_INVALID_ARG,
-                    "q, k, v, d_o, dq, dk, dv and the states must be 16-byte aligned, the "
-                    "per-token gates 4-byte");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (rows == 0) {   // no tokens: dS0 = dS_T
-        if (inject_launch_fault()) return fail(KLA_ERR_CUDA, "injected launch fault (KLA_FAULT_INJECT)");
-        return states_only(dS_T, dS0, (size_t)B * H * dk_ * dv_, s);
-    }
-    if (!q || !k || !v || !eta || !d_o || !dq || !dk || !dv)
-        return fail(KLA_ERR_INVALID_ARG, "q, k, v, eta, d_o, dq, dk and dv must be non-null");
-    const size_t need = kla::kWsHeader + kla::chunk_bwd_workspace_bytes(B, T, H, dk_, dtype);
-    if (workspace == nullptr || workspace_bytes < need)
-        return fail(KLA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
-                    workspace ? workspace_bytes : (size_t)0);
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return fail(KLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    if (inject_launch_fault()) return fail(KLA_ERR_CUDA, "injected launch fault (KLA_FAULT_INJECT)");
-    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(unsigned), s);   // status word
-    if (e != cudaSuccess) return cuda_fail(e, "status init");
-    kla::BwdProblem p{};
-    p.q = q; p.k = k; p.v = v; p.dout = d_o; p.alpha = alpha; p.eta = eta; p.S0 = S0;
-    p.dS_T = dS_T; p.eps = eps; p.dq = dq; p.dk = dk; p.dv = dv; p.dalpha = dalpha;
-    p.deta = deta; p.dS0 = dS0; p.B = B; p.T = T; p.H = H; p.d = dk_; p.dtype = dtype;
-    p.beta_mode = beta_mode;
-    p.status = static_cast<unsigned *>(workspace);
-    p.ws = static_cast<unsigned char *>(workspace) + kla::kWsHeader;
-    e = kla::launch_chunk_bwd(p, s);
-    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-    return ok();
+    if ((long)B * T > INT32_MAX)
+        return fail(KLA_ERR_UNSUPPORTED, "problem too large (B*T must fit in int32)");
+    return run_bwd(q, k, v, alpha, eta, eps, S0, d_o, dS_T, dq, dk, dv, dalpha, deta, dS0,
+                   nullptr, B, T, (int)((long)B * T), H, dk_, dv_, chunk, dtype, beta_mode,
+                   workspace, workspace_bytes, stream);
+}
+
+int kla_chunk_bwd_varlen(const void *q, const void *k, const void *v, const float *alpha,
+                         const float *eta, float eps, const float *S0, const void *d_o,
+                         const float *dS_T, void *dq, void *dk, void *dv, float *dalpha,
+                         float *deta, float *dS0, const int *cu_seqlens, int N, int total_T,
+                         int H, int dk_, int dv_, int chunk, int dtype, int beta_mode,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+    if (N < 0 || total_T < 0)
+        return fail(KLA_ERR_INVALID_ARG, "negative size (N=%d total_T=%d)", N, total_T);
+    if (N > 0 && total_T > 0 && !cu_seqlens)
+        return fail(KLA_ERR_INVALID_ARG, "cu_seqlens must be non-null");
+    if (!aligned4(cu_seqlens)) return fail(KLA_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
+    return run_bwd(q, k, v, alpha, eta, eps, S0, d_o, dS_T, dq, dk, dv, dalpha, deta, dS0,
+                   cu_seqlens, N, 0, total_T, H, dk_, dv_, chunk, dtype, beta_mode, workspace,
+                   workspace_bytes, stream);
 }
 
 size_t kla_ccq_query_workspace_size(int B, int T, int H, int dk, int dtype) {

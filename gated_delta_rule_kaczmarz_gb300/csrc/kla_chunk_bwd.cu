@@ -55,6 +55,28 @@ struct Vec {
     float alpha[C], eta[C], g[C], beta[C], eg[C], egc[C], den[C];
 };
 
+// Token rows and chunks of sequence n: fixed length (rows n T .. n T + T - 1,
+// chunks n nch ..) or packed varlen (cu_seqlens, chunk_prefix).  Recorded
+// states are indexed by chunk slot = chunk * H + head.
+struct SeqGeo {
+    long start, chunk0;
+    int len, nch;
+};
+__device__ __forceinline__ SeqGeo seq_geo(const BwdProblem &p, int n) {
+    SeqGeo g;
+    if (p.cu_seqlens) {
+        g.start = p.cu_seqlens[n];
+        g.len = p.cu_seqlens[n + 1] - p.cu_seqlens[n];
+        g.chunk0 = p.chunk_prefix[n];
+    } else {
+        g.start = (long)n * p.T;
+        g.len = p.T;
+        g.chunk0 = (long)n * ((p.T + C - 1) / C);
+    }
+    g.nch = (g.len + C - 1) / C;
+    return g;
+}
+
 template <typename Tin, int D>
 __device__ void load_kq(float (*K)[D + 1], float (*Q)[D + 1], Vec &v, const BwdProblem &p,
                         long row0, int nc, int h, int tid) {
@@ -166,13 +188,14 @@ struct DsSmem {
 };
 
 template <typename Tin, int D>
-__global__ void __launch_bounds__(NT, 1) bwd_dstate_kernel(BwdProblem p, int nch, float *dS_chk) {
+__global__ void __launch_bounds__(NT, 1) bwd_dstate_kernel(BwdProblem p, float *dS_chk) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     DsSmem<D> &sm = *reinterpret_cast<DsSmem<D> *>(smem_raw);
     const int tid = threadIdx.x;
-    const int unit = blockIdx.x, b = unit / p.H, h = unit % p.H;
+    const int unit = blockIdx.x, h = unit % p.H;
     const int jb = blockIdx.y * DVB;
     if (p.status != nullptr && *(volatile unsigned *)p.status != kDevOk) return;
+    const SeqGeo sg = seq_geo(p, unit / p.H);
     const Tin *dout = static_cast<const Tin *>(p.dout);
     const size_t sbase = (size_t)unit * D * D;
 
@@ -180,11 +203,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_dstate_kernel(BwdProblem p, int nch
         const int i = x / DVB, j = x % DVB;
         sm.dS[i][j] = p.dS_T ? p.dS_T[sbase + (size_t)i * D + jb + j] : 0.f;
     }
-    for (int c = nch - 1; c >= 0; --c) {
-        const long row0 = (long)b * p.T + (long)c * C;
-        const int nc = min(C, p.T - c * C);
+    for (int c = sg.nch - 1; c >= 0; --c) {
+        const long row0 = sg.start + (long)c * C;
+        const int nc = min(C, sg.len - c * C);
         __syncthreads();   // the previous chunk is done with every tile
-        float *rec = dS_chk + ((size_t)unit * nch + c) * D * D;   // dS' of chunk c
+        float *rec = dS_chk + ((size_t)(sg.chunk0 + c) * p.H + h) * D * D;   // dS' of chunk c
         for (int x = tid; x < D * DVB; x += NT) {
             const int i = x / DVB, j = x % DVB;
             rec[(size_t)i * D + jb + j] = sm.dS[i][j];
@@ -285,14 +308,14 @@ __device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, boo
 
 // Issues the asynchronous copies of chunk c's tiles into the staging arrays
 // (rows past the sequence end are zero filled).
-__device__ __forceinline__ void ds_prefetch(DsTcSmem &sm, const BwdProblem &p, int c, int nch,
-                                            int b, int h, int jb, const float *g_ws,
+__device__ __forceinline__ void ds_prefetch(DsTcSmem &sm, const BwdProblem &p, int c,
+                                            const SeqGeo &sg, int h, int jb, const float *g_ws,
                                             const __nv_bfloat16 *W_ws,
                                             const __nv_bfloat16 *A_ws, int tid) {
     constexpr int D = 128;
-    const long row0 = (long)b * p.T + (long)c * C;
-    const int nc = min(C, p.T - c * C);
-    const long slot = ((long)b * nch + c) * p.H + h;
+    const long row0 = sg.start + (long)c * C;
+    const int nc = min(C, sg.len - c * C);
+    const long slot = (sg.chunk0 + c) * p.H + h;
     const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
     const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
     const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(p.dout);
@@ -320,26 +343,27 @@ __device__ __forceinline__ void ds_prefetch(DsTcSmem &sm, const BwdProblem &p, i
 }
 
 __global__ void __launch_bounds__(NT, 1)
-bwd_dstate_tc_kernel(BwdProblem p, int nch, float *dS_chk, const float *g_ws,
+bwd_dstate_tc_kernel(BwdProblem p, float *dS_chk, const float *g_ws,
                      const __nv_bfloat16 *W_ws, const __nv_bfloat16 *A_ws) {
     constexpr int D = 128;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     DsTcSmem &sm = *reinterpret_cast<DsTcSmem *>(smem_raw);
     const int tid = threadIdx.x;
-    const int unit = blockIdx.x, b = unit / p.H, h = unit % p.H;
+    const int unit = blockIdx.x, h = unit % p.H;
     const int jb = blockIdx.y * DVB;
     if (p.status != nullptr && *(volatile unsigned *)p.status != kDevOk) return;
+    const SeqGeo sg = seq_geo(p, unit / p.H);
     const size_t sbase = (size_t)unit * D * D;
     for (int x = tid; x < D * DVB; x += NT) {
         const int i = x / DVB, j = x % DVB;
         sm.dS[i][j] = p.dS_T ? p.dS_T[sbase + (size_t)i * D + jb + j] : 0.f;
     }
-    ds_prefetch(sm, p, nch - 1, nch, b, h, jb, g_ws, W_ws, A_ws, tid);
-    for (int c = nch - 1; c >= 0; --c) {
-        const int nc = min(C, p.T - c * C);
+    if (sg.nch > 0) ds_prefetch(sm, p, sg.nch - 1, sg, h, jb, g_ws, W_ws, A_ws, tid);
+    for (int c = sg.nch - 1; c >= 0; --c) {
+        const int nc = min(C, sg.len - c * C);
         asm volatile("cp.async.wait_all;\n" ::: "memory");
         __syncthreads();   // chunk c's tiles have landed; the previous chunk is done
-        float *rec = dS_chk + ((size_t)unit * nch + c) * D * D;   // dS' of chunk c
+        float *rec = dS_chk + ((size_t)(sg.chunk0 + c) * p.H + h) * D * D;   // dS' of chunk c
         for (int x = tid; x < D * DVB; x += NT) {
             const int i = x / DVB, j = x % DVB;
             rec[(size_t)i * D + jb + j] = sm.dS[i][j];
@@ -354,7 +378,7 @@ bwd_dstate_tc_kernel(BwdProblem p, int nch, float *dS_chk, const float *g_ws,
         for (int x = tid; x < C * DVB; x += NT) sm.dO[x / DVB][x % DVB] = __bfloat162float(sm.dOb[x / DVB][x % DVB]);
         if (tid < C) sm.g[tid] = sm.gb[tid];
         __syncthreads();   // staging free: the next chunk's copies overlap this one's work
-        if (c > 0) ds_prefetch(sm, p, c - 1, nch, b, h, jb, g_ws, W_ws, A_ws, tid);
+        if (c > 0) ds_prefetch(sm, p, c - 1, sg, h, jb, g_ws, W_ws, A_ws, tid);
         if (tid < C) {
             sm.eg[tid] = __expf(sm.g[tid]);
             sm.egc[tid] = __expf(sm.g[C - 1] - sm.g[tid]);
@@ -550,7 +574,7 @@ __device__ void gram_v(const float (*K)[LK], const float (*Q)[LK], float (*Mkk)[
 }
 
 template <typename Tin, int D>
-__global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
+__global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch_fixed,
                                                           const float *S_chk,
                                                           const float *dS_chk) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -560,12 +584,19 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
     constexpr int IB = 32;      // rows of S and dS' per staged block
     Sm &sm = *reinterpret_cast<Sm *>(smem_raw);
     const int tid = threadIdx.x;
-    const int c = blockIdx.x, unit = blockIdx.y, b = unit / p.H, h = unit % p.H;
+    // one CTA per chunk slot: global chunk blockIdx.x, head blockIdx.y
+    const long gch = blockIdx.x;
+    const int h = blockIdx.y;
     if (p.status != nullptr && *(volatile unsigned *)p.status != kDevOk) return;
-    const long row0 = (long)b * p.T + (long)c * C;
-    const int nc = min(C, p.T - c * C);
-    const float *S = S_chk + ((size_t)unit * nch + c) * D * D;     // state at the chunk start
-    const float *dSp = dS_chk + ((size_t)unit * nch + c) * D * D;  // gradient at its end
+    if (p.cu_seqlens && gch >= p.chunk_prefix[p.n_seq]) return;   // past the last chunk
+    const int seq = p.cu_seqlens ? p.chunk_seq[gch] : (int)(gch / nch_fixed);
+    const SeqGeo sq = seq_geo(p, seq);
+    const int c = (int)(gch - sq.chunk0);
+    const long row0 = sq.start + (long)c * C;
+    const int nc = min(C, sq.len - c * C);
+    const size_t slot = (size_t)gch * p.H + h;
+    const float *S = S_chk + slot * D * D;     // state at the chunk start
+    const float *dSp = dS_chk + slot * D * D;  // gradient at its end
     const Tin *dout = static_cast<const Tin *>(p.dout);
     const Tin *vin = static_cast<const Tin *>(p.v);
     // layout A / P thread coordinates
@@ -1057,33 +1088,128 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch,
     }
 }
 
+// Varlen: validates cu_seqlens (cu[0] == 0, non-decreasing, cu[N] ==
+// total_T; a bad table sets the status word and every later kernel of the
+// call skips its work) and builds the chunk tables: the first chunk of each
+// sequence (chunk_prefix[N + 1]) and the sequence of each chunk (chunk_seq).
+constexpr int BP_THREADS = 1024;
+
+__global__ void __launch_bounds__(BP_THREADS)
+bwd_prep_kernel(const int *cu, int N, int total_T, int *chunk_prefix, int *chunk_seq,
+                unsigned *status) {
+    __shared__ int bad, carry;
+    __shared__ int warp_sums[BP_THREADS / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        bad = (cu[0] != 0 || cu[N] != total_T) ? 1 : 0;
+        carry = 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < N; i += BP_THREADS)
+        if (cu[i + 1] < cu[i]) atomicOr(&bad, 1);
+    __syncthreads();
+    if (bad) {
+        if (tid == 0) *status = kDevBadSeqlens;
+        return;
+    }
+    // exclusive prefix sum of the chunk counts, BP_THREADS sequences at a time
+    for (int base = 0; base < N; base += BP_THREADS) {
+        const int n = base + tid;
+        const int cnt = n < N ? (cu[n + 1] - cu[n] + C - 1) / C : 0;
+        int x = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) warp_sums[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int w = warp_sums[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, off);
+                if (lane >= off) w += y;
+            }
+            warp_sums[lane] = w;
+        }
+        __syncthreads();
+        const int incl = x + (warp ? warp_sums[warp - 1] : 0) + carry;
+        if (n < N) chunk_prefix[n] = incl - cnt;
+        __syncthreads();
+        if (tid == BP_THREADS - 1) carry = incl;
+        __syncthreads();
+    }
+    if (tid == 0) chunk_prefix[N] = carry;
+    __syncthreads();
+    for (int n = 0; n < N; ++n) {   // sequences in order; their chunks in parallel
+        const int c0 = chunk_prefix[n], c1 = chunk_prefix[n + 1];
+        for (int g = c0 + tid; g < c1; g += BP_THREADS) chunk_seq[g] = n;
+    }
+}
+
+long bwd_chunks(bool varlen, int n_seq, int T, int total_T) {
+    // every varlen sequence adds at most one partial chunk
+    return varlen ? ((long)total_T + C - 1) / C + n_seq : (long)n_seq * ((T + C - 1) / C);
+}
+
 // bf16 with d = 128 and at least one 64-row TMA box: the tensor-core forward
 // records the chunk-start states, and the dS chain reads its chunk workspace.
-bool bwd_uses_tc(int B, int T, int d, int dtype) {
-    return chunk_tc_supported(d, dtype) && (long)B * T >= C;
+bool bwd_uses_tc(long total_T, int d, int dtype) {
+    return chunk_tc_supported(d, dtype) && total_T >= C;
+}
+
+struct BwdLayout {
+    size_t tables, S, dS, tc, total;
+};
+BwdLayout bwd_layout(bool varlen, int n_seq, int T, int total_T, int H, int d, int dtype) {
+    const long nchunks = bwd_chunks(varlen, n_seq, T, total_T);
+    BwdLayout L;
+    L.tables = 0;
+    const size_t tab = varlen ? ((size_t)n_seq + 1 + (size_t)nchunks) * sizeof(int) : 0;
+    L.S = (tab + 255) / 256 * 256;
+    L.dS = L.S + (size_t)nchunks * H * d * d * sizeof(float);
+    L.tc = L.dS + (size_t)nchunks * H * d * d * sizeof(float);
+    L.total = L.tc + (bwd_uses_tc(total_T, d, dtype) ? chunk_tc_workspace_bytes(nchunks, H, n_seq)
+                                                     : 0);
+    return L;
 }
 
 template <typename Tin, int D>
-cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t s) {
-    const int nch = (p.T + C - 1) / C;
-    const int units = p.B * p.H;
-    float *S_chk = static_cast<float *>(p.ws);
-    float *dS_chk = S_chk + (size_t)units * nch * D * D;
-    const bool tc = bwd_uses_tc(p.B, p.T, D, p.dtype);
+cudaError_t launch_bwd_t(const BwdProblem &p0, cudaStream_t s) {
+    const bool varlen = p0.cu_seqlens != nullptr;
+    const long nchunks = bwd_chunks(varlen, p0.n_seq, p0.T, p0.total_T);
+    const int nch_fixed = varlen ? 0 : (p0.T + C - 1) / C;
+    const int units = p0.n_seq * p0.H;
+    const BwdLayout L = bwd_layout(varlen, p0.n_seq, p0.T, p0.total_T, p0.H, D, p0.dtype);
+    unsigned char *ws = static_cast<unsigned char *>(p0.ws);
+    BwdProblem p = p0;
+    cudaError_t e;
+    if (varlen) {
+        int *prefix = reinterpret_cast<int *>(ws + L.tables);
+        p.chunk_prefix = prefix;
+        p.chunk_seq = prefix + p0.n_seq + 1;
+        bwd_prep_kernel<<<1, BP_THREADS, 0, s>>>(p0.cu_seqlens, p0.n_seq, p0.total_T, prefix,
+                                                  prefix + p0.n_seq + 1, p0.status);
+        note_launch();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    float *S_chk = reinterpret_cast<float *>(ws + L.S);
+    float *dS_chk = reinterpret_cast<float *>(ws + L.dS);
+    const bool tc = bwd_uses_tc(p0.total_T, D, p0.dtype);
     // 1. states at the chunk starts (the forward, no outputs)
     Problem f{};
     f.q = p.q; f.k = p.k; f.v = p.v; f.alpha = p.alpha; f.eta = p.eta; f.eps = p.eps;
-    f.S0 = p.S0; f.o = nullptr; f.S_T = nullptr; f.cu_seqlens = nullptr;
-    f.n_seq = p.B; f.T = p.T; f.total_T = p.B * p.T; f.H = p.H; f.d = D; f.dtype = p.dtype;
-    f.beta_mode = p.beta_mode; f.S_chk = S_chk; f.status = p.status;
-    cudaError_t e;
+    f.S0 = p.S0; f.o = nullptr; f.S_T = nullptr; f.cu_seqlens = p.cu_seqlens;
+    f.n_seq = p.n_seq; f.T = varlen ? 0 : p.T; f.total_T = p.total_T; f.H = p.H; f.d = D;
+    f.dtype = p.dtype; f.beta_mode = p.beta_mode; f.S_chk = S_chk; f.status = p.status;
+    f.chunk_prefix = p.chunk_prefix;
     float *g_ws = nullptr;
     void *W_ws = nullptr, *A_ws = nullptr;
     if (tc) {
-        const long nchunks = (long)p.B * nch;
-        f.ws = dS_chk + (size_t)units * nch * D * D;
-        f.ws_bytes = chunk_tc_workspace_bytes(nchunks, p.H, p.B);
-        chunk_tc_ws_views(f.ws, nchunks, p.H, p.B, &g_ws, &W_ws, &A_ws);
+        f.ws = ws + L.tc;
+        f.ws_bytes = L.total - L.tc;
+        chunk_tc_ws_views(f.ws, nchunks, p.H, p.n_seq, &g_ws, &W_ws, &A_ws);
         e = launch_chunk_tc(f, nchunks, s);
     } else {
         e = launch_chunk_simt(f, s);
@@ -1108,29 +1234,28 @@ cudaError_t launch_bwd_t(const BwdProblem &p, cudaStream_t s) {
     }
     if (tc)
         bwd_dstate_tc_kernel<<<dim3(units, D / DVB), NT, sizeof(DsTcSmem), s>>>(
-            p, nch, dS_chk, g_ws, static_cast<const __nv_bfloat16 *>(W_ws),
+            p, dS_chk, g_ws, static_cast<const __nv_bfloat16 *>(W_ws),
             static_cast<const __nv_bfloat16 *>(A_ws));
     else
-        bwd_dstate_kernel<Tin, D><<<dim3(units, D / DVB), NT, sizeof(DsSmem<D>), s>>>(p, nch, dS_chk);
+        bwd_dstate_kernel<Tin, D><<<dim3(units, D / DVB), NT, sizeof(DsSmem<D>), s>>>(p, dS_chk);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // 3. token gradients
-    bwd_grads_kernel<Tin, D><<<dim3(nch, units), NT, sizeof(GrSmem<D>), s>>>(p, nch, S_chk, dS_chk);
+    // 3. token gradients, one CTA per chunk slot
+    bwd_grads_kernel<Tin, D><<<dim3((unsigned)nchunks, p.H), NT, sizeof(GrSmem<D>), s>>>(
+        p, nch_fixed, S_chk, dS_chk);
     note_launch();
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t chunk_bwd_workspace_bytes(int B, int T, int H, int d, int dtype) {
-    const size_t nch = (size_t)(T + C - 1) / C;
-    const size_t states = 2 * (size_t)B * H * nch * d * d * sizeof(float);
-    if (!bwd_uses_tc(B, T, d, dtype)) return states;
-    return states + chunk_tc_workspace_bytes((long)B * nch, H, B);
+size_t chunk_bwd_workspace_bytes(bool varlen, int n_seq, int T, int total_T, int H, int d,
+                                 int dtype) {
+    return bwd_layout(varlen, n_seq, T, total_T, H, d, dtype).total;
 }
 
 cudaError_t launch_chunk_bwd(const BwdProblem &p, cudaStream_t s) {
-    if (p.B == 0 || p.T == 0) return cudaSuccess;
+    if (p.n_seq == 0 || p.total_T == 0) return cudaSuccess;
     if (p.dtype == 1)
         return p.d == 128 ? launch_bwd_t<__nv_bfloat16, 128>(p, s)
                           : launch_bwd_t<__nv_bfloat16, 64>(p, s);

@@ -90,12 +90,15 @@ __global__ void __launch_bounds__(NT, 1) chunk_simt_kernel(Problem p) {
         sm.S[i][j] = p.S0 ? p.S0[sbase + (size_t)i * D + jb + j] : 0.f;
     }
 
-    const long nch = (len + C - 1) / C;
+    // first chunk of this sequence in the chunk-slot numbering of the
+    // recorded states (slot = chunk * H + head)
+    const long chunk0 =
+        p.cu_seqlens ? (p.chunk_prefix ? p.chunk_prefix[seq] : 0) : (long)seq * ((p.T + C - 1) / C);
     for (long c0 = 0; c0 < len; c0 += C) {
         const int nc = (int)min((long)C, len - c0);
         __syncthreads();  // previous chunk finished with K, Q, V, S
         if (p.S_chk) {    // the state at the chunk's start, for the backward pass
-            float *dst = p.S_chk + (((size_t)seq * H + h) * nch + c0 / C) * D * D;
+            float *dst = p.S_chk + ((size_t)(chunk0 + c0 / C) * H + h) * D * D;
             for (int x = tid; x < D * DVB; x += NT) {
                 const int i = x / DVB, j = x % DVB;
                 dst[(size_t)i * D + jb + j] = sm.S[i][j];

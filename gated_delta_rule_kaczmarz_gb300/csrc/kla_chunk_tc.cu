@@ -82,8 +82,9 @@ struct TcParams {
     __nv_bfloat16 *o_phi;
     float *S_T_phi;
     // Recording for the backward pass (two-launch path only): the state at
-    // every chunk start ([units][nch][128][128] fp32) and T of every chunk
-    // slot ([slots][64][64] bf16); o may then be null.
+    // every chunk start ([chunk slots][128][128] fp32, slot = chunk * H +
+    // head) and T of every chunk slot ([slots][64][64] bf16); o may then be
+    // null.
     float *S_chk;
     __nv_bfloat16 *T_chk;
     unsigned *flags;           // fused launch: one ready flag per work item, then the work-item
@@ -1029,8 +1030,8 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             }
             tc_fence_after();
             if (!kFused && p.S_chk) {   // S at the chunk's start, for the backward
-                float4 *dst = reinterpret_cast<float4 *>(p.S_chk + sbase * nch + (size_t)c * D * D +
-                                                         (size_t)L * D + j0 + c0);
+                float4 *dst = reinterpret_cast<float4 *>(
+                    p.S_chk + ((size_t)(chunk0 + c) * p.H + h) * D * D + (size_t)L * D + j0 + c0);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     dst[i] = make_float4(Sr[4 * i], Sr[4 * i + 1], Sr[4 * i + 2], Sr[4 * i + 3]);

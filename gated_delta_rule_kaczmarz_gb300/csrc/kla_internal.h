@@ -39,8 +39,9 @@ struct Problem {
     int mode;                // 0: KLA; 1: the CCQ product y = M_t q (tensor-core path only)
     float *csum;             // mode 1: [chunk slots][d] per-chunk key sums (fixed length:
                              // slot (b * n_chunks + c) * H + h)
-    float *S_chk;            // the state at every chunk start ([n_seq, H, n_chunks, d, d]
-                             // fp32) for the backward pass, or nullptr
+    float *S_chk;            // the state at every chunk start for the backward pass
+                             // ([chunk slots, d, d] fp32, slot = chunk * H + head), or nullptr
+    const int *chunk_prefix; // CUDA-core varlen recording: first chunk of each sequence
     void *T_chk;             // tensor-core path with S_chk: T of every chunk slot
                              // ([slots, 64, 64] bf16), or nullptr
     unsigned *status;        // device status word, or nullptr
@@ -79,18 +80,25 @@ cudaError_t launch_ccq_step(const void *q, const void *k, const float *lambda, f
                             float *ms, float *ns, void *q_clean, int BH, int d, int dtype,
                             cudaStream_t s);
 
-// Backward of the fixed-length chunkwise forward (kla_chunk_bwd.cu).
+// Backward of the chunkwise forward (kla_chunk_bwd.cu), fixed length or varlen.
 struct BwdProblem {
     const void *q, *k, *v, *dout;
     const float *alpha, *eta, *S0, *dS_T;
     float eps;
     void *dq, *dk, *dv;
     float *dalpha, *deta, *dS0;
-    int B, T, H, d, dtype, beta_mode;
+    int n_seq;               // B (fixed) or N (varlen)
+    int T;                   // fixed length (unused for varlen)
+    int total_T;             // token rows
+    const int *cu_seqlens;   // device, varlen only
+    int H, d, dtype, beta_mode;
     unsigned *status;
-    void *ws;                // chunk_bwd_workspace_bytes(B, T, H, d, dtype) after the header
+    void *ws;                // chunk_bwd_workspace_bytes(...) after the header
+    // set by the launcher: the chunk tables (varlen)
+    const int *chunk_prefix, *chunk_seq;
 };
-size_t chunk_bwd_workspace_bytes(int B, int T, int H, int d, int dtype);
+size_t chunk_bwd_workspace_bytes(bool varlen, int n_seq, int T, int total_T, int H, int d,
+                                 int dtype);
 cudaError_t launch_chunk_bwd(const BwdProblem &p, cudaStream_t s);
 
 // Tensor-core (tcgen05) prefill for bf16, d = 128.

@@ -263,6 +263,20 @@ KLA_API int kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
  * gradients).  Asynchronous on `stream`.
  */
 KLA_API size_t kla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dtype);
+
+/* Backward of kla_chunk_fwd_varlen_ex: packed q, k, v, d_o, dq, dk, dv
+ * [total_T, H, *], alpha, eta, dalpha, deta [total_T, H], cu_seqlens int32
+ * device [N + 1] (validated on the device: a bad table is reported by
+ * kla_workspace_status as KLA_ERR_INVALID_ARG and no gradient is written),
+ * S0, dS_T, dS0 [N, H, dk, dv]; otherwise as kla_chunk_bwd. */
+KLA_API size_t kla_chunk_bwd_varlen_workspace_size(int N, int total_T, int H, int dk, int dtype);
+KLA_API int kla_chunk_bwd_varlen(const void *q, const void *k, const void *v, const float *alpha,
+                                 const float *eta, float eps, const float *S0, const void *d_o,
+                                 const float *dS_T, void *dq, void *dk, void *dv, float *dalpha,
+                                 float *deta, float *dS0, const int *cu_seqlens, int N,
+                                 int total_T, int H, int dk_, int dv_, int chunk, int dtype,
+                                 int beta_mode, void *workspace, size_t workspace_bytes,
+                                 void *stream);
 KLA_API int kla_chunk_bwd(const void *q, const void *k, const void *v, const float *alpha,
                           const float *eta, float eps, const float *S0, const void *d_o,
                           const float *dS_T, void *dq, void *dk, void *dv, float *dalpha,

@@ -118,3 +118,59 @@ def test_backward_cuda_core_launches():
     kla.kla_chunk_bwd(*args)
     torch.cuda.synchronize()
     assert kla.kla_launch_count() - n0 == 3
+
+
+def _varlen_oracle_backward(inp, do, dST, mode="kaczmarz"):
+    """The backward oracle run sequence by sequence on the packed inputs."""
+    cu = inp["cu_seqlens"].tolist()
+    N = len(cu) - 1
+    outs = [np.zeros(inp["q"].shape), np.zeros(inp["k"].shape), np.zeros(inp["v"].shape),
+            np.zeros(inp["alpha"].shape), np.zeros(inp["eta"].shape),
+            np.zeros(inp["S0"].shape if inp["S0"] is not None else dST.shape)]
+    for n in range(N):
+        a, b = cu[n], cu[n + 1]
+        sl = lambda x: x[None, a:b]
+        S0 = None if inp["S0"] is None else inp["S0"][n:n + 1]
+        g = oracle.backward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["alpha"]),
+                            sl(inp["eta"]), inp["eps"], S0, sl(do), dST[n:n + 1], beta_mode=mode)
+        for i in range(5):
+            outs[i][a:b] = g[i][0]
+        outs[5][n] = g[5][0]
+    return outs
+
+
+@pytest.mark.parametrize("d,dtype,mode", [(128, "bf16", "kaczmarz"), (64, "fp32", "kaczmarz"),
+                                          (128, "bf16", "given")])
+def test_varlen_backward_parity(d, dtype, mode):
+    """Packed sequences (an empty one, shorter than a chunk, exact multiples,
+    ragged) against the oracle per sequence."""
+    from gated_delta_rule_kaczmarz_gb300.workloads import varlen_inputs
+    lens = [70, 0, 5, 128, 191, 64]
+    inp = varlen_inputs(lens, 2, d, d, dtype, seed=60 + d, s0_var=0.01)
+    rng = np.random.default_rng(61)
+    total = sum(lens)
+    t = torch.bfloat16 if dtype == "bf16" else torch.float32
+    do = torch.from_numpy(rng.standard_normal((total, 2, d)).astype(np.float32)).to(t)
+    dST = torch.from_numpy((0.1 * rng.standard_normal((len(lens), 2, d, d))).astype(np.float32))
+    g = cuda(dict(inp, do=do, dST=dST))
+    got = kla.kla_chunk_bwd_varlen(g["q"], g["k"], g["v"], g["alpha"], g["eta"], inp["eps"],
+                                   g["cu_seqlens"], g["S0"], g["do"], g["dST"], beta_mode=mode)
+    torch.cuda.synchronize()
+    ref = _varlen_oracle_backward(inp, do, dST, mode)
+    _check(got, ref, TOL[t])
+
+
+def test_varlen_backward_bad_seqlens_reported():
+    """A decreasing cu_seqlens is caught on the device; the status word says so."""
+    from gated_delta_rule_kaczmarz_gb300.workloads import varlen_inputs
+    inp = varlen_inputs([64, 64], 2, 128, 128, "bf16", seed=62)
+    g = cuda(inp)
+    cu = torch.tensor([0, 100, 64], dtype=torch.int32, device="cuda")   # not non-decreasing
+    do = torch.zeros_like(g["v"])
+    ws = torch.zeros(kla.kla_chunk_bwd_varlen_workspace_size(2, 128, 2, 128, 1),
+                     dtype=torch.uint8, device="cuda")
+    kla.kla_chunk_bwd_varlen(g["q"], g["k"], g["v"], g["alpha"], g["eta"], inp["eps"], cu, None,
+                             do, workspace=ws)
+    with pytest.raises(kla.KlaError) as ei:
+        kla.kla_workspace_status(ws)
+    assert ei.value.status == kla.binding.KLA_ERR_INVALID_ARG
