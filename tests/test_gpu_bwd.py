@@ -174,3 +174,20 @@ def test_varlen_backward_bad_seqlens_reported():
     with pytest.raises(kla.KlaError) as ei:
         kla.kla_workspace_status(ws)
     assert ei.value.status == kla.binding.KLA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("B,T,H,d,dtype", [
+    (1, 64, 1, 128, "bf16"),    # exactly one chunk, tensor-core states
+    (1, 65, 1, 128, "bf16"),    # one row into the second chunk
+    (3, 20, 1, 128, "bf16"),    # B*T < 64: CUDA-core states for bf16 d 128
+    (2, 127, 3, 64, "bf16")])   # d 64 bf16
+def test_backward_edge_shapes(B, T, H, d, dtype):
+    inp = prefill_inputs(B, T, H, d, d, dtype, seed=700 + T, s0_var=0.01)
+    do, dST = _grad_inputs(B, T, H, d, dtype, 701 + T)
+    g = cuda(dict(inp, do=do, dST=dST))
+    got = kla.kla_chunk_bwd(g["q"], g["k"], g["v"], g["alpha"], g["eta"], inp["eps"], g["S0"],
+                            g["do"], g["dST"])
+    torch.cuda.synchronize()
+    ref = oracle.backward(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["eta"], inp["eps"],
+                          inp["S0"], do, dST)
+    _check(got, ref, TOL[inp["q"].dtype])

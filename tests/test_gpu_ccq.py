@@ -129,3 +129,22 @@ def test_ccq_full_size_sampled():
         assert rel_err(Ms[b:b + 1, h:h + 1], M_ref) <= 1e-5
         assert rel_err(ms[b:b + 1, h:h + 1], m_ref) <= 1e-5
         assert float(ns[b, h]) == float(n_ref.reshape(-1)[0])
+
+
+def test_ccq_stats_carry_on_tensor_cores():
+    """Two tensor-core calls with the statistics carried equal one call over
+    the concatenation (bf16 d 128)."""
+    B, H, d = 2, 2, 128
+    inp = prefill_inputs(B, 512, H, d, d, "bf16", seed=170)
+    lam = _lam((B, 512, H), 14).cuda()
+    g = cuda(inp)
+    qc, st = kla.kla_ccq_query(g["q"], g["k"], lam)
+    qa, sa = kla.kla_ccq_query(g["q"][:, :256].contiguous(), g["k"][:, :256].contiguous(),
+                               lam[:, :256].contiguous())
+    qb, sb = kla.kla_ccq_query(g["q"][:, 256:].contiguous(), g["k"][:, 256:].contiguous(),
+                               lam[:, 256:].contiguous(), sa)
+    torch.cuda.synchronize()
+    ref = qc.double().cpu().numpy()
+    assert rel_err(torch.cat([qa, qb], 1), ref) <= 2e-2
+    for x, y in zip(sb, st):
+        assert rel_err(x, y.double().cpu().numpy()) <= 1e-5
