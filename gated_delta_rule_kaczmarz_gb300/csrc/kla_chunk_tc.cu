@@ -258,18 +258,29 @@ constexpr uint32_t P1_SMALL = 3 * 32768 + 8192;
 constexpr uint32_t P1_REGION = 109568;
 static_assert(P1_SMALL + 64 + 4 * 512 <= P1_REGION, "phase-1 region");
 constexpr uint32_t P1_SMEM = P1_REGION + 1024;   // + alignment slack
+// Longest wait of a follower worker for its leader's signal (a timing hint
+// only: past it the follower starts anyway).
+constexpr long long kStaggerLimitCycles = 40000;
 
 // Phase-1 worker: 256 threads (tid0 = 0..255) with named barrier `bar` over
 // them, shared memory `sm` (1024-aligned, P1_REGION bytes), work items
 // item0, item0 + step, ...  kFused: items run chunk-pair-major over all
 // (sequence, head) units, and each finished item is published through
 // p.flags for the state pass running in the same launch.
+//
+// `stagger` (optional, shared by the two workers of one CTA) offsets them:
+// the leader (stagger_role 1) raises it halfway through its first item, and
+// the follower (stagger_role 2) starts its first item only then (or after a
+// bounded wait).  Two workers that start together wait for their loads
+// together and then compete for the same pipes through every step of the
+// item; offset by half an item, one computes while the other loads.
 template <bool kFused>
 __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorMap *mk,
                                           const CUtensorMap *mv, const CUtensorMap *mw,
                                           const CUtensorMap *mu, const TcParams &p, long n_pairs,
                                           unsigned char *sm, int tid0, int bar, long item0,
-                                          long step) {
+                                          long step, volatile int *stagger = nullptr,
+                                          int stagger_role = 0) {
     // KQ: two 64-feature slabs of 32 KB, each [K rows 0..127 | Q rows 0..127]
     // (128-byte rows, 128-byte swizzle), so that [K; Q] is one N = 256
     // operand.  After the Gram products the Q half of slab p holds chunk p's
@@ -310,6 +321,14 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     const long n_items = n_pairs * p.H;
     uint32_t ph = 0;      // mbarrier phase parity of this worker's current item
     long pending = -1;    // fused: item written but not yet published (thread 0)
+    bool first = true;    // this worker's first item
+    if (stagger && stagger_role == 2) {
+        if (tid0 == 0) {
+            const long long t0 = clock64();
+            while (*stagger == 0 && clock64() - t0 < kStaggerLimitCycles) __nanosleep(64);
+        }
+        named_sync(bar, P1_THREADS);
+    }
     // Work items: item0, item0 + step, ...; or, with step == 0, items item0 +
     // (a global counter's next value), handed out in order as workers free up
     // (the fused launch: a late item then delays only its own unit).
@@ -544,6 +563,8 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     if (!ok) *sAbort = 1;
     named_sync(bar, P1_THREADS);
     const bool abort2 = *sAbort != 0;
+    if (first && stagger && stagger_role == 1 && tid == 0) *stagger = 1;
+    first = false;
 
     if (p.mode == 1) {
         // ---- the CCQ product y_t = M_t q_t: with W = 0, U~ = K, g = 0 and
@@ -739,6 +760,7 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     ph ^= 1u;
     if (*sAbort) break;
     }  // items
+    if (stagger && stagger_role == 1 && tid0 == 0) *stagger = 1;   // a leader with no item
     if (tid0 == 0) {
         bulk_wait_group0();   // every TMA store complete before the worker leaves
         if (kFused && pending >= 0) {
@@ -1024,11 +1046,10 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             const int b = c % NSTAGE;
             unsigned char *st = sm + b * ST_BYTES;
             const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NSTAGE) & 1);
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_px, par))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_ld[b], par_st))) {
                 fail();
                 break;
             }
-            tc_fence_after();
             if (!kFused && p.S_chk) {   // S at the chunk's start, for the backward
                 float4 *dst = reinterpret_cast<float4 *>(
                     p.S_chk + ((size_t)(chunk0 + c) * p.H + h) * D * D + (size_t)L * D + j0 + c0);
@@ -1036,24 +1057,41 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 for (int i = 0; i < 8; ++i)
                     dst[i] = make_float4(Sr[4 * i], Sr[4 * i + 1], Sr[4 * i + 2], Sr[4 * i + 3]);
             }
+            // what the stage alone gives (g, the decay factors, the U~ words) is
+            // read before the wait for the product
             const float *g = sG + b * C;
             const float gC = g[C - 1];
             const float egC = __expf(gC);
             const int nc = (int)min((long)C, len - (long)c * C);
-            float egt = 0.f;
+            float egt = 0.f, ft = 0.f;
+            uint4 wu[4];
+            if (pwarp) {
+                const int t = L - 64;
+                ft = __expf(gC - g[t]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    wu[k] = *reinterpret_cast<const uint4 *>(st + ST_U + sw128_offset(t, c0 + 8 * k));
+                    if (phi) wu[k] = make_uint4(0u, 0u, 0u, 0u);   // U~ = 0 in a transition pass
+                }
+            } else {
+                egt = __expf(g[L]);
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_px, par))) {
+                fail();
+                break;
+            }
+            tc_fence_after();
             if (pwarp) {
                 // ---- U = U~_b - P and U' = exp(g_C - g_t) U for token t = L - 64,
                 //      columns [c0, c0 + 32) ----
                 const int t = L - 64;
-                const float ft = __expf(gC - g[t]);
                 uint32_t r[32];
                 tmem_ld32(tb + lane_base + TM_PX + 64 * (c & 1) + c0, r);
                 tmem_ld_wait();
                 float u[32], uz[32];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    uint4 w = *reinterpret_cast<const uint4 *>(st + ST_U + sw128_offset(t, c0 + 8 * k));
-                    if (phi) w = make_uint4(0u, 0u, 0u, 0u);   // U~ = 0 in a transition pass
+                    const uint4 w = wu[k];
                     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -1084,7 +1122,6 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 // every read of this stage by the main warps precedes their
                 // bar_u arrival, which precedes the products whose completion
                 // frees the stage for the next load
-                egt = __expf(g[L]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_u);
             }
@@ -1197,9 +1234,12 @@ fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             state_run<true, kSplit>(&mq, &mk, &mw, &mu, &ma, p, sm, (int)blockIdx.x, tid);
         return;
     }
+    __shared__ int stagger;
+    if (tid == 0) stagger = 0;
+    __syncthreads();
     const int w = tid / P1_THREADS;
     intra_run<true>(&mq, &mk, &mv, &mw, &mu, p, n_pairs, sm + w * P1_REGION, tid % P1_THREADS,
-                    1 + w, (long)pre * p.n_units, 0);   // items from the shared counter
+                    1 + w, (long)pre * p.n_units, 0, &stagger, 1 + w);   // items from the shared counter
 }
 
 // ===================================================================== varlen prep
