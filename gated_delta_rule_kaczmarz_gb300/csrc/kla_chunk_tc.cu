@@ -188,7 +188,7 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, i
     // M = L21 D1
 #pragma unroll
     for (int m = 0; m < rows; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
-#pragma unroll 2
+#pragma unroll 1
     for (int s4 = 0; s4 < n / 4; ++s4) {
         float4 bb[4];
 #pragma unroll
@@ -218,7 +218,7 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, i
     }
     named_sync(bar, P1_THREADS);  // M complete; L21 no longer read
     // X = -D2 M, written over L21
-#pragma unroll 2
+#pragma unroll 1
     for (int s4 = 0; s4 < n / 4; ++s4) {
         float4 bb[4];
 #pragma unroll
@@ -373,9 +373,9 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     if (tid == 0) {
         bulk_wait_group_read0();   // the previous item's W / U~ stores have left shared memory
         mbar_expect_tx(&bars[0], 3u * 32768u);
-#pragma unroll
+#pragma unroll 1
         for (int q = 0; q < 2; ++q)
-#pragma unroll
+#pragma unroll 1
             for (int s = 0; s < 2; ++s) {
                 const int z = (int)(q ? r01 : r00);
                 tma_load_3d(KQ + s * 32768 + q * 8192, mk, &bars[0], 64 * s, h, z);
@@ -429,7 +429,7 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
         // [K K^T | K Q^T]: A = K (128 tokens), B = [K; Q] (256 rows), K = 128 features
         const uint32_t idesc = idesc_bf16_f32(128, 256, false, false);
         const uint32_t aKQ = smem_u32(KQ);
-#pragma unroll
+#pragma unroll 1
         for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * 32768 + (ks & 3) * 32;
             mma_bf16(tb + 0, sdesc_sw128(aKQ + off, 16, 1024), sdesc_sw128(aKQ + off, 16, 1024),
@@ -441,7 +441,7 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     // ---- beta_t from the key's squared norm (fp32 over the bf16 values);
     //      each thread half sums one 64-feature slab ----
     float n2 = 0.f;
-#pragma unroll
+#pragma unroll 2
     for (int ch = 0; ch < 8; ++ch) {
         const uint4 v = *reinterpret_cast<const uint4 *>(KQ + hf * 32768 + sw128_offset(r, ch * 8));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -542,7 +542,7 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
         // products.
         const bool live = t < nc;
         const float gam_t = live ? ex2_approx(gt2) : 0.f;
-#pragma unroll 2
+#pragma unroll 1
         for (int ch = 0; ch < 8; ++ch) {
             uint4 *pk4 = reinterpret_cast<uint4 *>(KQ + hf * 32768 + sw128_offset(r, ch * 8));
             const uint4 v = *pk4;
@@ -554,7 +554,7 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
             *pk4 = w;
         }
         if (!live) {
-#pragma unroll
+#pragma unroll 1
             for (int ch = 0; ch < 8; ++ch)
                 *reinterpret_cast<uint4 *>(sV + hf * 16384 + sw128_offset(r, ch * 8)) =
                     make_uint4(0u, 0u, 0u, 0u);
@@ -699,12 +699,12 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
         // A slabs (one per chunk's columns) at 32 KB; B = diag(exp g) K MN-major
         // (rows = tokens), its two 64-feature n-blocks 32 KB apart.
         const uint32_t id_w = idesc_bf16_f32(128, 128, false, true);
-#pragma unroll
+#pragma unroll 1
         for (int ks = 0; ks < 8; ++ks)
             mma_bf16(tb + 0, sdesc_sw128(aA + (ks >> 2) * 32768 + (ks & 3) * 32, 16, 1024),
                      sdesc_sw128(aK + ks * 2048, 32768, 1024), id_w, ks > 0);
         // U~ = (T diag beta) V: the same A; B = V MN-major, n-blocks 16 KB apart.
-#pragma unroll
+#pragma unroll 1
         for (int ks = 0; ks < 8; ++ks)
             mma_bf16(tb + 128, sdesc_sw128(aA + (ks >> 2) * 32768 + (ks & 3) * 32, 16, 1024),
                      sdesc_sw128(aV + ks * 2048, 16384, 1024), id_w, ks > 0);
@@ -742,11 +742,11 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     fence_async_smem();
     named_sync(bar, P1_THREADS);
     if (tid == 0 && ok) {
-#pragma unroll
+#pragma unroll 1
         for (int q = 0; q < 2; ++q) {
             if (!(q ? v1 : v0)) continue;
             const int y = (int)(((2L * pair + q) * p.H + h) * C);
-#pragma unroll
+#pragma unroll 1
             for (int s = 0; s < 2; ++s) {
                 tma_store_2d(mw, KQ + s * 32768 + q * 8192, 64 * s, y);
                 tma_store_2d(mu, sV + s * 16384 + q * 8192, 64 * s, y);
