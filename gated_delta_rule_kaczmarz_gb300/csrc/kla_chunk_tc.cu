@@ -298,14 +298,14 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     float *sBeta = sG2 + 128;
     float *sN2 = sBeta + 128;
 
-    if (status_bad(p.status)) return;
-
     if (tid0 == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
         mbar_init(&bars[2], 1);
         fence_mbar_init();
-        *sAbort = 0;
+        // an error already reported: read once, so that all the worker's
+        // threads agree (threads reading the word at different times might not)
+        *sAbort = status_bad(p.status) ? 1 : 0;
     }
     if ((tid0 >> 5) == 0) {
         tmem_alloc(tslot, 256);
@@ -315,6 +315,10 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     }
     named_sync(bar, P1_THREADS);
     tc_fence_after();
+    if (*sAbort) {
+        if ((tid0 >> 5) == 0) tmem_dealloc(*tslot, 256);
+        return;
+    }
 
     // Persistent: work items are (pair of chunks, head), head fastest, so that
     // CTAs running side by side read the same token rows of different heads.
@@ -872,7 +876,6 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
     const int c0 = 32 * hf;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    if (status_bad(p.status)) return;
     // transition-pass CTAs: two per (batch, segment >= 1, head), in that order
     const bool phi = kSplit && p.phi_first > 0 && bid >= p.phi_first;
     const int segP = kSplit ? p.seg_P : 1;
@@ -913,7 +916,9 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         mbar_init(&bar_s, 8);      // one arrival per main warp
         mbar_init(&bar_fin, 1);
         fence_mbar_init();
-        sAbort = 0;
+        // an error already reported: read once, so that the whole CTA
+        // agrees (threads reading the word at different times might not)
+        sAbort = status_bad(p.status) ? 1 : 0;
     }
     if (warp == 0) {
         tmem_alloc(&tslot, 512);
@@ -922,6 +927,10 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
     named_sync(3, P2_THREADS);
     tc_fence_after();
     const uint32_t tb = tslot;
+    if (sAbort) {
+        if (warp == 0) tmem_dealloc(tb, 512);
+        return;
+    }
 
     auto fail = [&]() {
         sAbort = 1;
