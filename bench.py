@@ -40,7 +40,7 @@ METRIC = "KLA chunkwise prefill tokens/s & % roofline; decode steps/s at B=256"
 # captures summarised in profiles/ (fused_kernel_layer_prefill.md,
 # decode_kernel_b128.md, ccq_layer_prefill.md).
 TRAFFIC_PREFILL = 68.21e6
-TRAFFIC_CCQ = 46.1e6 + 51.6e6
+TRAFFIC_CCQ = 48.5e6 + 51.6e6
 TRAFFIC_DECODE = 2 * (135.83e6 + 74.59e6)
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 BYTES_PER_TOKEN_HEAD = 1032          # q,k,v,o bf16 (4 x 256 B) + alpha, eta fp32 (8 B)
