@@ -823,12 +823,42 @@ constexpr uint32_t P2_SMEM = SM_G + NSTAGE * 256 + 1024;
 // Y in two buffers (chunk c uses buffer c % 2).
 constexpr uint32_t TM_PX = 0, TM_Z = 128, TM_Y = 192;
 
+// The same pass with kW dv columns per CTA: kW = 64 (above: two CTAs per
+// head, the shorter chain) or kW = 128 (one CTA per head: every product has
+// N = 128 for the same MMA count, the element-wise steps take twice as long,
+// and half as many CTAs carry the whole state; used where more CTAs than SMs
+// would run).  The wide pass has two stages (the stage holds all 128 columns
+// of U~) and one Y buffer (TMEM: [X | P] 2 x 128, Z 128, Y 128 columns).
+template <int kW>
+struct P2Cfg {
+    static constexpr int NST = kW == 64 ? 3 : 2;
+    static constexpr int NJ = kW / 64;                 // 32-column groups per main thread
+    static constexpr uint32_t U_BYTES = 64u * kW * 2u;   // U~ of a stage (64-column slabs)
+    static constexpr uint32_t ST_BYTES = ST_U + U_BYTES;
+    static constexpr uint32_t ST_TX = 32768u + 16384u + 8192u + U_BYTES + 256u;
+    static constexpr uint32_t S_SLAB = 128u * 64u * 2u;  // one 64-column slab of S_b
+    static constexpr uint32_t U_SLAB = 64u * 64u * 2u;   // one 64-column slab of U, U'
+    static constexpr uint32_t SM_S = NST * ST_BYTES, SM_U = SM_S + NJ * S_SLAB,
+                              SM_UZ = SM_U + NJ * U_SLAB, SM_G = SM_UZ + NJ * U_SLAB;
+    static constexpr uint32_t SMEM = SM_G + NST * 256 + 1024;
+    static constexpr uint32_t TM_PX = 0, TM_Z = 2 * kW, TM_Y = 3 * kW;
+    static constexpr uint32_t Y_STRIDE = kW == 64 ? 64 : 0;   // column offset of Y buffer 1
+};
+static_assert(P2Cfg<64>::NST == NSTAGE && P2Cfg<64>::ST_BYTES == ST_BYTES &&
+                  P2Cfg<64>::ST_TX == ST_TX && P2Cfg<64>::SM_S == SM_S &&
+                  P2Cfg<64>::SM_U == SM_U && P2Cfg<64>::SM_UZ == SM_UZ &&
+                  P2Cfg<64>::SM_G == SM_G && P2Cfg<64>::SMEM == P2_SMEM &&
+                  P2Cfg<64>::TM_Z == TM_Z && P2Cfg<64>::TM_Y == TM_Y,
+              "narrow state pass layout");
+static_assert(P2Cfg<128>::SMEM <= 232448 && P2Cfg<128>::TM_Y + 128 <= 512, "wide state pass");
+
+template <int kW>
 __device__ __forceinline__ void issue_stage(unsigned char *st, float *g_dst, uint64_t *bar,
                                             const CUtensorMap *mq, const CUtensorMap *mk,
                                             const CUtensorMap *mw, const CUtensorMap *mu,
                                             const CUtensorMap *ma, const float *g_src, int h,
                                             int row0, int slot, int j0) {
-    mbar_expect_tx(bar, ST_TX);
+    mbar_expect_tx(bar, P2Cfg<kW>::ST_TX);
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
         tma_load_3d(st + ST_QW + s * 16384, mq, bar, 64 * s, h, row0);
@@ -836,7 +866,9 @@ __device__ __forceinline__ void issue_stage(unsigned char *st, float *g_dst, uin
         tma_load_3d(st + ST_KT + s * 8192, mk, bar, 64 * s, h, row0);
     }
     tma_load_2d(st + ST_A, ma, bar, 0, slot * C);
-    tma_load_2d(st + ST_U, mu, bar, j0, slot * C);
+#pragma unroll
+    for (int s = 0; s < kW / 64; ++s)
+        tma_load_2d(st + ST_U + s * P2Cfg<kW>::U_SLAB, mu, bar, j0 + 64 * s, slot * C);
     bulk_load(g_dst, g_src, 256, bar);
 }
 
@@ -851,29 +883,33 @@ __device__ __forceinline__ void st_row_bf16x32(unsigned char *tile, int row, int
                        pack_bf2(x[8 * k + 4], x[8 * k + 5]), pack_bf2(x[8 * k + 6], x[8 * k + 7]));
 }
 
-// State pass of CTA `bid` (unit bid / 2, column half bid % 2) with threads
-// tid = 0 .. P2_THREADS-1 and shared memory `sm` (1024-aligned, P2_SMEM - 1024
-// bytes).  kFused: phase 1 runs in the same launch, and the load of chunk c
-// waits for the ready flag of the work item that holds it.
-template <bool kFused, bool kSplit>
+// State pass of CTA `bid` (kW = 64: unit bid / 2, column half bid % 2; kW =
+// 128: unit bid) with threads tid = 0 .. P2_THREADS-1 and shared memory `sm`
+// (1024-aligned, P2Cfg<kW>::SMEM - 1024 bytes).  kFused: phase 1 runs in the
+// same launch, and the load of chunk c waits for the ready flag of the work
+// item that holds it.
+template <bool kFused, bool kSplit, int kW = 64>
 __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorMap *mk,
                                           const CUtensorMap *mw, const CUtensorMap *mu,
                                           const CUtensorMap *ma, const TcParams &p,
                                           unsigned char *sm, int bid, int tid) {
-    __shared__ uint64_t bar_ld[NSTAGE];
-    __shared__ uint64_t bar_empty[NSTAGE];   // the products of a stage's chunk are done
+    using Cf = P2Cfg<kW>;
+    constexpr int NS = Cf::NST, NJ = Cf::NJ;
+    static_assert(!kSplit || kW == 64, "the transition passes use the narrow layout");
+    __shared__ uint64_t bar_ld[NS];
+    __shared__ uint64_t bar_empty[NS];   // the products of a stage's chunk are done
     __shared__ uint64_t bar_px, bar_u, bar_z, bar_s, bar_fin;
     __shared__ uint64_t bar_y[2];   // Y of chunk c completes on bar_y[c % 2]
     __shared__ uint32_t tslot;
     __shared__ int sAbort;
 
-    unsigned char *sS = sm + SM_S, *sU = sm + SM_U, *sUz = sm + SM_UZ;
-    float *sG = reinterpret_cast<float *>(sm + SM_G);
+    unsigned char *sS = sm + Cf::SM_S, *sU = sm + Cf::SM_U, *sUz = sm + Cf::SM_UZ;
+    float *sG = reinterpret_cast<float *>(sm + Cf::SM_G);
 
     const int warp = tid >> 5, lane = tid & 31;
     const int L = (warp & 3) * 32 + lane;       // TMEM lane (main warps)
     const int hf = (warp >> 2) & 1;             // column half (main warps)
-    const int c0 = 32 * hf;
+    const int c0 = 32 * NJ * hf;                // first of the thread's 32 NJ columns of the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     // transition-pass CTAs: two per (batch, segment >= 1, head), in that order
@@ -887,7 +923,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         bid = ((seqv * p.H + hh) << 1) | (k & 1);
         phi_base = (size_t)idx * D * D;
     }
-    const int unit = bid >> 1, jh = bid & 1, j0 = DVB * jh;
+    const int unit = kW == 64 ? bid >> 1 : bid, jh = kW == 64 ? (bid & 1) : 0, j0 = 64 * jh;
     const int rank = unit / p.H, h = unit % p.H;
     const int seq = p.order ? p.order[rank] : rank;
     long start, len, chunk0;
@@ -904,7 +940,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
     const size_t sbase = ((size_t)seq * p.H + h) * D * D;
 
     if (tid == 0) {
-        for (int i = 0; i < NSTAGE; ++i) {
+        for (int i = 0; i < NS; ++i) {
             mbar_init(&bar_ld[i], 1);
             mbar_init(&bar_empty[i], 1);
         }
@@ -939,14 +975,14 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
 
     if (warp == 8) {
         // ----------------------------------------------------------------- issuer
-        const uint32_t id_px = idesc_bf16_f32(128, DVB, false, true);
-        const uint32_t id_zy = idesc_bf16_f32(128, DVB, true, true);
+        const uint32_t id_px = idesc_bf16_f32(128, kW, false, true);
+        const uint32_t id_zy = idesc_bf16_f32(128, kW, true, true);
         const uint32_t aS = smem_u32(sS), aU = smem_u32(sU), aUz = smem_u32(sUz);
         int c = 0;
         for (; c < nch; ++c) {
-            const int b = c % NSTAGE;
-            unsigned char *st = sm + b * ST_BYTES;
-            const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NSTAGE) & 1);
+            const int b = c % NS;
+            unsigned char *st = sm + b * Cf::ST_BYTES;
+            const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NS) & 1);
             // stage landed, and S_c written to shared memory by the main warps
             const bool ok = mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_s, par);
             if (!__all_sync(0xffffffffu, ok)) { fail(); break; }
@@ -955,9 +991,10 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 const uint32_t aQW = smem_u32(st + ST_QW);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16(tb + TM_PX + 64 * (c & 1),
+                    mma_bf16(tb + Cf::TM_PX + kW * (c & 1),
                              sdesc_sw128(aQW + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                             sdesc_sw128(aS + ks * 2048, 8192, 1024), id_px, ks > 0);
+                             sdesc_sw128(aS + ks * 2048, kW == 64 ? 8192 : Cf::S_SLAB, 1024),
+                             id_px, ks > 0);
                 mma_commit(&bar_px);
             }
             __syncwarp();
@@ -968,14 +1005,15 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 // Z = K^T U': A = K read MN-major (M = dk, two 64-feature blocks)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tb + TM_Z, sdesc_sw128(aKT + ks * 2048, 8192, 1024),
+                    mma_bf16(tb + Cf::TM_Z, sdesc_sw128(aKT + ks * 2048, 8192, 1024),
                              sdesc_sw128(aUz + ks * 2048, 8192, 1024), id_zy, ks > 0);
                 mma_commit(&bar_z);
                 // Y = A U: A read MN-major from A^T; its second 64-row block
                 // (rows 64..127 of the product, never read) points at U~
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tb + TM_Y + 64 * (c & 1), sdesc_sw128(aA + ks * 2048, 8192, 1024),
+                    mma_bf16(tb + Cf::TM_Y + Cf::Y_STRIDE * (c & 1),
+                             sdesc_sw128(aA + ks * 2048, 8192, 1024),
                              sdesc_sw128(aU + ks * 2048, 8192, 1024), id_zy, ks > 0);
                 mma_commit(&bar_y[c & 1]);
                 mma_commit(&bar_empty[b]);   // the stage may be refilled
@@ -994,7 +1032,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         // n / 2, counted per unit).
         int n = 0;
         for (; n < nch; ++n) {
-            const int b = n % NSTAGE, k = n / NSTAGE;
+            const int b = n % NS, k = n / NS;
             if (k >= 1 &&
                 !__all_sync(0xffffffffu, mbar_wait(&bar_empty[b], (uint32_t)((k - 1) & 1)))) {
                 fail();
@@ -1011,7 +1049,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             if (lane == 0) {
                 if (kFused) fence_proxy_async_global();
                 const long slot = (chunk0 + n) * p.H + h;
-                issue_stage(sm + b * ST_BYTES, sG + b * C, &bar_ld[b], mq, mk, mw, mu, ma,
+                issue_stage<kW>(sm + b * Cf::ST_BYTES, sG + b * C, &bar_ld[b], mq, mk, mw, mu, ma,
                             p.g_ws + slot * C, h, (int)(start + (long)n * C), (int)slot, j0);
             }
             __syncwarp();
@@ -1019,12 +1057,15 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         // on an early exit, the loads still in flight (at most one per stage)
         // land before the CTA leaves
         if (sAbort)
-            for (int k = n > NSTAGE ? n - NSTAGE : 0; k < n; ++k)
-                (void)mbar_wait(&bar_ld[k % NSTAGE], (uint32_t)((k / NSTAGE) & 1));
+            for (int k = n > NS ? n - NS : 0; k < n; ++k)
+                (void)mbar_wait(&bar_ld[k % NS], (uint32_t)((k / NS) & 1));
     } else {
         // ----------------------------------------------------------------- main
+        // Thread (L, hf) holds row L of S_b for the tile columns
+        // [c0, c0 + 32 NJ) in NJ groups of 32 (group jj: columns cg = c0 + 32 jj,
+        // in 64-column slab cg / 64 of the bf16 operands).
         const size_t rs = (size_t)p.H * D;
-        float Sr[32];
+        float Sr[NJ][32];
         {
             // the initial state: S0, zero for a later segment of a split
             // sequence, the identity's columns for a transition pass
@@ -1035,36 +1076,47 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                          : nullptr;
             else if (s0)
                 s0 += sbase;
-            const float4 *src = reinterpret_cast<const float4 *>(s0 + (size_t)L * D + j0 + c0);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 v = s0 ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-                Sr[4 * i] = v.x; Sr[4 * i + 1] = v.y; Sr[4 * i + 2] = v.z; Sr[4 * i + 3] = v.w;
-            }
-            if (phi) {
+            for (int jj = 0; jj < NJ; ++jj) {
+                const int cg = c0 + 32 * jj;
+                const float4 *src = reinterpret_cast<const float4 *>(s0 + (size_t)L * D + j0 + cg);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) Sr[i] = (L == j0 + c0 + i) ? 1.f : 0.f;
+                for (int i = 0; i < 8; ++i) {
+                    const float4 v = s0 ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    Sr[jj][4 * i] = v.x; Sr[jj][4 * i + 1] = v.y;
+                    Sr[jj][4 * i + 2] = v.z; Sr[jj][4 * i + 3] = v.w;
+                }
+                if (phi) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) Sr[jj][i] = (L == j0 + cg + i) ? 1.f : 0.f;
+                }
+                st_row_bf16x32(sS + (cg >> 6) * Cf::S_SLAB, L, cg & 63, Sr[jj]);
             }
-            st_row_bf16x32(sS, L, c0, Sr);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_s);
         }
         const bool pwarp = (warp & 2) != 0;    // lanes 64..127: P rows (tokens L - 64)
         for (int c = 0; c < nch; ++c) {
-            const int b = c % NSTAGE;
-            unsigned char *st = sm + b * ST_BYTES;
-            const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NSTAGE) & 1);
+            const int b = c % NS;
+            unsigned char *st = sm + b * Cf::ST_BYTES;
+            const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NS) & 1);
+            const uint32_t tPX = tb + lane_base + Cf::TM_PX + kW * (c & 1);
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_ld[b], par_st))) {
                 fail();
                 break;
             }
             if (!kFused && p.S_chk) {   // S at the chunk's start, for the backward
-                float4 *dst = reinterpret_cast<float4 *>(
-                    p.S_chk + ((size_t)(chunk0 + c) * p.H + h) * D * D + (size_t)L * D + j0 + c0);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    dst[i] = make_float4(Sr[4 * i], Sr[4 * i + 1], Sr[4 * i + 2], Sr[4 * i + 3]);
+                for (int jj = 0; jj < NJ; ++jj) {
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        p.S_chk + ((size_t)(chunk0 + c) * p.H + h) * D * D + (size_t)L * D + j0 +
+                        c0 + 32 * jj);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(Sr[jj][4 * i], Sr[jj][4 * i + 1], Sr[jj][4 * i + 2],
+                                             Sr[jj][4 * i + 3]);
+                }
             }
             // what the stage alone gives (g, the decay factors, the U~ words) is
             // read before the wait for the product
@@ -1073,14 +1125,19 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             const float egC = __expf(gC);
             const int nc = (int)min((long)C, len - (long)c * C);
             float egt = 0.f, ft = 0.f;
-            uint4 wu[4];
+            uint4 wu[NJ][4];
             if (pwarp) {
                 const int t = L - 64;
                 ft = __expf(gC - g[t]);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    wu[k] = *reinterpret_cast<const uint4 *>(st + ST_U + sw128_offset(t, c0 + 8 * k));
-                    if (phi) wu[k] = make_uint4(0u, 0u, 0u, 0u);   // U~ = 0 in a transition pass
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int cg = c0 + 32 * jj;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        wu[jj][k] = *reinterpret_cast<const uint4 *>(
+                            st + ST_U + (cg >> 6) * Cf::U_SLAB + sw128_offset(t, (cg & 63) + 8 * k));
+                        if (phi) wu[jj][k] = make_uint4(0u, 0u, 0u, 0u);   // U~ = 0 in a transition pass
+                    }
                 }
             } else {
                 egt = __expf(g[L]);
@@ -1092,35 +1149,41 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             tc_fence_after();
             if (pwarp) {
                 // ---- U = U~_b - P and U' = exp(g_C - g_t) U for token t = L - 64,
-                //      columns [c0, c0 + 32) ----
+                //      the thread's columns ----
                 const int t = L - 64;
-                uint32_t r[32];
-                tmem_ld32(tb + lane_base + TM_PX + 64 * (c & 1) + c0, r);
-                tmem_ld_wait();
-                float u[32], uz[32];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint4 w = wu[k];
-                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int cg = c0 + 32 * jj;
+                    uint32_t r[32];
+                    tmem_ld32(tPX + cg, r);
+                    tmem_ld_wait();
+                    float u[32], uz[32];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        u[8 * k + 2 * e] = bf_lo(ww[e]) - __uint_as_float(r[8 * k + 2 * e]);
-                        u[8 * k + 2 * e + 1] = bf_hi(ww[e]) - __uint_as_float(r[8 * k + 2 * e + 1]);
+                    for (int k = 0; k < 4; ++k) {
+                        const uint4 w = wu[jj][k];
+                        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            u[8 * k + 2 * e] = bf_lo(ww[e]) - __uint_as_float(r[8 * k + 2 * e]);
+                            u[8 * k + 2 * e + 1] =
+                                bf_hi(ww[e]) - __uint_as_float(r[8 * k + 2 * e + 1]);
+                        }
                     }
-                }
 #pragma unroll
-                for (int i = 0; i < 32; ++i) uz[i] = ft * u[i];
-                st_row_bf16x32(sU, t, c0, u);
-                st_row_bf16x32(sUz, t, c0, uz);
+                    for (int i = 0; i < 32; ++i) uz[i] = ft * u[i];
+                    st_row_bf16x32(sU + (cg >> 6) * Cf::U_SLAB, t, cg & 63, u);
+                    st_row_bf16x32(sUz + (cg >> 6) * Cf::U_SLAB, t, cg & 63, uz);
+                }
                 if (t >= nc) {
-                    // rows past the sequence's end: clear this column half of K
-                    // (the next sequence's tokens or zero fill) in both slabs
+                    // rows past the sequence's end: clear columns [32 hf, 32 hf + 32)
+                    // of K (the next sequence's tokens or zero fill) in both slabs
                     const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        *reinterpret_cast<uint4 *>(st + ST_KT + sw128_offset(t, c0 + 8 * k)) = zero4;
-                        *reinterpret_cast<uint4 *>(st + ST_KT + 8192 + sw128_offset(t, c0 + 8 * k)) =
+                        *reinterpret_cast<uint4 *>(st + ST_KT + sw128_offset(t, 32 * hf + 8 * k)) =
                             zero4;
+                        *reinterpret_cast<uint4 *>(st + ST_KT + 8192 +
+                                                   sw128_offset(t, 32 * hf + 8 * k)) = zero4;
                     }
                 }
                 fence_async_smem();
@@ -1128,25 +1191,30 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_u);
             } else {
-                // every read of this stage by the main warps precedes their
-                // bar_u arrival, which precedes the products whose completion
-                // frees the stage for the next load
+                // every read of this stage by the main warps (and, with one Y
+                // buffer, of the previous chunk's Y) precedes their bar_u
+                // arrival, which precedes the products that overwrite them
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_u);
             }
 
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_z, par))) { fail(); break; }
             tc_fence_after();
-            // ---- S_b <- exp(g_C) S_b + Z (row L, columns [c0, c0 + 32)) ----
-            {
+            // ---- S_b <- exp(g_C) S_b + Z (row L, the thread's columns) ----
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) {
                 uint32_t r[32];
-                tmem_ld32(tb + lane_base + TM_Z + c0, r);
+                tmem_ld32(tb + lane_base + Cf::TM_Z + c0 + 32 * jj, r);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) Sr[i] = fmaf(egC, Sr[i], __uint_as_float(r[i]));
+                for (int i = 0; i < 32; ++i) Sr[jj][i] = fmaf(egC, Sr[jj][i], __uint_as_float(r[i]));
             }
             if (c + 1 < nch) {
-                st_row_bf16x32(sS, L, c0, Sr);
+#pragma unroll
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int cg = c0 + 32 * jj;
+                    st_row_bf16x32(sS + (cg >> 6) * Cf::S_SLAB, L, cg & 63, Sr[jj]);
+                }
                 fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
@@ -1159,39 +1227,46 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                     break;
                 }
                 tc_fence_after();
-                uint32_t xr[32], yr[32];
-                tmem_ld32(tb + lane_base + TM_PX + 64 * (c & 1) + c0, xr);
-                tmem_ld32(tb + lane_base + TM_Y + 64 * (c & 1) + c0, yr);
-                tmem_ld_wait();
-                tc_fence_before();
-                if (L < nc && (kFused || p.o != nullptr)) {
-                    uint4 *dst = reinterpret_cast<uint4 *>((phi ? p.o_phi : p.o) +
-                                                           (size_t)(start + (long)c * C + L) * rs +
-                                                           (size_t)h * D + j0 + c0);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint32_t w[4];
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int cg = c0 + 32 * jj;
+                    uint32_t xr[32], yr[32];
+                    tmem_ld32(tPX + cg, xr);
+                    tmem_ld32(tb + lane_base + Cf::TM_Y + Cf::Y_STRIDE * (c & 1) + cg, yr);
+                    tmem_ld_wait();
+                    if (L < nc && (kFused || p.o != nullptr)) {
+                        uint4 *dst = reinterpret_cast<uint4 *>((phi ? p.o_phi : p.o) +
+                                                               (size_t)(start + (long)c * C + L) * rs +
+                                                               (size_t)h * D + j0 + cg);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i = 8 * k + 2 * e;
-                            w[e] = pack_bf2(fmaf(egt, __uint_as_float(xr[i]), __uint_as_float(yr[i])),
-                                            fmaf(egt, __uint_as_float(xr[i + 1]),
-                                                 __uint_as_float(yr[i + 1])));
+                        for (int k = 0; k < 4; ++k) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int i = 8 * k + 2 * e;
+                                w[e] = pack_bf2(
+                                    fmaf(egt, __uint_as_float(xr[i]), __uint_as_float(yr[i])),
+                                    fmaf(egt, __uint_as_float(xr[i + 1]), __uint_as_float(yr[i + 1])));
+                            }
+                            dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
-                        dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
+                tc_fence_before();
             }
         }
         if (!sAbort && (phi ? p.S_T_phi != nullptr : p.S_T != nullptr)) {
-            float4 *dst = reinterpret_cast<float4 *>((phi ? p.S_T_phi + phi_base : p.S_T + sbase) +
-                                                     (size_t)L * D + j0 + c0);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(Sr[4 * i], Sr[4 * i + 1], Sr[4 * i + 2], Sr[4 * i + 3]);
+            for (int jj = 0; jj < NJ; ++jj) {
+                float4 *dst = reinterpret_cast<float4 *>(
+                    (phi ? p.S_T_phi + phi_base : p.S_T + sbase) + (size_t)L * D + j0 + c0 + 32 * jj);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    dst[i] = make_float4(Sr[jj][4 * i], Sr[jj][4 * i + 1], Sr[jj][4 * i + 2],
+                                         Sr[jj][4 * i + 3]);
+            }
         }
     }
-
     tc_fence_before();
     named_sync(3, P2_THREADS);
     if (warp == 0) tmem_dealloc(tb, 512);
@@ -1204,6 +1279,16 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     extern __shared__ unsigned char smraw[];
     state_run<false, true>(&mq, &mk, &mw, &mu, &ma, p, align1024(smraw), (int)blockIdx.x,
                            (int)threadIdx.x);
+}
+
+// One CTA per (sequence, head) carrying all 128 columns of its state.
+__global__ void __launch_bounds__(P2_THREADS, 1)
+state_kernel_wide(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                  const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
+                  const __grid_constant__ CUtensorMap ma, const TcParams p) {
+    extern __shared__ unsigned char smraw[];
+    state_run<false, false, 128>(&mq, &mk, &mw, &mu, &ma, p, align1024(smraw), (int)blockIdx.x,
+                                 (int)threadIdx.x);
 }
 
 // ===================================================================== fused launch
@@ -1618,6 +1703,17 @@ bool use_fused(const Problem &p) {
     return n_state + (P > 1 ? 2L * p.n_seq * (P - 1) * p.H : 0) <= sm_count() / 2;
 }
 
+// The two-launch state pass runs one 128-column CTA per (sequence, head)
+// where two 64-column CTAs per head would not all be resident at once (more
+// than one CTA per SM, so the pass is bound by how many chains run side by
+// side, not by the length of one); the sequence split keeps the narrow pass.
+// KLA_WIDE_STATE=0 / 1 forces either form.
+bool use_wide_state(long n_units, int P) {
+    if (P > 1) return false;
+    if (const char *e = getenv("KLA_WIDE_STATE")) return atoi(e) != 0;
+    return 2 * n_units > sm_count();
+}
+
 }  // namespace
 
 bool chunk_tc_supported(int d, int dtype) { return d == 128 && dtype == 1; }
@@ -1727,6 +1823,10 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
         if ((e = cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)P2_SMEM)) != cudaSuccess)
             return e;
+        if ((e = cudaFuncSetAttribute(state_kernel_wide,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)P2Cfg<128>::SMEM)) != cudaSuccess)
+            return e;
         attrs = true;
     }
     const long n_pairs = (n_chunks_upper + 1) / 2;
@@ -1779,8 +1879,13 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const long n_phi = P > 1 ? 2L * p0.n_seq * (P - 1) * p.H : 0;
-    state_kernel<<<(unsigned)(2L * p.n_seq * p.H + n_phi), P2_THREADS, P2_SMEM, s>>>(mq, mk, mw, mu,
-                                                                                     ma, tp);
+    const long n_units = (long)p.n_seq * p.H;
+    if (use_wide_state(n_units, P))
+        state_kernel_wide<<<(unsigned)n_units, P2_THREADS, P2Cfg<128>::SMEM, s>>>(mq, mk, mw, mu,
+                                                                                ma, tp);
+    else
+        state_kernel<<<(unsigned)(2 * n_units + n_phi), P2_THREADS, P2_SMEM, s>>>(mq, mk, mw, mu,
+                                                                                ma, tp);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess || P == 1) return e;
     return launch_split_tail(p0, p, tp, P, ws + split_base, SL, s);
