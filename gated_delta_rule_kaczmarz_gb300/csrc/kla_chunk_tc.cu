@@ -1125,12 +1125,14 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             const float egC = __expf(gC);
             const int nc = (int)min((long)C, len - (long)c * C);
             float egt = 0.f, ft = 0.f;
+            // (the wide form, at its register limit, reads its U~ words after the wait)
+            constexpr int NPRE = kW == 64 ? NJ : 0;
             uint4 wu[NJ][4];
             if (pwarp) {
                 const int t = L - 64;
                 ft = __expf(gC - g[t]);
 #pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) {
+                for (int jj = 0; jj < NPRE; ++jj) {
                     const int cg = c0 + 32 * jj;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -1160,7 +1162,12 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                     float u[32], uz[32];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint4 w = wu[jj][k];
+                        uint4 w = wu[jj][k];
+                        if (NPRE == 0) {
+                            w = *reinterpret_cast<const uint4 *>(
+                                st + ST_U + (cg >> 6) * Cf::U_SLAB + sw128_offset(t, (cg & 63) + 8 * k));
+                            if (phi) w = make_uint4(0u, 0u, 0u, 0u);
+                        }
                         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
