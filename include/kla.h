@@ -132,8 +132,10 @@ KLA_API size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv,
  * launches, or three when fused).  The environment variable KLA_SEQ_SPLIT=P
  * forces a factor (1 disables the split); the workspace size depends on that
  * choice and on the SM count of the current device, so query it on the device
- * and with the environment of the call.  Other dtypes and sizes run on the
- * CUDA cores (fp32 arithmetic).
+ * and with the environment of the call.  In two launches, the state pass runs
+ * one CTA per (sequence, head) instead of two when two per head would
+ * outnumber the SMs (KLA_WIDE_STATE=0 or 1 forces either; results agree to
+ * rounding).  Other dtypes and sizes run on the CUDA cores (fp32 arithmetic).
  */
 KLA_API int kla_chunk_fwd(const void *q, const void *k, const void *v,
                   const float *alpha, const float *eta, float eps,
