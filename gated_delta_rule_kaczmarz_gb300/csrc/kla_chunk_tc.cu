@@ -805,7 +805,6 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 // the fused launch, waits for the ready flags).  Both wait converged.
 constexpr int P2_MAIN = 256, P2_THREADS = P2_MAIN + 64;
 constexpr int NSTAGE = 3;
-constexpr int DVB = 64;   // dv columns per CTA
 // Stage layout (one chunk):
 //   QW: two 64-feature slabs of 16 KB, each [Q rows 0..63 | W rows 0..63]
 //   KT: K slab 0, K slab 1 (8 KB each)
@@ -848,7 +847,8 @@ static_assert(P2Cfg<64>::NST == NSTAGE && P2Cfg<64>::ST_BYTES == ST_BYTES &&
                   P2Cfg<64>::ST_TX == ST_TX && P2Cfg<64>::SM_S == SM_S &&
                   P2Cfg<64>::SM_U == SM_U && P2Cfg<64>::SM_UZ == SM_UZ &&
                   P2Cfg<64>::SM_G == SM_G && P2Cfg<64>::SMEM == P2_SMEM &&
-                  P2Cfg<64>::TM_Z == TM_Z && P2Cfg<64>::TM_Y == TM_Y,
+                  P2Cfg<64>::TM_PX == TM_PX && P2Cfg<64>::TM_Z == TM_Z &&
+                  P2Cfg<64>::TM_Y == TM_Y,
               "narrow state pass layout");
 static_assert(P2Cfg<128>::SMEM <= 232448 && P2Cfg<128>::TM_Y + 128 <= 512, "wide state pass");
 
