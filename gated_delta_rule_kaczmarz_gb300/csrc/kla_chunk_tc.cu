@@ -217,9 +217,14 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, i
         acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
     }
     named_sync(bar, P1_THREADS);  // M complete; L21 no longer read
-    // X = -D2 M, written over L21
+    // X = -D2 M, written over L21.  D2 is lower triangular (zeros above its
+    // diagonal are stored), so row rr needs columns s <= rr only: the loop
+    // stops after the last column block any row of this warp needs (the
+    // skipped terms are exact zeros).
+    const int rr_max = rows * (((q & ~31) + 31) / pcols) + rows - 1;
+    const int s4lim = rr_max / 4 + 1 < n / 4 ? rr_max / 4 + 1 : n / 4;
 #pragma unroll 1
-    for (int s4 = 0; s4 < n / 4; ++s4) {
+    for (int s4 = 0; s4 < s4lim; ++s4) {
         float4 bb[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
