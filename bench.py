@@ -39,7 +39,7 @@ METRIC = "KLA chunkwise prefill tokens/s & % roofline; decode steps/s at B=256"
 # launch scaled to B=256 and one CCQ query call (its two launches), from the ncu
 # captures summarised in profiles/ (fused_kernel_layer_prefill.md,
 # decode_kernel_b128.md, ccq_layer_prefill.md).
-TRAFFIC_PREFILL = 68.21e6
+TRAFFIC_PREFILL = 68.26e6
 TRAFFIC_CCQ = 48.5e6 + 51.6e6
 TRAFFIC_DECODE = 2 * (135.83e6 + 74.59e6)
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
