@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     kla_chunk_fwd,
     kla_chunk_fwd_ex,
     kla_chunk_fwd_noalloc,
+    kla_chunk_fwd_noalloc_status,
     kla_chunk_fwd_varlen,
     kla_chunk_fwd_varlen_ex,
     kla_chunk_fwd_varlen_workspace_size,

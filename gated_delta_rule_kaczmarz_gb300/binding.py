@@ -108,6 +108,8 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
         lib.kla_chunk_fwd_noalloc.restype = I
         lib.kla_chunk_fwd_noalloc.argtypes = [vp, vp, vp, fp, fp, F, fp, vp, fp,
                                               I, I, I, I, I, I, I, vp]
+        lib.kla_chunk_fwd_noalloc_status.restype = I
+        lib.kla_chunk_fwd_noalloc_status.argtypes = [vp]
         lib.kla_workspace_status.restype = I
         lib.kla_workspace_status.argtypes = [vp, Z, vp]
         _lib = lib
@@ -341,6 +343,15 @@ def kla_chunk_fwd_noalloc(q, k, v, alpha, eta, eps, S0=None, o=None, S_T=None, s
                                    _stream(stream))
     _check(st)
     return o, S_T
+
+
+def kla_chunk_fwd_noalloc_status(stream=None) -> int:
+    """Synchronises the stream and returns the device status that the last
+    kla_chunk_fwd_noalloc call on the current device recorded in the built-in
+    array (raises KlaError when it is not OK)."""
+    st = load().kla_chunk_fwd_noalloc_status(_stream(stream))
+    _check(st)
+    return st
 
 
 def kla_chunk_fwd_varlen(q, k, v, alpha, eta, eps, cu_seqlens, S0=None, o=None, S_T=None,

@@ -90,6 +90,12 @@ struct TcParams {
     unsigned *flags;           // fused launch: one ready flag per work item, then the work-item
                                // counter (all zeroed per call)
     int n_units;               // fused launch: sequences x heads
+    // fused launch: the bound (clock64 cycles) of every wait on a ready flag,
+    // and an optional word that nothing sets, zeroed per call, on which the
+    // state pass waits once before its first load (a test of the timeout
+    // path; nullptr in normal calls)
+    long long flag_wait_limit;
+    const unsigned *test_gate;
 };
 
 __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
@@ -974,7 +980,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
     }
 
     auto fail = [&]() {
-        sAbort = 1;
+        *(volatile int *)&sAbort = 1;   // read by the other warps' waits
         set_status(p.status, kDevTimeout);
     };
 
@@ -989,7 +995,8 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             unsigned char *st = sm + b * Cf::ST_BYTES;
             const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NS) & 1);
             // stage landed, and S_c written to shared memory by the main warps
-            const bool ok = mbar_wait(&bar_ld[b], par_st) && mbar_wait(&bar_s, par);
+            const bool ok = mbar_wait_or_abort(&bar_ld[b], par_st, &sAbort) &&
+                            mbar_wait_or_abort(&bar_s, par, &sAbort);
             if (!__all_sync(0xffffffffu, ok)) { fail(); break; }
             tc_fence_after();
             if (lane == 0) {
@@ -1003,7 +1010,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 mma_commit(&bar_px);
             }
             __syncwarp();
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_u, par))) { fail(); break; }
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_u, par, &sAbort))) { fail(); break; }
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t aKT = smem_u32(st + ST_KT), aA = smem_u32(st + ST_A);
@@ -1039,16 +1046,20 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         for (; n < nch; ++n) {
             const int b = n % NS, k = n / NS;
             if (k >= 1 &&
-                !__all_sync(0xffffffffu, mbar_wait(&bar_empty[b], (uint32_t)((k - 1) & 1)))) {
+                !__all_sync(0xffffffffu,
+                            mbar_wait_or_abort(&bar_empty[b], (uint32_t)((k - 1) & 1), &sAbort))) {
                 fail();
                 break;
             }
             int st = 1;
             if (kFused && lane == 0) {
-                const unsigned *f = p.flags + (long)(n >> 1) * p.n_units + unit;
                 const long long t0 = clock64();
-                while (ld_acquire_u32(f) == 0u)
-                    if (clock64() - t0 > kWaitLimitCycles) { st = 0; break; }
+                if (n == 0 && p.test_gate != nullptr)
+                    while (ld_acquire_u32(p.test_gate) == 0u)
+                        if (clock64() - t0 >= p.flag_wait_limit) { st = 0; break; }
+                const unsigned *f = p.flags + (long)(n >> 1) * p.n_units + unit;
+                while (st && ld_acquire_u32(f) == 0u)
+                    if (clock64() - t0 >= p.flag_wait_limit) { st = 0; break; }
             }
             if (!__shfl_sync(0xffffffffu, st, 0)) { fail(); break; }
             if (lane == 0) {
@@ -1107,7 +1118,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             unsigned char *st = sm + b * Cf::ST_BYTES;
             const uint32_t par = (uint32_t)(c & 1), par_st = (uint32_t)((c / NS) & 1);
             const uint32_t tPX = tb + lane_base + Cf::TM_PX + kW * (c & 1);
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_ld[b], par_st))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_ld[b], par_st, &sAbort))) {
                 fail();
                 break;
             }
@@ -1149,7 +1160,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             } else {
                 egt = __expf(g[L]);
             }
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_px, par))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_px, par, &sAbort))) {
                 fail();
                 break;
             }
@@ -1210,7 +1221,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 if (lane == 0) mbar_arrive(&bar_u);
             }
 
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_z, par))) { fail(); break; }
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_z, par, &sAbort))) { fail(); break; }
             tc_fence_after();
             // ---- S_b <- exp(g_C) S_b + Z (row L, the thread's columns) ----
 #pragma unroll
@@ -1234,7 +1245,8 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             }
             // ---- O_b = diag(exp g) X + Y for token t = L (X rows), after S is published ----
             if (!pwarp) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&bar_y[c & 1], (uint32_t)((c >> 1) & 1)))) {
+                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_y[c & 1],
+                                                                 (uint32_t)((c >> 1) & 1), &sAbort))) {
                     fail();
                     break;
                 }
@@ -1859,6 +1871,16 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
         }
         tp.flags = reinterpret_cast<unsigned *>(ws + L.meta);   // zeroed with the status word
         tp.n_units = p.n_seq * p.H;
+        // Test hook: KLA_TEST_FLAG_WAIT=<cycles> bounds every flag wait by
+        // that many cycles and makes the state pass first wait on a header
+        // word that nothing sets (zeroed with the status word), so that the
+        // wait runs out and the timeout path runs.
+        tp.flag_wait_limit = kWaitLimitCycles;
+        tp.test_gate = nullptr;
+        if (const char *e = getenv("KLA_TEST_FLAG_WAIT")) {
+            tp.flag_wait_limit = std::max(0LL, atoll(e));
+            tp.test_gate = p.status + 1;
+        }
         const int n_state = 2 * p.n_seq * p.H;
         const int n_phi = P > 1 ? 2 * p0.n_seq * (P - 1) * p.H : 0;
         cudaLaunchConfig_t cfg = {};

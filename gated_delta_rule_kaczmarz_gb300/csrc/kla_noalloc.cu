@@ -13,13 +13,23 @@
 // Host code may not use the array's name as a device address (on the host it
 // is only a stand-in symbol): the first call on each device, with that device
 // current, looks the address up with cudaGetSymbolAddress and caches it.  That
-// first call should therefore come before any stream capture.
+// first call should therefore come before any stream capture.  The cache is
+// keyed on the device's current context as well: after a device reset the
+// module is loaded again, possibly at another address, and the next call
+// looks the address up anew.
+//
+// The kernels record a bounded wait that gave up, or another device-side
+// error, in the status word at the start of the array;
+// kla_chunk_fwd_noalloc_status reads it (the array's address is not exposed
+// otherwise).
 //
 // All calls share the one array, and it keeps the contents of the last call.
 // The only part that must start at zero, the status word, is cleared on the
 // stream by every call before any kernel reads it.  Two calls whose work
 // overlaps on the GPU (different streams, or different host threads without
 // ordering) race on the array; callers must serialise them.
+
+#include <cuda.h>
 
 #include <cstdio>
 #include <mutex>
@@ -34,11 +44,46 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-std::mutex g_setup_lock;
-void *g_scratch_addr[kMaxDevices] = {};
+struct ScratchEntry {
+    void *addr;
+    unsigned long long ctx_id;   // context the address belongs to (0: unknown)
+};
 
-// Device address of the scratch array on the current device (set up once per
-// device).  Returns nullptr and fills `err` on failure.
+std::mutex g_setup_lock;
+ScratchEntry g_scratch[kMaxDevices] = {};
+
+// Identifier of the calling thread's current context (0 when the driver
+// cannot tell; the cache then keys on the device alone).
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static bool looked_up = false;
+    if (!looked_up) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(fn);
+        looked_up = true;
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+        ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the scratch array on the current device, looked up once
+// per device and context.  Returns nullptr and fills `err` on failure.
 void *scratch_for_current_device(cudaError_t &err) {
     int dev = -1;
     err = cudaGetDevice(&dev);
@@ -48,14 +93,16 @@ void *scratch_for_current_device(cudaError_t &err) {
         return nullptr;
     }
     std::lock_guard<std::mutex> guard(g_setup_lock);
-    if (g_scratch_addr[dev] == nullptr) {
+    ScratchEntry &e = g_scratch[dev];
+    if (e.addr == nullptr || e.ctx_id != current_context_id()) {
         void *ptr = nullptr;
-        err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);   // also makes the context current
         if (err != cudaSuccess) return nullptr;
-        g_scratch_addr[dev] = ptr;
+        e.addr = ptr;
+        e.ctx_id = current_context_id();
     }
     err = cudaSuccess;
-    return g_scratch_addr[dev];
+    return e.addr;
 }
 
 }  // namespace
@@ -86,4 +133,17 @@ extern "C" int kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v
     }
     return kla_chunk_fwd(q, k, v, alpha, eta, eps, S0, o, S_T, B, T, H, dk, dv, chunk, dtype,
                          scratch, kNoallocScratchBytes, stream);
+}
+
+extern "C" int kla_chunk_fwd_noalloc_status(void *stream) {
+    cudaError_t err = cudaSuccess;
+    void *scratch = scratch_for_current_device(err);
+    if (scratch == nullptr) {
+        char msg[256];
+        std::snprintf(msg, sizeof msg, "kla_chunk_fwd_noalloc_status: scratch set-up failed: %s",
+                      cudaGetErrorString(err));
+        kla::set_error_message(msg);
+        return KLA_ERR_CUDA;
+    }
+    return kla_workspace_status(scratch, kNoallocScratchBytes, stream);
 }

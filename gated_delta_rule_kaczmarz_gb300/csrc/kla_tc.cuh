@@ -54,6 +54,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     }
     return true;
 }
+// As mbar_wait, but also gives up as soon as *abort is non-zero: another warp
+// of the CTA has failed, and the phase waited for may then never complete
+// (a stage that was never loaded, an arrival that will not come).  Only for
+// phases that depend on other warps; copies and products already issued
+// complete by themselves and are drained with mbar_wait.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity,
+                                                   const volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort != 0 || clock64() - t0 > kWaitLimitCycles) return false;
+    }
+    return true;
+}
 
 // ------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,

@@ -238,6 +238,17 @@ KLA_API int kla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                                   int dtype, void *stream);
 
 /*
+ * Synchronises `stream` and returns the device status that the last
+ * kla_chunk_fwd_noalloc call on the current device recorded in its built-in
+ * array: KLA_OK or KLA_ERR_TIMEOUT (a bounded device-side wait gave up and
+ * the outputs of that call are incomplete).  The counterpart of
+ * kla_workspace_status for the call without a workspace; like that call it
+ * has no counterpart in the pages.  KLA_ERR_CUDA if the array's address
+ * cannot be looked up.
+ */
+KLA_API int kla_chunk_fwd_noalloc_status(void *stream);
+
+/*
  * Backward pass of the fixed-length chunkwise forward (kla_chunk_fwd_ex with
  * the same inputs and beta_mode): the gradients of the scalar
  *
@@ -336,6 +347,17 @@ KLA_API int kla_ccq_query_step(const void *q, const void *k, const float *lambda
  * using `workspace` recorded on the device: KLA_OK, KLA_ERR_INVALID_ARG
  * (cu_seqlens rejected) or KLA_ERR_TIMEOUT.  A workspace of 0 bytes (NULL)
  * has no status word and returns KLA_OK.
+ *
+ * Every wait of one CTA on another (the single-launch prefill's state pass
+ * waiting for a chunk pair to be published) and every wait on the CTA's own
+ * asynchronous copies and tensor-core products is bounded (about one second
+ * of SM clock).  A wait that runs out records KLA_ERR_TIMEOUT here; the CTA's
+ * other warps stop waiting on work that will not come, the copies and
+ * products it already issued are waited for (they complete by themselves),
+ * its tensor memory is released and it leaves.  For tests only, the
+ * environment variable KLA_TEST_FLAG_WAIT=<cycles> bounds the flag waits of
+ * the single-launch prefill by that many cycles and makes its state pass
+ * first wait on a header word that nothing sets, so that the wait runs out.
  */
 KLA_API int kla_workspace_status(const void *workspace, size_t workspace_bytes, void *stream);
 

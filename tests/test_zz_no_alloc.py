@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import gated_delta_rule_kaczmarz_gb300 as kla
+import oracle
 from gated_delta_rule_kaczmarz_gb300 import binding
 from gated_delta_rule_kaczmarz_gb300.workloads import prefill_inputs
 from tests._util import TOL, rel_err
@@ -24,6 +25,10 @@ def _ptr(t):
 
 @pytest.mark.gpu
 def test_noalloc_matches_kla_chunk_fwd_two_calls_in_a_row():
+    """Two differently shaped calls in a row share the built-in array (the
+    second reuses what the first left in it): each matches kla_chunk_fwd with
+    its own workspace, the device status of each is OK, and the smaller call
+    is also checked against the fp64 oracle."""
     lib = binding.load()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for seed, (B, T, H) in ((70, (2, 300, 4)), (71, (4, 2048, 8))):
@@ -37,10 +42,17 @@ def test_noalloc_matches_kla_chunk_fwd_two_calls_in_a_row():
                                        _ptr(d["eta"]), d["eps"], _ptr(d["S0"]), _ptr(o), _ptr(S_T),
                                        B, T, H, 128, 128, 64, binding.KLA_DTYPE_BF16, stream)
         assert st == binding.KLA_OK, lib.kla_last_error_message()
+        assert lib.kla_chunk_fwd_noalloc_status(stream) == binding.KLA_OK, \
+            lib.kla_last_error_message()
         torch.cuda.synchronize()
         tol = TOL[torch.bfloat16]
         assert rel_err(o, o_ref.cpu().double().numpy()) <= tol
         assert rel_err(S_T, S_ref.cpu().double().numpy()) <= tol
+        if T <= 300:
+            o_or, S_or = oracle.forward(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["eta"],
+                                        inp["eps"], inp["S0"], nthreads=8)
+            assert rel_err(o, o_or) <= tol
+            assert rel_err(S_T, S_or) <= tol
 
 
 @pytest.mark.gpu
