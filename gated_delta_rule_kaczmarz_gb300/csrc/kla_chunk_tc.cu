@@ -310,9 +310,10 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     float *sN2 = sBeta + 128;
 
     if (tid0 == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        mbar_init(&bars[2], 1);
+        mbar_init(&bars[0], 1);   // K and Q landed
+        mbar_init(&bars[1], 1);   // Gram products done
+        mbar_init(&bars[2], 1);   // W and U~ products done
+        mbar_init(&bars[3], 1);   // V landed
         fence_mbar_init();
         // an error already reported: read once, so that all the worker's
         // threads agree (threads reading the word at different times might not)
@@ -387,7 +388,10 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
 
     if (tid == 0) {
         bulk_wait_group_read0();   // the previous item's W / U~ stores have left shared memory
-        mbar_expect_tx(&bars[0], 3u * 32768u);
+        // K and Q first (the Gram products need them); V, needed only by the
+        // U~ product, on its own barrier behind them (not at all in the CCQ
+        // mode, which stores a zero tile from the V region)
+        mbar_expect_tx(&bars[0], 2u * 32768u);
 #pragma unroll 1
         for (int q = 0; q < 2; ++q)
 #pragma unroll 1
@@ -395,8 +399,16 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
                 const int z = (int)(q ? r01 : r00);
                 tma_load_3d(KQ + s * 32768 + q * 8192, mk, &bars[0], 64 * s, h, z);
                 tma_load_3d(KQ + s * 32768 + 16384 + q * 8192, mq, &bars[0], 64 * s, h, z);
-                tma_load_3d(sV + s * 16384 + q * 8192, mv, &bars[0], 64 * s, h, z);
             }
+        if (p.mode == 0) {
+            mbar_expect_tx(&bars[3], 32768u);
+#pragma unroll 1
+            for (int q = 0; q < 2; ++q)
+#pragma unroll 1
+                for (int s = 0; s < 2; ++s)
+                    tma_load_3d(sV + s * 16384 + q * 8192, mv, &bars[3], 64 * s, h,
+                                (int)(q ? r01 : r00));
+        }
         if (kFused && pending >= 0) {   // the previous item's outputs are complete
             bulk_wait_group0();
             fence_proxy_async_global();
@@ -568,12 +580,6 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
             if (!live) w = make_uint4(0u, 0u, 0u, 0u);
             *pk4 = w;
         }
-        if (!live) {
-#pragma unroll 1
-            for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4 *>(sV + hf * 16384 + sw128_offset(r, ch * 8)) =
-                    make_uint4(0u, 0u, 0u, 0u);
-        }
     }
     if (!ok) *sAbort = 1;
     named_sync(bar, P1_THREADS);
@@ -667,6 +673,19 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     merge_level<16>(KQ, scratch, tid, bar);   // 32 x 32 diagonal blocks
     merge_level<32>(KQ, scratch, tid, bar);   // the whole 64 x 64 inverse
 
+    // ---- V landed; rows past the chunk's end (another sequence's tokens or
+    //      TMA zero fill) are cleared so that nothing from them reaches U~ ----
+    if (!abort2 && !mbar_wait(&bars[3], ph)) {
+        *sAbort = 1;
+        set_status(p.status, kDevTimeout);
+    }
+    if (t >= nc) {
+#pragma unroll 1
+        for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4 *>(sV + hf * 16384 + sw128_offset(r, ch * 8)) =
+                make_uint4(0u, 0u, 0u, 0u);
+    }
+
     // ---- A operand = T diag(beta) in bf16, block diagonal over the two chunks;
     //      thread half hf converts columns [32 hf, 32 hf + 32) of row t ----
     {
@@ -707,7 +726,8 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     fence_async_smem();
     tc_fence_before();
     named_sync(bar, P1_THREADS);
-    if (tid == 0 && !abort2) {
+    const bool abort3 = *sAbort != 0;   // includes a wait for V that ran out
+    if (tid == 0 && !abort3) {
         tc_fence_after();
         const uint32_t aA = smem_u32(KQ + 16384), aK = smem_u32(KQ), aV = smem_u32(sV);
         // W = (T diag beta) (diag(exp g) K): M = 128 tokens, N = 128, K = 128 tokens;
@@ -730,8 +750,8 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     // ---- epilogue 2: W (first half) and U~ (second half) rows of token row r,
     //      bf16, staged in the now free K and V regions with the 128-byte
     //      swizzle of the tensor maps, then written by TMA stores; g ----
-    ok = !abort2 && mbar_wait(&bars[2], ph);
-    if (!abort2 && !ok) set_status(p.status, kDevTimeout);
+    ok = !abort3 && mbar_wait(&bars[2], ph);
+    if (!abort3 && !ok) set_status(p.status, kDevTimeout);
     tc_fence_after();
     if (ok) {
         unsigned char *stg = hf ? sV : KQ;
