@@ -862,7 +862,12 @@ constexpr uint32_t TM_PX = 0, TM_Z = 128, TM_Y = 192;
 template <int kW>
 struct P2Cfg {
     static constexpr int NST = kW == 64 ? 3 : 2;
-    static constexpr int NJ = kW / 64;                 // 32-column groups per main thread
+    static constexpr int NJ = kW / 64;                 // 64-column slabs of the tile
+    // main warps: four per 32-column group (one per TMEM lane quadrant), so
+    // that every main thread holds 32 columns of one row whatever kW; then
+    // the MMA issuer and the load warp
+    static constexpr int NMAIN = kW / 32 * 4;
+    static constexpr int THREADS = (NMAIN + 2) * 32;
     static constexpr uint32_t U_BYTES = 64u * kW * 2u;   // U~ of a stage (64-column slabs)
     static constexpr uint32_t ST_BYTES = ST_U + U_BYTES;
     static constexpr uint32_t ST_TX = 32768u + 16384u + 8192u + U_BYTES + 256u;
@@ -882,6 +887,7 @@ static_assert(P2Cfg<64>::NST == NSTAGE && P2Cfg<64>::ST_BYTES == ST_BYTES &&
                   P2Cfg<64>::TM_Y == TM_Y,
               "narrow state pass layout");
 static_assert(P2Cfg<128>::SMEM <= 232448 && P2Cfg<128>::TM_Y + 128 <= 512, "wide state pass");
+static_assert(P2Cfg<64>::THREADS == P2_THREADS, "narrow state pass threads");
 
 template <int kW>
 __device__ __forceinline__ void issue_stage(unsigned char *st, float *g_dst, uint64_t *bar,
@@ -925,8 +931,8 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                                           const CUtensorMap *ma, const TcParams &p,
                                           unsigned char *sm, int bid, int tid) {
     using Cf = P2Cfg<kW>;
-    constexpr int NS = Cf::NST, NJ = Cf::NJ;
-    static_assert(!kSplit || kW == 64, "the transition passes use the narrow layout");
+    constexpr int NS = Cf::NST, NJ = 1;   // one 32-column group per main thread
+    constexpr int NMAIN = Cf::NMAIN, NCG = kW / 32;
     __shared__ uint64_t bar_ld[NS];
     __shared__ uint64_t bar_empty[NS];   // the products of a stage's chunk are done
     __shared__ uint64_t bar_px, bar_u, bar_z, bar_s, bar_fin;
@@ -939,22 +945,24 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
 
     const int warp = tid >> 5, lane = tid & 31;
     const int L = (warp & 3) * 32 + lane;       // TMEM lane (main warps)
-    const int hf = (warp >> 2) & 1;             // column half (main warps)
-    const int c0 = 32 * NJ * hf;                // first of the thread's 32 NJ columns of the tile
+    const int hf = (warp >> 2) & (NCG - 1);     // 32-column group (main warps)
+    const int c0 = 32 * hf;                     // first of the thread's 32 columns of the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    // transition-pass CTAs: two per (batch, segment >= 1, head), in that order
+    // transition-pass CTAs: 64 / kW... per (batch, segment >= 1, head), in
+    // that order (two 64-column CTAs, or one 128-column CTA, per chain)
+    constexpr int CPC = kW == 64 ? 2 : 1;
     const bool phi = kSplit && p.phi_first > 0 && bid >= p.phi_first;
     const int segP = kSplit ? p.seg_P : 1;
     size_t phi_base = 0;
     if (phi) {
-        const int k = bid - p.phi_first, idx = k >> 1;
+        const int k = bid - p.phi_first, idx = k / CPC;
         const int hh = idx % p.H, r = idx / p.H, P1 = p.seg_P - 1;
         const int seqv = (r / P1) * p.seg_P + 1 + r % P1;
-        bid = ((seqv * p.H + hh) << 1) | (k & 1);
+        bid = (seqv * p.H + hh) * CPC + k % CPC;
         phi_base = (size_t)idx * D * D;
     }
-    const int unit = kW == 64 ? bid >> 1 : bid, jh = kW == 64 ? (bid & 1) : 0, j0 = 64 * jh;
+    const int unit = bid / CPC, jh = bid % CPC, j0 = 64 * jh;
     const int rank = unit / p.H, h = unit % p.H;
     const int seq = p.order ? p.order[rank] : rank;
     long start, len, chunk0;
@@ -976,11 +984,11 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             mbar_init(&bar_empty[i], 1);
         }
         mbar_init(&bar_px, 1);
-        mbar_init(&bar_u, 8);      // one arrival per main warp
+        mbar_init(&bar_u, NMAIN);   // one arrival per main warp
         mbar_init(&bar_z, 1);
         mbar_init(&bar_y[0], 1);
         mbar_init(&bar_y[1], 1);
-        mbar_init(&bar_s, 8);      // one arrival per main warp
+        mbar_init(&bar_s, NMAIN);   // one arrival per main warp
         mbar_init(&bar_fin, 1);
         fence_mbar_init();
         // an error already reported: read once, so that the whole CTA
@@ -991,7 +999,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         tmem_alloc(&tslot, 512);
         tmem_relinquish();
     }
-    named_sync(3, P2_THREADS);
+    named_sync(3, Cf::THREADS);
     tc_fence_after();
     const uint32_t tb = tslot;
     if (sAbort) {
@@ -1004,7 +1012,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         set_status(p.status, kDevTimeout);
     };
 
-    if (warp == 8) {
+    if (warp == NMAIN) {
         // ----------------------------------------------------------------- issuer
         const uint32_t id_px = idesc_bf16_f32(128, kW, false, true);
         const uint32_t id_zy = idesc_bf16_f32(128, kW, true, true);
@@ -1056,7 +1064,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         if (lane == 0) mma_commit(&bar_fin);
         __syncwarp();
         (void)mbar_wait(&bar_fin, 0u);
-    } else if (warp == 9) {
+    } else if (warp == NMAIN + 1) {
         // ----------------------------------------------------------------- loads
         // Chunk n goes to stage n % NSTAGE once the products of chunk
         // n - NSTAGE are done with it (bar_empty) and, in the fused launch,
@@ -1161,7 +1169,8 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             const float egC = __expf(gC);
             const int nc = (int)min((long)C, len - (long)c * C);
             float egt = 0.f, ft = 0.f;
-            // (the wide form, at its register limit, reads its U~ words after the wait)
+            // (the wide form, with 576 threads under its register limit, reads its
+            // U~ words after the wait)
             constexpr int NPRE = kW == 64 ? NJ : 0;
             uint4 wu[NJ][4];
             if (pwarp) {
@@ -1189,6 +1198,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 // ---- U = U~_b - P and U' = exp(g_C - g_t) U for token t = L - 64,
                 //      the thread's columns ----
                 const int t = L - 64;
+                if (kW == 64) {
 #pragma unroll
                 for (int jj = 0; jj < NJ; ++jj) {
                     const int cg = c0 + 32 * jj;
@@ -1217,16 +1227,53 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                     st_row_bf16x32(sU + (cg >> 6) * Cf::U_SLAB, t, cg & 63, u);
                     st_row_bf16x32(sUz + (cg >> 6) * Cf::U_SLAB, t, cg & 63, uz);
                 }
+                } else {
+                    // 16 columns at a time (register pressure of 576 threads)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int cg = c0 + 16 * hh;
+                        uint32_t r[16];
+                        tmem_ld16(tPX + cg, r);
+                        tmem_ld_wait();
+                        uint32_t pu[8], pz[8];
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            uint4 w = *reinterpret_cast<const uint4 *>(
+                                st + ST_U + (cg >> 6) * Cf::U_SLAB + sw128_offset(t, (cg & 63) + 8 * k));
+                            if (phi) w = make_uint4(0u, 0u, 0u, 0u);
+                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float u0 = bf_lo(ww[e]) - __uint_as_float(r[8 * k + 2 * e]);
+                                const float u1 = bf_hi(ww[e]) - __uint_as_float(r[8 * k + 2 * e + 1]);
+                                pu[4 * k + e] = pack_bf2(u0, u1);
+                                pz[4 * k + e] = pack_bf2(ft * u0, ft * u1);
+                            }
+                        }
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const uint32_t off = sw128_offset(t, (cg & 63) + 8 * k);
+                            *reinterpret_cast<uint4 *>(sU + (cg >> 6) * Cf::U_SLAB + off) =
+                                make_uint4(pu[4 * k], pu[4 * k + 1], pu[4 * k + 2], pu[4 * k + 3]);
+                            *reinterpret_cast<uint4 *>(sUz + (cg >> 6) * Cf::U_SLAB + off) =
+                                make_uint4(pz[4 * k], pz[4 * k + 1], pz[4 * k + 2], pz[4 * k + 3]);
+                        }
+                    }
+                }
                 if (t >= nc) {
-                    // rows past the sequence's end: clear columns [32 hf, 32 hf + 32)
-                    // of K (the next sequence's tokens or zero fill) in both slabs
+                    // rows past the sequence's end: clear this thread's share of
+                    // K's row (the next sequence's tokens or zero fill): with two
+                    // column groups, features [32 hf, 32 hf + 32) of both slabs;
+                    // with four, features [32 (hf % 2), + 32) of slab hf / 2
                     const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        *reinterpret_cast<uint4 *>(st + ST_KT + sw128_offset(t, 32 * hf + 8 * k)) =
-                            zero4;
-                        *reinterpret_cast<uint4 *>(st + ST_KT + 8192 +
-                                                   sw128_offset(t, 32 * hf + 8 * k)) = zero4;
+                    for (int sl = 0; sl < 2; ++sl) {
+                        if (NCG == 4 && sl != (hf >> 1)) continue;
+                        const int f0 = NCG == 4 ? 32 * (hf & 1) : 32 * hf;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            *reinterpret_cast<uint4 *>(st + ST_KT + sl * 8192 +
+                                                       sw128_offset(t, f0 + 8 * k)) = zero4;
                     }
                 }
                 fence_async_smem();
@@ -1271,19 +1318,28 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                     break;
                 }
                 tc_fence_after();
+                // 32 columns at once (kW = 64), or 16 at a time (kW = 128)
+                constexpr int OW = kW == 64 ? 32 : 16;
 #pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) {
-                    const int cg = c0 + 32 * jj;
-                    uint32_t xr[32], yr[32];
-                    tmem_ld32(tPX + cg, xr);
-                    tmem_ld32(tb + lane_base + Cf::TM_Y + Cf::Y_STRIDE * (c & 1) + cg, yr);
+                for (int hh = 0; hh < 32 / OW; ++hh) {
+                    const int cg = c0 + OW * hh;
+                    uint32_t xr[OW], yr[OW];
+                    if (OW == 32) {
+                        tmem_ld32(tPX + cg, *reinterpret_cast<uint32_t(*)[32]>(xr));
+                        tmem_ld32(tb + lane_base + Cf::TM_Y + Cf::Y_STRIDE * (c & 1) + cg,
+                                  *reinterpret_cast<uint32_t(*)[32]>(yr));
+                    } else {
+                        tmem_ld16(tPX + cg, *reinterpret_cast<uint32_t(*)[16]>(xr));
+                        tmem_ld16(tb + lane_base + Cf::TM_Y + Cf::Y_STRIDE * (c & 1) + cg,
+                                  *reinterpret_cast<uint32_t(*)[16]>(yr));
+                    }
                     tmem_ld_wait();
                     if (L < nc && (kFused || p.o != nullptr)) {
                         uint4 *dst = reinterpret_cast<uint4 *>((phi ? p.o_phi : p.o) +
                                                                (size_t)(start + (long)c * C + L) * rs +
                                                                (size_t)h * D + j0 + cg);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
+                        for (int k = 0; k < OW / 8; ++k) {
                             uint32_t w[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
@@ -1312,7 +1368,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         }
     }
     tc_fence_before();
-    named_sync(3, P2_THREADS);
+    named_sync(3, Cf::THREADS);
     if (warp == 0) tmem_dealloc(tb, 512);
 }
 
@@ -1325,14 +1381,16 @@ state_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                            (int)threadIdx.x);
 }
 
-// One CTA per (sequence, head) carrying all 128 columns of its state.
-__global__ void __launch_bounds__(P2_THREADS, 1)
+// One CTA per (sequence, head) -- or, with the sequence split, per virtual
+// sequence and per transition pass -- carrying all 128 columns of its state.
+constexpr int P2W_THREADS = P2Cfg<128>::THREADS;
+__global__ void __launch_bounds__(P2W_THREADS, 1)
 state_kernel_wide(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
                   const __grid_constant__ CUtensorMap ma, const TcParams p) {
     extern __shared__ unsigned char smraw[];
-    state_run<false, false, 128>(&mq, &mk, &mw, &mu, &ma, p, align1024(smraw), (int)blockIdx.x,
-                                 (int)threadIdx.x);
+    state_run<false, true, 128>(&mq, &mk, &mw, &mu, &ma, p, align1024(smraw), (int)blockIdx.x,
+                                (int)threadIdx.x);
 }
 
 // ===================================================================== fused launch
@@ -1363,13 +1421,14 @@ fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     const int pre = p.nch_fixed >= 4 ? 2 : 1;   // leading chunk pairs done by the state CTAs
     if ((int)blockIdx.x < n_state + n_phi) {
         // state-pass CTAs (then, with the sequence split, transition-pass CTAs,
-        // which only consume)
+        // which only consume); two 64-column CTAs per chain: the three load
+        // stages they keep in flight do not fit beside a 128-column tile
         const int unit = (int)blockIdx.x >> 1, jh = (int)blockIdx.x & 1;
         if ((int)blockIdx.x < n_state && jh < pre && tid < P1_THREADS)
             intra_run<true>(&mq, &mk, &mv, &mw, &mu, p, n_pairs, sm, tid, 1,
                             (long)jh * p.n_units + unit, n_items);
         if (tid < P2_THREADS)
-            state_run<true, kSplit>(&mq, &mk, &mw, &mu, &ma, p, sm, (int)blockIdx.x, tid);
+            state_run<true, kSplit, 64>(&mq, &mk, &mw, &mu, &ma, p, sm, (int)blockIdx.x, tid);
         return;
     }
     __shared__ int stagger;
@@ -1693,13 +1752,20 @@ WsLayout layout(long n_chunks, int H, int n_seq) {
     return L;
 }
 
+// Chains of a sequence split into P segments: P state passes and P - 1
+// transition passes per (sequence, head).
+long split_chains(long units, int P) { return units * P + units * (P - 1); }
+
 // Sequence split factor P for a fixed-length batch (1: none).  Each segment
-// is a whole number of 128-token tiles; by default the largest P in {8, 4, 2}
-// whose segments hold at least 1024 tokens and whose state and transition
-// passes (2 B H P + 2 B H (P - 1) CTAs) fit on the SMs at once -- few heads and
-// long sequences, where the serial chain of the state pass dominates.  The
-// environment variable KLA_SEQ_SPLIT=P sets it (any P whose segments are whole
-// 128-token tiles; KLA_SEQ_SPLIT=1 disables the split).
+// is a whole number of 128-token tiles.  By default the largest P in
+// {8, 4, 2} such that either the segments hold at least 1024 tokens and the
+// state and transition passes fit on the SMs at once as two 64-column CTAs
+// per chain, or the segments hold at least 4096 tokens and they fit as one
+// 128-column CTA per chain (a pass with two load stages, which pays only on
+// long chains) -- few heads and long sequences, where the serial chain of
+// the state pass dominates.  The environment variable KLA_SEQ_SPLIT=P sets
+// it (any P whose segments are whole 128-token tiles; KLA_SEQ_SPLIT=1
+// disables the split).
 int split_factor(int n_seq, int T, int H, bool varlen) {
     if (varlen || T <= 0) return 1;
     auto valid = [&](int P) { return P >= 2 && T % (P * 128) == 0; };
@@ -1707,12 +1773,18 @@ int split_factor(int n_seq, int T, int H, bool varlen) {
         const int P = atoi(e);
         return valid(P) ? P : 1;
     }
-    const long units = (long)n_seq * H;
-    for (int P = 8; P >= 2; P >>= 1)
-        if (valid(P) && T / P >= 1024 && 2 * units * P + 2 * units * (P - 1) <= sm_count())
-            return P;
+    const long units = (long)n_seq * H, sms = sm_count();
+    for (int P = 8; P >= 2; P >>= 1) {
+        if (!valid(P)) continue;
+        if (T / P >= 1024 && 2 * split_chains(units, P) <= sms) return P;
+        if (T / P >= 4096 && split_chains(units, P) <= sms) return P;
+    }
     return 1;
 }
+
+// A split whose chains in two 64-column CTAs each would outnumber the SMs
+// runs them as one 128-column CTA each (two launches).
+bool split_wide(long units, int P) { return P > 1 && 2 * split_chains(units, P) > sm_count(); }
 
 struct SplitLayout {
     size_t N, Phi, Qc, Sst, total;
@@ -1736,15 +1808,13 @@ SplitLayout split_layout(int n_seq, int T, int H, int P) {
 // The fused launch serves fixed-length batches with an even number of chunks
 // per (virtual) sequence whose state pass (with the sequence split: state and
 // transition passes) fits on at most half of the SMs; with fewer SMs left to
-// phase 1 its items arrive more slowly than the chain consumes them (measured
-// on long_context: 684 us fused against 650 us in two launches).
+// phase 1 its items arrive more slowly than the chain consumes them.
 bool use_fused(const Problem &p) {
     if (p.cu_seqlens != nullptr || p.T <= 0) return false;
     const int P = p.mode == 0 ? split_factor(p.n_seq, p.T, p.H, false) : 1;
     const int nch = (p.T / P + C - 1) / C;
     if (nch % 2 != 0) return false;
-    const long n_state = 2L * p.n_seq * P * p.H;
-    return n_state + (P > 1 ? 2L * p.n_seq * (P - 1) * p.H : 0) <= sm_count() / 2;
+    return 2 * split_chains((long)p.n_seq * p.H, P) <= sm_count() / 2;
 }
 
 // The two-launch state pass runs one 128-column CTA per (sequence, head)
@@ -1827,9 +1897,11 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     tp.eta = p.eta;
     tp.S0 = p.S0;
     tp.S_T = p.S_T;
+    const bool fused = !record && use_fused(p0);
+    bool wide_split = !fused && split_wide((long)p0.n_seq * p0.H, P);
     if (P > 1) {   // the virtual sequences' end states go to N, not to S_T
         tp.S_T = reinterpret_cast<float *>(ws + split_base + SL.N);
-        tp.phi_first = 2 * p.n_seq * p.H;
+        tp.phi_first = (wide_split ? 1 : 2) * p.n_seq * p.H;
         tp.o_phi = reinterpret_cast<__nv_bfloat16 *>(ws + split_base + SL.Qc);
         tp.S_T_phi = reinterpret_cast<float *>(ws + split_base + SL.Phi);
     }
@@ -1877,7 +1949,7 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     const long n_items = n_pairs * p.H;
     tp.S_chk = p0.S_chk;
     tp.T_chk = static_cast<__nv_bfloat16 *>(p0.T_chk);
-    if (!record && use_fused(p0)) {
+    if (fused) {
         static bool fattr = false;
         if (!fattr) {
             if ((e = cudaFuncSetAttribute(fused_kernel<false>,
@@ -1927,19 +1999,21 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
         (void)cudaGetLastError();
         tp.flags = nullptr;
         tp.n_units = 0;
+        wide_split = split_wide((long)p0.n_seq * p0.H, P);
+        if (P > 1) tp.phi_first = (wide_split ? 1 : 2) * p.n_seq * p.H;
     }
     const long grid1 = n_items < 2L * sm_count() ? n_items : 2L * sm_count();
     intra_kernel<<<(unsigned)grid1, P1_THREADS, P1_SMEM, s>>>(mq, mk, mv, mw, mu, tp, n_pairs);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const long n_phi = P > 1 ? 2L * p0.n_seq * (P - 1) * p.H : 0;
+    const long n_phi = P > 1 ? (long)p0.n_seq * (P - 1) * p.H : 0;   // transition chains
     const long n_units = (long)p.n_seq * p.H;
-    if (use_wide_state(n_units, P))
-        state_kernel_wide<<<(unsigned)n_units, P2_THREADS, P2Cfg<128>::SMEM, s>>>(mq, mk, mw, mu,
-                                                                                ma, tp);
+    if (wide_split || use_wide_state(n_units, P))
+        state_kernel_wide<<<(unsigned)(n_units + n_phi), P2W_THREADS, P2Cfg<128>::SMEM, s>>>(
+            mq, mk, mw, mu, ma, tp);
     else
-        state_kernel<<<(unsigned)(2 * n_units + n_phi), P2_THREADS, P2_SMEM, s>>>(mq, mk, mw, mu,
-                                                                                ma, tp);
+        state_kernel<<<(unsigned)(2 * (n_units + n_phi)), P2_THREADS, P2_SMEM, s>>>(mq, mk, mw, mu,
+                                                                                  ma, tp);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess || P == 1) return e;
     return launch_split_tail(p0, p, tp, P, ws + split_base, SL, s);

@@ -49,6 +49,29 @@ def test_split_forward_parity(split, B, T, H, P, with_S0, no_alpha, mode, launch
     assert rel_err(S, S_ref) <= 2e-2
 
 
+@pytest.mark.parametrize("B,T,H,P,with_S0,no_alpha,mode", [
+    (1, 4096, 16, 4, True, False, "kaczmarz"),   # 16 x 7 chains: two CTAs each would not fit
+    (2, 2048, 16, 2, False, True, "given"),      # 32 x 3 chains
+])
+def test_split_with_one_wide_cta_per_chain(split, B, T, H, P, with_S0, no_alpha, mode):
+    """A split whose state and transition chains in two 64-column CTAs each
+    would outnumber the SMs runs one 128-column CTA per chain: phase 1, the
+    state and transition launch, the combine and the correction."""
+    split(P)
+    inp = prefill_inputs(B, T, H, 128, 128, "bf16", seed=500 + T + P, s0_var=0.01)
+    g = cuda(inp)
+    S0 = inp["S0"] if with_S0 else None
+    n0 = kla.kla_launch_count()
+    o, S = kla.kla_chunk_fwd(g["q"], g["k"], g["v"], None if no_alpha else g["alpha"], g["eta"],
+                             inp["eps"], g["S0"] if with_S0 else None, beta_mode=mode)
+    torch.cuda.synchronize()
+    assert kla.kla_launch_count() - n0 == 4
+    o_ref, S_ref = oracle.forward(inp["q"], inp["k"], inp["v"], None if no_alpha else inp["alpha"],
+                                  inp["eta"], inp["eps"], S0, nthreads=16, beta_mode=mode)
+    assert rel_err(o, o_ref) <= 2e-2
+    assert rel_err(S, S_ref) <= 2e-2
+
+
 def test_split_matches_unsplit(split):
     """The split and the fused single-chain forward agree (both bf16 paths)."""
     inp = prefill_inputs(2, 1024, 2, 128, 128, "bf16", seed=9, s0_var=0.01)
@@ -88,7 +111,7 @@ def test_long_context_takes_the_split_sampled(monkeypatch):
     n0 = kla.kla_launch_count()
     o, S = kla.kla_chunk_fwd(g["q"], g["k"], g["v"], g["alpha"], g["eta"], wl.eps, g["S0"])
     torch.cuda.synchronize()
-    assert kla.kla_launch_count() - n0 == 4   # 96 state + transition CTAs: two launches
+    assert kla.kla_launch_count() - n0 == 4   # phase 1, state + transition, combine, correct
     for h in (0, 11):
         sl = lambda x: x[:, :, h:h + 1].contiguous()
         o_ref, S_ref = oracle.forward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["alpha"]),
