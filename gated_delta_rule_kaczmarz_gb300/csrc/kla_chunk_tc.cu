@@ -1516,30 +1516,32 @@ prep_kernel(const int *cu, int N, int total_T, int *chunk_prefix, int *order, un
 // S0 = I).  The segment start states follow in order from S_1 = S_end of
 // segment 0.
 
-// Per (batch, head, 32 columns): S_1 .. S_{P-1} into Sst (bf16, the
+// Per (batch, head, CBW columns): S_1 .. S_{P-1} into Sst (bf16, the
 // correction's operand) and S_P as S_T.  The columns are independent.
 constexpr int CB_THREADS = 256;
-constexpr size_t CB_SMEM = ((size_t)D * (D + 1) + (size_t)D * 33) * sizeof(float);
+constexpr int CBW = 16;   // state columns per CTA (two threads per row, CBW / 2 each)
+constexpr size_t CB_SMEM = ((size_t)D * (D + 1) + (size_t)D * (CBW + 1)) * sizeof(float);
 
 __global__ void __launch_bounds__(CB_THREADS)
 split_combine_kernel(const float *__restrict__ Nbuf, const float *__restrict__ Phi,
                      __nv_bfloat16 *__restrict__ Sst, float *__restrict__ S_T, int H, int P,
                      const unsigned *status) {
     extern __shared__ float cb_sm[];
-    float(*Ph)[D + 1] = reinterpret_cast<float(*)[D + 1]>(cb_sm);              // Phi_s
-    float(*Ss)[33] = reinterpret_cast<float(*)[33]>(cb_sm + (size_t)D * (D + 1));   // S_s block
+    constexpr int NX = CBW / 2;
+    float(*Ph)[D + 1] = reinterpret_cast<float(*)[D + 1]>(cb_sm);                        // Phi_s
+    float(*Ss)[CBW + 1] = reinterpret_cast<float(*)[CBW + 1]>(cb_sm + (size_t)D * (D + 1));   // S_s
     if (status_bad(status)) return;
-    const int unit = blockIdx.x, b = unit / H, h = unit % H, jb = blockIdx.y * 32;
-    const int tid = threadIdx.x, i = tid >> 1, j0 = (tid & 1) * 16;
-    float cur[16];
+    const int unit = blockIdx.x, b = unit / H, h = unit % H, jb = blockIdx.y * CBW;
+    const int tid = threadIdx.x, i = tid >> 1, j0 = (tid & 1) * NX;
+    float cur[NX];
     const float *n0 = Nbuf + ((size_t)b * P * H + h) * D * D + (size_t)i * D + jb + j0;
 #pragma unroll
-    for (int x = 0; x < 16; ++x) cur[x] = n0[x];
+    for (int x = 0; x < NX; ++x) cur[x] = n0[x];
     for (int sg = 1; sg < P; ++sg) {
         const size_t pidx = ((size_t)(b * (P - 1) + sg - 1) * H + h) * D * D;
         __nv_bfloat16 *dst = Sst + pidx + (size_t)i * D + jb + j0;
 #pragma unroll
-        for (int x = 0; x < 16; ++x) dst[x] = __float2bfloat16_rn(cur[x]);
+        for (int x = 0; x < NX; ++x) dst[x] = __float2bfloat16_rn(cur[x]);
         __syncthreads();   // the previous segment's product is done with Ph and Ss
         {   // Phi_s into shared memory: 16 float4 per thread, all issued first
             constexpr int NV = D * D / 4 / CB_THREADS;
@@ -1555,22 +1557,22 @@ split_combine_kernel(const float *__restrict__ Nbuf, const float *__restrict__ P
             }
         }
 #pragma unroll
-        for (int x = 0; x < 16; ++x) Ss[i][j0 + x] = cur[x];
+        for (int x = 0; x < NX; ++x) Ss[i][j0 + x] = cur[x];
         __syncthreads();
         const float *ns = Nbuf + ((size_t)(b * P + sg) * H + h) * D * D + (size_t)i * D + jb + j0;
 #pragma unroll
-        for (int x = 0; x < 16; ++x) cur[x] = ns[x];
+        for (int x = 0; x < NX; ++x) cur[x] = ns[x];
 #pragma unroll 4
         for (int kk = 0; kk < D; ++kk) {
             const float f = Ph[i][kk];
 #pragma unroll
-            for (int x = 0; x < 16; ++x) cur[x] = fmaf(f, Ss[kk][j0 + x], cur[x]);
+            for (int x = 0; x < NX; ++x) cur[x] = fmaf(f, Ss[kk][j0 + x], cur[x]);
         }
     }
     if (S_T) {
         float *dst = S_T + ((size_t)unit * D + i) * D + jb + j0;
 #pragma unroll
-        for (int x = 0; x < 16; ++x) dst[x] = cur[x];
+        for (int x = 0; x < NX; ++x) dst[x] = cur[x];
     }
 }
 
@@ -2032,7 +2034,7 @@ cudaError_t launch_split_tail(const Problem &p0, const Problem &p, const TcParam
             return e;
         battr = true;
     }
-    split_combine_kernel<<<dim3((unsigned)(p0.n_seq * p0.H), D / 32), CB_THREADS, CB_SMEM, s>>>(
+    split_combine_kernel<<<dim3((unsigned)(p0.n_seq * p0.H), D / CBW), CB_THREADS, CB_SMEM, s>>>(
         tp.S_T, tp.S_T_phi, Sst, p0.S_T, p0.H, P, p0.status);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
