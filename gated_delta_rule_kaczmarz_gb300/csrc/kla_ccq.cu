@@ -11,13 +11,10 @@
 // is unchanged and the read is o_t = S_t q_clean_t, so the CCQ layer is the
 // KLA forward run on q_clean.
 //
-// bf16 inputs with d = 128 take the tensor cores: y_t = M_t q_t is a gated
-// delta-rule product with no decay whose chunk write is K^T K, so the chunked
-// tcgen05 forward runs it in its CCQ mode (W = 0, U~ = K: the state pass
-// gives y = Q M_prev + lower(Q K^T) K and carries M); then
-// whose first phase also writes the sum of each chunk's keys; then
-//   ccq_finish_kernel: per (chunk, sequence, head) m_prev from those sums, the
-//     running key sum m_t inside the chunk, n_t, mu_t . q_t and q_clean_t.
+// bf16 inputs with d = 128 take the tensor cores (section below): the query
+// streams blocks of 128 tokens through tcgen05 products (Q K^T, K^T K and
+// Q M + A' K) with the finish in the products' epilogue; M is carried in fp32
+// and enters its product with Q rounded to bf16.
 //
 // Other inputs: two passes on the CUDA cores, fp32 arithmetic:
 //   ccq_prefix_kernel: per (sequence, head, 16-row block of M) the chunks in
@@ -30,11 +27,15 @@
 //     m_t = m_prev + sum_{j<=t in chunk} k_j,  n_t = n_prev + t + 1
 //     q_clean_t = q_t - lambda_t (y_t / n_t - mu_t (mu_t . q_t))
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "kla_internal.h"
+#include "kla_tc.cuh"
 
 namespace kla {
 namespace {
@@ -198,218 +199,715 @@ ccq_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 }
 
 // ---- tensor-core path (bf16, D = 128) ----
-constexpr int TD = 128;
+//
+// Per (sequence, head) the tokens go in blocks of NB = 128.  With M_b, m_b
+// the statistics before block b and, for token t of the block,
+//   s_t = (m_t . q_t) / n_t = (m_b . q_t + sum_{s<=t} q_t . k_s) / n_t,
+//   M_t q_t - s_t m_t = (Q M_b)_t - s_t m_b + sum_{s<=t} (q_t . k_s - s_t) k_s,
+// so with G = Q K^T and A'_ts = G_ts - s_t for s <= t (0 above the diagonal)
+//   O = Q M_b + A' K,   q_clean_t = q_t - lambda_t / n_t (O_t - s_t m_b),
+// and M_{b+1} = M_b + K^T K, m_{b+1} = m_b + the block's key sums.  No product
+// waits for another block's output: the only carried quantities are M and m,
+// so the blocks stream through the tensor cores and the finish is the
+// products' epilogue.
+//
+// ccq_query_tc_kernel: one CTA per (sequence, head, segment); a loader warp
+// (TMA, two stages of Q and K), an MMA warp and sixteen main warps.  M lives
+// in TMEM (fp32): it starts as the initial statistics, and the K^T K of every
+// block before the segment is added first (the prefix: keys only, two blocks
+// per stage), then the segment's blocks in order.  Per block of the segment the MMA warp issues
+// G = Q K^T, then M += K^T K once the main warps have copied M_b to shared
+// memory (bf16), then O = Q M_b + A' K once they have written A' (bf16 pairs
+// in TMEM).  Main thread (row L, 32-column group cg) forms the row's part of
+// s_t and of A', finishes its part of row L of the previous block from O
+// (staged in shared memory, stored by TMA) and copies its part of row L of M
+// for the next block.  Segments are cut so that prefix and own blocks cost about the
+// same in every CTA (a prefix block, keys only, costs about a quarter of a
+// segment block).
+namespace ctc {
+constexpr int D = 128;
+constexpr int NB = 128;                        // tokens per block
+constexpr uint32_t SLAB = 128u * 128u;         // 128 rows x 64 bf16, 128-byte swizzle
+constexpr uint32_t TILE = 2u * SLAB;           // 128 x 128 bf16: two 64-column slabs
+constexpr int NST = 2;                         // stages: Q and K of one block each
+constexpr uint32_t ST_Q = 0, ST_K = TILE, ST_BYTES = 2u * TILE;
+constexpr uint32_t SM_M = NST * ST_BYTES;      // M_b (bf16; B operand of Q M_b)
+constexpr uint32_t SM_OUT = SM_M + TILE;       // q_clean of a block (bf16), stored by TMA
+constexpr uint32_t SM_F = SM_OUT + TILE;       // fp32 scratch:
+constexpr uint32_t F_M = 0;                    //   m of three blocks [3][D]
+constexpr int NMAIN = 16, THREADS = (NMAIN + 2) * 32;  // main warps: 4 lane quadrants x NCG
+constexpr int NCG = NMAIN / 4, CW = D / NCG;   // column groups, columns per main thread
+constexpr int RG = NMAIN * 32 / 16;            // token-row groups of the key sums
+constexpr uint32_t F_X = F_M + 3 * D;          //   row partials of s_t [NCG][NB]
+constexpr uint32_t F_C = F_X + NCG * NB;       //   key-sum partials of the row groups [RG][D]
+constexpr uint32_t F_END = F_C + RG * D;
+constexpr uint32_t SMEM = SM_F + F_END * 4 + 1024;   // + alignment slack
+// TMEM columns: G = Q K^T, the fp32 statistics M (K^T K adds into it), the
+// output product O, and A' (bf16 pairs) in two buffers of 64 columns
+constexpr uint32_t TM_G = 0, TM_M = 128, TM_O = 256, TM_A = 384;
+constexpr int P_MAX = 8;
+constexpr float PREFIX_COST = 0.25f;           // a prefix block against a segment block
+static_assert(SMEM <= 232448 - 1024, "shared memory of the CCQ kernel");
+}  // namespace ctc
 
-__device__ __forceinline__ void unpack8(const uint4 v, float *f) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-}
-
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-                 "l"(src)
-                 : "memory");
-}
-
-// grid (nch, B * H); 256 threads, three CTAs per SM.  Every load is issued up
-// front: q and y rows of the chunk go to shared memory by asynchronous copies
-// (16-byte piece pc of token row t at position pc ^ 4 (t & 1), so that the
-// two tokens read by eight consecutive lanes fall in different banks), the
-// keys through registers into an fp32 tile, and half of the key sums of the
-// preceding chunks for feature tid % 128 into registers.  Thread j < 128 then
-// turns key column j into the running sums m_t (from m before the chunk), and
-// thread (t = tid / 4, part = tid % 4) finishes token t on the pieces part +
-// 4 x.
-constexpr int FK_LD = TD + 4;   // fp32 key row stride: 16-byte aligned rows
-constexpr size_t FK_SMEM = (size_t)CC * FK_LD * 4 + 2 * (size_t)CC * TD * 2 + 2 * TD * 4;
-
-__global__ void __launch_bounds__(CQ_THREADS, 3)
-ccq_finish_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                  const __nv_bfloat16 *__restrict__ y, const float *__restrict__ lambda,
-                  const float *__restrict__ ms0, const float *__restrict__ ns0,
-                  const float *__restrict__ csum, int T, int H, int nch,
-                  __nv_bfloat16 *__restrict__ q_clean, float *__restrict__ ms_T,
-                  float *__restrict__ ns_T) {
-    extern __shared__ __align__(16) unsigned char fsm[];
-    float *Ks = reinterpret_cast<float *>(fsm);                        // [CC][FK_LD]
-    unsigned char *Qs = fsm + (size_t)CC * FK_LD * 4;                  // [CC][256 B]
-    unsigned char *Ys = Qs + (size_t)CC * TD * 2;                      // [CC][256 B]
-    float *mp = reinterpret_cast<float *>(Ys + (size_t)CC * TD * 2);   // [2][TD]
-    const int tid = threadIdx.x, c = blockIdx.x;
-    const long unit = blockIdx.y, b = unit / H, h = unit % H;
-    const size_t tok_stride = (size_t)H * TD;
-    const size_t base = ((size_t)b * T * H + h) * TD;   // token 0 of (b, h)
-
-    // piece e of the chunk: token e / 16, 16-byte piece e % 16
-    uint4 ka[4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-        const int e = tid + x * CQ_THREADS, te = e >> 4, pc = e & 15, kt = c * CC + te;
-        if (kt < T) {
-            const size_t o = base + (size_t)kt * tok_stride + pc * 8;
-            const int pos = te * 256 + ((pc ^ ((te & 1) << 2)) << 4);
-            cp_async16(Qs + pos, q + o);
-            cp_async16(Ys + pos, y + o);
-            ka[x] = *reinterpret_cast<const uint4 *>(k + o);
-        } else {
-            ka[x] = make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
-    // m before the chunk: the initial sum plus the preceding chunks' sums,
-    // chunks cc = half, half + 2, ... for this thread
-    const int j = tid & (TD - 1), half = tid >> 7;
-    const float *cs = csum + ((size_t)b * nch * H + h) * TD + j;   // chunk cc at cc * H * TD
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    int cc = half;
-    for (; cc + 6 < c; cc += 8) {
-        a0 += cs[(size_t)cc * H * TD];
-        a1 += cs[(size_t)(cc + 2) * H * TD];
-        a2 += cs[(size_t)(cc + 4) * H * TD];
-        a3 += cs[(size_t)(cc + 6) * H * TD];
-    }
-    for (; cc < c; cc += 2) a0 += cs[(size_t)cc * H * TD];
-    mp[half * TD + j] = (a0 + a1) + (a2 + a3) + (half == 0 && ms0 ? ms0[unit * TD + j] : 0.f);
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-        const int e = tid + x * CQ_THREADS;
-        float f[8];
-        unpack8(ka[x], f);
-        float4 *dst = reinterpret_cast<float4 *>(Ks + (e >> 4) * FK_LD + (e & 15) * 8);
-        dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-        dst[1] = make_float4(f[4], f[5], f[6], f[7]);
-    }
-    const int t = tid >> 2, part = tid & 3, tok = c * CC + t;
-    const bool live = tok < T;
-    const float lam = live ? lambda[((size_t)b * T + tok) * H + h] : 0.f;
-    const float n0 = ns0 ? ns0[unit] : 0.f;
-    __syncthreads();
-    if (tid < TD) {
-        float run = mp[tid] + mp[TD + tid];
-#pragma unroll
-        for (int t0 = 0; t0 < CC; t0 += 16) {
-            float v[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = Ks[(t0 + i) * FK_LD + tid];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                run += v[i];
-                Ks[(t0 + i) * FK_LD + tid] = run;
-            }
-        }
-        if (c == nch - 1 && ms_T) ms_T[unit * TD + tid] = run;
-    }
-    if (c == nch - 1 && tid == 0 && ns_T) ns_T[unit] = n0 + (float)T;
-    asm volatile("cp.async.wait_all;\n" ::: "memory");
-    __syncthreads();
-
-    const float inv_n = 1.f / (n0 + (float)(c * CC + t + 1));
-    const float *mrow = Ks + t * FK_LD;
-    const int sw = (t & 1) << 2;
-    float muq = 0.f;
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-        const int pc = part + 4 * x;
-        float qf[8];
-        unpack8(*reinterpret_cast<const uint4 *>(Qs + t * 256 + ((pc ^ sw) << 4)), qf);
-        const float4 m0 = *reinterpret_cast<const float4 *>(mrow + pc * 8);
-        const float4 m1 = *reinterpret_cast<const float4 *>(mrow + pc * 8 + 4);
-        muq = fmaf(m0.x, qf[0], muq); muq = fmaf(m0.y, qf[1], muq);
-        muq = fmaf(m0.z, qf[2], muq); muq = fmaf(m0.w, qf[3], muq);
-        muq = fmaf(m1.x, qf[4], muq); muq = fmaf(m1.y, qf[5], muq);
-        muq = fmaf(m1.z, qf[6], muq); muq = fmaf(m1.w, qf[7], muq);
-    }
-    muq *= inv_n;   // mu_t . q_t
-    muq += __shfl_xor_sync(0xffffffffu, muq, 1);
-    muq += __shfl_xor_sync(0xffffffffu, muq, 2);
-    if (live) {
-        const size_t o0 = base + (size_t)tok * tok_stride;
-        const float mscale = inv_n * muq;
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const int pc = part + 4 * x;
-            float qf[8], yf[8], mf[8];
-            unpack8(*reinterpret_cast<const uint4 *>(Qs + t * 256 + ((pc ^ sw) << 4)), qf);
-            unpack8(*reinterpret_cast<const uint4 *>(Ys + t * 256 + ((pc ^ sw) << 4)), yf);
-            const float4 m0 = *reinterpret_cast<const float4 *>(mrow + pc * 8);
-            const float4 m1 = *reinterpret_cast<const float4 *>(mrow + pc * 8 + 4);
-            mf[0] = m0.x; mf[1] = m0.y; mf[2] = m0.z; mf[3] = m0.w;
-            mf[4] = m1.x; mf[5] = m1.y; mf[6] = m1.z; mf[7] = m1.w;
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-                const float c0 = yf[i] * inv_n - mf[i] * mscale;
-                const float c1 = yf[i + 1] * inv_n - mf[i + 1] * mscale;
-                const __nv_bfloat162 o2 = __floats2bfloat162_rn(qf[i] - lam * c0,
-                                                                qf[i + 1] - lam * c1);
-                w[i / 2] = *reinterpret_cast<const uint32_t *>(&o2);
-            }
-            *reinterpret_cast<uint4 *>(q_clean + o0 + pc * 8) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    }
-}
-
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-bool ccq_use_tc(int B, int T, int d, int dtype) {
-    return chunk_tc_supported(d, dtype) && (long)B * T >= CC;
-}
-
-// Tensor-core workspace after the header: the chunked forward's workspace,
-// y [B, T, H, 128] bf16, the chunk key sums [B, nch, H, 128] fp32.
-struct CcqTcLayout {
-    size_t tc, y, csum, total;
+struct CcqTcParams {
+    const float *lambda, *Ms0, *ms0, *ns0;
+    float *Ms_T, *ms_T, *ns_T;
+    unsigned *status;
+    int T, H, P;
+    int seg_start[ctc::P_MAX + 1];   // first block of each segment; seg_start[P] = blocks
 };
-CcqTcLayout ccq_tc_layout(int B, int T, int H) {
-    const long nch = (T + CC - 1) / CC;
-    CcqTcLayout L;
-    L.tc = 0;
-    L.y = align_up(chunk_tc_workspace_bytes((long)B * nch, H, B), 256);
-    L.csum = align_up(L.y + (size_t)B * T * H * TD * 2, 256);
-    L.total = L.csum + (size_t)B * H * nch * TD * 4;
-    return L;
+
+__device__ __forceinline__ unsigned char *ccq_align1024(unsigned char *p) {
+    const uint32_t a = tc::smem_u32(p);
+    return p + ((1024u - (a & 1023u)) & 1023u);
+}
+__device__ __forceinline__ void ccq_set_status(unsigned *status, unsigned code) {
+    if (status) atomicCAS(status, 0u, code);
+}
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);   // a -> low half
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+// 16 fp32 values -> bf16 columns [c0, c0 + 16) of row `row` of a 64-column
+// slab stored with the 128-byte swizzle.
+__device__ __forceinline__ void st_row16(unsigned char *slab, int row, int c0, const uint32_t *r) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+        *reinterpret_cast<uint4 *>(slab + tc::sw128_offset(row, c0 + 8 * k)) =
+            make_uint4(pack_bf2(__uint_as_float(r[8 * k + 0]), __uint_as_float(r[8 * k + 1])),
+                       pack_bf2(__uint_as_float(r[8 * k + 2]), __uint_as_float(r[8 * k + 3])),
+                       pack_bf2(__uint_as_float(r[8 * k + 4]), __uint_as_float(r[8 * k + 5])),
+                       pack_bf2(__uint_as_float(r[8 * k + 6]), __uint_as_float(r[8 * k + 7])));
+}
+// Barrier over `count` threads that also returns the OR of `pred` over them
+// (the same answer in every thread).
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.b32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1 : 0), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+// Operand descriptors for the 128 x 128 tiles: K-major (rows of 64-element
+// slabs, the K step of 16 elements is 32 bytes inside a slab) and MN-major
+// (K step of 16 rows = 2048 bytes; the two 64-element MN halves one slab
+// apart).
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int ks) {
+    return tc::sdesc_sw128(base + (uint32_t)(ks >> 2) * ctc::SLAB + (uint32_t)(ks & 3) * 32u, 16,
+                           1024);
+}
+__device__ __forceinline__ uint64_t mdesc(uint32_t base, int ks) {
+    return tc::sdesc_sw128(base + (uint32_t)ks * 2048u, ctc::SLAB, 1024);
+}
+
+// The items a CTA loads, in order: the npre prefix blocks (keys only) two to
+// an item (the second block's keys in the stage's query half), then the
+// segment's nb blocks (queries and keys); item i uses stage i % NST.
+//
+// Block n of the segment, in order on the tensor pipe:
+//   G_{n+1} = Q K^T of the next block (once A'_n is in TMEM: G is read),
+//   M += K_n^T K_n (once the main warps have copied M_n to shared memory),
+//   O_n = Q M_n + A'_n K (A' from TMEM).
+// The main warps, for block n: s_t and A'_n from G_n, then (after O_{n-1})
+// the finish of block n - 1 and the copy of M_n; so A'_n is formed while
+// O_{n-1} runs and G_{n+1} runs while block n - 1 is finished.
+__global__ void __launch_bounds__(ctc::THREADS, 1)
+ccq_query_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                    const __grid_constant__ CUtensorMap mo, const CcqTcParams p) {
+    using namespace ctc;
+    using namespace tc;
+    extern __shared__ unsigned char ccq_smem[];
+    unsigned char *sm = ccq_align1024(ccq_smem);
+    __shared__ uint64_t bar_ld[NST], bar_empty[NST];
+    __shared__ uint64_t bar_init, bar_pre, bar_g, bar_o, bar_a, bar_m, bar_fin;
+    __shared__ uint32_t tslot;
+    __shared__ int sAbort;
+    unsigned char *sM = sm + SM_M, *sOut = sm + SM_OUT;
+    float *fm = reinterpret_cast<float *>(sm + SM_F) + F_M;
+    float *fx = reinterpret_cast<float *>(sm + SM_F) + F_X;
+    float *fc = reinterpret_cast<float *>(sm + SM_F) + F_C;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int unit = blockIdx.x / p.P, seg = blockIdx.x % p.P;
+    const int bq = unit / p.H, h = unit % p.H;
+    const int npre = p.seg_start[seg];                  // prefix blocks
+    const int npi = (npre + 1) / 2;                     // prefix items
+    const int nb = p.seg_start[seg + 1] - npre;         // the segment's blocks
+
+    if (tid == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&bar_ld[i], 1);
+            mbar_init(&bar_empty[i], NMAIN + 1);   // the main warps' reads and the products
+        }
+        mbar_init(&bar_init, NMAIN);   // initial M in TMEM
+        mbar_init(&bar_pre, 1);        // prefix products done
+        mbar_init(&bar_g, 1);
+        mbar_init(&bar_o, 1);
+        mbar_init(&bar_a, NMAIN);      // one arrival per main warp
+        mbar_init(&bar_m, NMAIN);
+        mbar_init(&bar_fin, 1);
+        fence_mbar_init();
+        sAbort = (p.status != nullptr && *(volatile const unsigned *)p.status != kDevOk) ? 1 : 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(&tslot, 512);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tslot;
+    const int pre_abort = sAbort;   // read by every thread before any can change it
+    __syncthreads();
+    if (pre_abort || nb <= 0) {
+        if (warp == 0) tmem_dealloc(tb, 512);
+        return;
+    }
+    auto fail = [&]() {
+        *(volatile int *)&sAbort = 1;   // read by the other warps' waits
+        ccq_set_status(p.status, kDevTimeout);
+    };
+
+    if (warp == NMAIN + 1) {
+        // ------------------------------------------------------------ loader
+        const int nitems = npi + nb;
+        int i = 0;
+        for (; i < nitems; ++i) {
+            const int s = i % NST, k = i / NST;
+            if (k >= 1 &&
+                !__all_sync(0xffffffffu,
+                            mbar_wait_or_abort(&bar_empty[s], (uint32_t)((k - 1) & 1), &sAbort))) {
+                fail();
+                break;
+            }
+            if (lane == 0) {
+                unsigned char *st = sm + s * ST_BYTES;
+                if (i >= npi) {   // block npre + (i - npi): queries and keys
+                    const int tok0 = (npre + i - npi) * NB;
+                    mbar_expect_tx(&bar_ld[s], 4u * 16384u);
+#pragma unroll
+                    for (int sl = 0; sl < 2; ++sl) {
+                        tma_load_4d(st + ST_Q + sl * SLAB, &mq, &bar_ld[s], 64 * sl, h, tok0, bq);
+                        tma_load_4d(st + ST_K + sl * SLAB, &mk, &bar_ld[s], 64 * sl, h, tok0, bq);
+                    }
+                } else {          // prefix blocks 2i and 2i + 1: keys only
+                    const bool two = 2 * i + 1 < npre;
+                    mbar_expect_tx(&bar_ld[s], (two ? 4u : 2u) * 16384u);
+#pragma unroll
+                    for (int sl = 0; sl < 2; ++sl) {
+                        tma_load_4d(st + ST_K + sl * SLAB, &mk, &bar_ld[s], 64 * sl, h, 2 * i * NB, bq);
+                        if (two)
+                            tma_load_4d(st + ST_Q + sl * SLAB, &mk, &bar_ld[s], 64 * sl, h,
+                                        (2 * i + 1) * NB, bq);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        // on an early exit the loads still in flight (one per stage at most)
+        // land before the CTA leaves
+        if (sAbort)
+            for (int k = i > NST ? i - NST : 0; k < i; ++k)
+                (void)mbar_wait(&bar_ld[k % NST], (uint32_t)((k / NST) & 1));
+    } else if (warp == NMAIN) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t id_g = idesc_bf16_f32(128, 128, false, false);
+        constexpr uint32_t id_z = idesc_bf16_f32(128, 128, true, true);
+        constexpr uint32_t id_o = idesc_bf16_f32(128, 128, false, true);
+        const uint32_t aM = smem_u32(sM);
+        auto aQ = [&](int i) { return smem_u32(sm + (i % NST) * ST_BYTES + ST_Q); };
+        auto aK = [&](int i) { return smem_u32(sm + (i % NST) * ST_BYTES + ST_K); };
+        // M += K^T K for the keys at shared address a (read MN-major for both operands)
+        auto issue_z = [&](uint32_t a) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tb + TM_M, mdesc(a, ks), mdesc(a, ks), id_z, 1);
+        };
+        // G = Q K^T (both K-major) of item i into TMEM
+        auto issue_g = [&](int i) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tb + TM_G, kdesc(aQ(i), ks), kdesc(aK(i), ks), id_g, ks > 0);
+            mma_commit(&bar_g);
+        };
+        bool ok = true;
+        // ---- prefix: the initial M is in TMEM, then K^T K of every block before the segment
+        if (npre > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bar_init, 0u, &sAbort));
+            for (int i = 0; ok && i < npi; ++i) {
+                ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bar_ld[i % NST],
+                                                                (uint32_t)((i / NST) & 1), &sAbort));
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    issue_z(aK(i));
+                    if (2 * i + 1 < npre) issue_z(aQ(i));
+                    mma_commit(&bar_empty[i % NST]);
+                }
+                __syncwarp();
+            }
+            if (ok && lane == 0) mma_commit(&bar_pre);
+            __syncwarp();
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bar_ld[npi % NST],
+                                                                (uint32_t)((npi / NST) & 1), &sAbort));
+        if (!ok) fail();
+        if (ok) {
+            tc_fence_after();
+            if (lane == 0) issue_g(npi);
+            __syncwarp();
+        }
+        for (int n = 0; ok && n < nb; ++n) {
+            const int i = npi + n;
+            // A'_n in TMEM (G_n read), and the next block landed: G_{n+1}
+            bool w = mbar_wait_or_abort(&bar_a, (uint32_t)(n & 1), &sAbort);
+            if (w && n + 1 < nb)
+                w = mbar_wait_or_abort(&bar_ld[(i + 1) % NST], (uint32_t)(((i + 1) / NST) & 1),
+                                       &sAbort);
+            if (!__all_sync(0xffffffffu, w)) { fail(); break; }
+            tc_fence_after();
+            if (lane == 0 && n + 1 < nb) issue_g(i + 1);
+            __syncwarp();
+            // M_n copied out of TMEM: M += K_n^T K_n; then O_n = Q M_n + A'_n K
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_m, (uint32_t)(n & 1), &sAbort))) {
+                fail();
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                issue_z(aK(i));
+                const uint32_t tA = tb + TM_A + 64u * (uint32_t)(n & 1);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(tb + TM_O, kdesc(aQ(i), ks), mdesc(aM, ks), id_o, ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ts(tb + TM_O, tA + 8u * (uint32_t)ks, mdesc(aK(i), ks), id_o, 1);
+                mma_commit(&bar_o);
+                mma_commit(&bar_empty[i % NST]);   // the stage may be refilled
+            }
+            __syncwarp();
+        }
+        // every MMA issued has completed before the CTA releases its TMEM
+        if (lane == 0) mma_commit(&bar_fin);
+        __syncwarp();
+        (void)mbar_wait(&bar_fin, 0u);
+    } else {
+        // ------------------------------------------------------------ main warps
+        const int L = (warp & 3) * 32 + lane;   // TMEM lane: token row / row of M
+        const int cg = warp >> 2, j0 = CW * cg; // column group: columns [j0, j0 + CW)
+        const int cs = j0 & 63;                 // first column inside its 64-column slab
+        unsigned char *const sMs = sM + (j0 >> 6) * SLAB;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tM = tb + lane_base + TM_M + (uint32_t)j0;
+        const float n0 = p.ns0 ? p.ns0[unit] : 0.f;
+        bool bad = false;            // a wait of this warp gave up
+        // ---- the initial statistics: M in TMEM (and, without a prefix, as
+        //      bf16 in shared memory for Q M_0)
+        {
+            const float *m0 = p.Ms0 ? p.Ms0 + ((size_t)unit * D + L) * D + j0 : nullptr;
+            const bool v4 = m0 && (reinterpret_cast<uintptr_t>(m0) & 15u) == 0;
+#pragma unroll 1
+            for (int c4 = 0; c4 < CW / 16; ++c4) {
+                uint32_t r[16];
+                if (v4) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 v = reinterpret_cast<const float4 *>(m0 + 16 * c4)[i];
+                        r[4 * i] = __float_as_uint(v.x); r[4 * i + 1] = __float_as_uint(v.y);
+                        r[4 * i + 2] = __float_as_uint(v.z); r[4 * i + 3] = __float_as_uint(v.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(m0 ? m0[16 * c4 + i] : 0.f);
+                }
+                tmem_st16(tM + 16 * c4, r);
+                if (npre == 0) st_row16(sMs, L, cs + 16 * c4, r);
+            }
+            tmem_st_wait();
+            if (npre == 0) fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(npre > 0 ? &bar_init : &bar_m);
+        }
+        // ---- the prefix: key sums of the blocks before the segment (the
+        //      products add their K^T K to M meanwhile)
+        const int kc = tid & 15, krg = tid >> 4;   // 16-byte piece (features 8kc..), row group
+        float ka[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // adds rows krg, krg + RG, ... of the key tile at `kt` (two slabs)
+        auto key_sums = [&](const unsigned char *kt) __attribute__((always_inline)) {
+            const unsigned char *kb = kt + (kc >> 3) * SLAB;
+#pragma unroll
+            for (int i = 0; i < NB / RG; ++i) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(kb + sw128_offset(krg + RG * i, 8 * (kc & 7)));
+                ka[0] += bf_lo(w.x); ka[1] += bf_hi(w.x); ka[2] += bf_lo(w.y); ka[3] += bf_hi(w.y);
+                ka[4] += bf_lo(w.z); ka[5] += bf_hi(w.z); ka[6] += bf_lo(w.w); ka[7] += bf_hi(w.w);
+            }
+        };
+        auto put_key_sums = [&]() __attribute__((always_inline)) {
+            float4 *dst = reinterpret_cast<float4 *>(fc + krg * D + 8 * kc);
+            dst[0] = make_float4(ka[0], ka[1], ka[2], ka[3]);
+            dst[1] = make_float4(ka[4], ka[5], ka[6], ka[7]);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) ka[x] = 0.f;
+        };
+        // the sum of the row groups' partials of feature tid (< D)
+        auto sum_key_sums = [&]() __attribute__((always_inline)) -> float {
+            float c0 = 0.f, c1 = 0.f;
+#pragma unroll
+            for (int g = 0; g < RG; g += 2) {
+                c0 += fc[g * D + tid];
+                c1 += fc[(g + 1) * D + tid];
+            }
+            return c0 + c1;
+        };
+        for (int i = 0; i < npi; ++i) {
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_ld[i % NST],
+                                                            (uint32_t)((i / NST) & 1), &sAbort))) {
+                bad = true;
+                fail();
+                break;
+            }
+            key_sums(sm + (i % NST) * ST_BYTES + ST_K);
+            if (2 * i + 1 < npre) key_sums(sm + (i % NST) * ST_BYTES + ST_Q);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_empty[i % NST]);
+        }
+        put_key_sums();
+        named_sync(1, NMAIN * 32);
+        if (tid < D) fm[tid] = (p.ms0 ? p.ms0[(size_t)unit * D + tid] : 0.f) + sum_key_sums();
+        if (npre > 0) {
+            // M_0 = the initial M plus the prefix's K^T K, to shared memory (bf16)
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_pre, 0u, &sAbort))) {
+                bad = true;
+                fail();
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c4 = 0; c4 < CW / 16; ++c4) {
+                uint32_t r[16];
+                tmem_ld16(tM + 16 * c4, r);
+                tmem_ld_wait();
+                st_row16(sMs, L, cs + 16 * c4, r);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_m);
+        }
+        // m_0 visible, the partials' rows free again
+        const bool stop0 = named_sync_or(1, NMAIN * 32, bad);
+
+        // what the finish of a block needs, carried to the next iteration
+        float sp = 0.f, scale = 0.f; // s_t, lambda_t / n_t
+        // q_clean of block n from O (TMEM) and q_t (registers), staged in
+        // shared memory and stored by TMA (rows past the sequence's end are
+        // not written)
+        auto finish = [&](int n, const uint4 (&qp)[CW / 8]) __attribute__((always_inline)) {
+            const uint32_t tO = tb + lane_base + TM_O + (uint32_t)j0;
+            const float4 *mb4 = reinterpret_cast<const float4 *>(fm + (n % 3) * D + j0);
+            unsigned char *so = sOut + (j0 >> 6) * SLAB;
+#pragma unroll
+            for (int c2 = 0; c2 < CW / 32; ++c2) {
+                uint32_t rr[2][16];
+                tmem_ld16(tO + 32 * c2, rr[0]);
+                tmem_ld16(tO + 32 * c2 + 16, rr[1]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c1 = 0; c1 < 2; ++c1) {
+                    const int c4 = 2 * c2 + c1;
+                    const uint32_t (&r)[16] = rr[c1];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const uint4 qk = qp[2 * c4 + k];
+                        const uint32_t qw[4] = {qk.x, qk.y, qk.z, qk.w};
+                        const float4 ma = mb4[4 * c4 + 2 * k], mc = mb4[4 * c4 + 2 * k + 1];
+                        const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mc.x, mc.y, mc.z, mc.w};
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int x = 8 * k + 2 * e;
+                            const float o0 = __uint_as_float(r[x]) - sp * mv[2 * e];
+                            const float o1 = __uint_as_float(r[x + 1]) - sp * mv[2 * e + 1];
+                            w[e] = pack_bf2(bf_lo(qw[e]) - scale * o0, bf_hi(qw[e]) - scale * o1);
+                        }
+                        *reinterpret_cast<uint4 *>(so + sw128_offset(L, cs + 16 * c4 + 8 * k)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+            fence_async_smem();
+            named_sync(3, NMAIN * 32);
+            if (tid == 0) {
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl)
+                    tma_store_4d(&mo, sOut + sl * SLAB, 64 * sl, h, (npre + n) * NB, bq);
+                bulk_commit_group();
+            }
+        };
+        // block n; qc receives q_t of block n, qp holds that of block n - 1.
+        // Returns true when the CTA gives up.
+        auto step = [&](int n, uint4 (&qc)[CW / 8], const uint4 (&qp)[CW / 8]) __attribute__((always_inline)) -> bool {
+            const int i = npi + n;
+            const unsigned char *st = sm + (i % NST) * ST_BYTES;
+            const int tok = (npre + n) * NB + L;
+            const float lam_n = tok < p.T ? p.lambda[((size_t)bq * p.T + tok) * p.H + h] : 0.f;
+            bool ok = mbar_wait_or_abort(&bar_ld[i % NST], (uint32_t)((i / NST) & 1), &sAbort) &&
+                      mbar_wait_or_abort(&bar_g, (uint32_t)(n & 1), &sAbort);
+            if (!__all_sync(0xffffffffu, ok)) {
+                bad = true;
+                fail();
+            }
+            tc_fence_after();
+            // ---- row part of s_t: sum_{s <= t} G_ts and m_b . q_t over the half
+            const float *mb = fm + (n % 3) * D;
+            float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+            for (int c2 = 0; c2 < CW / 32; ++c2) {
+                uint32_t r[2][16];
+                tmem_ld16(tb + lane_base + TM_G + j0 + 32 * c2, r[0]);
+                tmem_ld16(tb + lane_base + TM_G + j0 + 32 * c2 + 16, r[1]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    rs0 += (j0 + 32 * c2 + x <= L) ? __uint_as_float(r[0][x]) : 0.f;
+                    rs1 += (j0 + 32 * c2 + 16 + x <= L) ? __uint_as_float(r[1][x]) : 0.f;
+                }
+            }
+            float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+            for (int k = 0; k < CW / 8; ++k)
+                qc[k] = *reinterpret_cast<const uint4 *>(st + ST_Q + (j0 >> 6) * SLAB +
+                                                         sw128_offset(L, cs + 8 * k));
+#pragma unroll
+            for (int k = 0; k < CW / 8; ++k) {
+                const uint32_t qw[4] = {qc[k].x, qc[k].y, qc[k].z, qc[k].w};
+                const float4 ma = reinterpret_cast<const float4 *>(mb + j0)[2 * k];
+                const float4 mc = reinterpret_cast<const float4 *>(mb + j0)[2 * k + 1];
+                d0 = fmaf(ma.x, bf_lo(qw[0]), d0); d1 = fmaf(ma.y, bf_hi(qw[0]), d1);
+                d2 = fmaf(ma.z, bf_lo(qw[1]), d2); d3 = fmaf(ma.w, bf_hi(qw[1]), d3);
+                d0 = fmaf(mc.x, bf_lo(qw[2]), d0); d1 = fmaf(mc.y, bf_hi(qw[2]), d1);
+                d2 = fmaf(mc.z, bf_lo(qw[3]), d2); d3 = fmaf(mc.w, bf_hi(qw[3]), d3);
+            }
+            fx[cg * NB + L] = (rs0 + rs1) + ((d0 + d1) + (d2 + d3));
+            key_sums(st + ST_K);
+            put_key_sums();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_empty[i % NST]);   // the stage is read
+            // the q_clean store of block n - 2 has read its staging tile
+            if (tid == 0) bulk_wait_group_read0();
+            if (named_sync_or(1, NMAIN * 32, bad)) return true;
+            const float nt = n0 + (float)(tok + 1);
+            float xs = 0.f;
+#pragma unroll
+            for (int g = 0; g < NCG; ++g) xs += fx[g * NB + L];
+            const float spn = xs / nt;
+            if (tid < D) fm[((n + 1) % 3) * D + tid] = mb[tid] + sum_key_sums();
+            // ---- A'_n = G_ts - s_t for s <= t, else 0: bf16 pairs into TMEM
+            const uint32_t tA = tb + lane_base + TM_A + 64u * (uint32_t)(n & 1) + (uint32_t)(j0 / 2);
+#pragma unroll
+            for (int h2 = 0; h2 < CW / 32; ++h2) {
+                uint32_t w[16];
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t r[16];
+                    tmem_ld16(tb + lane_base + TM_G + j0 + 32 * h2 + 16 * c2, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int s0 = j0 + 32 * h2 + 16 * c2 + 2 * e;
+                        w[8 * c2 + e] = pack_bf2(s0 <= L ? __uint_as_float(r[2 * e]) - spn : 0.f,
+                                                 s0 + 1 <= L ? __uint_as_float(r[2 * e + 1]) - spn : 0.f);
+                    }
+                }
+                tmem_st16(tA + 16 * h2, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_a);
+            if (n > 0) {
+                // ---- block n - 1: finished from O_{n-1}; then M_n (Z_{n-1}
+                //      added) to shared memory for O_n
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_or_abort(&bar_o, (uint32_t)((n - 1) & 1), &sAbort))) {
+                    bad = true;
+                    fail();
+                }
+                tc_fence_after();
+                finish(n - 1, qp);
+#pragma unroll
+                for (int c4 = 0; c4 < CW / 16; ++c4) {
+                    uint32_t r[16];
+                    tmem_ld16(tM + 16 * c4, r);
+                    tmem_ld_wait();
+                    st_row16(sMs, L, cs + 16 * c4, r);
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_m);
+            }
+            sp = spn;
+            scale = lam_n / nt;
+            // the scratch rows (fx, fc) and m_{b+1} settle before the next block
+            return named_sync_or(2, NMAIN * 32, bad);
+        };
+
+        uint4 qa[CW / 8], qb[CW / 8];
+        bool stop = stop0;
+        for (int n = 0; !stop && n < nb; n += 2) {
+            if ((stop = step(n, qa, qb))) break;
+            if (n + 1 < nb && (stop = step(n + 1, qb, qa))) break;
+        }
+        const bool aborted = named_sync_or(1, NMAIN * 32, bad || stop);
+        if (!aborted) {
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait_or_abort(&bar_o, (uint32_t)((nb - 1) & 1), &sAbort)))
+                fail();
+            tc_fence_after();
+            if ((nb - 1) & 1) finish(nb - 1, qb); else finish(nb - 1, qa);
+            if (seg == p.P - 1) {
+                if (p.Ms_T) {
+                    float *dst = p.Ms_T + ((size_t)unit * D + L) * D + j0;
+                    const bool a16 = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
+#pragma unroll
+                    for (int c4 = 0; c4 < CW / 16; ++c4) {
+                        uint32_t r[16];
+                        tmem_ld16(tM + 16 * c4, r);
+                        tmem_ld_wait();
+                        if (a16) {
+#pragma unroll
+                            for (int x = 0; x < 4; ++x)
+                                reinterpret_cast<float4 *>(dst + 16 * c4)[x] =
+                                    make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
+                                                __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+                        } else {
+#pragma unroll
+                            for (int x = 0; x < 16; ++x) dst[16 * c4 + x] = __uint_as_float(r[x]);
+                        }
+                    }
+                }
+                if (p.ms_T && tid < D) p.ms_T[(size_t)unit * D + tid] = fm[(nb % 3) * D + tid];
+                if (p.ns_T && tid == 0) p.ns_T[unit] = n0 + (float)p.T;
+            }
+        }
+        if (tid == 0) bulk_wait_group0();   // the q_clean stores have completed
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+bool ccq_use_tc(int d, int dtype) { return chunk_tc_supported(d, dtype); }
+
+int ccq_sm_count() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+            n = v;
+        else
+            return 148;
+    }
+    return n;
+}
+
+// Segments per (sequence, head): up to one CTA per SM, at most P_MAX.  A
+// segment starting at block b0 with nb blocks costs PREFIX_COST b0 + nb; the
+// cut minimises the largest cost (bisection on it, each segment as long as
+// that cost allows).
+struct CcqTcPlan {
+    int P;
+    int start[ctc::P_MAX + 1];
+};
+CcqTcPlan ccq_tc_plan(int B, int T, int H) {
+    const int nblk = (T + ctc::NB - 1) / ctc::NB;
+    const long units = std::max(1L, (long)B * H);
+    const int Pmax = (int)std::max(1L, std::min({(long)ctc::P_MAX, ccq_sm_count() / units,
+                                                 (long)nblk}));
+    auto cut = [&](double c, CcqTcPlan &pl) {
+        int b0 = 0, s = 0;
+        pl.start[0] = 0;
+        while (b0 < nblk && s < Pmax) {
+            const int len = std::max(1, (int)(c - ctc::PREFIX_COST * b0 + 1e-9));
+            b0 = std::min(nblk, b0 + len);
+            pl.start[++s] = b0;
+        }
+        pl.P = s;
+        return b0 >= nblk;
+    };
+    CcqTcPlan pl{};
+    double lo = 0.0, hi = (double)nblk;
+    for (int it = 0; it < 40; ++it) {
+        const double mid = 0.5 * (lo + hi);
+        if (cut(mid, pl)) hi = mid; else lo = mid;
+    }
+    cut(hi, pl);
+    return pl;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 ccq_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        void *ptr = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// [B][T][H][128] bf16 as a 4-d tensor (feature, head, token, sequence); box
+// 64 features x 1 head x 128 tokens: tokens past T read as zero, and are not
+// written by a store.
+bool ccq_map(CUtensorMap *m, const void *base, int B, int T, int H) {
+    const cuuint64_t dims[4] = {(cuuint64_t)ctc::D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)ctc::D * 2, (cuuint64_t)H * ctc::D * 2,
+                                   (cuuint64_t)T * H * ctc::D * 2};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)ctc::NB, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return ccq_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                           strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t launch_ccq_tc(const CcqProblem &p, cudaStream_t s) {
-    const int nch = (p.T + CC - 1) / CC;
-    const CcqTcLayout L = ccq_tc_layout(p.B, p.T, p.H);
-    unsigned char *ws = static_cast<unsigned char *>(p.ws) + kWsHeader;
-    __nv_bfloat16 *yb = reinterpret_cast<__nv_bfloat16 *>(ws + L.y);
-    float *csum = reinterpret_cast<float *>(ws + L.csum);
-    // y = M_t q_t on the tensor cores: the chunked forward in its CCQ mode,
-    // with the statistics M as its state (v = k feeds only the unused V tile;
-    // eta, here lambda, is read but does not enter)
-    Problem f{};
-    f.q = p.q; f.k = p.k; f.v = p.k;
-    f.alpha = nullptr; f.eta = p.lambda; f.eps = 0.f;
-    f.S0 = p.Ms0; f.S_T = p.Ms_T; f.o = yb;
-    f.cu_seqlens = nullptr;
-    f.n_seq = p.B; f.T = p.T; f.total_T = p.B * p.T; f.H = p.H; f.d = TD; f.dtype = p.dtype;
-    f.beta_mode = 1; f.mode = 1; f.csum = csum;
-    f.status = static_cast<unsigned *>(p.ws);
-    f.ws = ws + L.tc;
-    f.ws_bytes = L.y - L.tc;
-    const long nchunks = (long)p.B * nch;
-    cudaError_t e = cudaMemsetAsync(p.ws, 0, kWsHeader + chunk_tc_reset_bytes(f, nchunks), s);
+    if (ccq_encode_fn() == nullptr) return cudaErrorNotSupported;
+    const CcqTcPlan pl = ccq_tc_plan(p.B, p.T, p.H);
+    const int units = p.B * p.H;
+    CcqTcParams prm{};
+    prm.lambda = p.lambda;
+    prm.Ms0 = p.Ms0; prm.ms0 = p.ms0; prm.ns0 = p.ns0;
+    prm.Ms_T = p.Ms_T; prm.ms_T = p.ms_T; prm.ns_T = p.ns_T;
+    prm.status = static_cast<unsigned *>(p.ws);
+    prm.T = p.T; prm.H = p.H; prm.P = pl.P;
+    for (int i = 0; i <= pl.P; ++i) prm.seg_start[i] = pl.start[i];
+    CUtensorMap mq, mk, mo;
+    if (!ccq_map(&mq, p.q, p.B, p.T, p.H) || !ccq_map(&mk, p.k, p.B, p.T, p.H) ||
+        !ccq_map(&mo, p.q_clean, p.B, p.T, p.H))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaMemsetAsync(p.ws, 0, sizeof(unsigned), s);   // status word
     if (e != cudaSuccess) return e;
-    if ((e = launch_chunk_tc(f, nchunks, s)) != cudaSuccess) return e;
-    static bool fattr = false;
-    if (!fattr) {
-        if ((e = cudaFuncSetAttribute(ccq_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)FK_SMEM)) != cudaSuccess)
+    static bool attrs = false;
+    if (!attrs) {
+        if ((e = cudaFuncSetAttribute(ccq_query_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)ctc::SMEM)) != cudaSuccess)
             return e;
-        fattr = true;
+        attrs = true;
     }
-    const dim3 grid(nch, p.B * p.H);
-    ccq_finish_kernel<<<grid, CQ_THREADS, FK_SMEM, s>>>(
-        static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k), yb,
-        p.lambda, p.ms0, p.ns0, csum, p.T, p.H, nch, static_cast<__nv_bfloat16 *>(p.q_clean),
-        p.ms_T, p.ns_T);
+    ccq_query_tc_kernel<<<units * pl.P, ctc::THREADS, ctc::SMEM, s>>>(mq, mk, mo, prm);
     note_launch();
     return cudaGetLastError();
 }
@@ -510,7 +1008,7 @@ cudaError_t launch_ccq_step(const void *q, const void *k, const float *lambda, f
 }
 
 size_t ccq_workspace_bytes(int B, int T, int H, int d, int dtype) {
-    if (ccq_use_tc(B, T, d, dtype)) return kWsHeader + ccq_tc_layout(B, T, H).total;
+    if (ccq_use_tc(d, dtype)) return kWsHeader;   // the status word only
     const size_t nch = (size_t)(T + CC - 1) / CC;
     const size_t es = dtype == 1 ? 2 : 4;
     return kWsHeader + (size_t)B * H * nch * ((size_t)d * d * es + (size_t)d * 4);
@@ -518,7 +1016,7 @@ size_t ccq_workspace_bytes(int B, int T, int H, int d, int dtype) {
 
 cudaError_t launch_ccq(const CcqProblem &p, cudaStream_t s) {
     if (p.B == 0 || p.T == 0) return cudaSuccess;
-    if (ccq_use_tc(p.B, p.T, p.d, p.dtype)) return launch_ccq_tc(p, s);
+    if (ccq_use_tc(p.d, p.dtype)) return launch_ccq_tc(p, s);
     if (p.dtype == 1)
         return p.d == 128 ? launch_ccq_t<__nv_bfloat16, 128>(p, s)
                           : launch_ccq_t<__nv_bfloat16, 64>(p, s);

@@ -71,8 +71,6 @@ struct TcParams {
     __nv_bfloat16 *U_ws;       // [slots][64][128]   U~
     __nv_bfloat16 *A_ws;       // [slots][64 keys s][64 queries t]  A^T
     int beta_mode;             // 0: beta = eta / (||k||^2 + eps); 1: beta = eta
-    int mode;                  // 0: KLA; 1: the CCQ product (W = 0, U~ = K, no decay)
-    float *csum;               // CCQ mode: [slots][128] the sum of each chunk's keys
     // Sequence split (fixed length): every sequence is run as seg_P virtual
     // sequences of T / seg_P tokens.  State CTAs [0, phi_first) run the state
     // pass of the virtual sequences (S0 only for the first segment); CTAs from
@@ -389,8 +387,7 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     if (tid == 0) {
         bulk_wait_group_read0();   // the previous item's W / U~ stores have left shared memory
         // K and Q first (the Gram products need them); V, needed only by the
-        // U~ product, on its own barrier behind them (not at all in the CCQ
-        // mode, which stores a zero tile from the V region)
+        // U~ product, on its own barrier behind them
         mbar_expect_tx(&bars[0], 2u * 32768u);
 #pragma unroll 1
         for (int q = 0; q < 2; ++q)
@@ -400,15 +397,13 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
                 tma_load_3d(KQ + s * 32768 + q * 8192, mk, &bars[0], 64 * s, h, z);
                 tma_load_3d(KQ + s * 32768 + 16384 + q * 8192, mq, &bars[0], 64 * s, h, z);
             }
-        if (p.mode == 0) {
-            mbar_expect_tx(&bars[3], 32768u);
+        mbar_expect_tx(&bars[3], 32768u);
 #pragma unroll 1
-            for (int q = 0; q < 2; ++q)
+        for (int q = 0; q < 2; ++q)
 #pragma unroll 1
-                for (int s = 0; s < 2; ++s)
-                    tma_load_3d(sV + s * 16384 + q * 8192, mv, &bars[3], 64 * s, h,
-                                (int)(q ? r01 : r00));
-        }
+            for (int s = 0; s < 2; ++s)
+                tma_load_3d(sV + s * 16384 + q * 8192, mv, &bars[3], 64 * s, h,
+                            (int)(q ? r01 : r00));
         if (kFused && pending >= 0) {   // the previous item's outputs are complete
             bulk_wait_group0();
             fence_proxy_async_global();
@@ -586,55 +581,6 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     const bool abort2 = *sAbort != 0;
     if (first && stagger && stagger_role == 1 && tid == 0) *stagger = 1;
     first = false;
-
-    if (p.mode == 1) {
-        // ---- the CCQ product y_t = M_t q_t: with W = 0, U~ = K, g = 0 and
-        //      A = lower(Q K^T) the state pass computes y = Q M_prev + A K
-        //      and M <- M + K^T K.  K (decayed by exp(0) = 1, tails cleared) is
-        //      stored as U~; the V region, zeroed, as W.  Thread (chunk tid /
-        //      128, feature tid % 128) also sums its feature over the chunk ----
-        {
-            const int j = tid & 127, sl = tid >> 7;
-            const unsigned char *kb = KQ + (j >> 6) * 32768;
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-            for (int u = 0; u < 64; u += 2) {
-                s0 += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                    kb + sw128_offset(sl * 64 + u, j & 63)));
-                s1 += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                    kb + sw128_offset(sl * 64 + u + 1, j & 63)));
-            }
-            if ((sl ? v1 : v0) && !abort2)
-                p.csum[((2L * pair + sl) * p.H + h) * D + j] = s0 + s1;
-        }
-#pragma unroll 2
-        for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4 *>(sV + hf * 16384 + sw128_offset(r, ch * 8)) =
-                make_uint4(0u, 0u, 0u, 0u);
-        if (hf == 0 && vslot && !abort2) p.g_ws[slot_row] = 0.f;
-        if (kFused) __threadfence();
-        fence_async_smem();
-        named_sync(bar, P1_THREADS);
-        if (tid == 0 && !abort2) {
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                if (!(q ? v1 : v0)) continue;
-                const int y = (int)(((2L * pair + q) * p.H + h) * C);
-#pragma unroll
-                for (int s = 0; s < 2; ++s) {
-                    tma_store_2d(mw, sV + s * 16384 + q * 8192, 64 * s, y);
-                    tma_store_2d(mu, KQ + s * 32768 + q * 8192, 64 * s, y);
-                }
-            }
-            bulk_commit_group();
-            if (kFused) pending = item;
-        }
-        tc_fence_before();
-        named_sync(bar, P1_THREADS);   // smem and TMEM free for the next item
-        ph ^= 1u;                      // (bars[2] is not used in this mode)
-        if (*sAbort) break;
-        continue;
-    }
 
     // ---- T = (I + L)^{-1}, built up in block sizes 16 -> 32 -> 64: the
     //      diagonal 16 x 16 blocks by forward substitution (first half of the
@@ -1813,7 +1759,7 @@ SplitLayout split_layout(int n_seq, int T, int H, int P) {
 // phase 1 its items arrive more slowly than the chain consumes them.
 bool use_fused(const Problem &p) {
     if (p.cu_seqlens != nullptr || p.T <= 0) return false;
-    const int P = p.mode == 0 ? split_factor(p.n_seq, p.T, p.H, false) : 1;
+    const int P = split_factor(p.n_seq, p.T, p.H, false);
     const int nch = (p.T / P + C - 1) / C;
     if (nch % 2 != 0) return false;
     return 2 * split_chains((long)p.n_seq * p.H, P) <= sm_count() / 2;
@@ -1868,11 +1814,9 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     if (p0.n_seq == 0) return cudaSuccess;
     if (encode_fn() == nullptr) return cudaErrorNotSupported;
     // a split sequence runs as P virtual sequences of T / P tokens (same rows,
-    // same chunk slots); the CCQ mode does not split
+    // same chunk slots)
     const bool record = p0.S_chk != nullptr;   // backward recording: two launches, no split
-    const int P = (p0.mode == 0 && !record)
-                      ? split_factor(p0.n_seq, p0.T, p0.H, p0.cu_seqlens != nullptr)
-                      : 1;
+    const int P = !record ? split_factor(p0.n_seq, p0.T, p0.H, p0.cu_seqlens != nullptr) : 1;
     Problem p = p0;
     if (P > 1) {
         p.n_seq = p0.n_seq * P;
@@ -1892,8 +1836,6 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     tp.nch_fixed = p.cu_seqlens ? 0 : (p.T + C - 1) / C;
     tp.eps = p.eps;
     tp.beta_mode = p.beta_mode;
-    tp.mode = p.mode;
-    tp.csum = p.csum;
     tp.seg_P = P;
     tp.alpha = p.alpha;
     tp.eta = p.eta;

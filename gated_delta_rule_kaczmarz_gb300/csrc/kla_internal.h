@@ -36,9 +36,6 @@ struct Problem {
     int H, d;                // heads, dk == dv
     int dtype;               // kla_dtype
     int beta_mode;           // 0: beta = eta / (||k||^2 + eps); 1: beta = eta
-    int mode;                // 0: KLA; 1: the CCQ product y = M_t q (tensor-core path only)
-    float *csum;             // mode 1: [chunk slots][d] per-chunk key sums (fixed length:
-                             // slot (b * n_chunks + c) * H + h)
     float *S_chk;            // the state at every chunk start for the backward pass
                              // ([chunk slots, d, d] fp32, slot = chunk * H + head), or nullptr
     const int *chunk_prefix; // CUDA-core varlen recording: first chunk of each sequence

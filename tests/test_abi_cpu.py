@@ -175,8 +175,8 @@ def test_ccq_host_validation():
              ctypes.c_void_p(0x10010), 1 << 30, None) == binding.KLA_ERR_INVALID_ARG
     assert "aligned" in lib.kla_last_error_message().decode()
     assert lib.kla_ccq_query_workspace_size(1, 64, 1, 64, 1) > 0
-    # the tensor-core layout (bf16, dk 128) holds at least y and the chunk key sums
-    assert lib.kla_ccq_query_workspace_size(2, 256, 2, 128, 1) >= 2 * 256 * 2 * 128 * 2 + 2 * 2 * 4 * 128 * 4
+    # the tensor-core path (bf16, dk 128) keeps nothing but the status word
+    assert lib.kla_ccq_query_workspace_size(2, 256, 2, 128, 1) == 256
     g = lib.kla_ccq_query_step
     assert g(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 2, 2, 64, 1, None) == \
         binding.KLA_ERR_INVALID_ARG

@@ -31,8 +31,8 @@ def _stats(B, H, d, seed):
 @pytest.mark.parametrize("B,T,H,d,dtype,with_stats", [
     (2, 200, 2, 64, "fp32", False), (1, 130, 2, 128, "fp32", True),
     (2, 257, 2, 128, "bf16", False), (1, 64, 3, 128, "bf16", True), (2, 1, 2, 64, "bf16", True),
-    # tensor-core path: fused launch (even chunk count), two launches (odd),
-    # sequences shorter than a chunk (B*T >= 64)
+    # tensor-core path: whole and ragged 128-token blocks, several segments
+    # per sequence, sequences shorter than a block
     (2, 256, 2, 128, "bf16", True), (3, 448, 2, 128, "bf16", False), (1, 323, 5, 128, "bf16", True),
     (80, 1, 1, 128, "bf16", True), (3, 40, 2, 128, "bf16", False)])
 def test_ccq_query_parity(B, T, H, d, dtype, with_stats):
@@ -87,26 +87,31 @@ def test_ccq_step_equals_prefill(d, dtype):
     assert np.array_equal(ns.cpu().numpy(), ns_ref)
 
 
-@pytest.mark.parametrize("T,launches", [(256, 2), (320, 3)])
-def test_ccq_tensor_core_launches(T, launches):
-    """bf16 dk 128 runs the chunked tcgen05 forward in its CCQ mode (one fused
-    launch for an even chunk count, two otherwise; it also sums each chunk's
-    keys) plus the finish kernel; the status word in the workspace stays 0."""
-    B, H, d = 2, 2, 128
+@pytest.mark.parametrize("B,T,H", [(2, 256, 2), (2, 320, 2), (40, 256, 4), (1, 2048, 2)])
+def test_ccq_tensor_core_launches(B, T, H):
+    """bf16 dk 128 streams 128-token blocks through the tensor cores in one
+    launch: with few (sequence, head) pairs each sequence is cut into segments
+    whose CTAs first add the K^T K of the blocks before them; the status word
+    in the workspace stays 0 and the statistics are exact."""
+    d = 128
     inp = prefill_inputs(B, T, H, d, d, "bf16", seed=150)
     lam = _lam((B, T, H), 12)
+    st0 = _stats(B, H, d, 15)
     g = cuda(inp)
     ws = torch.zeros(kla.kla_ccq_query_workspace_size(B, T, H, d), dtype=torch.uint8,
                      device="cuda")
-    kla.kla_ccq_query(g["q"], g["k"], lam.cuda(), workspace=ws)   # first call sets attributes
+    stats = tuple(x.cuda() for x in st0)
+    kla.kla_ccq_query(g["q"], g["k"], lam.cuda(), stats, workspace=ws)   # sets attributes
     torch.cuda.synchronize()
     n0 = kla.kla_launch_count()
-    qc, _ = kla.kla_ccq_query(g["q"], g["k"], lam.cuda(), workspace=ws)
+    qc, (Ms, ms, ns) = kla.kla_ccq_query(g["q"], g["k"], lam.cuda(), stats, workspace=ws)
     torch.cuda.synchronize()
-    assert kla.kla_launch_count() - n0 == launches
+    assert kla.kla_launch_count() - n0 == 1
     assert kla.kla_workspace_status(ws) == 0
-    qc_ref, _ = oracle.ccq_query(inp["q"], inp["k"], lam)
+    qc_ref, (Ms_ref, ms_ref, ns_ref) = oracle.ccq_query(inp["q"], inp["k"], lam, st0)
     assert rel_err(qc, qc_ref) <= TOL[inp["q"].dtype]
+    assert rel_err(Ms, Ms_ref) <= 1e-5 and rel_err(ms, ms_ref) <= 1e-5
+    assert np.array_equal(ns.cpu().numpy(), ns_ref)
 
 
 def test_ccq_full_size_sampled():

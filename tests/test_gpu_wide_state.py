@@ -2,8 +2,8 @@
 head) in the two-launch forward, chosen when two 64-column CTAs per head
 would outnumber the SMs) against the fp64 oracle, error max|gpu - oracle| /
 max|oracle| <= 2e-2 (bf16).  KLA_WIDE_STATE=1 forces it on small cases; the
-forward, the varlen forward, the backward's state recording and the CCQ mode
-all run through it."""
+forward, the varlen forward and the backward's state recording run through
+it."""
 import numpy as np
 import pytest
 import torch
@@ -91,17 +91,3 @@ def test_wide_backward_parity(wide):
                           inp["S0"], do, dST, nthreads=8)
     for name, a, b in zip(("dq", "dk", "dv", "dalpha", "deta", "dS0"), got, ref):
         assert rel_err(a, b) <= 2e-2, name
-
-
-def test_wide_ccq_parity(wide):
-    wide(True)
-    B, T, H = 2, 448, 2
-    inp = prefill_inputs(B, T, H, 128, 128, "bf16", seed=75)
-    rng = np.random.default_rng(76)
-    lam = torch.from_numpy((1.0 / (1.0 + np.exp(-rng.standard_normal((B, T, H))))).astype(np.float32))
-    g = cuda(inp)
-    qc, (Ms, ms, ns) = kla.kla_ccq_query(g["q"], g["k"], lam.cuda())
-    torch.cuda.synchronize()
-    qc_ref, (Ms_ref, ms_ref, ns_ref) = oracle.ccq_query(inp["q"], inp["k"], lam)
-    assert rel_err(qc, qc_ref) <= 2e-2
-    assert rel_err(Ms, Ms_ref) <= 1e-5
