@@ -238,9 +238,11 @@ constexpr uint32_t F_M = 0;                    //   m of three blocks [3][D]
 constexpr int NMAIN = 16, THREADS = (NMAIN + 2) * 32;  // main warps: 4 lane quadrants x NCG
 constexpr int NCG = NMAIN / 4, CW = D / NCG;   // column groups, columns per main thread
 constexpr int RG = NMAIN * 32 / 16;            // token-row groups of the key sums
+constexpr int FC_LD = D + 8;                   // row stride of the key-sum partials (the
+                                               // four lanes of a feature hit four bank groups)
 constexpr uint32_t F_X = F_M + 3 * D;          //   row partials of s_t [NCG][NB]
-constexpr uint32_t F_C = F_X + NCG * NB;       //   key-sum partials of the row groups [RG][D]
-constexpr uint32_t F_END = F_C + RG * D;
+constexpr uint32_t F_C = F_X + NCG * NB;       //   key-sum partials, row groups paired [RG / 2][FC_LD]
+constexpr uint32_t F_END = F_C + RG / 2 * FC_LD;
 constexpr uint32_t SMEM = SM_F + F_END * 4 + 1024;   // + alignment slack
 // TMEM columns: G = Q K^T, the fp32 statistics M (K^T K adds into it), the
 // output product O, and A' (bf16 pairs) in two buffers of 64 columns
@@ -551,22 +553,30 @@ ccq_query_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
                 ka[4] += bf_lo(w.z); ka[5] += bf_hi(w.z); ka[6] += bf_lo(w.w); ka[7] += bf_hi(w.w);
             }
         };
+        // row groups krg and krg ^ 1 (lanes l and l ^ 16) combined by a shuffle,
+        // then one partial row per pair
         auto put_key_sums = [&]() __attribute__((always_inline)) {
-            float4 *dst = reinterpret_cast<float4 *>(fc + krg * D + 8 * kc);
-            dst[0] = make_float4(ka[0], ka[1], ka[2], ka[3]);
-            dst[1] = make_float4(ka[4], ka[5], ka[6], ka[7]);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) ka[x] += __shfl_xor_sync(0xffffffffu, ka[x], 16);
+            if ((krg & 1) == 0) {
+                float4 *dst = reinterpret_cast<float4 *>(fc + (krg >> 1) * FC_LD + 8 * kc);
+                dst[0] = make_float4(ka[0], ka[1], ka[2], ka[3]);
+                dst[1] = make_float4(ka[4], ka[5], ka[6], ka[7]);
+            }
 #pragma unroll
             for (int x = 0; x < 8; ++x) ka[x] = 0.f;
         };
-        // the sum of the row groups' partials of feature tid (< D)
+        // the sum over the partial rows of feature tid >> 2, by the four lanes
+        // tid & ~3 .. tid | 3 (lane part: rows part, part + 4, ...); every main
+        // thread calls it
         auto sum_key_sums = [&]() __attribute__((always_inline)) -> float {
-            float c0 = 0.f, c1 = 0.f;
+            const int f = tid >> 2, part = tid & 3;
+            float c = 0.f;
 #pragma unroll
-            for (int g = 0; g < RG; g += 2) {
-                c0 += fc[g * D + tid];
-                c1 += fc[(g + 1) * D + tid];
-            }
-            return c0 + c1;
+            for (int g = 0; g < RG / 8; ++g) c += fc[(part + 4 * g) * FC_LD + f];
+            c += __shfl_xor_sync(0xffffffffu, c, 1);
+            c += __shfl_xor_sync(0xffffffffu, c, 2);
+            return c;
         };
         for (int i = 0; i < npi; ++i) {
             if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_ld[i % NST],
@@ -582,7 +592,11 @@ ccq_query_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         }
         put_key_sums();
         named_sync(1, NMAIN * 32);
-        if (tid < D) fm[tid] = (p.ms0 ? p.ms0[(size_t)unit * D + tid] : 0.f) + sum_key_sums();
+        {
+            const float c = sum_key_sums();
+            if (tid < 4 * D && (tid & 3) == 0)
+                fm[tid >> 2] = (p.ms0 ? p.ms0[(size_t)unit * D + (tid >> 2)] : 0.f) + c;
+        }
         if (npre > 0) {
             // M_0 = the initial M plus the prefix's K^T K, to shared memory (bf16)
             if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_pre, 0u, &sAbort))) {
@@ -709,7 +723,10 @@ ccq_query_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
 #pragma unroll
             for (int g = 0; g < NCG; ++g) xs += fx[g * NB + L];
             const float spn = xs / nt;
-            if (tid < D) fm[((n + 1) % 3) * D + tid] = mb[tid] + sum_key_sums();
+            {
+                const float c = sum_key_sums();
+                if (tid < 4 * D && (tid & 3) == 0) fm[((n + 1) % 3) * D + (tid >> 2)] = mb[tid >> 2] + c;
+            }
             // ---- A'_n = G_ts - s_t for s <= t, else 0: bf16 pairs into TMEM
             const uint32_t tA = tb + lane_base + TM_A + 64u * (uint32_t)(n & 1) + (uint32_t)(j0 / 2);
 #pragma unroll

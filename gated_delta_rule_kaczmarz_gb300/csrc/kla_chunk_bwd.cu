@@ -40,6 +40,8 @@
 #include "kla_internal.h"
 #include "kla_simt_inverse.cuh"
 #include "kla_simt_tile.cuh"
+#include "kla_tc.cuh"
+#include "kla_tmap.h"
 
 namespace kla {
 namespace {
@@ -281,181 +283,366 @@ __global__ void __launch_bounds__(NT, 1) bwd_dstate_kernel(BwdProblem p, float *
     }
 }
 
-// dS chain for bf16, d = 128 from the tensor-core forward's chunk workspace:
-// W = T diag(beta exp g) K (bf16), A^T (bf16, row = key, column = query) and g
-// of every chunk, so that the chain needs no Gram product and no inverse:
+// dS chain for bf16, d = 128 on the tensor cores, from the tensor-core
+// forward's chunk workspace: W = T diag(beta exp g) K (bf16), A^T (bf16,
+// row = key, column = query) and g of every chunk, so that the chain needs no
+// Gram product and no inverse:
 //   dU = A_qk^T dO + diag(exp(g_C - g)) K dS'
 //   dS = exp(g_C) dS' + Q^T diag(exp g) dO - W^T dU
-// Row strides are multiples of 4 floats (float4 operands) offset from 32 banks.
-struct DsTcSmem {
-    float K[C][132], Q[C][132], W[C][132];
-    float At[C][C + 4];
-    float dS[128][DVB + 4];
-    float dO[C][DVB + 4], dU[C][DVB + 4];
-    float g[C], eg[C], egc[C];
-    // the next chunk's tiles as they arrive (bf16, cp.async), converted at the
-    // start of its iteration
-    __nv_bfloat16 Kb[C][128], Qb[C][128], Wb[C][128], Ab[C][C], dOb[C][DVB];
-    float gb[C];
-};
+// One CTA per (sequence, head), transposed so that the 128 value columns j of
+// dS are the rows of every product (one per TMEM lane):
+//   X = dS'^T K^T,  Y = dO^T A_qk            (128 x 64: column t a token)
+//   dU^T = X diag(exp(g_C - g)) + Y          (bf16 into TMEM: an MMA operand)
+//   D = dO^T diag(exp g) Q - dU^T W          (128 x 128)
+//   dS^T <- exp(g_C) dS'^T + D               (fp32 registers)
+// The serial chain per chunk is X -> dU -> D -> dS'; Y and the Q half of D
+// depend on the chunk's inputs only and are issued ahead.  A loader warp
+// brings each chunk's K, Q, dO (token rows), W and A^T (workspace) by TMA,
+// two chunks in flight; an MMA warp issues the products; eight main warps
+// hold the state, thread (lane j, half hf) the columns i in [64 hf, 64 hf + 64)
+// of row j of dS^T (so that the recorded dS' rows, fixed i, are written by
+// a warp as 32 consecutive floats).
+namespace dtc {
+constexpr int D = 128;
+constexpr int NS = 2;                                // stages
+constexpr uint32_t T64 = 64u * 128u;                 // 64 rows x 64 bf16 (one slab)
+constexpr uint32_t ST_K = 0, ST_Q = 2 * T64, ST_O = 4 * T64, ST_W = 6 * T64, ST_A = 8 * T64;
+constexpr uint32_t ST_BYTES = 9 * T64;               // K, Q, dO, W (two slabs each), A^T
+constexpr uint32_t ST_TX = ST_BYTES;                 // + g (bulk copy, 256 B)
+constexpr uint32_t SM_S = NS * ST_BYTES;             // dS'^T (bf16, 128 x 128, K-major)
+constexpr uint32_t SM_G = SM_S + 2 * 128u * 128u;    // g of each stage [NS][64]
+constexpr uint32_t SM_E = SM_G + NS * 256;           // exp g, exp(g_C - g) of each stage [NS][2][64]
+constexpr uint32_t SMEM = SM_E + NS * 512 + 1024;
+constexpr int NMAIN = 8, THREADS = (NMAIN + 2) * 32;
+constexpr uint32_t TM_X = 0, TM_Y = 64, TM_U = 128, TM_D = 256;   // D: two buffers of 128
+static_assert(SMEM <= 232448, "dS chain shared memory");
+}  // namespace dtc
 
-__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-                 "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
+__device__ __forceinline__ unsigned char *dtc_align1024(unsigned char *p) {
+    const uint32_t a = tc::smem_u32(p);
+    return p + ((1024u - (a & 1023u)) & 1023u);
+}
+__device__ __forceinline__ uint32_t dtc_pack(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);   // a -> low half
+    return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// Issues the asynchronous copies of chunk c's tiles into the staging arrays
-// (rows past the sequence end are zero filled).
-__device__ __forceinline__ void ds_prefetch(DsTcSmem &sm, const BwdProblem &p, int c,
-                                            const SeqGeo &sg, int h, int jb, const float *g_ws,
-                                            const __nv_bfloat16 *W_ws,
-                                            const __nv_bfloat16 *A_ws, int tid) {
-    constexpr int D = 128;
-    const long row0 = sg.start + (long)c * C;
-    const int nc = min(C, sg.len - c * C);
-    const long slot = (sg.chunk0 + c) * p.H + h;
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
-    const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(p.dout);
-    for (int e = tid; e < C * 16; e += NT) {   // K, Q, W: 16 pieces of 16 B per row
-        const int t = e >> 4, pc = e & 15;
-        const bool ok = t < nc;
-        const size_t src = ((size_t)(row0 + (ok ? t : 0)) * p.H + h) * D + pc * 8;
-        cp_async16_zfill(&sm.Kb[t][pc * 8], k + src, ok);
-        cp_async16_zfill(&sm.Qb[t][pc * 8], q + src, ok);
-        cp_async16_zfill(&sm.Wb[t][pc * 8], W_ws + ((size_t)slot * C + t) * D + pc * 8, true);
-    }
-    for (int e = tid; e < C * 8; e += NT) {    // A^T: 8 pieces per row
-        const int t = e >> 3, pc = e & 7;
-        cp_async16_zfill(&sm.Ab[t][pc * 8], A_ws + ((size_t)slot * C + t) * C + pc * 8, true);
-    }
-    for (int e = tid; e < C * (DVB / 8); e += NT) {   // dO columns [jb, jb + 32): 4 pieces per row
-        const int t = e >> 2, pc = e & 3;
-        const bool ok = t < nc;
-        cp_async16_zfill(&sm.dOb[t][pc * 8],
-                         dout + ((size_t)(row0 + (ok ? t : 0)) * p.H + h) * D + jb + pc * 8, ok);
-    }
-    if (tid < C / 4)
-        cp_async16_zfill(&sm.gb[tid * 4], g_ws + (size_t)slot * C + tid * 4, true);
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
+__global__ void __launch_bounds__(dtc::THREADS, 1)
+bwd_dstate_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                     const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mw,
+                     const __grid_constant__ CUtensorMap ma, BwdProblem p, float *dS_chk,
+                     const float *g_ws) {
+    using namespace dtc;
+    using namespace tc;
+    extern __shared__ unsigned char dtc_smem[];
+    unsigned char *sm = dtc_align1024(dtc_smem);
+    __shared__ uint64_t bar_ld[NS], bar_empty[NS];
+    __shared__ uint64_t bar_prep, bar_s, bar_x, bar_u, bar_d, bar_fin;
+    __shared__ uint32_t tslot;
+    __shared__ int sAbort;
+    unsigned char *sS = sm + SM_S;
+    float *sg = reinterpret_cast<float *>(sm + SM_G);
+    float *se = reinterpret_cast<float *>(sm + SM_E);
 
-__global__ void __launch_bounds__(NT, 1)
-bwd_dstate_tc_kernel(BwdProblem p, float *dS_chk, const float *g_ws,
-                     const __nv_bfloat16 *W_ws, const __nv_bfloat16 *A_ws) {
-    constexpr int D = 128;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    DsTcSmem &sm = *reinterpret_cast<DsTcSmem *>(smem_raw);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x, h = unit % p.H;
-    const int jb = blockIdx.y * DVB;
-    if (p.status != nullptr && *(volatile unsigned *)p.status != kDevOk) return;
-    const SeqGeo sg = seq_geo(p, unit / p.H);
+    const SeqGeo geo = seq_geo(p, unit / p.H);
+    const int nch = geo.nch;
     const size_t sbase = (size_t)unit * D * D;
-    for (int x = tid; x < D * DVB; x += NT) {
-        const int i = x / DVB, j = x % DVB;
-        sm.dS[i][j] = p.dS_T ? p.dS_T[sbase + (size_t)i * D + jb + j] : 0.f;
+
+    if (tid == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&bar_ld[i], 1);
+            mbar_init(&bar_empty[i], 1);
+        }
+        mbar_init(&bar_prep, NMAIN);
+        mbar_init(&bar_s, NMAIN);
+        mbar_init(&bar_x, 1);
+        mbar_init(&bar_u, NMAIN);
+        mbar_init(&bar_d, 1);
+        mbar_init(&bar_fin, 1);
+        fence_mbar_init();
+        sAbort = (p.status != nullptr && *(volatile const unsigned *)p.status != kDevOk) ? 1 : 0;
     }
-    if (sg.nch > 0) ds_prefetch(sm, p, sg.nch - 1, sg, h, jb, g_ws, W_ws, A_ws, tid);
-    for (int c = sg.nch - 1; c >= 0; --c) {
-        const int nc = min(C, sg.len - c * C);
-        asm volatile("cp.async.wait_all;\n" ::: "memory");
-        __syncthreads();   // chunk c's tiles have landed; the previous chunk is done
-        float *rec = dS_chk + ((size_t)(sg.chunk0 + c) * p.H + h) * D * D;   // dS' of chunk c
-        for (int x = tid; x < D * DVB; x += NT) {
-            const int i = x / DVB, j = x % DVB;
-            rec[(size_t)i * D + jb + j] = sm.dS[i][j];
-        }
-        for (int x = tid; x < C * D; x += NT) {
-            const int t = x >> 7, i = x & 127;
-            sm.K[t][i] = __bfloat162float(sm.Kb[t][i]);
-            sm.Q[t][i] = __bfloat162float(sm.Qb[t][i]);
-            sm.W[t][i] = __bfloat162float(sm.Wb[t][i]);
-        }
-        for (int x = tid; x < C * C; x += NT) sm.At[x >> 6][x & 63] = __bfloat162float(sm.Ab[x >> 6][x & 63]);
-        for (int x = tid; x < C * DVB; x += NT) sm.dO[x / DVB][x % DVB] = __bfloat162float(sm.dOb[x / DVB][x % DVB]);
-        if (tid < C) sm.g[tid] = sm.gb[tid];
-        __syncthreads();   // staging free: the next chunk's copies overlap this one's work
-        if (c > 0) ds_prefetch(sm, p, c - 1, sg, h, jb, g_ws, W_ws, A_ws, tid);
-        if (tid < C) {
-            sm.eg[tid] = __expf(sm.g[tid]);
-            sm.egc[tid] = __expf(sm.g[C - 1] - sm.g[tid]);
-        }
-        __syncthreads();
-        {   // dU = A_qk^T dO + diag(exp(g_C - g)) K dS': thread = tokens 2 tp, 2 tp + 1 x
-            // columns 4 jb4 .. 4 jb4 + 3 (float4 rows of dO and dS')
-            const int tp = tid >> 3, jb4 = (tid & 7) * 4, t0 = 2 * tp;
-            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int s2 = t0; s2 < C; ++s2) {   // A^T rows are zero left of the diagonal
-                const float4 o = *reinterpret_cast<const float4 *>(&sm.dO[s2][jb4]);
-                const float x0 = sm.At[t0][s2], x1 = sm.At[t0 + 1][s2];
-                a0[0] = fmaf(x0, o.x, a0[0]); a0[1] = fmaf(x0, o.y, a0[1]);
-                a0[2] = fmaf(x0, o.z, a0[2]); a0[3] = fmaf(x0, o.w, a0[3]);
-                a1[0] = fmaf(x1, o.x, a1[0]); a1[1] = fmaf(x1, o.y, a1[1]);
-                a1[2] = fmaf(x1, o.z, a1[2]); a1[3] = fmaf(x1, o.w, a1[3]);
-            }
-            float b0[4] = {0.f, 0.f, 0.f, 0.f}, b1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-            for (int i = 0; i < D; ++i) {
-                const float4 d4 = *reinterpret_cast<const float4 *>(&sm.dS[i][jb4]);
-                const float k0 = sm.K[t0][i], k1 = sm.K[t0 + 1][i];
-                b0[0] = fmaf(k0, d4.x, b0[0]); b0[1] = fmaf(k0, d4.y, b0[1]);
-                b0[2] = fmaf(k0, d4.z, b0[2]); b0[3] = fmaf(k0, d4.w, b0[3]);
-                b1[0] = fmaf(k1, d4.x, b1[0]); b1[1] = fmaf(k1, d4.y, b1[1]);
-                b1[2] = fmaf(k1, d4.z, b1[2]); b1[3] = fmaf(k1, d4.w, b1[3]);
-            }
-            const float e0 = sm.egc[t0], e1 = sm.egc[t0 + 1];
-            *reinterpret_cast<float4 *>(&sm.dU[t0][jb4]) =
-                make_float4(fmaf(e0, b0[0], a0[0]), fmaf(e0, b0[1], a0[1]),
-                            fmaf(e0, b0[2], a0[2]), fmaf(e0, b0[3], a0[3]));
-            *reinterpret_cast<float4 *>(&sm.dU[t0 + 1][jb4]) =
-                make_float4(fmaf(e1, b1[0], a1[0]), fmaf(e1, b1[1], a1[1]),
-                            fmaf(e1, b1[2], a1[2]), fmaf(e1, b1[3], a1[3]));
-        }
-        __syncthreads();
-        {   // dS <- exp(g_C) dS' + Q^T diag(exp g) dO - W^T dU: thread = rows 4 ib .. 4 ib + 3
-            // x columns 4 jb4 .. 4 jb4 + 3
-            const int ib = tid >> 3, jb4 = (tid & 7) * 4, i0 = 4 * ib;
-            float acc[4][4];
-            const float egC = sm.eg[C - 1];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const float4 d4 = *reinterpret_cast<const float4 *>(&sm.dS[i0 + m][jb4]);
-                acc[m][0] = egC * d4.x; acc[m][1] = egC * d4.y;
-                acc[m][2] = egC * d4.z; acc[m][3] = egC * d4.w;
-            }
-            for (int t = 0; t < nc; ++t) {
-                const float4 q4 = *reinterpret_cast<const float4 *>(&sm.Q[t][i0]);
-                const float4 w4 = *reinterpret_cast<const float4 *>(&sm.W[t][i0]);
-                const float4 o4 = *reinterpret_cast<const float4 *>(&sm.dO[t][jb4]);
-                const float4 u4 = *reinterpret_cast<const float4 *>(&sm.dU[t][jb4]);
-                const float et = sm.eg[t];
-                const float qv[4] = {q4.x * et, q4.y * et, q4.z * et, q4.w * et};
-                const float wv[4] = {-w4.x, -w4.y, -w4.z, -w4.w};
-                const float ov[4] = {o4.x, o4.y, o4.z, o4.w};
-                const float uv[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-#pragma unroll
-                    for (int n = 0; n < 4; ++n)
-                        acc[m][n] = fmaf(qv[m], ov[n], fmaf(wv[m], uv[n], acc[m][n]));
-            }
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-                *reinterpret_cast<float4 *>(&sm.dS[i0 + m][jb4]) =
-                    make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
-        }
+    if (warp == 0) {
+        tmem_alloc(&tslot, 512);
+        tmem_relinquish();
     }
-    asm volatile("cp.async.wait_all;\n" ::: "memory");
     __syncthreads();
-    if (p.dS0) {
-        for (int x = tid; x < D * DVB; x += NT) {
-            const int i = x / DVB, j = x % DVB;
-            p.dS0[sbase + (size_t)i * D + jb + j] = sm.dS[i][j];
+    tc_fence_after();
+    const uint32_t tb = tslot;
+    const int pre_abort = sAbort;   // read by every thread before any can change it
+    __syncthreads();
+    if (pre_abort) {
+        if (warp == 0) tmem_dealloc(tb, 512);
+        return;
+    }
+    auto fail = [&]() {
+        *(volatile int *)&sAbort = 1;
+        if (p.status) atomicCAS(p.status, 0u, kDevTimeout);
+    };
+    // step k handles chunk nch - 1 - k
+    auto slot_of = [&](int k) { return (geo.chunk0 + (nch - 1 - k)) * p.H + h; };
+
+    if (warp == NMAIN + 1) {
+        // ------------------------------------------------------------ loader
+        int k = 0;
+        for (; k < nch; ++k) {
+            const int s = k % NS, r = k / NS;
+            if (r >= 1 &&
+                !__all_sync(0xffffffffu,
+                            mbar_wait_or_abort(&bar_empty[s], (uint32_t)((r - 1) & 1), &sAbort))) {
+                fail();
+                break;
+            }
+            if (lane == 0) {
+                unsigned char *st = sm + s * ST_BYTES;
+                const int c = nch - 1 - k;
+                const int row0 = (int)(geo.start + (long)c * C);
+                const long slot = slot_of(k);
+                mbar_expect_tx(&bar_ld[s], ST_TX + 256u);
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+                    tma_load_3d(st + ST_K + sl * T64, &mk, &bar_ld[s], 64 * sl, h, row0);
+                    tma_load_3d(st + ST_Q + sl * T64, &mq, &bar_ld[s], 64 * sl, h, row0);
+                    tma_load_3d(st + ST_O + sl * T64, &mo, &bar_ld[s], 64 * sl, h, row0);
+                    tma_load_2d(st + ST_W + sl * T64, &mw, &bar_ld[s], 64 * sl, (int)(slot * C));
+                }
+                tma_load_2d(st + ST_A, &ma, &bar_ld[s], 0, (int)(slot * C));
+                bulk_load(sg + s * 64, g_ws + slot * C, 256u, &bar_ld[s]);
+            }
+            __syncwarp();
+        }
+        if (sAbort)
+            for (int r = k > NS ? k - NS : 0; r < k; ++r)
+                (void)mbar_wait(&bar_ld[r % NS], (uint32_t)((r / NS) & 1));
+    } else if (warp == NMAIN) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t id_x = idesc_bf16_f32(128, 64, false, false);   // dS'^T K^T
+        constexpr uint32_t id_y = idesc_bf16_f32(128, 64, true, false);    // dO^T A_qk
+        constexpr uint32_t id_q = idesc_bf16_f32(128, 128, true, true);    // dO^T (e^g Q)
+        constexpr uint32_t id_w = idesc_bf16_f32(128, 128, false, true);   // (-dU^T) W
+        const uint32_t aS = smem_u32(sS);
+        // the chunk-input products of step k: Y, and the Q half of D into buffer k % 2
+        auto issue_inputs = [&](int k) {
+            const uint32_t st = smem_u32(sm + (k % NS) * ST_BYTES);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)   // A = dO (MN-major, M = j), B = A^T rows (K-major)
+                mma_bf16(tb + TM_Y, sdesc_sw128(st + ST_O + ks * 2048, T64, 1024),
+                         sdesc_sw128(st + ST_A + ks * 32, 16, 1024), id_y, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)   // B = e^g Q (MN-major, N = i)
+                mma_bf16(tb + TM_D + 128u * (uint32_t)(k & 1),
+                         sdesc_sw128(st + ST_O + ks * 2048, T64, 1024),
+                         sdesc_sw128(st + ST_Q + ks * 2048, T64, 1024), id_q, ks > 0);
+        };
+        bool ok = true;
+        if (nch > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bar_ld[0], 0u, &sAbort) &&
+                                             mbar_wait_or_abort(&bar_prep, 0u, &sAbort));
+            if (ok) {
+                tc_fence_after();
+                if (lane == 0) issue_inputs(0);
+                __syncwarp();
+            }
+        }
+        for (int k = 0; ok && k < nch; ++k) {
+            const uint32_t st = smem_u32(sm + (k % NS) * ST_BYTES);
+            // X = dS'^T K^T once dS'^T is in shared memory
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_s, (uint32_t)(k & 1), &sAbort))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(tb + TM_X, sdesc_sw128(aS + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                             sdesc_sw128(st + ST_K + (ks >> 2) * T64 + (ks & 3) * 32, 16, 1024),
+                             id_x, ks > 0);
+                mma_commit(&bar_x);
+            }
+            __syncwarp();
+            // D += (-dU^T) W once dU^T (bf16) is in TMEM
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_u, (uint32_t)(k & 1), &sAbort))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16_ts(tb + TM_D + 128u * (uint32_t)(k & 1), tb + TM_U + 8u * (uint32_t)ks,
+                                sdesc_sw128(st + ST_W + ks * 2048, T64, 1024), id_w, 1);
+                mma_commit(&bar_d);
+                mma_commit(&bar_empty[k % NS]);
+            }
+            __syncwarp();
+            // the next chunk's input products (Y is read, D buffer (k + 1) % 2 too)
+            if (k + 1 < nch) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_or_abort(&bar_ld[(k + 1) % NS], (uint32_t)(((k + 1) / NS) & 1),
+                                                   &sAbort) &&
+                                    mbar_wait_or_abort(&bar_prep, (uint32_t)((k + 1) & 1), &sAbort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) issue_inputs(k + 1);
+                __syncwarp();
+            }
+        }
+        if (!ok) fail();
+        if (lane == 0) mma_commit(&bar_fin);
+        __syncwarp();
+        (void)mbar_wait(&bar_fin, 0u);
+    } else {
+        // ------------------------------------------------------------ main warps
+        const int j = (warp & 3) * 32 + lane;   // column of dS (TMEM lane)
+        const int hf = warp >> 2;               // rows i in [64 hf, 64 hf + 64)
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        unsigned char *const sSrow = sS + hf * 16384;
+        float ds[64];   // dS'^T[j][64 hf + x]
+#pragma unroll
+        for (int x = 0; x < 64; ++x)
+            ds[x] = p.dS_T ? p.dS_T[sbase + (size_t)(64 * hf + x) * D + j] : 0.f;
+        // dS' (rows i = 64 hf + x, column j) of the chunk of step k; coalesced over j
+        auto record = [&](int k) {
+            float *rec = dS_chk + (size_t)slot_of(k) * D * D + (size_t)(64 * hf) * D + j;
+#pragma unroll
+            for (int x = 0; x < 64; ++x) rec[(size_t)x * D] = ds[x];
+        };
+        // bf16 row j of dS'^T into shared memory (the A operand of X)
+        auto put_state = [&]() {
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+                *reinterpret_cast<uint4 *>(sSrow + sw128_offset(j, 8 * c8)) =
+                    make_uint4(dtc_pack(ds[8 * c8], ds[8 * c8 + 1]), dtc_pack(ds[8 * c8 + 2], ds[8 * c8 + 3]),
+                               dtc_pack(ds[8 * c8 + 4], ds[8 * c8 + 5]), dtc_pack(ds[8 * c8 + 6], ds[8 * c8 + 7]));
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_s);
+        };
+        // stage of step k landed: the rows past the sequence's end cleared (K,
+        // Q, dO, A^T), Q scaled by exp g, the decay factors of the chunk
+        const int mt = tid;   // 0 .. 255
+        auto prep = [&](int k) -> bool {
+            const int s = k % NS;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait_or_abort(&bar_ld[s], (uint32_t)((k / NS) & 1), &sAbort)))
+                return false;
+            unsigned char *st = sm + s * ST_BYTES;
+            const int c = nch - 1 - k;
+            const int nc = min(C, geo.len - c * C);
+            const float *g = sg + s * 64;
+            // thread: token t = mt >> 2, 16-byte pieces (mt & 3) + 4 u of its 16
+            const int t = mt >> 2;
+            const float et = __expf(g[t]);
+            const bool live = t < nc;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int pc = (mt & 3) + 4 * u, sl = pc >> 3;
+                const uint32_t off = sl * T64 + sw128_offset(t, 8 * (pc & 7));
+                uint4 *q4 = reinterpret_cast<uint4 *>(st + ST_Q + off);
+                uint4 w = *q4;
+                if (live) {
+                    w = make_uint4(dtc_pack(et * __uint_as_float(w.x << 16), et * __uint_as_float(w.x & 0xffff0000u)),
+                                   dtc_pack(et * __uint_as_float(w.y << 16), et * __uint_as_float(w.y & 0xffff0000u)),
+                                   dtc_pack(et * __uint_as_float(w.z << 16), et * __uint_as_float(w.z & 0xffff0000u)),
+                                   dtc_pack(et * __uint_as_float(w.w << 16), et * __uint_as_float(w.w & 0xffff0000u)));
+                } else {
+                    w = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4 *>(st + ST_K + off) = w;
+                    *reinterpret_cast<uint4 *>(st + ST_O + off) = w;
+                    if (u < 2)   // A^T row t: 8 pieces
+                        *reinterpret_cast<uint4 *>(st + ST_A + sw128_offset(t, 8 * ((mt & 3) + 4 * u))) = w;
+                }
+                *q4 = w;
+            }
+            if (mt < 64) {
+                se[s * 128 + mt] = __expf(g[mt]);
+                se[s * 128 + 64 + mt] = __expf(g[C - 1] - g[mt]);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_prep);
+            return true;
+        };
+
+        bool ok = true;
+        if (nch > 0) {
+            record(0);
+            put_state();
+            ok = prep(0);
+            if (!ok) fail();
+        }
+        for (int k = 0; ok && k < nch; ++k) {
+            const int s = k % NS;
+            // ---- dU^T = X diag(exp(g_C - g)) + Y for tokens t in [32 hf, 32 hf + 32)
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_x, (uint32_t)(k & 1), &sAbort))) {
+                fail();
+                break;
+            }
+            tc_fence_after();
+            {
+                uint32_t xr[32], yr[32];
+                tmem_ld32(tb + lane_base + TM_X + 32 * hf, xr);
+                tmem_ld32(tb + lane_base + TM_Y + 32 * hf, yr);
+                tmem_ld_wait();
+                const float *egc = se + s * 128 + 64 + 32 * hf;
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float u0 = fmaf(egc[2 * e], __uint_as_float(xr[2 * e]), __uint_as_float(yr[2 * e]));
+                    const float u1 = fmaf(egc[2 * e + 1], __uint_as_float(xr[2 * e + 1]),
+                                          __uint_as_float(yr[2 * e + 1]));
+                    w[e] = dtc_pack(-u0, -u1);
+                }
+                tmem_st16(tb + lane_base + TM_U + 16 * hf, w);
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_u);
+            // ---- the next chunk's stage, while D is completed
+            if (k + 1 < nch && !prep(k + 1)) {
+                fail();
+                break;
+            }
+            // ---- dS'^T <- exp(g_C) dS'^T + D
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_d, (uint32_t)(k & 1), &sAbort))) {
+                fail();
+                break;
+            }
+            tc_fence_after();
+            {
+                const float egC = se[s * 128 + C - 1];   // exp(g_C)
+                const uint32_t tD = tb + lane_base + TM_D + 128u * (uint32_t)(k & 1) + 64u * hf;
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t r[32];
+                    tmem_ld32(tD + 32 * c2, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        ds[32 * c2 + x] = fmaf(egC, ds[32 * c2 + x], __uint_as_float(r[x]));
+                }
+            }
+            tc_fence_before();
+            if (k + 1 < nch) {
+                record(k + 1);
+                put_state();
+            }
+        }
+        if (ok && !sAbort && p.dS0) {
+#pragma unroll
+            for (int x = 0; x < 64; ++x) p.dS0[sbase + (size_t)(64 * hf + x) * D + j] = ds[x];
         }
     }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 512);
 }
 
 // ------------------------------------------------------------ token gradients
@@ -1228,16 +1415,22 @@ cudaError_t launch_bwd_t(const BwdProblem &p0, cudaStream_t s) {
             return e;
         if ((e = cudaFuncSetAttribute(bwd_dstate_tc_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)sizeof(DsTcSmem))) != cudaSuccess)
+                                      (int)dtc::SMEM)) != cudaSuccess)
             return e;
         attr = true;
     }
-    if (tc)
-        bwd_dstate_tc_kernel<<<dim3(units, D / DVB), NT, sizeof(DsTcSmem), s>>>(
-            p, dS_chk, g_ws, static_cast<const __nv_bfloat16 *>(W_ws),
-            static_cast<const __nv_bfloat16 *>(A_ws));
-    else
+    if (tc) {
+        CUtensorMap mq, mk, mo, mw, ma;
+        const long slots = nchunks * p.H;
+        if (!tmap::rows_3d(&mq, p.q, p.H, p.total_T, C) || !tmap::rows_3d(&mk, p.k, p.H, p.total_T, C) ||
+            !tmap::rows_3d(&mo, p.dout, p.H, p.total_T, C) ||
+            !tmap::plain_2d(&mw, W_ws, D, slots * C, C) || !tmap::plain_2d(&ma, A_ws, C, slots * C, C))
+            return cudaErrorInvalidValue;
+        bwd_dstate_tc_kernel<<<units, dtc::THREADS, dtc::SMEM, s>>>(mq, mk, mo, mw, ma, p, dS_chk,
+                                                                     g_ws);
+    } else {
         bwd_dstate_kernel<Tin, D><<<dim3(units, D / DVB), NT, sizeof(DsSmem<D>), s>>>(p, dS_chk);
+    }
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 3. token gradients, one CTA per chunk slot
