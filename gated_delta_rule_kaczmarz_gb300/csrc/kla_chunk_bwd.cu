@@ -1275,6 +1275,538 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch_
     }
 }
 
+// ------------------------------------------------------ token gradients (tcgen05)
+// bf16 with d = 128: per chunk, the products of the gradient lines above on
+// the tensor cores, from the recorded S and dS' (fp32, converted to bf16 in
+// shared memory), the forward's T (bf16) and A^T, g of the chunk workspace.
+// Every product has M = 128 token rows: a chunk has 64, so two 64-row tiles
+// stored slab by slab one after the other act as one 128-row operand and
+// share the product ([dR ; dO] S^T gives dR S^T and dO S^T = pq; [dR ; dO] U^T
+// gives dR U^T and dO U^T; [X + X^T ; M1] K with M1 = dA_qk o Gamma); where
+// only one tile is meant, the other 64 rows are whatever follows it in shared
+// memory and their accumulator lanes are not read.  TMEM lane t holds token
+// t's row (lanes 64 + t: the second tile's token t).  Four product phases,
+// each followed by its epilogue on the CUDA cores:
+//   1. K S, A_qk^T dO, K dS', K K^T (lanes 64..: Q K^T)
+//      -> R = diag(beta)(V - diag(exp g) K S), dU = A_qk^T dO + diag(exp(g_C - g)) K dS'
+//   2. U = T R, dR = T^T dU  -> dV = diag(beta) dR, dbeta and dg from R
+//   3. [dR ; dO] U^T, U dS'^T, [dR ; dO] S^T  -> M1, X, their dg and dbeta terms
+//   4. [X + X^T ; M1] K + M1^T Q  -> dQ (lanes 64..), dK (lanes 0..63)
+// Shared memory (offsets in KB): [K | Q] 0, [dR | dO] 32, V 64, S 80, dS' 112,
+// T 144, A^T 152, R 160, U 176, dU 192, vectors 208; reused: dV staging and
+// then [X + X^T | M1] in R, the column-sum scratch in dU and V, X (fp32) in
+// S, zeros in U, dK staging in S and dQ staging in dU.
+namespace gtc {
+constexpr uint32_t KB = 1024;
+constexpr uint32_t SL = 8 * KB;        // one 64 x 64 bf16 slab (64 rows of 128 bytes)
+constexpr uint32_t O_KQ = 0, O_RO = 32 * KB, O_V = 64 * KB, O_S = 80 * KB, O_DS = 112 * KB,
+                   O_T = 144 * KB, O_A = 152 * KB, O_R = 160 * KB, O_U = 176 * KB,
+                   O_DU = 192 * KB, O_VEC = 208 * KB;
+constexpr uint32_t SMEM = O_VEC + 4 * KB + 1024;
+constexpr int NTH = 256;               // 8 warps: 2 per TMEM lane quadrant
+constexpr uint32_t C_A = 0, C_B = 128, C_C = 256, C_G = 384;   // TMEM columns
+static_assert(SMEM <= 232448, "gradient kernel shared memory");
+}  // namespace gtc
+
+// A 128-row K-major operand over two 64-row tiles stored slab by slab, one
+// slab pair every `pair` bytes (K step of 16 = 32 bytes within a slab).
+__device__ __forceinline__ uint64_t gk_desc(uint32_t base, int ks, uint32_t pair) {
+    return tc::sdesc_sw128(base + (uint32_t)(ks >> 2) * pair + (uint32_t)(ks & 3) * 32u, 16, 1024);
+}
+// An MN-major operand: K step of 16 rows = 2048 bytes, the 64-element MN
+// halves `lbo` bytes apart.
+__device__ __forceinline__ uint64_t gm_desc(uint32_t base, int ks, uint32_t lbo) {
+    return tc::sdesc_sw128(base + (uint32_t)ks * 2048u, lbo, 1024);
+}
+__device__ __forceinline__ uint32_t g_pack(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+__device__ __forceinline__ float g_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float g_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+// Element (row, col) of a 64-column bf16 slab with the 128-byte swizzle.
+__device__ __forceinline__ float g_at(const unsigned char *slab, int row, int col) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(slab + tc::sw128_offset(row, col)));
+}
+// 16 fp32 values -> bf16 columns [c0, c0 + 16) of row `row` of a slab.
+__device__ __forceinline__ void g_st16(unsigned char *slab, int row, int c0, const float *x) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+        *reinterpret_cast<uint4 *>(slab + tc::sw128_offset(row, c0 + 8 * k)) =
+            make_uint4(g_pack(x[8 * k], x[8 * k + 1]), g_pack(x[8 * k + 2], x[8 * k + 3]),
+                       g_pack(x[8 * k + 4], x[8 * k + 5]), g_pack(x[8 * k + 6], x[8 * k + 7]));
+}
+
+__global__ void __launch_bounds__(gtc::NTH, 1)
+bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
+                    const __grid_constant__ CUtensorMap mt, const __grid_constant__ CUtensorMap ma,
+                    const __grid_constant__ CUtensorMap mdq, const __grid_constant__ CUtensorMap mdk,
+                    const __grid_constant__ CUtensorMap mdv, BwdProblem p, int nch_fixed,
+                    const float *S_chk, const float *dS_chk, const float *g_ws) {
+    using namespace gtc;
+    using namespace tc;
+    extern __shared__ unsigned char g_smem[];
+    unsigned char *sm = g_smem + ((1024u - (smem_u32(g_smem) & 1023u)) & 1023u);
+    __shared__ uint64_t bar_ld, bar_mma;
+    __shared__ uint32_t tslot;
+    __shared__ int sBad;
+    float *vec = reinterpret_cast<float *>(sm + O_VEC);
+    float *vg = vec, *veg = vec + 64, *vegc = vec + 128, *vbeta = vec + 192, *vden = vec + 256,
+          *veta = vec + 320, *valpha = vec + 384, *vdbeta = vec + 448, *vdg = vec + 512,
+          *vp = vec + 576 /* [2][2][64]: the halves' p1, p2 */, *vred = vec + 832 /* [8] */;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long gch = blockIdx.x;
+    const int h = blockIdx.y;
+    if (p.status != nullptr && *(volatile unsigned *)p.status != kDevOk) return;
+    if (p.cu_seqlens && gch >= p.chunk_prefix[p.n_seq]) return;   // past the last chunk
+    const int seq = p.cu_seqlens ? p.chunk_seq[gch] : (int)(gch / nch_fixed);
+    const SeqGeo sq = seq_geo(p, seq);
+    const int c = (int)(gch - sq.chunk0);
+    const long row0 = sq.start + (long)c * C;
+    const int nc = min(C, sq.len - c * C);
+    const size_t slot = (size_t)gch * p.H + h;
+    // TMEM lane of this thread and its column half; rows 0..63 live in warps
+    // 0, 1, 4, 5 (lower), the second tile's rows in warps 2, 3, 6, 7 (upper)
+    const int L = (warp & 3) * 32 + lane, hf = warp >> 2;
+    const bool lower = L < 64;
+    const int t = L & 63;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+
+    if (tid == 0) {
+        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+        sBad = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(&tslot, 512);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tslot;
+    const uint32_t aKQ = smem_u32(sm + O_KQ), aRO = smem_u32(sm + O_RO), aS = smem_u32(sm + O_S),
+                   aDS = smem_u32(sm + O_DS), aT = smem_u32(sm + O_T), aA = smem_u32(sm + O_A),
+                   aR = smem_u32(sm + O_R), aU = smem_u32(sm + O_U), aDU = smem_u32(sm + O_DU);
+    int mph = 0;   // phase of bar_mma
+    auto mma_wait = [&]() {
+        if (!mbar_wait(&bar_mma, (uint32_t)(mph & 1))) sBad = 1;
+        ++mph;
+        tc_fence_after();
+    };
+
+    // ---- loads: K, Q, dO, V (token rows), T, A^T (chunk slot), g
+    if (tid == 0) {
+        mbar_expect_tx(&bar_ld, 10u * SL + 256u);
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+            tma_load_3d(sm + O_KQ + s2 * 2 * SL, &mk, &bar_ld, 64 * s2, h, (int)row0);
+            tma_load_3d(sm + O_KQ + s2 * 2 * SL + SL, &mq, &bar_ld, 64 * s2, h, (int)row0);
+            tma_load_3d(sm + O_RO + s2 * 2 * SL + SL, &mo, &bar_ld, 64 * s2, h, (int)row0);
+            tma_load_3d(sm + O_V + s2 * SL, &mv, &bar_ld, 64 * s2, h, (int)row0);
+        }
+        tma_load_2d(sm + O_T, &mt, &bar_ld, 0, (int)(slot * C));
+        tma_load_2d(sm + O_A, &ma, &bar_ld, 0, (int)(slot * C));
+        bulk_load(vg, g_ws + slot * C, 256u, &bar_ld);
+    }
+    if (tid < C) {
+        const bool ok = tid < nc;
+        const size_t r = (size_t)(row0 + tid) * p.H + h;
+        valpha[tid] = (ok && p.alpha) ? p.alpha[r] : 1.f;
+        veta[tid] = ok ? p.eta[r] : 0.f;
+    }
+    // ---- S and dS' of the chunk (fp32) to bf16 tiles (rows i, columns j in
+    //      two slabs of 128 rows); sum of S o dS' on the way
+    float sds = 0.f;
+    {
+        const float *S = S_chk + slot * 128 * 128, *dSp = dS_chk + slot * 128 * 128;
+        const int cq = tid & 31;   // float4 column group: j = 4 cq .. 4 cq + 3
+#pragma unroll 4
+        for (int r = 0; r < 16; ++r) {
+            const int i = (tid >> 5) + 8 * r;
+            const float4 a = *reinterpret_cast<const float4 *>(S + (size_t)i * 128 + 4 * cq);
+            const float4 b = *reinterpret_cast<const float4 *>(dSp + (size_t)i * 128 + 4 * cq);
+            sds = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, sds))));
+            const uint32_t off = (uint32_t)((4 * cq) >> 6) * 16 * KB + sw128_offset(i, (4 * cq) & 63);
+            *reinterpret_cast<uint2 *>(sm + O_S + off) = make_uint2(g_pack(a.x, a.y), g_pack(a.z, a.w));
+            *reinterpret_cast<uint2 *>(sm + O_DS + off) = make_uint2(g_pack(b.x, b.y), g_pack(b.z, b.w));
+        }
+    }
+    if (!mbar_wait(&bar_ld, 0u)) sBad = 1;
+    // ---- rows past the sequence's end: K, Q, dO, V cleared; chunk vectors
+    if (nc < C) {
+        for (int e = tid; e < (C - nc) * 16; e += NTH) {
+            const int tt = nc + (e >> 4), pc = e & 15, s2 = pc >> 3;
+            const uint32_t off = sw128_offset(tt, 8 * (pc & 7));
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(sm + O_KQ + s2 * 2 * SL + off) = z;
+            *reinterpret_cast<uint4 *>(sm + O_KQ + s2 * 2 * SL + SL + off) = z;
+            *reinterpret_cast<uint4 *>(sm + O_RO + s2 * 2 * SL + SL + off) = z;
+            *reinterpret_cast<uint4 *>(sm + O_V + s2 * SL + off) = z;
+        }
+    }
+    __syncthreads();
+    if (tid < C) {
+        float n2 = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < 128; ++i) {
+            const float k = g_at(sm + O_KQ + (i >> 6) * 2 * SL, tid, i & 63);
+            n2 = fmaf(k, k, n2);
+        }
+        const float den = n2 + p.eps;
+        vden[tid] = den;
+        const float b = p.beta_mode ? veta[tid] : (den != 0.f ? veta[tid] / den : 0.f);
+        vbeta[tid] = tid < nc ? b : 0.f;
+        veg[tid] = __expf(vg[tid]);
+        vegc[tid] = __expf(vg[C - 1] - vg[tid]);
+        vdg[tid] = 0.f;
+    }
+    fence_async_smem();
+    __syncthreads();
+
+    // ================= phase 1
+    if (tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t id_mn = idesc_bf16_f32(128, 128, false, true);
+        constexpr uint32_t id_kk = idesc_bf16_f32(128, 64, false, false);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)   // K S: B = S read MN-major (n = j, k = i)
+            mma_bf16(tb + C_A, gk_desc(aKQ, ks, 2 * SL), gm_desc(aS, ks, 16 * KB), id_mn, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)   // A_qk^T dO: A = A^T rows t, B = dO (n = j, k = s)
+            mma_bf16(tb + C_B, gk_desc(aA, ks, 0), gm_desc(aRO + SL, ks, 2 * SL), id_mn, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)   // K dS'
+            mma_bf16(tb + C_C, gk_desc(aKQ, ks, 2 * SL), gm_desc(aDS, ks, 16 * KB), id_mn, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)   // [K ; Q] K^T
+            mma_bf16(tb + C_G, gk_desc(aKQ, ks, 2 * SL), gk_desc(aKQ, ks, 2 * SL), id_kk, ks > 0);
+        mma_commit(&bar_mma);
+    }
+    __syncwarp();
+    mma_wait();
+    // ---- epilogue 1 (rows t of the lower lanes): R and dU to bf16 tiles
+    if (lower) {
+        const float et = veg[t], ec = vegc[t], bt = vbeta[t];
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+            const int j0 = 64 * hf + 32 * c2;
+            uint32_t ks_[32], da[32], db[32];
+            tmem_ld32(tb + lane_base + C_A + j0, ks_);
+            tmem_ld32(tb + lane_base + C_B + j0, da);
+            tmem_ld32(tb + lane_base + C_C + j0, db);
+            tmem_ld_wait();
+            float rr[32], uu[32];
+            const unsigned char *vs = sm + O_V + hf * SL;
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+                const float v = g_at(vs, t, 32 * c2 + x);
+                rr[x] = bt * (v - et * __uint_as_float(ks_[x]));
+                uu[x] = fmaf(ec, __uint_as_float(db[x]), __uint_as_float(da[x]));
+            }
+            g_st16(sm + O_R + hf * SL, t, 32 * c2, rr);
+            g_st16(sm + O_R + hf * SL, t, 32 * c2 + 16, rr + 16);
+            g_st16(sm + O_DU + hf * SL, t, 32 * c2, uu);
+            g_st16(sm + O_DU + hf * SL, t, 32 * c2 + 16, uu + 16);
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ================= phase 2
+    if (tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t id_u = idesc_bf16_f32(128, 128, false, true);
+        constexpr uint32_t id_r = idesc_bf16_f32(128, 128, true, true);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)   // U = T R: A = T rows t, B = R (n = j, k = s)
+            mma_bf16(tb + C_B, gk_desc(aT, ks, 0), gm_desc(aR, ks, SL), id_u, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)   // dR = T^T dU: A = T read MN-major (m = t, k = s)
+            mma_bf16(tb + C_C, gm_desc(aT, ks, SL), gm_desc(aDU, ks, SL), id_r, ks > 0);
+        mma_commit(&bar_mma);
+    }
+    __syncwarp();
+    mma_wait();
+    // ---- epilogue 2 (lower lanes): U, dR to bf16 tiles; dV; dbeta and dg from R
+    if (lower) {
+        const float et = veg[t], bt = vbeta[t];
+        float p1 = 0.f, p2 = 0.f;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+            const int j0 = 64 * hf + 32 * c2;
+            uint32_t ur[32], rr[32], kr[32];
+            tmem_ld32(tb + lane_base + C_B + j0, ur);
+            tmem_ld32(tb + lane_base + C_C + j0, rr);
+            tmem_ld32(tb + lane_base + C_A + j0, kr);
+            tmem_ld_wait();
+            float uf[32], df[32], dv[32];
+            const unsigned char *vs = sm + O_V + hf * SL;
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+                uf[x] = __uint_as_float(ur[x]);
+                df[x] = __uint_as_float(rr[x]);
+                dv[x] = bt * df[x];
+                const float v = g_at(vs, t, 32 * c2 + x);
+                p1 = fmaf(v - et * __uint_as_float(kr[x]), df[x], p1);   // (V - e^g K S) . dR
+                p2 = fmaf(v, df[x], p2);
+            }
+            g_st16(sm + O_U + hf * SL, t, 32 * c2, uf);
+            g_st16(sm + O_U + hf * SL, t, 32 * c2 + 16, uf + 16);
+            g_st16(sm + O_RO + hf * 2 * SL, t, 32 * c2, df);   // dR: first tile of the pair
+            g_st16(sm + O_RO + hf * 2 * SL, t, 32 * c2 + 16, df + 16);
+            g_st16(sm + O_R + hf * SL, t, 32 * c2, dv);        // dV staging (R is read)
+            g_st16(sm + O_R + hf * SL, t, 32 * c2 + 16, dv + 16);
+        }
+        vp[hf * 64 + t] = p1;
+        vp[128 + hf * 64 + t] = p2;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid < C) {
+        const float p1 = vp[tid] + vp[64 + tid], p2 = vp[128 + tid] + vp[192 + tid];
+        vdbeta[tid] = p1;
+        vdg[tid] += vbeta[tid] * (p1 - p2);   // -beta e^g (K S)_t . dR_t
+    }
+    // dV: TMA store of a whole chunk; a partial chunk row by row
+    {
+        __nv_bfloat16 *dvo = static_cast<__nv_bfloat16 *>(p.dv);
+        if (nc == C) {
+            if (tid == 0) {
+#pragma unroll
+                for (int s2 = 0; s2 < 2; ++s2)
+                    tma_store_3d(&mdv, sm + O_R + s2 * SL, 64 * s2, h, (int)row0);
+                bulk_commit_group();
+            }
+        } else {
+            for (int e = tid; e < nc * 128; e += NTH) {
+                const int tt = e >> 7, j = e & 127;
+                dvo[((size_t)(row0 + tt) * p.H + h) * 128 + j] =
+                    *reinterpret_cast<const __nv_bfloat16 *>(sm + O_R + (j >> 6) * SL + sw128_offset(tt, j & 63));
+            }
+        }
+    }
+
+    // ================= phase 3
+    if (tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t id_64 = idesc_bf16_f32(128, 64, false, false);
+        constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, false, false);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)   // [dR ; dO] U^T: B = U rows s (K-major)
+            mma_bf16(tb + C_A, gk_desc(aRO, ks, 2 * SL), gk_desc(aU, ks, SL), id_64, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)   // U dS'^T: B = dS' rows i (K-major)
+            mma_bf16(tb + C_B, gk_desc(aU, ks, SL), gk_desc(aDS, ks, 16 * KB), id_kk, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)   // [dR ; dO] S^T
+            mma_bf16(tb + C_C, gk_desc(aRO, ks, 2 * SL), gk_desc(aS, ks, 16 * KB), id_kk, ks > 0);
+        mma_commit(&bar_mma);
+    }
+    __syncwarp();
+    mma_wait();
+    // the dV store has read the staging tile before [X + X^T | M1] overwrites
+    // it; dbeta and dg of epilogue 2 are in place before the adds below
+    if (tid == 0) bulk_wait_group_read0();
+    __syncthreads();
+    // ---- epilogue 3: lower lanes row t of dR U^T -> X and the dA_kk terms;
+    //      upper lanes row t of dO U^T -> M1 = dA_qk o Gamma and its terms.
+    //      Column-sum scratch: E_qk in dU, E_kk in V (fp32 64 x 64); X in S.
+    float *Eqk = reinterpret_cast<float *>(sm + O_DU);
+    float *Ekk = reinterpret_cast<float *>(sm + O_V);
+    float *Xs = reinterpret_cast<float *>(sm + O_S);
+    {
+        const float gt = vg[t];
+        const int s0 = 32 * hf;
+        uint32_t dr[32], gr[32];
+        tmem_ld32(tb + lane_base + C_A + s0, dr);   // dR U^T (lower) / dO U^T (upper)
+        tmem_ld32(tb + lane_base + C_G + s0, gr);   // K K^T (lower) / Q K^T (upper)
+        tmem_ld_wait();
+        float rsum = 0.f, bsum = 0.f;
+        if (lower) {
+            const float bt = vbeta[t];
+            float xrow[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+                const int s2 = s0 + x;
+                const float xg = s2 < t ? -__uint_as_float(dr[x]) * __expf(gt - vg[s2]) : 0.f;
+                const float e = xg * __uint_as_float(gr[x]);   // . k_t k_s
+                bsum += e;
+                Ekk[t * 64 + s2] = bt * e;                     // dA_kk o A_kk
+                xrow[x] = bt * xg;                             // X
+            }
+            rsum = bt * bsum;
+#pragma unroll
+            for (int x = 0; x < 32; ++x) Xs[t * 64 + s0 + x] = xrow[x];
+        } else {
+            float m1[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+                const int s2 = s0 + x;
+                const float da = s2 <= t ? __uint_as_float(dr[x]) * __expf(gt - vg[s2]) : 0.f;
+                m1[x] = da;                                    // dA_qk o Gamma
+                const float ev = da * __uint_as_float(gr[x]);  // dA_qk o A_qk
+                rsum += ev;
+                Eqk[t * 64 + s2] = ev;
+            }
+            g_st16(sm + O_R + SL, t, s0, m1);                  // M1 tile [t][s]
+            g_st16(sm + O_R + SL, t, s0 + 16, m1 + 16);
+        }
+        // row sums of the two halves (both threads of a row add into vdg / vdbeta)
+        atomicAdd(&vdg[t], rsum);
+        if (lower) atomicAdd(&vdbeta[t], bsum);
+    }
+    __syncthreads();
+    if (tid < C) {   // column sums: dg_s -= sum_r E_qk[r][s] + E_kk[r][s]
+        float cs = 0.f;
+        for (int r = 0; r < C; ++r) cs += Eqk[r * 64 + tid] + Ekk[r * 64 + tid];
+        vdg[tid] -= cs;
+    }
+    {   // X + X^T (symmetric) to the first tile of the pair; zeros (8 KB) in U
+        const int r = tid >> 2, q = tid & 3;   // row r, columns 16 q .. 16 q + 15
+        float xx[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) xx[x] = Xs[r * 64 + 16 * q + x] + Xs[(16 * q + x) * 64 + r];
+        g_st16(sm + O_R, r, 16 * q, xx);
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(sm + O_U + r * 128 + 32 * q) = z;
+        *reinterpret_cast<uint4 *>(sm + O_U + r * 128 + 32 * q + 16) = z;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ================= phase 4
+    if (tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t id_k = idesc_bf16_f32(128, 128, false, true);
+        constexpr uint32_t id_q = idesc_bf16_f32(128, 128, true, true);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)   // [X + X^T ; M1] K: B = K read MN-major (n = i, k = s)
+            mma_bf16(tb + C_A, gk_desc(aR, ks, 0), gm_desc(aKQ, ks, 2 * SL), id_k, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)   // + [M1^T ; 0] Q: A = M1 read MN-major, zeros beyond
+            mma_bf16(tb + C_A, gm_desc(aR + SL, ks, aU - (aR + SL)), gm_desc(aKQ + SL, ks, 2 * SL),
+                     id_q, 1);
+        mma_commit(&bar_mma);
+    }
+    __syncwarp();
+    mma_wait();
+    // ---- final epilogue: dK (lower lanes), dQ (upper lanes), their dg terms
+    __nv_bfloat16 *dqo = static_cast<__nv_bfloat16 *>(p.dq), *dko = static_cast<__nv_bfloat16 *>(p.dk);
+    float red = 0.f;
+    {
+        const float et = veg[t], ec = vegc[t], bt = vbeta[t];
+        float cn = 0.f;   // the gradient through beta's key norm
+        if (lower && p.beta_mode == 0 && vden[t] != 0.f)
+            cn = -2.f * veta[t] * vdbeta[t] / (vden[t] * vden[t]);
+        float acc = 0.f;   // k . (U dS'^T)_t (lower) or q . pq_t (upper)
+        unsigned char *stg = lower ? sm + O_S : sm + O_DU;   // staging: dK in S, dQ in dU
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+            const int i0 = 64 * hf + 32 * c2;
+            uint32_t ar[32], br[32], cr[32];
+            tmem_ld32(tb + lane_base + C_C + i0, ar);   // dR S^T (lower) / pq (upper)
+            tmem_ld32(tb + lane_base + C_A + i0, cr);   // (X + X^T) K + M1^T Q / M1 K
+            if (lower) tmem_ld32(tb + lane_base + C_B + i0, br);   // U dS'^T
+            tmem_ld_wait();
+            float out[32];
+            const unsigned char *ks_ = sm + O_KQ + hf * 2 * SL + (lower ? 0 : SL);   // k_t or q_t
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+                const float kv = g_at(ks_, t, 32 * c2 + x);
+                if (lower) {
+                    const float uds = __uint_as_float(br[x]);
+                    out[x] = -bt * et * __uint_as_float(ar[x]) + ec * uds + __uint_as_float(cr[x]) + cn * kv;
+                    acc = fmaf(kv, uds, acc);
+                } else {
+                    const float pq = __uint_as_float(ar[x]);
+                    out[x] = et * pq + __uint_as_float(cr[x]);
+                    acc = fmaf(kv, pq, acc);
+                }
+            }
+            g_st16(stg + hf * SL, t, 32 * c2, out);
+            g_st16(stg + hf * SL, t, 32 * c2 + 16, out + 16);
+        }
+        if (lower) {
+            const float wk = ec * acc;
+            atomicAdd(&vdg[t], -wk);
+            red = wk;
+        } else {
+            atomicAdd(&vdg[t], et * acc);
+        }
+    }
+    fence_async_smem();
+    red += __shfl_xor_sync(0xffffffffu, red, 16);
+    red += __shfl_xor_sync(0xffffffffu, red, 8);
+    red += __shfl_xor_sync(0xffffffffu, red, 4);
+    red += __shfl_xor_sync(0xffffffffu, red, 2);
+    red += __shfl_xor_sync(0xffffffffu, red, 1);
+    // S o dS' partial sums of the conversion, reduced per warp
+    float sw = sds;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, off);
+    if (lane == 0) vred[warp] = red + sw * veg[C - 1];
+    tc_fence_before();
+    __syncthreads();
+    if (nc == C) {
+        if (tid == 0) {
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+                tma_store_3d(&mdk, sm + O_S + s2 * SL, 64 * s2, h, (int)row0);
+                tma_store_3d(&mdq, sm + O_DU + s2 * SL, 64 * s2, h, (int)row0);
+            }
+            bulk_commit_group();
+        }
+    } else {
+        for (int e = tid; e < nc * 128; e += NTH) {
+            const int tt = e >> 7, i = e & 127;
+            const uint32_t off = (i >> 6) * SL + sw128_offset(tt, i & 63);
+            const size_t o = ((size_t)(row0 + tt) * p.H + h) * 128 + i;
+            dko[o] = *reinterpret_cast<const __nv_bfloat16 *>(sm + O_S + off);
+            dqo[o] = *reinterpret_cast<const __nv_bfloat16 *>(sm + O_DU + off);
+        }
+    }
+    if (warp == 0) {   // dg_C onto g_{C-1}; reverse cumulative sum -> dlog(alpha)
+        float gc = 0.f;
+#pragma unroll
+        for (int w = 0; w < NTH / 32; ++w) gc += vred[w];
+        float d0 = vdg[lane], d1 = vdg[lane + 32];
+        if (lane == 31) d1 += gc;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {   // suffix sums
+            const float u0 = __shfl_down_sync(0xffffffffu, d0, off);
+            const float u1 = __shfl_down_sync(0xffffffffu, d1, off);
+            if (lane + off < 32) { d0 += u0; d1 += u1; }
+        }
+        d0 += __shfl_sync(0xffffffffu, d1, 0);
+        const float dl[2] = {d0, d1};
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+            const int tt = lane + 32 * q2;
+            if (tt < nc) {
+                const size_t r = (size_t)(row0 + tt) * p.H + h;
+                if (p.dalpha && p.alpha) p.dalpha[r] = dl[q2] / valpha[tt];
+                if (p.deta) {
+                    const float dbt = vdbeta[tt], den = vden[tt];
+                    p.deta[r] = p.beta_mode ? dbt : (den != 0.f ? dbt / den : 0.f);
+                }
+            }
+        }
+    }
+    if (tid == 0) {
+        bulk_wait_group0();
+        if (sBad && p.status) atomicCAS(p.status, 0u, kDevTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 512);
+}
+
 // Varlen: validates cu_seqlens (cu[0] == 0, non-decreasing, cu[N] ==
 // total_T; a bad table sets the status word and every later kernel of the
 // call skips its work) and builds the chunk tables: the first chunk of each
@@ -1347,7 +1879,7 @@ bool bwd_uses_tc(long total_T, int d, int dtype) {
 }
 
 struct BwdLayout {
-    size_t tables, S, dS, tc, total;
+    size_t tables, S, dS, Tm, tc, total;
 };
 BwdLayout bwd_layout(bool varlen, int n_seq, int T, int total_T, int H, int d, int dtype) {
     const long nchunks = bwd_chunks(varlen, n_seq, T, total_T);
@@ -1355,10 +1887,12 @@ BwdLayout bwd_layout(bool varlen, int n_seq, int T, int total_T, int H, int d, i
     L.tables = 0;
     const size_t tab = varlen ? ((size_t)n_seq + 1 + (size_t)nchunks) * sizeof(int) : 0;
     L.S = (tab + 255) / 256 * 256;
+    const bool tc = bwd_uses_tc(total_T, d, dtype);
     L.dS = L.S + (size_t)nchunks * H * d * d * sizeof(float);
-    L.tc = L.dS + (size_t)nchunks * H * d * d * sizeof(float);
-    L.total = L.tc + (bwd_uses_tc(total_T, d, dtype) ? chunk_tc_workspace_bytes(nchunks, H, n_seq)
-                                                     : 0);
+    L.Tm = L.dS + (size_t)nchunks * H * d * d * sizeof(float);
+    // tensor-core path: T (bf16) of every chunk slot, then the forward's workspace
+    L.tc = L.Tm + (tc ? ((size_t)nchunks * H * C * C * 2 + 1023) / 1024 * 1024 : 0);
+    L.total = L.tc + (tc ? chunk_tc_workspace_bytes(nchunks, H, n_seq) : 0);
     return L;
 }
 
@@ -1394,6 +1928,7 @@ cudaError_t launch_bwd_t(const BwdProblem &p0, cudaStream_t s) {
     float *g_ws = nullptr;
     void *W_ws = nullptr, *A_ws = nullptr;
     if (tc) {
+        f.T_chk = ws + L.Tm;
         f.ws = ws + L.tc;
         f.ws_bytes = L.total - L.tc;
         chunk_tc_ws_views(f.ws, nchunks, p.H, p.n_seq, &g_ws, &W_ws, &A_ws);
@@ -1434,8 +1969,32 @@ cudaError_t launch_bwd_t(const BwdProblem &p0, cudaStream_t s) {
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 3. token gradients, one CTA per chunk slot
-    bwd_grads_kernel<Tin, D><<<dim3((unsigned)nchunks, p.H), NT, sizeof(GrSmem<D>), s>>>(
-        p, nch_fixed, S_chk, dS_chk);
+    if (tc) {
+        static bool gattr = false;
+        if (!gattr) {
+            if ((e = cudaFuncSetAttribute(bwd_grads_tc_kernel,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)gtc::SMEM)) != cudaSuccess)
+                return e;
+            gattr = true;
+        }
+        CUtensorMap mq, mk, mv, mo, mt, ma, mdq, mdk, mdv;
+        const long slots = nchunks * p.H;
+        if (!tmap::rows_3d(&mq, p.q, p.H, p.total_T, C) || !tmap::rows_3d(&mk, p.k, p.H, p.total_T, C) ||
+            !tmap::rows_3d(&mv, p.v, p.H, p.total_T, C) ||
+            !tmap::rows_3d(&mo, p.dout, p.H, p.total_T, C) ||
+            !tmap::plain_2d(&mt, f.T_chk, C, slots * C, C) ||
+            !tmap::plain_2d(&ma, A_ws, C, slots * C, C) ||
+            !tmap::rows_3d(&mdq, p.dq, p.H, p.total_T, C) ||
+            !tmap::rows_3d(&mdk, p.dk, p.H, p.total_T, C) ||
+            !tmap::rows_3d(&mdv, p.dv, p.H, p.total_T, C))
+            return cudaErrorInvalidValue;
+        bwd_grads_tc_kernel<<<dim3((unsigned)nchunks, p.H), gtc::NTH, gtc::SMEM, s>>>(
+            mq, mk, mv, mo, mt, ma, mdq, mdk, mdv, p, nch_fixed, S_chk, dS_chk, g_ws);
+    } else {
+        bwd_grads_kernel<Tin, D><<<dim3((unsigned)nchunks, p.H), NT, sizeof(GrSmem<D>), s>>>(
+            p, nch_fixed, S_chk, dS_chk);
+    }
     note_launch();
     return cudaGetLastError();
 }
