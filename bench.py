@@ -47,8 +47,8 @@ if ROOT not in sys.path:
 METRIC = "KLA chunkwise prefill tokens/s & % roofline; decode steps/s at B=256"
 # DRAM bytes (read + write) per call from an ncu capture of the kernels as
 # they are now, or None where the kernels changed after the last capture.
-TRAFFIC = {"layer_prefill": None, "long_context": None, "varlen_64": None,
-           "decode_b256": 2 * (135.83e6 + 74.59e6), "ccq": None}
+TRAFFIC = {"layer_prefill": 55.78e6 + 16.38e6, "long_context": None, "varlen_64": None,
+           "decode_b256": 2 * (135.83e6 + 74.59e6), "ccq": 33.90e6 + 0.12e6}
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 BYTES_PER_TOKEN_HEAD = 1032          # q,k,v,o bf16 (4 x 256 B) + alpha, eta fp32 (8 B)
 CHUNK = 64
@@ -682,7 +682,7 @@ def ours(args):
                 "roofline": {"bound": "hbm", "achieved": bw_gbs, "peak": pk["hbm_gbs"],
                              "unit": "GB/s", "frac": bw_gbs / pk["hbm_gbs"], "traffic": None,
                              "kernel": "intra_kernel + state_kernel (recording the states) + "
-                                       "bwd_dstate_tc_kernel + bwd_grads_kernel",
+                                       "bwd_dstate_tc_kernel + bwd_grads_tc_kernel",
                              "algorithmic_bytes_per_call": bw["bytes"]}}
 
     cfg = head["config"]
