@@ -1932,6 +1932,9 @@ cudaError_t launch_bwd_t(const BwdProblem &p0, cudaStream_t s) {
         f.ws = ws + L.tc;
         f.ws_bytes = L.total - L.tc;
         chunk_tc_ws_views(f.ws, nchunks, p.H, p.n_seq, &g_ws, &W_ws, &A_ws);
+        // the single-launch form's ready flags start at zero
+        const size_t reset = chunk_tc_reset_bytes(f, nchunks);
+        if (reset > 0 && (e = cudaMemsetAsync(f.ws, 0, reset, s)) != cudaSuccess) return e;
         e = launch_chunk_tc(f, nchunks, s);
     } else {
         e = launch_chunk_simt(f, s);

@@ -283,7 +283,7 @@ constexpr long long kStaggerLimitCycles = 40000;
 // bounded wait).  Two workers that start together wait for their loads
 // together and then compete for the same pipes through every step of the
 // item; offset by half an item, one computes while the other loads.
-template <bool kFused>
+template <bool kFused, bool kRecord = true>
 __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorMap *mk,
                                           const CUtensorMap *mv, const CUtensorMap *mw,
                                           const CUtensorMap *mu, const TcParams &p, long n_pairs,
@@ -645,7 +645,7 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
             pk[2 * i] = pack_bf2(v.x * bs[0], v.y * bs[1]);
             pk[2 * i + 1] = pack_bf2(v.z * bs[2], v.w * bs[3]);
         }
-        if (!kFused && p.T_chk && vslot) {   // T row t, columns [32 hf, 32 hf + 32), for the backward
+        if (kRecord && p.T_chk && vslot) {   // T row t, columns [32 hf, 32 hf + 32), for the backward
             uint4 *dst = reinterpret_cast<uint4 *>(p.T_chk + slot_row * 64 + 32 * hf);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
@@ -871,7 +871,7 @@ __device__ __forceinline__ void st_row_bf16x32(unsigned char *tile, int row, int
 // (1024-aligned, P2Cfg<kW>::SMEM - 1024 bytes).  kFused: phase 1 runs in the
 // same launch, and the load of chunk c waits for the ready flag of the work
 // item that holds it.
-template <bool kFused, bool kSplit, int kW = 64>
+template <bool kFused, bool kSplit, int kW = 64, bool kRecord = true>
 __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorMap *mk,
                                           const CUtensorMap *mw, const CUtensorMap *mu,
                                           const CUtensorMap *ma, const TcParams &p,
@@ -1096,7 +1096,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 fail();
                 break;
             }
-            if (!kFused && p.S_chk) {   // S at the chunk's start, for the backward
+            if (kRecord && p.S_chk) {   // S at the chunk's start, for the backward
 #pragma unroll
                 for (int jj = 0; jj < NJ; ++jj) {
                     float4 *dst = reinterpret_cast<float4 *>(
@@ -1280,7 +1280,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                                   *reinterpret_cast<uint32_t(*)[16]>(yr));
                     }
                     tmem_ld_wait();
-                    if (L < nc && (kFused || p.o != nullptr)) {
+                    if (L < nc && (!kRecord || (phi ? p.o_phi : p.o) != nullptr)) {
                         uint4 *dst = reinterpret_cast<uint4 *>((phi ? p.o_phi : p.o) +
                                                                (size_t)(start + (long)c * C + L) * rs +
                                                                (size_t)h * D + j0 + cg);
@@ -1354,7 +1354,9 @@ constexpr int FU_THREADS = 2 * P1_THREADS;
 static_assert(FU_THREADS >= P2_THREADS, "fused block size");
 constexpr uint32_t FU_SMEM = P2_SMEM > 2 * P1_REGION + 1024 ? P2_SMEM : 2 * P1_REGION + 1024;
 
-template <bool kSplit>
+// kRecord: the call records S and T of every chunk for the backward (and
+// may write no outputs); the other instantiations carry no recording code.
+template <bool kSplit, bool kRecord>
 __global__ void __launch_bounds__(FU_THREADS, 1)
 fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mw,
@@ -1371,18 +1373,20 @@ fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         // stages they keep in flight do not fit beside a 128-column tile
         const int unit = (int)blockIdx.x >> 1, jh = (int)blockIdx.x & 1;
         if ((int)blockIdx.x < n_state && jh < pre && tid < P1_THREADS)
-            intra_run<true>(&mq, &mk, &mv, &mw, &mu, p, n_pairs, sm, tid, 1,
-                            (long)jh * p.n_units + unit, n_items);
+            intra_run<true, kRecord>(&mq, &mk, &mv, &mw, &mu, p, n_pairs, sm, tid, 1,
+                                     (long)jh * p.n_units + unit, n_items);
         if (tid < P2_THREADS)
-            state_run<true, kSplit, 64>(&mq, &mk, &mw, &mu, &ma, p, sm, (int)blockIdx.x, tid);
+            state_run<true, kSplit, 64, kRecord>(&mq, &mk, &mw, &mu, &ma, p, sm, (int)blockIdx.x,
+                                                 tid);
         return;
     }
     __shared__ int stagger;
     if (tid == 0) stagger = 0;
     __syncthreads();
     const int w = tid / P1_THREADS;
-    intra_run<true>(&mq, &mk, &mv, &mw, &mu, p, n_pairs, sm + w * P1_REGION, tid % P1_THREADS,
-                    1 + w, (long)pre * p.n_units, 0, &stagger, 1 + w);   // items from the shared counter
+    intra_run<true, kRecord>(&mq, &mk, &mv, &mw, &mu, p, n_pairs, sm + w * P1_REGION,
+                             tid % P1_THREADS, 1 + w, (long)pre * p.n_units, 0, &stagger,
+                             1 + w);   // items from the shared counter
 }
 
 // ===================================================================== varlen prep
@@ -1759,7 +1763,8 @@ SplitLayout split_layout(int n_seq, int T, int H, int P) {
 // phase 1 its items arrive more slowly than the chain consumes them.
 bool use_fused(const Problem &p) {
     if (p.cu_seqlens != nullptr || p.T <= 0) return false;
-    const int P = split_factor(p.n_seq, p.T, p.H, false);
+    // a call recording the chunk-start states for the backward does not split
+    const int P = p.S_chk ? 1 : split_factor(p.n_seq, p.T, p.H, false);
     const int nch = (p.T / P + C - 1) / C;
     if (nch % 2 != 0) return false;
     return 2 * split_chains((long)p.n_seq * p.H, P) <= sm_count() / 2;
@@ -1815,7 +1820,7 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     if (encode_fn() == nullptr) return cudaErrorNotSupported;
     // a split sequence runs as P virtual sequences of T / P tokens (same rows,
     // same chunk slots)
-    const bool record = p0.S_chk != nullptr;   // backward recording: two launches, no split
+    const bool record = p0.S_chk != nullptr;   // backward recording: no split
     const int P = !record ? split_factor(p0.n_seq, p0.T, p0.H, p0.cu_seqlens != nullptr) : 1;
     Problem p = p0;
     if (P > 1) {
@@ -1841,7 +1846,7 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     tp.eta = p.eta;
     tp.S0 = p.S0;
     tp.S_T = p.S_T;
-    const bool fused = !record && use_fused(p0);
+    const bool fused = use_fused(p0);
     bool wide_split = !fused && split_wide((long)p0.n_seq * p0.H, P);
     if (P > 1) {   // the virtual sequences' end states go to N, not to S_T
         tp.S_T = reinterpret_cast<float *>(ws + split_base + SL.N);
@@ -1896,10 +1901,13 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     if (fused) {
         static bool fattr = false;
         if (!fattr) {
-            if ((e = cudaFuncSetAttribute(fused_kernel<false>,
+            if ((e = cudaFuncSetAttribute(fused_kernel<false, false>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)FU_SMEM)) != cudaSuccess ||
-                (e = cudaFuncSetAttribute(fused_kernel<true>,
+                (e = cudaFuncSetAttribute(fused_kernel<true, false>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)FU_SMEM)) != cudaSuccess ||
+                (e = cudaFuncSetAttribute(fused_kernel<false, true>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)FU_SMEM)) != cudaSuccess)
                 return e;
@@ -1929,10 +1937,12 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = P > 1 ? cudaLaunchKernelEx(&cfg, fused_kernel<true>, mq, mk, mv, mw, mu, ma, tp,
-                                       n_pairs, n_state, n_phi)
-                  : cudaLaunchKernelEx(&cfg, fused_kernel<false>, mq, mk, mv, mw, mu, ma, tp,
-                                       n_pairs, n_state, n_phi);
+        e = record  ? cudaLaunchKernelEx(&cfg, fused_kernel<false, true>, mq, mk, mv, mw, mu, ma,
+                                         tp, n_pairs, n_state, n_phi)
+            : P > 1 ? cudaLaunchKernelEx(&cfg, fused_kernel<true, false>, mq, mk, mv, mw, mu, ma,
+                                         tp, n_pairs, n_state, n_phi)
+                    : cudaLaunchKernelEx(&cfg, fused_kernel<false, false>, mq, mk, mv, mw, mu, ma,
+                                         tp, n_pairs, n_state, n_phi);
         if (e == cudaSuccess) {
             note_launch();
             if (P == 1) return cudaSuccess;
