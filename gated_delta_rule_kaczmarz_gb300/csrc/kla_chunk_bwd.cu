@@ -300,8 +300,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_dstate_kernel(BwdProblem p, float *
 // brings each chunk's K, Q, dO (token rows), W and A^T (workspace) by TMA,
 // two chunks in flight; an MMA warp issues the products; eight main warps
 // hold the state, thread (lane j, half hf) the columns i in [64 hf, 64 hf + 64)
-// of row j of dS^T (so that the recorded dS' rows, fixed i, are written by
-// a warp as 32 consecutive floats).
+// of row j of dS^T (so that dS0's rows, fixed i, are written by
+// a warp as 32 consecutive floats), and dS' of every chunk is recorded as
+// the bf16 dS'^T tile that feeds X (a bulk copy of shared memory).
 namespace dtc {
 constexpr int D = 128;
 constexpr int NS = 2;                                // stages
@@ -330,7 +331,7 @@ __device__ __forceinline__ uint32_t dtc_pack(float a, float b) {
 __global__ void __launch_bounds__(dtc::THREADS, 1)
 bwd_dstate_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mw,
-                     const __grid_constant__ CUtensorMap ma, BwdProblem p, float *dS_chk,
+                     const __grid_constant__ CUtensorMap ma, BwdProblem p, unsigned char *dS_img,
                      const float *g_ws) {
     using namespace dtc;
     using namespace tc;
@@ -448,12 +449,17 @@ bwd_dstate_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_consta
         }
         for (int k = 0; ok && k < nch; ++k) {
             const uint32_t st = smem_u32(sm + (k % NS) * ST_BYTES);
-            // X = dS'^T K^T once dS'^T is in shared memory
+            // X = dS'^T K^T once dS'^T is in shared memory; dS' of the step's
+            // chunk recorded as that bf16 tile (32 KB image)
             if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_s, (uint32_t)(k & 1), &sAbort))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            if (lane == 0) {
+                bulk_store(dS_img + (size_t)slot_of(k) * 32768, sS, 32768u);
+                bulk_commit_group();
+            }
             if (lane == 0) {
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
@@ -463,12 +469,14 @@ bwd_dstate_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_consta
                 mma_commit(&bar_x);
             }
             __syncwarp();
-            // D += (-dU^T) W once dU^T (bf16) is in TMEM
+            // D += (-dU^T) W once dU^T (bf16) is in TMEM; the record has read
+            // dS'^T before D lets the main warps overwrite it
             if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_u, (uint32_t)(k & 1), &sAbort))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            if (lane == 0) bulk_wait_group_read0();
             if (lane == 0) {
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
@@ -493,7 +501,10 @@ bwd_dstate_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_consta
             }
         }
         if (!ok) fail();
-        if (lane == 0) mma_commit(&bar_fin);
+        if (lane == 0) {
+            mma_commit(&bar_fin);
+            bulk_wait_group0();
+        }
         __syncwarp();
         (void)mbar_wait(&bar_fin, 0u);
     } else {
@@ -506,12 +517,6 @@ bwd_dstate_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_consta
 #pragma unroll
         for (int x = 0; x < 64; ++x)
             ds[x] = p.dS_T ? p.dS_T[sbase + (size_t)(64 * hf + x) * D + j] : 0.f;
-        // dS' (rows i = 64 hf + x, column j) of the chunk of step k; coalesced over j
-        auto record = [&](int k) {
-            float *rec = dS_chk + (size_t)slot_of(k) * D * D + (size_t)(64 * hf) * D + j;
-#pragma unroll
-            for (int x = 0; x < 64; ++x) rec[(size_t)x * D] = ds[x];
-        };
         // bf16 row j of dS'^T into shared memory (the A operand of X)
         auto put_state = [&]() {
 #pragma unroll
@@ -572,7 +577,6 @@ bwd_dstate_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_consta
 
         bool ok = true;
         if (nch > 0) {
-            record(0);
             put_state();
             ok = prep(0);
             if (!ok) fail();
@@ -630,10 +634,7 @@ bwd_dstate_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_consta
                 }
             }
             tc_fence_before();
-            if (k + 1 < nch) {
-                record(k + 1);
-                put_state();
-            }
+            if (k + 1 < nch) put_state();
         }
         if (ok && !sAbort && p.dS0) {
 #pragma unroll
@@ -1277,8 +1278,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch_
 
 // ------------------------------------------------------ token gradients (tcgen05)
 // bf16 with d = 128: per chunk, the products of the gradient lines above on
-// the tensor cores, from the recorded S and dS' (fp32, converted to bf16 in
-// shared memory), the forward's T (bf16) and A^T, g of the chunk workspace.
+// the tensor cores, from the recorded S and dS'^T (bf16 operand tiles as the
+// forward's state pass and the dS chain held them, loaded by bulk copies),
+// the forward's T (bf16) and A^T, g of the chunk workspace.
 // Every product has M = 128 token rows: a chunk has 64, so two 64-row tiles
 // stored slab by slab one after the other act as one 128-row operand and
 // share the product ([dR ; dO] S^T gives dR S^T and dO S^T = pq; [dR ; dO] U^T
@@ -1292,7 +1294,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch_
 //   2. U = T R, dR = T^T dU  -> dV = diag(beta) dR, dbeta and dg from R
 //   3. [dR ; dO] U^T, U dS'^T, [dR ; dO] S^T  -> M1, X, their dg and dbeta terms
 //   4. [X + X^T ; M1] K + M1^T Q  -> dQ (lanes 64..), dK (lanes 0..63)
-// Shared memory (offsets in KB): [K | Q] 0, [dR | dO] 32, V 64, S 80, dS' 112,
+// Shared memory (offsets in KB): [K | Q] 0, [dR | dO] 32, V 64, S 80, dS'^T 112,
 // T 144, A^T 152, R 160, U 176, dU 192, vectors 208; reused: dV staging and
 // then [X + X^T | M1] in R, the column-sum scratch in dU and V, X (fp32) in
 // S, zeros in U, dK staging in S and dQ staging in dU.
@@ -1343,7 +1345,7 @@ bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
                     const __grid_constant__ CUtensorMap mt, const __grid_constant__ CUtensorMap ma,
                     const __grid_constant__ CUtensorMap mdq, const __grid_constant__ CUtensorMap mdk,
                     const __grid_constant__ CUtensorMap mdv, BwdProblem p, int nch_fixed,
-                    const float *S_chk, const float *dS_chk, const float *g_ws) {
+                    const unsigned char *S_img, const unsigned char *dS_img, const float *g_ws) {
     using namespace gtc;
     using namespace tc;
     extern __shared__ unsigned char g_smem[];
@@ -1397,9 +1399,12 @@ bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         tc_fence_after();
     };
 
-    // ---- loads: K, Q, dO, V (token rows), T, A^T (chunk slot), g
+    // ---- loads: K, Q, dO, V (token rows), T, A^T (chunk slot), g, and the
+    //      recorded bf16 tiles of S (rows i) and dS'^T (rows j), 32 KB each
     if (tid == 0) {
-        mbar_expect_tx(&bar_ld, 10u * SL + 256u);
+        mbar_expect_tx(&bar_ld, 10u * SL + 256u + 65536u);
+        bulk_load(sm + O_S, S_img + slot * 32768, 32768u, &bar_ld);
+        bulk_load(sm + O_DS, dS_img + slot * 32768, 32768u, &bar_ld);
 #pragma unroll
         for (int s2 = 0; s2 < 2; ++s2) {
             tma_load_3d(sm + O_KQ + s2 * 2 * SL, &mk, &bar_ld, 64 * s2, h, (int)row0);
@@ -1417,24 +1422,26 @@ bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         valpha[tid] = (ok && p.alpha) ? p.alpha[r] : 1.f;
         veta[tid] = ok ? p.eta[r] : 0.f;
     }
-    // ---- S and dS' of the chunk (fp32) to bf16 tiles (rows i, columns j in
-    //      two slabs of 128 rows); sum of S o dS' on the way
+    if (!mbar_wait(&bar_ld, 0u)) sBad = 1;
+    // ---- sum of S o dS' (the dg_C term): row i of S, column i of dS'^T,
+    //      the half jq of the columns j
     float sds = 0.f;
     {
-        const float *S = S_chk + slot * 128 * 128, *dSp = dS_chk + slot * 128 * 128;
-        const int cq = tid & 31;   // float4 column group: j = 4 cq .. 4 cq + 3
-#pragma unroll 4
-        for (int r = 0; r < 16; ++r) {
-            const int i = (tid >> 5) + 8 * r;
-            const float4 a = *reinterpret_cast<const float4 *>(S + (size_t)i * 128 + 4 * cq);
-            const float4 b = *reinterpret_cast<const float4 *>(dSp + (size_t)i * 128 + 4 * cq);
-            sds = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, sds))));
-            const uint32_t off = (uint32_t)((4 * cq) >> 6) * 16 * KB + sw128_offset(i, (4 * cq) & 63);
-            *reinterpret_cast<uint2 *>(sm + O_S + off) = make_uint2(g_pack(a.x, a.y), g_pack(a.z, a.w));
-            *reinterpret_cast<uint2 *>(sm + O_DS + off) = make_uint2(g_pack(b.x, b.y), g_pack(b.z, b.w));
+        const int i = tid >> 1, jq = tid & 1;
+        const unsigned char *srow = sm + O_S + jq * 16 * KB;
+        const unsigned char *dcol = sm + O_DS + (i >> 6) * 16 * KB;
+#pragma unroll 2
+        for (int c8 = 0; c8 < 8; ++c8) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(srow + sw128_offset(i, 8 * c8));
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = 64 * jq + 8 * c8 + 2 * e;
+                sds = fmaf(g_lo(ww[e]), g_at(dcol, j, i & 63), sds);
+                sds = fmaf(g_hi(ww[e]), g_at(dcol, j + 1, i & 63), sds);
+            }
         }
     }
-    if (!mbar_wait(&bar_ld, 0u)) sBad = 1;
     // ---- rows past the sequence's end: K, Q, dO, V cleared; chunk vectors
     if (nc < C) {
         for (int e = tid; e < (C - nc) * 16; e += NTH) {
@@ -1470,6 +1477,7 @@ bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     if (tid == 0) {
         tc_fence_after();
         constexpr uint32_t id_mn = idesc_bf16_f32(128, 128, false, true);
+        constexpr uint32_t id_k128 = idesc_bf16_f32(128, 128, false, false);
         constexpr uint32_t id_kk = idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)   // K S: B = S read MN-major (n = j, k = i)
@@ -1478,8 +1486,8 @@ bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         for (int ks = 0; ks < 4; ++ks)   // A_qk^T dO: A = A^T rows t, B = dO (n = j, k = s)
             mma_bf16(tb + C_B, gk_desc(aA, ks, 0), gm_desc(aRO + SL, ks, 2 * SL), id_mn, ks > 0);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)   // K dS'
-            mma_bf16(tb + C_C, gk_desc(aKQ, ks, 2 * SL), gm_desc(aDS, ks, 16 * KB), id_mn, ks > 0);
+        for (int ks = 0; ks < 8; ++ks)   // K dS': B = dS'^T rows j (K-major)
+            mma_bf16(tb + C_C, gk_desc(aKQ, ks, 2 * SL), gk_desc(aDS, ks, 16 * KB), id_k128, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)   // [K ; Q] K^T
             mma_bf16(tb + C_G, gk_desc(aKQ, ks, 2 * SL), gk_desc(aKQ, ks, 2 * SL), id_kk, ks > 0);
@@ -1596,12 +1604,13 @@ bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         tc_fence_after();
         constexpr uint32_t id_64 = idesc_bf16_f32(128, 64, false, false);
         constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, false, false);
+        constexpr uint32_t id_umn = idesc_bf16_f32(128, 128, false, true);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)   // [dR ; dO] U^T: B = U rows s (K-major)
             mma_bf16(tb + C_A, gk_desc(aRO, ks, 2 * SL), gk_desc(aU, ks, SL), id_64, ks > 0);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)   // U dS'^T: B = dS' rows i (K-major)
-            mma_bf16(tb + C_B, gk_desc(aU, ks, SL), gk_desc(aDS, ks, 16 * KB), id_kk, ks > 0);
+        for (int ks = 0; ks < 8; ++ks)   // U dS'^T: B = dS'^T read MN-major (n = i, k = j)
+            mma_bf16(tb + C_B, gk_desc(aU, ks, SL), gm_desc(aDS, ks, 16 * KB), id_umn, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)   // [dR ; dO] S^T
             mma_bf16(tb + C_C, gk_desc(aRO, ks, 2 * SL), gk_desc(aS, ks, 16 * KB), id_kk, ks > 0);
@@ -1888,8 +1897,11 @@ BwdLayout bwd_layout(bool varlen, int n_seq, int T, int total_T, int H, int d, i
     const size_t tab = varlen ? ((size_t)n_seq + 1 + (size_t)nchunks) * sizeof(int) : 0;
     L.S = (tab + 255) / 256 * 256;
     const bool tc = bwd_uses_tc(total_T, d, dtype);
-    L.dS = L.S + (size_t)nchunks * H * d * d * sizeof(float);
-    L.Tm = L.dS + (size_t)nchunks * H * d * d * sizeof(float);
+    // S and dS' per chunk slot: fp32 [d][d], or on the tensor-core path the
+    // two 32 KB bf16 tile images
+    const size_t per = tc ? 32768 : (size_t)d * d * sizeof(float);
+    L.dS = L.S + (size_t)nchunks * H * per;
+    L.Tm = L.dS + (size_t)nchunks * H * per;
     // tensor-core path: T (bf16) of every chunk slot, then the forward's workspace
     L.tc = L.Tm + (tc ? ((size_t)nchunks * H * C * C * 2 + 1023) / 1024 * 1024 : 0);
     L.total = L.tc + (tc ? chunk_tc_workspace_bytes(nchunks, H, n_seq) : 0);
@@ -1964,8 +1976,8 @@ cudaError_t launch_bwd_t(const BwdProblem &p0, cudaStream_t s) {
             !tmap::rows_3d(&mo, p.dout, p.H, p.total_T, C) ||
             !tmap::plain_2d(&mw, W_ws, D, slots * C, C) || !tmap::plain_2d(&ma, A_ws, C, slots * C, C))
             return cudaErrorInvalidValue;
-        bwd_dstate_tc_kernel<<<units, dtc::THREADS, dtc::SMEM, s>>>(mq, mk, mo, mw, ma, p, dS_chk,
-                                                                     g_ws);
+        bwd_dstate_tc_kernel<<<units, dtc::THREADS, dtc::SMEM, s>>>(
+            mq, mk, mo, mw, ma, p, reinterpret_cast<unsigned char *>(dS_chk), g_ws);
     } else {
         bwd_dstate_kernel<Tin, D><<<dim3(units, D / DVB), NT, sizeof(DsSmem<D>), s>>>(p, dS_chk);
     }
@@ -1993,7 +2005,9 @@ cudaError_t launch_bwd_t(const BwdProblem &p0, cudaStream_t s) {
             !tmap::rows_3d(&mdv, p.dv, p.H, p.total_T, C))
             return cudaErrorInvalidValue;
         bwd_grads_tc_kernel<<<dim3((unsigned)nchunks, p.H), gtc::NTH, gtc::SMEM, s>>>(
-            mq, mk, mv, mo, mt, ma, mdq, mdk, mdv, p, nch_fixed, S_chk, dS_chk, g_ws);
+            mq, mk, mv, mo, mt, ma, mdq, mdk, mdv, p, nch_fixed,
+            reinterpret_cast<const unsigned char *>(S_chk), reinterpret_cast<const unsigned char *>(dS_chk),
+            g_ws);
     } else {
         bwd_grads_kernel<Tin, D><<<dim3((unsigned)nchunks, p.H), NT, sizeof(GrSmem<D>), s>>>(
             p, nch_fixed, S_chk, dS_chk);

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(NT, 1) chunk_simt_kernel(Problem p) {
         const int nc = (int)min((long)C, len - c0);
         __syncthreads();  // previous chunk finished with K, Q, V, S
         if (p.S_chk) {    // the state at the chunk's start, for the backward pass
-            float *dst = p.S_chk + ((size_t)(chunk0 + c0 / C) * H + h) * D * D;
+            float *dst = static_cast<float *>(p.S_chk) + ((size_t)(chunk0 + c0 / C) * H + h) * D * D;
             for (int x = tid; x < D * DVB; x += NT) {
                 const int i = x / DVB, j = x % DVB;
                 dst[(size_t)i * D + jb + j] = sm.S[i][j];

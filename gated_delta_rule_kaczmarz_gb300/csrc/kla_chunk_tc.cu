@@ -79,11 +79,12 @@ struct TcParams {
     int seg_P, phi_first;
     __nv_bfloat16 *o_phi;
     float *S_T_phi;
-    // Recording for the backward pass (two-launch path only): the state at
-    // every chunk start ([chunk slots][128][128] fp32, slot = chunk * H +
-    // head) and T of every chunk slot ([slots][64][64] bf16); o may then be
+    // Recording for the backward pass: the state at every chunk start (per
+    // slot = chunk * H + head, two 16 KB images of the bf16 operand tiles of
+    // its column halves, copied from shared memory as the state pass holds
+    // them) and T of every chunk slot ([slots][64][64] bf16); o may then be
     // null.
-    float *S_chk;
+    unsigned char *S_chk;
     __nv_bfloat16 *T_chk;
     unsigned *flags;           // fused launch: one ready flag per work item, then the work-item
                                // counter (all zeroed per call)
@@ -973,6 +974,14 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                             mbar_wait_or_abort(&bar_s, par, &sAbort);
             if (!__all_sync(0xffffffffu, ok)) { fail(); break; }
             tc_fence_after();
+            if (kRecord && p.S_chk && !phi && lane == 0) {
+                // S at the chunk's start, for the backward: the bf16 tile as it is
+                unsigned char *dst = p.S_chk + ((size_t)(chunk0 + c) * p.H + h) * 32768 + 16384 * jh;
+#pragma unroll
+                for (int sl = 0; sl < kW / 64; ++sl)
+                    bulk_store(dst + 16384 * sl, sS + sl * Cf::S_SLAB, 16384u);
+                bulk_commit_group();
+            }
             if (lane == 0) {
                 const uint32_t aQW = smem_u32(st + ST_QW);
 #pragma unroll
@@ -986,6 +995,8 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             __syncwarp();
             if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_u, par, &sAbort))) { fail(); break; }
             tc_fence_after();
+            // the recorded copy has read S_c before Z lets the main warps overwrite it
+            if (kRecord && p.S_chk && !phi && lane == 0) bulk_wait_group_read0();
             if (lane == 0) {
                 const uint32_t aKT = smem_u32(st + ST_KT), aA = smem_u32(st + ST_A);
                 // Z = K^T U': A = K read MN-major (M = dk, two 64-feature blocks)
@@ -1008,6 +1019,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         }
         // every MMA issued has completed before the CTA releases its TMEM
         if (lane == 0) mma_commit(&bar_fin);
+        if (kRecord && p.S_chk && lane == 0) bulk_wait_group0();
         __syncwarp();
         (void)mbar_wait(&bar_fin, 0u);
     } else if (warp == NMAIN + 1) {
@@ -1095,18 +1107,6 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_ld[b], par_st, &sAbort))) {
                 fail();
                 break;
-            }
-            if (kRecord && p.S_chk) {   // S at the chunk's start, for the backward
-#pragma unroll
-                for (int jj = 0; jj < NJ; ++jj) {
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        p.S_chk + ((size_t)(chunk0 + c) * p.H + h) * D * D + (size_t)L * D + j0 +
-                        c0 + 32 * jj);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(Sr[jj][4 * i], Sr[jj][4 * i + 1], Sr[jj][4 * i + 2],
-                                             Sr[jj][4 * i + 3]);
-                }
             }
             // what the stage alone gives (g, the decay factors, the U~ words) is
             // read before the wait for the product
@@ -1896,7 +1896,7 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     }
     const long n_pairs = (n_chunks_upper + 1) / 2;
     const long n_items = n_pairs * p.H;
-    tp.S_chk = p0.S_chk;
+    tp.S_chk = static_cast<unsigned char *>(p0.S_chk);
     tp.T_chk = static_cast<__nv_bfloat16 *>(p0.T_chk);
     if (fused) {
         static bool fattr = false;

@@ -36,8 +36,11 @@ struct Problem {
     int H, d;                // heads, dk == dv
     int dtype;               // kla_dtype
     int beta_mode;           // 0: beta = eta / (||k||^2 + eps); 1: beta = eta
-    float *S_chk;            // the state at every chunk start for the backward pass
-                             // ([chunk slots, d, d] fp32, slot = chunk * H + head), or nullptr
+    void *S_chk;             // the state at every chunk start for the backward pass, or
+                             // nullptr; slot = chunk * H + head.  CUDA-core path: [slots, d, d]
+                             // fp32; tensor-core path: per slot the two 16 KB images of the
+                             // bf16 128 x 64 operand tiles of the state's column halves
+                             // (128-byte swizzle), as the state pass holds them
     const int *chunk_prefix; // CUDA-core varlen recording: first chunk of each sequence
     void *T_chk;             // tensor-core path with S_chk: T of every chunk slot
                              // ([slots, 64, 64] bf16), or nullptr
