@@ -27,8 +27,6 @@
 //     m_t = m_prev + sum_{j<=t in chunk} k_j,  n_t = n_prev + t + 1
 //     q_clean_t = q_t - lambda_t (y_t / n_t - mu_t (mu_t . q_t))
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -36,6 +34,7 @@
 
 #include "kla_internal.h"
 #include "kla_tc.cuh"
+#include "kla_tmap.h"
 
 namespace kla {
 namespace {
@@ -872,36 +871,8 @@ CcqTcPlan ccq_tc_plan(int B, int T, int H) {
     return pl;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 ccq_encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        cudaDriverEntryPointQueryResult q;
-        void *ptr = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-// [B][T][H][128] bf16 as a 4-d tensor (feature, head, token, sequence); box
-// 64 features x 1 head x 128 tokens: tokens past T read as zero, and are not
-// written by a store.
-bool ccq_map(CUtensorMap *m, const void *base, int B, int T, int H) {
-    const cuuint64_t dims[4] = {(cuuint64_t)ctc::D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
-    const cuuint64_t strides[3] = {(cuuint64_t)ctc::D * 2, (cuuint64_t)H * ctc::D * 2,
-                                   (cuuint64_t)T * H * ctc::D * 2};
-    const cuuint32_t box[4] = {64, 1, (cuuint32_t)ctc::NB, 1};
-    const cuuint32_t es[4] = {1, 1, 1, 1};
-    return ccq_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
-                           strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 cudaError_t launch_ccq_tc(const CcqProblem &p, cudaStream_t s) {
-    if (ccq_encode_fn() == nullptr) return cudaErrorNotSupported;
+    if (tmap::encode_fn() == nullptr) return cudaErrorNotSupported;
     const CcqTcPlan pl = ccq_tc_plan(p.B, p.T, p.H);
     const int units = p.B * p.H;
     CcqTcParams prm{};
@@ -912,8 +883,9 @@ cudaError_t launch_ccq_tc(const CcqProblem &p, cudaStream_t s) {
     prm.T = p.T; prm.H = p.H; prm.P = pl.P;
     for (int i = 0; i <= pl.P; ++i) prm.seg_start[i] = pl.start[i];
     CUtensorMap mq, mk, mo;
-    if (!ccq_map(&mq, p.q, p.B, p.T, p.H) || !ccq_map(&mk, p.k, p.B, p.T, p.H) ||
-        !ccq_map(&mo, p.q_clean, p.B, p.T, p.H))
+    if (!tmap::seq_4d(&mq, p.q, p.B, p.T, p.H, ctc::NB) ||
+        !tmap::seq_4d(&mk, p.k, p.B, p.T, p.H, ctc::NB) ||
+        !tmap::seq_4d(&mo, p.q_clean, p.B, p.T, p.H, ctc::NB))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(p.ws, 0, sizeof(unsigned), s);   // status word
     if (e != cudaSuccess) return e;

@@ -46,6 +46,7 @@
 
 #include "kla_internal.h"
 #include "kla_tc.cuh"
+#include "kla_tmap.h"
 
 namespace kla {
 namespace {
@@ -1639,42 +1640,6 @@ split_correct_kernel(const __grid_constant__ CUtensorMap mqc, const __grid_const
 }
 
 // ===================================================================== host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        cudaDriverEntryPointQueryResult q;
-        void *ptr = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-bool map_3d_rows(CUtensorMap *m, const void *base, int H, long rows) {
-    // [rows][H][128] bf16; box = 64 feature columns x 1 head x 64 rows
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-    const cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
-    const cuuint32_t es[3] = {1, 1, 1};
-    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                       strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
-}
-
-bool map_2d(CUtensorMap *m, const void *base, int cols, long rows, int box_rows) {
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-    const cuuint32_t es[2] = {1, 1};
-    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
-                       strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
-}
-
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Number of SMs of the current device (persistent grids).
@@ -1817,7 +1782,7 @@ cudaError_t launch_split_tail(const Problem &p0, const Problem &p, const TcParam
 
 cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t s) {
     if (p0.n_seq == 0) return cudaSuccess;
-    if (encode_fn() == nullptr) return cudaErrorNotSupported;
+    if (tmap::encode_fn() == nullptr) return cudaErrorNotSupported;
     // a split sequence runs as P virtual sequences of T / P tokens (same rows,
     // same chunk slots)
     const bool record = p0.S_chk != nullptr;   // backward recording: no split
@@ -1868,9 +1833,11 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
 
     CUtensorMap mq, mk, mv, mw, mu, ma;
     const long slots = n_chunks_upper * p.H;
-    if (!map_3d_rows(&mq, p.q, p.H, p.total_T) || !map_3d_rows(&mk, p.k, p.H, p.total_T) ||
-        !map_3d_rows(&mv, p.v, p.H, p.total_T) || !map_2d(&mw, tp.W_ws, D, slots * C, C) ||
-        !map_2d(&mu, tp.U_ws, D, slots * C, C) || !map_2d(&ma, tp.A_ws, C, slots * C, C))
+    if (!tmap::rows_3d(&mq, p.q, p.H, p.total_T, C) || !tmap::rows_3d(&mk, p.k, p.H, p.total_T, C) ||
+        !tmap::rows_3d(&mv, p.v, p.H, p.total_T, C) ||
+        !tmap::plain_2d(&mw, tp.W_ws, D, slots * C, C) ||
+        !tmap::plain_2d(&mu, tp.U_ws, D, slots * C, C) ||
+        !tmap::plain_2d(&ma, tp.A_ws, C, slots * C, C))
         return cudaErrorInvalidValue;
 
     cudaError_t e;
@@ -1991,8 +1958,9 @@ cudaError_t launch_split_tail(const Problem &p0, const Problem &p, const TcParam
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     CUtensorMap mqc, mo, mss;
-    if (!map_3d_rows(&mqc, tp.o_phi, p.H, p.total_T) || !map_3d_rows(&mo, p0.o, p.H, p.total_T) ||
-        !map_2d(&mss, Sst, D, (long)p0.n_seq * (P - 1) * p.H * D, 128))
+    if (!tmap::rows_3d(&mqc, tp.o_phi, p.H, p.total_T, C) ||
+        !tmap::rows_3d(&mo, p0.o, p.H, p.total_T, C) ||
+        !tmap::plain_2d(&mss, Sst, D, (long)p0.n_seq * (P - 1) * p.H * D, 128))
         return cudaErrorInvalidValue;
     static bool cattr = false;
     if (!cattr) {

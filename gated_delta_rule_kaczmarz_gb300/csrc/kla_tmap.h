@@ -48,5 +48,19 @@ inline bool plain_2d(CUtensorMap *m, const void *base, int cols, long rows, int 
            CUDA_SUCCESS;
 }
 
+// [B][T][H][128] bf16 as a 4-d tensor (feature, head, token, sequence): box
+// 64 features x 1 head x box_rows tokens; tokens past T read as zero and are
+// not written by a store.
+inline bool seq_4d(CUtensorMap *m, const void *base, int B, int T, int H, int box_rows) {
+    const cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {256, (cuuint64_t)H * 256, (cuuint64_t)T * H * 256};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                       strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 }  // namespace tmap
 }  // namespace kla

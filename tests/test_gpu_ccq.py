@@ -153,3 +153,40 @@ def test_ccq_stats_carry_on_tensor_cores():
     assert rel_err(torch.cat([qa, qb], 1), ref) <= 2e-2
     for x, y in zip(sb, st):
         assert rel_err(x, y.double().cpu().numpy()) <= 1e-5
+
+
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "fp32")])
+def test_ccq_lambda_zero_is_identity(d, dtype):
+    """lambda = 0 leaves the query unchanged (CCQ, "O Mecanismo": q_clean =
+    (I - lambda Sigma) q), bit for bit, on the tensor-core and CUDA-core
+    paths, while the statistics still advance."""
+    B, T, H = 2, 300, 2
+    inp = prefill_inputs(B, T, H, d, d, dtype, seed=180)
+    lam = torch.zeros(B, T, H)
+    g = cuda(inp)
+    qc, (Ms, ms, ns) = kla.kla_ccq_query(g["q"], g["k"], lam.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(qc.cpu(), inp["q"])
+    _, (Ms_ref, ms_ref, ns_ref) = oracle.ccq_query(inp["q"], inp["k"], lam)
+    assert rel_err(Ms, Ms_ref) <= 1e-5 and rel_err(ms, ms_ref) <= 1e-5
+
+
+def test_ccq_keys_with_a_common_mean_and_zero_keys():
+    """Keys k_t = mu + noise with |mu| of the order of the noise's norm (the
+    covariance is then a small difference M/n - mu mu^T), a few zero keys
+    (they still count in n_t), over several segments per sequence."""
+    B, T, H, d = 1, 1000, 2, 128
+    inp = prefill_inputs(B, T, H, d, d, "bf16", seed=181)
+    rng = np.random.default_rng(182)
+    mu = rng.standard_normal((1, 1, H, d)) / np.sqrt(d)
+    k = inp["k"].double().numpy() * 0.5 + mu
+    k[:, [0, 7, 300, 999]] = 0.0
+    inp["k"] = torch.from_numpy(k).to(torch.bfloat16)
+    lam = _lam((B, T, H), 183)
+    g = cuda(inp)
+    qc, (Ms, ms, ns) = kla.kla_ccq_query(g["q"], g["k"], lam.cuda())
+    torch.cuda.synchronize()
+    qc_ref, (Ms_ref, ms_ref, ns_ref) = oracle.ccq_query(inp["q"], inp["k"], lam)
+    assert rel_err(qc, qc_ref) <= TOL[inp["q"].dtype]
+    assert rel_err(Ms, Ms_ref) <= 1e-5 and rel_err(ms, ms_ref) <= 1e-5
+    assert np.array_equal(ns.cpu().numpy(), ns_ref)
