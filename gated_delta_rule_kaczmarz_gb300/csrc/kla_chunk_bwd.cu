@@ -1455,20 +1455,31 @@ bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         }
     }
     __syncthreads();
-    if (tid < C) {
+    {   // ||k_t||^2: four threads per row t = tid / 4, 32 features each
+        const int tr = tid >> 2, part = tid & 3;
+        const unsigned char *krow = sm + O_KQ + (part >> 1) * 2 * SL;
         float n2 = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < 128; ++i) {
-            const float k = g_at(sm + O_KQ + (i >> 6) * 2 * SL, tid, i & 63);
-            n2 = fmaf(k, k, n2);
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(krow + sw128_offset(tr, 32 * (part & 1) + 8 * c8));
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                n2 = fmaf(g_lo(ww[e]), g_lo(ww[e]), n2);
+                n2 = fmaf(g_hi(ww[e]), g_hi(ww[e]), n2);
+            }
         }
-        const float den = n2 + p.eps;
-        vden[tid] = den;
-        const float b = p.beta_mode ? veta[tid] : (den != 0.f ? veta[tid] / den : 0.f);
-        vbeta[tid] = tid < nc ? b : 0.f;
-        veg[tid] = __expf(vg[tid]);
-        vegc[tid] = __expf(vg[C - 1] - vg[tid]);
-        vdg[tid] = 0.f;
+        n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
+        n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
+        if (part == 0) {
+            const float den = n2 + p.eps;
+            vden[tr] = den;
+            const float b = p.beta_mode ? veta[tr] : (den != 0.f ? veta[tr] / den : 0.f);
+            vbeta[tr] = tr < nc ? b : 0.f;
+            veg[tr] = __expf(vg[tr]);
+            vegc[tr] = __expf(vg[C - 1] - vg[tr]);
+            vdg[tr] = 0.f;
+        }
     }
     fence_async_smem();
     __syncthreads();
@@ -1670,11 +1681,19 @@ bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         if (lower) atomicAdd(&vdbeta[t], bsum);
     }
     __syncthreads();
-    if (tid < C) {   // column sums: dg_s -= sum_r E_qk[r][s] + E_kk[r][s]
-        float cs = 0.f;
-        for (int r = 0; r < C; ++r) cs += Eqk[r * 64 + tid] + Ekk[r * 64 + tid];
-        vdg[tid] -= cs;
+    {   // column sums: dg_s -= sum_r E_qk[r][s] + E_kk[r][s]; four threads per
+        // column s = tid % 64, 16 rows each
+        const int sc = tid & 63, q = tid >> 6;
+        float c0 = 0.f, c1 = 0.f;
+#pragma unroll
+        for (int r = 16 * q; r < 16 * q + 16; r += 2) {
+            c0 += Eqk[r * 64 + sc] + Ekk[r * 64 + sc];
+            c1 += Eqk[(r + 1) * 64 + sc] + Ekk[(r + 1) * 64 + sc];
+        }
+        vp[q * 64 + sc] = c0 + c1;   // (the half partials of epilogue 2 are consumed)
     }
+    __syncthreads();
+    if (tid < C) vdg[tid] -= (vp[tid] + vp[64 + tid]) + (vp[128 + tid] + vp[192 + tid]);
     {   // X + X^T (symmetric) to the first tile of the pair; zeros (8 KB) in U
         const int r = tid >> 2, q = tid & 3;   // row r, columns 16 q .. 16 q + 15
         float xx[16];
