@@ -1296,8 +1296,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_kernel(BwdProblem p, int nch_
 //   4. [X + X^T ; M1] K + M1^T Q  -> dQ (lanes 64..), dK (lanes 0..63)
 // Shared memory (offsets in KB): [K | Q] 0, [dR | dO] 32, V 64, S 80, dS'^T 112,
 // T 144, A^T 152, R 160, U 176, dU 192, vectors 208; reused: dV staging and
-// then [X + X^T | M1] in R, the column-sum scratch in dU and V, X (fp32) in
-// S, zeros in U, dK staging in S and dQ staging in dU.
+// then [X + X^T | M1] in R, the column-sum scratch in dS'^T, T and A^T, X
+// (fp32) in S, zeros in U, dK staging in S and dQ staging in dU.
 namespace gtc {
 constexpr uint32_t KB = 1024;
 constexpr uint32_t SL = 8 * KB;        // one 64 x 64 bf16 slab (64 rows of 128 bytes)
@@ -1635,9 +1635,14 @@ bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
     __syncthreads();
     // ---- epilogue 3: lower lanes row t of dR U^T -> X and the dA_kk terms;
     //      upper lanes row t of dO U^T -> M1 = dA_qk o Gamma and its terms.
-    //      Column-sum scratch: E_qk in dU, E_kk in V (fp32 64 x 64); X in S.
-    float *Eqk = reinterpret_cast<float *>(sm + O_DU);
-    float *Ekk = reinterpret_cast<float *>(sm + O_V);
+    //      fp32 64 x 64 scratch with rows EL floats apart (a thread writes its
+    //      row in 16-byte pieces; the 8 rows of a quarter warp fall in 8
+    //      different bank groups): E_qk and E_kk for the column sums in the
+    //      dS'^T, T and A^T tiles, X in the S tile (all read by the products).
+    constexpr int EL = 68;
+    static_assert(2 * 64 * EL * 4 <= O_R - O_DS && 64 * EL * 4 <= O_DS - O_S, "scratch");
+    float *Eqk = reinterpret_cast<float *>(sm + O_DS);
+    float *Ekk = Eqk + 64 * EL;
     float *Xs = reinterpret_cast<float *>(sm + O_S);
     {
         const float gt = vg[t];
@@ -1649,30 +1654,38 @@ bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         float rsum = 0.f, bsum = 0.f;
         if (lower) {
             const float bt = vbeta[t];
-            float xrow[32];
+            float xrow[32], erow[32];
 #pragma unroll
             for (int x = 0; x < 32; ++x) {
                 const int s2 = s0 + x;
                 const float xg = s2 < t ? -__uint_as_float(dr[x]) * __expf(gt - vg[s2]) : 0.f;
                 const float e = xg * __uint_as_float(gr[x]);   // . k_t k_s
                 bsum += e;
-                Ekk[t * 64 + s2] = bt * e;                     // dA_kk o A_kk
+                erow[x] = bt * e;                              // dA_kk o A_kk
                 xrow[x] = bt * xg;                             // X
             }
             rsum = bt * bsum;
 #pragma unroll
-            for (int x = 0; x < 32; ++x) Xs[t * 64 + s0 + x] = xrow[x];
+            for (int x = 0; x < 32; x += 4) {
+                *reinterpret_cast<float4 *>(Ekk + t * EL + s0 + x) =
+                    make_float4(erow[x], erow[x + 1], erow[x + 2], erow[x + 3]);
+                *reinterpret_cast<float4 *>(Xs + t * EL + s0 + x) =
+                    make_float4(xrow[x], xrow[x + 1], xrow[x + 2], xrow[x + 3]);
+            }
         } else {
-            float m1[32];
+            float m1[32], erow[32];
 #pragma unroll
             for (int x = 0; x < 32; ++x) {
                 const int s2 = s0 + x;
                 const float da = s2 <= t ? __uint_as_float(dr[x]) * __expf(gt - vg[s2]) : 0.f;
                 m1[x] = da;                                    // dA_qk o Gamma
-                const float ev = da * __uint_as_float(gr[x]);  // dA_qk o A_qk
-                rsum += ev;
-                Eqk[t * 64 + s2] = ev;
+                erow[x] = da * __uint_as_float(gr[x]);         // dA_qk o A_qk
+                rsum += erow[x];
             }
+#pragma unroll
+            for (int x = 0; x < 32; x += 4)
+                *reinterpret_cast<float4 *>(Eqk + t * EL + s0 + x) =
+                    make_float4(erow[x], erow[x + 1], erow[x + 2], erow[x + 3]);
             g_st16(sm + O_R + SL, t, s0, m1);                  // M1 tile [t][s]
             g_st16(sm + O_R + SL, t, s0 + 16, m1 + 16);
         }
@@ -1687,18 +1700,26 @@ bwd_grads_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constan
         float c0 = 0.f, c1 = 0.f;
 #pragma unroll
         for (int r = 16 * q; r < 16 * q + 16; r += 2) {
-            c0 += Eqk[r * 64 + sc] + Ekk[r * 64 + sc];
-            c1 += Eqk[(r + 1) * 64 + sc] + Ekk[(r + 1) * 64 + sc];
+            c0 += Eqk[r * EL + sc] + Ekk[r * EL + sc];
+            c1 += Eqk[(r + 1) * EL + sc] + Ekk[(r + 1) * EL + sc];
         }
         vp[q * 64 + sc] = c0 + c1;   // (the half partials of epilogue 2 are consumed)
     }
     __syncthreads();
     if (tid < C) vdg[tid] -= (vp[tid] + vp[64 + tid]) + (vp[128 + tid] + vp[192 + tid]);
-    {   // X + X^T (symmetric) to the first tile of the pair; zeros (8 KB) in U
-        const int r = tid >> 2, q = tid & 3;   // row r, columns 16 q .. 16 q + 15
+    {   // X + X^T (symmetric) to the first tile of the pair; zeros (8 KB) in U.
+        // Row r = tid % 64 (consecutive lanes: the column reads are contiguous,
+        // the row reads 16-byte pieces in 8 bank groups), columns 16 q .. + 15
+        const int r = tid & 63, q = tid >> 6;
         float xx[16];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) xx[x] = Xs[r * 64 + 16 * q + x] + Xs[(16 * q + x) * 64 + r];
+        for (int x = 0; x < 16; x += 4) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(Xs + r * EL + 16 * q + x);
+            xx[x] = a4.x + Xs[(16 * q + x) * EL + r];
+            xx[x + 1] = a4.y + Xs[(16 * q + x + 1) * EL + r];
+            xx[x + 2] = a4.z + Xs[(16 * q + x + 2) * EL + r];
+            xx[x + 3] = a4.w + Xs[(16 * q + x + 3) * EL + r];
+        }
         g_st16(sm + O_R, r, 16 * q, xx);
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4 *>(sm + O_U + r * 128 + 32 * q) = z;
