@@ -799,7 +799,7 @@ constexpr uint32_t P2_SMEM = SM_G + NSTAGE * 256 + 1024;
 
 // TMEM columns (fp32 accumulators, 128 lanes): [X | P] in two buffers, Z, and
 // Y in two buffers (chunk c uses buffer c % 2).
-constexpr uint32_t TM_PX = 0, TM_Z = 128, TM_Y = 192;
+constexpr uint32_t TM_PX = 0, TM_S = 128, TM_Y = 192;
 
 // The same pass with kW dv columns per CTA: kW = 64 (above: two CTAs per
 // head, the shorter chain) or kW = 128 (one CTA per head: every product has
@@ -824,14 +824,14 @@ struct P2Cfg {
     static constexpr uint32_t SM_S = NST * ST_BYTES, SM_U = SM_S + NJ * S_SLAB,
                               SM_UZ = SM_U + NJ * U_SLAB, SM_G = SM_UZ + NJ * U_SLAB;
     static constexpr uint32_t SMEM = SM_G + NST * 256 + 1024;
-    static constexpr uint32_t TM_PX = 0, TM_Z = 2 * kW, TM_Y = 3 * kW;
+    static constexpr uint32_t TM_PX = 0, TM_S = 2 * kW, TM_Y = 3 * kW;
     static constexpr uint32_t Y_STRIDE = kW == 64 ? 64 : 0;   // column offset of Y buffer 1
 };
 static_assert(P2Cfg<64>::NST == NSTAGE && P2Cfg<64>::ST_BYTES == ST_BYTES &&
                   P2Cfg<64>::ST_TX == ST_TX && P2Cfg<64>::SM_S == SM_S &&
                   P2Cfg<64>::SM_U == SM_U && P2Cfg<64>::SM_UZ == SM_UZ &&
                   P2Cfg<64>::SM_G == SM_G && P2Cfg<64>::SMEM == P2_SMEM &&
-                  P2Cfg<64>::TM_PX == TM_PX && P2Cfg<64>::TM_Z == TM_Z &&
+                  P2Cfg<64>::TM_PX == TM_PX && P2Cfg<64>::TM_S == TM_S &&
                   P2Cfg<64>::TM_Y == TM_Y,
               "narrow state pass layout");
 static_assert(P2Cfg<128>::SMEM <= 232448 && P2Cfg<128>::TM_Y + 128 <= 512, "wide state pass");
@@ -883,7 +883,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
     constexpr int NMAIN = Cf::NMAIN, NCG = kW / 32;
     __shared__ uint64_t bar_ld[NS];
     __shared__ uint64_t bar_empty[NS];   // the products of a stage's chunk are done
-    __shared__ uint64_t bar_px, bar_u, bar_z, bar_s, bar_fin;
+    __shared__ uint64_t bar_px, bar_u, bar_u2, bar_z, bar_s, bar_fin;
     __shared__ uint64_t bar_y[2];   // Y of chunk c completes on bar_y[c % 2]
     __shared__ uint32_t tslot;
     __shared__ int sAbort;
@@ -932,7 +932,8 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             mbar_init(&bar_empty[i], 1);
         }
         mbar_init(&bar_px, 1);
-        mbar_init(&bar_u, NMAIN);   // one arrival per main warp
+        mbar_init(&bar_u, NMAIN);    // one arrival per main warp: U' written, S scaled
+        mbar_init(&bar_u2, NMAIN);   // one arrival per main warp: U written
         mbar_init(&bar_z, 1);
         mbar_init(&bar_y[0], 1);
         mbar_init(&bar_y[1], 1);
@@ -999,13 +1000,21 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             // the recorded copy has read S_c before Z lets the main warps overwrite it
             if (kRecord && p.S_chk && !phi && lane == 0) bulk_wait_group_read0();
             if (lane == 0) {
-                const uint32_t aKT = smem_u32(st + ST_KT), aA = smem_u32(st + ST_A);
-                // Z = K^T U': A = K read MN-major (M = dk, two 64-feature blocks)
+                const uint32_t aKT = smem_u32(st + ST_KT);
+                // S_b += K^T U' (S_b, scaled by exp(g_C) by the main warps, is the
+                // accumulator): A = K read MN-major (M = dk, two 64-feature blocks)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tb + Cf::TM_Z, sdesc_sw128(aKT + ks * 2048, 8192, 1024),
-                             sdesc_sw128(aUz + ks * 2048, 8192, 1024), id_zy, ks > 0);
+                    mma_bf16(tb + Cf::TM_S, sdesc_sw128(aKT + ks * 2048, 8192, 1024),
+                             sdesc_sw128(aUz + ks * 2048, 8192, 1024), id_zy, 1u);
                 mma_commit(&bar_z);
+            }
+            __syncwarp();
+            // U (the B operand of Y) is written after U'
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_u2, par, &sAbort))) { fail(); break; }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t aA = smem_u32(st + ST_A);
                 // Y = A U: A read MN-major from A^T; its second 64-row block
                 // (rows 64..127 of the product, never read) points at U~
 #pragma unroll
@@ -1094,7 +1103,9 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                     for (int i = 0; i < 32; ++i) Sr[jj][i] = (L == j0 + cg + i) ? 1.f : 0.f;
                 }
                 st_row_bf16x32(sS + (cg >> 6) * Cf::S_SLAB, L, cg & 63, Sr[jj]);
+                tmem_st_f32x32(tb + lane_base + Cf::TM_S + cg, Sr[jj]);
             }
+            tmem_st_wait();
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_s);
@@ -1136,6 +1147,19 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             } else {
                 egt = __expf(g[L]);
             }
+            // ---- S_b <- exp(g_C) S_b in TMEM (row L, the thread's columns), while
+            //      [X | P] runs; Z then accumulates into it ----
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) {
+                uint32_t r[32];
+                tmem_ld32(tb + lane_base + Cf::TM_S + c0 + 32 * jj, r);
+                tmem_ld_wait();
+                float s[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[i] = egC * __uint_as_float(r[i]);
+                tmem_st_f32x32(tb + lane_base + Cf::TM_S + c0 + 32 * jj, s);
+            }
+            tmem_st_wait();
             if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_px, par, &sAbort))) {
                 fail();
                 break;
@@ -1145,6 +1169,10 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 // ---- U = U~_b - P and U' = exp(g_C - g_t) U for token t = L - 64,
                 //      the thread's columns ----
                 const int t = L - 64;
+                // U' (the B operand of the S update) is written and published
+                // first; U (for Y) after
+                float u[32];            // kW = 64: U of the thread's 32 columns
+                uint32_t pu[2][8];      // kW = 128: U in bf16 pairs, two 16-column halves
                 if (kW == 64) {
 #pragma unroll
                 for (int jj = 0; jj < NJ; ++jj) {
@@ -1152,7 +1180,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                     uint32_t r[32];
                     tmem_ld32(tPX + cg, r);
                     tmem_ld_wait();
-                    float u[32], uz[32];
+                    float uz[32];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         uint4 w = wu[jj][k];
@@ -1171,7 +1199,6 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                     }
 #pragma unroll
                     for (int i = 0; i < 32; ++i) uz[i] = ft * u[i];
-                    st_row_bf16x32(sU + (cg >> 6) * Cf::U_SLAB, t, cg & 63, u);
                     st_row_bf16x32(sUz + (cg >> 6) * Cf::U_SLAB, t, cg & 63, uz);
                 }
                 } else {
@@ -1182,7 +1209,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                         uint32_t r[16];
                         tmem_ld16(tPX + cg, r);
                         tmem_ld_wait();
-                        uint32_t pu[8], pz[8];
+                        uint32_t pz[8];
 #pragma unroll
                         for (int k = 0; k < 2; ++k) {
                             uint4 w = *reinterpret_cast<const uint4 *>(
@@ -1193,15 +1220,13 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                             for (int e = 0; e < 4; ++e) {
                                 const float u0 = bf_lo(ww[e]) - __uint_as_float(r[8 * k + 2 * e]);
                                 const float u1 = bf_hi(ww[e]) - __uint_as_float(r[8 * k + 2 * e + 1]);
-                                pu[4 * k + e] = pack_bf2(u0, u1);
+                                pu[hh][4 * k + e] = pack_bf2(u0, u1);
                                 pz[4 * k + e] = pack_bf2(ft * u0, ft * u1);
                             }
                         }
 #pragma unroll
                         for (int k = 0; k < 2; ++k) {
                             const uint32_t off = sw128_offset(t, (cg & 63) + 8 * k);
-                            *reinterpret_cast<uint4 *>(sU + (cg >> 6) * Cf::U_SLAB + off) =
-                                make_uint4(pu[4 * k], pu[4 * k + 1], pu[4 * k + 2], pu[4 * k + 3]);
                             *reinterpret_cast<uint4 *>(sUz + (cg >> 6) * Cf::U_SLAB + off) =
                                 make_uint4(pz[4 * k], pz[4 * k + 1], pz[4 * k + 2], pz[4 * k + 3]);
                         }
@@ -1227,30 +1252,51 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_u);
+                if (kW == 64) {
+                    st_row_bf16x32(sU + (c0 >> 6) * Cf::U_SLAB, t, c0 & 63, u);
+                } else {
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const int cg = c0 + 16 * hh;
+                            *reinterpret_cast<uint4 *>(sU + (cg >> 6) * Cf::U_SLAB +
+                                                       sw128_offset(t, (cg & 63) + 8 * k)) =
+                                make_uint4(pu[hh][4 * k], pu[hh][4 * k + 1], pu[hh][4 * k + 2],
+                                           pu[hh][4 * k + 3]);
+                        }
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_u2);
             } else {
                 // every read of this stage by the main warps (and, with one Y
-                // buffer, of the previous chunk's Y) precedes their bar_u
-                // arrival, which precedes the products that overwrite them
+                // buffer, of the previous chunk's Y) and their scaling of S_b
+                // precede their bar_u and bar_u2 arrivals, which precede the
+                // products that overwrite or accumulate into them
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar_u);
+                if (lane == 0) {
+                    mbar_arrive(&bar_u);
+                    mbar_arrive(&bar_u2);
+                }
             }
 
             if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_z, par, &sAbort))) { fail(); break; }
             tc_fence_after();
-            // ---- S_b <- exp(g_C) S_b + Z (row L, the thread's columns) ----
-#pragma unroll
-            for (int jj = 0; jj < NJ; ++jj) {
-                uint32_t r[32];
-                tmem_ld32(tb + lane_base + Cf::TM_Z + c0 + 32 * jj, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) Sr[jj][i] = fmaf(egC, Sr[jj][i], __uint_as_float(r[i]));
-            }
+            // ---- S_b = exp(g_C) S_b + Z is complete in TMEM: its bf16 copy for the
+            //      next [X | P] (row L, the thread's columns) ----
             if (c + 1 < nch) {
 #pragma unroll
                 for (int jj = 0; jj < NJ; ++jj) {
                     const int cg = c0 + 32 * jj;
-                    st_row_bf16x32(sS + (cg >> 6) * Cf::S_SLAB, L, cg & 63, Sr[jj]);
+                    uint32_t r[32];
+                    tmem_ld32(tb + lane_base + Cf::TM_S + cg, r);
+                    tmem_ld_wait();
+                    float s[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(r[i]);
+                    st_row_bf16x32(sS + (cg >> 6) * Cf::S_SLAB, L, cg & 63, s);
                 }
                 fence_async_smem();
                 tc_fence_before();
@@ -1303,14 +1349,19 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
             }
         }
         if (!sAbort && (phi ? p.S_T_phi != nullptr : p.S_T != nullptr)) {
+            // the final state (S0 itself when the sequence is empty), from TMEM
+            tc_fence_after();
 #pragma unroll
             for (int jj = 0; jj < NJ; ++jj) {
+                uint32_t r[32];
+                tmem_ld32(tb + lane_base + Cf::TM_S + c0 + 32 * jj, r);
+                tmem_ld_wait();
                 float4 *dst = reinterpret_cast<float4 *>(
                     (phi ? p.S_T_phi + phi_base : p.S_T + sbase) + (size_t)L * D + j0 + c0 + 32 * jj);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    dst[i] = make_float4(Sr[jj][4 * i], Sr[jj][4 * i + 1], Sr[jj][4 * i + 2],
-                                         Sr[jj][4 * i + 3]);
+                    dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                         __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
             }
         }
     }

@@ -278,6 +278,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
                  ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
                  : "memory");
 }
+// 32 fp32 values into 32 consecutive columns of the calling warp's lanes.
+__device__ __forceinline__ void tmem_st_f32x32(uint32_t taddr, const float (&x)[32]) {
+    uint32_t lo[16], hi[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        lo[i] = __float_as_uint(x[i]);
+        hi[i] = __float_as_uint(x[16 + i]);
+    }
+    tmem_st16(taddr, lo);
+    tmem_st16(taddr + 16, hi);
+}
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
