@@ -782,7 +782,7 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 // L >= 64) and the 32 columns [32 hf, 32 hf + 32) of the tile, hf = warp / 4;
 // warp 8 issues every MMA from lane 0; warp 9 issues the stage loads (and, in
 // the fused launch, waits for the ready flags).  Both wait converged.
-constexpr int P2_MAIN = 256, P2_THREADS = P2_MAIN + 64;
+constexpr int P2_MAIN = 256, P2_THREADS = P2_MAIN + 96;
 constexpr int NSTAGE = 3;
 // Stage layout (one chunk):
 //   QW: two 64-feature slabs of 16 KB, each [Q rows 0..63 | W rows 0..63]
@@ -813,9 +813,9 @@ struct P2Cfg {
     static constexpr int NJ = kW / 64;                 // 64-column slabs of the tile
     // main warps: four per 32-column group (one per TMEM lane quadrant), so
     // that every main thread holds 32 columns of one row whatever kW; then
-    // the MMA issuer and the load warp
+    // the MMA issuer of the chain, the load warp and the issuer of Y
     static constexpr int NMAIN = kW / 32 * 4;
-    static constexpr int THREADS = (NMAIN + 2) * 32;
+    static constexpr int THREADS = (NMAIN + 3) * 32;
     static constexpr uint32_t U_BYTES = 64u * kW * 2u;   // U~ of a stage (64-column slabs)
     static constexpr uint32_t ST_BYTES = ST_U + U_BYTES;
     static constexpr uint32_t ST_TX = 32768u + 16384u + 8192u + U_BYTES + 256u;
@@ -835,6 +835,7 @@ static_assert(P2Cfg<64>::NST == NSTAGE && P2Cfg<64>::ST_BYTES == ST_BYTES &&
                   P2Cfg<64>::TM_Y == TM_Y,
               "narrow state pass layout");
 static_assert(P2Cfg<128>::SMEM <= 232448 && P2Cfg<128>::TM_Y + 128 <= 512, "wide state pass");
+static_assert(SM_UZ + 8192 - SM_S == 32768, "S0 staging: the S, U and U' operands of the narrow pass");
 static_assert(P2Cfg<64>::THREADS == P2_THREADS, "narrow state pass threads");
 
 template <int kW>
@@ -883,7 +884,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
     constexpr int NMAIN = Cf::NMAIN, NCG = kW / 32;
     __shared__ uint64_t bar_ld[NS];
     __shared__ uint64_t bar_empty[NS];   // the products of a stage's chunk are done
-    __shared__ uint64_t bar_px, bar_u, bar_u2, bar_z, bar_s, bar_fin;
+    __shared__ uint64_t bar_px, bar_u, bar_u2, bar_z, bar_s, bar_fin, bar_fin_y;
     __shared__ uint64_t bar_y[2];   // Y of chunk c completes on bar_y[c % 2]
     __shared__ uint32_t tslot;
     __shared__ int sAbort;
@@ -925,11 +926,34 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
     }
     const int nch = (int)((len + C - 1) / C);
     const size_t sbase = ((size_t)seq * p.H + h) * D * D;
+    // the initial state: S0, zero for a later segment of a split sequence, the
+    // identity's columns for a transition pass (s0 == nullptr for the last two)
+    const float *s0 = p.S0;
+    if (segP > 1)
+        s0 = (!phi && p.S0 && seq % segP == 0) ? p.S0 + ((size_t)(seq / segP) * p.H + h) * D * D
+                                               : nullptr;
+    else if (s0)
+        s0 += sbase;
+    // In the fused launch the main warps first compute a phase-1 item; the MMA
+    // and load warps meanwhile copy the CTA's 64 columns of S0 into shared
+    // memory (the S, U and U' operand space, 32 KB, unused until the pass
+    // starts) as 16-byte chunk ch of row r at chunk slot ch * 128 + r, which
+    // the main warps then read without bank conflicts.
+    const bool pre_s0 = kFused && kW == 64 && s0 != nullptr;
+    float4 *s0_stage = reinterpret_cast<float4 *>(sm + Cf::SM_S);
+    if (pre_s0 && warp >= NMAIN) {
+        const int i = tid - NMAIN * 32;   // 0 .. 63
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            const int idx = k * 64 + i, ch = idx >> 7, r = idx & 127;
+            s0_stage[idx] = *reinterpret_cast<const float4 *>(s0 + (size_t)r * D + j0 + 4 * ch);
+        }
+    }
 
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&bar_ld[i], 1);
-            mbar_init(&bar_empty[i], 1);
+            mbar_init(&bar_empty[i], 2);   // committed by both MMA issuers
         }
         mbar_init(&bar_px, 1);
         mbar_init(&bar_u, NMAIN);    // one arrival per main warp: U' written, S scaled
@@ -939,6 +963,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         mbar_init(&bar_y[1], 1);
         mbar_init(&bar_s, NMAIN);   // one arrival per main warp
         mbar_init(&bar_fin, 1);
+        mbar_init(&bar_fin_y, 1);
         fence_mbar_init();
         // an error already reported: read once, so that the whole CTA
         // agrees (threads reading the word at different times might not)
@@ -1008,22 +1033,7 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
                     mma_bf16(tb + Cf::TM_S, sdesc_sw128(aKT + ks * 2048, 8192, 1024),
                              sdesc_sw128(aUz + ks * 2048, 8192, 1024), id_zy, 1u);
                 mma_commit(&bar_z);
-            }
-            __syncwarp();
-            // U (the B operand of Y) is written after U'
-            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_u2, par, &sAbort))) { fail(); break; }
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t aA = smem_u32(st + ST_A);
-                // Y = A U: A read MN-major from A^T; its second 64-row block
-                // (rows 64..127 of the product, never read) points at U~
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tb + Cf::TM_Y + Cf::Y_STRIDE * (c & 1),
-                             sdesc_sw128(aA + ks * 2048, 8192, 1024),
-                             sdesc_sw128(aU + ks * 2048, 8192, 1024), id_zy, ks > 0);
-                mma_commit(&bar_y[c & 1]);
-                mma_commit(&bar_empty[b]);   // the stage may be refilled
+                mma_commit(&bar_empty[b]);   // [X | P] and Z are done with the stage
             }
             __syncwarp();
         }
@@ -1032,6 +1042,37 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         if (kRecord && p.S_chk && lane == 0) bulk_wait_group0();
         __syncwarp();
         (void)mbar_wait(&bar_fin, 0u);
+    } else if (warp == NMAIN + 2) {
+        // ----------------------------------------------------------------- Y issue
+        // Y = A U once U is written (bar_u2), from a thread of its own: an MMA
+        // issue waits for room in the tensor pipe, and the chain's issuer must
+        // be free when the next state is published.
+        const uint32_t id_zy = idesc_bf16_f32(128, kW, true, true);
+        const uint32_t aU = smem_u32(sU);
+        for (int c = 0; c < nch; ++c) {
+            if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bar_u2, (uint32_t)(c & 1), &sAbort))) {
+                fail();
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t aA = smem_u32(sm + (c % NS) * Cf::ST_BYTES + ST_A);
+                // A read MN-major from A^T; its second 64-row block (rows 64..127
+                // of the product, never read) points at U~
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tb + Cf::TM_Y + Cf::Y_STRIDE * (c & 1),
+                             sdesc_sw128(aA + ks * 2048, 8192, 1024),
+                             sdesc_sw128(aU + ks * 2048, 8192, 1024), id_zy, ks > 0);
+                mma_commit(&bar_y[c & 1]);
+                mma_commit(&bar_empty[c % NS]);   // Y is done with the stage
+            }
+            __syncwarp();
+        }
+        // every MMA of this thread has completed before the CTA releases its TMEM
+        if (lane == 0) mma_commit(&bar_fin_y);
+        __syncwarp();
+        (void)mbar_wait(&bar_fin_y, 0u);
     } else if (warp == NMAIN + 1) {
         // ----------------------------------------------------------------- loads
         // Chunk n goes to stage n % NSTAGE once the products of chunk
@@ -1079,22 +1120,15 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         const size_t rs = (size_t)p.H * D;
         float Sr[NJ][32];
         {
-            // the initial state: S0, zero for a later segment of a split
-            // sequence, the identity's columns for a transition pass
-            const float *s0 = p.S0;
-            if (segP > 1)
-                s0 = (!phi && p.S0 && seq % segP == 0)
-                         ? p.S0 + ((size_t)(seq / segP) * p.H + h) * D * D
-                         : nullptr;
-            else if (s0)
-                s0 += sbase;
 #pragma unroll
             for (int jj = 0; jj < NJ; ++jj) {
                 const int cg = c0 + 32 * jj;
                 const float4 *src = reinterpret_cast<const float4 *>(s0 + (size_t)L * D + j0 + cg);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float4 v = s0 ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 v = pre_s0 ? s0_stage[(cg / 4 + i) * 128 + L]
+                                   : s0     ? src[i]
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
                     Sr[jj][4 * i] = v.x; Sr[jj][4 * i + 1] = v.y;
                     Sr[jj][4 * i + 2] = v.z; Sr[jj][4 * i + 3] = v.w;
                 }
@@ -1102,6 +1136,8 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
 #pragma unroll
                     for (int i = 0; i < 32; ++i) Sr[jj][i] = (L == j0 + cg + i) ? 1.f : 0.f;
                 }
+                // every main warp has read the staged S0 before any overwrites it
+                if (pre_s0) named_sync(4, NMAIN * 32);
                 st_row_bf16x32(sS + (cg >> 6) * Cf::S_SLAB, L, cg & 63, Sr[jj]);
                 tmem_st_f32x32(tb + lane_base + Cf::TM_S + cg, Sr[jj]);
             }
