@@ -942,10 +942,10 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
     const bool pre_s0 = kFused && kW == 64 && s0 != nullptr;
     float4 *s0_stage = reinterpret_cast<float4 *>(sm + Cf::SM_S);
     if (pre_s0 && warp >= NMAIN) {
-        const int i = tid - NMAIN * 32;   // 0 .. 63
-#pragma unroll 8
-        for (int k = 0; k < 32; ++k) {
-            const int idx = k * 64 + i, ch = idx >> 7, r = idx & 127;
+        constexpr int NH = Cf::THREADS - NMAIN * 32;   // the helper threads
+#pragma unroll 4
+        for (int idx = tid - NMAIN * 32; idx < 2048; idx += NH) {
+            const int ch = idx >> 7, r = idx & 127;   // 16 chunks of 16 bytes x 128 rows
             s0_stage[idx] = *reinterpret_cast<const float4 *>(s0 + (size_t)r * D + j0 + 4 * ch);
         }
     }
