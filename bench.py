@@ -47,7 +47,7 @@ if ROOT not in sys.path:
 METRIC = "KLA chunkwise prefill tokens/s & % roofline; decode steps/s at B=256"
 # DRAM bytes (read + write) per call from an ncu capture of the kernels as
 # they are now, or None where the kernels changed after the last capture.
-TRAFFIC = {"layer_prefill": 55.78e6 + 16.38e6, "long_context": None, "varlen_64": None,
+TRAFFIC = {"layer_prefill": 54.42e6 + 14.14e6, "long_context": None, "varlen_64": None,
            "decode_b256": 2 * (135.83e6 + 74.59e6), "ccq": 33.90e6 + 0.12e6}
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 BYTES_PER_TOKEN_HEAD = 1032          # q,k,v,o bf16 (4 x 256 B) + alpha, eta fp32 (8 B)
@@ -399,9 +399,9 @@ def time_e2e(pf, steps, flush, stream, dev):
 
 KERNELS = {
     "layer_prefill": "fused_kernel (the whole prefill call is this one launch)",
-    "long_context": "the whole call with the sequence split: intra_kernel + state_kernel "
-                    "(state and transition passes) + split_combine_kernel + "
-                    "split_correct_kernel",
+    "long_context": "the whole call with the sequence split: intra_kernel + state_kernel_wide "
+                    "(state and transition passes, one 128-column CTA per chain) + "
+                    "split_combine_kernel + split_correct_kernel",
     "varlen_64": "the whole call: prep_kernel + intra_kernel + state_kernel_wide",
 }
 
