@@ -27,11 +27,12 @@
 // the two 64-column halves of the state run in two CTAs, since the columns
 // of S evolve independently.  Per chunk, with S_b the CTA's dk x 64 slice:
 //   [X | P] = [Q ; W] S_b ;  U = U~_b - P
-//   Z = K^T (diag(exp(g_C - g)) U) ;  Y = A U
-//   S_b <- exp(g_C) S_b + Z (fp32 registers) ;  O_b = diag(exp g) X + Y
-// The serial chain is [X | P] -> U -> Z -> S; a dedicated warp issues the
-// MMAs and TMA loads (three chunks in flight), and the outputs of a chunk are
-// formed and stored while the next chunk's first product runs.
+//   S_b <- exp(g_C) S_b + K^T (diag(exp(g_C - g)) U)   (S_b fp32 in TMEM)
+//   Y = A U ;  O_b = diag(exp g) X + Y
+// The serial chain is [X | P] -> U -> K^T U' -> S_b to shared memory; one
+// warp issues the chain's MMAs, another Y, a third the TMA loads (three
+// chunks in flight), and the outputs of a chunk are formed and stored while
+// the next chunk's first product runs.
 
 // All waits are bounded (kla_tc.cuh); a wait that gives up sets the status
 // word to a timeout code and the CTA leaves after releasing TMEM.
@@ -771,17 +772,24 @@ intra_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 // SMs side by side.  Per chunk, with S_b = S[:, j0 : j0 + 64] (dk x 64):
 //   [X | P] = [Q ; W] S_b                           M=128, N=64, K=128 (dk)
 //   U = U~_b - P,  U' = diag(exp(g_C - g)) U  (bf16 -> shared memory)
-//   Z = K^T U',  Y = A U                             M=128, N=64, K=64 (tokens)
-//   S_b <- exp(g_C) S_b + Z ;  O_b = diag(exp g) X + Y
+//   S_b += K^T U',  Y = A U                          M=128, N=64, K=64 (tokens)
+//   O_b = diag(exp g) X + Y
 // where A = lower(Gamma o Q K^T), and W, U~, A^T and g come from phase 1; Q
-// and K are read from the inputs.  The serial chain per chunk is one 8-step
-// MMA, the U update, one 4-step MMA and the S update.
+// and K are read from the inputs.  S_b is kept in fp32 in TMEM as the
+// accumulator of K^T U': the main warps scale it by exp(g_C) while [X | P]
+// runs and copy it to shared memory in bf16 after the product.  The serial
+// chain per chunk is one 8-step MMA, the U update, one 4-step MMA and the
+// bf16 copy of S_b.
 //
 // Warp roles: warps 0-7 ("main") own TMEM lane L = 32 (warp % 4) + lane
 // (= dk row L of S_b, = token L of X / Y for L < 64, = token L - 64 of P for
 // L >= 64) and the 32 columns [32 hf, 32 hf + 32) of the tile, hf = warp / 4;
-// warp 8 issues every MMA from lane 0; warp 9 issues the stage loads (and, in
-// the fused launch, waits for the ready flags).  Both wait converged.
+// warp 8 issues the chain's MMAs from lane 0; warp 9 issues the stage loads
+// (and, in the fused launch, waits for the ready flags); warp 10 issues Y.
+// An MMA issue waits for room in the tensor pipe (about 50 ns per M = 128
+// product whatever N), so the product off the chain has a thread of its own:
+// the chain's issuer is then free when the next S_b is published.  The three
+// wait converged.
 constexpr int P2_MAIN = 256, P2_THREADS = P2_MAIN + 96;
 constexpr int NSTAGE = 3;
 // Stage layout (one chunk):
@@ -797,8 +805,8 @@ constexpr uint32_t SM_S = NSTAGE * ST_BYTES, SM_U = SM_S + 16384, SM_UZ = SM_U +
                    SM_G = SM_UZ + 8192;
 constexpr uint32_t P2_SMEM = SM_G + NSTAGE * 256 + 1024;
 
-// TMEM columns (fp32 accumulators, 128 lanes): [X | P] in two buffers, Z, and
-// Y in two buffers (chunk c uses buffer c % 2).
+// TMEM columns (fp32, 128 lanes): [X | P] in two buffers, S_b (the
+// accumulator of K^T U'), and Y in two buffers (chunk c uses buffer c % 2).
 constexpr uint32_t TM_PX = 0, TM_S = 128, TM_Y = 192;
 
 // The same pass with kW dv columns per CTA: kW = 64 (above: two CTAs per
@@ -806,7 +814,7 @@ constexpr uint32_t TM_PX = 0, TM_S = 128, TM_Y = 192;
 // N = 128 for the same MMA count, the element-wise steps take twice as long,
 // and half as many CTAs carry the whole state; used where more CTAs than SMs
 // would run).  The wide pass has two stages (the stage holds all 128 columns
-// of U~) and one Y buffer (TMEM: [X | P] 2 x 128, Z 128, Y 128 columns).
+// of U~) and one Y buffer (TMEM: [X | P] 2 x 128, S_b 128, Y 128 columns).
 template <int kW>
 struct P2Cfg {
     static constexpr int NST = kW == 64 ? 3 : 2;
