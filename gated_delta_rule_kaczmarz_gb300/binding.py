@@ -183,7 +183,10 @@ def _mode(beta_mode) -> int:
 
 def _workspace(nbytes, device, workspace):
     if nbytes == 0:
-        return None, 0
+        # a path that needs none still records its status in a given workspace
+        if workspace is None:
+            return None, 0
+        return workspace, workspace.numel() * workspace.element_size()
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
     if workspace.numel() * workspace.element_size() < nbytes:

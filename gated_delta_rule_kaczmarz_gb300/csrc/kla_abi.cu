@@ -113,7 +113,12 @@ kla_status run_prefill(kla::Problem &p, bool varlen, void *workspace, size_t wor
         p.ws = static_cast<unsigned char *>(workspace) + kla::kWsHeader;
         p.ws_bytes = workspace_bytes - kla::kWsHeader;
     } else {
-        p.status = nullptr;
+        // a path that needs no workspace still records its status in one the
+        // caller passes, so that kla_workspace_status reads this call's
+        p.status = (workspace != nullptr && workspace_bytes >= sizeof(unsigned) &&
+                    (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0)
+                       ? static_cast<unsigned *>(workspace)
+                       : nullptr;
         p.ws = nullptr;
         p.ws_bytes = 0;
     }

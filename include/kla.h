@@ -346,7 +346,9 @@ KLA_API int kla_ccq_query_step(const void *q, const void *k, const float *lambda
  * Synchronises `stream` and returns the status that the last prefill call
  * using `workspace` recorded on the device: KLA_OK, KLA_ERR_INVALID_ARG
  * (cu_seqlens rejected) or KLA_ERR_TIMEOUT.  A workspace of 0 bytes (NULL)
- * has no status word and returns KLA_OK.
+ * has no status word and returns KLA_OK.  A prefill whose path needs no
+ * workspace still records its status in a workspace the caller passes (at
+ * least 4 bytes, 256-byte aligned).
  *
  * Every wait of one CTA on another (the single-launch prefill's state pass
  * waiting for a chunk pair to be published) and every wait on the CTA's own

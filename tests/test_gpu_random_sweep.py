@@ -1,0 +1,131 @@
+"""Seeded random-shape sweep of the GPU entry points against the fp64 oracle.
+
+The other GPU tests pick their shapes by hand (chunk and block boundaries,
+edge values); this one draws them: batch sizes, sequence lengths (including
+one-token, empty and ragged sequences), head counts, key-norm spreads,
+initial states, write-coefficient modes and the no-decay case, for the
+fixed-length forward on both kernel families, the packed (varlen) forward,
+the CCQ query and the backward.  Every draw comes from a fixed seed, so a
+failure names a reproducible case.  Error measure and tolerances as in
+tests/_util.py (max |gpu - oracle| / max |oracle| <= 2e-2 for bf16 inputs,
+1e-4 for fp32); the device status word must read OK after every call."""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_kaczmarz_gb300 as kla
+import oracle
+from gated_delta_rule_kaczmarz_gb300 import binding
+from gated_delta_rule_kaczmarz_gb300.workloads import prefill_inputs, varlen_inputs
+from tests._util import TOL, cuda, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _draw_forward(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        bf16 = i % 4 != 3
+        d = 128 if bf16 or rng.random() < 0.5 else 64
+        cases.append(dict(B=int(rng.integers(1, 6)), T=int(rng.integers(1, 601)),
+                          H=int(rng.integers(1, 7)), d=d, dtype="bf16" if bf16 else "fp32",
+                          sigma=float(rng.choice([0.3, 0.5, 1.0])),
+                          s0=float(rng.choice([0.0, 0.01])),
+                          mode=str(rng.choice(["kaczmarz", "given"])),
+                          no_alpha=bool(rng.random() < 0.2), seed=int(rng.integers(1 << 30))))
+    return cases
+
+
+def _draw_varlen(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        N = int(rng.integers(1, 9))
+        lens = [int(x) for x in rng.integers(0, 401, N)]
+        if N > 2:
+            lens[int(rng.integers(N))] = 0                  # an empty sequence
+            lens[int(rng.integers(N))] = 1                  # a one-token sequence
+        cases.append(dict(lens=lens, H=int(rng.integers(1, 5)), s0=float(rng.choice([0.0, 0.01])),
+                          seed=int(rng.integers(1 << 30))))
+    return cases
+
+
+FWD = _draw_forward(12, 20261203)
+VARLEN = _draw_varlen(6, 20261204)
+
+
+@pytest.mark.parametrize("case", FWD, ids=[f"fwd{i}" for i in range(len(FWD))])
+def test_random_forward(case):
+    c = case
+    inp = prefill_inputs(c["B"], c["T"], c["H"], c["d"], c["d"], c["dtype"], seed=c["seed"],
+                         key_norm_sigma=c["sigma"], s0_var=c["s0"])
+    alpha = None if c["no_alpha"] else inp["alpha"]
+    g = cuda(inp)
+    dt = binding.KLA_DTYPE_BF16 if c["dtype"] == "bf16" else binding.KLA_DTYPE_F32
+    nb = kla.kla_chunk_fwd_workspace_size(c["B"], c["T"], c["H"], c["d"], c["d"], dtype=dt)
+    ws = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
+    o, S = kla.kla_chunk_fwd(g["q"], g["k"], g["v"], None if alpha is None else g["alpha"],
+                             g["eta"], inp["eps"], g["S0"], workspace=ws, beta_mode=c["mode"])
+    assert kla.kla_workspace_status(ws) == binding.KLA_OK
+    o_ref, S_ref = oracle.forward(inp["q"], inp["k"], inp["v"], alpha, inp["eta"], inp["eps"],
+                                  inp["S0"], nthreads=8, beta_mode=c["mode"])
+    tol = TOL[inp["q"].dtype]
+    assert rel_err(o, o_ref) <= tol
+    assert rel_err(S, S_ref) <= tol
+
+
+@pytest.mark.parametrize("case", VARLEN, ids=[f"varlen{i}" for i in range(len(VARLEN))])
+def test_random_varlen(case):
+    c = case
+    inp = varlen_inputs(c["lens"], c["H"], 128, 128, "bf16", seed=c["seed"], s0_var=c["s0"])
+    d = cuda(inp)
+    o, S = kla.kla_chunk_fwd_varlen(d["q"], d["k"], d["v"], d["alpha"], d["eta"], d["eps"],
+                                    d["cu_seqlens"], d["S0"], check_status=True)
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.forward_varlen(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["eta"],
+                                         inp["eps"], inp["cu_seqlens"], inp["S0"], nthreads=8)
+    if sum(c["lens"]) > 0:
+        assert rel_err(o, o_ref) <= 2e-2
+    assert rel_err(S, S_ref) <= 2e-2
+
+
+def _lam(shape, seed):
+    rng = np.random.default_rng(seed)
+    return torch.from_numpy((1.0 / (1.0 + np.exp(-rng.standard_normal(shape)))).astype(np.float32))
+
+
+@pytest.mark.parametrize("seed", [31, 32, 33, 34])
+def test_random_ccq_query(seed):
+    rng = np.random.default_rng(seed)
+    B, T, H = int(rng.integers(1, 5)), int(rng.integers(1, 501)), int(rng.integers(1, 5))
+    inp = prefill_inputs(B, T, H, 128, 128, "bf16", seed=seed)
+    lam = _lam((B, T, H), seed + 1)
+    qc, (Ms, ms, ns) = kla.kla_ccq_query(cuda(inp)["q"], cuda(inp)["k"], lam.cuda())
+    torch.cuda.synchronize()
+    qc_ref, (Ms_ref, ms_ref, ns_ref) = oracle.ccq_query(inp["q"], inp["k"], lam, None)
+    assert rel_err(qc, qc_ref) <= 2e-2, (B, T, H)
+    assert rel_err(Ms, Ms_ref) <= 1e-5 and rel_err(ms, ms_ref) <= 1e-5
+    assert np.array_equal(ns.cpu().numpy(), ns_ref)
+
+
+@pytest.mark.parametrize("seed", [41, 42, 43])
+def test_random_backward(seed):
+    rng = np.random.default_rng(seed)
+    bf16 = seed != 43
+    d = 128 if bf16 else 64
+    B, T, H = int(rng.integers(1, 4)), int(rng.integers(1, 201)), int(rng.integers(1, 4))
+    dtype = "bf16" if bf16 else "fp32"
+    inp = prefill_inputs(B, T, H, d, d, dtype, seed=seed, s0_var=0.01)
+    t = torch.bfloat16 if bf16 else torch.float32
+    do = torch.from_numpy(rng.standard_normal((B, T, H, d)).astype(np.float32)).to(t)
+    dST = torch.from_numpy((0.1 * rng.standard_normal((B, H, d, d))).astype(np.float32))
+    g = cuda(dict(inp, do=do, dST=dST))
+    got = kla.kla_chunk_bwd(g["q"], g["k"], g["v"], g["alpha"], g["eta"], inp["eps"], g["S0"],
+                            g["do"], g["dST"])
+    torch.cuda.synchronize()
+    ref = oracle.backward(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["eta"], inp["eps"],
+                          inp["S0"], do, dST, nthreads=8)
+    tol = TOL[t]
+    for name, a, b in zip(("dq", "dk", "dv", "dalpha", "deta", "dS0"), got, ref):
+        assert rel_err(a, b) <= tol, (name, B, T, H, dtype)
