@@ -225,3 +225,25 @@ def test_random_noalloc(seed):
     assert kla.kla_chunk_fwd_noalloc_status() == binding.KLA_OK
     torch.testing.assert_close(o2, o1, rtol=0, atol=0)
     torch.testing.assert_close(S2, S1, rtol=0, atol=0)
+
+
+# The launch-form boundaries on this GPU (152 SMs): the fused launch needs an
+# even number of chunks and 2 B H <= 76; the two-launch state pass turns wide
+# when 2 B H > 152.  Lengths on both sides of chunk (64-token) boundaries.
+BOUNDARY = [(B, T, H) for (B, H) in ((19, 2), (13, 3), (38, 2), (39, 2))
+            for T in (64, 65, 128, 129, 192, 193)]
+
+
+@pytest.mark.parametrize("B,T,H", BOUNDARY)
+def test_launch_form_boundaries(B, T, H):
+    inp = prefill_inputs(B, T, H, 128, 128, "bf16", seed=B * 1000 + T + H, s0_var=0.01)
+    g = cuda(inp)
+    ws = torch.empty(kla.kla_chunk_fwd_workspace_size(B, T, H, 128, 128), dtype=torch.uint8,
+                     device="cuda")
+    o, S = kla.kla_chunk_fwd(g["q"], g["k"], g["v"], g["alpha"], g["eta"], inp["eps"], g["S0"],
+                             workspace=ws)
+    assert kla.kla_workspace_status(ws) == binding.KLA_OK
+    o_ref, S_ref = oracle.forward(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["eta"],
+                                  inp["eps"], inp["S0"], nthreads=16)
+    assert rel_err(o, o_ref) <= 2e-2
+    assert rel_err(S, S_ref) <= 2e-2
