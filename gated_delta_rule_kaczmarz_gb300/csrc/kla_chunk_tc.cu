@@ -172,6 +172,72 @@ __device__ __forceinline__ float *lslot(unsigned char *kq, int p) {
 
 constexpr int P1_THREADS = 256;
 
+// The last doubling step (n = 32, one block per chunk, 128 threads per chunk),
+// with the zeros of the triangular factors skipped and the work spread evenly
+// over the four warps of a chunk.  M = L21 D1: column c of M needs rows s >= c
+// of D1 only, so the thread of L21 row `lane` forms the 4-column blocks w and
+// 7 - w of its row (8 - w and w + 1 steps of four rows of D1).  X = -D2 M: row
+// r needs columns s <= r of D2 only, so warp w forms the row groups w and
+// 7 - w (4 rows each; lane / 8 the row, lane % 8 the column block), again
+// w + 1 and 8 - w steps.  M goes through `scratch` with its float4 index
+// XORed with (row % 8), which keeps the row-per-lane stores and the row reads
+// free of bank conflicts.
+__device__ __forceinline__ void merge_top(unsigned char *kq, float *scratch, int tid, int bar) {
+    const int p = tid >> 7, w = (tid >> 5) & 3, lane = tid & 31;
+    float *Lp = lslot(kq, p);
+    float *Mp = scratch + p * 1024;
+    {
+        const int r = 32 + lane;
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+            const int cb = k ? 7 - w : w;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 1
+            for (int s4 = cb; s4 < 8; ++s4) {
+                const float4 a = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, 4 * s4));
+                const float am[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int s = 4 * s4 + e;
+                    const float4 b = *reinterpret_cast<const float4 *>(Lp + s * 64 + lsw(s, 4 * cb));
+                    a0 = fmaf(am[e], b.x, a0);
+                    a1 = fmaf(am[e], b.y, a1);
+                    a2 = fmaf(am[e], b.z, a2);
+                    a3 = fmaf(am[e], b.w, a3);
+                }
+            }
+            *reinterpret_cast<float4 *>(Mp + lane * 32 + ((cb ^ (lane & 7)) << 2)) =
+                make_float4(a0, a1, a2, a3);
+        }
+    }
+    named_sync(bar, P1_THREADS);  // M complete; L21 no longer read
+    {
+        const int pc = lane & 7;
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+            const int j = k ? 7 - w : w;
+            const int rr = 4 * j + (lane >> 3), r = 32 + rr;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 1
+            for (int s4 = 0; s4 <= j; ++s4) {
+                const float4 a = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, 32 + 4 * s4));
+                const float am[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int s = 4 * s4 + e;
+                    const float4 b = *reinterpret_cast<const float4 *>(Mp + s * 32 + ((pc ^ (s & 7)) << 2));
+                    a0 = fmaf(am[e], b.x, a0);
+                    a1 = fmaf(am[e], b.y, a1);
+                    a2 = fmaf(am[e], b.z, a2);
+                    a3 = fmaf(am[e], b.w, a3);
+                }
+            }
+            *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, 4 * pc)) = make_float4(-a0, -a1, -a2, -a3);
+        }
+    }
+    named_sync(bar, P1_THREADS);
+}
+
 // One doubling step of the blocked inverse, in place in the fp32 L storage
 // of both chunks: for every diagonal block of size 2n whose two diagonal
 // n x n blocks already hold D1 = (I + L11)^{-1} and D2 = (I + L22)^{-1},
@@ -620,7 +686,7 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
         named_sync(bar, P1_THREADS);
     }
     merge_level<16>(KQ, scratch, tid, bar);   // 32 x 32 diagonal blocks
-    merge_level<32>(KQ, scratch, tid, bar);   // the whole 64 x 64 inverse
+    merge_top(KQ, scratch, tid, bar);         // the whole 64 x 64 inverse
 
     // ---- V landed; rows past the chunk's end (another sequence's tokens or
     //      TMA zero fill) are cleared so that nothing from them reaches U~ ----
