@@ -48,9 +48,17 @@ METRIC = "KLA chunkwise prefill tokens/s & % roofline; decode steps/s at B=256"
 # DRAM bytes (read + write) per call from an ncu capture of the kernels as
 # they are now, or None where the kernels changed after the last capture.
 TRAFFIC = {"layer_prefill": 54.42e6 + 14.14e6, "long_context": None, "varlen_64": None,
+           "tiny_fp32": None,
            "decode_b256": 2 * (135.83e6 + 74.59e6), "ccq": 33.90e6 + 0.12e6}
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 BYTES_PER_TOKEN_HEAD = 1032          # q,k,v,o bf16 (4 x 256 B) + alpha, eta fp32 (8 B)
+
+
+def bytes_per_token_head(d: int, elem: int) -> int:
+    """q, k, v read and o written (d elements of `elem` bytes each) plus
+    alpha and eta (fp32): 1032 B for bf16 with d = 128 (and for fp32 with
+    d = 64)."""
+    return 4 * d * elem + 8
 CHUNK = 64
 
 
@@ -206,10 +214,10 @@ def cpu_baseline(name, inp, wl):
         used = min(cores, n_seq * wl.H)
         sample = (f"the first {n_seq} packed sequences, all {wl.H} heads "
                   f"({work // wl.H} tokens), one thread per (sequence, head)")
-    elif name == "layer_prefill":
+    elif name in ("layer_prefill", "tiny_fp32"):
         secs, work = oracle_sample(inp, wl.B * wl.H, wl.T, cores)
         used = min(cores, wl.B * wl.H)
-        sample = (f"the whole layer workload ({wl.B * wl.H} (b,h) units x {wl.T} tokens), "
+        sample = (f"the whole {name} workload ({wl.B * wl.H} (b,h) units x {wl.T} tokens), "
                   "one thread per unit")
     else:
         units, tokens = wl.B * wl.H, 2048
@@ -287,8 +295,9 @@ class Prefill:
         else:
             self.n_seq = wl.B
             self.tokens = wl.B * wl.T
-            wsb = kla.kla_chunk_fwd_workspace_size(wl.B, wl.T, wl.H, wl.d, wl.d, CHUNK,
-                                                   binding.KLA_DTYPE_BF16)
+            wsb = kla.kla_chunk_fwd_workspace_size(
+                wl.B, wl.T, wl.H, wl.d, wl.d, CHUNK,
+                binding.KLA_DTYPE_F32 if q.dtype == torch.float32 else binding.KLA_DTYPE_BF16)
             self.names = ("q", "k", "v", "alpha", "eta", "S0")
         self.names = tuple(n for n in self.names if self.inp_cpu[n] is not None)
         self.g = {n: self.inp_cpu[n].to(dev) for n in self.names}
@@ -298,7 +307,8 @@ class Prefill:
         th = self.tokens * wl.H
         units = self.n_seq * wl.H
         s0_bytes = 0 if self.inp_cpu["S0"] is None else units * wl.d * wl.d * 4
-        self.alg_bytes = th * BYTES_PER_TOKEN_HEAD + s0_bytes + units * wl.d * wl.d * 4
+        self.alg_bytes = (th * bytes_per_token_head(wl.d, q.element_size()) + s0_bytes
+                          + units * wl.d * wl.d * 4)
         self.flops = th * flops_per_token_head(wl.d)
 
     def call(self, d, o, S_T, stream):
@@ -403,6 +413,9 @@ KERNELS = {
                     "(state and transition passes, one 128-column CTA per chain) + "
                     "split_combine_kernel + split_correct_kernel",
     "varlen_64": "the whole call: prep_kernel + intra_kernel + state_kernel_wide",
+    "tiny_fp32": "chunk_simt_kernel (the fp32 CUDA-core chunk kernel: one launch of 4 CTAs, one "
+                 "per head and 32-column block, each walking the 4 chunks in order; latency-bound "
+                 "at 512 token-heads)",
 }
 
 
@@ -639,6 +652,9 @@ def ours(args):
     for name in ("long_context", "varlen_64"):
         legs[name], cpu_inputs[name] = prefill_leg(name, args, world, dev, pk, pk_src,
                                                    args.big_steps, 0, False)
+    # the small fp32 correctness workload (inputs far below L2: flushed)
+    legs["tiny_fp32"], cpu_inputs["tiny_fp32"] = prefill_leg(
+        "tiny_fp32", args, world, dev, pk, pk_src, args.steps, 256 << 20, False)
 
     dec = time_decode(args, dev, reps=args.decode_reps)
     cq = time_ccq(args, dev, reps=5)
@@ -702,6 +718,7 @@ def ours(args):
         "clocks": clocks,
         "long_context": legs["long_context"],
         "varlen_64": legs["varlen_64"],
+        "tiny_fp32": legs["tiny_fp32"],
         "decode": decode,
         "ccq": ccq,
         "backward": backward,

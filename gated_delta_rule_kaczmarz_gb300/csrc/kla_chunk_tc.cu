@@ -1629,10 +1629,14 @@ prep_kernel(const int *cu, int N, int total_T, int *chunk_prefix, int *order, un
 // segment 0.
 
 // Per (batch, head, CBW columns): S_1 .. S_{P-1} into Sst (bf16, the
-// correction's operand) and S_P as S_T.  The columns are independent.
+// correction's operand) and S_P as S_T.  The columns are independent.  Each
+// thread owns NX columns of one row; Phi_{s+1} and N_{s+1} are fetched into
+// registers while the product of segment s runs, and the shared-memory rows
+// are float4-aligned (Phi rows of D + 4 floats, S rows of CBW + 4).
 constexpr int CB_THREADS = 256;
 constexpr int CBW = 16;   // state columns per CTA (two threads per row, CBW / 2 each)
-constexpr size_t CB_SMEM = ((size_t)D * (D + 1) + (size_t)D * (CBW + 1)) * sizeof(float);
+constexpr int CB_PH = D + 4, CB_SS = CBW + 4;
+constexpr size_t CB_SMEM = ((size_t)D * CB_PH + (size_t)D * CB_SS) * sizeof(float);
 
 __global__ void __launch_bounds__(CB_THREADS)
 split_combine_kernel(const float *__restrict__ Nbuf, const float *__restrict__ Phi,
@@ -1640,51 +1644,94 @@ split_combine_kernel(const float *__restrict__ Nbuf, const float *__restrict__ P
                      const unsigned *status) {
     extern __shared__ float cb_sm[];
     constexpr int NX = CBW / 2;
-    float(*Ph)[D + 1] = reinterpret_cast<float(*)[D + 1]>(cb_sm);                        // Phi_s
-    float(*Ss)[CBW + 1] = reinterpret_cast<float(*)[CBW + 1]>(cb_sm + (size_t)D * (D + 1));   // S_s
+    constexpr int NV = D * D / 4 / CB_THREADS;   // float4 of Phi per thread
+    float(*Ph)[CB_PH] = reinterpret_cast<float(*)[CB_PH]>(cb_sm);                       // Phi_s
+    float(*Ss)[CB_SS] = reinterpret_cast<float(*)[CB_SS]>(cb_sm + (size_t)D * CB_PH);   // S_s
     if (status_bad(status)) return;
     const int unit = blockIdx.x, b = unit / H, h = unit % H, jb = blockIdx.y * CBW;
     const int tid = threadIdx.x, i = tid >> 1, j0 = (tid & 1) * NX;
-    float cur[NX];
-    const float *n0 = Nbuf + ((size_t)b * P * H + h) * D * D + (size_t)i * D + jb + j0;
+    auto n_block = [&](int sg) {   // row i, columns jb + j0 .. of N_sg
+        return reinterpret_cast<const float4 *>(Nbuf + ((size_t)(b * P + sg) * H + h) * D * D +
+                                                (size_t)i * D + jb + j0);
+    };
+    auto phi_of = [&](int sg) {    // Phi of segment sg >= 1
+        return reinterpret_cast<const float4 *>(Phi + ((size_t)(b * (P - 1) + sg - 1) * H + h) * D * D);
+    };
+    float cur[NX], nx[NX];
+    float4 buf[NV];
+    {
+        const float4 *n0 = n_block(0);
+        const float4 a0 = n0[0], a1 = n0[1];
+        cur[0] = a0.x; cur[1] = a0.y; cur[2] = a0.z; cur[3] = a0.w;
+        cur[4] = a1.x; cur[5] = a1.y; cur[6] = a1.z; cur[7] = a1.w;
+    }
+    if (P > 1) {
+        const float4 *src = phi_of(1);
 #pragma unroll
-    for (int x = 0; x < NX; ++x) cur[x] = n0[x];
+        for (int n = 0; n < NV; ++n) buf[n] = src[tid + n * CB_THREADS];
+        const float4 *n1 = n_block(1);
+        const float4 a0 = n1[0], a1 = n1[1];
+        nx[0] = a0.x; nx[1] = a0.y; nx[2] = a0.z; nx[3] = a0.w;
+        nx[4] = a1.x; nx[5] = a1.y; nx[6] = a1.z; nx[7] = a1.w;
+#pragma unroll
+        for (int n = 0; n < NV; ++n) {
+            const int e = (tid + n * CB_THREADS) * 4;
+            *reinterpret_cast<float4 *>(&Ph[e / D][e % D]) = buf[n];
+        }
+    }
     for (int sg = 1; sg < P; ++sg) {
-        const size_t pidx = ((size_t)(b * (P - 1) + sg - 1) * H + h) * D * D;
-        __nv_bfloat16 *dst = Sst + pidx + (size_t)i * D + jb + j0;
-#pragma unroll
-        for (int x = 0; x < NX; ++x) dst[x] = __float2bfloat16_rn(cur[x]);
-        __syncthreads();   // the previous segment's product is done with Ph and Ss
-        {   // Phi_s into shared memory: 16 float4 per thread, all issued first
-            constexpr int NV = D * D / 4 / CB_THREADS;
-            float4 buf[NV];
-            const float4 *src = reinterpret_cast<const float4 *>(Phi + pidx);
+        // S_sg: the correction's operand (bf16), and the product's right factor
+        __nv_bfloat16 *dst = Sst + ((size_t)(b * (P - 1) + sg - 1) * H + h) * D * D +
+                             (size_t)i * D + jb + j0;
+        uint4 pk;
+        pk.x = pack_bf2(cur[0], cur[1]); pk.y = pack_bf2(cur[2], cur[3]);
+        pk.z = pack_bf2(cur[4], cur[5]); pk.w = pack_bf2(cur[6], cur[7]);
+        *reinterpret_cast<uint4 *>(dst) = pk;
+        *reinterpret_cast<float4 *>(&Ss[i][j0]) = make_float4(cur[0], cur[1], cur[2], cur[3]);
+        *reinterpret_cast<float4 *>(&Ss[i][j0 + 4]) = make_float4(cur[4], cur[5], cur[6], cur[7]);
+        __syncthreads();   // Ss written; Ph holds Phi_sg
+        const bool more = sg + 1 < P;
+        float nn[NX];
+        if (more) {        // the next segment's Phi and N, in flight during the product
+            const float4 *src = phi_of(sg + 1);
 #pragma unroll
             for (int n = 0; n < NV; ++n) buf[n] = src[tid + n * CB_THREADS];
-#pragma unroll
-            for (int n = 0; n < NV; ++n) {
-                const int e = (tid + n * CB_THREADS) * 4, r = e / D, c = e % D;
-                Ph[r][c] = buf[n].x; Ph[r][c + 1] = buf[n].y;
-                Ph[r][c + 2] = buf[n].z; Ph[r][c + 3] = buf[n].w;
-            }
+            const float4 *nb = n_block(sg + 1);
+            const float4 a0 = nb[0], a1 = nb[1];
+            nn[0] = a0.x; nn[1] = a0.y; nn[2] = a0.z; nn[3] = a0.w;
+            nn[4] = a1.x; nn[5] = a1.y; nn[6] = a1.z; nn[7] = a1.w;
         }
 #pragma unroll
-        for (int x = 0; x < NX; ++x) Ss[i][j0 + x] = cur[x];
-        __syncthreads();
-        const float *ns = Nbuf + ((size_t)(b * P + sg) * H + h) * D * D + (size_t)i * D + jb + j0;
+        for (int x = 0; x < NX; ++x) cur[x] = nx[x];
+#pragma unroll 2
+        for (int k4 = 0; k4 < D; k4 += 4) {
+            const float4 f = *reinterpret_cast<const float4 *>(&Ph[i][k4]);
+            const float fk[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-        for (int x = 0; x < NX; ++x) cur[x] = ns[x];
-#pragma unroll 4
-        for (int kk = 0; kk < D; ++kk) {
-            const float f = Ph[i][kk];
+            for (int e = 0; e < 4; ++e) {
+                const float4 s0 = *reinterpret_cast<const float4 *>(&Ss[k4 + e][j0]);
+                const float4 s1 = *reinterpret_cast<const float4 *>(&Ss[k4 + e][j0 + 4]);
+                cur[0] = fmaf(fk[e], s0.x, cur[0]); cur[1] = fmaf(fk[e], s0.y, cur[1]);
+                cur[2] = fmaf(fk[e], s0.z, cur[2]); cur[3] = fmaf(fk[e], s0.w, cur[3]);
+                cur[4] = fmaf(fk[e], s1.x, cur[4]); cur[5] = fmaf(fk[e], s1.y, cur[5]);
+                cur[6] = fmaf(fk[e], s1.z, cur[6]); cur[7] = fmaf(fk[e], s1.w, cur[7]);
+            }
+        }
+        __syncthreads();   // Ph and Ss are no longer read
+        if (more) {
 #pragma unroll
-            for (int x = 0; x < NX; ++x) cur[x] = fmaf(f, Ss[kk][j0 + x], cur[x]);
+            for (int x = 0; x < NX; ++x) nx[x] = nn[x];
+#pragma unroll
+            for (int n = 0; n < NV; ++n) {
+                const int e = (tid + n * CB_THREADS) * 4;
+                *reinterpret_cast<float4 *>(&Ph[e / D][e % D]) = buf[n];
+            }
         }
     }
     if (S_T) {
-        float *dst = S_T + ((size_t)unit * D + i) * D + jb + j0;
-#pragma unroll
-        for (int x = 0; x < NX; ++x) dst[x] = cur[x];
+        float4 *dst = reinterpret_cast<float4 *>(S_T + ((size_t)unit * D + i) * D + jb + j0);
+        dst[0] = make_float4(cur[0], cur[1], cur[2], cur[3]);
+        dst[1] = make_float4(cur[4], cur[5], cur[6], cur[7]);
     }
 }
 
