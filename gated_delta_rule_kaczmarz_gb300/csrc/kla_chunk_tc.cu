@@ -73,12 +73,15 @@ struct TcParams {
     __nv_bfloat16 *U_ws;       // [slots][64][128]   U~
     __nv_bfloat16 *A_ws;       // [slots][64 keys s][64 queries t]  A^T
     int beta_mode;             // 0: beta = eta / (||k||^2 + eps); 1: beta = eta
-    // Sequence split (fixed length): every sequence is run as seg_P virtual
-    // sequences of T / seg_P tokens.  State CTAs [0, phi_first) run the state
-    // pass of the virtual sequences (S0 only for the first segment); CTAs from
-    // phi_first on run the transition pass of the later segments (S0 = I,
-    // U~ read as 0), whose outputs are Q_corr rows (o_phi) and Phi (S_T_phi).
+    // Sequence split (fixed length): every sequence of seg_T tokens (seg_nch
+    // chunks) is run as seg_P virtual sequences (segments) of whole 128-token
+    // tiles: the first seg_r segments hold seg_q + 1 tiles, the others seg_q.
+    // State CTAs [0, phi_first) run the state pass of the virtual sequences
+    // (S0 only for the first segment); CTAs from phi_first on run the
+    // transition pass of the later segments (S0 = I, U~ read as 0), whose
+    // outputs are Q_corr rows (o_phi) and Phi (S_T_phi).
     int seg_P, phi_first;
+    int seg_T, seg_nch, seg_q, seg_r;
     __nv_bfloat16 *o_phi;
     float *S_T_phi;
     // Recording for the backward pass: the state at every chunk start (per
@@ -114,6 +117,12 @@ __device__ __forceinline__ bool status_bad(const unsigned *status) {
 
 // Chunk g of head h: its sequence, first token row, valid length.  False when
 // g lies beyond the last chunk (the grid is sized by an upper bound).
+// Segment s of a split sequence: its first 128-token tile and its tile count.
+__host__ __device__ __forceinline__ void seg_tiles(int q, int r, int s, int &tile0, int &ntiles) {
+    tile0 = s * q + (s < r ? s : r);
+    ntiles = q + (s < r ? 1 : 0);
+}
+
 __device__ __forceinline__ bool slot_info(const TcParams &p, long g, int &seq, long &row0,
                                           int &nc) {
     if (p.chunk_prefix == nullptr) {
@@ -993,6 +1002,12 @@ __device__ __forceinline__ void state_run(const CUtensorMap *mq, const CUtensorM
         start = p.cu_seqlens[seq];
         len = (long)p.cu_seqlens[seq + 1] - start;
         chunk0 = p.chunk_prefix[seq];
+    } else if (segP > 1) {   // segment seq % segP of sequence seq / segP
+        int tile0, ntiles;
+        seg_tiles(p.seg_q, p.seg_r, seq % segP, tile0, ntiles);
+        start = (long)(seq / segP) * p.seg_T + 128L * tile0;
+        len = 128L * ntiles;
+        chunk0 = (long)(seq / segP) * p.seg_nch + 2L * tile0;
     } else {
         start = (long)seq * p.T;
         len = p.T;
@@ -1744,8 +1759,8 @@ constexpr uint32_t CR_A = 0, CR_B = 32768, CR_O = 65536, CR_SMEM = 98304 + 1024;
 
 __global__ void __launch_bounds__(CR_THREADS)
 split_correct_kernel(const __grid_constant__ CUtensorMap mqc, const __grid_constant__ CUtensorMap mo,
-                     const __grid_constant__ CUtensorMap mss, int H, int T, int P,
-                     int tiles_per_seg, unsigned *status) {
+                     const __grid_constant__ CUtensorMap mss, int H, int T, int P, int seg_q,
+                     int seg_r, int later_tiles, unsigned *status) {
     extern __shared__ unsigned char smraw[];
     unsigned char *sm = align1024(smraw);
     __shared__ uint64_t bar_ld, bar_mma;
@@ -1753,15 +1768,18 @@ split_correct_kernel(const __grid_constant__ CUtensorMap mqc, const __grid_const
     __shared__ int sok;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (status_bad(status)) return;
-    long r = blockIdx.x;
-    const int t_in = (int)(r % tiles_per_seg);
-    r /= tiles_per_seg;
-    const int h = (int)(r % H);
-    r /= H;   // b * (P - 1) + (segment - 1)
-    const long b = r / (P - 1);
-    const int sg = 1 + (int)(r % (P - 1));
-    const int row0 = (int)(b * T + (long)sg * (T / P) + (long)t_in * 128);
-    const int srow = (int)((r * H + h) * D);   // first row of S_s in the bf16 array
+    // CTA = (batch, head, tile after the first segment), tiles in order
+    long x = blockIdx.x;
+    const int tau = (int)(x % later_tiles);
+    x /= later_tiles;
+    const int h = (int)(x % H);
+    const long b = x / H;
+    int t0, n0;
+    seg_tiles(seg_q, seg_r, 0, t0, n0);
+    const int j = n0 + tau;   // tile of the sequence, and its segment
+    const int sg = j < seg_r * (seg_q + 1) ? j / (seg_q + 1) : seg_r + (j - seg_r * (seg_q + 1)) / seg_q;
+    const int row0 = (int)(b * T + 128L * j);
+    const int srow = (int)(((b * (P - 1) + sg - 1) * H + h) * D);   // first row of S_s (bf16 array)
     if (tid == 0) {
         mbar_init(&bar_ld, 1);
         mbar_init(&bar_mma, 1);
@@ -1881,30 +1899,44 @@ WsLayout layout(long n_chunks, int H, int n_seq) {
 // transition passes per (sequence, head).
 long split_chains(long units, int P) { return units * P + units * (P - 1); }
 
-// Sequence split factor P for a fixed-length batch (1: none).  Each segment
-// is a whole number of 128-token tiles.  By default the largest P in
-// {8, 4, 2} such that either the segments hold at least 1024 tokens and the
-// state and transition passes fit on the SMs at once as two 64-column CTAs
-// per chain, or the segments hold at least 4096 tokens and they fit as one
-// 128-column CTA per chain (a pass with two load stages, which pays only on
-// long chains) -- few heads and long sequences, where the serial chain of
-// the state pass dominates.  The environment variable KLA_SEQ_SPLIT=P sets
-// it (any P whose segments are whole 128-token tiles; KLA_SEQ_SPLIT=1
+// Sequence split factor P for a fixed-length batch (1: none).  The sequence
+// is cut into P segments of whole 128-token tiles, as equal as the tile count
+// allows (the first ones one tile longer).  A P is eligible if its state and
+// transition passes fit on the SMs at once, as two 64-column CTAs per chain
+// with segments of at least 1024 tokens, or as one 128-column CTA per chain
+// (a pass with two load stages, which pays only on long chains) with
+// segments of at least 4096 tokens; of the eligible P <= 8 (and no split)
+// the one with the shortest longest chain is taken, weighing a 128-column
+// chain step as 3/2 of a 64-column one -- few heads and long sequences, where
+// the serial chain of the state pass dominates.  The environment variable
+// KLA_SEQ_SPLIT=P sets it (any P up to the tile count; KLA_SEQ_SPLIT=1
 // disables the split).
 int split_factor(int n_seq, int T, int H, bool varlen) {
-    if (varlen || T <= 0) return 1;
-    auto valid = [&](int P) { return P >= 2 && T % (P * 128) == 0; };
+    if (varlen || T <= 0 || T % 128 != 0) return 1;
+    const int tiles = T / 128;
+    auto valid = [&](int P) { return P >= 2 && P <= tiles; };
     if (const char *e = getenv("KLA_SEQ_SPLIT")) {
         const int P = atoi(e);
         return valid(P) ? P : 1;
     }
     const long units = (long)n_seq * H, sms = sm_count();
-    for (int P = 8; P >= 2; P >>= 1) {
-        if (!valid(P)) continue;
-        if (T / P >= 1024 && 2 * split_chains(units, P) <= sms) return P;
-        if (T / P >= 4096 && split_chains(units, P) <= sms) return P;
+    // chain cost in half-steps: a 64-column chain step counts 2, a 128-column
+    // one 3 (measured about 1.4 and 2.1 us per chunk)
+    long best_cost = (long)(T / C) * (2 * units <= sms ? 2 : 3);
+    int best = 1;
+    for (int P = 2; P <= 8 && P <= tiles; ++P) {
+        const int shortest = tiles / P, longest = (tiles + P - 1) / P;
+        long cost = -1;
+        if (shortest * 128 >= 1024 && 2 * split_chains(units, P) <= sms)
+            cost = 2L * 2 * longest;
+        else if (shortest * 128 >= 4096 && split_chains(units, P) <= sms)
+            cost = 3L * 2 * longest;
+        if (cost >= 0 && cost < best_cost) {
+            best_cost = cost;
+            best = P;
+        }
     }
-    return 1;
+    return best;
 }
 
 // A split whose chains in two 64-column CTAs each would outnumber the SMs
@@ -1931,13 +1963,15 @@ SplitLayout split_layout(int n_seq, int T, int H, int P) {
 }
 
 // The fused launch serves fixed-length batches with an even number of chunks
-// per (virtual) sequence whose state pass (with the sequence split: state and
-// transition passes) fits on at most half of the SMs; with fewer SMs left to
+// per (virtual) sequence, equal segments when split, whose state pass (with
+// the sequence split: state and transition passes) fits on at most half of
+// the SMs; with fewer SMs left to
 // phase 1 its items arrive more slowly than the chain consumes them.
 bool use_fused(const Problem &p) {
     if (p.cu_seqlens != nullptr || p.T <= 0) return false;
     // a call recording the chunk-start states for the backward does not split
     const int P = p.S_chk ? 1 : split_factor(p.n_seq, p.T, p.H, false);
+    if (P > 1 && p.T % (P * 128) != 0) return false;   // segments of unequal length
     const int nch = (p.T / P + C - 1) / C;
     if (nch % 2 != 0) return false;
     return 2 * split_chains((long)p.n_seq * p.H, P) <= sm_count() / 2;
@@ -2015,12 +2049,25 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     tp.eps = p.eps;
     tp.beta_mode = p.beta_mode;
     tp.seg_P = P;
+    if (P > 1) {
+        tp.seg_T = p0.T;
+        tp.seg_nch = p0.T / C;
+        tp.seg_q = p0.T / 128 / P;
+        tp.seg_r = p0.T / 128 % P;
+    }
     tp.alpha = p.alpha;
     tp.eta = p.eta;
     tp.S0 = p.S0;
     tp.S_T = p.S_T;
     const bool fused = use_fused(p0);
     bool wide_split = !fused && split_wide((long)p0.n_seq * p0.H, P);
+    if (P > 1 && !fused) {
+        // phase 1 of the two-launch path runs over the real sequences (the
+        // chunk slots are the same); only the state pass sees the segments
+        tp.n_seq = p0.n_seq;
+        tp.T = p0.T;
+        tp.nch_fixed = p0.T / C;
+    }
     if (P > 1) {   // the virtual sequences' end states go to N, not to S_T
         tp.S_T = reinterpret_cast<float *>(ws + split_base + SL.N);
         tp.phi_first = (wide_split ? 1 : 2) * p.n_seq * p.H;
@@ -2178,10 +2225,12 @@ cudaError_t launch_split_tail(const Problem &p0, const Problem &p, const TcParam
             return e;
         cattr = true;
     }
-    const int tiles_per_seg = p0.T / P / 128;
-    const long n_tiles = (long)p0.n_seq * (P - 1) * p.H * tiles_per_seg;
-    split_correct_kernel<<<(unsigned)n_tiles, CR_THREADS, CR_SMEM, s>>>(mqc, mo, mss, p.H, p0.T, P,
-                                                                        tiles_per_seg, p0.status);
+    int t0, n0;
+    seg_tiles(tp.seg_q, tp.seg_r, 0, t0, n0);
+    const int later_tiles = p0.T / 128 - n0;
+    const long n_tiles = (long)p0.n_seq * p.H * later_tiles;
+    split_correct_kernel<<<(unsigned)n_tiles, CR_THREADS, CR_SMEM, s>>>(
+        mqc, mo, mss, p.H, p0.T, P, tp.seg_q, tp.seg_r, later_tiles, p0.status);
     note_launch();
     return cudaGetLastError();
 }

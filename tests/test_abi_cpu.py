@@ -212,7 +212,7 @@ def test_backward_host_validation():
 def test_sequence_split_workspace(monkeypatch):
     """The split's buffers (per-segment end states, transitions, the
     correction rows, the start states) enlarge the forward's workspace; a
-    factor whose segments are not whole 128-token tiles is ignored."""
+    factor above the sequence's count of 128-token tiles is ignored."""
     lib = binding.load()
     size = lambda: lib.kla_chunk_fwd_workspace_size(1, 32768, 16, 128, 128, 64, 1)
     monkeypatch.setenv("KLA_SEQ_SPLIT", "1")
@@ -221,5 +221,10 @@ def test_sequence_split_workspace(monkeypatch):
     split2 = size()
     # correction rows alone: T * H * 128 bf16
     assert split2 - base >= 32768 * 16 * 128 * 2
-    monkeypatch.setenv("KLA_SEQ_SPLIT", "3")   # 32768 is not a multiple of 3 * 128
-    assert size() == base
+    monkeypatch.setenv("KLA_SEQ_SPLIT", "3")   # segments of 86 + 85 + 85 tiles
+    assert size() > base
+    small = lambda: lib.kla_chunk_fwd_workspace_size(1, 256, 16, 128, 128, 64, 1)
+    monkeypatch.setenv("KLA_SEQ_SPLIT", "1")
+    small_base = small()
+    monkeypatch.setenv("KLA_SEQ_SPLIT", "3")   # 256 tokens: two tiles
+    assert small() == small_base

@@ -27,12 +27,17 @@ def split(monkeypatch):
 
 
 # launches: the fused launch (phase 1, state and transition passes) when the
-# state and transition CTAs fit on half of the SMs, else phase 1 and the state
-# + transition launch; then the combine and the correction
+# segments are equal and the state and transition CTAs fit on half of the
+# SMs, else phase 1 and the state + transition launch; then the combine and
+# the correction.  Segments are whole 128-token tiles, as equal as the tile
+# count allows (640 tokens in 2: 3 + 2 tiles; 896 in 3: 3 + 2 + 2; 512 in 3:
+# 2 + 1 + 1; 1152 in 8: 2 + 1 x 7).
 @pytest.mark.parametrize("B,T,H,P,with_S0,no_alpha,mode,launches", [
     (1, 512, 2, 2, True, False, "kaczmarz", 3), (2, 512, 2, 4, True, False, "kaczmarz", 3),
     (2, 768, 3, 3, False, False, "kaczmarz", 3), (1, 1024, 2, 8, True, True, "kaczmarz", 3),
-    (2, 256, 2, 2, True, False, "given", 3), (4, 1024, 8, 2, True, False, "kaczmarz", 4)])
+    (2, 256, 2, 2, True, False, "given", 3), (4, 1024, 8, 2, True, False, "kaczmarz", 4),
+    (1, 640, 2, 2, True, False, "kaczmarz", 4), (2, 896, 3, 3, True, True, "kaczmarz", 4),
+    (1, 512, 2, 3, False, False, "given", 4), (1, 1152, 2, 8, True, False, "kaczmarz", 4)])
 def test_split_forward_parity(split, B, T, H, P, with_S0, no_alpha, mode, launches):
     split(P)
     inp = prefill_inputs(B, T, H, 128, 128, "bf16", seed=400 + T + P, s0_var=0.01)
@@ -52,6 +57,7 @@ def test_split_forward_parity(split, B, T, H, P, with_S0, no_alpha, mode, launch
 @pytest.mark.parametrize("B,T,H,P,with_S0,no_alpha,mode", [
     (1, 4096, 16, 4, True, False, "kaczmarz"),   # 16 x 7 chains: two CTAs each would not fit
     (2, 2048, 16, 2, False, True, "given"),      # 32 x 3 chains
+    (1, 4608, 16, 5, True, False, "kaczmarz"),   # 16 x 9 chains, segments of 8 + 7 x 4 tiles
 ])
 def test_split_with_one_wide_cta_per_chain(split, B, T, H, P, with_S0, no_alpha, mode):
     """A split whose state and transition chains in two 64-column CTAs each
@@ -87,8 +93,8 @@ def test_split_matches_unsplit(split):
 
 
 def test_split_invalid_factor_falls_back(split):
-    """A factor whose segments are not whole 128-token tiles runs unsplit."""
-    split(3)
+    """A factor above the sequence's count of 128-token tiles runs unsplit."""
+    split(5)
     inp = prefill_inputs(1, 512, 2, 128, 128, "bf16", seed=10)
     g = cuda(inp)
     n0 = kla.kla_launch_count()
@@ -119,3 +125,38 @@ def test_long_context_takes_the_split_sampled(monkeypatch):
                                       None if inp["S0"] is None else inp["S0"][:, h:h + 1])
         assert rel_err(o[:, :, h:h + 1], o_ref) <= 2e-2
         assert rel_err(S[:, h:h + 1], S_ref) <= 2e-2
+
+
+def _unequal_draws(n, seed):
+    """Seeded shapes whose forced factor leaves segments of unequal length:
+    T a whole number of 128-token tiles (2 to 12), P from 2 to min(8, tiles)
+    not dividing it."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        tiles = int(rng.integers(2, 13))
+        P = int(rng.integers(2, min(8, tiles) + 1))
+        if tiles % P == 0:
+            continue
+        cases.append(dict(B=int(rng.integers(1, 4)), T=128 * tiles, H=int(rng.integers(1, 5)),
+                          P=P, s0=float(rng.choice([0.0, 0.01])), seed=int(rng.integers(1 << 30))))
+    return cases
+
+
+UNEQUAL = _unequal_draws(6, 20261203)
+
+
+@pytest.mark.parametrize("case", UNEQUAL, ids=[f"unequal{i}" for i in range(len(UNEQUAL))])
+def test_split_unequal_segments_random(split, case):
+    c = case
+    split(c["P"])
+    inp = prefill_inputs(c["B"], c["T"], c["H"], 128, 128, "bf16", seed=c["seed"], s0_var=c["s0"])
+    g = cuda(inp)
+    n0 = kla.kla_launch_count()
+    o, S = kla.kla_chunk_fwd(g["q"], g["k"], g["v"], g["alpha"], g["eta"], inp["eps"], g["S0"])
+    torch.cuda.synchronize()
+    assert kla.kla_launch_count() - n0 == 4   # phase 1, state + transition, combine, correction
+    o_ref, S_ref = oracle.forward(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["eta"],
+                                  inp["eps"], inp["S0"], nthreads=8)
+    assert rel_err(o, o_ref) <= 2e-2
+    assert rel_err(S, S_ref) <= 2e-2
