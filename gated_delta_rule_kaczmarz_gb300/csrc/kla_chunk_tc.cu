@@ -576,12 +576,23 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     // element (exponent clamped at 0, where the mask discards it) and masked
     // by a select, so that the loop has no data-dependent branch.
     const float gt2 = sG2[r];
+    // A warp's 32 rows are all in one half of their chunk (t < 32 or t >= 32,
+    // the same for the whole warp), so the column blocks that the triangle
+    // leaves empty (L: columns 32..63 of rows t < 32; A^T: columns 0..31 of
+    // rows t >= 32) are written as zeros without being formed.
     if (ok) {
         if (hf == 0) {
             float *Lrow = lslot(KQ, slot) + t * 64;
             const int lim = (t < nc) ? t : 0;     // L row t has columns s < t
 #pragma unroll 1
             for (int g16 = 0; g16 < 4; ++g16) {
+                if (g16 >= 2 && t < 32) {
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4)
+                        *reinterpret_cast<float4 *>(Lrow + lsw(t, g16 * 16 + i)) =
+                            make_float4(0.f, 0.f, 0.f, 0.f);
+                    continue;
+                }
                 uint32_t rr[16];
                 tmem_ld16(tb + lane_base + cb + g16 * 16, rr);
                 float gs[16];
@@ -609,6 +620,14 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
             const int hi = nc;                      // A^T row t has columns u in [t, nc)
 #pragma unroll 1
             for (int g16 = 0; g16 < 4; ++g16) {
+                if (g16 < 2 && t >= 32) {
+                    if (vslot) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.A_ws + slot_row * 64 + g16 * 16);
+                        dst[0] = make_uint4(0u, 0u, 0u, 0u);
+                        dst[1] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    continue;
+                }
                 uint32_t rr[16];
                 tmem_ld16(tb + lane_base + 128 + cb + g16 * 16, rr);
                 float gu[16];
