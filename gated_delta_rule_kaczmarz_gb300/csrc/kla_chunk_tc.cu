@@ -164,6 +164,12 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // a -> low half
     return *reinterpret_cast<const uint32_t *>(&v);
 }
+// A bf16 pair as two floats (low half first).
+__device__ __forceinline__ float2 bf2_f2(uint32_t u) { return make_float2(bf_lo(u), bf_hi(u)); }
+// Two fp32 lanes per instruction (each lane rounded as the scalar operation).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 bcast2(float a) { return make_float2(a, a); }
 
 // fp32 64 x 64 matrices in shared memory, one per chunk, rows of 64 floats;
 // the float4 index within a row is XORed with (row % 16) so that a thread per
@@ -200,7 +206,7 @@ __device__ __forceinline__ void merge_top(unsigned char *kq, float *scratch, int
 #pragma unroll 1
         for (int k = 0; k < 2; ++k) {
             const int cb = k ? 7 - w : w;
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll 1
             for (int s4 = cb; s4 < 8; ++s4) {
                 const float4 a = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, 4 * s4));
@@ -209,14 +215,12 @@ __device__ __forceinline__ void merge_top(unsigned char *kq, float *scratch, int
                 for (int e = 0; e < 4; ++e) {
                     const int s = 4 * s4 + e;
                     const float4 b = *reinterpret_cast<const float4 *>(Lp + s * 64 + lsw(s, 4 * cb));
-                    a0 = fmaf(am[e], b.x, a0);
-                    a1 = fmaf(am[e], b.y, a1);
-                    a2 = fmaf(am[e], b.z, a2);
-                    a3 = fmaf(am[e], b.w, a3);
+                    a01 = fma2(bcast2(am[e]), make_float2(b.x, b.y), a01);
+                    a23 = fma2(bcast2(am[e]), make_float2(b.z, b.w), a23);
                 }
             }
             *reinterpret_cast<float4 *>(Mp + lane * 32 + ((cb ^ (lane & 7)) << 2)) =
-                make_float4(a0, a1, a2, a3);
+                make_float4(a01.x, a01.y, a23.x, a23.y);
         }
     }
     named_sync(bar, P1_THREADS);  // M complete; L21 no longer read
@@ -226,7 +230,7 @@ __device__ __forceinline__ void merge_top(unsigned char *kq, float *scratch, int
         for (int k = 0; k < 2; ++k) {
             const int j = k ? 7 - w : w;
             const int rr = 4 * j + (lane >> 3), r = 32 + rr;
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll 1
             for (int s4 = 0; s4 <= j; ++s4) {
                 const float4 a = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, 32 + 4 * s4));
@@ -235,13 +239,12 @@ __device__ __forceinline__ void merge_top(unsigned char *kq, float *scratch, int
                 for (int e = 0; e < 4; ++e) {
                     const int s = 4 * s4 + e;
                     const float4 b = *reinterpret_cast<const float4 *>(Mp + s * 32 + ((pc ^ (s & 7)) << 2));
-                    a0 = fmaf(am[e], b.x, a0);
-                    a1 = fmaf(am[e], b.y, a1);
-                    a2 = fmaf(am[e], b.z, a2);
-                    a3 = fmaf(am[e], b.w, a3);
+                    a01 = fma2(bcast2(am[e]), make_float2(b.x, b.y), a01);
+                    a23 = fma2(bcast2(am[e]), make_float2(b.z, b.w), a23);
                 }
             }
-            *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, 4 * pc)) = make_float4(-a0, -a1, -a2, -a3);
+            *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, 4 * pc)) =
+                make_float4(-a01.x, -a01.y, -a23.x, -a23.y);
         }
     }
     named_sync(bar, P1_THREADS);
@@ -266,10 +269,10 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, i
     const int pr = q / pcols, pc = q % pcols;        // rows [rows*pr, +rows), cols [4pc, +4)
     float *Lp = lslot(kq, p);
     float *Mp = scratch + blkid * n * n;
-    float acc[rows][4];
+    float2 acc[rows][2];
     // M = L21 D1
 #pragma unroll
-    for (int m = 0; m < rows; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+    for (int m = 0; m < rows; ++m) acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
 #pragma unroll 1
     for (int s4 = 0; s4 < n / 4; ++s4) {
         float4 bb[4];
@@ -285,18 +288,16 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, i
             const float am[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                acc[m][0] = fmaf(am[e], bb[e].x, acc[m][0]);
-                acc[m][1] = fmaf(am[e], bb[e].y, acc[m][1]);
-                acc[m][2] = fmaf(am[e], bb[e].z, acc[m][2]);
-                acc[m][3] = fmaf(am[e], bb[e].w, acc[m][3]);
+                acc[m][0] = fma2(bcast2(am[e]), make_float2(bb[e].x, bb[e].y), acc[m][0]);
+                acc[m][1] = fma2(bcast2(am[e]), make_float2(bb[e].z, bb[e].w), acc[m][1]);
             }
         }
     }
 #pragma unroll
     for (int m = 0; m < rows; ++m) {
         *reinterpret_cast<float4 *>(Mp + (rows * pr + m) * n + 4 * pc) =
-            make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
-        acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+            make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
+        acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
     }
     named_sync(bar, P1_THREADS);  // M complete; L21 no longer read
     // X = -D2 M, written over L21.  D2 is lower triangular (zeros above its
@@ -318,10 +319,8 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, i
             const float am[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                acc[m][0] = fmaf(am[e], bb[e].x, acc[m][0]);
-                acc[m][1] = fmaf(am[e], bb[e].y, acc[m][1]);
-                acc[m][2] = fmaf(am[e], bb[e].z, acc[m][2]);
-                acc[m][3] = fmaf(am[e], bb[e].w, acc[m][3]);
+                acc[m][0] = fma2(bcast2(am[e]), make_float2(bb[e].x, bb[e].y), acc[m][0]);
+                acc[m][1] = fma2(bcast2(am[e]), make_float2(bb[e].z, bb[e].w), acc[m][1]);
             }
         }
     }
@@ -329,7 +328,7 @@ __device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, i
     for (int m = 0; m < rows; ++m) {
         const int r = o + n + rows * pr + m;
         *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, o + 4 * pc)) =
-            make_float4(-acc[m][0], -acc[m][1], -acc[m][2], -acc[m][3]);
+            make_float4(-acc[m][0].x, -acc[m][0].y, -acc[m][1].x, -acc[m][1].y);
     }
     named_sync(bar, P1_THREADS);
 }
@@ -540,18 +539,18 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
 
     // ---- beta_t from the key's squared norm (fp32 over the bf16 values);
     //      each thread half sums one 64-feature slab ----
-    float n2 = 0.f;
+    float2 n2p = make_float2(0.f, 0.f);   // even and odd features
 #pragma unroll 2
     for (int ch = 0; ch < 8; ++ch) {
         const uint4 v = *reinterpret_cast<const uint4 *>(KQ + hf * 32768 + sw128_offset(r, ch * 8));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float x0 = bf_lo(w[i]), x1 = bf_hi(w[i]);
-            n2 = fmaf(x0, x0, n2);
-            n2 = fmaf(x1, x1, n2);
+            const float2 x = bf2_f2(w[i]);
+            n2p = fma2(x, x, n2p);
         }
     }
+    const float n2 = n2p.x + n2p.y;
     if (hf) sN2[r] = n2;
     named_sync(bar, P1_THREADS);
     float bt = 0.f;
@@ -665,10 +664,11 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
         for (int ch = 0; ch < 8; ++ch) {
             uint4 *pk4 = reinterpret_cast<uint4 *>(KQ + hf * 32768 + sw128_offset(r, ch * 8));
             const uint4 v = *pk4;
-            uint4 w = make_uint4(pack_bf2(gam_t * bf_lo(v.x), gam_t * bf_hi(v.x)),
-                                 pack_bf2(gam_t * bf_lo(v.y), gam_t * bf_hi(v.y)),
-                                 pack_bf2(gam_t * bf_lo(v.z), gam_t * bf_hi(v.z)),
-                                 pack_bf2(gam_t * bf_lo(v.w), gam_t * bf_hi(v.w)));
+            const float2 gg = bcast2(gam_t);
+            float2 a0 = mul2(gg, bf2_f2(v.x)), a1 = mul2(gg, bf2_f2(v.y));
+            float2 a2 = mul2(gg, bf2_f2(v.z)), a3 = mul2(gg, bf2_f2(v.w));
+            uint4 w = make_uint4(pack_bf2(a0.x, a0.y), pack_bf2(a1.x, a1.y),
+                                 pack_bf2(a2.x, a2.y), pack_bf2(a3.x, a3.y));
             if (!live) w = make_uint4(0u, 0u, 0u, 0u);
             *pk4 = w;
         }
