@@ -127,9 +127,11 @@ __device__ __forceinline__ bool slot_info(const TcParams &p, long g, int &seq, l
                                           int &nc) {
     if (p.chunk_prefix == nullptr) {
         if (p.nch_fixed <= 0) return false;
-        seq = (int)(g / p.nch_fixed);
+        // 32-bit division: chunk slots stay below 2^31 (the host checks)
+        const uint32_t q = (uint32_t)g / (uint32_t)p.nch_fixed;
+        seq = (int)q;
         if (seq >= p.n_seq) return false;
-        const int c = (int)(g % p.nch_fixed);
+        const int c = (int)((uint32_t)g - q * (uint32_t)p.nch_fixed);
         row0 = (long)seq * p.T + (long)c * C;
         nc = min(C, p.T - c * C);
         return true;
@@ -443,13 +445,16 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     long pair;
     int h;
+    // (32-bit divisions: work items stay below 2^31, which the host checks)
     if (kFused) {   // item = (pair within the sequence) * units + (sequence * H + head)
-        const long u = item % p.n_units;
-        pair = (item / p.n_units) + (u / p.H) * (p.nch_fixed / 2);
-        h = (int)(u % p.H);
+        const uint32_t i32 = (uint32_t)item, pu = i32 / (uint32_t)p.n_units;
+        const uint32_t u = i32 - pu * (uint32_t)p.n_units, su = u / (uint32_t)p.H;
+        pair = (long)pu + (long)su * (p.nch_fixed / 2);
+        h = (int)(u - su * (uint32_t)p.H);
     } else {
-        pair = item / p.H;
-        h = (int)(item % p.H);
+        const uint32_t i32 = (uint32_t)item, pq = i32 / (uint32_t)p.H;
+        pair = (long)pq;
+        h = (int)(i32 - pq * (uint32_t)p.H);
     }
     int seq0, seq1, nc0, nc1;
     long r00, r01;
@@ -2043,6 +2048,9 @@ cudaError_t launch_split_tail(const Problem &p0, const Problem &p, const TcParam
 
 cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t s) {
     if (p0.n_seq == 0) return cudaSuccess;
+    // the kernels index work items and chunk slots in 32 bits
+    if (n_chunks_upper > INT32_MAX || (n_chunks_upper + 1) / 2 * (long)p0.H > INT32_MAX)
+        return cudaErrorInvalidValue;
     if (tmap::encode_fn() == nullptr) return cudaErrorNotSupported;
     // a split sequence runs as P virtual sequences of T / P tokens (same rows,
     // same chunk slots)
