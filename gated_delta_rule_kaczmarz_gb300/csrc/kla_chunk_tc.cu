@@ -1774,26 +1774,23 @@ split_combine_kernel(const float *__restrict__ Nbuf, const float *__restrict__ P
     }
 }
 
-// o[rows] += Q_corr[rows] S_s for 128 token rows of one (batch, segment >= 1,
-// head): one tcgen05 MMA chain (M = 128 tokens, N = 128, K = 128), A = Q_corr
-// rows (K-major, TMA), B = S_s in bf16 (MN-major, TMA), o rows loaded by TMA,
-// added to in shared memory and stored by TMA.
+// o[rows] += Q_corr[rows] S_s for the 128-row tiles of the later segments:
+// per tile one tcgen05 MMA chain (M = 128 tokens, N = 128, K = 128), A =
+// Q_corr rows (K-major, TMA), B = S_s in bf16 (MN-major, TMA), o rows loaded
+// by TMA, added to in shared memory and stored by TMA.  Persistent: CTA i
+// takes a contiguous run of tiles (tiles in (batch, head, tile) order, so a
+// run shares S_s for many tiles and reloads it only when the segment
+// changes); the next tile's Q_corr rows (and S_s) load while this tile's sum
+// is formed, its o rows once this tile's store has read shared memory.
 constexpr int CR_THREADS = 128;
 constexpr uint32_t CR_A = 0, CR_B = 32768, CR_O = 65536, CR_SMEM = 98304 + 1024;
 
-__global__ void __launch_bounds__(CR_THREADS)
-split_correct_kernel(const __grid_constant__ CUtensorMap mqc, const __grid_constant__ CUtensorMap mo,
-                     const __grid_constant__ CUtensorMap mss, int H, int T, int P, int seg_q,
-                     int seg_r, int later_tiles, unsigned *status) {
-    extern __shared__ unsigned char smraw[];
-    unsigned char *sm = align1024(smraw);
-    __shared__ uint64_t bar_ld, bar_mma;
-    __shared__ uint32_t tslot;
-    __shared__ int sok;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (status_bad(status)) return;
-    // CTA = (batch, head, tile after the first segment), tiles in order
-    long x = blockIdx.x;
+struct CrTile {
+    int h, row0, srow;
+};
+
+__device__ __forceinline__ CrTile cr_tile(long x, int H, int T, int P, int seg_q, int seg_r,
+                                          int later_tiles) {
     const int tau = (int)(x % later_tiles);
     x /= later_tiles;
     const int h = (int)(x % H);
@@ -1802,10 +1799,31 @@ split_correct_kernel(const __grid_constant__ CUtensorMap mqc, const __grid_const
     seg_tiles(seg_q, seg_r, 0, t0, n0);
     const int j = n0 + tau;   // tile of the sequence, and its segment
     const int sg = j < seg_r * (seg_q + 1) ? j / (seg_q + 1) : seg_r + (j - seg_r * (seg_q + 1)) / seg_q;
-    const int row0 = (int)(b * T + 128L * j);
-    const int srow = (int)(((b * (P - 1) + sg - 1) * H + h) * D);   // first row of S_s (bf16 array)
+    CrTile c;
+    c.h = h;
+    c.row0 = (int)(b * T + 128L * j);
+    c.srow = (int)(((b * (P - 1) + sg - 1) * H + h) * D);   // first row of S_s (bf16 array)
+    return c;
+}
+
+__global__ void __launch_bounds__(CR_THREADS)
+split_correct_kernel(const __grid_constant__ CUtensorMap mqc, const __grid_constant__ CUtensorMap mo,
+                     const __grid_constant__ CUtensorMap mss, int H, int T, int P, int seg_q,
+                     int seg_r, int later_tiles, long n_tiles, unsigned *status) {
+    extern __shared__ unsigned char smraw[];
+    unsigned char *sm = align1024(smraw);
+    __shared__ uint64_t bar_a, bar_o, bar_b, bar_mma;
+    __shared__ uint32_t tslot;
+    __shared__ int sok;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (status_bad(status)) return;
+    const long x0 = (long)blockIdx.x * n_tiles / gridDim.x;
+    const long x1 = (long)(blockIdx.x + 1) * n_tiles / gridDim.x;
+    if (x0 >= x1) return;
     if (tid == 0) {
-        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_a, 1);
+        mbar_init(&bar_o, 1);
+        mbar_init(&bar_b, 1);
         mbar_init(&bar_mma, 1);
         fence_mbar_init();
         sok = 1;
@@ -1817,73 +1835,118 @@ split_correct_kernel(const __grid_constant__ CUtensorMap mqc, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tslot;
-    if (tid == 0) {
-        mbar_expect_tx(&bar_ld, 3u * 32768u);
-#pragma unroll
-        for (int sl = 0; sl < 2; ++sl)
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                tma_load_3d(sm + CR_A + sl * 16384 + hf * 8192, &mqc, &bar_ld, 64 * sl, h, row0 + 64 * hf);
-                tma_load_3d(sm + CR_O + sl * 16384 + hf * 8192, &mo, &bar_ld, 64 * sl, h, row0 + 64 * hf);
-            }
-#pragma unroll
-        for (int nb = 0; nb < 2; ++nb) tma_load_2d(sm + CR_B + nb * 16384, &mss, &bar_ld, 64 * nb, srow);
-        bool ok = mbar_wait(&bar_ld, 0u);
-        if (ok) {
-            tc_fence_after();
-            const uint32_t aA = smem_u32(sm + CR_A), aB = smem_u32(sm + CR_B);
-            const uint32_t id = idesc_bf16_f32(128, 128, false, true);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                mma_bf16(tb, sdesc_sw128(aA + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                         sdesc_sw128(aB + ks * 2048, 16384, 1024), id, ks > 0);
-            mma_commit(&bar_mma);
-            ok = mbar_wait(&bar_mma, 0u);
-            if (!ok) (void)mbar_wait(&bar_mma, 0u);   // the MMAs finish before TMEM is freed
-        } else {
-            (void)mbar_wait(&bar_ld, 0u);             // copies in flight land before the CTA leaves
-        }
-        if (!ok) {
-            sok = 0;
-            set_status(status, kDevTimeout);
-        }
-    }
-    __syncthreads();
-    tc_fence_after();
-    if (sok) {
-        const int rrow = warp * 32 + lane;
-#pragma unroll 1
-        for (int c4 = 0; c4 < 4; ++c4) {
-            uint32_t rr[32];
-            tmem_ld32(tb + ((uint32_t)(warp * 32) << 16) + c4 * 32, rr);
-            tmem_ld_wait();
-            unsigned char *tile = sm + CR_O + (c4 >> 1) * 16384;
-            const int col0 = (32 * c4) & 63;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint4 *pk = reinterpret_cast<uint4 *>(tile + sw128_offset(rrow, col0 + 8 * k));
-                const uint4 v = *pk;
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                uint32_t o4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    o4[e] = pack_bf2(bf_lo(w[e]) + __uint_as_float(rr[8 * k + 2 * e]),
-                                     bf_hi(w[e]) + __uint_as_float(rr[8 * k + 2 * e + 1]));
-                *pk = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-            }
-        }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && sok) {
+    auto load_rows = [&](const CUtensorMap *m, unsigned char *dst, uint64_t *bar, const CrTile &c) {
+        mbar_expect_tx(bar, 32768u);
 #pragma unroll
         for (int sl = 0; sl < 2; ++sl)
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf)
-                tma_store_3d(&mo, sm + CR_O + sl * 16384 + hf * 8192, 64 * sl, h, row0 + 64 * hf);
-        bulk_commit_group();
-        bulk_wait_group0();
+                tma_load_3d(dst + sl * 16384 + hf * 8192, m, bar, 64 * sl, c.h, c.row0 + 64 * hf);
+    };
+    auto load_s = [&](int srow) {
+        mbar_expect_tx(&bar_b, 32768u);
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) tma_load_2d(sm + CR_B + nb * 16384, &mss, &bar_b, 64 * nb, srow);
+    };
+    // thread 0's bookkeeping: loads issued per barrier (phase parities) and
+    // the S_s rows in shared memory
+    uint32_t n_a = 0, n_o = 0, n_b = 0, n_mma = 0;
+    int cur_srow = -1;
+    if (tid == 0) {
+        const CrTile c = cr_tile(x0, H, T, P, seg_q, seg_r, later_tiles);
+        load_s(c.srow);
+        cur_srow = c.srow;
+        ++n_b;
+        load_rows(&mqc, sm + CR_A, &bar_a, c);
+        ++n_a;
+        load_rows(&mo, sm + CR_O, &bar_o, c);
+        ++n_o;
+    }
+    for (long x = x0; x < x1; ++x) {
+        const CrTile c = cr_tile(x, H, T, P, seg_q, seg_r, later_tiles);
+        if (tid == 0) {
+            // this tile's S_s (the last one loaded) and Q_corr rows
+            bool ok = mbar_wait(&bar_b, (n_b - 1) & 1u) && mbar_wait(&bar_a, (n_a - 1) & 1u);
+            if (ok) {
+                tc_fence_after();
+                const uint32_t aA = smem_u32(sm + CR_A), aB = smem_u32(sm + CR_B);
+                const uint32_t id = idesc_bf16_f32(128, 128, false, true);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(tb, sdesc_sw128(aA + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                             sdesc_sw128(aB + ks * 2048, 16384, 1024), id, ks > 0);
+                mma_commit(&bar_mma);
+                ++n_mma;
+                ok = mbar_wait(&bar_mma, (n_mma - 1) & 1u);
+                if (!ok) (void)mbar_wait(&bar_mma, (n_mma - 1) & 1u);   // done before TMEM is reused
+            }
+            if (ok && x + 1 < x1) {   // A and B are free: the next tile's operands
+                const CrTile cn = cr_tile(x + 1, H, T, P, seg_q, seg_r, later_tiles);
+                if (cn.srow != cur_srow) {
+                    load_s(cn.srow);
+                    cur_srow = cn.srow;
+                    ++n_b;
+                }
+                load_rows(&mqc, sm + CR_A, &bar_a, cn);
+                ++n_a;
+            }
+            if (ok) ok = mbar_wait(&bar_o, (n_o - 1) & 1u);
+            if (!ok) {
+                sok = 0;
+                set_status(status, kDevTimeout);
+            }
+        }
+        __syncthreads();
+        if (!sok) break;
+        tc_fence_after();
+        {
+            const int rrow = warp * 32 + lane;
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t rr[32];
+                tmem_ld32(tb + ((uint32_t)(warp * 32) << 16) + c4 * 32, rr);
+                tmem_ld_wait();
+                unsigned char *tile = sm + CR_O + (c4 >> 1) * 16384;
+                const int col0 = (32 * c4) & 63;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    uint4 *pk = reinterpret_cast<uint4 *>(tile + sw128_offset(rrow, col0 + 8 * k));
+                    const uint4 v = *pk;
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t o4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        o4[e] = pack_bf2(bf_lo(w[e]) + __uint_as_float(rr[8 * k + 2 * e]),
+                                         bf_hi(w[e]) + __uint_as_float(rr[8 * k + 2 * e + 1]));
+                    *pk = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();   // the sum is in shared memory; TMEM is free for the next product
+        if (tid == 0) {
+#pragma unroll
+            for (int sl = 0; sl < 2; ++sl)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+                    tma_store_3d(&mo, sm + CR_O + sl * 16384 + hf * 8192, 64 * sl, c.h, c.row0 + 64 * hf);
+            bulk_commit_group();
+            if (x + 1 < x1) {   // the next tile's o rows once the store has read these
+                bulk_wait_group_read0();
+                load_rows(&mo, sm + CR_O, &bar_o,
+                          cr_tile(x + 1, H, T, P, seg_q, seg_r, later_tiles));
+                ++n_o;
+            }
+        }
+    }
+    if (tid == 0) {
+        bulk_wait_group0();   // every store complete before the CTA leaves
+        if (!sok) {           // loads still in flight land before shared memory is released
+            if (n_a) (void)mbar_wait(&bar_a, (n_a - 1) & 1u);
+            if (n_o) (void)mbar_wait(&bar_o, (n_o - 1) & 1u);
+            if (n_b) (void)mbar_wait(&bar_b, (n_b - 1) & 1u);
+        }
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 128);
@@ -2256,8 +2319,9 @@ cudaError_t launch_split_tail(const Problem &p0, const Problem &p, const TcParam
     seg_tiles(tp.seg_q, tp.seg_r, 0, t0, n0);
     const int later_tiles = p0.T / 128 - n0;
     const long n_tiles = (long)p0.n_seq * p.H * later_tiles;
-    split_correct_kernel<<<(unsigned)n_tiles, CR_THREADS, CR_SMEM, s>>>(
-        mqc, mo, mss, p.H, p0.T, P, tp.seg_q, tp.seg_r, later_tiles, p0.status);
+    const long grid = std::min<long>(n_tiles, 2L * sm_count());   // two CTAs per SM
+    split_correct_kernel<<<(unsigned)grid, CR_THREADS, CR_SMEM, s>>>(
+        mqc, mo, mss, p.H, p0.T, P, tp.seg_q, tp.seg_r, later_tiles, n_tiles, p0.status);
     note_launch();
     return cudaGetLastError();
 }
