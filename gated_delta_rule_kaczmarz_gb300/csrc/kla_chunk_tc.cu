@@ -189,6 +189,62 @@ __device__ __forceinline__ float *lslot(unsigned char *kq, int p) {
 
 constexpr int P1_THREADS = 256;
 
+// The first doubling step (n = 16: blocks of 32 at offsets o = 0, 32 of both
+// chunks, four blocks), with the triangular zeros skipped and the work
+// balanced: warps 0-3 take blocks 0, 1 and warps 4-7 blocks 2, 3 (lane / 16
+// the block, lane % 16 the row or row-and-column).  M = L21 D1: warp w forms
+// 4-column block cb (w % 4 for w < 4, 3 - w % 4 after) of all 16 rows from
+// rows s >= 4 cb of D1 (4 - cb steps).  X = -D2 M: warp w forms row group j
+// (the same rule; 4 rows x 4 column blocks) from columns s <= 4 j + 3 of D2
+// (j + 1 steps).  Every warp runs five steps.  M goes through `scratch` in
+// rows of 20 floats (float4-aligned, and the row-per-lane stores spread over
+// the banks).
+__device__ __forceinline__ void merge_mid(unsigned char *kq, float *scratch, int tid, int bar) {
+    constexpr int MS = 20;
+    const int w = tid >> 5, lane = tid & 31;
+    const int sel = w < 4 ? (w & 3) : 3 - (w & 3);
+    const int blk = (w < 4 ? 0 : 2) + (lane >> 4);
+    const int o = 32 * (blk & 1);
+    float *Lp = lslot(kq, blk >> 1);
+    float *Mb = scratch + blk * 16 * MS;
+    {
+        const int cb = sel, rho = lane & 15, r = o + 16 + rho;
+        float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+#pragma unroll 1
+        for (int s4 = cb; s4 < 4; ++s4) {
+            const float4 a = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, o + 4 * s4));
+            const float am[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int s = o + 4 * s4 + e;
+                const float4 b = *reinterpret_cast<const float4 *>(Lp + s * 64 + lsw(s, o + 4 * cb));
+                a01 = fma2(bcast2(am[e]), make_float2(b.x, b.y), a01);
+                a23 = fma2(bcast2(am[e]), make_float2(b.z, b.w), a23);
+            }
+        }
+        *reinterpret_cast<float4 *>(Mb + rho * MS + 4 * cb) = make_float4(a01.x, a01.y, a23.x, a23.y);
+    }
+    named_sync(bar, P1_THREADS);  // M complete; L21 no longer read
+    {
+        const int j = sel, rr = lane & 15, rho = 4 * j + (rr >> 2), cb = rr & 3, r = o + 16 + rho;
+        float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+#pragma unroll 1
+        for (int s4 = 0; s4 <= j; ++s4) {
+            const float4 a = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, o + 16 + 4 * s4));
+            const float am[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 b = *reinterpret_cast<const float4 *>(Mb + (4 * s4 + e) * MS + 4 * cb);
+                a01 = fma2(bcast2(am[e]), make_float2(b.x, b.y), a01);
+                a23 = fma2(bcast2(am[e]), make_float2(b.z, b.w), a23);
+            }
+        }
+        *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, o + 4 * cb)) =
+            make_float4(-a01.x, -a01.y, -a23.x, -a23.y);
+    }
+    named_sync(bar, P1_THREADS);
+}
+
 // The last doubling step (n = 32, one block per chunk, 128 threads per chunk),
 // with the zeros of the triangular factors skipped and the work spread evenly
 // over the four warps of a chunk.  M = L21 D1: column c of M needs rows s >= c
@@ -252,88 +308,6 @@ __device__ __forceinline__ void merge_top(unsigned char *kq, float *scratch, int
     named_sync(bar, P1_THREADS);
 }
 
-// One doubling step of the blocked inverse, in place in the fp32 L storage
-// of both chunks: for every diagonal block of size 2n whose two diagonal
-// n x n blocks already hold D1 = (I + L11)^{-1} and D2 = (I + L22)^{-1},
-// replace its lower-left block L21 by -D2 L21 D1.  All P1_THREADS threads;
-// each computes a (rows x 4) patch of the n x n products.  M = L21 D1 goes
-// through `scratch` (row-major n x n per block), so the step needs two
-// barriers.
-template <int n>
-__device__ __forceinline__ void merge_level(unsigned char *kq, float *scratch, int tid, int bar) {
-    constexpr int nblk = 64 / (2 * n);               // blocks of size 2n per chunk
-    constexpr int tpb = P1_THREADS / (2 * nblk);     // threads per block (both chunks)
-    constexpr int rows = n * n / 4 / tpb;            // patch rows per thread (4 columns each)
-    static_assert(rows >= 1 && rows * 4 * tpb == n * n, "patch tiling");
-    const int blkid = tid / tpb, q = tid % tpb;
-    const int p = blkid / nblk, o = 2 * n * (blkid % nblk);
-    constexpr int pcols = n / 4;                     // column patches per row band
-    const int pr = q / pcols, pc = q % pcols;        // rows [rows*pr, +rows), cols [4pc, +4)
-    float *Lp = lslot(kq, p);
-    float *Mp = scratch + blkid * n * n;
-    float2 acc[rows][2];
-    // M = L21 D1
-#pragma unroll
-    for (int m = 0; m < rows; ++m) acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
-#pragma unroll 1
-    for (int s4 = 0; s4 < n / 4; ++s4) {
-        float4 bb[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int r = o + 4 * s4 + e;
-            bb[e] = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, o + 4 * pc));
-        }
-#pragma unroll
-        for (int m = 0; m < rows; ++m) {
-            const int r = o + n + rows * pr + m;
-            const float4 a = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, o + 4 * s4));
-            const float am[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc[m][0] = fma2(bcast2(am[e]), make_float2(bb[e].x, bb[e].y), acc[m][0]);
-                acc[m][1] = fma2(bcast2(am[e]), make_float2(bb[e].z, bb[e].w), acc[m][1]);
-            }
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < rows; ++m) {
-        *reinterpret_cast<float4 *>(Mp + (rows * pr + m) * n + 4 * pc) =
-            make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
-        acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
-    }
-    named_sync(bar, P1_THREADS);  // M complete; L21 no longer read
-    // X = -D2 M, written over L21.  D2 is lower triangular (zeros above its
-    // diagonal are stored), so row rr needs columns s <= rr only: the loop
-    // stops after the last column block any row of this warp needs (the
-    // skipped terms are exact zeros).
-    const int rr_max = rows * (((q & ~31) + 31) / pcols) + rows - 1;
-    const int s4lim = rr_max / 4 + 1 < n / 4 ? rr_max / 4 + 1 : n / 4;
-#pragma unroll 1
-    for (int s4 = 0; s4 < s4lim; ++s4) {
-        float4 bb[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            bb[e] = *reinterpret_cast<const float4 *>(Mp + (4 * s4 + e) * n + 4 * pc);
-#pragma unroll
-        for (int m = 0; m < rows; ++m) {
-            const int r = o + n + rows * pr + m;
-            const float4 a = *reinterpret_cast<const float4 *>(Lp + r * 64 + lsw(r, o + n + 4 * s4));
-            const float am[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc[m][0] = fma2(bcast2(am[e]), make_float2(bb[e].x, bb[e].y), acc[m][0]);
-                acc[m][1] = fma2(bcast2(am[e]), make_float2(bb[e].z, bb[e].w), acc[m][1]);
-            }
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < rows; ++m) {
-        const int r = o + n + rows * pr + m;
-        *reinterpret_cast<float4 *>(Lp + r * 64 + lsw(r, o + 4 * pc)) =
-            make_float4(-acc[m][0].x, -acc[m][0].y, -acc[m][1].x, -acc[m][1].y);
-    }
-    named_sync(bar, P1_THREADS);
-}
 
 // ===================================================================== phase 1
 // Two threads per token row r of the item (r = tid % 128, the TMEM lane its
@@ -718,7 +692,7 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
         }
         named_sync(bar, P1_THREADS);
     }
-    merge_level<16>(KQ, scratch, tid, bar);   // 32 x 32 diagonal blocks
+    merge_mid(KQ, scratch, tid, bar);         // 32 x 32 diagonal blocks
     merge_top(KQ, scratch, tid, bar);         // the whole 64 x 64 inverse
 
     // ---- V landed; rows past the chunk's end (another sequence's tokens or
