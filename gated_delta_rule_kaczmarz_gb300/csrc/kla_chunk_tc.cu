@@ -2089,8 +2089,9 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     if (n_chunks_upper > INT32_MAX || (n_chunks_upper + 1) / 2 * (long)p0.H > INT32_MAX)
         return cudaErrorInvalidValue;
     if (tmap::encode_fn() == nullptr) return cudaErrorNotSupported;
-    // a split sequence runs as P virtual sequences of T / P tokens (same rows,
-    // same chunk slots)
+    // a split sequence runs as P virtual sequences (its segments: same rows,
+    // same chunk slots); p keeps the virtual count, and T / P as the segment
+    // length of an equal split (the fused launch's item order)
     const bool record = p0.S_chk != nullptr;   // backward recording: no split
     const int P = !record ? split_factor(p0.n_seq, p0.T, p0.H, p0.cu_seqlens != nullptr) : 1;
     Problem p = p0;

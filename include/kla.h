@@ -125,12 +125,14 @@ KLA_API size_t kla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv,
  * Execution (bf16, dk = dv = 128, B*T >= 64): the tensor-core kernels, as one
  * cooperative launch when the state pass of every (batch, head) fits on half
  * of the SMs and each sequence has an even number of chunks, else as two.
- * Few heads with long sequences run the sequence split: each sequence as P
- * segments (P in {2, 4, 8}, segments of whole 128-token tiles and at least
- * 1024 tokens, chosen so that the state and transition passes fit on the
- * SMs), whose start states are chained and whose outputs are corrected (four
- * launches, or three when fused).  The environment variable KLA_SEQ_SPLIT=P
- * forces a factor (1 disables the split); the workspace size depends on that
+ * Few heads with long sequences (T a multiple of 128) run the sequence split:
+ * each sequence as P <= 8 segments of whole 128-token tiles, as equal as the
+ * tile count allows (at least 1024 tokens each, or 4096 with one CTA per
+ * chain), P chosen for the shortest chain among those whose state and
+ * transition passes fit on the SMs at once; the segments' start states are
+ * chained and their outputs corrected (four launches, or three when fused,
+ * which needs equal segments).  The environment variable KLA_SEQ_SPLIT=P
+ * forces a factor up to T / 128 (1 disables the split); the workspace size depends on that
  * choice and on the SM count of the current device, so query it on the device
  * and with the environment of the call.  In two launches, the state pass runs
  * one CTA per (sequence, head) instead of two when two per head would
