@@ -66,6 +66,7 @@ struct TcParams {
     __nv_bfloat16 *o;
     const int *cu_seqlens;     // varlen only
     const int *chunk_prefix;   // varlen only: first chunk of each sequence, [N+1]
+    const int2 *chunk_tab;     // varlen only: (first token row, tokens) of each chunk
     const int *order;          // varlen only: sequences by decreasing length, [N]
     unsigned *status;
     float *g_ws;               // [slots][64]        g_t (in-chunk cumulative log decay)
@@ -115,40 +116,32 @@ __device__ __forceinline__ bool status_bad(const unsigned *status) {
     return status != nullptr && *(volatile const unsigned *)status != kDevOk;
 }
 
-// Chunk g of head h: its sequence, first token row, valid length.  False when
-// g lies beyond the last chunk (the grid is sized by an upper bound).
 // Segment s of a split sequence: its first 128-token tile and its tile count.
 __host__ __device__ __forceinline__ void seg_tiles(int q, int r, int s, int &tile0, int &ntiles) {
     tile0 = s * q + (s < r ? s : r);
     ntiles = q + (s < r ? 1 : 0);
 }
 
-__device__ __forceinline__ bool slot_info(const TcParams &p, long g, int &seq, long &row0,
-                                          int &nc) {
+// Chunk slot g: its first token row and valid length.  False when g lies
+// beyond the last chunk (the grid is sized by an upper bound).
+__device__ __forceinline__ bool slot_info(const TcParams &p, long g, long &row0, int &nc) {
     if (p.chunk_prefix == nullptr) {
         if (p.nch_fixed <= 0) return false;
         // 32-bit division: chunk slots stay below 2^31 (the host checks)
         const uint32_t q = (uint32_t)g / (uint32_t)p.nch_fixed;
-        seq = (int)q;
-        if (seq >= p.n_seq) return false;
+        if ((int)q >= p.n_seq) return false;
         const int c = (int)((uint32_t)g - q * (uint32_t)p.nch_fixed);
-        row0 = (long)seq * p.T + (long)c * C;
+        row0 = (long)q * p.T + (long)c * C;
         nc = min(C, p.T - c * C);
         return true;
     }
+    // the chunk table written by the preparation kernel (one entry past the
+    // last chunk slot, so that the read needs no bound first)
     const int total = p.chunk_prefix[p.n_seq];
+    const int2 e = p.chunk_tab[g];
     if (g >= total) return false;
-    int lo = 0, hi = p.n_seq - 1;  // last sequence whose first chunk is <= g
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.chunk_prefix[mid] <= g) lo = mid; else hi = mid - 1;
-    }
-    seq = lo;
-    const int c = (int)(g - p.chunk_prefix[seq]);
-    const long start = p.cu_seqlens[seq];
-    const long len = (long)p.cu_seqlens[seq + 1] - start;
-    row0 = start + (long)c * C;
-    nc = (int)min((long)C, len - (long)c * C);
+    row0 = e.x;
+    nc = e.y;
     return nc > 0;
 }
 
@@ -430,10 +423,10 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
         pair = (long)pq;
         h = (int)(i32 - pq * (uint32_t)p.H);
     }
-    int seq0, seq1, nc0, nc1;
+    int nc0, nc1;
     long r00, r01;
-    const bool v0 = slot_info(p, 2 * pair, seq0, r00, nc0);
-    const bool v1 = slot_info(p, 2 * pair + 1, seq1, r01, nc1);
+    const bool v0 = slot_info(p, 2 * pair, r00, nc0);
+    const bool v1 = slot_info(p, 2 * pair + 1, r01, nc1);
     if (!v0) { nc0 = 0; r00 = 0; }
     if (!v1) { nc1 = 0; r01 = 0; }
     if (!v0 && !v1) continue;
@@ -1566,11 +1559,14 @@ fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
 // ===================================================================== varlen prep
 // One CTA: validates cu_seqlens, writes the first chunk of every sequence
-// (chunk_prefix[N+1]) and a longest-first order of the sequences.
+// (chunk_prefix[N+1]), the first token row and token count of every chunk
+// (chunk_tab, so that phase 1 finds a chunk with one load) and a
+// longest-first order of the sequences.
 constexpr int PREP_THREADS = 1024;
 
 __global__ void __launch_bounds__(PREP_THREADS)
-prep_kernel(const int *cu, int N, int total_T, int *chunk_prefix, int *order, unsigned *status) {
+prep_kernel(const int *cu, int N, int total_T, int *chunk_prefix, int *order, int2 *chunk_tab,
+            unsigned *status) {
     __shared__ int bad;
     __shared__ int warp_sums[PREP_THREADS / 32];
     __shared__ int carry;
@@ -1615,6 +1611,15 @@ prep_kernel(const int *cu, int N, int total_T, int *chunk_prefix, int *order, un
         __syncthreads();
     }
     if (tid == 0) chunk_prefix[N] = carry;
+    __syncthreads();
+    // (first token row, tokens) of every chunk: a warp per sequence, its
+    // lanes over the sequence's chunks
+    for (int n = warp; n < N; n += PREP_THREADS / 32) {
+        const int c0 = chunk_prefix[n], nc = chunk_prefix[n + 1] - c0;
+        const int start = cu[n], len = cu[n + 1] - start;
+        for (int c = lane; c < nc; c += 32)
+            chunk_tab[c0 + c] = make_int2(start + c * C, min(C, len - c * C));
+    }
     // longest-first order (stable); identity for very large N
     for (int n = tid; n < N; n += PREP_THREADS) {
         int rank = n;
@@ -1942,10 +1947,17 @@ struct WsLayout {
     size_t meta, g, W, U, A, total;
 };
 
+// Offset (in ints) of the varlen chunk table in the meta area: after the
+// chunk prefix [N + 1] and the order [N], on an 8-byte boundary.
+size_t tab_offset(int n_seq) { return ((size_t)2 * n_seq + 1 + 1) & ~(size_t)1; }
+
 WsLayout layout(long n_chunks, int H, int n_seq) {
     const size_t slots = (size_t)n_chunks * H;
-    // meta: the varlen chunk table and order, or the fused launch's ready flags
-    const size_t meta_ints = std::max((size_t)2 * n_seq + 1, (size_t)((n_chunks + 1) / 2) * H + 1);
+    // meta: the varlen chunk prefix, order and chunk table (from an 8-byte
+    // boundary, one entry per chunk slot and one past), or the fused
+    // launch's ready flags
+    const size_t meta_ints = std::max(tab_offset(n_seq) + 2 * ((size_t)n_chunks + 1),
+                                      (size_t)((n_chunks + 1) / 2) * H + 1);
     WsLayout L;
     L.meta = 0;
     L.g = align_up(meta_ints * sizeof(int), 1024);
@@ -2148,8 +2160,10 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     tp.A_ws = reinterpret_cast<__nv_bfloat16 *>(ws + L.A);
     int *chunk_prefix = reinterpret_cast<int *>(ws + L.meta);
     int *order = chunk_prefix + p.n_seq + 1;
+    int2 *chunk_tab = reinterpret_cast<int2 *>(chunk_prefix + tab_offset(p.n_seq));
     tp.chunk_prefix = p.cu_seqlens ? chunk_prefix : nullptr;
     tp.order = p.cu_seqlens ? order : nullptr;
+    tp.chunk_tab = p.cu_seqlens ? chunk_tab : nullptr;
 
     CUtensorMap mq, mk, mv, mw, mu, ma;
     const long slots = n_chunks_upper * p.H;
@@ -2163,7 +2177,7 @@ cudaError_t launch_chunk_tc(const Problem &p0, long n_chunks_upper, cudaStream_t
     cudaError_t e;
     if (p.cu_seqlens) {
         prep_kernel<<<1, PREP_THREADS, 0, s>>>(p.cu_seqlens, p.n_seq, p.total_T, chunk_prefix,
-                                               order, p.status);
+                                               order, chunk_tab, p.status);
         note_launch();
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
