@@ -434,18 +434,23 @@ __device__ __forceinline__ void intra_run(const CUtensorMap *mq, const CUtensorM
     const bool vslot = slot ? v1 : v0;
 
     if (tid == 0) {
-        bulk_wait_group_read0();   // the previous item's W / U~ stores have left shared memory
         // K and Q first (the Gram products need them); V, needed only by the
-        // U~ product, on its own barrier behind them
+        // U~ product, on its own barrier behind them.  The previous item's
+        // W / U~ stores read the K halves and V's region: Q is loaded before
+        // waiting for them to leave shared memory.
         mbar_expect_tx(&bars[0], 2u * 32768u);
 #pragma unroll 1
         for (int q = 0; q < 2; ++q)
 #pragma unroll 1
-            for (int s = 0; s < 2; ++s) {
-                const int z = (int)(q ? r01 : r00);
-                tma_load_3d(KQ + s * 32768 + q * 8192, mk, &bars[0], 64 * s, h, z);
-                tma_load_3d(KQ + s * 32768 + 16384 + q * 8192, mq, &bars[0], 64 * s, h, z);
-            }
+            for (int s = 0; s < 2; ++s)
+                tma_load_3d(KQ + s * 32768 + 16384 + q * 8192, mq, &bars[0], 64 * s, h,
+                            (int)(q ? r01 : r00));
+        bulk_wait_group_read0();
+#pragma unroll 1
+        for (int q = 0; q < 2; ++q)
+#pragma unroll 1
+            for (int s = 0; s < 2; ++s)
+                tma_load_3d(KQ + s * 32768 + q * 8192, mk, &bars[0], 64 * s, h, (int)(q ? r01 : r00));
         mbar_expect_tx(&bars[3], 32768u);
 #pragma unroll 1
         for (int q = 0; q < 2; ++q)
