@@ -47,7 +47,7 @@ if ROOT not in sys.path:
 METRIC = "KLA chunkwise prefill tokens/s & % roofline; decode steps/s at B=256"
 # DRAM bytes (read + write) per call from an ncu capture of the kernels as
 # they are now, or None where the kernels changed after the last capture.
-TRAFFIC = {"layer_prefill": 54.41e6 + 14.30e6, "long_context": None, "varlen_64": None,
+TRAFFIC = {"layer_prefill": 56.03e6 + 16.03e6, "long_context": None, "varlen_64": None,
            "tiny_fp32": None,
            "decode_b256": 2 * (135.83e6 + 74.59e6), "ccq": 33.90e6 + 0.12e6}
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
