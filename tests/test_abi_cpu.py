@@ -228,3 +228,22 @@ def test_sequence_split_workspace(monkeypatch):
     small_base = small()
     monkeypatch.setenv("KLA_SEQ_SPLIT", "3")   # 256 tokens: two tiles
     assert small() == small_base
+
+
+def test_default_split_choice(monkeypatch):
+    """The default split factor, seen through the workspace size (which
+    depends on it): the long-context shape (B1 H16 T32768) takes five
+    segments of unequal length (16 x 9 chains fit one 128-column CTA each on
+    148-152 SMs, six would not), the layer shape (B4 H8 T2048) no split."""
+    lib = binding.load()
+    def size(B, T, H, P=None):
+        if P is None:
+            monkeypatch.delenv("KLA_SEQ_SPLIT", raising=False)
+        else:
+            monkeypatch.setenv("KLA_SEQ_SPLIT", str(P))
+        return lib.kla_chunk_fwd_workspace_size(B, T, H, 128, 128, 64, 1)
+    long_default = size(1, 32768, 16)
+    assert long_default == size(1, 32768, 16, 5)
+    assert long_default != size(1, 32768, 16, 4)
+    assert long_default != size(1, 32768, 16, 6)
+    assert size(4, 2048, 8) == size(4, 2048, 8, 1)
