@@ -247,3 +247,9 @@ def test_default_split_choice(monkeypatch):
     assert long_default != size(1, 32768, 16, 4)
     assert long_default != size(1, 32768, 16, 6)
     assert size(4, 2048, 8) == size(4, 2048, 8, 1)
+    # two heads of 32K tokens: eight equal segments (60 chains of two CTAs)
+    assert size(1, 32768, 2) == size(1, 32768, 2, 8)
+    # B2 H4 T8192: five unequal segments of 13 + 13 + 13 + 13 + 12 tiles, two
+    # 64-column CTAs per chain (8 x 9 chains, 144 CTAs)
+    assert size(2, 8192, 4) == size(2, 8192, 4, 5)
+    assert size(2, 8192, 4) != size(2, 8192, 4, 4)
